@@ -1,0 +1,508 @@
+"""Benchmark of the WKV-7 hot path on one GB300 (or N, one process per GPU).
+
+Headline line: WKV-7 decode state-GB/s on the 2.9B geometry (32 layers x 40
+heads x 64, batch 32, fp32 state in place, one token per step, 32 layer
+launches per step replayed from CUDA graphs, a pool of 16 input sets per layer
+cycled).  A step is one token through all 32 layers.  The prefill figure
+(2.9B geometry, 8 x 4096 tokens, bf16 inputs) rides in the same JSON line
+under "prefill".
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Multi-GPU (torchrun): every rank runs the same per-GPU workload on its own
+GPU (weak scaling; the heads are independent, so there is no data-path
+collective); rank 0 prints value = all ranks' bytes / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+N_HEAD = 64
+STATE_BYTES = 2 * 4 * N_HEAD * N_HEAD           # state read + write per head-step
+STEP_BYTES = STATE_BYTES + 6 * 4 * N_HEAD + 4 * N_HEAD  # + six input vectors + o = 34,560
+PREFILL_BYTES_PER_TOKEN_HEAD = 5 * 2 * N_HEAD + 4 * N_HEAD + 4 * N_HEAD  # bf16 r,k,v,kk,a; fp32 w, o = 1,152
+PREFILL_FLOP_PER_TOKEN_HEAD = 26 * N_HEAD * N_HEAD  # chunked form, C = N = 64: 106,496
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 1024 * 1024
+
+METRIC = "WKV-7 decode state-GB/s & prefill tokens/s on 1 GB300; % of roofline"
+
+
+# --------------------------------------------------------------------------
+# host-side helpers (also exercised by the CPU tests)
+
+def load_peaks() -> tuple[dict, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env() -> tuple[int, int, int]:
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity when world == 1)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def source_digest(paths) -> str:
+    h = hashlib.sha256()
+    for p in paths:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def kernel_traffic(kernel: str, workload: str, src_files) -> float | None:
+    """DRAM bytes per launch from the committed ncu summary, if the kernel's
+    sources are unchanged since it was taken (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel, {}).get(workload)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("source_digest") != source_digest(src_files):
+        return None
+    return float(rec["dram_bytes_per_launch"])
+
+
+def smi_index(local: int) -> str:
+    """nvidia-smi's name for the local CUDA device (index or UUID)."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").strip()
+    if vis:
+        ids = [x.strip() for x in vis.split(",") if x.strip()]
+        if local < len(ids):
+            return ids[local]
+    return str(local)
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling around a timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: str, period_ms: int = 50):
+        self.gpu_index = gpu_index
+        self.period_ms = period_ms
+        self.proc = None
+        self.lines: list[str] = []
+        self._reader = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 f"-lms={self.period_ms}", f"-i={self.gpu_index}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return self
+
+        def read():
+            for line in self.proc.stdout:
+                self.lines.append(line.strip())
+        self._reader = threading.Thread(target=read, daemon=True)
+        self._reader.start()
+        return self
+
+    def stop(self) -> dict:
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self._reader:
+                self._reader.join(timeout=2)
+        return summarize_clocks(self.lines)
+
+
+def summarize_clocks(lines) -> dict:
+    sm, smax, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in lines:
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 9:
+            continue
+        try:
+            sm.append(float(parts[1]))
+            smax.append(float(parts[2]))
+        except ValueError:
+            continue
+        for name, flag in zip(names, parts[5:9]):
+            if flag.lower().startswith("active"):
+                reasons.add(name)
+    if not sm:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+            "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# GPU arm
+
+NAMES = ("r", "w", "k", "v", "kk", "a")
+
+
+class DecodeWorkload:
+    """32 layer slabs of state, a pool of input sets per layer, per-layer o."""
+
+    def __init__(self, layers, B, H, pool, dev, seed):
+        import torch
+
+        from rwkv_linear_attention_gb300 import inputs
+        self.layers, self.B, self.H, self.P = layers, B, H, pool
+        self.dev = dev
+        # pool[name]: [P, layers, B, H, N] so that one step's inputs for all
+        # layers are one contiguous block (one host->device copy per input)
+        x = inputs.draw_rwkkva((pool, layers, B, H, N_HEAD), seed=seed, device=dev)
+        self.pool = {n: x[n].contiguous() for n in NAMES}
+        self.state = torch.zeros(layers, B, H, N_HEAD, N_HEAD, device=dev)
+        self.o = torch.empty(layers, B, H, N_HEAD, device=dev)
+
+    def launch_step(self, p, src=None):
+        import rwkv_linear_attention_gb300 as wkv7
+        src = src or {n: self.pool[n][p] for n in NAMES}
+        for layer in range(self.layers):
+            wkv7.step(*(src[n][layer] for n in NAMES), self.state[layer], self.o[layer])
+
+    def warm(self, steps):
+        for s in range(steps):
+            self.launch_step(s % self.P)
+
+    def capture(self, stream):
+        import torch
+        graphs = []
+        for p in range(self.P):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                self.launch_step(p)
+            graphs.append(g)
+        return graphs
+
+    def bytes_per_step(self):
+        return self.layers * self.B * self.H * STEP_BYTES
+
+    def state_bytes_per_step(self):
+        return self.layers * self.B * self.H * STATE_BYTES
+
+
+def time_graphs(graphs, steps, warmup, stream, world):
+    import torch
+    for s in range(warmup):
+        graphs[s % len(graphs)].replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for s in range(steps):
+            graphs[s % len(graphs)].replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end)
+
+
+def decode_e2e(wl, steps, warmup, stream, world):
+    """Same metric through the public API with host buffers: every step copies
+    that step's inputs (all 32 layers) from pinned host memory, runs the 32
+    layer calls and reads o back into pinned host memory; each step is one
+    captured graph of those copies and calls."""
+    import torch
+    host_pool = {n: wl.pool[n].cpu().pin_memory() for n in NAMES}
+    dev_in = {n: torch.empty_like(wl.pool[n][0]) for n in NAMES}
+    o_host = torch.empty(wl.o.shape, dtype=torch.float32).pin_memory()
+    graphs = []
+    for p in range(wl.P):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for n in NAMES:
+                dev_in[n].copy_(host_pool[n][p], non_blocking=True)
+            wl.launch_step(p, src=dev_in)
+            o_host.copy_(wl.o, non_blocking=True)
+        graphs.append(g)
+    ms = time_graphs(graphs, steps, warmup, stream, world)
+    h2d = sum(dev_in[n].numel() * 4 for n in NAMES)
+    d2h = o_host.numel() * 4
+    del graphs
+    return ms, h2d, d2h
+
+
+def prefill_bench(dev, steps, warmup, world):
+    import torch
+
+    import rwkv_linear_attention_gb300 as wkv7
+    from rwkv_linear_attention_gb300 import inputs
+    cfg = inputs.PREFILL_2P9B
+    lens = [cfg["T"]] * cfg["num_seqs"]
+    p = inputs.prefill_inputs(lens, cfg["H"], cfg["N"], seed=1002, device=dev)
+    cu = p["cu_seqlens"]
+    cu_dev = cu.to(dev)
+    T_total = int(cu[-1])
+    o = torch.empty(T_total, cfg["H"], N_HEAD, device=dev)
+    sf = torch.empty(len(lens), cfg["H"], N_HEAD, N_HEAD, device=dev)
+    ws_bytes = wkv7.prefill_workspace_size(len(lens), T_total, cfg["H"])
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def call():
+        wkv7.prefill(p["r"], p["w"], p["k"], p["v"], p["kk"], p["a"], cu_dev, final_state=sf, o=o,
+                     workspace=ws if ws_bytes else None, cu_seqlens_host=cu, stream=stream)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            call()
+    torch.cuda.synchronize()
+    wkv7.check_device_status(stream)
+    barrier(world)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(steps):
+            call()
+        end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = max_over_ranks(start.elapsed_time(end), world, dev) / steps
+    token_heads = T_total * cfg["H"]
+    return {
+        "tokens": T_total, "token_heads": token_heads, "ms_per_call": ms,
+        "algorithmic_bytes": token_heads * PREFILL_BYTES_PER_TOKEN_HEAD,
+        "algorithmic_flop": token_heads * PREFILL_FLOP_PER_TOKEN_HEAD,
+        "input_bytes_gt_l2": token_heads * PREFILL_BYTES_PER_TOKEN_HEAD > L2_BYTES,
+    }
+
+
+def cpu_baseline_decode(B, H, layers, budget_s=15.0):
+    """The oracle, as it stands, on the host cores: a bounded sample of decode
+    steps (all B x H heads of as many layers as fit the time budget)."""
+    import numpy as np
+
+    import oracle
+    from rwkv_linear_attention_gb300 import inputs
+    threads = oracle.default_threads()
+    x = inputs.draw_rwkkva((B, H, N_HEAD), seed=1, device="cpu")
+    arrs = [x[n].numpy() for n in NAMES]
+    s0 = inputs.initial_state(B, H, N_HEAD, seed=1).double().numpy()
+    t0 = time.perf_counter()
+    oracle.step(*arrs, state=s0, nthreads=threads)
+    one = max(time.perf_counter() - t0, 1e-4)
+    n_layer_steps = max(1, int(budget_s / one))
+    t0 = time.perf_counter()
+    for _ in range(n_layer_steps):
+        _, s0 = oracle.step(*arrs, state=s0, nthreads=threads)
+    dt = time.perf_counter() - t0
+    gbs = n_layer_steps * B * H * STATE_BYTES / dt / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n_layer_steps} layer-steps of B={B} x H={H} heads (fp64, {dt:.1f} s)"}
+
+
+def run_ours(args):
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from __graft_entry__ import build
+    if rank == 0:
+        build()
+    barrier(world)
+    if rank != 0:
+        build()
+
+    from rwkv_linear_attention_gb300 import inputs
+    peaks, peak_kind = load_peaks()
+    cfg = inputs.DECODE_2P9B
+    B = args.batch
+    wl = DecodeWorkload(cfg["layers"], B, cfg["H"], cfg["pool"], dev, seed=1001 + rank)
+    wl.warm(min(cfg["warm_tokens"], 64))
+    stream = torch.cuda.Stream(device=dev)
+    graphs = wl.capture(stream)
+
+    sampler = ClockSampler(smi_index(local))
+    sampler.start()
+    ms = time_graphs(graphs, args.steps, args.warmup, stream, world)
+    clocks = sampler.stop()
+    ms = max_over_ranks(ms, world, dev)
+    ms_step = ms / args.steps
+    launches = wl.layers * args.steps
+    value = world * wl.state_bytes_per_step() * args.steps / (ms / 1e3) / 1e9
+    launch_s = ms / 1e3 / launches
+    achieved = wl.B * wl.H * STEP_BYTES / launch_s / 1e9
+    step_src = [os.path.join(ROOT, "rwkv_linear_attention_gb300", "csrc", "wkv7_step.cu")]
+    traffic = kernel_traffic("wkv7_step_kernel", f"B={B},H={cfg['H']}", step_src)
+    del graphs
+
+    e2e_ms, h2d, d2h = decode_e2e(wl, max(args.steps // 4, 8), args.warmup, stream, world)
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
+    e2e_steps = max(args.steps // 4, 8)
+    e2e_value = world * wl.state_bytes_per_step() * e2e_steps / (e2e_ms / 1e3) / 1e9
+    del wl
+    torch.cuda.empty_cache()
+
+    pre = prefill_bench(dev, args.prefill_steps, max(args.warmup, 3), world)
+    pre_tokens_s = world * pre["tokens"] / (pre["ms_per_call"] / 1e3)
+    pre_gbs = pre["algorithmic_bytes"] / (pre["ms_per_call"] / 1e3) / 1e9
+    pre_tflops = pre["algorithmic_flop"] / (pre["ms_per_call"] / 1e3) / 1e12
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded; r,k,v~N(0,1), k/sqrt(N), w=-0.606531*sigmoid(N(0,1)), unit kk, a=sigmoid(N(0,1)))",
+        "config": {
+            "workload": f"WKV-7 decode, 2.9B geometry: 32 layers x H=40 x N=64, B={B}, fp32 state in place, "
+                        "one token per step (32 launches), 16 input sets per layer cycled, CUDA-graph replay",
+            "layers": cfg["layers"], "B": B, "H": cfg["H"], "N": N_HEAD,
+            "state_bytes_per_step": cfg["layers"] * B * cfg["H"] * STATE_BYTES,
+            "l2": "inputs larger than L2 (state touched per step = "
+                  f"{cfg['layers'] * B * cfg['H'] * STATE_BYTES / 2**20:.0f} MiB > 129 MiB)"
+                  if cfg["layers"] * B * cfg["H"] * STATE_BYTES > L2_BYTES else "L2-resident (state < L2)",
+            "parallelism": f"replicas x{world} (independent heads, no collective)",
+        },
+        "roofline": {
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+            "kernel": "wkv7_step_kernel", "algorithmic_bytes_per_launch": B * cfg["H"] * STEP_BYTES,
+            "peak_kind": f"{peak_kind} (copy bandwidth)",
+        },
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "how": "per step: pinned H2D of all 32 layers' inputs, 32 wkv7_step calls, D2H of o; one CUDA graph per step"},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "prefill": {
+            "metric": "prefill tokens/s", "value": round(pre_tokens_s, 1), "unit": "tokens/s",
+            "ms_per_call": round(pre["ms_per_call"], 4), "calls": args.prefill_steps,
+            "config": {"workload": "WKV-7 chunked prefill, 2.9B geometry: 8 x 4096 tokens, H=40, N=64, "
+                                   "bf16 r,k,v,kk,a, fp32 w, zero initial state, final state out",
+                       "l2": "inputs larger than L2"},
+            "roofline": {"bound": "hbm", "achieved": round(pre_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(pre_gbs / peaks["hbm_gbs"], 4), "traffic": None,
+                         "tensor_tflops": round(pre_tflops, 2),
+                         "tensor_frac_of_bf16": round(pre_tflops / peaks["bf16_tflops"], 4)},
+        },
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_decode(B, cfg["H"], cfg["layers"], budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The reference arm: the fp64 oracle, as it stands, on the host cores,
+    on the same metric and workload; each step a bounded sample."""
+    import torch  # noqa: F401  (same environment as the GPU arm)
+
+    import oracle
+    from rwkv_linear_attention_gb300 import inputs
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    cfg = inputs.DECODE_2P9B
+    B, H = args.batch, cfg["H"]
+    threads = oracle.default_threads()
+    x = inputs.draw_rwkkva((B, H, N_HEAD), seed=1, device="cpu")
+    arrs = [x[n].numpy() for n in NAMES]
+    s = inputs.initial_state(B, H, N_HEAD, seed=1).double().numpy()
+    # size each step so that warmup + steps take about args.cpu_budget seconds
+    t0 = time.perf_counter()
+    oracle.step(*arrs, state=s, nthreads=threads)
+    one = max(time.perf_counter() - t0, 1e-4)
+    per_step_layers = max(1, min(cfg["layers"], int(args.cpu_budget / (one * (args.steps + args.warmup)))))
+    for _ in range(args.warmup):
+        for _ in range(per_step_layers):
+            _, s = oracle.step(*arrs, state=s, nthreads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        for _ in range(per_step_layers):
+            _, s = oracle.step(*arrs, state=s, nthreads=threads)
+    dt = time.perf_counter() - t0
+    value = args.steps * per_step_layers * B * H * STATE_BYTES / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3 / args.steps, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": f"WKV-7 decode, 2.9B geometry: B={B}, H={H}, N=64; each step a sample of "
+                               f"{per_step_layers} of 32 layers (fp64 oracle on host cores)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{per_step_layers} layer(s) x B={B} x H={H} heads per step"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4096)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--batch", type=int, default=32, help="decode batch B (2.9B geometry: 1, 8 or 32)")
+    ap.add_argument("--prefill-steps", type=int, default=20)
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for the CPU baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,162 @@
+/*
+ * wkv7.h -- C ABI of the WKV-7 recurrence on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation (per head, head size N, state S = [K, V] = [N, N] fp32):
+ *
+ *     z   = kk^T S_old
+ *     S   = diag(exp w) S_old - (kk .* a) z^T + k v^T
+ *     o   = S^T r
+ *
+ * This is the per-head WKV7 update of the Core AI model zoo note
+ * "Recurrent / linear-attention LLMs on Core AI", section 1 ("decode
+ * recurrence lowers to standard ops"): decay and delta term both act on the
+ * old state, the k v^T write follows, and the read-out sees the new state.
+ * w is the log-decay (the decay factor is exp(w)); kk is used exactly as
+ * given (the caller normalises it); a is a per-channel vector.  The state
+ * layout [K, V] with the value channel contiguous is the recState layout of
+ * section 2 of the same note.
+ *
+ * Conventions shared by every call:
+ *   - Only N = 64 is supported (the head size of every RWKV-7 model the
+ *     pages name); any other N returns WKV7_ERR_UNSUPPORTED.
+ *   - All tensor pointers are DEVICE pointers owned by the caller and must be
+ *     16-byte aligned (WKV7_ERR_ALIGNMENT otherwise).  The library allocates
+ *     no memory and keeps no per-call state.
+ *   - Every call is stream-ordered on `stream` (0 = legacy default stream)
+ *     and returns without synchronising.  A launch failure returns
+ *     WKV7_ERR_CUDA; errors found on the device (malformed cu_seqlens, an
+ *     expired bounded wait) are recorded in a per-device status word that
+ *     wkv7_check_device_status() reads and clears.
+ *   - No call ever aborts, traps or asserts on the device; invalid arguments
+ *     are rejected on the host before any launch.
+ *   - All arithmetic is fp32 with fp32 state; decode inputs are fp32,
+ *     prefill inputs r, k, v, kk, a may be bf16 (w is always fp32).
+ */
+#ifndef WKV7_H
+#define WKV7_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define WKV7_API __attribute__((visibility("default")))
+#else
+#define WKV7_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    WKV7_OK = 0,
+    WKV7_ERR_INVALID_ARG = 1,  /* null pointer, bad size, malformed cu_seqlens, forbidden aliasing */
+    WKV7_ERR_UNSUPPORTED = 2,  /* N != 64, unknown dtype */
+    WKV7_ERR_ALIGNMENT = 3,    /* a tensor pointer is not 16-byte aligned */
+    WKV7_ERR_CUDA = 4,         /* a CUDA runtime/launch error (see wkv7_last_cuda_error) */
+    WKV7_ERR_TIMEOUT = 5,      /* a bounded device-side wait expired (device status) */
+    WKV7_ERR_WORKSPACE = 6,    /* workspace missing or smaller than wkv7_prefill_workspace_size */
+    WKV7_ERR_DEVICE_BOUNDS = 7 /* the device found an index out of range (device status) */
+} wkv7_status;
+
+typedef enum {
+    WKV7_F32 = 0,
+    WKV7_BF16 = 1
+} wkv7_dtype;
+
+#define WKV7_HEAD_SIZE 64
+
+/*
+ * wkv7_step -- one decode token for B * H independent heads.
+ *
+ * The recurrent "step(id, state:)" of the SwiftRWKV inference page
+ * ("Recurrent -- step(id, state:), one token at a time carrying RWKVState"),
+ * restricted to the WKV part: the state is read and written in place.
+ *
+ *   r, w, k, v, kk, a : fp32 [B, H, N]      inputs of this token (w = log-decay)
+ *   state             : fp32 [B, H, N, N]   [K][V], read and overwritten
+ *   o                 : fp32 [B, H, N]      output o = S_new^T r
+ *
+ * B >= 0, H >= 1; B * H * N * N must fit in int64.  B == 0 is a no-op.
+ * `state` must not overlap any input or `o` (WKV7_ERR_INVALID_ARG).
+ */
+WKV7_API wkv7_status wkv7_step(int B, int H, int N,
+                      const float *r, const float *w, const float *k,
+                      const float *v, const float *kk, const float *a,
+                      float *state, float *o, cudaStream_t stream);
+
+/*
+ * wkv7_prefill_workspace_size -- bytes of device workspace wkv7_prefill
+ * needs for this shape (may be 0; the result depends only on the arguments).
+ */
+WKV7_API size_t wkv7_prefill_workspace_size(int num_seqs, int T_total, int H, int N);
+
+/*
+ * wkv7_prefill -- the recurrence over packed variable-length sequences.
+ *
+ * The parallel "prefill(ids, state:)" pass of the SwiftRWKV inference page
+ * (a whole prompt in one launch, "What the prefill path is made of"), with
+ * the batch packed by cu_seqlens instead of right padding.  The result equals
+ * running wkv7_step over each sequence's tokens in order.
+ *
+ *   num_seqs        : number of sequences (>= 0)
+ *   T_total         : total tokens (>= 0)
+ *   cu_seqlens      : DEVICE int32 [num_seqs + 1]; sequence b owns tokens
+ *                     cu_seqlens[b] .. cu_seqlens[b+1]-1; cu_seqlens[0] = 0,
+ *                     non-decreasing, cu_seqlens[num_seqs] = T_total.
+ *                     Zero-length sequences are allowed.
+ *   cu_seqlens_host : optional HOST copy of the same array (NULL allowed).
+ *                     When given it is validated on the host and used to
+ *                     schedule long sequences first; it must equal the device
+ *                     array.  When NULL the device validates cu_seqlens and a
+ *                     malformed array is reported by wkv7_check_device_status.
+ *   x_dtype         : WKV7_F32 or WKV7_BF16, the type of r, k, v, kk, a
+ *   r, k, v, kk, a  : x_dtype [T_total, H, N]  (token-major)
+ *   w               : fp32 [T_total, H, N]     log-decay
+ *   initial_state   : fp32 [num_seqs, H, N, N] or NULL (= zeros)
+ *   final_state     : fp32 [num_seqs, H, N, N] or NULL (not written); may be
+ *                     the same pointer as initial_state (in-place carry), but
+ *                     must not partially overlap it
+ *   o               : fp32 [T_total, H, N]     outputs of every token
+ *   workspace       : device memory of at least
+ *                     wkv7_prefill_workspace_size(...) bytes (may be NULL when
+ *                     that size is 0); its contents need not be initialised
+ *                     and are not preserved.  Calls that overlap on the GPU
+ *                     must use distinct workspaces.
+ *
+ * Precondition for the chunked formulation: w >= -2.5 elementwise (every
+ * RWKV-7 model has w in (-0.6066, 0)); see the design notes.
+ */
+WKV7_API wkv7_status wkv7_prefill(int num_seqs, int T_total, int H, int N,
+                         const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                         wkv7_dtype x_dtype,
+                         const void *r, const float *w, const void *k,
+                         const void *v, const void *kk, const void *a,
+                         const float *initial_state, float *final_state, float *o,
+                         void *workspace, size_t workspace_bytes,
+                         cudaStream_t stream);
+
+/* Static English text for a status code (never NULL). */
+WKV7_API const char *wkv7_status_string(wkv7_status status);
+
+/*
+ * wkv7_check_device_status -- synchronise `stream`, then read and clear the
+ * current device's status word.  Returns WKV7_OK, WKV7_ERR_TIMEOUT,
+ * WKV7_ERR_DEVICE_BOUNDS, WKV7_ERR_INVALID_ARG (malformed device cu_seqlens)
+ * or WKV7_ERR_CUDA (the synchronisation itself failed).
+ */
+WKV7_API wkv7_status wkv7_check_device_status(cudaStream_t stream);
+
+/* Text of the last CUDA error seen by this thread's calls ("" if none). */
+WKV7_API const char *wkv7_last_cuda_error(void);
+
+/* ABI version: 100 * major + minor. */
+WKV7_API int wkv7_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WKV7_H */

@@ -1,0 +1,131 @@
+"""WKV-7 recurrence on one NVIDIA GB300: Python binding of the C ABI.
+
+Two calls, both thin argument marshalling over ``libwkv7.so`` -- every step
+of the computation runs in the library's CUDA kernels:
+
+* :func:`step` -- one decode token for B x H heads, the fp32 state updated in
+  place;
+* :func:`prefill` -- packed variable-length sequences (``cu_seqlens``), with
+  optional initial states and final states out.
+
+Per head, with state S = [K, V] (Core AI model zoo note "Recurrent /
+linear-attention LLMs on Core AI", section 1):
+``S = diag(exp w) S - (kk*a)(kk^T S) + k v^T ; o = S^T r``.
+
+Tensors must be CUDA, contiguous, 16-byte aligned; the current torch stream
+is used.  There is no CPU path: without the CUDA library every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import WKV7Error  # noqa: F401
+
+__all__ = ["step", "prefill", "prefill_workspace_size", "check_device_status", "WKV7Error", "HEAD_SIZE"]
+
+HEAD_SIZE = 64
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need_cuda(name, t, dtype, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (no CPU path exists)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def step(r, w, k, v, kk, a, state, o=None, stream=None):
+    """One decode token: inputs fp32 [B, H, N]; ``state`` fp32 [B, H, N, N]
+    updated in place.  Returns ``o`` fp32 [B, H, N] (allocated if None)."""
+    B, H, N = r.shape
+    for name, t in (("r", r), ("w", w), ("k", k), ("v", v), ("kk", kk), ("a", a)):
+        _need_cuda(name, t, torch.float32, (B, H, N))
+    _need_cuda("state", state, torch.float32, (B, H, N, N))
+    if o is None:
+        o = torch.empty((B, H, N), device=r.device, dtype=torch.float32)
+    _need_cuda("o", o, torch.float32, (B, H, N))
+    lib = _lib.load()
+    st = lib.wkv7_step(B, H, N, _ptr(r), _ptr(w), _ptr(k), _ptr(v), _ptr(kk), _ptr(a),
+                       _ptr(state), _ptr(o), _stream(stream))
+    _lib.check(st, "wkv7_step")
+    return o
+
+
+def prefill_workspace_size(num_seqs: int, T_total: int, H: int, N: int = HEAD_SIZE) -> int:
+    return int(_lib.load().wkv7_prefill_workspace_size(num_seqs, T_total, H, N))
+
+
+def prefill(r, w, k, v, kk, a, cu_seqlens, initial_state=None, final_state=None, o=None,
+            workspace=None, cu_seqlens_host=None, want_final_state=True, stream=None):
+    """Packed varlen prefill.
+
+    r, k, v, kk, a: [T_total, H, N] fp32 or bf16 (one dtype for all five);
+    w: fp32 [T_total, H, N]; ``cu_seqlens``: int32 CUDA [num_seqs + 1].
+    ``initial_state``: fp32 [num_seqs, H, N, N] or None (zeros).
+    ``final_state``: output buffer (may be ``initial_state`` for an in-place
+    carry); allocated when None and ``want_final_state``.
+    ``cu_seqlens_host``: optional CPU int32 copy (validated on the host, used
+    for scheduling).  Returns ``(o, final_state)``.
+    """
+    T_total, H, N = r.shape
+    xdt = r.dtype
+    if xdt not in (torch.float32, torch.bfloat16):
+        raise TypeError("r, k, v, kk, a must be float32 or bfloat16")
+    for name, t in (("r", r), ("k", k), ("v", v), ("kk", kk), ("a", a)):
+        _need_cuda(name, t, xdt, (T_total, H, N))
+    _need_cuda("w", w, torch.float32, (T_total, H, N))
+    _need_cuda("cu_seqlens", cu_seqlens, torch.int32)
+    num_seqs = cu_seqlens.shape[0] - 1
+    if initial_state is not None:
+        _need_cuda("initial_state", initial_state, torch.float32, (num_seqs, H, N, N))
+    if final_state is None and want_final_state:
+        final_state = torch.empty((num_seqs, H, N, N), device=r.device, dtype=torch.float32)
+    if final_state is not None:
+        _need_cuda("final_state", final_state, torch.float32, (num_seqs, H, N, N))
+    if o is None:
+        o = torch.empty((T_total, H, N), device=r.device, dtype=torch.float32)
+    _need_cuda("o", o, torch.float32, (T_total, H, N))
+    host_ptr = None
+    if cu_seqlens_host is not None:
+        if cu_seqlens_host.device.type != "cpu" or cu_seqlens_host.dtype != torch.int32:
+            raise TypeError("cu_seqlens_host must be a CPU int32 tensor")
+        cu_seqlens_host = cu_seqlens_host.contiguous()
+        host_ptr = _ptr(cu_seqlens_host)
+    lib = _lib.load()
+    need = int(lib.wkv7_prefill_workspace_size(num_seqs, T_total, H, N))
+    ws_bytes = 0
+    if need > 0:
+        if workspace is None:
+            workspace = torch.empty(need, device=r.device, dtype=torch.uint8)
+        _need_cuda("workspace", workspace, torch.uint8)
+        ws_bytes = workspace.numel()
+    st = lib.wkv7_prefill(num_seqs, T_total, H, N, _ptr(cu_seqlens), host_ptr,
+                          _lib.BF16 if xdt == torch.bfloat16 else _lib.F32,
+                          _ptr(r), _ptr(w), _ptr(k), _ptr(v), _ptr(kk), _ptr(a),
+                          _ptr(initial_state), _ptr(final_state), _ptr(o),
+                          _ptr(workspace) if need > 0 else None, ws_bytes, _stream(stream))
+    _lib.check(st, "wkv7_prefill")
+    return o, final_state
+
+
+def check_device_status(stream=None) -> None:
+    """Synchronise the stream and raise if a kernel recorded a device-side error."""
+    st = _lib.load().wkv7_check_device_status(_stream(stream))
+    _lib.check(st, "device status")

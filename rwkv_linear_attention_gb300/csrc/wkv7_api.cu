@@ -1,0 +1,200 @@
+// Host side of the C ABI (include/wkv7.h): argument validation, the
+// per-device status word, and the launches.  No call allocates memory.
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "wkv7_internal.cuh"
+
+namespace {
+
+// One status word per device, set by kernels with atomicOr and read/cleared
+// by wkv7_check_device_status.
+__device__ unsigned g_wkv7_device_status = 0u;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_status_mutex;
+unsigned *g_status_ptr[kMaxDevices] = {};
+
+thread_local char g_last_cuda_error[256] = "";
+
+wkv7_status cuda_fail(cudaError_t e) {
+    std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s: %s", cudaGetErrorName(e),
+                  cudaGetErrorString(e));
+    return WKV7_ERR_CUDA;
+}
+
+// Device address of the status word on the current device (looked up once).
+wkv7_status status_word(unsigned **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return WKV7_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_status_mutex);
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_wkv7_device_status);
+        if (e != cudaSuccess) return cuda_fail(e);
+        g_status_ptr[dev] = static_cast<unsigned *>(p);
+    }
+    *out = g_status_ptr[dev];
+    return WKV7_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Byte ranges [p, p + n) and [q, q + m) overlap.
+bool overlaps(const void *p, size_t n, const void *q, size_t m) {
+    if (!p || !q || n == 0 || m == 0) return false;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(q);
+    return a < b + m && b < a + n;
+}
+
+constexpr long long kMaxHeads = 1ll << 30;   // B*H (or num_seqs*H) limit
+constexpr long long kMaxTokens = 1ll << 31;  // int32 token indices
+
+}  // namespace
+
+extern "C" {
+
+int wkv7_abi_version(void) { return 100; }
+
+const char *wkv7_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char *wkv7_status_string(wkv7_status s) {
+    switch (s) {
+        case WKV7_OK: return "ok";
+        case WKV7_ERR_INVALID_ARG: return "invalid argument";
+        case WKV7_ERR_UNSUPPORTED: return "unsupported (only head size N = 64 is supported)";
+        case WKV7_ERR_ALIGNMENT: return "a tensor pointer is not 16-byte aligned";
+        case WKV7_ERR_CUDA: return "CUDA error";
+        case WKV7_ERR_TIMEOUT: return "a bounded device-side wait expired";
+        case WKV7_ERR_WORKSPACE: return "workspace missing or too small";
+        case WKV7_ERR_DEVICE_BOUNDS: return "device found an index out of range";
+    }
+    return "unknown status";
+}
+
+wkv7_status wkv7_step(int B, int H, int N, const float *r, const float *w, const float *k,
+                      const float *v, const float *kk, const float *a, float *state, float *o,
+                      cudaStream_t stream) {
+    if (N != wkv7::kN) return WKV7_ERR_UNSUPPORTED;
+    if (B < 0 || H <= 0) return WKV7_ERR_INVALID_ARG;
+    const long long heads = (long long)B * H;
+    if (heads > kMaxHeads) return WKV7_ERR_INVALID_ARG;
+    if (heads == 0) return WKV7_OK;
+    const void *ptrs[8] = {r, w, k, v, kk, a, state, o};
+    for (const void *p : ptrs)
+        if (!p) return WKV7_ERR_INVALID_ARG;
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return WKV7_ERR_ALIGNMENT;
+    const size_t vec_bytes = (size_t)heads * N * sizeof(float);
+    const size_t state_bytes = vec_bytes * N;
+    const void *ins[7] = {r, w, k, v, kk, a, o};
+    for (const void *p : ins)
+        if (overlaps(state, state_bytes, p, vec_bytes)) return WKV7_ERR_INVALID_ARG;
+    for (int i = 0; i < 6; ++i)
+        if (overlaps(o, vec_bytes, ins[i], vec_bytes)) return WKV7_ERR_INVALID_ARG;
+    cudaError_t e = wkv7::launch_step(heads, r, w, k, v, kk, a, state, o, stream);
+    return e == cudaSuccess ? WKV7_OK : cuda_fail(e);
+}
+
+size_t wkv7_prefill_workspace_size(int num_seqs, int T_total, int H, int N) {
+    if (N != wkv7::kN || num_seqs < 0 || T_total < 0 || H <= 0) return 0;
+    return wkv7::prefill_workspace_bytes(num_seqs, T_total, H);
+}
+
+wkv7_status wkv7_prefill(int num_seqs, int T_total, int H, int N, const int32_t *cu_seqlens,
+                         const int32_t *cu_seqlens_host, wkv7_dtype x_dtype, const void *r,
+                         const float *w, const void *k, const void *v, const void *kk,
+                         const void *a, const float *initial_state, float *final_state,
+                         float *o, void *workspace, size_t workspace_bytes,
+                         cudaStream_t stream) {
+    if (N != wkv7::kN) return WKV7_ERR_UNSUPPORTED;
+    if (x_dtype != WKV7_F32 && x_dtype != WKV7_BF16) return WKV7_ERR_UNSUPPORTED;
+    if (num_seqs < 0 || T_total < 0 || H <= 0) return WKV7_ERR_INVALID_ARG;
+    if ((long long)num_seqs * H > kMaxHeads || (long long)T_total * H * N >= (1ll << 62))
+        return WKV7_ERR_INVALID_ARG;
+    if ((long long)T_total >= kMaxTokens) return WKV7_ERR_INVALID_ARG;
+    if (num_seqs == 0) return T_total == 0 ? WKV7_OK : WKV7_ERR_INVALID_ARG;
+    if (!cu_seqlens) return WKV7_ERR_INVALID_ARG;
+    if (T_total > 0 && (!r || !w || !k || !v || !kk || !a || !o)) return WKV7_ERR_INVALID_ARG;
+    const void *ptrs[11] = {cu_seqlens, r, w, k, v, kk, a, initial_state, final_state, o, nullptr};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return WKV7_ERR_ALIGNMENT;
+
+    if (cu_seqlens_host) {
+        if (cu_seqlens_host[0] != 0 || cu_seqlens_host[num_seqs] != T_total)
+            return WKV7_ERR_INVALID_ARG;
+        for (int b = 0; b < num_seqs; ++b)
+            if (cu_seqlens_host[b + 1] < cu_seqlens_host[b]) return WKV7_ERR_INVALID_ARG;
+    }
+
+    const size_t x_elem = x_dtype == WKV7_BF16 ? 2 : 4;
+    const size_t tok_elems = (size_t)T_total * H * N;
+    const size_t state_bytes = (size_t)num_seqs * H * N * N * sizeof(float);
+    const size_t o_bytes = tok_elems * sizeof(float);
+    // Outputs must not overlap inputs; final_state may equal initial_state
+    // exactly but must not partially overlap it.
+    const void *xins[5] = {r, k, v, kk, a};
+    for (const void *p : xins) {
+        if (overlaps(o, o_bytes, p, tok_elems * x_elem)) return WKV7_ERR_INVALID_ARG;
+        if (overlaps(final_state, state_bytes, p, tok_elems * x_elem)) return WKV7_ERR_INVALID_ARG;
+    }
+    if (overlaps(o, o_bytes, w, tok_elems * 4) || overlaps(final_state, state_bytes, w, tok_elems * 4))
+        return WKV7_ERR_INVALID_ARG;
+    if (overlaps(o, o_bytes, final_state, state_bytes) || overlaps(o, o_bytes, initial_state, state_bytes))
+        return WKV7_ERR_INVALID_ARG;
+    if (final_state != initial_state && overlaps(final_state, state_bytes, initial_state, state_bytes))
+        return WKV7_ERR_INVALID_ARG;
+    if (overlaps(o, o_bytes, cu_seqlens, (size_t)(num_seqs + 1) * 4) ||
+        overlaps(final_state, state_bytes, cu_seqlens, (size_t)(num_seqs + 1) * 4))
+        return WKV7_ERR_INVALID_ARG;
+
+    const size_t need = wkv7::prefill_workspace_bytes(num_seqs, T_total, H);
+    if (need > 0 && (!workspace || workspace_bytes < need)) return WKV7_ERR_WORKSPACE;
+    if (workspace && need > 0) {
+        if (!aligned16(workspace)) return WKV7_ERR_ALIGNMENT;
+        if (overlaps(workspace, need, o, o_bytes) || overlaps(workspace, need, final_state, state_bytes))
+            return WKV7_ERR_INVALID_ARG;
+    }
+
+    unsigned *status = nullptr;
+    wkv7_status st = status_word(&status);
+    if (st != WKV7_OK) return st;
+
+    wkv7::PrefillArgs args;
+    args.num_seqs = num_seqs;
+    args.T_total = T_total;
+    args.H = H;
+    args.cu_seqlens = cu_seqlens;
+    args.order = nullptr;
+    args.x_dtype = x_dtype;
+    args.r = r; args.w = w; args.k = k; args.v = v; args.kk = kk; args.a = a;
+    args.initial_state = initial_state;
+    args.final_state = final_state;
+    args.o = o;
+    args.status = status;
+    cudaError_t e = wkv7::launch_prefill(args, workspace, workspace_bytes, stream);
+    return e == cudaSuccess ? WKV7_OK : cuda_fail(e);
+}
+
+wkv7_status wkv7_check_device_status(cudaStream_t stream) {
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    unsigned host = 0;
+    e = cudaMemcpyFromSymbol(&host, g_wkv7_device_status, sizeof(host));
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (host) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbol(g_wkv7_device_status, &zero, sizeof(zero));
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    if (host & wkv7::kDevTimeout) return WKV7_ERR_TIMEOUT;
+    if (host & wkv7::kDevBounds) return WKV7_ERR_DEVICE_BOUNDS;
+    if (host & wkv7::kDevBadSeqlens) return WKV7_ERR_INVALID_ARG;
+    return WKV7_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,55 @@
+// Internal declarations shared by the host API and the kernel translation
+// units.  Not part of the C ABI (that is include/wkv7.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "wkv7.h"
+
+namespace wkv7 {
+
+constexpr int kN = 64;  // head size: the only one supported
+
+// Bits of the per-device status word (read by wkv7_check_device_status).
+enum : unsigned {
+    kDevTimeout = 1u,     // a bounded wait expired
+    kDevBounds = 2u,      // an index was out of range
+    kDevBadSeqlens = 4u,  // device cu_seqlens malformed
+};
+
+__device__ __forceinline__ void report(unsigned *status, unsigned bit) {
+    if (status) atomicOr(status, bit);
+}
+
+// Decode: one token for n_heads = B * H heads.
+cudaError_t launch_step(long long n_heads, const float *r, const float *w, const float *k,
+                        const float *v, const float *kk, const float *a, float *state,
+                        float *o, cudaStream_t stream);
+
+struct PrefillArgs {
+    int num_seqs;
+    int T_total;
+    int H;
+    const int32_t *cu_seqlens;   // device [num_seqs + 1]
+    const int32_t *order;        // device [num_seqs] schedule (longest first) or nullptr
+    wkv7_dtype x_dtype;
+    const void *r;
+    const float *w;
+    const void *k;
+    const void *v;
+    const void *kk;
+    const void *a;
+    const float *initial_state;  // nullable
+    float *final_state;          // nullable
+    float *o;
+    unsigned *status;            // device status word
+};
+
+// Prefill: the chunked tensor-core kernel.
+cudaError_t launch_prefill(const PrefillArgs &args, void *workspace, size_t workspace_bytes,
+                           cudaStream_t stream);
+size_t prefill_workspace_bytes(int num_seqs, int T_total, int H);
+
+}  // namespace wkv7

@@ -102,3 +102,11 @@ def prefill_inputs(seqlens, H: int, N: int = 64, seed: int = 1002, device="cpu",
     out = draw_rwkkva((T_total, H, N), seed, device, x_dtype=x_dtype)
     out["cu_seqlens"] = cu
     return out
+
+
+# Workload shapes of the five named configurations.
+DECODE_2P9B = dict(layers=32, H=40, N=64, batches=(1, 8, 32), warm_tokens=256, pool=16, steps=1024)
+PREFILL_2P9B = dict(num_seqs=8, T=4096, H=40, N=64)
+DECODE_7P2B = dict(layers=32, H=64, N=64, B=256, pool=16, steps=1024, state_std=0.1)
+VARLEN_7P2B = dict(num_seqs=16, lo=1, hi=32768, H=64, N=64, single_T=32768, state_std=0.1)
+SMALL_0P1B = dict(B=1, T=64, H=12, N=64)

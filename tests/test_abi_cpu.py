@@ -1,0 +1,159 @@
+"""The C-ABI library builds, loads and exports every declared symbol; host-side
+argument checks return the documented status codes.  No GPU is needed: every
+call here is rejected on the host before any CUDA call is made."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from rwkv_linear_attention_gb300 import _lib
+from rwkv_linear_attention_gb300 import build as cuda_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "wkv7.h")
+
+FAKE = 0x10000  # a 16-byte-aligned address that is never dereferenced
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cuda_build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"WKV7_API\s+[\w\s\*]+?\b(wkv7_\w+)\s*\(", text)))
+
+
+def test_header_declares_expected_entry_points():
+    names = declared_functions()
+    assert set(names) == set(_lib.EXPORTS), names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} not exported"
+
+
+def test_no_torch_types_in_the_abi():
+    text = open(HEADER).read()
+    assert "torch" not in text.lower().replace("pytorch", "")
+    assert "at::" not in text and "Tensor" not in text
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        s = lib.wkv7_status_string(code)
+        assert s and isinstance(s, bytes)
+    assert lib.wkv7_status_string(0) == b"ok"
+    assert lib.wkv7_abi_version() == 100
+
+
+def _step(lib, B=2, H=3, N=64, ptrs=None):
+    ptrs = ptrs or [FAKE + i * (1 << 24) for i in range(8)]
+    P = ctypes.c_void_p
+    return lib.wkv7_step(B, H, N, *[P(p) for p in ptrs], P(0))
+
+
+def test_step_rejects_unsupported_head_size(lib):
+    assert _step(lib, N=32) == _lib.ERR_UNSUPPORTED
+    assert _step(lib, N=128) == _lib.ERR_UNSUPPORTED
+
+
+def test_step_rejects_bad_sizes_and_nulls(lib):
+    assert _step(lib, B=-1) == _lib.ERR_INVALID_ARG
+    assert _step(lib, H=0) == _lib.ERR_INVALID_ARG
+    ptrs = [FAKE + i * (1 << 24) for i in range(8)]
+    for i in range(8):
+        bad = list(ptrs)
+        bad[i] = 0
+        assert _step(lib, ptrs=bad) == _lib.ERR_INVALID_ARG
+
+
+def test_step_zero_batch_is_noop(lib):
+    assert _step(lib, B=0) == _lib.OK
+
+
+def test_step_rejects_misaligned(lib):
+    ptrs = [FAKE + i * (1 << 24) for i in range(8)]
+    for i in range(8):
+        bad = list(ptrs)
+        bad[i] += 4
+        assert _step(lib, ptrs=bad) == _lib.ERR_ALIGNMENT
+
+
+def test_step_rejects_state_aliasing_an_input(lib):
+    ptrs = [FAKE + i * (1 << 24) for i in range(8)]
+    ptrs[6] = ptrs[3]  # state over v
+    assert _step(lib, ptrs=ptrs) == _lib.ERR_INVALID_ARG
+
+
+def _prefill(lib, num_seqs=2, T=10, H=2, N=64, cu_host=None, dtype=_lib.BF16, ptrs=None,
+             s0=None, sf=None, ws=None, ws_bytes=0):
+    P = ctypes.c_void_p
+    base = ptrs or [FAKE + i * (1 << 26) for i in range(8)]
+    host = None
+    if cu_host is not None:
+        arr = (ctypes.c_int32 * len(cu_host))(*cu_host)
+        host = ctypes.cast(arr, P)
+    return lib.wkv7_prefill(num_seqs, T, H, N, P(base[0]), host, dtype,
+                            *[P(p) for p in base[1:7]], P(s0), P(sf), P(base[7]),
+                            P(ws), ws_bytes, P(0))
+
+
+def test_prefill_rejects_unsupported(lib):
+    assert _prefill(lib, N=48) == _lib.ERR_UNSUPPORTED
+    assert _prefill(lib, dtype=7) == _lib.ERR_UNSUPPORTED
+
+
+def test_prefill_rejects_malformed_host_cu_seqlens(lib):
+    assert _prefill(lib, cu_host=[0, 6, 4]) == _lib.ERR_INVALID_ARG   # decreasing and wrong total
+    assert _prefill(lib, cu_host=[1, 5, 10]) == _lib.ERR_INVALID_ARG  # does not start at 0
+    assert _prefill(lib, cu_host=[0, 5, 9]) == _lib.ERR_INVALID_ARG   # does not end at T_total
+    assert _prefill(lib, cu_host=[0, 7, 6, 10][:3] + [10], num_seqs=3) == _lib.ERR_INVALID_ARG
+
+
+def test_prefill_rejects_misaligned_and_null(lib):
+    ptrs = [FAKE + i * (1 << 26) for i in range(8)]
+    for i in range(8):
+        bad = list(ptrs)
+        bad[i] += 2
+        assert _prefill(lib, ptrs=bad, cu_host=[0, 4, 10]) == _lib.ERR_ALIGNMENT
+    bad = list(ptrs)
+    bad[0] = 0
+    assert _prefill(lib, ptrs=bad) == _lib.ERR_INVALID_ARG
+
+
+def test_prefill_rejects_partial_state_overlap(lib):
+    s0 = FAKE + 40 * (1 << 26)
+    assert _prefill(lib, cu_host=[0, 4, 10], s0=s0, sf=s0 + 256) == _lib.ERR_INVALID_ARG
+
+
+def test_prefill_rejects_output_over_input(lib):
+    ptrs = [FAKE + i * (1 << 26) for i in range(8)]
+    ptrs[7] = ptrs[1]  # o over r
+    assert _prefill(lib, ptrs=ptrs, cu_host=[0, 4, 10]) == _lib.ERR_INVALID_ARG
+
+
+def test_prefill_empty_batch(lib):
+    assert _prefill(lib, num_seqs=0, T=0) == _lib.OK
+    assert _prefill(lib, num_seqs=0, T=5) == _lib.ERR_INVALID_ARG
+
+
+def test_workspace_size_is_pure(lib):
+    a = lib.wkv7_prefill_workspace_size(8, 32768, 40, 64)
+    b = lib.wkv7_prefill_workspace_size(8, 32768, 40, 64)
+    assert a == b
+    assert lib.wkv7_prefill_workspace_size(8, 32768, 40, 32) == 0
+
+
+def test_product_package_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "rwkv_linear_attention_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "wkv7_oracle" not in text, f

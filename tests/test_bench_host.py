@@ -1,0 +1,80 @@
+"""Host-side logic of bench.py: the multi-rank timing reduction (gloo,
+world_size 2, on CPU), clock parsing, the traffic record guard."""
+import json
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    r, w, _ = bench.dist_env()
+    assert (r, w) == (rank, world)
+    bench.barrier(world)
+    m = bench.max_over_ranks(10.0 + 5.0 * rank, world)
+    out[rank] = m
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world2():
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as mgr:
+        out = mgr.dict()
+        procs = [ctx.Process(target=_worker, args=(r, 2, port, out)) for r in range(2)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(timeout=120)
+            assert p.exitcode == 0
+        assert out[0] == out[1] == 15.0
+
+
+def test_single_rank_is_identity():
+    assert bench.max_over_ranks(3.5, 1) == 3.5
+
+
+def test_summarize_clocks():
+    lines = ["0, 1965, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+             "0, 1905, 2070, 1200.0, 0x4, Not Active, Not Active, Not Active, Active",
+             "garbage"]
+    c = bench.summarize_clocks(lines)
+    assert c["samples"] == 2 and c["sm_max_mhz"] == 2070.0
+    assert c["sm_mhz"] == 1935.0 and c["reasons"] == ["sw_power_cap"]
+    assert bench.summarize_clocks([])["samples"] == 0
+
+
+def test_traffic_record_requires_matching_source(tmp_path, monkeypatch):
+    src = tmp_path / "k.cu"
+    src.write_text("kernel v1")
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    rec = {"kern": {"wl": {"source_digest": bench.source_digest([str(src)]), "dram_bytes_per_launch": 123.0}}}
+    (prof / "traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.kernel_traffic("kern", "wl", [str(src)]) == 123.0
+    src.write_text("kernel v2")
+    assert bench.kernel_traffic("kern", "wl", [str(src)]) is None
+
+
+def test_byte_and_flop_constants():
+    assert bench.STEP_BYTES == 34560
+    assert bench.PREFILL_BYTES_PER_TOKEN_HEAD == 1152
+    assert bench.PREFILL_FLOP_PER_TOKEN_HEAD == 106496
+
+
+def test_warmup_floor():
+    with pytest.raises(SystemExit):
+        bench.main(["--warmup", "2"])
