@@ -47,6 +47,9 @@ struct PrefillArgs {
     unsigned *status;            // device status word
 };
 
+// Prefill, token-serial form (one warp per 16-column slice, tokens in order).
+cudaError_t launch_prefill_scan(const PrefillArgs &args, cudaStream_t stream);
+
 // Prefill: the chunked tensor-core kernel.
 cudaError_t launch_prefill(const PrefillArgs &args, void *workspace, size_t workspace_bytes,
                            cudaStream_t stream);

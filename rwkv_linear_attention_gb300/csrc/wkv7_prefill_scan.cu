@@ -184,9 +184,7 @@ wkv7_prefill_scan_kernel(PrefillArgs p) {
 
 }  // namespace
 
-size_t prefill_workspace_bytes(int, int, int) { return 0; }
-
-cudaError_t launch_prefill(const PrefillArgs &args, void *, size_t, cudaStream_t stream) {
+cudaError_t launch_prefill_scan(const PrefillArgs &args, cudaStream_t stream) {
     const long long pairs = (long long)args.num_seqs * args.H;
     if (pairs <= 0) return cudaSuccess;
     if (args.x_dtype == WKV7_BF16)
