@@ -353,6 +353,14 @@ def run_ours(args):
 
     from rwkv_linear_attention_gb300 import inputs
     peaks, peak_kind = load_peaks()
+    if args.workload == "prefill":
+        pre = prefill_bench(dev, args.prefill_steps, args.warmup, world)
+        if rank == 0:
+            gbs = pre["algorithmic_bytes"] / (pre["ms_per_call"] / 1e3) / 1e9
+            print(json.dumps({"workload": "prefill 2.9B (8 x 4096, H=40, bf16)", "ms_per_call": pre["ms_per_call"],
+                              "tokens_per_s": world * pre["tokens"] / (pre["ms_per_call"] / 1e3),
+                              "achieved_gbs": gbs, "frac": gbs / peaks["hbm_gbs"]}), flush=True)
+        return
     cfg = inputs.DECODE_2P9B
     B = args.batch
     wl = DecodeWorkload(cfg["layers"], B, cfg["H"], cfg["pool"], dev, seed=1001 + rank)
@@ -374,6 +382,12 @@ def run_ours(args):
     traffic = kernel_traffic("wkv7_step_kernel", f"B={B},H={cfg['H']}", step_src)
     del graphs
 
+    if args.workload == "decode":
+        if rank == 0:
+            print(json.dumps({"workload": f"decode 2.9B B={B}", "ms_per_step": ms_step, "value_gbs": value,
+                              "achieved_gbs": achieved, "frac": achieved / peaks["hbm_gbs"], "clocks": clocks}),
+                  flush=True)
+        return
     e2e_ms, h2d, d2h = decode_e2e(wl, max(args.steps // 4, 8), args.warmup, stream, world)
     e2e_ms = max_over_ranks(e2e_ms, world, dev)
     e2e_steps = max(args.steps // 4, 8)
@@ -495,6 +509,8 @@ def main(argv=None):
     ap.add_argument("--prefill-steps", type=int, default=20)
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=("all", "decode", "prefill"), default="all",
+                    help="all (the contract line); decode or prefill alone, for profiling")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

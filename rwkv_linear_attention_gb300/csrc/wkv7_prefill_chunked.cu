@@ -36,6 +36,9 @@
 // TMA (2-D tiles of 64 tokens x 64 channels of the packed [T, H, 64] arrays);
 // the next chunk's tiles load while the current chunk's last phases run.
 //
+// Inputs r, k, v, kk, a are bf16 (w fp32); fp32-input prefill is served by
+// the token-serial kernel instead.
+//
 // Precision: inputs are used exactly; every MMA operand is rounded to tf32
 // (round to nearest) and accumulates in fp32.  The decay factors of the Gram
 // operands are taken relative to the chunk's middle token, so for
@@ -85,7 +88,7 @@ struct Layout {
     static constexpr int kAlloc = kBytes + 1024;   // slack to align the base to 1024 B
     static constexpr uint32_t kTmaBytes = 5 * kTile + 16384;
 };
-static_assert(Layout<4>::kAlloc <= 232448, "fp32 layout exceeds shared memory");
+static_assert(Layout<2>::kAlloc <= 232448, "layout exceeds shared memory");
 
 __device__ __forceinline__ uint32_t to_tf32(float x) {
     uint32_t r;
@@ -95,6 +98,9 @@ __device__ __forceinline__ uint32_t to_tf32(float x) {
 __device__ __forceinline__ void st_tf32x4(unsigned char *p, float a, float b, float c, float d) {
     *reinterpret_cast<uint4 *>(p) = make_uint4(to_tf32(a), to_tf32(b), to_tf32(c), to_tf32(d));
 }
+// Reciprocal of a decay factor (fast approximate divide, ~2 ulp).  Its
+// result only feeds tf32 operands, whose rounding (2^-11) dominates.
+__device__ __forceinline__ float rcp(float x) { return __fdividef(1.f, x); }
 __device__ __forceinline__ float4 ld_f4(const unsigned char *p) {
     return *reinterpret_cast<const float4 *>(p);
 }
@@ -102,16 +108,6 @@ __device__ __forceinline__ float4 ld_f4(const unsigned char *p) {
 // Raw input access (row-major [64 tokens][64 channels] tile of x).
 template <typename X>
 struct Raw;
-template <>
-struct Raw<float> {
-    static constexpr int kB = 4;
-    __device__ static float4 ld4(const unsigned char *tile, int t, int i) {
-        return *reinterpret_cast<const float4 *>(tile + (t * 64 + i) * 4);
-    }
-    __device__ static float ld1(const unsigned char *tile, int t, int i) {
-        return *reinterpret_cast<const float *>(tile + (t * 64 + i) * 4);
-    }
-};
 template <>
 struct Raw<__nv_bfloat16> {
     static constexpr int kB = 2;
@@ -291,7 +287,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
                 if (t > 0) {
                     ep = ld_f4(reinterpret_cast<unsigned char *>(Et + (t - 1) * 64 + i));
                 } else {
-                    ep = make_float4(1.f / eref[i], 1.f / eref[i + 1], 1.f / eref[i + 2], 1.f / eref[i + 3]);
+                    ep = make_float4(rcp(eref[i]), rcp(eref[i + 1]), rcp(eref[i + 2]), rcp(eref[i + 3]));
                 }
                 const float4 xr = RawX::ld4(rr, t, i), xk = RawX::ld4(rk, t, i);
                 const float4 xkk = RawX::ld4(rkk, t, i), xa = RawX::ld4(ra, t, i);
@@ -299,10 +295,10 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
                           valid * xr.z * e.z, valid * xr.w * e.w);
                 st_tf32x4(AG + sw128_off(64 + t, i, 128), valid * xkk.x * ep.x, valid * xkk.y * ep.y,
                           valid * xkk.z * ep.z, valid * xkk.w * ep.w);
-                st_tf32x4(BG + sw128_off(t, i, 128), valid * xkk.x * xa.x / e.x, valid * xkk.y * xa.y / e.y,
-                          valid * xkk.z * xa.z / e.z, valid * xkk.w * xa.w / e.w);
-                st_tf32x4(BG + sw128_off(64 + t, i, 128), valid * xk.x / e.x, valid * xk.y / e.y,
-                          valid * xk.z / e.z, valid * xk.w / e.w);
+                const float4 ei = make_float4(valid * rcp(e.x), valid * rcp(e.y), valid * rcp(e.z), valid * rcp(e.w));
+                st_tf32x4(BG + sw128_off(t, i, 128), xkk.x * xa.x * ei.x, xkk.y * xa.y * ei.y,
+                          xkk.z * xa.z * ei.z, xkk.w * xa.w * ei.w);
+                st_tf32x4(BG + sw128_off(64 + t, i, 128), xk.x * ei.x, xk.y * ei.y, xk.z * ei.z, xk.w * ei.w);
             }
             // V^T: B_chain[j][64 + s] = v[s][j]
 #pragma unroll
@@ -336,28 +332,23 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
             unsigned char *BY = sm + L::P + 32768;
             if (q >= 2) {
                 const int t = 32 * (q - 2) + lane;  // Q rows of G sit in TMEM lanes 64..127
-                float v[32];
-                for (int half = 0; half < 2; ++half) {
-                    tmem_ld32(tmem + lane_off + kColG + 64 * hf + 32 * half, v);
-                    if (hf == 0) {  // L_c[t][s], s < t
+                float v[64];
+                tmem_ld64(tmem + lane_off + kColG + 64 * hf, v);
+                if (hf == 0) {  // L_c[t][s], s < t
 #pragma unroll
-                        for (int j = 0; j < 32; j += 4) {
-                            const int s0 = 32 * half + j;
-                            float4 x;
-                            x.x = (s0 < t) ? v[j] : 0.f;
-                            x.y = (s0 + 1 < t) ? v[j + 1] : 0.f;
-                            x.z = (s0 + 2 < t) ? v[j + 2] : 0.f;
-                            x.w = (s0 + 3 < t) ? v[j + 3] : 0.f;
-                            *reinterpret_cast<float4 *>(LC + t * kLd + s0) = x;
-                        }
-                    } else {  // B_Y[64 + s][t] = L_k[t][s]
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const int sidx = 32 * half + j;
-                            *reinterpret_cast<uint32_t *>(BY + sw128_off(64 + sidx, t, 128)) =
-                                to_tf32(sidx < t ? v[j] : 0.f);
-                        }
+                    for (int s0 = 0; s0 < 64; s0 += 4) {
+                        float4 x;
+                        x.x = (s0 < t) ? v[s0] : 0.f;
+                        x.y = (s0 + 1 < t) ? v[s0 + 1] : 0.f;
+                        x.z = (s0 + 2 < t) ? v[s0 + 2] : 0.f;
+                        x.w = (s0 + 3 < t) ? v[s0 + 3] : 0.f;
+                        *reinterpret_cast<float4 *>(LC + t * kLd + s0) = x;
                     }
+                } else {  // B_Y[64 + s][t] = L_k[t][s]
+#pragma unroll
+                    for (int sidx = 0; sidx < 64; ++sidx)
+                        *reinterpret_cast<uint32_t *>(BY + sw128_off(64 + sidx, t, 128)) =
+                            to_tf32(sidx < t ? v[sidx] : 0.f);
                 }
             } else {
                 // Qa^T: B_Y[i][t] = kk[t][i] e^{g_{t-1}[i]}  (= kk * E[t-1] * eref, or kk at t = 0)
@@ -382,62 +373,100 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
         fence_proxy_async_smem();
         __syncthreads();
 
-        // ---- phase 4: T = (I + L_c)^{-1}, blocked by 16; T kept in TS (fp32), then T^T -> BX
+        // ---- phase 4: T = (I + L_c)^{-1} in fp32 (TS), then T^T -> BX.
+        // Diagonal 16x16 blocks by right-looking substitution in registers;
+        // then the 32x32 halves T_A, T_B (T_10 = -T_11 L_10 T_00, likewise
+        // T_32), then T_BA = -T_B (L_BA T_A).  Only lower-triangular entries of
+        // TS are ever written or read; T^T takes zeros above the diagonal.
         {
             const float *LC = reinterpret_cast<const float *>(sm + L::AX);
             float *TS = reinterpret_cast<float *>(sm + L::P);
-            float *XS = reinterpret_cast<float *>(sm + L::P + 64 * kLd * 4);
+            float *XS = reinterpret_cast<float *>(sm + L::P + 64 * kLd * 4);  // 32 x 32 scratch
             if (tid < 64) {
-                const int bb = tid >> 4, j = tid & 15;
+                const int bb = tid >> 4, j = tid & 15, o = 16 * bb;
                 float x[16];
 #pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    float acc = (t == j) ? 1.f : 0.f;
+                for (int t = 0; t < 16; ++t) x[t] = (t == j) ? 1.f : 0.f;
 #pragma unroll
-                    for (int u = 0; u < t; ++u) acc = fmaf(-LC[(16 * bb + t) * kLd + 16 * bb + u], x[u], acc);
-                    x[t] = acc;
+                for (int u = 0; u < 15; ++u) {
+#pragma unroll
+                    for (int t = u + 1; t < 16; ++t) x[t] = fmaf(-LC[(o + t) * kLd + o + u], x[u], x[t]);
                 }
 #pragma unroll
-                for (int t = 0; t < 16; ++t) TS[(16 * bb + t) * kLd + 16 * bb + j] = x[t];
-            } else {
-                // zero the strictly upper blocks (bi < bj)
-                for (int e = tid - 64; e < 6 * 256; e += kThreads - 64) {
-                    const int blk = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-                    const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-                    const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-                    TS[(16 * bi + r) * kLd + 16 * bj + cc] = 0.f;
-                }
+                for (int t = 0; t < 16; ++t)
+                    if (t >= j) TS[(o + t) * kLd + o + j] = x[t];
             }
             __syncthreads();
-            for (int d = 1; d <= 3; ++d) {
-                const int nblk = 4 - d;
-                for (int e = tid; e < nblk * 256; e += kThreads) {
-                    const int bj = e >> 8, r = (e >> 4) & 15, cc = e & 15, bi = bj + d;
-                    float acc = 0.f;
-                    for (int kb = bj; kb < bi; ++kb) {
+            // Y1 = L_10 T_00 -> XS[0..255], Y3 = L_32 T_22 -> XS[256..511]  (T lower triangular:
+            // entries above the diagonal are never written, so they are masked, not read as zero)
+            {
+                const int blk = tid >> 7, r = (tid >> 3) & 15, c0 = (tid & 7) * 2;
+                const int o = 32 * blk;  // block (1,0) at rows 16.., cols 0..; block (3,2) at rows 48.., cols 32..
+                float y0 = 0.f, y1 = 0.f;
 #pragma unroll
-                        for (int u = 0; u < 16; ++u)
-                            acc = fmaf(LC[(16 * bi + r) * kLd + 16 * kb + u], TS[(16 * kb + u) * kLd + 16 * bj + cc], acc);
-                    }
-                    XS[e] = acc;
+                for (int u = 0; u < 16; ++u) {
+                    const float l = LC[(o + 16 + r) * kLd + o + u];
+                    const float2 tt = *reinterpret_cast<const float2 *>(TS + (o + u) * kLd + o + c0);
+                    y0 = fmaf(l, u >= c0 ? tt.x : 0.f, y0);
+                    y1 = fmaf(l, u > c0 ? tt.y : 0.f, y1);
                 }
-                __syncthreads();
-                for (int e = tid; e < nblk * 256; e += kThreads) {
-                    const int bj = e >> 8, r = (e >> 4) & 15, cc = e & 15, bi = bj + d;
-                    float acc = 0.f;
-#pragma unroll
-                    for (int u = 0; u < 16; ++u)
-                        acc = fmaf(TS[(16 * bi + r) * kLd + 16 * bi + u], XS[(bj << 8) + (u << 4) + cc], acc);
-                    TS[(16 * bi + r) * kLd + 16 * bj + cc] = -acc;
-                }
-                __syncthreads();
+                *reinterpret_cast<float2 *>(XS + blk * 256 + r * 16 + c0) = make_float2(y0, y1);
             }
-            // T^T into BX: BX[n][k] = T[k][n]
+            __syncthreads();
+            // T_10 = -T_11 Y1, T_32 = -T_33 Y3
+            {
+                const int blk = tid >> 7, r = (tid >> 3) & 15, c0 = (tid & 7) * 2;
+                const int o = 32 * blk;
+                float t0 = 0.f, t1 = 0.f;
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const float a = u <= r ? TS[(o + 16 + r) * kLd + o + 16 + u] : 0.f;
+                    const float2 y = *reinterpret_cast<const float2 *>(XS + blk * 256 + u * 16 + c0);
+                    t0 = fmaf(a, y.x, t0);
+                    t1 = fmaf(a, y.y, t1);
+                }
+                *reinterpret_cast<float2 *>(TS + (o + 16 + r) * kLd + o + c0) = make_float2(-t0, -t1);
+            }
+            __syncthreads();
+            // Z = L_BA T_A (32 x 32) -> XS
+            {
+                const int r = tid >> 3, c0 = (tid & 7) * 4;
+                float z0 = 0.f, z1 = 0.f, z2 = 0.f, z3 = 0.f;
+#pragma unroll
+                for (int u = 0; u < 32; ++u) {
+                    const float l = LC[(32 + r) * kLd + u];
+                    const float4 tA = *reinterpret_cast<const float4 *>(TS + u * kLd + c0);
+                    z0 = fmaf(l, u >= c0 ? tA.x : 0.f, z0);
+                    z1 = fmaf(l, u >= c0 + 1 ? tA.y : 0.f, z1);
+                    z2 = fmaf(l, u >= c0 + 2 ? tA.z : 0.f, z2);
+                    z3 = fmaf(l, u >= c0 + 3 ? tA.w : 0.f, z3);
+                }
+                *reinterpret_cast<float4 *>(XS + r * 32 + c0) = make_float4(z0, z1, z2, z3);
+            }
+            __syncthreads();
+            // T_BA = -T_B Z
+            {
+                const int r = tid >> 3, c0 = (tid & 7) * 4;
+                float t0 = 0.f, t1 = 0.f, t2 = 0.f, t3 = 0.f;
+#pragma unroll
+                for (int u = 0; u < 32; ++u) {
+                    const float a = u <= r ? TS[(32 + r) * kLd + 32 + u] : 0.f;
+                    const float4 z = *reinterpret_cast<const float4 *>(XS + u * 32 + c0);
+                    t0 = fmaf(a, z.x, t0);
+                    t1 = fmaf(a, z.y, t1);
+                    t2 = fmaf(a, z.z, t2);
+                    t3 = fmaf(a, z.w, t3);
+                }
+                *reinterpret_cast<float4 *>(TS + (32 + r) * kLd + c0) = make_float4(-t0, -t1, -t2, -t3);
+            }
+            __syncthreads();
+            // T^T into BX: BX[n][k] = T[k][n] (zero above the diagonal)
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 const int n = tid & 63, kc = (tid >> 6) + 4 * m, k0 = 4 * kc;
-                st_tf32x4(sm + L::BX + sw128_off(n, k0, 64), TS[k0 * kLd + n], TS[(k0 + 1) * kLd + n],
-                          TS[(k0 + 2) * kLd + n], TS[(k0 + 3) * kLd + n]);
+                st_tf32x4(sm + L::BX + sw128_off(n, k0, 64), k0 >= n ? TS[k0 * kLd + n] : 0.f,
+                          k0 + 1 >= n ? TS[(k0 + 1) * kLd + n] : 0.f, k0 + 2 >= n ? TS[(k0 + 2) * kLd + n] : 0.f,
+                          k0 + 3 >= n ? TS[(k0 + 3) * kLd + n] : 0.f);
             }
             __syncthreads();  // LC (in AX) is dead from here on
         }
@@ -447,16 +476,12 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
             unsigned char *AXo = sm + L::AX;
             if (q < 2 && hf == 0) {
                 const int t = 32 * q + lane;  // R rows of G sit in TMEM lanes 0..63
-                float v[32];
-                for (int half = 0; half < 2; ++half) {
-                    tmem_ld32(tmem + lane_off + kColG + 32 * half, v);
+                float v[64];
+                tmem_ld64(tmem + lane_off + kColG, v);
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4) {
-                        const int s0 = 32 * half + j;
-                        st_tf32x4(AXo + sw128_off(t, s0, 128), s0 <= t ? v[j] : 0.f, s0 + 1 <= t ? v[j + 1] : 0.f,
-                                  s0 + 2 <= t ? v[j + 2] : 0.f, s0 + 3 <= t ? v[j + 3] : 0.f);
-                    }
-                }
+                for (int s0 = 0; s0 < 64; s0 += 4)
+                    st_tf32x4(AXo + sw128_off(t, s0, 128), s0 <= t ? v[s0] : 0.f, s0 + 1 <= t ? v[s0 + 1] : 0.f,
+                              s0 + 2 <= t ? v[s0 + 2] : 0.f, s0 + 3 <= t ? v[s0 + 3] : 0.f);
             } else {
                 // Cb^T[i][s] = kk[s][i] a[s][i] e^{g_C[i] - g_s[i]} = c * E[63][i] / E[s][i]
                 const int idx = tid - 64;  // warps 2..7 -> 0..191
@@ -467,7 +492,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         const int ss = s0 + u;
-                        x[u] = (ss < lc) ? RawX::ld1(rkk, ss, i) * RawX::ld1(ra, ss, i) * (e63 / Et[ss * 64 + i]) : 0.f;
+                        x[u] = (ss < lc) ? RawX::ld1(rkk, ss, i) * RawX::ld1(ra, ss, i) * (e63 * rcp(Et[ss * 64 + i])) : 0.f;
                     }
                     st_tf32x4(AXo + sw128_off(64 + i, s0, 128), x[0], x[1], x[2], x[3]);
                 }
@@ -540,7 +565,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int ss = s0 + u;
-                    x[u] = (ss < lc) ? RawX::ld1(rk, ss, i) * (e63 / Et[ss * 64 + i]) : 0.f;
+                    x[u] = (ss < lc) ? RawX::ld1(rk, ss, i) * (e63 * rcp(Et[ss * 64 + i])) : 0.f;
                 }
                 *reinterpret_cast<float4 *>(AC + sw128_off(64 + i, 64 + s0, 128)) = make_float4(x[0], x[1], x[2], x[3]);
             }
@@ -700,8 +725,10 @@ cudaError_t launch_prefill(const PrefillArgs &args, void *, size_t, cudaStream_t
         if (args.initial_state == args.final_state) return cudaSuccess;
         return cudaMemcpyAsync(args.final_state, args.initial_state, state_bytes, cudaMemcpyDeviceToDevice, stream);
     }
+    // bf16 inputs (the prefill format) take the chunked tensor-core kernel;
+    // fp32 inputs take the exact token-serial kernel.
     if (args.x_dtype == WKV7_BF16) return launch_typed<__nv_bfloat16>(args, stream);
-    return launch_typed<float>(args, stream);
+    return launch_prefill_scan(args, stream);
 }
 
 }  // namespace wkv7
