@@ -26,7 +26,7 @@ __device__ __forceinline__ void report(unsigned *status, unsigned bit) {
 // Decode: one token for n_heads = B * H heads.
 cudaError_t launch_step(long long n_heads, const float *r, const float *w, const float *k,
                         const float *v, const float *kk, const float *a, float *state,
-                        float *o, cudaStream_t stream);
+                        float *o, unsigned *status, cudaStream_t stream);
 
 struct PrefillArgs {
     int num_seqs;

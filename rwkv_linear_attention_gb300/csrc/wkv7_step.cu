@@ -6,128 +6,239 @@
 //     z = kk^T S ;  S' = diag(exp w) S - (kk .* a) z^T + k v^T ;  o = S'^T r
 //
 // The step moves 32 KB of state per head (read + write) against 1.8 KB of
-// vectors, so it is bound by HBM bandwidth.  Work split: the 64 value columns
-// of a head evolve independently given the per-row vectors, so a head is cut
-// into four 16-column slices and each slice is one warp's private problem --
-// no shared memory and no block-level barrier.  Lane L owns the eight key rows
-// 8*(L>>2) .. 8*(L>>2)+7 and the four value columns 4*(L&3) .. +3 of its
-// slice, i.e. eight float4 (128-bit) words of state.  Each warp load
-// instruction covers eight rows x 64 contiguous bytes.  The two reductions
-// over the key rows (kk^T S and S'^T r) are a per-lane sum over eight rows
-// followed by three xor-shuffles across the row groups.
+// vectors: it is bound by HBM bandwidth, so the kernel is built around
+// keeping enough bytes in flight on every SM regardless of register
+// pressure.  It is persistent: CTA c owns heads c, c + G, c + 2G, ... (G =
+// grid size, a multiple of the SM count), and streams them through a
+// four-stage shared-memory ring.  One thread issues 1-D bulk async copies
+// (the head's 16 KB state plus its six 256-byte input vectors) into a stage
+// and the stage's mbarrier completes when the bytes land; the four warps
+// compute; the new state goes back to global memory with one bulk async store
+// from the same stage.  While one head is computed, the next three are in
+// flight.
+//
+// Compute split (unchanged from the register form): the 64 value columns of a
+// head evolve independently given the per-row vectors, so warp w owns columns
+// 16w .. 16w+15; lane L holds key rows 8*(L>>2) .. +7 and columns 4*(L&3) ..
+// +3 of that slice; the two reductions over key rows (kk^T S and S'^T r) are
+// a per-lane sum over eight rows and three xor-shuffles.
+//
+// Launch order: programmatic dependent launch.  The kernel waits for the
+// preceding grid (griddepcontrol.wait) before it touches global memory, so
+// back-to-back calls on the same state stay ordered, while the launch and
+// block scheduling of the next call overlap the tail of this one.
+#include <cuda_runtime.h>
+
+#include "sm103_ptx.cuh"
 #include "wkv7_internal.cuh"
 
 namespace wkv7 {
 namespace {
 
-constexpr int kWarpsPerBlock = 4;  // one head per 128-thread block
-constexpr int kSlices = 4;         // 16-column slices per head
+using namespace ptx;
 
-__device__ __forceinline__ float4 ld_state(const float *p) {
-    return *reinterpret_cast<const float4 *>(p);
-}
-__device__ __forceinline__ void st_state(float *p, const float4 &x) {
-    *reinterpret_cast<float4 *>(p) = x;
-}
-__device__ __forceinline__ float4 ld_in(const float *p) {
-    return __ldg(reinterpret_cast<const float4 *>(p));
-}
+constexpr int kThreads = 128;
+constexpr int kStages = 4;
+constexpr uint32_t kStateBytes = kN * kN * 4;  // 16 KB
+constexpr uint32_t kVecBytes = kN * 4;         // 256 B
+constexpr uint32_t kMaxPolls = 1u << 24;
+
+struct Stage {
+    float S[kN * kN];
+    float vec[6][kN];  // r, w, k, v, kk, a
+};
+static_assert(sizeof(Stage) % 128 == 0, "stage size");
+constexpr size_t kSmemBytes = kStages * sizeof(Stage) + kStages * sizeof(unsigned long long);
+
 __device__ __forceinline__ float comp(const float4 &x, int c) {
     return c == 0 ? x.x : c == 1 ? x.y : c == 2 ? x.z : x.w;
 }
 
-__global__ void __launch_bounds__(kWarpsPerBlock * 32)
-wkv7_step_kernel(long long n_units, const float *__restrict__ r, const float *__restrict__ w,
+__global__ void __launch_bounds__(kThreads)
+wkv7_step_kernel(long long n_heads, const float *__restrict__ r, const float *__restrict__ w,
                  const float *__restrict__ k, const float *__restrict__ v,
                  const float *__restrict__ kk, const float *__restrict__ a,
-                 float *__restrict__ state, float *__restrict__ o) {
-    const int lane = threadIdx.x & 31;
-    const long long unit = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-    if (unit >= n_units) return;
-    const long long head = unit / kSlices;
-    const int slice = (int)(unit % kSlices);
-    const int rg = lane >> 2;         // row group: rows 8*rg .. 8*rg+7
-    const int col = slice * 16 + (lane & 3) * 4;
+                 float *__restrict__ state, float *__restrict__ o, unsigned *status) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    Stage *st = reinterpret_cast<Stage *>(smem);
+    unsigned long long *full = reinterpret_cast<unsigned long long *>(smem + kStages * sizeof(Stage));
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    // Nothing in global memory is touched before the preceding grid is done.
+    grid_dep_wait();
+
+    const long long first = blockIdx.x, stride = gridDim.x;
+    const long long count = n_heads > first ? (n_heads - 1 - first) / stride + 1 : 0;
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(smem_addr(&full[s]), 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    const float *const vsrc[6] = {r, w, k, v, kk, a};
+    auto issue = [&](long long idx) {
+        const long long head = first + idx * stride;
+        const int s = static_cast<int>(idx % kStages);
+        const uint32_t bar = smem_addr(&full[s]);
+        mbar_arrive_expect_tx(bar, kStateBytes + 6 * kVecBytes);
+        bulk_load(smem_addr(st[s].S), state + head * (kN * kN), kStateBytes, bar);
+#pragma unroll
+        for (int i = 0; i < 6; ++i) bulk_load(smem_addr(st[s].vec[i]), vsrc[i] + head * kN, kVecBytes, bar);
+    };
+    long long issued = 0;
+    if (tid == 0) {
+        for (; issued < count && issued < kStages; ++issued) issue(issued);
+    }
+    grid_dep_launch();
+
+    const int rg = lane >> 2;
     const int row0 = rg * 8;
+    const int col = warp * 16 + (lane & 3) * 4;
+    long long failed_at = -1;
+    for (long long idx = 0; idx < count; ++idx) {
+        const int s = static_cast<int>(idx % kStages);
+        const uint32_t parity = static_cast<uint32_t>((idx / kStages) & 1);
+        const bool got = mbar_wait_bounded(smem_addr(&full[s]), parity, kMaxPolls);
+        if (__syncthreads_or(got ? 0 : 1)) {
+            failed_at = idx;
+            break;
+        }
+        const long long head = first + idx * stride;
+        Stage &S = st[s];
 
-    // State first: the bulk of the bytes, all eight loads in flight at once.
-    float *S = state + head * (kN * kN) + (long long)row0 * kN + col;
-    float4 s[8];
+        float4 x[8];
 #pragma unroll
-    for (int m = 0; m < 8; ++m) s[m] = ld_state(S + m * kN);
+        for (int m = 0; m < 8; ++m) x[m] = *reinterpret_cast<const float4 *>(&S.S[(row0 + m) * kN + col]);
+        const float4 r0 = *reinterpret_cast<const float4 *>(&S.vec[0][row0]);
+        const float4 r1 = *reinterpret_cast<const float4 *>(&S.vec[0][row0 + 4]);
+        const float4 w0 = *reinterpret_cast<const float4 *>(&S.vec[1][row0]);
+        const float4 w1 = *reinterpret_cast<const float4 *>(&S.vec[1][row0 + 4]);
+        const float4 k0 = *reinterpret_cast<const float4 *>(&S.vec[2][row0]);
+        const float4 k1 = *reinterpret_cast<const float4 *>(&S.vec[2][row0 + 4]);
+        const float4 vv = *reinterpret_cast<const float4 *>(&S.vec[3][col]);
+        const float4 kk0 = *reinterpret_cast<const float4 *>(&S.vec[4][row0]);
+        const float4 kk1 = *reinterpret_cast<const float4 *>(&S.vec[4][row0 + 4]);
+        const float4 a0 = *reinterpret_cast<const float4 *>(&S.vec[5][row0]);
+        const float4 a1 = *reinterpret_cast<const float4 *>(&S.vec[5][row0 + 4]);
 
-    const long long vb = head * kN + row0;
-    const float4 w0 = ld_in(w + vb), w1 = ld_in(w + vb + 4);
-    const float4 kk0 = ld_in(kk + vb), kk1 = ld_in(kk + vb + 4);
-    const float4 a0 = ld_in(a + vb), a1 = ld_in(a + vb + 4);
-    const float4 k0 = ld_in(k + vb), k1 = ld_in(k + vb + 4);
-    const float4 r0 = ld_in(r + vb), r1 = ld_in(r + vb + 4);
-    const float4 vv = ld_in(v + head * kN + col);
+        float kkr[8], kr[8], rr[8], dr[8], cr[8];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            kkr[m] = comp(kk0, m); kkr[m + 4] = comp(kk1, m);
+            kr[m] = comp(k0, m);   kr[m + 4] = comp(k1, m);
+            rr[m] = comp(r0, m);   rr[m + 4] = comp(r1, m);
+            dr[m] = expf(comp(w0, m)); dr[m + 4] = expf(comp(w1, m));
+            cr[m] = comp(kk0, m) * comp(a0, m); cr[m + 4] = comp(kk1, m) * comp(a1, m);
+        }
+        // z = kk^T S over the old state
+        float z0 = 0.f, z1 = 0.f, z2 = 0.f, z3 = 0.f;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            z0 = fmaf(kkr[m], x[m].x, z0);
+            z1 = fmaf(kkr[m], x[m].y, z1);
+            z2 = fmaf(kkr[m], x[m].z, z2);
+            z3 = fmaf(kkr[m], x[m].w, z3);
+        }
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            z0 += __shfl_xor_sync(0xffffffffu, z0, off);
+            z1 += __shfl_xor_sync(0xffffffffu, z1, off);
+            z2 += __shfl_xor_sync(0xffffffffu, z2, off);
+            z3 += __shfl_xor_sync(0xffffffffu, z3, off);
+        }
+        // S' = diag(exp w) S - (kk .* a) z^T + k v^T, then o = S'^T r
+        float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const float d = dr[m], c = cr[m], kv = kr[m];
+            x[m].x = fmaf(d, x[m].x, fmaf(-c, z0, kv * vv.x));
+            x[m].y = fmaf(d, x[m].y, fmaf(-c, z1, kv * vv.y));
+            x[m].z = fmaf(d, x[m].z, fmaf(-c, z2, kv * vv.z));
+            x[m].w = fmaf(d, x[m].w, fmaf(-c, z3, kv * vv.w));
+            o0 = fmaf(rr[m], x[m].x, o0);
+            o1 = fmaf(rr[m], x[m].y, o1);
+            o2 = fmaf(rr[m], x[m].z, o2);
+            o3 = fmaf(rr[m], x[m].w, o3);
+            *reinterpret_cast<float4 *>(&S.S[(row0 + m) * kN + col]) = x[m];
+        }
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            o0 += __shfl_xor_sync(0xffffffffu, o0, off);
+            o1 += __shfl_xor_sync(0xffffffffu, o1, off);
+            o2 += __shfl_xor_sync(0xffffffffu, o2, off);
+            o3 += __shfl_xor_sync(0xffffffffu, o3, off);
+        }
+        if (rg == 0) *reinterpret_cast<float4 *>(o + head * kN + col) = make_float4(o0, o1, o2, o3);
 
-    float kkr[8], kr[8], rr[8], dr[8], cr[8];
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        kkr[m] = comp(kk0, m); kkr[m + 4] = comp(kk1, m);
-        kr[m] = comp(k0, m);   kr[m + 4] = comp(k1, m);
-        rr[m] = comp(r0, m);   rr[m + 4] = comp(r1, m);
-        dr[m] = expf(comp(w0, m)); dr[m + 4] = expf(comp(w1, m));
-        cr[m] = comp(kk0, m) * comp(a0, m); cr[m + 4] = comp(kk1, m) * comp(a1, m);
+        fence_proxy_async_smem();  // the new state in this stage -> visible to the bulk store
+        __syncthreads();
+        if (tid == 0) {
+            bulk_store(state + head * (kN * kN), smem_addr(S.S), kStateBytes);
+            bulk_commit();
+            // refill the previous stage once its store has read it
+            if (idx >= 1 && issued < count) {
+                bulk_wait_read<1>();
+                issue(issued);
+                ++issued;
+            }
+        }
     }
+    if (tid == 0) {
+        if (failed_at >= 0) {
+            report(status, kDevTimeout);
+            // let every load still outstanding land before the CTA's shared memory goes away
+            for (long long idx = failed_at; idx < issued; ++idx)
+                mbar_wait_bounded(smem_addr(&full[idx % kStages]), static_cast<uint32_t>((idx / kStages) & 1),
+                                  kMaxPolls);
+        }
+        bulk_wait<0>();
+    }
+}
 
-    // z = kk^T S over the old state: eight rows here, 64 rows across lanes.
-    float z0 = 0.f, z1 = 0.f, z2 = 0.f, z3 = 0.f;
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-        z0 = fmaf(kkr[m], s[m].x, z0);
-        z1 = fmaf(kkr[m], s[m].y, z1);
-        z2 = fmaf(kkr[m], s[m].z, z2);
-        z3 = fmaf(kkr[m], s[m].w, z3);
-    }
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-        z0 += __shfl_xor_sync(0xffffffffu, z0, off);
-        z1 += __shfl_xor_sync(0xffffffffu, z1, off);
-        z2 += __shfl_xor_sync(0xffffffffu, z2, off);
-        z3 += __shfl_xor_sync(0xffffffffu, z3, off);
-    }
+struct LaunchShape {
+    int grid_cap = 0;  // CTAs per wave (SMs x resident CTAs per SM)
+};
 
-    // S' = diag(exp w) S - (kk .* a) z^T + k v^T, then o = S'^T r.
-    float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-        const float d = dr[m], c = cr[m], kv = kr[m];
-        s[m].x = fmaf(d, s[m].x, fmaf(-c, z0, kv * vv.x));
-        s[m].y = fmaf(d, s[m].y, fmaf(-c, z1, kv * vv.y));
-        s[m].z = fmaf(d, s[m].z, fmaf(-c, z2, kv * vv.z));
-        s[m].w = fmaf(d, s[m].w, fmaf(-c, z3, kv * vv.w));
-        o0 = fmaf(rr[m], s[m].x, o0);
-        o1 = fmaf(rr[m], s[m].y, o1);
-        o2 = fmaf(rr[m], s[m].z, o2);
-        o3 = fmaf(rr[m], s[m].w, o3);
-    }
-#pragma unroll
-    for (int m = 0; m < 8; ++m) st_state(S + m * kN, s[m]);
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-        o0 += __shfl_xor_sync(0xffffffffu, o0, off);
-        o1 += __shfl_xor_sync(0xffffffffu, o1, off);
-        o2 += __shfl_xor_sync(0xffffffffu, o2, off);
-        o3 += __shfl_xor_sync(0xffffffffu, o3, off);
-    }
-    if (rg == 0) *reinterpret_cast<float4 *>(o + head * kN + col) = make_float4(o0, o1, o2, o3);
+LaunchShape shape_for_device() {
+    static int cached_dev = -1;
+    static LaunchShape cached;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return LaunchShape{};
+    if (dev == cached_dev) return cached;
+    LaunchShape s;
+    int sms = 0, per_sm = 0;
+    if (cudaFuncSetAttribute(wkv7_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes)) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, wkv7_step_kernel, kThreads, kSmemBytes) !=
+            cudaSuccess)
+        return LaunchShape{};
+    s.grid_cap = sms * (per_sm > 0 ? per_sm : 1);
+    cached = s;
+    cached_dev = dev;
+    return s;
 }
 
 }  // namespace
 
 cudaError_t launch_step(long long n_heads, const float *r, const float *w, const float *k,
                         const float *v, const float *kk, const float *a, float *state,
-                        float *o, cudaStream_t stream) {
+                        float *o, unsigned *status, cudaStream_t stream) {
     if (n_heads <= 0) return cudaSuccess;
-    const long long n_units = n_heads * kSlices;
-    const long long blocks = (n_units + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    wkv7_step_kernel<<<(unsigned)blocks, kWarpsPerBlock * 32, 0, stream>>>(
-        n_units, r, w, k, v, kk, a, state, o);
-    return cudaGetLastError();
+    const LaunchShape shape = shape_for_device();
+    if (shape.grid_cap <= 0) return cudaErrorInvalidDevice;
+    const long long grid = n_heads < shape.grid_cap ? n_heads : shape.grid_cap;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, wkv7_step_kernel, n_heads, r, w, k, v, kk, a, state, o, status);
 }
 
 }  // namespace wkv7
