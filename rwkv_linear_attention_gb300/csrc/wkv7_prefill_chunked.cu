@@ -20,28 +20,35 @@
 // Substituting Z and folding every state-independent product gives one
 // matrix product per chunk on the state's critical path:
 //
-//   [ O                     ]   [ Ra - Mt Qa   | M_k - Mt L_k  ]   [ S0 ]
-//   [ S_C - e^{g_C} * S0    ] = [ -Ct Qa       | Kb^T - Ct L_k ] . [ V  ]
+//   [ O                  ]   [ Ra - Mt Qa | M_k - Mt L_k  ]   [ S0 ]
+//   [ S_C - e^{g_C} * S0 ] = [ -Ct Qa     | Kb^T - Ct L_k ] . [ V  ]      (A_chain)
 //
-// with Mt = M_c T and Ct = Cb^T T.  Per chunk this kernel runs four tf32
-// MMAs, all M = 128 with fp32 accumulators in tensor memory:
-//   G  = [R ; Q] [C ; K]^T      (the four Gram blocks at once; 128x128x64)
-//   X  = [M_c ; Cb^T] T         ([Mt ; Ct]; 128x64x64)
-//   Y  = X [Qa | L_k]           (128x128x64)
-//   D  = A_chain [S0 ; V]       (128x64x128)
-// Everything else (cumulative decay, the exponentials, masks, the blocked
-// 64x64 unit-lower-triangular inverse, operand staging) is SIMT work on the
-// same CTA.  One CTA owns one (sequence, head) pair and walks its chunks in
-// order; the fp32 state lives in registers between chunks.  Inputs arrive by
-// TMA (2-D tiles of 64 tokens x 64 channels of the packed [T, H, 64] arrays);
-// the next chunk's tiles load while the current chunk's last phases run.
+// with [Mt ; Ct] = [M_c ; Cb^T] T.  Per chunk four tf32 MMAs run, all with
+// M = 128, fp32 accumulators in tensor memory and the A operand read from
+// tensor memory:
+//   G       = [R ; Q] [C ; K]^T                 (the four Gram blocks; 128x128x64)
+//   X       = [M_c ; Cb^T] T                     (128x64x64)
+//   A_chain = base - X [Qa | L_k]                (accumulated onto base = [Ra | M_k ; 0 | Kb^T]; 128x128x64)
+//   D       = A_chain [S0 ; V]                   (128x64x128)
+// The SIMT work (cumulative decay, exponentials, masks, the blocked 64x64
+// unit-lower-triangular inverse, operand staging) is software-pipelined with
+// the MMAs: the next chunk's decay and Gram operands are built while this
+// chunk's X and A_chain products run, and the next chunk's Gram product runs
+// while this chunk's outputs are written.  One CTA (512 threads) owns one
+// (sequence, head) pair and walks its chunks in order; the fp32 state lives
+// in registers between chunks.  Inputs arrive by TMA as 2-D tiles of
+// 64 tokens x 64 channels of the packed [T, H, 64] arrays (bf16 tiles in the
+// 128-byte swizzled layout, so both row- and column-wise reads are free of
+// bank conflicts).
 //
 // Inputs r, k, v, kk, a are bf16 (w fp32); fp32-input prefill is served by
 // the token-serial kernel instead.
 //
-// Precision: inputs are used exactly; every MMA operand is rounded to tf32
-// (round to nearest) and accumulates in fp32.  The decay factors of the Gram
-// operands are taken relative to the chunk's middle token, so for
+// Precision: inputs are used exactly; operands staged by threads are rounded
+// to tf32 (to nearest); operands that one MMA hands to the next stay in
+// tensor memory (the hardware reads them at tf32 precision); accumulation is
+// fp32 and the state carried between chunks is fp32.  The decay factors of
+// the Gram operands are taken relative to the chunk's 32nd token, so for
 // w >= -2.5 every factor lies within e^{+-80} (finite in fp32).
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -55,40 +62,45 @@ namespace {
 using namespace ptx;
 
 constexpr int kC = 64;          // chunk length
-constexpr int kThreads = 256;   // warp w reads TMEM lanes 32*(w%4).., column half w/4
+constexpr int kThreads = 512;   // warp w: TMEM lane quarter w % 4, column group w / 4
 constexpr uint32_t kMaxPolls = 1u << 24;
 
 // TMEM columns
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColG = 0, kColX = 128, kColY = 192, kColD = 320;
+constexpr uint32_t kColG = 0;     // G; then [M_c ; Cb^T] in its first 64 columns
+constexpr uint32_t kColX = 128;   // X = [Mt ; Ct]
+constexpr uint32_t kColAC = 192;  // A_chain (128 columns)
+constexpr uint32_t kColD = 320;   // D = [O ; S_C - e^{g_C} S0]
+constexpr uint32_t kColAG = 384;  // A operand of G = [R ; Q] (for the next chunk)
+constexpr uint32_t kColAT = 448;  // A operand [0 ; diag(e^{g_C - g_ref})] of the transposing product
 
-// LC / TS scratch: fp32 64 x 68 (row stride 272 B keeps float4 rows conflict-free)
-constexpr int kLd = 68;
+constexpr int kLd = 68;  // padded row stride (floats) of the fp32 L_c / T scratch
 
-template <int XB>
-struct Layout {
-    static constexpr int kTile = 64 * 64 * XB;     // one raw x tile
-    static constexpr int R = 0;
-    static constexpr int K = R + kTile;
-    static constexpr int KK = K + kTile;
-    static constexpr int A = KK + kTile;
-    static constexpr int W = A + kTile;            // fp32 w -> cumulative g -> E = e^{g - g_ref}
-    static constexpr int AX = W + 16384;           // 32 KB: [M_c ; Cb^T] operand; earlier LC scratch, raw v tile at +16 KB
-    static constexpr int BX = AX + 32768;          // 16 KB: T^T operand
-    static constexpr int P = BX + 16384;           // 64 KB: [A_G | B_G] -> TS/X scratch + B_Y -> [A_Y | B_Y] -> A_chain
-    static constexpr int BC = P + 65536;           // 32 KB: B_chain = [S0^T | V^T] (64 rows x K 128)
-    static constexpr int MISC = BC + 32768;        // per-channel vectors, barriers
-    static constexpr int M_EREF = MISC;            // 64 f32: e^{g_ref}
-    static constexpr int M_GC = MISC + 256;        // 64 f32: e^{g_C}
-    static constexpr int M_TOT = MISC + 512;       // 4 x 64 f32: cumsum partials
-    static constexpr int M_BAR_TMA = MISC + 1536;
-    static constexpr int M_BAR_MMA = MISC + 1544;
-    static constexpr int M_SLOT = MISC + 1552;
-    static constexpr int kBytes = MISC + 1600;
-    static constexpr int kAlloc = kBytes + 1024;   // slack to align the base to 1024 B
-    static constexpr uint32_t kTmaBytes = 5 * kTile + 16384;
-};
-static_assert(Layout<2>::kAlloc <= 232448, "layout exceeds shared memory");
+// Shared memory map (bytes from a 1024-aligned base)
+constexpr int kTile = 64 * 64 * 2;  // one bf16 raw tile
+constexpr int SM_R = 0, SM_K = SM_R + kTile, SM_KK = SM_K + kTile, SM_A = SM_KK + kTile, SM_V = SM_A + kTile;
+constexpr int SM_W = SM_V + kTile;         // fp32 w tile -> E = e^{g - g_ref} (swizzled)
+constexpr int SM_EI = SM_W + 16384;        // fp32 1/E = e^{g_ref - g} (swizzled like E)
+constexpr int SM_BG = SM_EI + 16384;       // B operand of G: [C ; K]  (128 x K64)
+constexpr int SM_BY = SM_BG + 32768;       // B operand of A_chain: [Qa^T ; L_k^T] (128 x K64)
+constexpr int SM_BX = SM_BY + 32768;       // B operand of X: T^T (64 x K64)
+constexpr int SM_BC = SM_BX + 16384;       // B operand of D: [S0^T | V^T] (64 x K128)
+constexpr int SM_LC = SM_BC + 32768;       // fp32 L_c [64][kLd]
+constexpr int SM_TS = SM_LC + 64 * kLd * 4;  // fp32 T [64][kLd]
+constexpr int SM_XS = SM_TS + 64 * kLd * 4;  // fp32 32 x 32 scratch
+constexpr int SM_TOT = SM_XS + 4096;       // 8 x 64 cumsum partials
+constexpr int SM_GREF = SM_TOT + 2048;     // 64: g_ref
+constexpr int SM_EREF = SM_GREF + 256;     // 2 x 64: e^{g_ref} (double-buffered across chunks)
+constexpr int SM_E63 = SM_EREF + 512;      // 64: e^{g_C - g_ref}
+constexpr int SM_GC = SM_E63 + 256;        // 2 x 64: e^{g_C} (double-buffered across chunks)
+constexpr int SM_BAR = SM_GC + 512;        // 5 mbarriers
+constexpr int SM_SLOT = SM_BAR + 64;
+constexpr int kSmemBytes = SM_SLOT + 64;
+constexpr int kSmemAlloc = kSmemBytes + 1024;
+static_assert(kSmemAlloc <= 232448, "shared memory layout too large");
+static_assert(SM_BG % 1024 == 0 && SM_BY % 1024 == 0 && SM_BX % 1024 == 0 && SM_BC % 1024 == 0,
+              "operand tiles must be 1024-byte aligned");
+constexpr uint32_t kTmaBytes = 5 * kTile + 16384;
 
 __device__ __forceinline__ uint32_t to_tf32(float x) {
     uint32_t r;
@@ -98,36 +110,44 @@ __device__ __forceinline__ uint32_t to_tf32(float x) {
 __device__ __forceinline__ void st_tf32x4(unsigned char *p, float a, float b, float c, float d) {
     *reinterpret_cast<uint4 *>(p) = make_uint4(to_tf32(a), to_tf32(b), to_tf32(c), to_tf32(d));
 }
-// Reciprocal of a decay factor (fast approximate divide, ~2 ulp).  Its
-// result only feeds tf32 operands, whose rounding (2^-11) dominates.
+// Reciprocal of a decay factor (fast approximate divide, ~2 ulp); it only
+// feeds tf32 operands, whose rounding dominates.
 __device__ __forceinline__ float rcp(float x) { return __fdividef(1.f, x); }
-__device__ __forceinline__ float4 ld_f4(const unsigned char *p) {
-    return *reinterpret_cast<const float4 *>(p);
+__device__ __forceinline__ float bf2f(uint32_t lo16) { return __uint_as_float(lo16 << 16); }
+
+// bf16 raw tile [64 tokens][64 channels] in the TMA 128-byte swizzle layout.
+__device__ __forceinline__ uint32_t raw_off(int t, int i) {
+    return t * 128 + ((((i >> 3) ^ (t & 7)) << 4) | ((i & 7) << 1));
+}
+__device__ __forceinline__ float raw1(const unsigned char *tile, int t, int i) {
+    return bf2f(*reinterpret_cast<const unsigned short *>(tile + raw_off(t, i)));
+}
+// eight consecutive channels i .. i+7 (i % 8 == 0)
+__device__ __forceinline__ void raw8(const unsigned char *tile, int t, int i, float *f) {
+    const uint4 u = *reinterpret_cast<const uint4 *>(tile + raw_off(t, i));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        f[2 * j] = bf2f(w[j] & 0xffffu);
+        f[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+    }
+}
+// four consecutive channels i .. i+3 (i % 4 == 0)
+__device__ __forceinline__ float4 raw4(const unsigned char *tile, int t, int i) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(tile + raw_off(t, i));
+    return make_float4(bf2f(u.x & 0xffffu), __uint_as_float(u.x & 0xffff0000u), bf2f(u.y & 0xffffu),
+                       __uint_as_float(u.y & 0xffff0000u));
 }
 
-// Raw input access (row-major [64 tokens][64 channels] tile of x).
-template <typename X>
-struct Raw;
-template <>
-struct Raw<__nv_bfloat16> {
-    static constexpr int kB = 2;
-    __device__ static float4 ld4(const unsigned char *tile, int t, int i) {
-        const uint2 u = *reinterpret_cast<const uint2 *>(tile + (t * 64 + i) * 2);
-        return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
-                           __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
-    }
-    __device__ static float ld1(const unsigned char *tile, int t, int i) {
-        const unsigned short u = *reinterpret_cast<const unsigned short *>(tile + (t * 64 + i) * 2);
-        return __uint_as_float(static_cast<uint32_t>(u) << 16);
-    }
-};
+// E table [64][64] fp32 with 16-byte chunks XOR-swizzled by (t mod 8).
+__device__ __forceinline__ int eidx(int t, int i) { return t * 64 + ((((i >> 2) ^ (t & 7)) << 2) | (i & 3)); }
 
 struct TensorMaps {
     CUtensorMap r, k, v, kk, a, w;
 };
 
-// All threads wait on an mbarrier phase; the outcome is made uniform so that
-// either every thread continues or every thread leaves together.
+// All threads wait on an mbarrier phase; the outcome is uniform, so either
+// every thread continues or every thread leaves together.
 __device__ __forceinline__ bool wait_uniform(uint32_t bar, uint32_t parity, unsigned *status) {
     const bool ok = mbar_wait_bounded(bar, parity, kMaxPolls);
     const int any_fail = __syncthreads_or(ok ? 0 : 1);
@@ -135,6 +155,8 @@ __device__ __forceinline__ bool wait_uniform(uint32_t bar, uint32_t parity, unsi
     return any_fail == 0;
 }
 
+// Shared-memory operand writes and tensor-memory stores by all threads ->
+// visible to the MMA issued after this barrier.
 __device__ __forceinline__ void sync_for_mma() {
     fence_proxy_async_smem();
     tc_fence_before_sync();
@@ -142,17 +164,16 @@ __device__ __forceinline__ void sync_for_mma() {
     tc_fence_after_sync();
 }
 
-template <typename X>
 __global__ void __launch_bounds__(kThreads, 1)
 wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps maps) {
-    using L = Layout<Raw<X>::kB>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_addr(sm);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int q = warp & 3, hf = warp >> 2;  // TMEM lane quarter, column half
+    const int q = warp & 3, cg = warp >> 2;
     const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
+    const int m = 32 * q + lane;  // TMEM lane (row) this thread reads and writes
 
     const int H = p.H;
     const int rank = static_cast<int>(blockIdx.x) / H;
@@ -170,218 +191,280 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
     const int len = eos - bos;
     const int nchunks = (len + kC - 1) / kC;
     const long long tok_stride = static_cast<long long>(H) * 64;
-    float *eref = reinterpret_cast<float *>(sm + L::M_EREF);
-    float *gC = reinterpret_cast<float *>(sm + L::M_GC);
-    const uint32_t bar_tma = sbase + L::M_BAR_TMA, bar_mma = sbase + L::M_BAR_MMA;
 
-    // State rows held by warps with q in {2, 3}: row i, columns [32*hf, 32*hf+32).
+    // State: rows i = m - 64 (lanes 64..127), columns 16*cg .. 16*cg+15.
     const bool state_thread = q >= 2;
-    const int srow = 32 * (q - 2) + lane;
-    float s[32];
+    const int si = m - 64;
+    float s[16];
     const long long sslot = (static_cast<long long>(b) * H + h) * 4096;
     if (state_thread) {
         if (p.initial_state) {
-            const float4 *src = reinterpret_cast<const float4 *>(p.initial_state + sslot + srow * 64 + 32 * hf);
+            const float4 *src = reinterpret_cast<const float4 *>(p.initial_state + sslot + si * 64 + 16 * cg);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < 4; ++j) {
                 const float4 x = src[j];
                 s[4 * j] = x.x; s[4 * j + 1] = x.y; s[4 * j + 2] = x.z; s[4 * j + 3] = x.w;
             }
         } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) s[j] = 0.f;
+            for (int j = 0; j < 16; ++j) s[j] = 0.f;
         }
     }
     if (nchunks == 0) {
         if (state_thread && p.final_state) {
-            float4 *dst = reinterpret_cast<float4 *>(p.final_state + sslot + srow * 64 + 32 * hf);
+            float4 *dst = reinterpret_cast<float4 *>(p.final_state + sslot + si * 64 + 16 * cg);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) dst[j] = make_float4(s[4 * j], s[4 * j + 1], s[4 * j + 2], s[4 * j + 3]);
+            for (int j = 0; j < 4; ++j) dst[j] = make_float4(s[4 * j], s[4 * j + 1], s[4 * j + 2], s[4 * j + 3]);
         }
         return;
     }
 
+    unsigned char *rr = sm + SM_R, *rk = sm + SM_K, *rkk = sm + SM_KK, *ra = sm + SM_A, *rv = sm + SM_V;
+    float *E = reinterpret_cast<float *>(sm + SM_W);
+    float *EI = reinterpret_cast<float *>(sm + SM_EI);
+    float *TOT = reinterpret_cast<float *>(sm + SM_TOT);
+    float *GREF = reinterpret_cast<float *>(sm + SM_GREF);
+    float *EREF = reinterpret_cast<float *>(sm + SM_EREF);
+    float *E63 = reinterpret_cast<float *>(sm + SM_E63);
+    float *GC = reinterpret_cast<float *>(sm + SM_GC);
+    const uint32_t bar_tma = sbase + SM_BAR, bar_g = bar_tma + 8, bar_x = bar_tma + 16, bar_y = bar_tma + 24,
+                   bar_d = bar_tma + 32;
+
     if (tid == 0) {
         mbar_init(bar_tma, 1);
-        mbar_init(bar_mma, 1);
+        mbar_init(bar_g, 1);
+        mbar_init(bar_x, 1);
+        mbar_init(bar_y, 1);
+        mbar_init(bar_d, 1);
         fence_mbar_init();
     }
-    if (warp == 0) tmem_alloc(sbase + L::M_SLOT, kTmemCols);
-    // B_chain rows j, K 0..63 <- S0[i][j] (tf32)
+    if (warp == 0) tmem_alloc(sbase + SM_SLOT, kTmemCols);
+    // B_chain rows j, K 0..63 <- S0[i][j]
     if (state_thread) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-            *reinterpret_cast<uint32_t *>(sm + L::BC + sw128_off(32 * hf + j, srow, 64)) = to_tf32(s[j]);
+        for (int j = 0; j < 16; ++j)
+            *reinterpret_cast<uint32_t *>(sm + SM_BC + sw128_off(16 * cg + j, si, 64)) = to_tf32(s[j]);
     }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm + L::M_SLOT);
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm + SM_SLOT);
 
     auto issue_tma = [&](int chunk) {
-        const int y = bos + chunk * kC;
-        const int x = h * 64;
-        mbar_arrive_expect_tx(bar_tma, L::kTmaBytes);
-        tma_load_2d(sbase + L::R, &maps.r, x, y, bar_tma);
-        tma_load_2d(sbase + L::K, &maps.k, x, y, bar_tma);
-        tma_load_2d(sbase + L::KK, &maps.kk, x, y, bar_tma);
-        tma_load_2d(sbase + L::A, &maps.a, x, y, bar_tma);
-        tma_load_2d(sbase + L::W, &maps.w, x, y, bar_tma);
-        tma_load_2d(sbase + L::AX + 16384, &maps.v, x, y, bar_tma);
+        const int y = bos + chunk * kC, x = h * 64;
+        mbar_arrive_expect_tx(bar_tma, kTmaBytes);
+        tma_load_2d(sbase + SM_R, &maps.r, x, y, bar_tma);
+        tma_load_2d(sbase + SM_K, &maps.k, x, y, bar_tma);
+        tma_load_2d(sbase + SM_KK, &maps.kk, x, y, bar_tma);
+        tma_load_2d(sbase + SM_A, &maps.a, x, y, bar_tma);
+        tma_load_2d(sbase + SM_V, &maps.v, x, y, bar_tma);
+        tma_load_2d(sbase + SM_W, &maps.w, x, y, bar_tma);
     };
-    if (tid == 0) issue_tma(0);
+    auto chunk_len = [&](int chunk) { return min(kC, eos - (bos + chunk * kC)); };
 
-    uint32_t mma_parity = 0;
-    bool alive = true;
-    using RawX = Raw<X>;
-    unsigned char *rr = sm + L::R, *rk = sm + L::K, *rkk = sm + L::KK, *ra = sm + L::A, *rv = sm + L::AX + 16384;
-    float *Et = reinterpret_cast<float *>(sm + L::W);  // [64][64]
+    // ---- phase 1: masked cumulative log-decay g; E = e^{g - g_ref} (g_ref = g[31]) in place
+    auto phase1 = [&](int lc, int gbuf) {
+        const int ch = tid & 63, seg = tid >> 6;  // rows 8*seg .. 8*seg+7
+        float g[8];
+        float acc = 0.f;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int t = 8 * seg + u;
+            acc += (t < lc) ? E[t * 64 + ch] : 0.f;  // the w tile, row-major as loaded
+            g[u] = acc;
+        }
+        TOT[seg * 64 + ch] = acc;
+        __syncthreads();
+        float pre = 0.f;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) pre += (u < seg) ? TOT[u * 64 + ch] : 0.f;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) g[u] += pre;
+        if (seg == 3) GREF[ch] = g[7];
+        __syncthreads();
+        const float gr = GREF[ch];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            E[eidx(8 * seg + u, ch)] = __expf(g[u] - gr);
+            EI[eidx(8 * seg + u, ch)] = __expf(gr - g[u]);
+        }
+        if (seg == 0) EREF[gbuf * 64 + ch] = __expf(gr);
+        if (seg == 7) {
+            E63[ch] = __expf(g[7] - gr);
+            GC[gbuf * 64 + ch] = __expf(g[7]);
+        }
+    };
+
+    // ---- phase 2: A_G = [R ; Q] into TMEM, B_G = [C ; K] into shared memory
+    auto phase2 = [&](int lc, const float *eref) {
+        {
+            const bool rrow = m < 64;
+            const int t = rrow ? m : m - 64;
+            const int i0 = 16 * cg;
+            const float valid = t < lc ? 1.f : 0.f;
+            float x[16];
+            raw8(rrow ? rr : rkk, t, i0, x);
+            raw8(rrow ? rr : rkk, t, i0 + 8, x + 8);
+            uint32_t wds[16];
+#pragma unroll
+            for (int j = 0; j < 16; j += 4) {
+                float4 e;
+                if (rrow) {
+                    e = *reinterpret_cast<const float4 *>(E + eidx(t, i0 + j));
+                } else if (t > 0) {
+                    e = *reinterpret_cast<const float4 *>(E + eidx(t - 1, i0 + j));
+                } else {
+                    const float4 er = *reinterpret_cast<const float4 *>(eref + i0 + j);
+                    e = make_float4(rcp(er.x), rcp(er.y), rcp(er.z), rcp(er.w));
+                }
+                wds[j] = to_tf32(valid * x[j] * e.x);
+                wds[j + 1] = to_tf32(valid * x[j + 1] * e.y);
+                wds[j + 2] = to_tf32(valid * x[j + 2] * e.z);
+                wds[j + 3] = to_tf32(valid * x[j + 3] * e.w);
+            }
+            tmem_st16(tmem + lane_off + kColAG + i0, wds);
+            // A_T row m: e^{g_C - g_ref}[m - 64] on the diagonal of its lower half, zero elsewhere
+#pragma unroll
+            for (int j = 0; j < 16; ++j) wds[j] = (m >= 64 && i0 + j == m - 64) ? to_tf32(E63[m - 64]) : 0u;
+            tmem_st16(tmem + lane_off + kColAT + i0, wds);
+        }
+        unsigned char *BG = sm + SM_BG;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int task = tid + kThreads * u;
+            const int n = task >> 4, i = (task & 15) * 4;
+            const int sidx = n & 63;
+            const float4 e = *reinterpret_cast<const float4 *>(EI + eidx(sidx, i));
+            const float valid = sidx < lc ? 1.f : 0.f;
+            const float4 ei = make_float4(valid * e.x, valid * e.y, valid * e.z, valid * e.w);
+            if (n < 64) {
+                const float4 xkk = raw4(rkk, sidx, i), xa = raw4(ra, sidx, i);
+                st_tf32x4(BG + sw128_off(n, i, 128), xkk.x * xa.x * ei.x, xkk.y * xa.y * ei.y,
+                          xkk.z * xa.z * ei.z, xkk.w * xa.w * ei.w);
+            } else {
+                const float4 xk = raw4(rk, sidx, i);
+                st_tf32x4(BG + sw128_off(n, i, 128), xk.x * ei.x, xk.y * ei.y, xk.z * ei.z, xk.w * ei.w);
+            }
+        }
+    };
+
+    // V^T into B_chain (K 64..127)
+    auto write_vt = [&](int lc) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int task = tid + kThreads * u;
+            const int j = task & 63, s0 = 4 * (task >> 6);
+            float vv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) vv[e] = (s0 + e < lc) ? raw1(rv, s0 + e, j) : 0.f;
+            st_tf32x4(sm + SM_BC + sw128_off(j, 64 + s0, 64), vv[0], vv[1], vv[2], vv[3]);
+        }
+    };
+
+    // Gram product G = [R ; Q] [C ; K]^T, and the transposing product
+    // [0 ; diag(e^{g_C - g_ref})] [C ; K]^T, whose lower half is [Cb^T | Kb^T]
+    // (Cb^T[i][s] = e^{g_C - g_ref}[i] C[s][i], likewise Kb^T), into A_chain's columns.
+    auto issue_gram = [&]() {
+#pragma unroll
+        for (int kq = 0; kq < 8; ++kq)
+            mma_tf32_tmem_a(tmem + kColG, tmem + kColAG + 8 * kq,
+                            sdesc_sw128(sbase + SM_BG + (kq >> 2) * 128 * 128 + (kq & 3) * 32),
+                            idesc_tf32(128, 128), kq > 0);
+    };
+    auto issue_transpose = [&]() {
+#pragma unroll
+        for (int kq = 0; kq < 8; ++kq)
+            mma_tf32_tmem_a(tmem + kColAC, tmem + kColAT + 8 * kq,
+                            sdesc_sw128(sbase + SM_BG + (kq >> 2) * 128 * 128 + (kq & 3) * 32),
+                            idesc_tf32(128, 128), kq > 0);
+    };
+
+    // ---- prologue: chunk 0 up to its Gram product
+    if (tid == 0) issue_tma(0);
+    bool alive = wait_uniform(bar_tma, 0, p.status);
+    if (alive) {
+        phase1(chunk_len(0), 0);
+        __syncthreads();
+        phase2(chunk_len(0), EREF);
+        write_vt(chunk_len(0));
+        sync_for_mma();
+        if (tid == 0) {
+            issue_gram();
+            issue_transpose();
+            mma_commit(bar_g);
+        }
+        alive = wait_uniform(bar_g, 0, p.status);
+        tc_fence_after_sync();
+    }
 
     for (int c = 0; c < nchunks && alive; ++c) {
         const int t0 = bos + c * kC;
-        const int lc = min(kC, eos - t0);
+        const int lc = chunk_len(c);
+        const bool has_next = c + 1 < nchunks;
+        const uint32_t par = static_cast<uint32_t>(c & 1);
+        const float *erc = EREF + (c & 1) * 64;  // e^{g_ref} of this chunk
 
-        if (!wait_uniform(bar_tma, static_cast<uint32_t>(c & 1), p.status)) { alive = false; break; }
-
-        // ---- phase 2a: masked cumulative log-decay g (in place in the w tile)
+        // ---- phase 3: read G.  M_c (masked) -> A_chain columns 0..63 of rows t, which with
+        // the transposing product's Cb^T below them form A_X = [M_c ; Cb^T]; M_k (masked) ->
+        // A_chain rows t, K 64..; L_c -> LC; L_k^T and Qa^T -> B_Y.
         {
-            const int ch = tid & 63, qq = tid >> 6;
-            float g[16];
-            float acc = 0.f;
+            uint32_t wds[32];
+            const int gcol = (cg < 2 ? 0 : 64) + 32 * (cg & 1);  // M_c | M_k (q<2), L_c | L_k (q>=2)
+            const int s0 = 32 * (cg & 1);
+            // Qa^T into B_Y rows 0..63: Qa[t][i] = kk e^{g_{t-1}}
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int t = 16 * qq + u;
-                acc += (t < lc) ? Et[t * 64 + ch] : 0.f;
-                g[u] = acc;
-            }
-            float *tot = reinterpret_cast<float *>(sm + L::M_TOT);
-            tot[qq * 64 + ch] = acc;
-            __syncthreads();
-            float pre = 0.f;
-            for (int u = 0; u < qq; ++u) pre += tot[u * 64 + ch];
+            for (int u = 0; u < 2; ++u) {
+                const int task = tid + kThreads * u;
+                const int i = task & 63, tb = 4 * (task >> 6);
+                const float er = erc[i];
+                float x[4];
 #pragma unroll
-            for (int u = 0; u < 16; ++u) Et[(16 * qq + u) * 64 + ch] = pre + g[u];
-            __syncthreads();
-            // ---- phase 2b: E = e^{g - g_ref}, g_ref = g[31]; eref = e^{g_ref}
-            const float gr = Et[31 * 64 + ch];
-            __syncthreads();
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int t = 16 * qq + u;
-                Et[t * 64 + ch] = __expf(Et[t * 64 + ch] - gr);
-            }
-            if (qq == 0) eref[ch] = __expf(gr);
-            __syncthreads();
-        }
-
-        // ---- phase 2c: Gram operands A_G = [R ; Q] (rows t), B_G = [C ; K] (rows s), V^T into B_chain
-        {
-            unsigned char *AG = sm + L::P, *BG = sm + L::P + 32768;
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const int task = tid + kThreads * m;
-                const int t = task >> 4, i = (task & 15) * 4;
-                const float valid = t < lc ? 1.f : 0.f;
-                const float4 e = ld_f4(reinterpret_cast<unsigned char *>(Et + t * 64 + i));
-                float4 ep;  // e^{g_{t-1} - g_ref}
-                if (t > 0) {
-                    ep = ld_f4(reinterpret_cast<unsigned char *>(Et + (t - 1) * 64 + i));
-                } else {
-                    ep = make_float4(rcp(eref[i]), rcp(eref[i + 1]), rcp(eref[i + 2]), rcp(eref[i + 3]));
+                for (int e = 0; e < 4; ++e) {
+                    const int t = tb + e;
+                    const float f = (t == 0) ? 1.f : E[eidx(t - 1, i)] * er;
+                    x[e] = (t < lc) ? raw1(rkk, t, i) * f : 0.f;
                 }
-                const float4 xr = RawX::ld4(rr, t, i), xk = RawX::ld4(rk, t, i);
-                const float4 xkk = RawX::ld4(rkk, t, i), xa = RawX::ld4(ra, t, i);
-                st_tf32x4(AG + sw128_off(t, i, 128), valid * xr.x * e.x, valid * xr.y * e.y,
-                          valid * xr.z * e.z, valid * xr.w * e.w);
-                st_tf32x4(AG + sw128_off(64 + t, i, 128), valid * xkk.x * ep.x, valid * xkk.y * ep.y,
-                          valid * xkk.z * ep.z, valid * xkk.w * ep.w);
-                const float4 ei = make_float4(valid * rcp(e.x), valid * rcp(e.y), valid * rcp(e.z), valid * rcp(e.w));
-                st_tf32x4(BG + sw128_off(t, i, 128), xkk.x * xa.x * ei.x, xkk.y * xa.y * ei.y,
-                          xkk.z * xa.z * ei.z, xkk.w * xa.w * ei.w);
-                st_tf32x4(BG + sw128_off(64 + t, i, 128), xk.x * ei.x, xk.y * ei.y, xk.z * ei.z, xk.w * ei.w);
+                st_tf32x4(sm + SM_BY + sw128_off(i, tb, 128), x[0], x[1], x[2], x[3]);
             }
-            // V^T: B_chain[j][64 + s] = v[s][j]
+            float v[32];
+            tmem_ld32(tmem + lane_off + kColG + gcol, v);
+            if (q < 2) {
+                const int t = m;
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const int j = tid & 63, sc = (tid >> 6) + 4 * m, s0 = 4 * sc;
-                float vv[4];
+                for (int j = 0; j < 32; ++j) wds[j] = to_tf32(s0 + j <= t ? v[j] : 0.f);
+                tmem_st32_issue(tmem + lane_off + kColAC + gcol, wds);
+            } else {
+                const int t = m - 64;
+                if (cg < 2) {
+                    float *LC = reinterpret_cast<float *>(sm + SM_LC);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) vv[e] = (s0 + e < lc) ? RawX::ld1(rv, s0 + e, j) : 0.f;
-                st_tf32x4(sm + L::BC + sw128_off(j, 64 + s0, 64), vv[0], vv[1], vv[2], vv[3]);
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<float4 *>(LC + t * kLd + s0 + j) =
+                            make_float4(s0 + j < t ? v[j] : 0.f, s0 + j + 1 < t ? v[j + 1] : 0.f,
+                                        s0 + j + 2 < t ? v[j + 2] : 0.f, s0 + j + 3 < t ? v[j + 3] : 0.f);
+                } else {
+                    unsigned char *BY = sm + SM_BY;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        *reinterpret_cast<uint32_t *>(BY + sw128_off(64 + s0 + j, t, 128)) =
+                            to_tf32(s0 + j < t ? v[j] : 0.f);
+                }
             }
+            tmem_wait_st();
         }
         sync_for_mma();
+        // The raw tiles and E are no longer read for this chunk: fetch the next one.
+        if (tid == 0 && has_next) issue_tma(c + 1);
 
-        // ---- MMA G: [R ; Q] x [C ; K]^T -> TMEM G (128 x 128)
-        if (tid == 0) {
-#pragma unroll
-            for (int kq = 0; kq < 8; ++kq) {
-                const uint32_t koff = (kq >> 2) * 128 * 128 + (kq & 3) * 32;
-                mma_tf32(tmem + kColG, sdesc_sw128(sbase + L::P + koff),
-                         sdesc_sw128(sbase + L::P + 32768 + koff), idesc_tf32(128, 128), kq > 0);
-            }
-            mma_commit(bar_mma);
-        }
-        if (!wait_uniform(bar_mma, mma_parity, p.status)) { alive = false; break; }
-        mma_parity ^= 1u;
-        tc_fence_after_sync();
-
-        // ---- phase 3: L_c -> LC scratch, L_k^T -> B_Y rows 64.., Qa^T -> B_Y rows 0..63
-        {
-            float *LC = reinterpret_cast<float *>(sm + L::AX);
-            unsigned char *BY = sm + L::P + 32768;
-            if (q >= 2) {
-                const int t = 32 * (q - 2) + lane;  // Q rows of G sit in TMEM lanes 64..127
-                float v[64];
-                tmem_ld64(tmem + lane_off + kColG + 64 * hf, v);
-                if (hf == 0) {  // L_c[t][s], s < t
-#pragma unroll
-                    for (int s0 = 0; s0 < 64; s0 += 4) {
-                        float4 x;
-                        x.x = (s0 < t) ? v[s0] : 0.f;
-                        x.y = (s0 + 1 < t) ? v[s0 + 1] : 0.f;
-                        x.z = (s0 + 2 < t) ? v[s0 + 2] : 0.f;
-                        x.w = (s0 + 3 < t) ? v[s0 + 3] : 0.f;
-                        *reinterpret_cast<float4 *>(LC + t * kLd + s0) = x;
-                    }
-                } else {  // B_Y[64 + s][t] = L_k[t][s]
-#pragma unroll
-                    for (int sidx = 0; sidx < 64; ++sidx)
-                        *reinterpret_cast<uint32_t *>(BY + sw128_off(64 + sidx, t, 128)) =
-                            to_tf32(sidx < t ? v[sidx] : 0.f);
-                }
-            } else {
-                // Qa^T: B_Y[i][t] = kk[t][i] e^{g_{t-1}[i]}  (= kk * E[t-1] * eref, or kk at t = 0)
-                const int lt = (warp & 1) * 32 + lane + 64 * (warp >> 2);  // warps 0,1,4,5 -> 0..127
-#pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    const int i = lt & 63;
-                    const int tc = (lt >> 6) + 2 * m;  // 0..15
-                    const int tb = 4 * tc;
-                    const float er = eref[i];
-                    float x[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int t = tb + e;
-                        const float f = (t == 0) ? 1.f : Et[(t - 1) * 64 + i] * er;
-                        x[e] = (t < lc) ? RawX::ld1(rkk, t, i) * f : 0.f;
-                    }
-                    st_tf32x4(BY + sw128_off(i, tb, 128), x[0], x[1], x[2], x[3]);
-                }
-            }
-        }
-        fence_proxy_async_smem();
-        __syncthreads();
-
-        // ---- phase 4: T = (I + L_c)^{-1} in fp32 (TS), then T^T -> BX.
+        // ---- phase 4: T = (I + L_c)^{-1} in fp32, then T^T -> B_X.
         // Diagonal 16x16 blocks by right-looking substitution in registers;
-        // then the 32x32 halves T_A, T_B (T_10 = -T_11 L_10 T_00, likewise
-        // T_32), then T_BA = -T_B (L_BA T_A).  Only lower-triangular entries of
-        // TS are ever written or read; T^T takes zeros above the diagonal.
+        // then T_10 = -T_11 L_10 T_00 (and T_32 likewise), then
+        // T_BA = -T_B (L_BA T_A) on the 32x32 halves.  Only lower-triangular
+        // entries are written or read; T^T takes zeros above the diagonal.
         {
-            const float *LC = reinterpret_cast<const float *>(sm + L::AX);
-            float *TS = reinterpret_cast<float *>(sm + L::P);
-            float *XS = reinterpret_cast<float *>(sm + L::P + 64 * kLd * 4);  // 32 x 32 scratch
+            const float *LC = reinterpret_cast<const float *>(sm + SM_LC);
+            float *TS = reinterpret_cast<float *>(sm + SM_TS);
+            float *XS = reinterpret_cast<float *>(sm + SM_XS);
             if (tid < 64) {
                 const int bb = tid >> 4, j = tid & 15, o = 16 * bb;
                 float x[16];
@@ -397,254 +480,158 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
                     if (t >= j) TS[(o + t) * kLd + o + j] = x[t];
             }
             __syncthreads();
-            // Y1 = L_10 T_00 -> XS[0..255], Y3 = L_32 T_22 -> XS[256..511]  (T lower triangular:
-            // entries above the diagonal are never written, so they are masked, not read as zero)
-            {
-                const int blk = tid >> 7, r = (tid >> 3) & 15, c0 = (tid & 7) * 2;
-                const int o = 32 * blk;  // block (1,0) at rows 16.., cols 0..; block (3,2) at rows 48.., cols 32..
-                float y0 = 0.f, y1 = 0.f;
+            {   // Y1 = L_10 T_00 -> XS[0..255], Y3 = L_32 T_22 -> XS[256..511]
+                const int blk = tid >> 8, r = (tid >> 4) & 15, cc = tid & 15, o = 32 * blk;
+                float y = 0.f;
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const float l = LC[(o + 16 + r) * kLd + o + u];
-                    const float2 tt = *reinterpret_cast<const float2 *>(TS + (o + u) * kLd + o + c0);
-                    y0 = fmaf(l, u >= c0 ? tt.x : 0.f, y0);
-                    y1 = fmaf(l, u > c0 ? tt.y : 0.f, y1);
-                }
-                *reinterpret_cast<float2 *>(XS + blk * 256 + r * 16 + c0) = make_float2(y0, y1);
+                for (int u = 0; u < 16; ++u)
+                    y = fmaf(LC[(o + 16 + r) * kLd + o + u], u >= cc ? TS[(o + u) * kLd + o + cc] : 0.f, y);
+                XS[blk * 256 + r * 16 + cc] = y;
             }
             __syncthreads();
-            // T_10 = -T_11 Y1, T_32 = -T_33 Y3
-            {
-                const int blk = tid >> 7, r = (tid >> 3) & 15, c0 = (tid & 7) * 2;
-                const int o = 32 * blk;
-                float t0 = 0.f, t1 = 0.f;
+            {   // T_10 = -T_11 Y1, T_32 = -T_33 Y3
+                const int blk = tid >> 8, r = (tid >> 4) & 15, cc = tid & 15, o = 32 * blk;
+                float t_ = 0.f;
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const float a = u <= r ? TS[(o + 16 + r) * kLd + o + 16 + u] : 0.f;
-                    const float2 y = *reinterpret_cast<const float2 *>(XS + blk * 256 + u * 16 + c0);
-                    t0 = fmaf(a, y.x, t0);
-                    t1 = fmaf(a, y.y, t1);
-                }
-                *reinterpret_cast<float2 *>(TS + (o + 16 + r) * kLd + o + c0) = make_float2(-t0, -t1);
+                for (int u = 0; u < 16; ++u)
+                    t_ = fmaf(u <= r ? TS[(o + 16 + r) * kLd + o + 16 + u] : 0.f, XS[blk * 256 + u * 16 + cc], t_);
+                TS[(o + 16 + r) * kLd + o + cc] = -t_;
             }
             __syncthreads();
-            // Z = L_BA T_A (32 x 32) -> XS
-            {
-                const int r = tid >> 3, c0 = (tid & 7) * 4;
-                float z0 = 0.f, z1 = 0.f, z2 = 0.f, z3 = 0.f;
+            {   // Z = L_BA T_A (32 x 32) -> XS
+                const int r = tid >> 4, c0 = (tid & 15) * 2;
+                float z0 = 0.f, z1 = 0.f;
 #pragma unroll
                 for (int u = 0; u < 32; ++u) {
                     const float l = LC[(32 + r) * kLd + u];
-                    const float4 tA = *reinterpret_cast<const float4 *>(TS + u * kLd + c0);
+                    const float2 tA = *reinterpret_cast<const float2 *>(TS + u * kLd + c0);
                     z0 = fmaf(l, u >= c0 ? tA.x : 0.f, z0);
                     z1 = fmaf(l, u >= c0 + 1 ? tA.y : 0.f, z1);
-                    z2 = fmaf(l, u >= c0 + 2 ? tA.z : 0.f, z2);
-                    z3 = fmaf(l, u >= c0 + 3 ? tA.w : 0.f, z3);
                 }
-                *reinterpret_cast<float4 *>(XS + r * 32 + c0) = make_float4(z0, z1, z2, z3);
+                *reinterpret_cast<float2 *>(XS + r * 32 + c0) = make_float2(z0, z1);
             }
             __syncthreads();
-            // T_BA = -T_B Z
-            {
-                const int r = tid >> 3, c0 = (tid & 7) * 4;
-                float t0 = 0.f, t1 = 0.f, t2 = 0.f, t3 = 0.f;
+            {   // T_BA = -T_B Z
+                const int r = tid >> 4, c0 = (tid & 15) * 2;
+                float t0_ = 0.f, t1_ = 0.f;
 #pragma unroll
                 for (int u = 0; u < 32; ++u) {
                     const float a = u <= r ? TS[(32 + r) * kLd + 32 + u] : 0.f;
-                    const float4 z = *reinterpret_cast<const float4 *>(XS + u * 32 + c0);
-                    t0 = fmaf(a, z.x, t0);
-                    t1 = fmaf(a, z.y, t1);
-                    t2 = fmaf(a, z.z, t2);
-                    t3 = fmaf(a, z.w, t3);
+                    const float2 z = *reinterpret_cast<const float2 *>(XS + u * 32 + c0);
+                    t0_ = fmaf(a, z.x, t0_);
+                    t1_ = fmaf(a, z.y, t1_);
                 }
-                *reinterpret_cast<float4 *>(TS + (32 + r) * kLd + c0) = make_float4(-t0, -t1, -t2, -t3);
+                *reinterpret_cast<float2 *>(TS + (32 + r) * kLd + c0) = make_float2(-t0_, -t1_);
             }
             __syncthreads();
-            // T^T into BX: BX[n][k] = T[k][n] (zero above the diagonal)
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const int n = tid & 63, kc = (tid >> 6) + 4 * m, k0 = 4 * kc;
-                st_tf32x4(sm + L::BX + sw128_off(n, k0, 64), k0 >= n ? TS[k0 * kLd + n] : 0.f,
+            for (int u = 0; u < 2; ++u) {  // T^T into B_X: BX[n][k] = T[k][n]
+                const int task = tid + kThreads * u;
+                const int n = task & 63, k0 = 4 * (task >> 6);
+                st_tf32x4(sm + SM_BX + sw128_off(n, k0, 64), k0 >= n ? TS[k0 * kLd + n] : 0.f,
                           k0 + 1 >= n ? TS[(k0 + 1) * kLd + n] : 0.f, k0 + 2 >= n ? TS[(k0 + 2) * kLd + n] : 0.f,
                           k0 + 3 >= n ? TS[(k0 + 3) * kLd + n] : 0.f);
             }
-            __syncthreads();  // LC (in AX) is dead from here on
-        }
-
-        // ---- phase 4b: A_X = [M_c ; Cb^T]; e^{g_C} saved for the state update
-        {
-            unsigned char *AXo = sm + L::AX;
-            if (q < 2 && hf == 0) {
-                const int t = 32 * q + lane;  // R rows of G sit in TMEM lanes 0..63
-                float v[64];
-                tmem_ld64(tmem + lane_off + kColG, v);
-#pragma unroll
-                for (int s0 = 0; s0 < 64; s0 += 4)
-                    st_tf32x4(AXo + sw128_off(t, s0, 128), s0 <= t ? v[s0] : 0.f, s0 + 1 <= t ? v[s0 + 1] : 0.f,
-                              s0 + 2 <= t ? v[s0 + 2] : 0.f, s0 + 3 <= t ? v[s0 + 3] : 0.f);
-            } else {
-                // Cb^T[i][s] = kk[s][i] a[s][i] e^{g_C[i] - g_s[i]} = c * E[63][i] / E[s][i]
-                const int idx = tid - 64;  // warps 2..7 -> 0..191
-                for (int e = idx; e < 1024; e += 192) {
-                    const int i = e & 63, sc = e >> 6, s0 = 4 * sc;
-                    const float e63 = Et[63 * 64 + i];
-                    float x[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int ss = s0 + u;
-                        x[u] = (ss < lc) ? RawX::ld1(rkk, ss, i) * RawX::ld1(ra, ss, i) * (e63 * rcp(Et[ss * 64 + i])) : 0.f;
-                    }
-                    st_tf32x4(AXo + sw128_off(64 + i, s0, 128), x[0], x[1], x[2], x[3]);
-                }
-                if (idx < 64) gC[idx] = Et[63 * 64 + idx] * eref[idx];
-            }
         }
         sync_for_mma();
 
-        // ---- MMA X: [M_c ; Cb^T] (128 x 64) x T -> TMEM X (128 x 64)
+        // ---- MMA X = [M_c ; Cb^T] T   (A_X lives in A_chain's columns 0..63)
         if (tid == 0) {
 #pragma unroll
-            for (int kq = 0; kq < 8; ++kq) {
-                mma_tf32(tmem + kColX, sdesc_sw128(sbase + L::AX + (kq >> 2) * 128 * 128 + (kq & 3) * 32),
-                         sdesc_sw128(sbase + L::BX + (kq >> 2) * 64 * 128 + (kq & 3) * 32),
-                         idesc_tf32(128, 64), kq > 0);
-            }
-            mma_commit(bar_mma);
+            for (int kq = 0; kq < 8; ++kq)
+                mma_tf32_tmem_a(tmem + kColX, tmem + kColAC + 8 * kq,
+                                sdesc_sw128(sbase + SM_BX + (kq >> 2) * 64 * 128 + (kq & 3) * 32),
+                                idesc_tf32(128, 64), kq > 0);
+            mma_commit(bar_x);
         }
-        if (!wait_uniform(bar_mma, mma_parity, p.status)) { alive = false; break; }
-        mma_parity ^= 1u;
+        // ---- next chunk, phase 1 (overlaps MMA X)
+        if (has_next) {
+            if (!wait_uniform(bar_tma, static_cast<uint32_t>((c + 1) & 1), p.status)) { alive = false; break; }
+            phase1(chunk_len(c + 1), (c + 1) & 1);
+        }
+        if (!wait_uniform(bar_x, par, p.status)) { alive = false; break; }
         tc_fence_after_sync();
-
-        // ---- phase 5: A_Y = X (rows m, K = t) into P[0, 32K)
+        // A_chain columns 0..63 (A_X, now consumed) <- base [Ra ; 0], Ra[t][i] = R[t][i] e^{g_ref}[i]
         {
-            float v[32];
-            tmem_ld32(tmem + lane_off + kColX + 32 * hf, v);
-            const int m = 32 * q + lane;
-#pragma unroll
-            for (int j = 0; j < 32; j += 4)
-                st_tf32x4(sm + L::P + sw128_off(m, 32 * hf + j, 128), v[j], v[j + 1], v[j + 2], v[j + 3]);
-        }
-        sync_for_mma();
-
-        // ---- MMA Y: [Mt ; Ct] x [Qa | L_k] -> TMEM Y (128 x 128)
-        if (tid == 0) {
-#pragma unroll
-            for (int kq = 0; kq < 8; ++kq) {
-                const uint32_t koff = (kq >> 2) * 128 * 128 + (kq & 3) * 32;
-                mma_tf32(tmem + kColY, sdesc_sw128(sbase + L::P + koff),
-                         sdesc_sw128(sbase + L::P + 32768 + koff), idesc_tf32(128, 128), kq > 0);
-            }
-            mma_commit(bar_mma);
-        }
-        if (!wait_uniform(bar_mma, mma_parity, p.status)) { alive = false; break; }
-        mma_parity ^= 1u;
-        tc_fence_after_sync();
-
-        // ---- phase 6: A_chain (128 x K 128) in P
-        //   rows t:    [ Ra - Mt Qa | M_k - Mt L_k ]      rows 64+i: [ -Ct Qa | Kb^T - Ct L_k ]
-        {
-            unsigned char *AC = sm + L::P;
-            // pass 1: Ra (rows t, K 0..63) and Kb^T (rows 64+i, K 64..127) base values, fp32
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const int task = tid + kThreads * m;
-                const int t = task >> 4, i = (task & 15) * 4;
-                const float valid = t < lc ? 1.f : 0.f;
-                const float4 e = ld_f4(reinterpret_cast<unsigned char *>(Et + t * 64 + i));
-                const float4 xr = RawX::ld4(rr, t, i);
-                const float4 er = ld_f4(reinterpret_cast<unsigned char *>(eref + i));
-                *reinterpret_cast<float4 *>(AC + sw128_off(t, i, 128)) =
-                    make_float4(valid * xr.x * e.x * er.x, valid * xr.y * e.y * er.y,
-                                valid * xr.z * e.z * er.z, valid * xr.w * e.w * er.w);
-            }
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const int i = tid & 63, sc = (tid >> 6) + 4 * m, s0 = 4 * sc;
-                const float e63 = Et[63 * 64 + i];
-                float x[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int ss = s0 + u;
-                    x[u] = (ss < lc) ? RawX::ld1(rk, ss, i) * (e63 * rcp(Et[ss * 64 + i])) : 0.f;
-                }
-                *reinterpret_cast<float4 *>(AC + sw128_off(64 + i, 64 + s0, 128)) = make_float4(x[0], x[1], x[2], x[3]);
-            }
-            __syncthreads();
-            // pass 2: combine with TMEM (Y, and M_k from G); each entry is rounded to tf32 once
-            const int mrow = 32 * q + lane;
-            float y[32], g[32];
-            for (int half = 0; half < 2; ++half) {
-                const int kb = 64 * hf + 32 * half;  // K columns of A_chain handled here
-                tmem_ld32(tmem + lane_off + kColY + kb, y);
-                if (q < 2 && hf == 1) tmem_ld32(tmem + lane_off + kColG + kb, g);  // R K^T block (M_k)
-#pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    unsigned char *dst = AC + sw128_off(mrow, kb + j, 128);
-                    float o4[4];
-                    if ((q < 2 && hf == 0) || (q >= 2 && hf == 1)) {
-                        const uint4 cur = *reinterpret_cast<const uint4 *>(dst);
-                        o4[0] = __uint_as_float(cur.x) - y[j];
-                        o4[1] = __uint_as_float(cur.y) - y[j + 1];
-                        o4[2] = __uint_as_float(cur.z) - y[j + 2];
-                        o4[3] = __uint_as_float(cur.w) - y[j + 3];
-                    } else if (q < 2) {  // M_k - Mt L_k, M_k masked to s <= t
-                        const int s0 = kb - 64 + j;
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) o4[u] = (s0 + u <= mrow ? g[j + u] : 0.f) - y[j + u];
-                    } else {  // -Ct Qa
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) o4[u] = -y[j + u];
-                    }
-                    st_tf32x4(dst, o4[0], o4[1], o4[2], o4[3]);
-                }
-            }
-        }
-        sync_for_mma();
-
-        // The raw tiles, E and AX are no longer read: fetch the next chunk now.
-        if (tid == 0 && c + 1 < nchunks) issue_tma(c + 1);
-
-        // ---- MMA chain: A_chain (128 x 128) x [S0 ; V] -> TMEM D (128 x 64)
-        if (tid == 0) {
-#pragma unroll
-            for (int kq = 0; kq < 16; ++kq) {
-                mma_tf32(tmem + kColD, sdesc_sw128(sbase + L::P + (kq >> 2) * 128 * 128 + (kq & 3) * 32),
-                         sdesc_sw128(sbase + L::BC + (kq >> 2) * 64 * 128 + (kq & 3) * 32),
-                         idesc_tf32(128, 64), kq > 0);
-            }
-            mma_commit(bar_mma);
-        }
-        if (!wait_uniform(bar_mma, mma_parity, p.status)) { alive = false; break; }
-        mma_parity ^= 1u;
-        tc_fence_after_sync();
-
-        // ---- phase 7: outputs and the state update
-        {
-            float v[32];
-            tmem_ld32(tmem + lane_off + kColD + 32 * hf, v);
+            float v[16];
+            uint32_t wds[16];
             if (q < 2) {
-                const int t = 32 * q + lane;
-                if (t < lc) {
-                    float4 *dst = reinterpret_cast<float4 *>(p.o + (t0 + t) * tok_stride + h * 64 + 32 * hf);
+                tmem_ld16(tmem + lane_off + kColAG + 16 * cg, v);  // R (this chunk's Gram A operand)
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-                }
+                for (int j = 0; j < 16; ++j) wds[j] = to_tf32(v[j] * erc[16 * cg + j]);
             } else {
-                const float decay = gC[srow];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    s[j] = fmaf(decay, s[j], v[j]);
-                    *reinterpret_cast<uint32_t *>(sm + L::BC + sw128_off(32 * hf + j, srow, 64)) = to_tf32(s[j]);
-                }
+                for (int j = 0; j < 16; ++j) wds[j] = 0u;
             }
+            tmem_st16(tmem + lane_off + kColAC + 16 * cg, wds);
         }
         sync_for_mma();
+
+        // ---- MMA A_chain -= X [Qa | L_k]  (negated A, accumulating onto the base)
+        if (tid == 0) {
+#pragma unroll
+            for (int kq = 0; kq < 8; ++kq)
+                mma_tf32_tmem_a(tmem + kColAC, tmem + kColX + 8 * kq,
+                                sdesc_sw128(sbase + SM_BY + (kq >> 2) * 128 * 128 + (kq & 3) * 32),
+                                idesc_tf32(128, 128) | kIdescNegateA, 1);
+            mma_commit(bar_y);
+        }
+        // ---- next chunk, phase 2 (overlaps the A_chain product)
+        if (has_next) phase2(chunk_len(c + 1), EREF + ((c + 1) & 1) * 64);
+        sync_for_mma();
+        if (!wait_uniform(bar_y, par, p.status)) { alive = false; break; }
+        tc_fence_after_sync();
+
+        // ---- MMA D = A_chain [S0 ; V]; then the next chunk's Gram products
+        if (tid == 0) {
+#pragma unroll
+            for (int kq = 0; kq < 16; ++kq)
+                mma_tf32_tmem_a(tmem + kColD, tmem + kColAC + 8 * kq,
+                                sdesc_sw128(sbase + SM_BC + (kq >> 2) * 64 * 128 + (kq & 3) * 32),
+                                idesc_tf32(128, 64), kq > 0);
+            mma_commit(bar_d);
+            if (has_next) issue_gram();
+        }
+        if (!wait_uniform(bar_d, par, p.status)) { alive = false; break; }
+        tc_fence_after_sync();
+        // A_chain is consumed: the next chunk's transposing product may overwrite it.
+        if (tid == 0 && has_next) {
+            issue_transpose();
+            mma_commit(bar_g);
+        }
+
+        // ---- phase 5: outputs, the state update, the next chunk's V^T
+        {
+            float v[16];
+            tmem_ld16(tmem + lane_off + kColD + 16 * cg, v);
+            if (q < 2) {
+                const int t = m;
+                if (t < lc) {
+                    float4 *dst = reinterpret_cast<float4 *>(p.o + (t0 + t) * tok_stride + h * 64 + 16 * cg);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                }
+            } else {
+                const float decay = GC[(c & 1) * 64 + si];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    s[j] = fmaf(decay, s[j], v[j]);
+                    *reinterpret_cast<uint32_t *>(sm + SM_BC + sw128_off(16 * cg + j, si, 64)) = to_tf32(s[j]);
+                }
+            }
+            if (has_next) write_vt(chunk_len(c + 1));
+        }
+        sync_for_mma();
+        if (has_next) {
+            if (!wait_uniform(bar_g, static_cast<uint32_t>((c + 1) & 1), p.status)) { alive = false; break; }
+            tc_fence_after_sync();
+        }
     }
 
     if (alive && state_thread && p.final_state) {
-        float4 *dst = reinterpret_cast<float4 *>(p.final_state + sslot + srow * 64 + 32 * hf);
+        float4 *dst = reinterpret_cast<float4 *>(p.final_state + sslot + si * 64 + 16 * cg);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) dst[j] = make_float4(s[4 * j], s[4 * j + 1], s[4 * j + 2], s[4 * j + 3]);
+        for (int j = 0; j < 4; ++j) dst[j] = make_float4(s[4 * j], s[4 * j + 1], s[4 * j + 2], s[4 * j + 3]);
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -673,6 +660,8 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
+// 2-D map over a packed [T_total, H*64] array with 64 x 64 boxes: bf16 tiles
+// in the 128-byte swizzle layout, fp32 (w) tiles unswizzled.
 bool make_map(CUtensorMap *map, const void *base, bool bf16, int T_total, int H) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
@@ -683,31 +672,31 @@ bool make_map(CUtensorMap *map, const void *base, bool bf16, int T_total, int H)
     cuuint32_t estr[2] = {1, 1};
     return enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
                const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               bf16 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename X>
-cudaError_t launch_typed(const PrefillArgs &args, cudaStream_t stream) {
-    using L = Layout<Raw<X>::kB>;
-    const bool bf16 = Raw<X>::kB == 2;
+cudaError_t launch_chunked(const PrefillArgs &args, cudaStream_t stream) {
     TensorMaps maps;
-    if (!make_map(&maps.r, args.r, bf16, args.T_total, args.H) ||
-        !make_map(&maps.k, args.k, bf16, args.T_total, args.H) ||
-        !make_map(&maps.v, args.v, bf16, args.T_total, args.H) ||
-        !make_map(&maps.kk, args.kk, bf16, args.T_total, args.H) ||
-        !make_map(&maps.a, args.a, bf16, args.T_total, args.H) ||
+    if (!make_map(&maps.r, args.r, true, args.T_total, args.H) ||
+        !make_map(&maps.k, args.k, true, args.T_total, args.H) ||
+        !make_map(&maps.v, args.v, true, args.T_total, args.H) ||
+        !make_map(&maps.kk, args.kk, true, args.T_total, args.H) ||
+        !make_map(&maps.a, args.a, true, args.T_total, args.H) ||
         !make_map(&maps.w, args.w, false, args.T_total, args.H))
         return cudaErrorInvalidValue;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(wkv7_prefill_chunked_kernel<X>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    static int attr_dev = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (attr_dev != dev) {
+        e = cudaFuncSetAttribute(wkv7_prefill_chunked_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemAlloc);
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        attr_dev = dev;
     }
     const long long pairs = static_cast<long long>(args.num_seqs) * args.H;
-    wkv7_prefill_chunked_kernel<X><<<static_cast<unsigned>(pairs), kThreads, L::kAlloc, stream>>>(args, maps);
+    wkv7_prefill_chunked_kernel<<<static_cast<unsigned>(pairs), kThreads, kSmemAlloc, stream>>>(args, maps);
     return cudaGetLastError();
 }
 
@@ -727,7 +716,7 @@ cudaError_t launch_prefill(const PrefillArgs &args, void *, size_t, cudaStream_t
     }
     // bf16 inputs (the prefill format) take the chunked tensor-core kernel;
     // fp32 inputs take the exact token-serial kernel.
-    if (args.x_dtype == WKV7_BF16) return launch_typed<__nv_bfloat16>(args, stream);
+    if (args.x_dtype == WKV7_BF16) return launch_chunked(args, stream);
     return launch_prefill_scan(args, stream);
 }
 
