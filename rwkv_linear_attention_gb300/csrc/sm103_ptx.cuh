@@ -50,6 +50,30 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     return false;
 }
 
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Named barrier `id` over `count` threads (a multiple of 32).
+template <int ID, int COUNT>
+__device__ __forceinline__ void named_sync() {
+    asm volatile("bar.sync %0, %1;" ::"n"(ID), "n"(COUNT) : "memory");
+}
+// Named barrier with an OR-reduction of `pred` over the participating threads.
+template <int ID, int COUNT>
+__device__ __forceinline__ int named_sync_or(int pred) {
+    int r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.s32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.s32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(pred), "n"(ID), "n"(COUNT)
+        : "memory");
+    return r;
+}
+
 // ---------------------------------------------------------------- fences
 
 // Generic-proxy shared-memory writes -> visible to the async proxy (MMA/TMA).

@@ -62,7 +62,8 @@ namespace {
 using namespace ptx;
 
 constexpr int kC = 64;          // chunk length
-constexpr int kThreads = 512;   // warp w: TMEM lane quarter w % 4, column group w / 4
+constexpr int kThreads = 512;   // worker warps w < 16: TMEM lane quarter w % 4, column group w / 4
+constexpr int kBlock = kThreads + 32;  // + one warp that issues every MMA
 constexpr uint32_t kMaxPolls = 1u << 24;
 
 // TMEM columns
@@ -93,7 +94,7 @@ constexpr int SM_GREF = SM_TOT + 2048;     // 64: g_ref
 constexpr int SM_EREF = SM_GREF + 256;     // 2 x 64: e^{g_ref} (double-buffered across chunks)
 constexpr int SM_E63 = SM_EREF + 512;      // 64: e^{g_C - g_ref}
 constexpr int SM_GC = SM_E63 + 256;        // 2 x 64: e^{g_C} (double-buffered across chunks)
-constexpr int SM_BAR = SM_GC + 512;        // 5 mbarriers
+constexpr int SM_BAR = SM_GC + 512;        // 7 mbarriers
 constexpr int SM_SLOT = SM_BAR + 64;
 constexpr int kSmemBytes = SM_SLOT + 64;
 constexpr int kSmemAlloc = kSmemBytes + 1024;
@@ -146,25 +147,34 @@ struct TensorMaps {
     CUtensorMap r, k, v, kk, a, w;
 };
 
-// All threads wait on an mbarrier phase; the outcome is uniform, so either
-// every thread continues or every thread leaves together.
+// Barriers among the 512 worker threads (the MMA warp never joins them).
+__device__ __forceinline__ void wsync() { named_sync<1, kThreads>(); }
+
+// All workers wait on an mbarrier phase; the outcome is uniform, so either
+// every worker continues or every worker leaves together.
 __device__ __forceinline__ bool wait_uniform(uint32_t bar, uint32_t parity, unsigned *status) {
     const bool ok = mbar_wait_bounded(bar, parity, kMaxPolls);
-    const int any_fail = __syncthreads_or(ok ? 0 : 1);
+    const int any_fail = named_sync_or<1, kThreads>(ok ? 0 : 1);
     if (any_fail && threadIdx.x == 0) report(status, kDevTimeout);
     return any_fail == 0;
 }
 
-// Shared-memory operand writes and tensor-memory stores by all threads ->
-// visible to the MMA issued after this barrier.
+// Shared-memory operand writes and tensor-memory stores by all workers ->
+// visible to the tensor core and to every worker after this barrier.
 __device__ __forceinline__ void sync_for_mma() {
     fence_proxy_async_smem();
     tc_fence_before_sync();
-    __syncthreads();
+    wsync();
     tc_fence_after_sync();
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// Operands for the next MMA step are in place: publish them and tell the MMA warp.
+__device__ __forceinline__ void handoff(uint32_t bar_rdy) {
+    sync_for_mma();
+    if (threadIdx.x == 0) mbar_arrive(bar_rdy);
+}
+
+__global__ void __launch_bounds__(kBlock, 1)
 wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps maps) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(
@@ -228,7 +238,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
     float *E63 = reinterpret_cast<float *>(sm + SM_E63);
     float *GC = reinterpret_cast<float *>(sm + SM_GC);
     const uint32_t bar_tma = sbase + SM_BAR, bar_g = bar_tma + 8, bar_x = bar_tma + 16, bar_y = bar_tma + 24,
-                   bar_d = bar_tma + 32;
+                   bar_d = bar_tma + 32, bar_rdy = bar_tma + 40, bar_i = bar_tma + 48;
 
     if (tid == 0) {
         mbar_init(bar_tma, 1);
@@ -236,6 +246,8 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
         mbar_init(bar_x, 1);
         mbar_init(bar_y, 1);
         mbar_init(bar_d, 1);
+        mbar_init(bar_rdy, 1);
+        mbar_init(bar_i, 1);
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(sbase + SM_SLOT, kTmemCols);
@@ -274,14 +286,14 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
             g[u] = acc;
         }
         TOT[seg * 64 + ch] = acc;
-        __syncthreads();
+        wsync();
         float pre = 0.f;
 #pragma unroll
         for (int u = 0; u < 8; ++u) pre += (u < seg) ? TOT[u * 64 + ch] : 0.f;
 #pragma unroll
         for (int u = 0; u < 8; ++u) g[u] += pre;
         if (seg == 3) GREF[ch] = g[7];
-        __syncthreads();
+        wsync();
         const float gr = GREF[ch];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
@@ -379,20 +391,96 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
                             idesc_tf32(128, 128), kq > 0);
     };
 
+    bool alive = true;
+    if (warp == kThreads / 32) {
+        // ======== the MMA warp: one lane issues every tensor-core product, in
+        // the order the workers hand the operands over (bar_rdy), so operand
+        // staging never waits for MMA issue.
+        if (lane == 0) {
+            uint32_t rp = 0, ip = 0;
+            auto ready = [&]() {
+                const bool ok = mbar_wait_bounded(bar_rdy, rp, kMaxPolls);
+                rp ^= 1u;
+                tc_fence_after_sync();
+                return ok;
+            };
+            auto wait_own = [&]() {  // the MMA warp's own wait on products it chains
+                const bool ok = mbar_wait_bounded(bar_i, ip, kMaxPolls);
+                ip ^= 1u;
+                tc_fence_after_sync();
+                return ok;
+            };
+            bool ok = ready();  // chunk 0: Gram operands
+            if (ok) {
+                issue_gram();
+                issue_transpose();
+                mma_commit(bar_g);
+            }
+            for (int c = 0; c < nchunks && ok; ++c) {
+                const bool has_next = c + 1 < nchunks;
+                const uint32_t par = static_cast<uint32_t>(c & 1);
+                // X = [M_c ; Cb^T] T in three products (A_X lives in A_chain's columns 0..63):
+                //   X_R = B_R T_B -> X[:, 32:64);  B_L -= X_R L_BA (in place);  X_L = B_L T_A -> X[:, 0:32)
+                if (!(ok = ready())) break;
+#pragma unroll
+                for (int kq = 0; kq < 4; ++kq)
+                    mma_tf32_tmem_a(tmem + kColX + 32, tmem + kColAC + 32 + 8 * kq,
+                                    sdesc_sw128(sbase + SM_BX + kq * 32), idesc_tf32(128, 32), kq > 0);
+                mma_commit(bar_i);
+                if (!(ok = wait_own())) break;
+#pragma unroll
+                for (int kq = 0; kq < 4; ++kq)
+                    mma_tf32_tmem_a(tmem + kColAC, tmem + kColX + 32 + 8 * kq,
+                                    sdesc_sw128(sbase + SM_BX + 4096 + kq * 32),
+                                    idesc_tf32(128, 32) | kIdescNegateA, 1);
+                mma_commit(bar_i);
+                if (!(ok = wait_own())) break;
+#pragma unroll
+                for (int kq = 0; kq < 4; ++kq)
+                    mma_tf32_tmem_a(tmem + kColX, tmem + kColAC + 8 * kq, sdesc_sw128(sbase + SM_BX + 8192 + kq * 32),
+                                    idesc_tf32(128, 32), kq > 0);
+                mma_commit(bar_x);
+                // A_chain -= X [Qa | L_k]  (negated A, accumulating onto the base [Ra | M_k ; 0 | Kb^T])
+                if (!(ok = ready())) break;
+#pragma unroll
+                for (int kq = 0; kq < 8; ++kq)
+                    mma_tf32_tmem_a(tmem + kColAC, tmem + kColX + 8 * kq,
+                                    sdesc_sw128(sbase + SM_BY + (kq >> 2) * 128 * 128 + (kq & 3) * 32),
+                                    idesc_tf32(128, 128) | kIdescNegateA, 1);
+                mma_commit(bar_y);
+                // D = A_chain [S0 ; V]
+                if (!(ok = mbar_wait_bounded(bar_y, par, kMaxPolls))) break;
+                tc_fence_after_sync();
+#pragma unroll
+                for (int kq = 0; kq < 16; ++kq)
+                    mma_tf32_tmem_a(tmem + kColD, tmem + kColAC + 8 * kq,
+                                    sdesc_sw128(sbase + SM_BC + (kq >> 2) * 64 * 128 + (kq & 3) * 32),
+                                    idesc_tf32(128, 64), kq > 0);
+                mma_commit(bar_d);
+                if (has_next) {
+                    // the next chunk's Gram products; the transposing one overwrites A_chain,
+                    // so it waits for D to complete
+                    if (!(ok = ready())) break;
+                    issue_gram();
+                    if (!(ok = mbar_wait_bounded(bar_d, par, kMaxPolls))) break;
+                    tc_fence_after_sync();
+                    issue_transpose();
+                    mma_commit(bar_g);
+                }
+            }
+            if (!ok) report(p.status, kDevTimeout);
+        }
+    } else {
+    // ======== the 512 worker threads
     // ---- prologue: chunk 0 up to its Gram product
     if (tid == 0) issue_tma(0);
-    bool alive = wait_uniform(bar_tma, 0, p.status);
+    alive = wait_uniform(bar_tma, 0, p.status);
     if (alive) {
         phase1(chunk_len(0), 0);
-        __syncthreads();
+        wsync();
         phase2(chunk_len(0), EREF);
         write_vt(chunk_len(0));
-        sync_for_mma();
-        if (tid == 0) {
-            issue_gram();
-            issue_transpose();
-            mma_commit(bar_g);
-        }
+        handoff(bar_rdy);
         alive = wait_uniform(bar_g, 0, p.status);
         tc_fence_after_sync();
     }
@@ -456,11 +544,12 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
         // The raw tiles and E are no longer read for this chunk: fetch the next one.
         if (tid == 0 && has_next) issue_tma(c + 1);
 
-        // ---- phase 4: T = (I + L_c)^{-1} in fp32, then T^T -> B_X.
-        // Diagonal 16x16 blocks by right-looking substitution in registers;
-        // then T_10 = -T_11 L_10 T_00 (and T_32 likewise), then
-        // T_BA = -T_B (L_BA T_A) on the 32x32 halves.  Only lower-triangular
-        // entries are written or read; T^T takes zeros above the diagonal.
+        // ---- phase 4: the two 32x32 diagonal halves of T = (I + L_c)^{-1}, in fp32:
+        // T_A = (I + L_AA)^{-1}, T_B = (I + L_BB)^{-1} (16x16 diagonal blocks by right-looking
+        // substitution in registers, then T_10 = -T_11 L_10 T_00 and T_32 likewise).  The
+        // off-diagonal half T_BA = -T_B L_BA T_A is never formed: with [M_c ; Cb^T] = [B_L | B_R],
+        //   X_R = B_R T_B,   X_L = (B_L - X_R L_BA) T_A
+        // are three small MMAs.  Their B operands T_B^T, L_BA^T, T_A^T go to B_X.
         {
             const float *LC = reinterpret_cast<const float *>(sm + SM_LC);
             float *TS = reinterpret_cast<float *>(sm + SM_TS);
@@ -479,7 +568,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
                 for (int t = 0; t < 16; ++t)
                     if (t >= j) TS[(o + t) * kLd + o + j] = x[t];
             }
-            __syncthreads();
+            wsync();
             {   // Y1 = L_10 T_00 -> XS[0..255], Y3 = L_32 T_22 -> XS[256..511]
                 const int blk = tid >> 8, r = (tid >> 4) & 15, cc = tid & 15, o = 32 * blk;
                 float y = 0.f;
@@ -488,7 +577,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
                     y = fmaf(LC[(o + 16 + r) * kLd + o + u], u >= cc ? TS[(o + u) * kLd + o + cc] : 0.f, y);
                 XS[blk * 256 + r * 16 + cc] = y;
             }
-            __syncthreads();
+            wsync();
             {   // T_10 = -T_11 Y1, T_32 = -T_33 Y3
                 const int blk = tid >> 8, r = (tid >> 4) & 15, cc = tid & 15, o = 32 * blk;
                 float t_ = 0.f;
@@ -497,54 +586,28 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
                     t_ = fmaf(u <= r ? TS[(o + 16 + r) * kLd + o + 16 + u] : 0.f, XS[blk * 256 + u * 16 + cc], t_);
                 TS[(o + 16 + r) * kLd + o + cc] = -t_;
             }
-            __syncthreads();
-            {   // Z = L_BA T_A (32 x 32) -> XS
-                const int r = tid >> 4, c0 = (tid & 15) * 2;
-                float z0 = 0.f, z1 = 0.f;
+            wsync();
+            // B_X: [T_B^T | L_BA^T | T_A^T], each 32 rows x K 32 (B[n][k] = M[k][n])
 #pragma unroll
-                for (int u = 0; u < 32; ++u) {
-                    const float l = LC[(32 + r) * kLd + u];
-                    const float2 tA = *reinterpret_cast<const float2 *>(TS + u * kLd + c0);
-                    z0 = fmaf(l, u >= c0 ? tA.x : 0.f, z0);
-                    z1 = fmaf(l, u >= c0 + 1 ? tA.y : 0.f, z1);
-                }
-                *reinterpret_cast<float2 *>(XS + r * 32 + c0) = make_float2(z0, z1);
-            }
-            __syncthreads();
-            {   // T_BA = -T_B Z
-                const int r = tid >> 4, c0 = (tid & 15) * 2;
-                float t0_ = 0.f, t1_ = 0.f;
-#pragma unroll
-                for (int u = 0; u < 32; ++u) {
-                    const float a = u <= r ? TS[(32 + r) * kLd + 32 + u] : 0.f;
-                    const float2 z = *reinterpret_cast<const float2 *>(XS + u * 32 + c0);
-                    t0_ = fmaf(a, z.x, t0_);
-                    t1_ = fmaf(a, z.y, t1_);
-                }
-                *reinterpret_cast<float2 *>(TS + (32 + r) * kLd + c0) = make_float2(-t0_, -t1_);
-            }
-            __syncthreads();
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {  // T^T into B_X: BX[n][k] = T[k][n]
+            for (int u = 0; u < 2; ++u) {
                 const int task = tid + kThreads * u;
-                const int n = task & 63, k0 = 4 * (task >> 6);
-                st_tf32x4(sm + SM_BX + sw128_off(n, k0, 64), k0 >= n ? TS[k0 * kLd + n] : 0.f,
-                          k0 + 1 >= n ? TS[(k0 + 1) * kLd + n] : 0.f, k0 + 2 >= n ? TS[(k0 + 2) * kLd + n] : 0.f,
-                          k0 + 3 >= n ? TS[(k0 + 3) * kLd + n] : 0.f);
+                if (task < 768) {
+                    const int op = task >> 8, n = (task >> 3) & 31, k0 = 4 * (task & 7);
+                    float e[4];
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const int k = k0 + jj;
+                        if (op == 0)      e[jj] = k >= n ? TS[(32 + k) * kLd + 32 + n] : 0.f;
+                        else if (op == 1) e[jj] = LC[(32 + k) * kLd + n];
+                        else              e[jj] = k >= n ? TS[k * kLd + n] : 0.f;
+                    }
+                    st_tf32x4(sm + SM_BX + op * 4096 + sw128_off(n, k0, 32), e[0], e[1], e[2], e[3]);
+                }
             }
         }
-        sync_for_mma();
+        handoff(bar_rdy);  // -> X = [M_c ; Cb^T] T
 
-        // ---- MMA X = [M_c ; Cb^T] T   (A_X lives in A_chain's columns 0..63)
-        if (tid == 0) {
-#pragma unroll
-            for (int kq = 0; kq < 8; ++kq)
-                mma_tf32_tmem_a(tmem + kColX, tmem + kColAC + 8 * kq,
-                                sdesc_sw128(sbase + SM_BX + (kq >> 2) * 64 * 128 + (kq & 3) * 32),
-                                idesc_tf32(128, 64), kq > 0);
-            mma_commit(bar_x);
-        }
-        // ---- next chunk, phase 1 (overlaps MMA X)
+        // ---- next chunk, phase 1 (overlaps X_L)
         if (has_next) {
             if (!wait_uniform(bar_tma, static_cast<uint32_t>((c + 1) & 1), p.status)) { alive = false; break; }
             phase1(chunk_len(c + 1), (c + 1) & 1);
@@ -565,40 +628,15 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
             }
             tmem_st16(tmem + lane_off + kColAC + 16 * cg, wds);
         }
-        sync_for_mma();
+        handoff(bar_rdy);  // -> A_chain -= X [Qa | L_k], then D = A_chain [S0 ; V]
 
-        // ---- MMA A_chain -= X [Qa | L_k]  (negated A, accumulating onto the base)
-        if (tid == 0) {
-#pragma unroll
-            for (int kq = 0; kq < 8; ++kq)
-                mma_tf32_tmem_a(tmem + kColAC, tmem + kColX + 8 * kq,
-                                sdesc_sw128(sbase + SM_BY + (kq >> 2) * 128 * 128 + (kq & 3) * 32),
-                                idesc_tf32(128, 128) | kIdescNegateA, 1);
-            mma_commit(bar_y);
-        }
-        // ---- next chunk, phase 2 (overlaps the A_chain product)
-        if (has_next) phase2(chunk_len(c + 1), EREF + ((c + 1) & 1) * 64);
-        sync_for_mma();
-        if (!wait_uniform(bar_y, par, p.status)) { alive = false; break; }
-        tc_fence_after_sync();
-
-        // ---- MMA D = A_chain [S0 ; V]; then the next chunk's Gram products
-        if (tid == 0) {
-#pragma unroll
-            for (int kq = 0; kq < 16; ++kq)
-                mma_tf32_tmem_a(tmem + kColD, tmem + kColAC + 8 * kq,
-                                sdesc_sw128(sbase + SM_BC + (kq >> 2) * 64 * 128 + (kq & 3) * 32),
-                                idesc_tf32(128, 64), kq > 0);
-            mma_commit(bar_d);
-            if (has_next) issue_gram();
+        // ---- next chunk, phase 2 (overlaps the A_chain and D products)
+        if (has_next) {
+            phase2(chunk_len(c + 1), EREF + ((c + 1) & 1) * 64);
+            handoff(bar_rdy);  // -> the next chunk's Gram products
         }
         if (!wait_uniform(bar_d, par, p.status)) { alive = false; break; }
         tc_fence_after_sync();
-        // A_chain is consumed: the next chunk's transposing product may overwrite it.
-        if (tid == 0 && has_next) {
-            issue_transpose();
-            mma_commit(bar_g);
-        }
 
         // ---- phase 5: outputs, the state update, the next chunk's V^T
         {
@@ -633,6 +671,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
 #pragma unroll
         for (int j = 0; j < 4; ++j) dst[j] = make_float4(s[4 * j], s[4 * j + 1], s[4 * j + 2], s[4 * j + 3]);
     }
+    }  // workers
     tc_fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
@@ -696,7 +735,7 @@ cudaError_t launch_chunked(const PrefillArgs &args, cudaStream_t stream) {
         attr_dev = dev;
     }
     const long long pairs = static_cast<long long>(args.num_seqs) * args.H;
-    wkv7_prefill_chunked_kernel<<<static_cast<unsigned>(pairs), kThreads, kSmemAlloc, stream>>>(args, maps);
+    wkv7_prefill_chunked_kernel<<<static_cast<unsigned>(pairs), kBlock, kSmemAlloc, stream>>>(args, maps);
     return cudaGetLastError();
 }
 
