@@ -379,6 +379,7 @@ def run_ours(args):
     launch_s = ms / 1e3 / launches
     achieved = wl.B * wl.H * STEP_BYTES / launch_s / 1e9
     step_src = [os.path.join(ROOT, "rwkv_linear_attention_gb300", "csrc", "wkv7_step.cu")]
+    prefill_src = [os.path.join(ROOT, "rwkv_linear_attention_gb300", "csrc", "wkv7_prefill_chunked.cu")]
     traffic = kernel_traffic("wkv7_step_kernel", f"B={B},H={cfg['H']}", step_src)
     del graphs
 
@@ -441,7 +442,10 @@ def run_ours(args):
                                    "bf16 r,k,v,kk,a, fp32 w, zero initial state, final state out",
                        "l2": "inputs larger than L2"},
             "roofline": {"bound": "hbm", "achieved": round(pre_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": round(pre_gbs / peaks["hbm_gbs"], 4), "traffic": None,
+                         "frac": round(pre_gbs / peaks["hbm_gbs"], 4),
+                         "traffic": kernel_traffic("wkv7_prefill_chunked_kernel", "2.9B 8x4096 H=40", prefill_src),
+                         "kernel": "wkv7_prefill_chunked_kernel",
+                         "algorithmic_bytes_per_launch": pre["algorithmic_bytes"],
                          "tensor_tflops": round(pre_tflops, 2),
                          "tensor_frac_of_bf16": round(pre_tflops / peaks["bf16_tflops"], 4)},
         },
