@@ -310,6 +310,75 @@ def prefill_bench(dev, steps, warmup, world):
     }
 
 
+def time_stream(fn, steps, warmup, stream):
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            fn()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(steps):
+            fn()
+        end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / steps
+
+
+def run_configs(args, dev, peaks):
+    """One JSON line per named workload (decode at every batch, both prefill
+    workloads), for the design notes; not the contract line."""
+    import torch
+
+    import rwkv_linear_attention_gb300 as wkv7
+    from rwkv_linear_attention_gb300 import inputs
+    hbm = peaks["hbm_gbs"]
+    stream = torch.cuda.Stream(device=dev)
+    # decode: 2.9B geometry at B = 1, 8, 32; 7.2B geometry at B = 256
+    for label, cfg, B in [("decode 2.9B", inputs.DECODE_2P9B, 1), ("decode 2.9B", inputs.DECODE_2P9B, 8),
+                          ("decode 2.9B", inputs.DECODE_2P9B, 32), ("decode 7.2B", inputs.DECODE_7P2B, 256)]:
+        wl = DecodeWorkload(cfg["layers"], B, cfg["H"], 4, dev, seed=7)
+        graphs = wl.capture(stream)
+        steps = max(8, args.steps // (1 if B < 256 else 64))
+        ms = time_graphs(graphs, steps, args.warmup, stream, 1) / steps
+        launch_us = ms * 1e3 / wl.layers
+        gbs = wl.B * wl.H * STEP_BYTES / (launch_us * 1e-6) / 1e9
+        print(json.dumps({"workload": f"{label} B={B}", "us_per_launch": round(launch_us, 3),
+                          "state_gbs": round(wl.state_bytes_per_step() / (ms * 1e-3) / 1e9, 1),
+                          "achieved_gbs": round(gbs, 1), "frac": round(gbs / hbm, 4)}), flush=True)
+        del graphs, wl
+        torch.cuda.empty_cache()
+    # prefill: 2.9B 8 x 4096; 7.2B varlen (16 x U[1, 32768]); 7.2B single 32768
+    v = inputs.VARLEN_7P2B
+    cases = [("prefill 2.9B 8x4096", [4096] * 8, 40, False),
+             ("prefill 7.2B varlen 16 x U[1,32768]", inputs.seqlens_uniform(v["num_seqs"], v["lo"], v["hi"], 1004), 64, True),
+             ("prefill 7.2B 1x32768", [v["single_T"]], 64, True)]
+    for label, lens, H, with_s0 in cases:
+        p = inputs.prefill_inputs(lens, H, 64, seed=11, device=dev)
+        cu = p["cu_seqlens"]
+        cu_dev = cu.to(dev)
+        T = int(cu[-1])
+        s0 = inputs.initial_state(len(lens), H, 64, seed=11, std=0.1, device=dev) if with_s0 else None
+        o = torch.empty(T, H, 64, device=dev)
+        sf = torch.empty(len(lens), H, 64, 64, device=dev)
+        ws_n = wkv7.prefill_workspace_size(len(lens), T, H)
+        ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=dev)
+
+        def call():
+            wkv7.prefill(p["r"], p["w"], p["k"], p["v"], p["kk"], p["a"], cu_dev, initial_state=s0, final_state=sf,
+                         o=o, workspace=ws if ws_n else None, cu_seqlens_host=cu, stream=stream)
+        ms = time_stream(call, max(3, args.prefill_steps // 4), 2, stream)
+        wkv7.check_device_status(stream)
+        nbytes = T * H * PREFILL_BYTES_PER_TOKEN_HEAD + (2 if with_s0 else 1) * len(lens) * H * 16384
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        print(json.dumps({"workload": label, "tokens": T, "ms_per_call": round(ms, 4),
+                          "tokens_per_s": round(T / (ms * 1e-3), 1), "achieved_gbs": round(gbs, 1),
+                          "frac": round(gbs / hbm, 4), "roofline_ms": round(nbytes / hbm / 1e6, 4)}), flush=True)
+        del p, o, sf, ws
+        torch.cuda.empty_cache()
+
+
 def cpu_baseline_decode(B, H, layers, budget_s=15.0):
     """The oracle, as it stands, on the host cores: a bounded sample of decode
     steps (all B x H heads of as many layers as fit the time budget)."""
@@ -353,6 +422,10 @@ def run_ours(args):
 
     from rwkv_linear_attention_gb300 import inputs
     peaks, peak_kind = load_peaks()
+    if args.workload == "configs":
+        if rank == 0:
+            run_configs(args, dev, peaks)
+        return
     if args.workload == "prefill":
         pre = prefill_bench(dev, args.prefill_steps, args.warmup, world)
         if rank == 0:
@@ -513,8 +586,9 @@ def main(argv=None):
     ap.add_argument("--prefill-steps", type=int, default=20)
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=("all", "decode", "prefill"), default="all",
-                    help="all (the contract line); decode or prefill alone, for profiling")
+    ap.add_argument("--workload", choices=("all", "decode", "prefill", "configs"), default="all",
+                    help="all (the contract line); decode or prefill alone, for profiling; "
+                         "configs: one line per named workload")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -179,7 +179,14 @@ wkv7_status wkv7_prefill(int num_seqs, int T_total, int H, int N, const int32_t 
     args.final_state = final_state;
     args.o = o;
     args.status = status;
-    cudaError_t e = wkv7::launch_prefill(args, workspace, workspace_bytes, stream);
+    cudaError_t e = cudaSuccess;
+    if (need > 0 && wkv7::prefill_wants_order(args, cu_seqlens_host)) {
+        int32_t *order = static_cast<int32_t *>(workspace);
+        e = wkv7::launch_prefill_order(cu_seqlens, num_seqs, order, stream);
+        if (e != cudaSuccess) return cuda_fail(e);
+        args.order = order;
+    }
+    e = wkv7::launch_prefill(args, workspace, workspace_bytes, stream);
     return e == cudaSuccess ? WKV7_OK : cuda_fail(e);
 }
 

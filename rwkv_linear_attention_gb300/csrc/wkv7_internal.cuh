@@ -54,5 +54,9 @@ cudaError_t launch_prefill_scan(const PrefillArgs &args, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillArgs &args, void *workspace, size_t workspace_bytes,
                            cudaStream_t stream);
 size_t prefill_workspace_bytes(int num_seqs, int T_total, int H);
+// Whether this batch is worth a longest-first schedule, and the kernel that
+// writes it (order[rank] = sequence index) into device memory.
+bool prefill_wants_order(const PrefillArgs &args, const int32_t *cu_seqlens_host);
+cudaError_t launch_prefill_order(const int32_t *cu_seqlens, int num_seqs, int32_t *order, cudaStream_t stream);
 
 }  // namespace wkv7

@@ -677,6 +677,50 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
+// ---------------------------------------------------------------- scheduling
+
+// Longest-first order of the sequences: order[rank] = sequence index, by
+// descending length, ties by index.  One CTA sorts (key, index) pairs with a
+// bitonic network in shared memory.  Blocks of the prefill kernel are handed
+// out in blockIdx order as SMs free up, so launching the longest pairs first
+// keeps a long sequence from starting last and stretching the tail.
+constexpr int kOrderThreads = 1024;
+constexpr int kMaxOrdered = 4096;  // sequences sorted on the device; more keep input order
+
+__global__ void __launch_bounds__(kOrderThreads)
+wkv7_prefill_order_kernel(const int32_t *__restrict__ cu, int num_seqs, int32_t *__restrict__ order) {
+    __shared__ unsigned long long key[kMaxOrdered];
+    int n2 = 1;
+    while (n2 < num_seqs) n2 <<= 1;
+    for (int i = threadIdx.x; i < n2; i += kOrderThreads) {
+        unsigned long long k = ~0ull;  // padding sorts last
+        if (i < num_seqs) {
+            const int len = max(0, cu[i + 1] - cu[i]);
+            // ascending sort of (~len, index) = descending length, then index
+            k = (static_cast<unsigned long long>(0x7fffffff - len) << 32) | static_cast<unsigned>(i);
+        }
+        key[i] = k;
+    }
+    __syncthreads();
+    for (int size = 2; size <= n2; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = threadIdx.x; i < n2; i += kOrderThreads) {
+                const int j = i ^ stride;
+                if (j > i) {
+                    const bool up = (i & size) == 0;
+                    const unsigned long long a = key[i], b = key[j];
+                    if ((a > b) == up) {
+                        key[i] = b;
+                        key[j] = a;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+    for (int i = threadIdx.x; i < num_seqs; i += kOrderThreads) order[i] = static_cast<int32_t>(key[i] & 0xffffffffu);
+}
+
 // ---------------------------------------------------------------- host side
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -741,7 +785,26 @@ cudaError_t launch_chunked(const PrefillArgs &args, cudaStream_t stream) {
 
 }  // namespace
 
-size_t prefill_workspace_bytes(int, int, int) { return 0; }
+// Workspace: the longest-first order of the sequences (int32 per sequence),
+// for batches of 2 .. kMaxOrdered sequences.
+size_t prefill_workspace_bytes(int num_seqs, int, int) {
+    if (num_seqs < 2 || num_seqs > kMaxOrdered) return 0;
+    return (static_cast<size_t>(num_seqs) * sizeof(int32_t) + 255) & ~static_cast<size_t>(255);
+}
+
+bool prefill_wants_order(const PrefillArgs &args, const int32_t *cu_seqlens_host) {
+    if (args.num_seqs < 2 || args.num_seqs > kMaxOrdered || args.x_dtype != WKV7_BF16) return false;
+    if (!cu_seqlens_host) return true;  // lengths unknown on the host: sort on the device
+    const int32_t len0 = cu_seqlens_host[1] - cu_seqlens_host[0];
+    for (int b = 1; b < args.num_seqs; ++b)
+        if (cu_seqlens_host[b + 1] - cu_seqlens_host[b] != len0) return true;
+    return false;  // all lengths equal: the input order is already longest-first
+}
+
+cudaError_t launch_prefill_order(const int32_t *cu_seqlens, int num_seqs, int32_t *order, cudaStream_t stream) {
+    wkv7_prefill_order_kernel<<<1, kOrderThreads, 0, stream>>>(cu_seqlens, num_seqs, order);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_prefill(const PrefillArgs &args, void *, size_t, cudaStream_t stream) {
     const long long pairs = static_cast<long long>(args.num_seqs) * args.H;

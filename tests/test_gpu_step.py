@@ -197,3 +197,19 @@ def test_step_rejects_bad_arguments_on_gpu(dev):
             B, H, N, *[wkv7._ptr(x[n]) for n in NAMES], wkv7._ptr(state),
             wkv7._ptr(big[1:]), wkv7._stream()), "misaligned o")
     assert e.value.status == wkv7._lib.ERR_ALIGNMENT
+
+
+@pytest.mark.parametrize("B,H", [(8191, 1), (128, 64)], ids=["8191-heads", "8192-heads"])
+def test_step_either_side_of_the_large_batch_form(dev, B, H):
+    """Both decode forms (shared-memory ring below 8192 heads, register form from
+    8192 heads) against the oracle, from a random state."""
+    N = 64
+    x = inputs.decode_inputs(B, H, N, steps=1, seed=B + H, device=dev)
+    x = {n: t[0].contiguous() for n, t in x.items()}
+    s0 = inputs.initial_state(B, H, N, seed=B, device=dev)
+    state = s0.clone()
+    o = _step(x, state)
+    wkv7.check_device_status()
+    o_ref, s_ref = oracle.step(*(x[n] for n in NAMES), state=s0.double().cpu())
+    assert rel_err(o, o_ref) <= TOL
+    assert rel_err(state, s_ref) <= TOL
