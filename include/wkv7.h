@@ -138,6 +138,38 @@ WKV7_API wkv7_status wkv7_prefill(int num_seqs, int T_total, int H, int N,
                          void *workspace, size_t workspace_bytes,
                          cudaStream_t stream);
 
+/*
+ * wkv7_prefill_noalloc -- wkv7_prefill without a caller-supplied workspace.
+ *
+ * For callers that cannot allocate device memory when they run the prefill:
+ * a serving engine whose memory plan reserves the whole device up front so
+ * that request handling never allocates, code recorded during CUDA stream
+ * capture (where cudaMalloc is not permitted), or a host program that only
+ * receives pointers to buffers owned by someone else.  The pages have no
+ * counterpart; the arguments are those of wkv7_prefill without `workspace`.
+ *
+ * The scratch this call needs (the longest-first order of the sequences)
+ * lives in a fixed device array of WKV7_NOALLOC_MAX_SEQS int32 entries
+ * (16 KB) that the library reserves on every GPU that loads it, until the
+ * process exits.  num_seqs > WKV7_NOALLOC_MAX_SEQS returns
+ * WKV7_ERR_WORKSPACE.  The call allocates nothing.  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress, with
+ * that device current); make that first call before any stream capture.
+ * All calls on a device share the array: calls that overlap on the GPU (on
+ * different streams, or launched from different threads without ordering)
+ * race on it and must be serialised by the caller.  Each call overwrites the
+ * entries it uses before reading them.
+ */
+#define WKV7_NOALLOC_MAX_SEQS 4096
+
+WKV7_API wkv7_status wkv7_prefill_noalloc(int num_seqs, int T_total, int H, int N,
+                         const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                         wkv7_dtype x_dtype,
+                         const void *r, const float *w, const void *k,
+                         const void *v, const void *kk, const void *a,
+                         const float *initial_state, float *final_state, float *o,
+                         cudaStream_t stream);
+
 /* Static English text for a status code (never NULL). */
 WKV7_API const char *wkv7_status_string(wkv7_status status);
 

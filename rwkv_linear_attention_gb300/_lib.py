@@ -29,6 +29,7 @@ EXPORTS = (
     "wkv7_step",
     "wkv7_prefill_workspace_size",
     "wkv7_prefill",
+    "wkv7_prefill_noalloc",
     "wkv7_status_string",
     "wkv7_check_device_status",
     "wkv7_last_cuda_error",
@@ -53,6 +54,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.wkv7_prefill_workspace_size.argtypes = [I, I, I, I]
     lib.wkv7_prefill.restype = I
     lib.wkv7_prefill.argtypes = [I, I, I, I, P, P, I, P, P, P, P, P, P, P, P, P, P, S, P]
+    lib.wkv7_prefill_noalloc.restype = I
+    lib.wkv7_prefill_noalloc.argtypes = [I, I, I, I, P, P, I, P, P, P, P, P, P, P, P, P, P]
     lib.wkv7_status_string.restype = ctypes.c_char_p
     lib.wkv7_status_string.argtypes = [I]
     lib.wkv7_check_device_status.restype = I
