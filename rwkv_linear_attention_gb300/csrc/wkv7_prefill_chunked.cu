@@ -23,12 +23,15 @@
 //   [ O                  ]   [ Ra - Mt Qa | M_k - Mt L_k  ]   [ S0 ]
 //   [ S_C - e^{g_C} * S0 ] = [ -Ct Qa     | Kb^T - Ct L_k ] . [ V  ]      (A_chain)
 //
-// with [Mt ; Ct] = [M_c ; Cb^T] T.  Per chunk four tf32 MMAs run, all with
-// M = 128, fp32 accumulators in tensor memory and the A operand read from
-// tensor memory:
+// with [Mt ; Ct] = [M_c ; Cb^T] T.  Every row i of the lower half carries the
+// factor e^{g_C - g_ref}[i] (Cb^T = diag(e^{g_C - g_ref}) C^T, likewise Kb^T);
+// the kernel keeps the lower half without it and applies it to the state rows
+// of the product.  Per chunk these tf32 MMAs run, all with M = 128, fp32
+// accumulators in tensor memory and the A operand read from tensor memory:
 //   G       = [R ; Q] [C ; K]^T                 (the four Gram blocks; 128x128x64)
-//   X       = [M_c ; Cb^T] T                     (128x64x64)
-//   A_chain = base - X [Qa | L_k]                (accumulated onto base = [Ra | M_k ; 0 | Kb^T]; 128x128x64)
+//   [. ; C^T | K^T] = [0 ; I] [C ; K]^T          (the transposes, no SIMT transposition)
+//   X       = [M_c ; C^T] T                      (three small products, see phase 4)
+//   A_chain = base - X [Qa | L_k]                (accumulated onto base = [Ra | M_k ; 0 | K^T]; 128x128x64)
 //   D       = A_chain [S0 ; V]                   (128x64x128)
 // The SIMT work (cumulative decay, exponentials, masks, the blocked 64x64
 // unit-lower-triangular inverse, operand staging) is software-pipelined with
@@ -68,12 +71,12 @@ constexpr uint32_t kMaxPolls = 1u << 24;
 
 // TMEM columns
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColG = 0;     // G; then [M_c ; Cb^T] in its first 64 columns
+constexpr uint32_t kColG = 0;     // G
 constexpr uint32_t kColX = 128;   // X = [Mt ; Ct]
 constexpr uint32_t kColAC = 192;  // A_chain (128 columns)
 constexpr uint32_t kColD = 320;   // D = [O ; S_C - e^{g_C} S0]
 constexpr uint32_t kColAG = 384;  // A operand of G = [R ; Q] (for the next chunk)
-constexpr uint32_t kColAT = 448;  // A operand [0 ; diag(e^{g_C - g_ref})] of the transposing product
+constexpr uint32_t kColAT = 448;  // constant A operand [0 ; I] of the transposing product
 
 constexpr int kLd = 68;  // padded row stride (floats) of the fp32 L_c / T scratch
 
@@ -81,8 +84,7 @@ constexpr int kLd = 68;  // padded row stride (floats) of the fp32 L_c / T scrat
 constexpr int kTile = 64 * 64 * 2;  // one bf16 raw tile
 constexpr int SM_R = 0, SM_K = SM_R + kTile, SM_KK = SM_K + kTile, SM_A = SM_KK + kTile, SM_V = SM_A + kTile;
 constexpr int SM_W = SM_V + kTile;         // fp32 w tile -> E = e^{g - g_ref} (swizzled)
-constexpr int SM_EI = SM_W + 16384;        // fp32 1/E = e^{g_ref - g} (swizzled like E)
-constexpr int SM_BG = SM_EI + 16384;       // B operand of G: [C ; K]  (128 x K64)
+constexpr int SM_BG = SM_W + 16384;        // B operand of G: [C ; K]  (128 x K64)
 constexpr int SM_BY = SM_BG + 32768;       // B operand of A_chain: [Qa^T ; L_k^T] (128 x K64)
 constexpr int SM_BX = SM_BY + 32768;       // B operand of X: T^T (64 x K64)
 constexpr int SM_BC = SM_BX + 16384;       // B operand of D: [S0^T | V^T] (64 x K128)
@@ -92,8 +94,8 @@ constexpr int SM_XS = SM_TS + 64 * kLd * 4;  // fp32 32 x 32 scratch
 constexpr int SM_TOT = SM_XS + 4096;       // 8 x 64 cumsum partials
 constexpr int SM_GREF = SM_TOT + 2048;     // 64: g_ref
 constexpr int SM_EREF = SM_GREF + 256;     // 2 x 64: e^{g_ref} (double-buffered across chunks)
-constexpr int SM_E63 = SM_EREF + 512;      // 64: e^{g_C - g_ref}
-constexpr int SM_GC = SM_E63 + 256;        // 2 x 64: e^{g_C} (double-buffered across chunks)
+constexpr int SM_E63 = SM_EREF + 512;      // 2 x 64: e^{g_C - g_ref} (double-buffered across chunks)
+constexpr int SM_GC = SM_E63 + 512;        // 2 x 64: e^{g_C} (double-buffered across chunks)
 constexpr int SM_BAR = SM_GC + 512;        // 7 mbarriers
 constexpr int SM_SLOT = SM_BAR + 64;
 constexpr int kSmemBytes = SM_SLOT + 64;
@@ -133,18 +135,12 @@ __device__ __forceinline__ void raw8(const unsigned char *tile, int t, int i, fl
         f[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
     }
 }
-// four consecutive channels i .. i+3 (i % 4 == 0)
-__device__ __forceinline__ float4 raw4(const unsigned char *tile, int t, int i) {
-    const uint2 u = *reinterpret_cast<const uint2 *>(tile + raw_off(t, i));
-    return make_float4(bf2f(u.x & 0xffffu), __uint_as_float(u.x & 0xffff0000u), bf2f(u.y & 0xffffu),
-                       __uint_as_float(u.y & 0xffff0000u));
-}
-
 // E table [64][64] fp32 with 16-byte chunks XOR-swizzled by (t mod 8).
 __device__ __forceinline__ int eidx(int t, int i) { return t * 64 + ((((i >> 2) ^ (t & 7)) << 2) | (i & 3)); }
 
 struct TensorMaps {
     CUtensorMap r, k, v, kk, a, w;
+    CUtensorMap o;  // fp32 output, 64 x 32 boxes in the 128-byte swizzle layout (stores)
 };
 
 // Barriers among the 512 worker threads (the MMA warp never joins them).
@@ -231,7 +227,6 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
 
     unsigned char *rr = sm + SM_R, *rk = sm + SM_K, *rkk = sm + SM_KK, *ra = sm + SM_A, *rv = sm + SM_V;
     float *E = reinterpret_cast<float *>(sm + SM_W);
-    float *EI = reinterpret_cast<float *>(sm + SM_EI);
     float *TOT = reinterpret_cast<float *>(sm + SM_TOT);
     float *GREF = reinterpret_cast<float *>(sm + SM_GREF);
     float *EREF = reinterpret_cast<float *>(sm + SM_EREF);
@@ -274,7 +269,8 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
     };
     auto chunk_len = [&](int chunk) { return min(kC, eos - (bos + chunk * kC)); };
 
-    // ---- phase 1: masked cumulative log-decay g; E = e^{g - g_ref} (g_ref = g[31]) in place
+    // ---- phase 1: masked cumulative log-decay g; E = e^{g - g_ref} (g_ref = g[31]) in place;
+    // the Gram B operand [C ; K] from the same registers
     auto phase1 = [&](int lc, int gbuf) {
         const int ch = tid & 63, seg = tid >> 6;  // rows 8*seg .. 8*seg+7
         float g[8];
@@ -295,19 +291,25 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
         if (seg == 3) GREF[ch] = g[7];
         wsync();
         const float gr = GREF[ch];
+        unsigned char *BG = sm + SM_BG;
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-            E[eidx(8 * seg + u, ch)] = __expf(g[u] - gr);
-            EI[eidx(8 * seg + u, ch)] = __expf(gr - g[u]);
+            const int t = 8 * seg + u;
+            E[eidx(t, ch)] = __expf(g[u] - gr);
+            // B_G = [C ; K]: C[s][i] = kk a e^{g_ref - g_s}, K[s][i] = k e^{g_ref - g_s} (rows s = t, 64 + t)
+            const float ei = t < lc ? __expf(gr - g[u]) : 0.f;
+            *reinterpret_cast<uint32_t *>(BG + sw128_off(t, ch, 128)) =
+                to_tf32(raw1(rkk, t, ch) * raw1(ra, t, ch) * ei);
+            *reinterpret_cast<uint32_t *>(BG + sw128_off(64 + t, ch, 128)) = to_tf32(raw1(rk, t, ch) * ei);
         }
         if (seg == 0) EREF[gbuf * 64 + ch] = __expf(gr);
         if (seg == 7) {
-            E63[ch] = __expf(g[7] - gr);
+            E63[gbuf * 64 + ch] = __expf(g[7] - gr);
             GC[gbuf * 64 + ch] = __expf(g[7]);
         }
     };
 
-    // ---- phase 2: A_G = [R ; Q] into TMEM, B_G = [C ; K] into shared memory
+    // ---- phase 2: A_G = [R ; Q] into TMEM
     auto phase2 = [&](int lc, const float *eref) {
         {
             const bool rrow = m < 64;
@@ -335,28 +337,6 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
                 wds[j + 3] = to_tf32(valid * x[j + 3] * e.w);
             }
             tmem_st16(tmem + lane_off + kColAG + i0, wds);
-            // A_T row m: e^{g_C - g_ref}[m - 64] on the diagonal of its lower half, zero elsewhere
-#pragma unroll
-            for (int j = 0; j < 16; ++j) wds[j] = (m >= 64 && i0 + j == m - 64) ? to_tf32(E63[m - 64]) : 0u;
-            tmem_st16(tmem + lane_off + kColAT + i0, wds);
-        }
-        unsigned char *BG = sm + SM_BG;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int task = tid + kThreads * u;
-            const int n = task >> 4, i = (task & 15) * 4;
-            const int sidx = n & 63;
-            const float4 e = *reinterpret_cast<const float4 *>(EI + eidx(sidx, i));
-            const float valid = sidx < lc ? 1.f : 0.f;
-            const float4 ei = make_float4(valid * e.x, valid * e.y, valid * e.z, valid * e.w);
-            if (n < 64) {
-                const float4 xkk = raw4(rkk, sidx, i), xa = raw4(ra, sidx, i);
-                st_tf32x4(BG + sw128_off(n, i, 128), xkk.x * xa.x * ei.x, xkk.y * xa.y * ei.y,
-                          xkk.z * xa.z * ei.z, xkk.w * xa.w * ei.w);
-            } else {
-                const float4 xk = raw4(rk, sidx, i);
-                st_tf32x4(BG + sw128_off(n, i, 128), xk.x * ei.x, xk.y * ei.y, xk.z * ei.z, xk.w * ei.w);
-            }
         }
     };
 
@@ -374,8 +354,10 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
     };
 
     // Gram product G = [R ; Q] [C ; K]^T, and the transposing product
-    // [0 ; diag(e^{g_C - g_ref})] [C ; K]^T, whose lower half is [Cb^T | Kb^T]
-    // (Cb^T[i][s] = e^{g_C - g_ref}[i] C[s][i], likewise Kb^T), into A_chain's columns.
+    // [0 ; I] [C ; K]^T, whose lower half is [C^T | K^T] -- Cb^T and Kb^T without their
+    // row factor e^{g_C - g_ref}[i] (Cb^T[i][s] = e^{g_C - g_ref}[i] C[s][i]).  That factor
+    // multiplies every row of the lower half of A_chain, so it is applied to the
+    // state rows of D instead.
     auto issue_gram = [&]() {
 #pragma unroll
         for (int kq = 0; kq < 8; ++kq)
@@ -472,7 +454,13 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
         }
     } else {
     // ======== the 512 worker threads
-    // ---- prologue: chunk 0 up to its Gram product
+    // ---- prologue: the constant A_T = [0 ; I]; chunk 0 up to its Gram products
+    {
+        uint32_t wds[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) wds[j] = (m >= 64 && 16 * cg + j == m - 64) ? 0x3f800000u : 0u;
+        tmem_st16(tmem + lane_off + kColAT + 16 * cg, wds);
+    }
     if (tid == 0) issue_tma(0);
     alive = wait_uniform(bar_tma, 0, p.status);
     if (alive) {
@@ -539,6 +527,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
                 }
             }
             tmem_wait_st();
+            if (tid == 0) bulk_wait_read<0>();  // the previous chunk's O stores have read T's scratch
         }
         sync_for_mma();
         // The raw tiles and E are no longer read for this chunk: fetch the next one.
@@ -644,22 +633,35 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
             tmem_ld16(tmem + lane_off + kColD + 16 * cg, v);
             if (q < 2) {
                 const int t = m;
-                if (t < lc) {
+                if (lc == kC) {
+                    // full chunk: stage row t in T's scratch as two 64 x 32 boxes (128-byte
+                    // swizzle), written out below by two TMA stores
+                    unsigned char *box = sm + SM_TS + (cg >> 1) * 8192 + t * 128;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        *reinterpret_cast<float4 *>(box + (((4 * (cg & 1) + j) ^ (t & 7)) << 4)) =
+                            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                } else if (t < lc) {
                     float4 *dst = reinterpret_cast<float4 *>(p.o + (t0 + t) * tok_stride + h * 64 + 16 * cg);
 #pragma unroll
                     for (int j = 0; j < 4; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
                 }
             } else {
-                const float decay = GC[(c & 1) * 64 + si];
+                const float decay = GC[(c & 1) * 64 + si], rowf = E63[(c & 1) * 64 + si];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    s[j] = fmaf(decay, s[j], v[j]);
+                    s[j] = fmaf(decay, s[j], rowf * v[j]);
                     *reinterpret_cast<uint32_t *>(sm + SM_BC + sw128_off(16 * cg + j, si, 64)) = to_tf32(s[j]);
                 }
             }
             if (has_next) write_vt(chunk_len(c + 1));
         }
         sync_for_mma();
+        if (tid == 0 && lc == kC) {
+            tma_store_2d(&maps.o, h * 64, t0, sbase + SM_TS);
+            tma_store_2d(&maps.o, h * 64 + 32, t0, sbase + SM_TS + 8192);
+            bulk_commit();
+        }
         if (has_next) {
             if (!wait_uniform(bar_g, static_cast<uint32_t>((c + 1) & 1), p.status)) { alive = false; break; }
             tc_fence_after_sync();
@@ -671,6 +673,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
 #pragma unroll
         for (int j = 0; j < 4; ++j) dst[j] = make_float4(s[4 * j], s[4 * j + 1], s[4 * j + 2], s[4 * j + 3]);
     }
+    if (tid == 0) bulk_wait<0>();  // every O store has completed
     }  // workers
     tc_fence_before_sync();
     __syncthreads();
@@ -759,6 +762,19 @@ bool make_map(CUtensorMap *map, const void *base, bool bf16, int T_total, int H)
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 output [T_total, H*64] written as 64-row x 32-column boxes in the 128-byte swizzle layout.
+bool make_out_map(CUtensorMap *map, void *base, int T_total, int H) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(H) * 64, static_cast<cuuint64_t>(T_total)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(H) * 64 * 4};
+    cuuint32_t box[2] = {32, 64};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 cudaError_t launch_chunked(const PrefillArgs &args, cudaStream_t stream) {
     TensorMaps maps;
     if (!make_map(&maps.r, args.r, true, args.T_total, args.H) ||
@@ -766,7 +782,7 @@ cudaError_t launch_chunked(const PrefillArgs &args, cudaStream_t stream) {
         !make_map(&maps.v, args.v, true, args.T_total, args.H) ||
         !make_map(&maps.kk, args.kk, true, args.T_total, args.H) ||
         !make_map(&maps.a, args.a, true, args.T_total, args.H) ||
-        !make_map(&maps.w, args.w, false, args.T_total, args.H))
+        !make_map(&maps.w, args.w, false, args.T_total, args.H) || !make_out_map(&maps.o, args.o, args.T_total, args.H))
         return cudaErrorInvalidValue;
     static int attr_dev = -1;
     int dev = 0;
