@@ -42,11 +42,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return done != 0;
 }
 
-// Bounded wait: gives up after max_tries polls (each poll may suspend the
-// thread for a short, hardware-chosen time).  Returns false on expiry.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t max_tries) {
-    for (uint32_t i = 0; i < max_tries; ++i)
+// Global nanosecond timer.
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait: polls until the phase completes, giving up (returning false)
+// once timeout_ns of global time have passed or after max_tries polls,
+// whichever comes first (each poll may suspend the thread for a short,
+// hardware-chosen time).
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t max_tries,
+                                                  uint64_t timeout_ns = 2000000000ull) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1; i < max_tries; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0 && global_ns() - t0 > timeout_ns) return false;
+    }
     return false;
 }
 

@@ -96,8 +96,8 @@ constexpr int SM_GREF = SM_TOT + 2048;     // 64: g_ref
 constexpr int SM_EREF = SM_GREF + 256;     // 2 x 64: e^{g_ref} (double-buffered across chunks)
 constexpr int SM_E63 = SM_EREF + 512;      // 2 x 64: e^{g_C - g_ref} (double-buffered across chunks)
 constexpr int SM_GC = SM_E63 + 512;        // 2 x 64: e^{g_C} (double-buffered across chunks)
-constexpr int SM_BAR = SM_GC + 512;        // 7 mbarriers
-constexpr int SM_SLOT = SM_BAR + 64;
+constexpr int SM_BAR = SM_GC + 512;        // 9 mbarriers
+constexpr int SM_SLOT = SM_BAR + 128;
 constexpr int kSmemBytes = SM_SLOT + 64;
 constexpr int kSmemAlloc = kSmemBytes + 1024;
 static_assert(kSmemAlloc <= 232448, "shared memory layout too large");
@@ -165,9 +165,9 @@ __device__ __forceinline__ void sync_for_mma() {
 }
 
 // Operands for the next MMA step are in place: publish them and tell the MMA warp.
-__device__ __forceinline__ void handoff(uint32_t bar_rdy) {
+__device__ __forceinline__ void handoff(uint32_t rdy) {
     sync_for_mma();
-    if (threadIdx.x == 0) mbar_arrive(bar_rdy);
+    if (threadIdx.x == 0) mbar_arrive(rdy);
 }
 
 __global__ void __launch_bounds__(kBlock, 1)
@@ -232,8 +232,14 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
     float *EREF = reinterpret_cast<float *>(sm + SM_EREF);
     float *E63 = reinterpret_cast<float *>(sm + SM_E63);
     float *GC = reinterpret_cast<float *>(sm + SM_GC);
+    // Product-complete barriers (tensor-core commits) and one operands-ready barrier per
+    // handoff from the workers to the MMA warp.  Each handoff barrier completes once per
+    // chunk and the workers cannot reach the same handoff of the next chunk before the MMA
+    // warp has consumed this one (they first wait on a product it issues after it), so a
+    // waiter never misses a phase.
     const uint32_t bar_tma = sbase + SM_BAR, bar_g = bar_tma + 8, bar_x = bar_tma + 16, bar_y = bar_tma + 24,
-                   bar_d = bar_tma + 32, bar_rdy = bar_tma + 40, bar_i = bar_tma + 48;
+                   bar_d = bar_tma + 32, bar_i = bar_tma + 40;
+    const uint32_t rdy_x = bar_tma + 48, rdy_y = bar_tma + 56, rdy_g = bar_tma + 64;
 
     if (tid == 0) {
         mbar_init(bar_tma, 1);
@@ -241,8 +247,10 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
         mbar_init(bar_x, 1);
         mbar_init(bar_y, 1);
         mbar_init(bar_d, 1);
-        mbar_init(bar_rdy, 1);
         mbar_init(bar_i, 1);
+        mbar_init(rdy_x, 1);
+        mbar_init(rdy_y, 1);
+        mbar_init(rdy_g, 1);
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(sbase + SM_SLOT, kTmemCols);
@@ -376,13 +384,12 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
     bool alive = true;
     if (warp == kThreads / 32) {
         // ======== the MMA warp: one lane issues every tensor-core product, in
-        // the order the workers hand the operands over (bar_rdy), so operand
-        // staging never waits for MMA issue.
+        // the order the workers hand the operands over, so operand staging never
+        // waits for MMA issue.
         if (lane == 0) {
-            uint32_t rp = 0, ip = 0;
-            auto ready = [&]() {
-                const bool ok = mbar_wait_bounded(bar_rdy, rp, kMaxPolls);
-                rp ^= 1u;
+            uint32_t ip = 0;
+            auto ready = [&](uint32_t rdy, uint32_t parity) {
+                const bool ok = mbar_wait_bounded(rdy, parity, kMaxPolls);
                 tc_fence_after_sync();
                 return ok;
             };
@@ -392,7 +399,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
                 tc_fence_after_sync();
                 return ok;
             };
-            bool ok = ready();  // chunk 0: Gram operands
+            bool ok = ready(rdy_g, 0);  // chunk 0: Gram operands
             if (ok) {
                 issue_gram();
                 issue_transpose();
@@ -403,7 +410,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
                 const uint32_t par = static_cast<uint32_t>(c & 1);
                 // X = [M_c ; Cb^T] T in three products (A_X lives in A_chain's columns 0..63):
                 //   X_R = B_R T_B -> X[:, 32:64);  B_L -= X_R L_BA (in place);  X_L = B_L T_A -> X[:, 0:32)
-                if (!(ok = ready())) break;
+                if (!(ok = ready(rdy_x, par))) break;
 #pragma unroll
                 for (int kq = 0; kq < 4; ++kq)
                     mma_tf32_tmem_a(tmem + kColX + 32, tmem + kColAC + 32 + 8 * kq,
@@ -423,7 +430,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
                                     idesc_tf32(128, 32), kq > 0);
                 mma_commit(bar_x);
                 // A_chain -= X [Qa | L_k]  (negated A, accumulating onto the base [Ra | M_k ; 0 | Kb^T])
-                if (!(ok = ready())) break;
+                if (!(ok = ready(rdy_y, par))) break;
 #pragma unroll
                 for (int kq = 0; kq < 8; ++kq)
                     mma_tf32_tmem_a(tmem + kColAC, tmem + kColX + 8 * kq,
@@ -442,7 +449,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
                 if (has_next) {
                     // the next chunk's Gram products; the transposing one overwrites A_chain,
                     // so it waits for D to complete
-                    if (!(ok = ready())) break;
+                    if (!(ok = ready(rdy_g, static_cast<uint32_t>((c + 1) & 1)))) break;
                     issue_gram();
                     if (!(ok = mbar_wait_bounded(bar_d, par, kMaxPolls))) break;
                     tc_fence_after_sync();
@@ -468,7 +475,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
         wsync();
         phase2(chunk_len(0), EREF);
         write_vt(chunk_len(0));
-        handoff(bar_rdy);
+        handoff(rdy_g);
         alive = wait_uniform(bar_g, 0, p.status);
         tc_fence_after_sync();
     }
@@ -482,26 +489,11 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
 
         // ---- phase 3: read G.  M_c (masked) -> A_chain columns 0..63 of rows t, which with
         // the transposing product's Cb^T below them form A_X = [M_c ; Cb^T]; M_k (masked) ->
-        // A_chain rows t, K 64..; L_c -> LC; L_k^T and Qa^T -> B_Y.
+        // A_chain rows t, K 64..; L_c -> LC; L_k^T -> B_Y.
         {
             uint32_t wds[32];
             const int gcol = (cg < 2 ? 0 : 64) + 32 * (cg & 1);  // M_c | M_k (q<2), L_c | L_k (q>=2)
             const int s0 = 32 * (cg & 1);
-            // Qa^T into B_Y rows 0..63: Qa[t][i] = kk e^{g_{t-1}}
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int task = tid + kThreads * u;
-                const int i = task & 63, tb = 4 * (task >> 6);
-                const float er = erc[i];
-                float x[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int t = tb + e;
-                    const float f = (t == 0) ? 1.f : E[eidx(t - 1, i)] * er;
-                    x[e] = (t < lc) ? raw1(rkk, t, i) * f : 0.f;
-                }
-                st_tf32x4(sm + SM_BY + sw128_off(i, tb, 128), x[0], x[1], x[2], x[3]);
-            }
             float v[32];
             tmem_ld32(tmem + lane_off + kColG + gcol, v);
             if (q < 2) {
@@ -530,8 +522,6 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
             if (tid == 0) bulk_wait_read<0>();  // the previous chunk's O stores have read T's scratch
         }
         sync_for_mma();
-        // The raw tiles and E are no longer read for this chunk: fetch the next one.
-        if (tid == 0 && has_next) issue_tma(c + 1);
 
         // ---- phase 4: the two 32x32 diagonal halves of T = (I + L_c)^{-1}, in fp32:
         // T_A = (I + L_AA)^{-1}, T_B = (I + L_BB)^{-1} (16x16 diagonal blocks by right-looking
@@ -556,8 +546,24 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
 #pragma unroll
                 for (int t = 0; t < 16; ++t)
                     if (t >= j) TS[(o + t) * kLd + o + j] = x[t];
+            } else {
+                // the other warps meanwhile: Qa^T into B_Y rows 0..63, Qa[t][i] = kk e^{g_{t-1}}
+                for (int task = tid - 64; task < 1024; task += kThreads - 64) {
+                    const int i = task & 63, tb = 4 * (task >> 6);
+                    const float er = erc[i];
+                    float x[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int t = tb + e;
+                        const float f = (t == 0) ? 1.f : E[eidx(t - 1, i)] * er;
+                        x[e] = (t < lc) ? raw1(rkk, t, i) * f : 0.f;
+                    }
+                    st_tf32x4(sm + SM_BY + sw128_off(i, tb, 128), x[0], x[1], x[2], x[3]);
+                }
             }
             wsync();
+            // The raw tiles and E are no longer read for this chunk: fetch the next one.
+            if (tid == 0 && has_next) issue_tma(c + 1);
             {   // Y1 = L_10 T_00 -> XS[0..255], Y3 = L_32 T_22 -> XS[256..511]
                 const int blk = tid >> 8, r = (tid >> 4) & 15, cc = tid & 15, o = 32 * blk;
                 float y = 0.f;
@@ -594,7 +600,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
                 }
             }
         }
-        handoff(bar_rdy);  // -> X = [M_c ; Cb^T] T
+        handoff(rdy_x);  // -> X = [M_c ; Cb^T] T
 
         // ---- next chunk, phase 1 (overlaps X_L)
         if (has_next) {
@@ -617,12 +623,12 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
             }
             tmem_st16(tmem + lane_off + kColAC + 16 * cg, wds);
         }
-        handoff(bar_rdy);  // -> A_chain -= X [Qa | L_k], then D = A_chain [S0 ; V]
+        handoff(rdy_y);  // -> A_chain -= X [Qa | L_k], then D = A_chain [S0 ; V]
 
         // ---- next chunk, phase 2 (overlaps the A_chain and D products)
         if (has_next) {
             phase2(chunk_len(c + 1), EREF + ((c + 1) & 1) * 64);
-            handoff(bar_rdy);  // -> the next chunk's Gram products
+            handoff(rdy_g);  // -> the next chunk's Gram products
         }
         if (!wait_uniform(bar_d, par, p.status)) { alive = false; break; }
         tc_fence_after_sync();
