@@ -91,8 +91,8 @@ constexpr int SM_BC = SM_BX + 16384;       // B operand of D: [S0^T | V^T] (64 x
 constexpr int SM_LC = SM_BC + 32768;       // fp32 L_c [64][kLd]
 constexpr int SM_TS = SM_LC + 64 * kLd * 4;  // fp32 T [64][kLd]
 constexpr int SM_XS = SM_TS + 64 * kLd * 4;  // fp32 32 x 32 scratch
-constexpr int SM_TOT = SM_XS + 4096;       // 8 x 64 cumsum partials
-constexpr int SM_GREF = SM_TOT + 2048;     // 64: g_ref
+constexpr int SM_TOT = SM_XS + 4096;       // 16 x 64 cumsum partials
+constexpr int SM_GREF = SM_TOT + 4096;     // 64: g_ref
 constexpr int SM_EREF = SM_GREF + 256;     // 2 x 64: e^{g_ref} (double-buffered across chunks)
 constexpr int SM_E63 = SM_EREF + 512;      // 2 x 64: e^{g_C - g_ref} (double-buffered across chunks)
 constexpr int SM_GC = SM_E63 + 512;        // 2 x 64: e^{g_C} (double-buffered across chunks)
@@ -122,8 +122,10 @@ __device__ __forceinline__ float bf2f(uint32_t lo16) { return __uint_as_float(lo
 __device__ __forceinline__ uint32_t raw_off(int t, int i) {
     return t * 128 + ((((i >> 3) ^ (t & 7)) << 4) | ((i & 7) << 1));
 }
-__device__ __forceinline__ float raw1(const unsigned char *tile, int t, int i) {
-    return bf2f(*reinterpret_cast<const unsigned short *>(tile + raw_off(t, i)));
+// channels i, i+1 (i even)
+__device__ __forceinline__ float2 raw2(const unsigned char *tile, int t, int i) {
+    const uint32_t u = *reinterpret_cast<const uint32_t *>(tile + raw_off(t, i));
+    return make_float2(bf2f(u & 0xffffu), __uint_as_float(u & 0xffff0000u));
 }
 // eight consecutive channels i .. i+7 (i % 8 == 0)
 __device__ __forceinline__ void raw8(const unsigned char *tile, int t, int i, float *f) {
@@ -278,42 +280,55 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
     auto chunk_len = [&](int chunk) { return min(kC, eos - (bos + chunk * kC)); };
 
     // ---- phase 1: masked cumulative log-decay g; E = e^{g - g_ref} (g_ref = g[31]) in place;
-    // the Gram B operand [C ; K] from the same registers
+    // the Gram B operand [C ; K] from the same registers.  Thread: channels 2cp, 2cp+1 of
+    // rows 4 seg .. 4 seg + 3 (16 row segments; their totals are scanned through TOT).
     auto phase1 = [&](int lc, int gbuf) {
-        const int ch = tid & 63, seg = tid >> 6;  // rows 8*seg .. 8*seg+7
-        float g[8];
-        float acc = 0.f;
+        const int ch = 2 * (tid & 31), seg = tid >> 5;
+        float2 g[4];
+        float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int t = 8 * seg + u;
-            acc += (t < lc) ? E[t * 64 + ch] : 0.f;  // the w tile, row-major as loaded
+        for (int u = 0; u < 4; ++u) {
+            const int t = 4 * seg + u;
+            if (t < lc) {  // the w tile, row-major as loaded
+                const float2 wv = *reinterpret_cast<const float2 *>(E + t * 64 + ch);
+                acc.x += wv.x;
+                acc.y += wv.y;
+            }
             g[u] = acc;
         }
-        TOT[seg * 64 + ch] = acc;
+        *reinterpret_cast<float2 *>(TOT + seg * 64 + ch) = acc;
         wsync();
-        float pre = 0.f;
+        float2 pre = make_float2(0.f, 0.f);
+        for (int u = 0; u < seg; ++u) {
+            const float2 tv = *reinterpret_cast<const float2 *>(TOT + u * 64 + ch);
+            pre.x += tv.x;
+            pre.y += tv.y;
+        }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) pre += (u < seg) ? TOT[u * 64 + ch] : 0.f;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) g[u] += pre;
-        if (seg == 3) GREF[ch] = g[7];
+        for (int u = 0; u < 4; ++u) {
+            g[u].x += pre.x;
+            g[u].y += pre.y;
+        }
+        if (seg == 7) *reinterpret_cast<float2 *>(GREF + ch) = g[3];  // row 31
         wsync();
-        const float gr = GREF[ch];
+        const float2 gr = *reinterpret_cast<const float2 *>(GREF + ch);
         unsigned char *BG = sm + SM_BG;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int t = 8 * seg + u;
-            E[eidx(t, ch)] = __expf(g[u] - gr);
+        for (int u = 0; u < 4; ++u) {
+            const int t = 4 * seg + u;
+            *reinterpret_cast<float2 *>(E + eidx(t, ch)) = make_float2(__expf(g[u].x - gr.x), __expf(g[u].y - gr.y));
             // B_G = [C ; K]: C[s][i] = kk a e^{g_ref - g_s}, K[s][i] = k e^{g_ref - g_s} (rows s = t, 64 + t)
-            const float ei = t < lc ? __expf(gr - g[u]) : 0.f;
-            *reinterpret_cast<uint32_t *>(BG + sw128_off(t, ch, 128)) =
-                to_tf32(raw1(rkk, t, ch) * raw1(ra, t, ch) * ei);
-            *reinterpret_cast<uint32_t *>(BG + sw128_off(64 + t, ch, 128)) = to_tf32(raw1(rk, t, ch) * ei);
+            const bool valid = t < lc;
+            const float ex = valid ? __expf(gr.x - g[u].x) : 0.f, ey = valid ? __expf(gr.y - g[u].y) : 0.f;
+            const float2 kkv = raw2(rkk, t, ch), av = raw2(ra, t, ch), kv = raw2(rk, t, ch);
+            *reinterpret_cast<uint2 *>(BG + sw128_off(t, ch, 128)) =
+                make_uint2(to_tf32(kkv.x * av.x * ex), to_tf32(kkv.y * av.y * ey));
+            *reinterpret_cast<uint2 *>(BG + sw128_off(64 + t, ch, 128)) = make_uint2(to_tf32(kv.x * ex), to_tf32(kv.y * ey));
         }
-        if (seg == 0) EREF[gbuf * 64 + ch] = __expf(gr);
-        if (seg == 7) {
-            E63[gbuf * 64 + ch] = __expf(g[7] - gr);
-            GC[gbuf * 64 + ch] = __expf(g[7]);
+        if (seg == 0) *reinterpret_cast<float2 *>(EREF + gbuf * 64 + ch) = make_float2(__expf(gr.x), __expf(gr.y));
+        if (seg == 15) {  // row 63
+            *reinterpret_cast<float2 *>(E63 + gbuf * 64 + ch) = make_float2(__expf(g[3].x - gr.x), __expf(g[3].y - gr.y));
+            *reinterpret_cast<float2 *>(GC + gbuf * 64 + ch) = make_float2(__expf(g[3].x), __expf(g[3].y));
         }
     };
 
@@ -349,15 +364,23 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
     };
 
     // V^T into B_chain (K 64..127)
+    // Thread: columns j, j+1 (j even) of tokens s0 .. s0+3.  Half the lanes store row j first,
+    // half row j+1, so each quarter-warp's 16-byte stores land in 8 distinct bank groups.
     auto write_vt = [&](int lc) {
+        const int j = 2 * (tid & 31), s0 = 4 * (tid >> 5);
+        float a0[4], a1[4];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int task = tid + kThreads * u;
-            const int j = task & 63, s0 = 4 * (task >> 6);
-            float vv[4];
+        for (int e = 0; e < 4; ++e) {
+            const float2 x = s0 + e < lc ? raw2(rv, s0 + e, j) : make_float2(0.f, 0.f);
+            a0[e] = x.x;
+            a1[e] = x.y;
+        }
+        const bool odd_first = (tid >> 2) & 1;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) vv[e] = (s0 + e < lc) ? raw1(rv, s0 + e, j) : 0.f;
-            st_tf32x4(sm + SM_BC + sw128_off(j, 64 + s0, 64), vv[0], vv[1], vv[2], vv[3]);
+        for (int h = 0; h < 2; ++h) {
+            const bool odd = (h == 0) == odd_first;
+            st_tf32x4(sm + SM_BC + sw128_off(j + (odd ? 1 : 0), 64 + s0, 64), odd ? a1[0] : a0[0], odd ? a1[1] : a0[1],
+                      odd ? a1[2] : a0[2], odd ? a1[3] : a0[3]);
         }
     };
 
@@ -548,17 +571,27 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
                     if (t >= j) TS[(o + t) * kLd + o + j] = x[t];
             } else {
                 // the other warps meanwhile: Qa^T into B_Y rows 0..63, Qa[t][i] = kk e^{g_{t-1}}
-                for (int task = tid - 64; task < 1024; task += kThreads - 64) {
-                    const int i = task & 63, tb = 4 * (task >> 6);
-                    const float er = erc[i];
-                    float x[4];
+                // (task: channels i, i+1 of tokens tb .. tb+3; row order alternated as in write_vt)
+                for (int task = tid - 64; task < 512; task += kThreads - 64) {
+                    const int i = 2 * (task & 31), tb = 4 * (task >> 5);
+                    const float2 er = *reinterpret_cast<const float2 *>(erc + i);
+                    float x0[4], x1[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int t = tb + e;
-                        const float f = (t == 0) ? 1.f : E[eidx(t - 1, i)] * er;
-                        x[e] = (t < lc) ? raw1(rkk, t, i) * f : 0.f;
+                        const float2 f = t == 0 ? make_float2(1.f, 1.f)
+                                                : *reinterpret_cast<const float2 *>(E + eidx(t - 1, i));
+                        const float2 kv = t < lc ? raw2(rkk, t, i) : make_float2(0.f, 0.f);
+                        x0[e] = t == 0 ? kv.x : kv.x * f.x * er.x;
+                        x1[e] = t == 0 ? kv.y : kv.y * f.y * er.y;
                     }
-                    st_tf32x4(sm + SM_BY + sw128_off(i, tb, 128), x[0], x[1], x[2], x[3]);
+                    const bool odd_first = (task >> 2) & 1;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const bool odd = (h == 0) == odd_first;
+                        st_tf32x4(sm + SM_BY + sw128_off(i + (odd ? 1 : 0), tb, 128), odd ? x1[0] : x0[0],
+                                  odd ? x1[1] : x0[1], odd ? x1[2] : x0[2], odd ? x1[3] : x0[3]);
+                    }
                 }
             }
             wsync();
