@@ -512,37 +512,34 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
 
         // ---- phase 3: read G.  M_c (masked) -> A_chain columns 0..63 of rows t, which with
         // the transposing product's Cb^T below them form A_X = [M_c ; Cb^T]; M_k (masked) ->
-        // A_chain rows t, K 64..; L_c -> LC; L_k^T -> B_Y.
-        {
+        // A_chain rows t, K 64..; L_c -> LC; L_k^T -> B_Y (16 + 16 columns per lower-lane warp).
+        if (q < 2) {
             uint32_t wds[32];
-            const int gcol = (cg < 2 ? 0 : 64) + 32 * (cg & 1);  // M_c | M_k (q<2), L_c | L_k (q>=2)
+            const int gcol = (cg < 2 ? 0 : 64) + 32 * (cg & 1);  // M_c | M_k
             const int s0 = 32 * (cg & 1);
+            const int t = m;
             float v[32];
             tmem_ld32(tmem + lane_off + kColG + gcol, v);
-            if (q < 2) {
-                const int t = m;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) wds[j] = to_tf32(s0 + j <= t ? v[j] : 0.f);
-                tmem_st32_issue(tmem + lane_off + kColAC + gcol, wds);
-            } else {
-                const int t = m - 64;
-                if (cg < 2) {
-                    float *LC = reinterpret_cast<float *>(sm + SM_LC);
-#pragma unroll
-                    for (int j = 0; j < 32; j += 4)
-                        *reinterpret_cast<float4 *>(LC + t * kLd + s0 + j) =
-                            make_float4(s0 + j < t ? v[j] : 0.f, s0 + j + 1 < t ? v[j + 1] : 0.f,
-                                        s0 + j + 2 < t ? v[j + 2] : 0.f, s0 + j + 3 < t ? v[j + 3] : 0.f);
-                } else {
-                    unsigned char *BY = sm + SM_BY;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        *reinterpret_cast<uint32_t *>(BY + sw128_off(64 + s0 + j, t, 128)) =
-                            to_tf32(s0 + j < t ? v[j] : 0.f);
-                }
-            }
+            for (int j = 0; j < 32; ++j) wds[j] = to_tf32(s0 + j <= t ? v[j] : 0.f);
+            tmem_st32_issue(tmem + lane_off + kColAC + gcol, wds);
             tmem_wait_st();
             if (tid == 0) bulk_wait_read<0>();  // the previous chunk's O stores have read T's scratch
+        } else {
+            const int t = m - 64, s0 = 16 * cg;
+            float v[16];
+            tmem_ld16(tmem + lane_off + kColG + s0, v);
+            float *LCw = reinterpret_cast<float *>(sm + SM_LC);
+#pragma unroll
+            for (int j = 0; j < 16; j += 4)
+                *reinterpret_cast<float4 *>(LCw + t * kLd + s0 + j) =
+                    make_float4(s0 + j < t ? v[j] : 0.f, s0 + j + 1 < t ? v[j + 1] : 0.f,
+                                s0 + j + 2 < t ? v[j + 2] : 0.f, s0 + j + 3 < t ? v[j + 3] : 0.f);
+            tmem_ld16(tmem + lane_off + kColG + 64 + s0, v);
+            unsigned char *BY = sm + SM_BY;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                *reinterpret_cast<uint32_t *>(BY + sw128_off(64 + s0 + j, t, 128)) = to_tf32(s0 + j < t ? v[j] : 0.f);
         }
         sync_for_mma();
 
