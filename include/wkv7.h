@@ -57,7 +57,7 @@ typedef enum {
     WKV7_ERR_ALIGNMENT = 3,    /* a tensor pointer is not 16-byte aligned */
     WKV7_ERR_CUDA = 4,         /* a CUDA runtime/launch error (see wkv7_last_cuda_error) */
     WKV7_ERR_TIMEOUT = 5,      /* a bounded device-side wait expired (device status) */
-    WKV7_ERR_WORKSPACE = 6,    /* workspace missing or smaller than wkv7_prefill_workspace_size */
+    WKV7_ERR_WORKSPACE = 6,    /* workspace missing or too small to hold the sequence order */
     WKV7_ERR_DEVICE_BOUNDS = 7 /* the device found an index out of range (device status) */
 } wkv7_status;
 
@@ -88,8 +88,23 @@ WKV7_API wkv7_status wkv7_step(int B, int H, int N,
                       float *state, float *o, cudaStream_t stream);
 
 /*
- * wkv7_prefill_workspace_size -- bytes of device workspace wkv7_prefill
- * needs for this shape (may be 0; the result depends only on the arguments).
+ * wkv7_prefill_workspace_size -- bytes of device workspace with which
+ * wkv7_prefill can use every schedule for this shape (may be 0; the result
+ * depends only on the arguments).  It holds:
+ *   - the longest-first order of the sequences, 4 bytes per sequence rounded
+ *     up to 256, for 2 <= num_seqs <= 4096 (required: a smaller workspace
+ *     returns WKV7_ERR_WORKSPACE);
+ *   - for T_total >= 1024, scratch for the tail split (optional): 256 state
+ *     slots of 16 KB, then 256 bytes per token-head for up to
+ *     min(T_total * H, 2^20) token-heads.  When the (sequence, head)
+ *     pairs do not fill the last wave of CTAs (P mod SMs <= SMs / 3), the
+ *     pairs of that wave are cut into chunk-aligned segments that run
+ *     concurrently; a segment after the first runs from a zero state and once
+ *     more from the identity state with v = 0, and two small kernels chain
+ *     the true boundary states and add the carried-in state's contribution
+ *     to the outputs (exact up to rounding: the recurrence is linear in the
+ *     state).  This needs cu_seqlens_host; with less scratch than a plan
+ *     needs, or without the host copy, every pair runs whole.
  */
 WKV7_API size_t wkv7_prefill_workspace_size(int num_seqs, int T_total, int H, int N);
 
@@ -109,9 +124,10 @@ WKV7_API size_t wkv7_prefill_workspace_size(int num_seqs, int T_total, int H, in
  *                     Zero-length sequences are allowed.
  *   cu_seqlens_host : optional HOST copy of the same array (NULL allowed).
  *                     When given it is validated on the host and used to
- *                     schedule long sequences first; it must equal the device
- *                     array.  When NULL the device validates cu_seqlens and a
- *                     malformed array is reported by wkv7_check_device_status.
+ *                     schedule long sequences first and to plan the tail
+ *                     split; it must equal the device array.  When NULL the
+ *                     device validates cu_seqlens and a malformed array is
+ *                     reported by wkv7_check_device_status.
  *   x_dtype         : WKV7_F32 or WKV7_BF16, the type of r, k, v, kk, a
  *   r, k, v, kk, a  : x_dtype [T_total, H, N]  (token-major)
  *   w               : fp32 [T_total, H, N]     log-decay
@@ -120,14 +136,18 @@ WKV7_API size_t wkv7_prefill_workspace_size(int num_seqs, int T_total, int H, in
  *                     the same pointer as initial_state (in-place carry), but
  *                     must not partially overlap it
  *   o               : fp32 [T_total, H, N]     outputs of every token
- *   workspace       : device memory of at least
- *                     wkv7_prefill_workspace_size(...) bytes (may be NULL when
- *                     that size is 0); its contents need not be initialised
- *                     and are not preserved.  Calls that overlap on the GPU
- *                     must use distinct workspaces.
+ *   workspace       : device memory, 16-byte aligned, of workspace_bytes
+ *                     bytes: wkv7_prefill_workspace_size(...) for every
+ *                     schedule, at least its sequence-order part (may be NULL
+ *                     when that part is 0).  Its contents need not be
+ *                     initialised and are not preserved; it must not overlap
+ *                     any other argument.  Calls that overlap on the GPU must
+ *                     use distinct workspaces.
  *
  * Precondition for the chunked formulation: w >= -2.5 elementwise (every
- * RWKV-7 model has w in (-0.6066, 0)); see the design notes.
+ * RWKV-7 model has w in (-0.6066, 0)).  The chunked kernel takes a chunk's
+ * decay factors relative to its 32nd token, so for such w every factor lies
+ * within e^{+-80}, finite in fp32.
  */
 WKV7_API wkv7_status wkv7_prefill(int num_seqs, int T_total, int H, int N,
                          const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,

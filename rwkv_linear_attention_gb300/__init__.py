@@ -82,7 +82,10 @@ def prefill(r, w, k, v, kk, a, cu_seqlens, initial_state=None, final_state=None,
     ``final_state``: output buffer (may be ``initial_state`` for an in-place
     carry); allocated when None and ``want_final_state``.
     ``cu_seqlens_host``: optional CPU int32 copy (validated on the host, used
-    for scheduling).  Returns ``(o, final_state)``.
+    for scheduling).  ``workspace``: uint8 CUDA buffer; ``prefill_workspace_size``
+    bytes enable every schedule, and a smaller one is accepted as long as it
+    holds the sequence order (the tail split is then skipped); allocated when
+    None.  Returns ``(o, final_state)``.
     """
     T_total, H, N = r.shape
     xdt = r.dtype

@@ -155,12 +155,19 @@ wkv7_status wkv7_prefill(int num_seqs, int T_total, int H, int N, const int32_t 
         overlaps(final_state, state_bytes, cu_seqlens, (size_t)(num_seqs + 1) * 4))
         return WKV7_ERR_INVALID_ARG;
 
-    const size_t need = wkv7::prefill_workspace_bytes(num_seqs, T_total, H);
+    // Only the sequence order is required; a larger workspace (up to
+    // wkv7_prefill_workspace_size) also enables the tail-split schedule.
+    const size_t need = wkv7::prefill_workspace_min_bytes(num_seqs);
     if (need > 0 && (!workspace || workspace_bytes < need)) return WKV7_ERR_WORKSPACE;
-    if (workspace && need > 0) {
+    if (!workspace) workspace_bytes = 0;
+    if (workspace_bytes > 0) {
         if (!aligned16(workspace)) return WKV7_ERR_ALIGNMENT;
-        if (overlaps(workspace, need, o, o_bytes) || overlaps(workspace, need, final_state, state_bytes))
-            return WKV7_ERR_INVALID_ARG;
+        const void *others[9] = {o, final_state, initial_state, r, w, k, v, kk, a};
+        const size_t sizes[9] = {o_bytes, state_bytes, state_bytes, tok_elems * x_elem, tok_elems * 4,
+                                 tok_elems * x_elem, tok_elems * x_elem, tok_elems * x_elem, tok_elems * x_elem};
+        for (int i = 0; i < 9; ++i)
+            if (overlaps(workspace, workspace_bytes, others[i], sizes[i])) return WKV7_ERR_INVALID_ARG;
+        if (overlaps(workspace, workspace_bytes, cu_seqlens, (size_t)(num_seqs + 1) * 4)) return WKV7_ERR_INVALID_ARG;
     }
 
     unsigned *status = nullptr;
@@ -173,6 +180,7 @@ wkv7_status wkv7_prefill(int num_seqs, int T_total, int H, int N, const int32_t 
     args.H = H;
     args.cu_seqlens = cu_seqlens;
     args.order = nullptr;
+    args.cu_seqlens_host = cu_seqlens_host;
     args.x_dtype = x_dtype;
     args.r = r; args.w = w; args.k = k; args.v = v; args.kk = kk; args.a = a;
     args.initial_state = initial_state;

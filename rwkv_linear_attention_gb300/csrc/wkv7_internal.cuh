@@ -34,6 +34,7 @@ struct PrefillArgs {
     int H;
     const int32_t *cu_seqlens;   // device [num_seqs + 1]
     const int32_t *order;        // device [num_seqs] schedule (longest first) or nullptr
+    const int32_t *cu_seqlens_host;  // host copy of cu_seqlens or nullptr (scheduling only)
     wkv7_dtype x_dtype;
     const void *r;
     const float *w;
@@ -53,7 +54,8 @@ cudaError_t launch_prefill_scan(const PrefillArgs &args, cudaStream_t stream);
 // Prefill: the chunked tensor-core kernel.
 cudaError_t launch_prefill(const PrefillArgs &args, void *workspace, size_t workspace_bytes,
                            cudaStream_t stream);
-size_t prefill_workspace_bytes(int num_seqs, int T_total, int H);
+size_t prefill_workspace_bytes(int num_seqs, int T_total, int H);  // for the fastest schedule
+size_t prefill_workspace_min_bytes(int num_seqs);                 // required (the sequence order)
 // Whether this batch is worth a longest-first schedule, and the kernel that
 // writes it (order[rank] = sequence index) into device memory.
 bool prefill_wants_order(const PrefillArgs &args, const int32_t *cu_seqlens_host);

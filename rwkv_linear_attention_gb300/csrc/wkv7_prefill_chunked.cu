@@ -56,6 +56,10 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <algorithm>
+#include <numeric>
+#include <vector>
+
 #include "sm103_ptx.cuh"
 #include "wkv7_internal.cuh"
 
@@ -142,7 +146,56 @@ __device__ __forceinline__ int eidx(int t, int i) { return t * 64 + ((((i >> 2) 
 
 struct TensorMaps {
     CUtensorMap r, k, v, kk, a, w;
-    CUtensorMap o;  // fp32 output, 64 x 32 boxes in the 128-byte swizzle layout (stores)
+    CUtensorMap o;     // fp32 output, 64 x 32 boxes in the 128-byte swizzle layout (stores)
+    CUtensorMap ohat;  // fp32 [rows, 64] carry-in readout of transfer items, same boxes
+};
+
+// ---- Tail split.  A CTA runs one work item.  Items 0 .. main_items-1 are whole
+// (sequence, head) pairs in schedule order (blockIdx = rank * H + h).  The pairs
+// that would run alone in a last, mostly idle wave of CTAs are instead cut into
+// k chunk-aligned segments, each running concurrently on its own SM.  The
+// recurrence is linear in the state: over a segment, S_end = P S_in + S_part with
+// P the product of the per-token transitions diag(e^w) - (kk*a) kk^T, and
+// o_t = o_part_t + S_in^T (P_t^T r_t).  So for segment j >= 1 of a split pair
+// two items run, one from S = 0 (o_part into o, S_part into a slot) and one from
+// S = I with v = 0 (P_t^T r_t into a scratch row, P into a slot); segment 0
+// runs from the true initial state.  Two small kernels then chain the true
+// boundary states (S_in(j+1) = P(j) S_in(j) + S_part(j)) and add S_in(j)^T
+// P_t^T r_t to the outputs of segment j.
+enum : int16_t { kItemWhole = 0, kItemPart = 1, kItemTransfer = 2 };
+struct SplitItem {
+    int32_t pair;       // b * H + h
+    int16_t c0, c1;     // chunk range [c0, c1) of the pair
+    int16_t kind;       // kItemWhole (segment 0 too), kItemPart, kItemTransfer
+    int16_t slot;       // state slot for the final state (-1: the caller's final_state)
+    int32_t ohat_row;   // first scratch row of a transfer item's readout
+};
+constexpr int kMaxSplitItems = 256;
+constexpr int kMaxSplitPairs = 48;
+constexpr int kMaxSegs = 16;
+struct SplitPlan {
+    int main_items;
+    int n_items;
+    float *slots;   // kMaxSplitItems x 4096 fp32 states
+    float *ohat;    // scratch rows x 64 fp32
+    SplitItem item[kMaxSplitItems];
+};
+struct FixSeg {
+    int16_t c0, c1;
+    int16_t slot_part, slot_transfer;  // slot_part of segment 0: its (true) final state
+    int32_t ohat_row;
+    int32_t blk0;  // first output-fix block of this segment
+};
+struct FixPair {
+    int32_t b, h, nseg;
+    FixSeg seg[kMaxSegs];
+};
+struct FixPlan {
+    int n_pairs;
+    int n_blocks;  // output-fix blocks (one per chunk of every segment j >= 1)
+    float *slots;
+    float *ohat;
+    FixPair pair[kMaxSplitPairs];
 };
 
 // Barriers among the 512 worker threads (the MMA warp never joins them).
@@ -173,7 +226,8 @@ __device__ __forceinline__ void handoff(uint32_t rdy) {
 }
 
 __global__ void __launch_bounds__(kBlock, 1)
-wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps maps) {
+wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps maps,
+                            const __grid_constant__ SplitPlan plan) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -184,9 +238,21 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
     const int m = 32 * q + lane;  // TMEM lane (row) this thread reads and writes
 
     const int H = p.H;
-    const int rank = static_cast<int>(blockIdx.x) / H;
-    const int h = static_cast<int>(blockIdx.x) % H;
-    const int b = p.order ? p.order[rank] : rank;
+    int b, h, c_begin = 0, c_end = -1, kind = kItemWhole, slot = -1, ohat_row = 0;
+    if (static_cast<int>(blockIdx.x) < plan.main_items) {
+        const int rank = static_cast<int>(blockIdx.x) / H;
+        h = static_cast<int>(blockIdx.x) % H;
+        b = p.order ? p.order[rank] : rank;
+    } else {
+        const SplitItem &it = plan.item[blockIdx.x - plan.main_items];
+        b = it.pair / H;
+        h = it.pair % H;
+        c_begin = it.c0;
+        c_end = it.c1;
+        kind = it.kind;
+        slot = it.slot;
+        ohat_row = it.ohat_row;
+    }
     if (b < 0 || b >= p.num_seqs) {
         if (tid == 0) report(p.status, kDevBounds);
         return;
@@ -197,7 +263,12 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
         return;
     }
     const int len = eos - bos;
-    const int nchunks = (len + kC - 1) / kC;
+    if (c_end < 0) c_end = (len + kC - 1) / kC;
+    if (c_begin < 0 || c_end < c_begin || (c_end > c_begin && (c_end - 1) * kC >= len)) {
+        if (tid == 0) report(p.status, kDevBadSeqlens);  // the schedule disagrees with the device lengths
+        return;
+    }
+    const int nchunks = c_end - c_begin;  // chunks of this item; loop indices below are relative to c_begin
     const long long tok_stride = static_cast<long long>(H) * 64;
 
     // State: rows i = m - 64 (lanes 64..127), columns 16*cg .. 16*cg+15.
@@ -206,7 +277,10 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
     float s[16];
     const long long sslot = (static_cast<long long>(b) * H + h) * 4096;
     if (state_thread) {
-        if (p.initial_state) {
+        if (kind == kItemTransfer) {  // S = I
+#pragma unroll
+            for (int j = 0; j < 16; ++j) s[j] = (16 * cg + j == si) ? 1.f : 0.f;
+        } else if (kind == kItemWhole && p.initial_state) {
             const float4 *src = reinterpret_cast<const float4 *>(p.initial_state + sslot + si * 64 + 16 * cg);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -268,7 +342,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm + SM_SLOT);
 
     auto issue_tma = [&](int chunk) {
-        const int y = bos + chunk * kC, x = h * 64;
+        const int y = bos + (c_begin + chunk) * kC, x = h * 64;
         mbar_arrive_expect_tx(bar_tma, kTmaBytes);
         tma_load_2d(sbase + SM_R, &maps.r, x, y, bar_tma);
         tma_load_2d(sbase + SM_K, &maps.k, x, y, bar_tma);
@@ -277,7 +351,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
         tma_load_2d(sbase + SM_V, &maps.v, x, y, bar_tma);
         tma_load_2d(sbase + SM_W, &maps.w, x, y, bar_tma);
     };
-    auto chunk_len = [&](int chunk) { return min(kC, eos - (bos + chunk * kC)); };
+    auto chunk_len = [&](int chunk) { return min(kC, eos - (bos + (c_begin + chunk) * kC)); };
 
     // ---- phase 1: masked cumulative log-decay g; E = e^{g - g_ref} (g_ref = g[31]) in place;
     // the Gram B operand [C ; K] from the same registers.  Thread: channels 2cp, 2cp+1 of
@@ -367,6 +441,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
     // Thread: columns j, j+1 (j even) of tokens s0 .. s0+3.  Half the lanes store row j first,
     // half row j+1, so each quarter-warp's 16-byte stores land in 8 distinct bank groups.
     auto write_vt = [&](int lc) {
+        if (kind == kItemTransfer) lc = 0;  // v = 0
         const int j = 2 * (tid & 31), s0 = 4 * (tid >> 5);
         float a0[4], a1[4];
 #pragma unroll
@@ -504,7 +579,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
     }
 
     for (int c = 0; c < nchunks && alive; ++c) {
-        const int t0 = bos + c * kC;
+        const int t0 = bos + (c_begin + c) * kC;
         const int lc = chunk_len(c);
         const bool has_next = c + 1 < nchunks;
         const uint32_t par = static_cast<uint32_t>(c & 1);
@@ -678,7 +753,9 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
                         *reinterpret_cast<float4 *>(box + (((4 * (cg & 1) + j) ^ (t & 7)) << 4)) =
                             make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
                 } else if (t < lc) {
-                    float4 *dst = reinterpret_cast<float4 *>(p.o + (t0 + t) * tok_stride + h * 64 + 16 * cg);
+                    float4 *dst = reinterpret_cast<float4 *>(
+                        kind == kItemTransfer ? plan.ohat + (static_cast<long long>(ohat_row) + c * kC + t) * 64 + 16 * cg
+                                              : p.o + (t0 + t) * tok_stride + h * 64 + 16 * cg);
 #pragma unroll
                     for (int j = 0; j < 4; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
                 }
@@ -694,8 +771,13 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
         }
         sync_for_mma();
         if (tid == 0 && lc == kC) {
-            tma_store_2d(&maps.o, h * 64, t0, sbase + SM_TS);
-            tma_store_2d(&maps.o, h * 64 + 32, t0, sbase + SM_TS + 8192);
+            if (kind == kItemTransfer) {
+                tma_store_2d(&maps.ohat, 0, ohat_row + c * kC, sbase + SM_TS);
+                tma_store_2d(&maps.ohat, 32, ohat_row + c * kC, sbase + SM_TS + 8192);
+            } else {
+                tma_store_2d(&maps.o, h * 64, t0, sbase + SM_TS);
+                tma_store_2d(&maps.o, h * 64 + 32, t0, sbase + SM_TS + 8192);
+            }
             bulk_commit();
         }
         if (has_next) {
@@ -704,8 +786,9 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
         }
     }
 
-    if (alive && state_thread && p.final_state) {
-        float4 *dst = reinterpret_cast<float4 *>(p.final_state + sslot + si * 64 + 16 * cg);
+    float *fdst = slot >= 0 ? plan.slots + static_cast<long long>(slot) * 4096 : p.final_state ? p.final_state + sslot : nullptr;
+    if (alive && state_thread && fdst) {
+        float4 *dst = reinterpret_cast<float4 *>(fdst + si * 64 + 16 * cg);
 #pragma unroll
         for (int j = 0; j < 4; ++j) dst[j] = make_float4(s[4 * j], s[4 * j + 1], s[4 * j + 2], s[4 * j + 3]);
     }
@@ -760,6 +843,103 @@ wkv7_prefill_order_kernel(const int32_t *__restrict__ cu, int num_seqs, int32_t 
     for (int i = threadIdx.x; i < num_seqs; i += kOrderThreads) order[i] = static_cast<int32_t>(key[i] & 0xffffffffu);
 }
 
+// ---------------------------------------------------------------- tail-split fix-up
+
+constexpr int kFixThreads = 256;
+
+// One CTA per split pair: the true state at every segment boundary, in order,
+// S_in(j+1) = P(j) S_in(j) + S_part(j), written over S_part(j)'s slot; the
+// last one is the pair's final state.
+__global__ void __launch_bounds__(kFixThreads)
+wkv7_prefill_split_chain_kernel(const __grid_constant__ FixPlan fp, float *final_state, int H) {
+    __shared__ float sin_[64 * 64];
+    const FixPair &pr = fp.pair[blockIdx.x];
+    const int tid = threadIdx.x, i = tid >> 2, c0 = 16 * (tid & 3);
+    const float *s0 = fp.slots + static_cast<long long>(pr.seg[0].slot_part) * 4096;
+    for (int e = tid; e < 4096; e += kFixThreads) sin_[e] = s0[e];
+    __syncthreads();
+    for (int j = 1; j < pr.nseg; ++j) {
+        const float *P = fp.slots + static_cast<long long>(pr.seg[j].slot_transfer) * 4096;
+        float *Sp = fp.slots + static_cast<long long>(pr.seg[j].slot_part) * 4096;
+        float acc[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) acc[x] = Sp[i * 64 + c0 + x];
+        for (int u = 0; u < 64; ++u) {
+            const float pv = P[i * 64 + u];
+#pragma unroll
+            for (int x = 0; x < 16; ++x) acc[x] = fmaf(pv, sin_[u * 64 + c0 + x], acc[x]);
+        }
+        __syncthreads();  // every thread has read S_in(j)
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+            sin_[i * 64 + c0 + x] = acc[x];
+            Sp[i * 64 + c0 + x] = acc[x];
+        }
+        __syncthreads();
+    }
+    if (final_state) {
+        float *dst = final_state + (static_cast<long long>(pr.b) * H + pr.h) * 4096;
+        for (int e = tid; e < 4096; e += kFixThreads) dst[e] = sin_[e];
+    }
+}
+
+// One CTA per chunk of every segment j >= 1: o_t += S_in(j)^T (P_t^T r_t).
+__global__ void __launch_bounds__(kFixThreads)
+wkv7_prefill_split_ofix_kernel(const __grid_constant__ FixPlan fp, PrefillArgs p) {
+    __shared__ float sin_[64 * 64];
+    __shared__ float oh[64 * 65];
+    const int blk = static_cast<int>(blockIdx.x);
+    int pi = -1, j = -1;
+    for (int a = 0; a < fp.n_pairs && pi < 0; ++a)
+        for (int g = 1; g < fp.pair[a].nseg; ++g) {
+            const FixSeg &sg = fp.pair[a].seg[g];
+            if (blk >= sg.blk0 && blk < sg.blk0 + (sg.c1 - sg.c0)) {
+                pi = a;
+                j = g;
+                break;
+            }
+        }
+    if (pi < 0) {
+        if (threadIdx.x == 0) report(p.status, kDevBounds);
+        return;
+    }
+    const FixPair &pr = fp.pair[pi];
+    const FixSeg &sg = pr.seg[j];
+    const int chunk = blk - sg.blk0;
+    const int tid = threadIdx.x;
+    const float *Sin = fp.slots + static_cast<long long>(pr.seg[j - 1].slot_part) * 4096;  // true S at the boundary
+    const float *orow = fp.ohat + (static_cast<long long>(sg.ohat_row) + chunk * 64) * 64;
+    for (int e = tid; e < 4096; e += kFixThreads) {
+        sin_[e] = Sin[e];
+        oh[(e >> 6) * 65 + (e & 63)] = orow[e];
+    }
+    __syncthreads();
+    const int bos = p.cu_seqlens[pr.b], eos = p.cu_seqlens[pr.b + 1];
+    const int t0 = bos + (sg.c0 + chunk) * 64;
+    const int lc = min(64, eos - t0);
+    const int t = tid >> 2, c0 = 16 * (tid & 3);
+    if (t < lc) {
+        float acc[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) acc[x] = 0.f;
+        for (int i = 0; i < 64; ++i) {
+            const float hv = oh[t * 65 + i];
+#pragma unroll
+            for (int x = 0; x < 16; ++x) acc[x] = fmaf(hv, sin_[i * 64 + c0 + x], acc[x]);
+        }
+        float4 *dst = reinterpret_cast<float4 *>(p.o + (static_cast<long long>(t0) + t) * p.H * 64 + pr.h * 64 + c0);
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            float4 v = dst[x];
+            v.x += acc[4 * x];
+            v.y += acc[4 * x + 1];
+            v.z += acc[4 * x + 2];
+            v.w += acc[4 * x + 3];
+            dst[x] = v;
+        }
+    }
+}
+
 // ---------------------------------------------------------------- host side
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -811,7 +991,114 @@ bool make_out_map(CUtensorMap *map, void *base, int T_total, int H) {
            CUDA_SUCCESS;
 }
 
-cudaError_t launch_chunked(const PrefillArgs &args, cudaStream_t stream) {
+// fp32 [rows, 64] scratch of the transfer items' readouts, same boxes as the output.
+bool make_ohat_map(CUtensorMap *map, float *base, long long rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {64, static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {64 * 4};
+    cuuint32_t box[2] = {32, 64};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+constexpr size_t kSlotsBytes = static_cast<size_t>(kMaxSplitItems) * 4096 * sizeof(float);
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+// The tail-split schedule (see SplitItem).  With P pairs on S SMs (one CTA per SM),
+// the last r = P mod S pairs in schedule order (the shortest) would run alone in a
+// last wave; when r <= S/3 each is cut into k segments (2k - 1 items, all running
+// concurrently) with k as large as the SMs, kMaxSegs and the scratch allow.  Needs
+// the host copy of cu_seqlens; returns false (whole pairs only) otherwise.
+bool plan_split(const PrefillArgs &a, unsigned char *split_ws, size_t split_bytes, SplitPlan &plan, FixPlan &fix) {
+    const long long P = static_cast<long long>(a.num_seqs) * a.H;
+    plan.main_items = static_cast<int>(P);
+    plan.n_items = 0;
+    plan.slots = plan.ohat = nullptr;
+    fix.n_pairs = fix.n_blocks = 0;
+    if (!a.cu_seqlens_host || !split_ws || split_bytes < kSlotsBytes + 64 * 256) return false;
+    const long long rows_cap = static_cast<long long>((split_bytes - kSlotsBytes) / 256) & ~63ll;
+    const int S = sm_count();
+    if (S <= 0) return false;
+    const long long r = P % S;
+    if (r == 0 || 3 * r > S || r > kMaxSplitPairs) return false;
+    auto len = [&](int b) { return a.cu_seqlens_host[b + 1] - a.cu_seqlens_host[b]; };
+    // the schedule's sequence order: the device order kernel's (descending length, ties by index)
+    std::vector<int> ord(a.num_seqs);
+    std::iota(ord.begin(), ord.end(), 0);
+    if (a.order) std::stable_sort(ord.begin(), ord.end(), [&](int x, int y) { return len(x) > len(y); });
+    struct Tail { int b, h, n; };
+    std::vector<Tail> tail;
+    for (long long bi = P - r; bi < P; ++bi) {
+        const int b = ord[bi / a.H];
+        tail.push_back({b, static_cast<int>(bi % a.H), (len(b) + kC - 1) / kC});
+    }
+    auto segs = [&](const Tail &t, int k) { return t.n > 32767 ? 1 : std::min(k, t.n / 2); };
+    for (int k = static_cast<int>(std::min<long long>(kMaxSegs, (S / r + 1) / 2)); k >= 2; --k) {
+        long long items = 0, rows = 0, nsplit = 0;
+        for (const Tail &t : tail) {
+            const int kp = segs(t, k);
+            if (kp < 2) {
+                items += 1;
+                continue;
+            }
+            items += 2 * kp - 1;
+            ++nsplit;
+            rows += static_cast<long long>(t.n - t.n / kp) * 64;
+        }
+        if (nsplit == 0 || items > kMaxSplitItems || items > S || rows > rows_cap) continue;
+        plan.main_items = static_cast<int>(P - r);
+        plan.slots = fix.slots = reinterpret_cast<float *>(split_ws);
+        plan.ohat = fix.ohat = reinterpret_cast<float *>(split_ws + kSlotsBytes);
+        int n = 0, slot = 0, blk = 0;
+        long long row = 0;
+        for (const Tail &t : tail) {
+            const int pair = t.b * a.H + t.h, kp = segs(t, k);
+            if (kp < 2) {
+                plan.item[n++] = {pair, 0, static_cast<int16_t>(t.n), kItemWhole, -1, 0};
+                continue;
+            }
+            FixPair &fp = fix.pair[fix.n_pairs++];
+            fp.b = t.b;
+            fp.h = t.h;
+            fp.nseg = kp;
+            for (int j = 0; j < kp; ++j) {
+                const int16_t c0 = static_cast<int16_t>(j * t.n / kp), c1 = static_cast<int16_t>((j + 1) * t.n / kp);
+                FixSeg &sg = fp.seg[j];
+                sg.c0 = c0;
+                sg.c1 = c1;
+                sg.slot_part = static_cast<int16_t>(slot);
+                plan.item[n++] = {pair, c0, c1, j == 0 ? kItemWhole : kItemPart, static_cast<int16_t>(slot++), 0};
+                if (j == 0) {
+                    sg.slot_transfer = -1;
+                    sg.ohat_row = 0;
+                    sg.blk0 = 0;
+                    continue;
+                }
+                sg.slot_transfer = static_cast<int16_t>(slot);
+                sg.ohat_row = static_cast<int32_t>(row);
+                sg.blk0 = blk;
+                plan.item[n++] = {pair, c0, c1, kItemTransfer, static_cast<int16_t>(slot++), static_cast<int32_t>(row)};
+                row += static_cast<long long>(c1 - c0) * 64;
+                blk += c1 - c0;
+            }
+        }
+        plan.n_items = n;
+        fix.n_blocks = blk;
+        return true;
+    }
+    return false;
+}
+
+cudaError_t launch_chunked(const PrefillArgs &args, unsigned char *split_ws, size_t split_bytes, cudaStream_t stream) {
     TensorMaps maps;
     if (!make_map(&maps.r, args.r, true, args.T_total, args.H) ||
         !make_map(&maps.k, args.k, true, args.T_total, args.H) ||
@@ -819,6 +1106,11 @@ cudaError_t launch_chunked(const PrefillArgs &args, cudaStream_t stream) {
         !make_map(&maps.kk, args.kk, true, args.T_total, args.H) ||
         !make_map(&maps.a, args.a, true, args.T_total, args.H) ||
         !make_map(&maps.w, args.w, false, args.T_total, args.H) || !make_out_map(&maps.o, args.o, args.T_total, args.H))
+        return cudaErrorInvalidValue;
+    SplitPlan plan;
+    FixPlan fix;
+    const bool split = plan_split(args, split_ws, split_bytes, plan, fix);
+    if (split && !make_ohat_map(&maps.ohat, plan.ohat, static_cast<long long>((split_bytes - kSlotsBytes) / 256) & ~63ll))
         return cudaErrorInvalidValue;
     static int attr_dev = -1;
     int dev = 0;
@@ -830,18 +1122,35 @@ cudaError_t launch_chunked(const PrefillArgs &args, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         attr_dev = dev;
     }
-    const long long pairs = static_cast<long long>(args.num_seqs) * args.H;
-    wkv7_prefill_chunked_kernel<<<static_cast<unsigned>(pairs), kBlock, kSmemAlloc, stream>>>(args, maps);
+    wkv7_prefill_chunked_kernel<<<static_cast<unsigned>(plan.main_items + plan.n_items), kBlock, kSmemAlloc, stream>>>(
+        args, maps, plan);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || !split) return e;
+    wkv7_prefill_split_chain_kernel<<<fix.n_pairs, kFixThreads, 0, stream>>>(fix, args.final_state, args.H);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    wkv7_prefill_split_ofix_kernel<<<fix.n_blocks, kFixThreads, 0, stream>>>(fix, args);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-// Workspace: the longest-first order of the sequences (int32 per sequence),
-// for batches of 2 .. kMaxOrdered sequences.
-size_t prefill_workspace_bytes(int num_seqs, int, int) {
+// Workspace: [the longest-first order of the sequences (int32 per sequence, for
+// batches of 2 .. kMaxOrdered sequences) | tail-split scratch: kMaxSplitItems
+// state slots, then readout rows of 64 fp32 for up to min(T_total*H, 2^20)
+// token-heads (none below 1024 tokens)].  Only the order part is required.
+size_t prefill_workspace_min_bytes(int num_seqs) {
     if (num_seqs < 2 || num_seqs > kMaxOrdered) return 0;
     return (static_cast<size_t>(num_seqs) * sizeof(int32_t) + 255) & ~static_cast<size_t>(255);
+}
+
+size_t prefill_workspace_bytes(int num_seqs, int T_total, int H) {
+    size_t bytes = prefill_workspace_min_bytes(num_seqs);
+    if (T_total >= 1024 && num_seqs >= 1) {
+        const long long rows = std::min<long long>(static_cast<long long>(T_total) * H, 1ll << 20) & ~63ll;
+        bytes += kSlotsBytes + static_cast<size_t>(rows) * 256;
+    }
+    return bytes;
 }
 
 bool prefill_wants_order(const PrefillArgs &args, const int32_t *cu_seqlens_host) {
@@ -858,7 +1167,7 @@ cudaError_t launch_prefill_order(const int32_t *cu_seqlens, int num_seqs, int32_
     return cudaGetLastError();
 }
 
-cudaError_t launch_prefill(const PrefillArgs &args, void *, size_t, cudaStream_t stream) {
+cudaError_t launch_prefill(const PrefillArgs &args, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
     const long long pairs = static_cast<long long>(args.num_seqs) * args.H;
     if (pairs <= 0) return cudaSuccess;
     const size_t state_bytes = static_cast<size_t>(pairs) * 4096 * sizeof(float);
@@ -870,7 +1179,11 @@ cudaError_t launch_prefill(const PrefillArgs &args, void *, size_t, cudaStream_t
     }
     // bf16 inputs (the prefill format) take the chunked tensor-core kernel;
     // fp32 inputs take the exact token-serial kernel.
-    if (args.x_dtype == WKV7_BF16) return launch_chunked(args, stream);
+    if (args.x_dtype == WKV7_BF16) {
+        const size_t head = prefill_workspace_min_bytes(args.num_seqs);
+        unsigned char *split_ws = workspace && workspace_bytes > head ? static_cast<unsigned char *>(workspace) + head : nullptr;
+        return launch_chunked(args, split_ws, split_ws ? workspace_bytes - head : 0, stream);
+    }
     return launch_prefill_scan(args, stream);
 }
 

@@ -54,7 +54,7 @@ extern "C" wkv7_status wkv7_prefill_noalloc(int num_seqs, int T_total, int H, in
                                             const float *initial_state, float *final_state, float *o,
                                             cudaStream_t stream) {
     if (num_seqs > WKV7_NOALLOC_MAX_SEQS) return WKV7_ERR_WORKSPACE;
-    const size_t need = wkv7_prefill_workspace_size(num_seqs, T_total, H, N);
+    const size_t need = N == wkv7::kN ? wkv7::prefill_workspace_min_bytes(num_seqs) : 0;
     if (need > sizeof(g_prefill_noalloc_scratch)) return WKV7_ERR_WORKSPACE;
     void *scratch = nullptr;
     if (need > 0) {

@@ -163,6 +163,63 @@ def test_prefill_7p2b_single_32768(dev):
         _check(p, o, sf, s0=s0, heads=range(h0, h0 + 32))
 
 
+# Tail split: with P (sequence, head) pairs on S SMs, the last r = P mod S pairs are
+# cut into segments when 0 < r <= S/3 (and r <= 48).  These shapes split on a GB300
+# (S = 152): one ragged sequence of 8 heads (10 segments per pair) and three unequal
+# sequences of 10 heads (the schedule's longest-first order, 3 segments).
+SPLIT_CASES = [([3000], 8, 21), ([2000, 1500, 700], 10, 22)]
+SPLIT_IDS = ["1x3000-H8", "unequal-H10"]
+
+
+def _expect_split(num_seqs, H):
+    S = torch.cuda.get_device_properties(0).multi_processor_count
+    r = (num_seqs * H) % S
+    return 0 < r and 3 * r <= S and r <= 48
+
+
+@pytest.mark.parametrize("lens,H,seed", SPLIT_CASES, ids=SPLIT_IDS)
+def test_tail_split_against_oracle(dev, lens, H, seed):
+    p = inputs.prefill_inputs(lens, H, 64, seed=seed, device=dev)
+    s0 = inputs.initial_state(len(lens), H, 64, seed=seed, device=dev)
+    cu = p["cu_seqlens"]
+    need = wkv7.prefill_workspace_size(len(lens), cu[-1].item(), H)
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device=dev)
+    o, sf = wkv7.prefill(p["r"], p["w"], p["k"], p["v"], p["kk"], p["a"], cu.to(dev), initial_state=s0,
+                         cu_seqlens_host=cu, workspace=ws)
+    wkv7.check_device_status()
+    _check(p, o, sf, s0=s0)
+    # the split scratch (after the 256-byte-rounded sequence order) holds boundary states iff it ran
+    head = 0 if len(lens) < 2 else 256
+    touched = bool((ws[head:head + 16384] != 0xFF).any())
+    assert touched == _expect_split(len(lens), H)
+
+
+@pytest.mark.parametrize("lens,H,seed", SPLIT_CASES, ids=SPLIT_IDS)
+def test_tail_split_matches_whole_pairs(dev, lens, H, seed):
+    """The same batch with a workspace that only holds the sequence order, so every
+    pair runs whole: both schedules agree within the prefill bound."""
+    p = inputs.prefill_inputs(lens, H, 64, seed=seed, device=dev)
+    s0 = inputs.initial_state(len(lens), H, 64, seed=seed, device=dev)
+    o1, s1 = _run(p, dev, s0=s0)
+    cu = p["cu_seqlens"]
+    small = torch.empty(256, dtype=torch.uint8, device=dev)
+    o2, s2 = wkv7.prefill(p["r"], p["w"], p["k"], p["v"], p["kk"], p["a"], cu.to(dev), initial_state=s0,
+                          cu_seqlens_host=cu, workspace=small)
+    wkv7.check_device_status()
+    assert rel_err(o1, o2) <= TOL
+    assert rel_err(s1, s2) <= TOL
+
+
+def test_tail_split_in_place_state(dev):
+    lens, H = [3000], 8
+    p = inputs.prefill_inputs(lens, H, 64, seed=23, device=dev)
+    s0 = inputs.initial_state(1, H, 64, seed=23, device=dev)
+    s = s0.clone()
+    o, sf = _run(p, dev, s0=s, final=s)
+    assert sf.data_ptr() == s.data_ptr()
+    _check(p, o, sf, s0=s0)
+
+
 def test_step_and_prefill_agree(dev):
     """The recurrent path (wkv7_step token by token) and the prefill path agree
     within the prefill bound on the same fp32 inputs."""
