@@ -171,7 +171,7 @@ struct SplitItem {
     int32_t ohat_row;   // first scratch row of a transfer item's readout
 };
 constexpr int kMaxSplitItems = 256;
-constexpr int kMaxSplitPairs = 48;
+constexpr int kMaxSplitPairs = 80;
 constexpr int kMaxSegs = 16;
 struct SplitPlan {
     int main_items;
@@ -1015,9 +1015,12 @@ int sm_count() {
 
 // The tail-split schedule (see SplitItem).  With P pairs on S SMs (one CTA per SM),
 // the last r = P mod S pairs in schedule order (the shortest) would run alone in a
-// last wave; when r <= S/3 each is cut into k segments (2k - 1 items, all running
-// concurrently) with k as large as the SMs, kMaxSegs and the scratch allow.  Needs
-// the host copy of cu_seqlens; returns false (whole pairs only) otherwise.
+// last wave.  When r <= S/3 each is cut into k equal segments (2k - 1 items, all
+// running at once) with k as large as the SMs, kMaxSegs and the scratch allow.
+// When S/3 < r <= S/2 each is cut in two, 2:1: the long first segments and S - r
+// of the short items start together, the other short items follow as the first
+// short ones finish, so the tail takes about 2/3 of a pair.  Needs the host copy
+// of cu_seqlens; returns false (whole pairs only) otherwise.
 bool plan_split(const PrefillArgs &a, unsigned char *split_ws, size_t split_bytes, SplitPlan &plan, FixPlan &fix) {
     const long long P = static_cast<long long>(a.num_seqs) * a.H;
     plan.main_items = static_cast<int>(P);
@@ -1029,7 +1032,8 @@ bool plan_split(const PrefillArgs &a, unsigned char *split_ws, size_t split_byte
     const int S = sm_count();
     if (S <= 0) return false;
     const long long r = P % S;
-    if (r == 0 || 3 * r > S || r > kMaxSplitPairs) return false;
+    if (r == 0 || 2 * r > S || r > kMaxSplitPairs) return false;
+    const bool two_to_one = 3 * r > S;
     auto len = [&](int b) { return a.cu_seqlens_host[b + 1] - a.cu_seqlens_host[b]; };
     // the schedule's sequence order: the device order kernel's (descending length, ties by index)
     std::vector<int> ord(a.num_seqs);
@@ -1041,8 +1045,14 @@ bool plan_split(const PrefillArgs &a, unsigned char *split_ws, size_t split_byte
         const int b = ord[bi / a.H];
         tail.push_back({b, static_cast<int>(bi % a.H), (len(b) + kC - 1) / kC});
     }
-    auto segs = [&](const Tail &t, int k) { return t.n > 32767 ? 1 : std::min(k, t.n / 2); };
-    for (int k = static_cast<int>(std::min<long long>(kMaxSegs, (S / r + 1) / 2)); k >= 2; --k) {
+    // segment j of a pair of n chunks cut into kp segments: [bound(j), bound(j + 1))
+    auto segs = [&](const Tail &t, int k) { return t.n > 32767 || t.n < 3 ? 1 : std::min(k, t.n / 2); };
+    auto bound = [&](const Tail &t, int kp, int j) {
+        if (two_to_one) return j == 0 ? 0 : j == 1 ? (2 * t.n + 2) / 3 : t.n;
+        return j * t.n / kp;
+    };
+    const int k_hi = two_to_one ? 2 : static_cast<int>(std::min<long long>(kMaxSegs, (S / r + 1) / 2));
+    for (int k = k_hi; k >= 2; --k) {
         long long items = 0, rows = 0, nsplit = 0;
         for (const Tail &t : tail) {
             const int kp = segs(t, k);
@@ -1052,12 +1062,13 @@ bool plan_split(const PrefillArgs &a, unsigned char *split_ws, size_t split_byte
             }
             items += 2 * kp - 1;
             ++nsplit;
-            rows += static_cast<long long>(t.n - t.n / kp) * 64;
+            rows += static_cast<long long>(t.n - bound(t, kp, 1)) * 64;
         }
-        if (nsplit == 0 || items > kMaxSplitItems || items > S || rows > rows_cap) continue;
+        if (nsplit == 0 || items > kMaxSplitItems || (!two_to_one && items > S) || rows > rows_cap) continue;
         plan.main_items = static_cast<int>(P - r);
         plan.slots = fix.slots = reinterpret_cast<float *>(split_ws);
         plan.ohat = fix.ohat = reinterpret_cast<float *>(split_ws + kSlotsBytes);
+        // items in dispatch order: whole tail pairs and first segments, then the rest
         int n = 0, slot = 0, blk = 0;
         long long row = 0;
         for (const Tail &t : tail) {
@@ -1070,25 +1081,31 @@ bool plan_split(const PrefillArgs &a, unsigned char *split_ws, size_t split_byte
             fp.b = t.b;
             fp.h = t.h;
             fp.nseg = kp;
-            for (int j = 0; j < kp; ++j) {
-                const int16_t c0 = static_cast<int16_t>(j * t.n / kp), c1 = static_cast<int16_t>((j + 1) * t.n / kp);
+            FixSeg &sg = fp.seg[0];
+            sg.c0 = 0;
+            sg.c1 = static_cast<int16_t>(bound(t, kp, 1));
+            sg.slot_part = static_cast<int16_t>(slot);
+            sg.slot_transfer = -1;
+            sg.ohat_row = 0;
+            sg.blk0 = 0;
+            plan.item[n++] = {pair, sg.c0, sg.c1, kItemWhole, static_cast<int16_t>(slot++), 0};
+        }
+        for (int f = 0; f < fix.n_pairs; ++f) {
+            FixPair &fp = fix.pair[f];
+            const Tail t{fp.b, fp.h, (len(fp.b) + kC - 1) / kC};
+            const int pair = fp.b * a.H + fp.h;
+            for (int j = 1; j < fp.nseg; ++j) {
                 FixSeg &sg = fp.seg[j];
-                sg.c0 = c0;
-                sg.c1 = c1;
+                sg.c0 = static_cast<int16_t>(bound(t, fp.nseg, j));
+                sg.c1 = static_cast<int16_t>(bound(t, fp.nseg, j + 1));
                 sg.slot_part = static_cast<int16_t>(slot);
-                plan.item[n++] = {pair, c0, c1, j == 0 ? kItemWhole : kItemPart, static_cast<int16_t>(slot++), 0};
-                if (j == 0) {
-                    sg.slot_transfer = -1;
-                    sg.ohat_row = 0;
-                    sg.blk0 = 0;
-                    continue;
-                }
+                plan.item[n++] = {pair, sg.c0, sg.c1, kItemPart, static_cast<int16_t>(slot++), 0};
                 sg.slot_transfer = static_cast<int16_t>(slot);
                 sg.ohat_row = static_cast<int32_t>(row);
                 sg.blk0 = blk;
-                plan.item[n++] = {pair, c0, c1, kItemTransfer, static_cast<int16_t>(slot++), static_cast<int32_t>(row)};
-                row += static_cast<long long>(c1 - c0) * 64;
-                blk += c1 - c0;
+                plan.item[n++] = {pair, sg.c0, sg.c1, kItemTransfer, static_cast<int16_t>(slot++), static_cast<int32_t>(row)};
+                row += static_cast<long long>(sg.c1 - sg.c0) * 64;
+                blk += sg.c1 - sg.c0;
             }
         }
         plan.n_items = n;
