@@ -184,7 +184,6 @@ struct FixSeg {
     int16_t c0, c1;
     int16_t slot_part, slot_transfer;  // slot_part of segment 0: its (true) final state
     int32_t ohat_row;
-    int32_t blk0;  // first output-fix block of this segment
 };
 struct FixPair {
     int32_t b, h, nseg;
@@ -192,7 +191,7 @@ struct FixPair {
 };
 struct FixPlan {
     int n_pairs;
-    int n_blocks;  // output-fix blocks (one per chunk of every segment j >= 1)
+    int n_blocks;  // output-fix blocks per pair: the most chunks after a first segment
     float *slots;
     float *ohat;
     FixPair pair[kMaxSplitPairs];
@@ -847,95 +846,110 @@ wkv7_prefill_order_kernel(const int32_t *__restrict__ cu, int num_seqs, int32_t 
 
 constexpr int kFixThreads = 256;
 
+// 64x64 products in fp32 on 256 threads, each owning a 4x4 tile (rows 4 tr.., columns
+// 4 tc..): acc += A B with A held transposed (At[k][row], stride kLdT) and B row-major
+// (stride 64), both in shared memory; per k one 16-byte load of each gives 16 FMAs.
+constexpr int kLdT = 68;
+__device__ __forceinline__ void mm64_tile(const float *At, const float *B, int tr, int tc, float (&acc)[4][4]) {
+#pragma unroll 8
+    for (int k = 0; k < 64; ++k) {
+        const float4 a = *reinterpret_cast<const float4 *>(At + k * kLdT + 4 * tr);
+        const float4 b = *reinterpret_cast<const float4 *>(B + k * 64 + 4 * tc);
+        const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(av[r], bv[c], acc[r][c]);
+    }
+}
+// global row-major 64x64 fp32 -> shared, transposed (dst[k][row], stride kLdT)
+__device__ __forceinline__ void load_t64(float *dst, const float *src) {
+    for (int e = threadIdx.x; e < 1024; e += kFixThreads) {
+        const float4 x = reinterpret_cast<const float4 *>(src)[e];
+        const int row = e >> 4, k0 = 4 * (e & 15);
+        dst[(k0 + 0) * kLdT + row] = x.x;
+        dst[(k0 + 1) * kLdT + row] = x.y;
+        dst[(k0 + 2) * kLdT + row] = x.z;
+        dst[(k0 + 3) * kLdT + row] = x.w;
+    }
+}
+
 // One CTA per split pair: the true state at every segment boundary, in order,
 // S_in(j+1) = P(j) S_in(j) + S_part(j), written over S_part(j)'s slot; the
 // last one is the pair's final state.
 __global__ void __launch_bounds__(kFixThreads)
 wkv7_prefill_split_chain_kernel(const __grid_constant__ FixPlan fp, float *final_state, int H) {
-    __shared__ float sin_[64 * 64];
+    __shared__ __align__(16) float sin_[64 * 64];
+    __shared__ __align__(16) float pt[64 * kLdT];  // P(j) transposed
     const FixPair &pr = fp.pair[blockIdx.x];
-    const int tid = threadIdx.x, i = tid >> 2, c0 = 16 * (tid & 3);
-    const float *s0 = fp.slots + static_cast<long long>(pr.seg[0].slot_part) * 4096;
-    for (int e = tid; e < 4096; e += kFixThreads) sin_[e] = s0[e];
-    __syncthreads();
+    const int tid = threadIdx.x, tr = tid >> 4, tc = tid & 15;
+    const float4 *s0 = reinterpret_cast<const float4 *>(fp.slots + static_cast<long long>(pr.seg[0].slot_part) * 4096);
+    for (int e = tid; e < 1024; e += kFixThreads) reinterpret_cast<float4 *>(sin_)[e] = s0[e];
     for (int j = 1; j < pr.nseg; ++j) {
-        const float *P = fp.slots + static_cast<long long>(pr.seg[j].slot_transfer) * 4096;
+        load_t64(pt, fp.slots + static_cast<long long>(pr.seg[j].slot_transfer) * 4096);
         float *Sp = fp.slots + static_cast<long long>(pr.seg[j].slot_part) * 4096;
-        float acc[16];
+        float acc[4][4];
 #pragma unroll
-        for (int x = 0; x < 16; ++x) acc[x] = Sp[i * 64 + c0 + x];
-        for (int u = 0; u < 64; ++u) {
-            const float pv = P[i * 64 + u];
-#pragma unroll
-            for (int x = 0; x < 16; ++x) acc[x] = fmaf(pv, sin_[u * 64 + c0 + x], acc[x]);
+        for (int r = 0; r < 4; ++r) {
+            const float4 v = *reinterpret_cast<const float4 *>(Sp + (4 * tr + r) * 64 + 4 * tc);
+            acc[r][0] = v.x; acc[r][1] = v.y; acc[r][2] = v.z; acc[r][3] = v.w;
         }
-        __syncthreads();  // every thread has read S_in(j)
+        __syncthreads();  // P(j)^T and S_in(j) in shared memory
+        mm64_tile(pt, sin_, tr, tc, acc);
+        __syncthreads();  // every thread has read S_in(j) and P(j)
 #pragma unroll
-        for (int x = 0; x < 16; ++x) {
-            sin_[i * 64 + c0 + x] = acc[x];
-            Sp[i * 64 + c0 + x] = acc[x];
+        for (int r = 0; r < 4; ++r) {
+            const float4 v = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+            *reinterpret_cast<float4 *>(sin_ + (4 * tr + r) * 64 + 4 * tc) = v;
+            *reinterpret_cast<float4 *>(Sp + (4 * tr + r) * 64 + 4 * tc) = v;
         }
-        __syncthreads();
     }
+    __syncthreads();
     if (final_state) {
-        float *dst = final_state + (static_cast<long long>(pr.b) * H + pr.h) * 4096;
-        for (int e = tid; e < 4096; e += kFixThreads) dst[e] = sin_[e];
+        float4 *dst = reinterpret_cast<float4 *>(final_state + (static_cast<long long>(pr.b) * H + pr.h) * 4096);
+        for (int e = tid; e < 1024; e += kFixThreads) dst[e] = reinterpret_cast<const float4 *>(sin_)[e];
     }
 }
 
-// One CTA per chunk of every segment j >= 1: o_t += S_in(j)^T (P_t^T r_t).
+// Grid (chunks after a pair's first segment, split pairs): o_t += S_in(j)^T (P_t^T r_t)
+// for every token of segment j >= 1, as the 64x64x64 product [P_t^T r_t]_t S_in(j).
 __global__ void __launch_bounds__(kFixThreads)
 wkv7_prefill_split_ofix_kernel(const __grid_constant__ FixPlan fp, PrefillArgs p) {
-    __shared__ float sin_[64 * 64];
-    __shared__ float oh[64 * 65];
-    const int blk = static_cast<int>(blockIdx.x);
-    int pi = -1, j = -1;
-    for (int a = 0; a < fp.n_pairs && pi < 0; ++a)
-        for (int g = 1; g < fp.pair[a].nseg; ++g) {
-            const FixSeg &sg = fp.pair[a].seg[g];
-            if (blk >= sg.blk0 && blk < sg.blk0 + (sg.c1 - sg.c0)) {
-                pi = a;
-                j = g;
-                break;
-            }
-        }
-    if (pi < 0) {
-        if (threadIdx.x == 0) report(p.status, kDevBounds);
-        return;
-    }
-    const FixPair &pr = fp.pair[pi];
+    __shared__ __align__(16) float sin_[64 * 64];
+    __shared__ __align__(16) float oht[64 * kLdT];  // readout rows, transposed
+    const FixPair &pr = fp.pair[blockIdx.y];
+    const int chunk = pr.seg[1].c0 + static_cast<int>(blockIdx.x);
+    int j = 1;
+    while (j < pr.nseg && chunk >= pr.seg[j].c1) ++j;
+    if (j >= pr.nseg) return;  // past this pair's last chunk
     const FixSeg &sg = pr.seg[j];
-    const int chunk = blk - sg.blk0;
-    const int tid = threadIdx.x;
-    const float *Sin = fp.slots + static_cast<long long>(pr.seg[j - 1].slot_part) * 4096;  // true S at the boundary
-    const float *orow = fp.ohat + (static_cast<long long>(sg.ohat_row) + chunk * 64) * 64;
-    for (int e = tid; e < 4096; e += kFixThreads) {
-        sin_[e] = Sin[e];
-        oh[(e >> 6) * 65 + (e & 63)] = orow[e];
-    }
+    const int tid = threadIdx.x, tr = tid >> 4, tc = tid & 15;
+    // S_in(j): the true state at the segment's start (segment 0's slot or, for j >= 2,
+    // the chain kernel's result over S_part(j - 1))
+    const float4 *Sin = reinterpret_cast<const float4 *>(fp.slots + static_cast<long long>(pr.seg[j - 1].slot_part) * 4096);
+    for (int e = tid; e < 1024; e += kFixThreads) reinterpret_cast<float4 *>(sin_)[e] = Sin[e];
+    load_t64(oht, fp.ohat + (static_cast<long long>(sg.ohat_row) + (chunk - sg.c0) * 64) * 64);
     __syncthreads();
+    float acc[4][4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
+    mm64_tile(oht, sin_, tr, tc, acc);
     const int bos = p.cu_seqlens[pr.b], eos = p.cu_seqlens[pr.b + 1];
-    const int t0 = bos + (sg.c0 + chunk) * 64;
+    const int t0 = bos + chunk * 64;
     const int lc = min(64, eos - t0);
-    const int t = tid >> 2, c0 = 16 * (tid & 3);
-    if (t < lc) {
-        float acc[16];
 #pragma unroll
-        for (int x = 0; x < 16; ++x) acc[x] = 0.f;
-        for (int i = 0; i < 64; ++i) {
-            const float hv = oh[t * 65 + i];
-#pragma unroll
-            for (int x = 0; x < 16; ++x) acc[x] = fmaf(hv, sin_[i * 64 + c0 + x], acc[x]);
-        }
-        float4 *dst = reinterpret_cast<float4 *>(p.o + (static_cast<long long>(t0) + t) * p.H * 64 + pr.h * 64 + c0);
-#pragma unroll
-        for (int x = 0; x < 4; ++x) {
-            float4 v = dst[x];
-            v.x += acc[4 * x];
-            v.y += acc[4 * x + 1];
-            v.z += acc[4 * x + 2];
-            v.w += acc[4 * x + 3];
-            dst[x] = v;
+    for (int r = 0; r < 4; ++r) {
+        const int t = 4 * tr + r;
+        if (t < lc) {
+            float4 *dst = reinterpret_cast<float4 *>(p.o + (static_cast<long long>(t0) + t) * p.H * 64 + pr.h * 64 + 4 * tc);
+            float4 v = *dst;
+            v.x += acc[r][0];
+            v.y += acc[r][1];
+            v.z += acc[r][2];
+            v.w += acc[r][3];
+            *dst = v;
         }
     }
 }
@@ -1087,7 +1101,6 @@ bool plan_split(const PrefillArgs &a, unsigned char *split_ws, size_t split_byte
             sg.slot_part = static_cast<int16_t>(slot);
             sg.slot_transfer = -1;
             sg.ohat_row = 0;
-            sg.blk0 = 0;
             plan.item[n++] = {pair, sg.c0, sg.c1, kItemWhole, static_cast<int16_t>(slot++), 0};
         }
         for (int f = 0; f < fix.n_pairs; ++f) {
@@ -1102,11 +1115,10 @@ bool plan_split(const PrefillArgs &a, unsigned char *split_ws, size_t split_byte
                 plan.item[n++] = {pair, sg.c0, sg.c1, kItemPart, static_cast<int16_t>(slot++), 0};
                 sg.slot_transfer = static_cast<int16_t>(slot);
                 sg.ohat_row = static_cast<int32_t>(row);
-                sg.blk0 = blk;
                 plan.item[n++] = {pair, sg.c0, sg.c1, kItemTransfer, static_cast<int16_t>(slot++), static_cast<int32_t>(row)};
                 row += static_cast<long long>(sg.c1 - sg.c0) * 64;
-                blk += sg.c1 - sg.c0;
             }
+            blk = std::max(blk, fp.seg[fp.nseg - 1].c1 - fp.seg[1].c0);
         }
         plan.n_items = n;
         fix.n_blocks = blk;
@@ -1146,7 +1158,7 @@ cudaError_t launch_chunked(const PrefillArgs &args, unsigned char *split_ws, siz
     wkv7_prefill_split_chain_kernel<<<fix.n_pairs, kFixThreads, 0, stream>>>(fix, args.final_state, args.H);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    wkv7_prefill_split_ofix_kernel<<<fix.n_blocks, kFixThreads, 0, stream>>>(fix, args);
+    wkv7_prefill_split_ofix_kernel<<<dim3(fix.n_blocks, fix.n_pairs), kFixThreads, 0, stream>>>(fix, args);
     return cudaGetLastError();
 }
 
