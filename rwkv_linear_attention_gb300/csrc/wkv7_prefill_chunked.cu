@@ -109,17 +109,21 @@ static_assert(SM_BG % 1024 == 0 && SM_BY % 1024 == 0 && SM_BX % 1024 == 0 && SM_
               "operand tiles must be 1024-byte aligned");
 constexpr uint32_t kTmaBytes = 5 * kTile + 16384;
 
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
+// An fp32 value as a tf32 MMA operand, rounded to nearest (ties away from zero):
+// the tensor core reads the top 19 bits of each 32-bit operand and ignores the low
+// 13, so adding half a tf32 ulp (bit 12) to the bit pattern makes that truncation
+// round.  Used only for words the tensor core consumes.
+__device__ __forceinline__ uint32_t to_tf32(float x) { return __float_as_uint(x) + 0x1000u; }
 __device__ __forceinline__ void st_tf32x4(unsigned char *p, float a, float b, float c, float d) {
     *reinterpret_cast<uint4 *>(p) = make_uint4(to_tf32(a), to_tf32(b), to_tf32(c), to_tf32(d));
 }
-// Reciprocal of a decay factor (fast approximate divide, ~2 ulp); it only
-// feeds tf32 operands, whose rounding dominates.
-__device__ __forceinline__ float rcp(float x) { return __fdividef(1.f, x); }
+// Reciprocal of a decay factor (the hardware approximation, rcp.approx.ftz, ~1 ulp);
+// it only feeds tf32 operands, whose rounding dominates.  Factors lie in e^{+-80}.
+__device__ __forceinline__ float rcp(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
 __device__ __forceinline__ float bf2f(uint32_t lo16) { return __uint_as_float(lo16 << 16); }
 
 // bf16 raw tile [64 tokens][64 channels] in the TMA 128-byte swizzle layout.
@@ -352,9 +356,9 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
     };
     auto chunk_len = [&](int chunk) { return min(kC, eos - (bos + (c_begin + chunk) * kC)); };
 
-    // ---- phase 1: masked cumulative log-decay g; E = e^{g - g_ref} (g_ref = g[31]) in place;
-    // the Gram B operand [C ; K] from the same registers.  Thread: channels 2cp, 2cp+1 of
-    // rows 4 seg .. 4 seg + 3 (16 row segments; their totals are scanned through TOT).
+    // ---- phase 1: masked cumulative log-decay g; E = e^{g - g_ref} (g_ref = g[31]) in place.
+    // Thread: channels 2cp, 2cp+1 of rows 4 seg .. 4 seg + 3 (16 row segments; their totals
+    // are scanned through TOT).
     auto phase1 = [&](int lc, int gbuf) {
         const int ch = 2 * (tid & 31), seg = tid >> 5;
         float2 g[4];
@@ -385,18 +389,10 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
         if (seg == 7) *reinterpret_cast<float2 *>(GREF + ch) = g[3];  // row 31
         wsync();
         const float2 gr = *reinterpret_cast<const float2 *>(GREF + ch);
-        unsigned char *BG = sm + SM_BG;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int t = 4 * seg + u;
             *reinterpret_cast<float2 *>(E + eidx(t, ch)) = make_float2(__expf(g[u].x - gr.x), __expf(g[u].y - gr.y));
-            // B_G = [C ; K]: C[s][i] = kk a e^{g_ref - g_s}, K[s][i] = k e^{g_ref - g_s} (rows s = t, 64 + t)
-            const bool valid = t < lc;
-            const float ex = valid ? __expf(gr.x - g[u].x) : 0.f, ey = valid ? __expf(gr.y - g[u].y) : 0.f;
-            const float2 kkv = raw2(rkk, t, ch), av = raw2(ra, t, ch), kv = raw2(rk, t, ch);
-            *reinterpret_cast<uint2 *>(BG + sw128_off(t, ch, 128)) =
-                make_uint2(to_tf32(kkv.x * av.x * ex), to_tf32(kkv.y * av.y * ey));
-            *reinterpret_cast<uint2 *>(BG + sw128_off(64 + t, ch, 128)) = make_uint2(to_tf32(kv.x * ex), to_tf32(kv.y * ey));
         }
         if (seg == 0) *reinterpret_cast<float2 *>(EREF + gbuf * 64 + ch) = make_float2(__expf(gr.x), __expf(gr.y));
         if (seg == 15) {  // row 63
@@ -405,8 +401,25 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
         }
     };
 
-    // ---- phase 2: A_G = [R ; Q] into TMEM
+    // ---- phase 2: A_G = [R ; Q] into TMEM; the Gram B operand B_G = [C ; K] (rows s, 64 + s),
+    // C[s][i] = kk a e^{g_ref - g_s}, K[s][i] = k e^{g_ref - g_s}, with e^{g_ref - g_s} = 1 / E[s][i]
     auto phase2 = [&](int lc, const float *eref) {
+        {
+            const int ch = 2 * (tid & 31), seg = tid >> 5;
+            unsigned char *BG = sm + SM_BG;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int t = 4 * seg + u;
+                const float2 e = *reinterpret_cast<const float2 *>(E + eidx(t, ch));
+                const bool valid = t < lc;
+                const float ex = valid ? rcp(e.x) : 0.f, ey = valid ? rcp(e.y) : 0.f;
+                const float2 kkv = raw2(rkk, t, ch), av = raw2(ra, t, ch), kv = raw2(rk, t, ch);
+                *reinterpret_cast<uint2 *>(BG + sw128_off(t, ch, 128)) =
+                    make_uint2(to_tf32(kkv.x * av.x * ex), to_tf32(kkv.y * av.y * ey));
+                *reinterpret_cast<uint2 *>(BG + sw128_off(64 + t, ch, 128)) =
+                    make_uint2(to_tf32(kv.x * ex), to_tf32(kv.y * ey));
+            }
+        }
         {
             const bool rrow = m < 64;
             const int t = rrow ? m : m - 64;
