@@ -451,8 +451,10 @@ def run_ours(args):
     value = world * wl.state_bytes_per_step() * args.steps / (ms / 1e3) / 1e9
     launch_s = ms / 1e3 / launches
     achieved = wl.B * wl.H * STEP_BYTES / launch_s / 1e9
-    step_src = [os.path.join(ROOT, "rwkv_linear_attention_gb300", "csrc", "wkv7_step.cu")]
-    prefill_src = [os.path.join(ROOT, "rwkv_linear_attention_gb300", "csrc", "wkv7_prefill_chunked.cu")]
+    csrc = os.path.join(ROOT, "rwkv_linear_attention_gb300", "csrc")
+    shared = [os.path.join(csrc, "sm103_ptx.cuh"), os.path.join(csrc, "wkv7_internal.cuh")]
+    step_src = [os.path.join(csrc, "wkv7_step.cu")] + shared
+    prefill_src = [os.path.join(csrc, "wkv7_prefill_chunked.cu")] + shared
     traffic = kernel_traffic("wkv7_step_kernel", f"B={B},H={cfg['H']}", step_src)
     del graphs
 
