@@ -135,6 +135,12 @@ __device__ __forceinline__ float2 raw2(const unsigned char *tile, int t, int i) 
     const uint32_t u = *reinterpret_cast<const uint32_t *>(tile + raw_off(t, i));
     return make_float2(bf2f(u & 0xffffu), __uint_as_float(u & 0xffff0000u));
 }
+// four consecutive channels i .. i+3 (i % 4 == 0)
+__device__ __forceinline__ float4 raw4(const unsigned char *tile, int t, int i) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(tile + raw_off(t, i));
+    return make_float4(bf2f(u.x & 0xffffu), __uint_as_float(u.x & 0xffff0000u), bf2f(u.y & 0xffffu),
+                       __uint_as_float(u.y & 0xffff0000u));
+}
 // eight consecutive channels i .. i+7 (i % 8 == 0)
 __device__ __forceinline__ void raw8(const unsigned char *tile, int t, int i, float *f) {
     const uint4 u = *reinterpret_cast<const uint4 *>(tile + raw_off(t, i));
@@ -402,48 +408,67 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
     };
 
     // ---- phase 2: A_G = [R ; Q] into TMEM; the Gram B operand B_G = [C ; K] (rows s, 64 + s),
-    // C[s][i] = kk a e^{g_ref - g_s}, K[s][i] = k e^{g_ref - g_s}, with e^{g_ref - g_s} = 1 / E[s][i]
+    // C[s][i] = kk a e^{g_ref - g_s}, K[s][i] = k e^{g_ref - g_s}, with e^{g_ref - g_s} = 1 / E[s][i].
+    // Rows past the chunk's end are zero.
     auto phase2 = [&](int lc, const float *eref) {
-        {
-            const int ch = 2 * (tid & 31), seg = tid >> 5;
+        {   // B_G: thread = row t, channels 4 cq .. 4 cq + 3 and 32 + 4 cq .. 32 + 4 cq + 3, so that
+            // each 8- or 16-byte access of a quarter-warp (one row) covers 8 distinct bank groups
+            const int t = tid >> 3, cq = tid & 7;
             unsigned char *BG = sm + SM_BG;
+            uint4 cw[2], kw[2];
+            if (t < lc) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int t = 4 * seg + u;
-                const float2 e = *reinterpret_cast<const float2 *>(E + eidx(t, ch));
-                const bool valid = t < lc;
-                const float ex = valid ? rcp(e.x) : 0.f, ey = valid ? rcp(e.y) : 0.f;
-                const float2 kkv = raw2(rkk, t, ch), av = raw2(ra, t, ch), kv = raw2(rk, t, ch);
-                *reinterpret_cast<uint2 *>(BG + sw128_off(t, ch, 128)) =
-                    make_uint2(to_tf32(kkv.x * av.x * ex), to_tf32(kkv.y * av.y * ey));
-                *reinterpret_cast<uint2 *>(BG + sw128_off(64 + t, ch, 128)) =
-                    make_uint2(to_tf32(kv.x * ex), to_tf32(kv.y * ey));
+                for (int h = 0; h < 2; ++h) {
+                    const int c4 = 4 * cq + 32 * h;
+                    const float4 kkv = raw4(rkk, t, c4), av = raw4(ra, t, c4), kv = raw4(rk, t, c4);
+                    const float4 e = *reinterpret_cast<const float4 *>(E + eidx(t, c4));
+                    const float2 e0 = make_float2(rcp(e.x), rcp(e.y)), e1 = make_float2(rcp(e.z), rcp(e.w));
+                    const float2 c0 = __fmul2_rn(__fmul2_rn(make_float2(kkv.x, kkv.y), make_float2(av.x, av.y)), e0);
+                    const float2 c1 = __fmul2_rn(__fmul2_rn(make_float2(kkv.z, kkv.w), make_float2(av.z, av.w)), e1);
+                    const float2 k0 = __fmul2_rn(make_float2(kv.x, kv.y), e0);
+                    const float2 k1 = __fmul2_rn(make_float2(kv.z, kv.w), e1);
+                    cw[h] = make_uint4(to_tf32(c0.x), to_tf32(c0.y), to_tf32(c1.x), to_tf32(c1.y));
+                    kw[h] = make_uint4(to_tf32(k0.x), to_tf32(k0.y), to_tf32(k1.x), to_tf32(k1.y));
+                }
+            } else {
+                cw[0] = cw[1] = kw[0] = kw[1] = make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                *reinterpret_cast<uint4 *>(BG + sw128_off(t, 4 * cq + 32 * h, 128)) = cw[h];
+                *reinterpret_cast<uint4 *>(BG + sw128_off(64 + t, 4 * cq + 32 * h, 128)) = kw[h];
             }
         }
-        {
+        {   // A_G: thread = TMEM lane m (row t of R, or of Q for m >= 64), channels 16 cg ..
             const bool rrow = m < 64;
             const int t = rrow ? m : m - 64;
             const int i0 = 16 * cg;
-            const float valid = t < lc ? 1.f : 0.f;
-            float x[16];
-            raw8(rrow ? rr : rkk, t, i0, x);
-            raw8(rrow ? rr : rkk, t, i0 + 8, x + 8);
             uint32_t wds[16];
+            if (t < lc) {
+                float x[16];
+                raw8(rrow ? rr : rkk, t, i0, x);
+                raw8(rrow ? rr : rkk, t, i0 + 8, x + 8);
 #pragma unroll
-            for (int j = 0; j < 16; j += 4) {
-                float4 e;
-                if (rrow) {
-                    e = *reinterpret_cast<const float4 *>(E + eidx(t, i0 + j));
-                } else if (t > 0) {
-                    e = *reinterpret_cast<const float4 *>(E + eidx(t - 1, i0 + j));
-                } else {
-                    const float4 er = *reinterpret_cast<const float4 *>(eref + i0 + j);
-                    e = make_float4(rcp(er.x), rcp(er.y), rcp(er.z), rcp(er.w));
+                for (int j = 0; j < 16; j += 4) {
+                    float4 e;
+                    if (rrow) {
+                        e = *reinterpret_cast<const float4 *>(E + eidx(t, i0 + j));
+                    } else if (t > 0) {
+                        e = *reinterpret_cast<const float4 *>(E + eidx(t - 1, i0 + j));
+                    } else {
+                        const float4 er = *reinterpret_cast<const float4 *>(eref + i0 + j);
+                        e = make_float4(rcp(er.x), rcp(er.y), rcp(er.z), rcp(er.w));
+                    }
+                    const float2 p0 = __fmul2_rn(make_float2(x[j], x[j + 1]), make_float2(e.x, e.y));
+                    const float2 p1 = __fmul2_rn(make_float2(x[j + 2], x[j + 3]), make_float2(e.z, e.w));
+                    wds[j] = to_tf32(p0.x);
+                    wds[j + 1] = to_tf32(p0.y);
+                    wds[j + 2] = to_tf32(p1.x);
+                    wds[j + 3] = to_tf32(p1.y);
                 }
-                wds[j] = to_tf32(valid * x[j] * e.x);
-                wds[j + 1] = to_tf32(valid * x[j + 1] * e.y);
-                wds[j + 2] = to_tf32(valid * x[j + 2] * e.z);
-                wds[j + 3] = to_tf32(valid * x[j + 3] * e.w);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) wds[j] = 0u;
             }
             tmem_st16(tmem + lane_off + kColAG + i0, wds);
         }
