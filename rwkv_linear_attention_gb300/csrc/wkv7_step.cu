@@ -73,12 +73,6 @@ wkv7_step_kernel(long long n_heads, const float *__restrict__ r, const float *__
 
     const long long first = blockIdx.x, stride = gridDim.x;
     const long long count = n_heads > first ? (n_heads - 1 - first) / stride + 1 : 0;
-    if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(smem_addr(&full[s]), 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
-
     const float *const vsrc[6] = {r, w, k, v, kk, a};
     auto issue = [&](long long idx) {
         const long long head = first + idx * stride;
@@ -89,10 +83,14 @@ wkv7_step_kernel(long long n_heads, const float *__restrict__ r, const float *__
 #pragma unroll
         for (int i = 0; i < 6; ++i) bulk_load(smem_addr(st[s].vec[i]), vsrc[i] + head * kN, kVecBytes, bar);
     };
+    // thread 0 sets up the barriers and starts the first loads before the block syncs
     long long issued = 0;
     if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(smem_addr(&full[s]), 1);
+        fence_mbar_init();
         for (; issued < count && issued < kStages; ++issued) issue(issued);
     }
+    __syncthreads();
     grid_dep_launch();
 
     const int rg = lane >> 2;
@@ -195,7 +193,9 @@ wkv7_step_kernel(long long n_heads, const float *__restrict__ r, const float *__
                 mbar_wait_bounded(smem_addr(&full[idx % kStages]), static_cast<uint32_t>((idx / kStages) & 1),
                                   kMaxPolls);
         }
-        bulk_wait<0>();
+        // the last state stores have read shared memory; their writes are complete when the
+        // grid is (which is what the next dependent launch waits for)
+        bulk_wait_read<0>();
     }
 }
 
