@@ -52,6 +52,9 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     P = ctypes.c_void_p
     f.argtypes = [ctypes.c_int, P, ctypes.c_int, ctypes.c_int,
                   P, P, P, P, P, P, P, P, P, ctypes.c_int]
+    t = lib.wkv7_oracle_tail
+    t.restype = ctypes.c_int
+    t.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int, P, P, P, P, P, P, P, P, ctypes.c_double, P]
     return lib
 
 
@@ -132,3 +135,32 @@ def step(r, w, k, v, kk, a, state, nthreads: int | None = None, lib=None):
     B = arrs[0].shape[0]
     cu = np.arange(B + 1, dtype=np.int64)
     return run(*arrs, cu_seqlens=cu, s0=state, nthreads=nthreads, lib=lib)
+
+
+def tail(o, r, k, v, rk, ln_w, ln_b, g, eps, lib=None):
+    """The time-mix tail after WKV (group norm per head, bonus, gate), in double.
+
+    o: WKV outputs [rows, H, N] (taken in double); r, k, v, g: [rows, H, N];
+    rk, ln_w, ln_b: [H, N]; eps: the norm's epsilon.  Returns y [rows, H, N]
+    float64.
+    """
+    lib = lib or load()
+    if hasattr(o, "detach"):
+        o = o.detach().cpu().double().numpy()
+    od = np.ascontiguousarray(o, dtype=np.float64)
+    rows, H, N = od.shape
+    xs = [_as_f32(x) for x in (r, k, v)]
+    params = [_as_f32(x) for x in (rk, ln_w, ln_b)]
+    gg = _as_f32(g)
+    for x in xs + [gg]:
+        if x.shape != (rows, H, N):
+            raise ValueError(f"row input shape {x.shape} != {(rows, H, N)}")
+    for x in params:
+        if x.shape != (H, N):
+            raise ValueError(f"parameter shape {x.shape} != {(H, N)}")
+    y = np.zeros((rows, H, N), dtype=np.float64)
+    rc = lib.wkv7_oracle_tail(rows, H, N, _ptr(od), *[_ptr(x) for x in xs], *[_ptr(x) for x in params],
+                              _ptr(gg), float(eps), _ptr(y))
+    if rc != 0:
+        raise ValueError(f"wkv7_oracle_tail failed with code {rc}")
+    return y

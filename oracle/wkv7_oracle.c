@@ -192,3 +192,60 @@ int wkv7_oracle_run(int num_seqs, const int64_t *cu_seqlens, int H, int N,
     free(threads);
     return rc;
 }
+
+/*
+ * wkv7_oracle_tail -- the tail of the time-mix block that follows WKV, in
+ * double, one (row, head) at a time.  The SwiftRWKV inference page names its
+ * parts ("the tail of tmix (group norm, bonus, gate)", in "What the decode
+ * path is made of" and in the fp32-stream prefill notes) and the RWKV-X page
+ * lists the per-head bonus weight r_k ([n_head, head_size]).  Written out
+ * (readings where the pages give no formula, also in the design notes: the
+ * group is one head's N channels, the variance is the mean squared deviation,
+ * eps is an argument, ln_w and ln_b are per channel of each head, the bonus
+ * is added after the norm's affine part and the gate multiplies the sum):
+ *
+ *     mu  = (1/N) sum_j o_j ,   var = (1/N) sum_j (o_j - mu)^2
+ *     y_j = ( (o_j - mu) / sqrt(var + eps) * ln_w_j + ln_b_j
+ *             + (sum_i r_i k_i rk_i) v_j ) * g_j
+ *
+ *   n_rows          : rows (tokens of a packed prefill, or B for a decode step)
+ *   o               : double [n_rows, H, N]   the WKV outputs
+ *   r, k, v, g      : float  [n_rows, H, N]
+ *   rk, ln_w, ln_b  : float  [H, N]           per-layer parameters
+ *   eps             : the norm's epsilon (>= 0)
+ *   y               : double [n_rows, H, N]   (written)
+ * Returns 0, or -1 on a malformed argument.
+ */
+int wkv7_oracle_tail(int64_t n_rows, int H, int N, const double *o, const float *r, const float *k,
+                     const float *v, const float *rk, const float *ln_w, const float *ln_b,
+                     const float *g, double eps, double *y)
+{
+    int64_t row;
+    int h, i, j;
+
+    if (n_rows < 0 || H <= 0 || N <= 0 || eps < 0.0)
+        return -1;
+    if (n_rows > 0 && (!o || !r || !k || !v || !rk || !ln_w || !ln_b || !g || !y))
+        return -1;
+    for (row = 0; row < n_rows; ++row) {
+        for (h = 0; h < H; ++h) {
+            const size_t base = ((size_t)row * (size_t)H + (size_t)h) * (size_t)N;
+            const size_t pbase = (size_t)h * (size_t)N;
+            double mu = 0.0, var = 0.0, bonus = 0.0, inv;
+            for (j = 0; j < N; ++j)
+                mu += o[base + j];
+            mu /= (double)N;
+            for (j = 0; j < N; ++j)
+                var += (o[base + j] - mu) * (o[base + j] - mu);
+            var /= (double)N;
+            inv = 1.0 / sqrt(var + eps);
+            for (i = 0; i < N; ++i)
+                bonus += (double)r[base + i] * (double)k[base + i] * (double)rk[pbase + i];
+            for (j = 0; j < N; ++j) {
+                const double normed = (o[base + j] - mu) * inv * (double)ln_w[pbase + j] + (double)ln_b[pbase + j];
+                y[base + j] = (normed + bonus * (double)v[base + j]) * (double)g[base + j];
+            }
+        }
+    }
+    return 0;
+}

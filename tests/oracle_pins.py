@@ -311,6 +311,109 @@ def pin_zero_length(lib):
     _close(s, np.zeros_like(s0), 0.0, "zero-length zero state")
 
 
+# --------------------------------------------------------------------------
+# (e) the time-mix tail after WKV: y = (GroupNorm_head(o) * ln_w + ln_b
+#     + (sum_i r_i k_i rk_i) v) * g   (SwiftRWKV page: "group norm, bonus, gate")
+
+
+def _tail_draw(rows, H, N, seed):
+    g = _rng(seed)
+    o = g.standard_normal((rows, H, N))
+    r, k, v, gate = (_f32(g.standard_normal((rows, H, N))) for _ in range(4))
+    rk, ln_w, ln_b = (_f32(g.standard_normal((H, N))) for _ in range(3))
+    return o, r, k, v, rk, ln_w, ln_b, gate
+
+
+def _tail(lib, o, r, k, v, rk, ln_w, ln_b, gate, eps):
+    return oracle.tail(o, r, k, v, rk, ln_w, ln_b, gate, eps, lib=lib)
+
+
+def pin_tail_golden_hand_n2(lib):
+    """One row, one head, N = 2, worked by hand (tests/golden/tail_n2_hand.txt)."""
+    vals = {}
+    for line in open(os.path.join(GOLDEN, "tail_n2_hand.txt")):
+        line = line.split("#", 1)[0].split()
+        if line:
+            vals[line[0]] = [float(x) for x in line[1:]]
+    row = lambda n: _f32(vals[n]).reshape(1, 1, 2)
+    par = lambda n: _f32(vals[n]).reshape(1, 2)
+    o = np.array(vals["o"], dtype=np.float64).reshape(1, 1, 2)
+    for eps, want in ((0.0, "eps0"), (3.0, "eps3")):
+        y = _tail(lib, o, row("r"), row("k"), row("v"), par("rk"), par("ln_w"), par("ln_b"), row("g"), eps)
+        _close(y.reshape(2), vals[want], 1e-15, f"hand-worked tail, eps={eps}")
+
+
+def pin_tail_standardises(lib):
+    """ln_w = 1, ln_b = 0, rk = 0, g = 1, eps = 0: every (row, head) of y has mean 0 and
+    mean square 1 (the group norm with the population variance)."""
+    rows, H, N = 5, 3, 16
+    o, r, k, v, _, _, _, _ = _tail_draw(rows, H, N, seed=40)
+    ones, zeros = np.ones((H, N), np.float32), np.zeros((H, N), np.float32)
+    y = _tail(lib, o, r, k, v, zeros, ones, zeros, np.ones((rows, H, N), np.float32), 0.0)
+    _close(y.mean(axis=-1), np.zeros((rows, H)), 1e-13, "mean of the normalised head")
+    _close((y * y).mean(axis=-1), np.ones((rows, H)), 1e-12, "mean square of the normalised head")
+
+
+def pin_tail_shift_and_scale_invariance(lib):
+    """With eps = 0 the tail ignores a shift and a positive scale of each head's o."""
+    rows, H, N = 4, 2, 8
+    o, r, k, v, rk, ln_w, ln_b, gate = _tail_draw(rows, H, N, seed=41)
+    y0 = _tail(lib, o, r, k, v, rk, ln_w, ln_b, gate, 0.0)
+    shift = _rng(42).standard_normal((rows, H, 1))
+    y1 = _tail(lib, 2.5 * o + shift, r, k, v, rk, ln_w, ln_b, gate, 0.0)
+    _close(y1, y0, 1e-12, "shift and scale of o")
+
+
+def pin_tail_gate_scales_the_sum(lib):
+    """y is linear in the gate: doubling g doubles every y (the gate multiplies the
+    normalised part and the bonus together)."""
+    rows, H, N = 3, 2, 8
+    o, r, k, v, rk, ln_w, ln_b, gate = _tail_draw(rows, H, N, seed=43)
+    y1 = _tail(lib, o, r, k, v, rk, ln_w, ln_b, gate, 1e-3)
+    y2 = _tail(lib, o, r, k, v, rk, ln_w, ln_b, 2 * gate, 1e-3)
+    _close(y2, 2 * y1, 1e-14, "gate linearity")
+
+
+def pin_tail_bonus_unit_vectors(lib):
+    """ln_w = ln_b = 0, g = 1: y = (sum_i r_i k_i rk_i) v.  With r = k = e_p the bonus is
+    rk_p; with r = e_p, k = e_q (p != q) it is 0."""
+    rows, H, N = 1, 2, 6
+    o, _, _, v, rk, _, _, _ = _tail_draw(rows, H, N, seed=44)
+    zeros = np.zeros((H, N), np.float32)
+    ones = np.ones((rows, H, N), np.float32)
+    for p, q in ((1, 1), (4, 4), (1, 4)):
+        r = np.zeros((rows, H, N), np.float32)
+        k = np.zeros((rows, H, N), np.float32)
+        r[..., p] = 1.0
+        k[..., q] = 1.0
+        y = _tail(lib, o, r, k, v, rk, zeros, zeros, ones, 1e-3)
+        want = (rk[:, p] if p == q else np.zeros(H)).reshape(1, H, 1) * v.astype(np.float64)
+        _close(y, want, 0.0, f"bonus with r = e_{p}, k = e_{q}")
+
+
+def pin_tail_constant_head(lib):
+    """A head whose o is constant has zero variance: with eps > 0 its normalised part is
+    0 and y = (ln_b + bonus v) g."""
+    rows, H, N = 2, 2, 4
+    _, r, k, v, rk, ln_w, ln_b, gate = _tail_draw(rows, H, N, seed=45)
+    o = np.full((rows, H, N), 0.75)
+    y = _tail(lib, o, r, k, v, rk, ln_w, ln_b, gate, 1e-2)
+    zeros = np.zeros((H, N), np.float32)
+    y_b = _tail(lib, np.zeros((rows, H, N)), r, k, v, rk, zeros, ln_b, gate, 1e-2)
+    _close(y, y_b, 0.0, "constant head equals zero head with ln_w = 0")
+
+
+def pin_tail_heads_use_their_parameters(lib):
+    """Permuting heads together with their per-head parameters permutes y."""
+    rows, H, N = 3, 4, 8
+    o, r, k, v, rk, ln_w, ln_b, gate = _tail_draw(rows, H, N, seed=46)
+    y = _tail(lib, o, r, k, v, rk, ln_w, ln_b, gate, 1e-3)
+    perm = [2, 0, 3, 1]
+    yp = _tail(lib, o[:, perm], r[:, perm], k[:, perm], v[:, perm], rk[perm], ln_w[perm], ln_b[perm],
+               gate[:, perm], 1e-3)
+    _close(yp, y[:, perm], 0.0, "head permutation")
+
+
 ALL_PINS = [
     pin_golden_hand_n2,
     pin_t1_zero_state,
@@ -324,4 +427,11 @@ ALL_PINS = [
     pin_equivariance,
     pin_packing,
     pin_zero_length,
+    pin_tail_golden_hand_n2,
+    pin_tail_standardises,
+    pin_tail_shift_and_scale_invariance,
+    pin_tail_gate_scales_the_sum,
+    pin_tail_bonus_unit_vectors,
+    pin_tail_constant_head,
+    pin_tail_heads_use_their_parameters,
 ]

@@ -31,6 +31,18 @@ MUTANTS = [
     ("wrong_head_offset", "((size_t)t * (size_t)H + (size_t)h) * (size_t)N",
      "((size_t)t * (size_t)H + (size_t)(H - 1 - h)) * (size_t)N"),
     ("last_token_dropped", "for (t = t_begin; t < t_end; ++t)", "for (t = t_begin; t + 1 < t_end; ++t)"),
+    # the time-mix tail
+    ("tail_unbiased_variance", "var /= (double)N;", "var /= (double)(N - 1);"),
+    ("tail_eps_outside_sqrt", "inv = 1.0 / sqrt(var + eps);", "inv = 1.0 / (sqrt(var) + eps);"),
+    ("tail_mean_not_subtracted", "(o[base + j] - mu) * inv", "o[base + j] * inv"),
+    ("tail_second_moment_not_centred", "var += (o[base + j] - mu) * (o[base + j] - mu);",
+     "var += o[base + j] * o[base + j];"),
+    ("tail_gate_only_on_norm", "y[base + j] = (normed + bonus * (double)v[base + j]) * (double)g[base + j];",
+     "y[base + j] = normed * (double)g[base + j] + bonus * (double)v[base + j];"),
+    ("tail_bonus_without_rk", "bonus += (double)r[base + i] * (double)k[base + i] * (double)rk[pbase + i];",
+     "bonus += (double)r[base + i] * (double)k[base + i];"),
+    ("tail_bonus_times_wrong_v", "bonus * (double)v[base + j]", "bonus * (double)v[base + (N - 1 - j)]"),
+    ("tail_parameters_of_head_zero", "const size_t pbase = (size_t)h * (size_t)N;", "const size_t pbase = 0;"),
 ]
 
 
