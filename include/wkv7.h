@@ -88,6 +88,57 @@ WKV7_API wkv7_status wkv7_step(int B, int H, int N,
                       float *state, float *o, cudaStream_t stream);
 
 /*
+ * The time-mix tail after WKV, per row and head of N channels:
+ *
+ *     y = (GroupNorm_head(o) * ln_w + ln_b + (sum_i r_i k_i r_k_i) v) * g
+ *
+ * GroupNorm_head(o)_j = (o_j - mean(o)) / sqrt(var(o) + eps) over the head's N
+ * channels (var = the mean squared deviation).  The SwiftRWKV inference page
+ * names these parts of the tail ("group norm, bonus, gate"; fused with the
+ * recurrent step's kernels in "What the decode path is made of" and run over
+ * the B*T rows of a prompt in the fp32-stream prefill notes); the RWKV-X page
+ * lists r_k as a per-head weight [n_head, head_size].  The pages print no
+ * formula and no eps: the group is one head, eps is the caller's, ln_w and
+ * ln_b are per channel of each head, the bonus is added after the norm's
+ * affine part and the gate multiplies the sum.
+ *
+ * wkv7_step_tail -- wkv7_step with the tail fused into the same kernel.
+ *
+ *   r, w, k, v, kk, a, state : as wkv7_step
+ *   o                 : fp32 [B, H, N] (the WKV output) or NULL (not written)
+ *   r_k, ln_w, ln_b   : fp32 [H, N]    per-layer parameters
+ *   g                 : fp32 [B, H, N] the gate of this token
+ *   eps               : the norm's epsilon, finite and >= 0
+ *   y                 : fp32 [B, H, N] output
+ *
+ * All pointers are device pointers, 16-byte aligned.  `state` overlaps nothing
+ * else; o and y overlap no input, no parameter and not each other
+ * (WKV7_ERR_INVALID_ARG).
+ */
+WKV7_API wkv7_status wkv7_step_tail(int B, int H, int N,
+                      const float *r, const float *w, const float *k,
+                      const float *v, const float *kk, const float *a,
+                      float *state, float *o,
+                      const float *r_k, const float *ln_w, const float *ln_b,
+                      const float *g, float eps, float *y, cudaStream_t stream);
+
+/*
+ * wkv7_tmix_tail -- the tail over n_rows packed rows, e.g. the outputs of
+ * wkv7_prefill ([T_total, H, N]).
+ *
+ *   o               : fp32 [n_rows, H, N]   the WKV outputs
+ *   r, k, v, g      : x_dtype [n_rows, H, N] (x_dtype WKV7_F32 or WKV7_BF16)
+ *   r_k, ln_w, ln_b : fp32 [H, N]
+ *   eps             : finite, >= 0
+ *   y               : fp32 [n_rows, H, N]; may be the same pointer as o (in
+ *                     place), otherwise it overlaps no argument
+ */
+WKV7_API wkv7_status wkv7_tmix_tail(int n_rows, int H, int N, wkv7_dtype x_dtype,
+                      const float *o, const void *r, const void *k, const void *v,
+                      const void *g, const float *r_k, const float *ln_w,
+                      const float *ln_b, float eps, float *y, cudaStream_t stream);
+
+/*
  * wkv7_prefill_workspace_size -- bytes of device workspace with which
  * wkv7_prefill can use every schedule for this shape (may be 0; the result
  * depends only on the arguments).  It holds:

@@ -24,7 +24,8 @@ import torch
 from . import _lib
 from ._lib import WKV7Error  # noqa: F401
 
-__all__ = ["step", "prefill", "prefill_workspace_size", "check_device_status", "WKV7Error", "HEAD_SIZE"]
+__all__ = ["step", "step_tail", "tmix_tail", "prefill", "prefill_workspace_size", "check_device_status",
+           "WKV7Error", "HEAD_SIZE"]
 
 HEAD_SIZE = 64
 
@@ -66,6 +67,61 @@ def step(r, w, k, v, kk, a, state, o=None, stream=None):
                        _ptr(state), _ptr(o), _stream(stream))
     _lib.check(st, "wkv7_step")
     return o
+
+
+def step_tail(r, w, k, v, kk, a, state, r_k, ln_w, ln_b, g, eps, y=None, o=None, want_o=False, stream=None):
+    """One decode token with the time-mix tail fused:
+    ``y = (GroupNorm_head(o) * ln_w + ln_b + (sum_i r_i k_i r_k_i) v) * g``.
+
+    Inputs and ``g`` fp32 [B, H, N]; ``r_k``, ``ln_w``, ``ln_b`` fp32 [H, N];
+    ``state`` updated in place.  Returns ``y`` (and ``o``, the WKV output, when
+    ``want_o`` or ``o`` is given: ``(y, o)``).
+    """
+    B, H, N = r.shape
+    for name, t in (("r", r), ("w", w), ("k", k), ("v", v), ("kk", kk), ("a", a), ("g", g)):
+        _need_cuda(name, t, torch.float32, (B, H, N))
+    for name, t in (("r_k", r_k), ("ln_w", ln_w), ("ln_b", ln_b)):
+        _need_cuda(name, t, torch.float32, (H, N))
+    _need_cuda("state", state, torch.float32, (B, H, N, N))
+    if y is None:
+        y = torch.empty((B, H, N), device=r.device, dtype=torch.float32)
+    _need_cuda("y", y, torch.float32, (B, H, N))
+    if o is None and want_o:
+        o = torch.empty((B, H, N), device=r.device, dtype=torch.float32)
+    if o is not None:
+        _need_cuda("o", o, torch.float32, (B, H, N))
+    lib = _lib.load()
+    st = lib.wkv7_step_tail(B, H, N, _ptr(r), _ptr(w), _ptr(k), _ptr(v), _ptr(kk), _ptr(a), _ptr(state),
+                            _ptr(o), _ptr(r_k), _ptr(ln_w), _ptr(ln_b), _ptr(g), float(eps), _ptr(y),
+                            _stream(stream))
+    _lib.check(st, "wkv7_step_tail")
+    return (y, o) if o is not None else y
+
+
+def tmix_tail(o, r, k, v, g, r_k, ln_w, ln_b, eps, y=None, stream=None):
+    """The time-mix tail over packed rows (e.g. a prefill's outputs):
+    ``o`` fp32 [rows, H, N]; ``r``, ``k``, ``v``, ``g`` fp32 or bf16 [rows, H, N]
+    (one dtype); ``r_k``, ``ln_w``, ``ln_b`` fp32 [H, N].  ``y`` may be ``o``
+    (in place); allocated when None.  Returns ``y``.
+    """
+    rows, H, N = o.shape
+    _need_cuda("o", o, torch.float32, (rows, H, N))
+    xdt = r.dtype
+    if xdt not in (torch.float32, torch.bfloat16):
+        raise TypeError("r, k, v, g must be float32 or bfloat16")
+    for name, t in (("r", r), ("k", k), ("v", v), ("g", g)):
+        _need_cuda(name, t, xdt, (rows, H, N))
+    for name, t in (("r_k", r_k), ("ln_w", ln_w), ("ln_b", ln_b)):
+        _need_cuda(name, t, torch.float32, (H, N))
+    if y is None:
+        y = torch.empty((rows, H, N), device=o.device, dtype=torch.float32)
+    _need_cuda("y", y, torch.float32, (rows, H, N))
+    lib = _lib.load()
+    st = lib.wkv7_tmix_tail(rows, H, N, _lib.BF16 if xdt == torch.bfloat16 else _lib.F32, _ptr(o), _ptr(r), _ptr(k),
+                            _ptr(v), _ptr(g), _ptr(r_k), _ptr(ln_w), _ptr(ln_b), float(eps), _ptr(y),
+                            _stream(stream))
+    _lib.check(st, "wkv7_tmix_tail")
+    return y
 
 
 def prefill_workspace_size(num_seqs: int, T_total: int, H: int, N: int = HEAD_SIZE) -> int:

@@ -27,6 +27,8 @@ BF16 = 1
 
 EXPORTS = (
     "wkv7_step",
+    "wkv7_step_tail",
+    "wkv7_tmix_tail",
     "wkv7_prefill_workspace_size",
     "wkv7_prefill",
     "wkv7_prefill_noalloc",
@@ -50,6 +52,11 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
     lib.wkv7_step.restype = I
     lib.wkv7_step.argtypes = [I, I, I, P, P, P, P, P, P, P, P, P]
+    F = ctypes.c_float
+    lib.wkv7_step_tail.restype = I
+    lib.wkv7_step_tail.argtypes = [I, I, I, P, P, P, P, P, P, P, P, P, P, P, P, F, P, P]
+    lib.wkv7_tmix_tail.restype = I
+    lib.wkv7_tmix_tail.argtypes = [I, I, I, I, P, P, P, P, P, P, P, P, F, P, P]
     lib.wkv7_prefill_workspace_size.restype = S
     lib.wkv7_prefill_workspace_size.argtypes = [I, I, I, I]
     lib.wkv7_prefill.restype = I

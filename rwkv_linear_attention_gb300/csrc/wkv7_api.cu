@@ -1,5 +1,6 @@
 // Host side of the C ABI (include/wkv7.h): argument validation, the
 // per-device status word, and the launches.  No call allocates memory.
+#include <cmath>
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
@@ -99,7 +100,73 @@ wkv7_status wkv7_step(int B, int H, int N, const float *r, const float *w, const
     unsigned *status = nullptr;
     wkv7_status st = status_word(&status);
     if (st != WKV7_OK) return st;
-    cudaError_t e = wkv7::launch_step(heads, r, w, k, v, kk, a, state, o, status, stream);
+    cudaError_t e = wkv7::launch_step(heads, r, w, k, v, kk, a, state, o, nullptr, status, stream);
+    return e == cudaSuccess ? WKV7_OK : cuda_fail(e);
+}
+
+wkv7_status wkv7_step_tail(int B, int H, int N, const float *r, const float *w, const float *k,
+                           const float *v, const float *kk, const float *a, float *state, float *o,
+                           const float *r_k, const float *ln_w, const float *ln_b, const float *g,
+                           float eps, float *y, cudaStream_t stream) {
+    if (N != wkv7::kN) return WKV7_ERR_UNSUPPORTED;
+    if (B < 0 || H <= 0 || !(eps >= 0.f) || !std::isfinite(eps)) return WKV7_ERR_INVALID_ARG;
+    const long long heads = (long long)B * H;
+    if (heads > kMaxHeads) return WKV7_ERR_INVALID_ARG;
+    if (heads == 0) return WKV7_OK;
+    const void *ptrs[12] = {r, w, k, v, kk, a, state, r_k, ln_w, ln_b, g, y};
+    for (const void *p : ptrs)
+        if (!p) return WKV7_ERR_INVALID_ARG;
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return WKV7_ERR_ALIGNMENT;
+    if (o && !aligned16(o)) return WKV7_ERR_ALIGNMENT;
+    const size_t vec_bytes = (size_t)heads * N * sizeof(float);
+    const size_t state_bytes = vec_bytes * N;
+    const size_t par_bytes = (size_t)H * N * sizeof(float);
+    const void *ins[9] = {r, w, k, v, kk, a, g, o, y};
+    for (const void *p : ins)
+        if (overlaps(state, state_bytes, p, vec_bytes)) return WKV7_ERR_INVALID_ARG;
+    for (const float *p : {r_k, ln_w, ln_b})
+        if (overlaps(state, state_bytes, p, par_bytes)) return WKV7_ERR_INVALID_ARG;
+    // the outputs o (when given) and y overlap no input, no parameter and not each other
+    for (const void *out : {(const void *)o, (const void *)y}) {
+        for (int i = 0; i < 7; ++i)
+            if (overlaps(out, vec_bytes, ins[i], vec_bytes)) return WKV7_ERR_INVALID_ARG;
+        for (const float *p : {r_k, ln_w, ln_b})
+            if (overlaps(out, vec_bytes, p, par_bytes)) return WKV7_ERR_INVALID_ARG;
+    }
+    if (overlaps(o, vec_bytes, y, vec_bytes)) return WKV7_ERR_INVALID_ARG;
+    unsigned *status = nullptr;
+    wkv7_status st = status_word(&status);
+    if (st != WKV7_OK) return st;
+    const wkv7::TailArgs tail{r_k, ln_w, ln_b, g, y, eps, H};
+    cudaError_t e = wkv7::launch_step(heads, r, w, k, v, kk, a, state, o, &tail, status, stream);
+    return e == cudaSuccess ? WKV7_OK : cuda_fail(e);
+}
+
+wkv7_status wkv7_tmix_tail(int n_rows, int H, int N, wkv7_dtype x_dtype, const float *o, const void *r,
+                           const void *k, const void *v, const void *g, const float *r_k, const float *ln_w,
+                           const float *ln_b, float eps, float *y, cudaStream_t stream) {
+    if (N != wkv7::kN) return WKV7_ERR_UNSUPPORTED;
+    if (x_dtype != WKV7_F32 && x_dtype != WKV7_BF16) return WKV7_ERR_UNSUPPORTED;
+    if (n_rows < 0 || H <= 0 || !(eps >= 0.f) || !std::isfinite(eps)) return WKV7_ERR_INVALID_ARG;
+    if ((long long)n_rows * H > kMaxHeads * 64) return WKV7_ERR_INVALID_ARG;
+    if (n_rows == 0) return WKV7_OK;
+    const void *ptrs[9] = {o, r, k, v, g, r_k, ln_w, ln_b, y};
+    for (const void *p : ptrs)
+        if (!p) return WKV7_ERR_INVALID_ARG;
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return WKV7_ERR_ALIGNMENT;
+    const size_t x_elem = x_dtype == WKV7_BF16 ? 2 : 4;
+    const size_t elems = (size_t)n_rows * H * N;
+    const size_t par_bytes = (size_t)H * N * sizeof(float);
+    // y may be o itself (in place) but overlaps nothing else
+    if (y != o && overlaps(y, elems * 4, o, elems * 4)) return WKV7_ERR_INVALID_ARG;
+    for (const void *p : {r, k, v, g})
+        if (overlaps(y, elems * 4, p, elems * x_elem)) return WKV7_ERR_INVALID_ARG;
+    for (const float *p : {r_k, ln_w, ln_b})
+        if (overlaps(y, elems * 4, p, par_bytes)) return WKV7_ERR_INVALID_ARG;
+    const wkv7::TailArgs tail{r_k, ln_w, ln_b, g, y, eps, H};
+    cudaError_t e = wkv7::launch_tmix_tail(n_rows, x_dtype, o, r, k, v, tail, stream);
     return e == cudaSuccess ? WKV7_OK : cuda_fail(e);
 }
 

@@ -23,10 +23,27 @@ __device__ __forceinline__ void report(unsigned *status, unsigned bit) {
     if (status) atomicOr(status, bit);
 }
 
-// Decode: one token for n_heads = B * H heads.
+// The time-mix tail after WKV, per (row, head) of N = 64 channels:
+//   y = (GroupNorm_head(o) * ln_w + ln_b + (sum_i r_i k_i rk_i) v) * g
+struct TailArgs {
+    const float *rk;    // [H, 64]
+    const float *ln_w;  // [H, 64]
+    const float *ln_b;  // [H, 64]
+    const void *g;      // [rows, H, 64], the row inputs' type
+    float *y;           // [rows, H, 64] fp32
+    float eps;
+    int H;
+};
+
+// Decode: one token for n_heads = B * H heads; with `tail` the time-mix tail is
+// fused into the epilogue (o may then be null).
 cudaError_t launch_step(long long n_heads, const float *r, const float *w, const float *k,
                         const float *v, const float *kk, const float *a, float *state,
-                        float *o, unsigned *status, cudaStream_t stream);
+                        float *o, const TailArgs *tail, unsigned *status, cudaStream_t stream);
+
+// The time-mix tail over packed rows: o fp32 [n_rows, H, 64]; r, k, v, g of x_dtype.
+cudaError_t launch_tmix_tail(long long n_rows, wkv7_dtype x_dtype, const float *o, const void *r,
+                             const void *k, const void *v, const TailArgs &tail, cudaStream_t stream);
 
 struct PrefillArgs {
     int num_seqs;

@@ -58,12 +58,59 @@ __device__ __forceinline__ float comp(const float4 &x, int c) {
     return c == 0 ? x.x : c == 1 ? x.y : c == 2 ? x.z : x.w;
 }
 
+// The time-mix tail of one head in the decode layout (four warps; lane L of warp w holds
+// key rows row0 .. row0+7 and value columns col .. col+3, and o0..o3 = o[col .. col+3],
+// the same in every row group):
+//   y = (GroupNorm_head(o) * ln_w + ln_b + (sum_i r_i k_i rk_i) v) * g
+// The mean and the variance (two passes) are summed within the warp by shuffles and
+// across the four warps through `red` (8 floats of shared memory, two block barriers;
+// every thread of the block takes part).
+__device__ __forceinline__ float4 tail_epilogue(const TailArgs &t, long long head, int warp, int lane, int row0,
+                                                int col, const float (&rr)[8], const float (&kr)[8],
+                                                const float4 &vv, float o0, float o1, float o2, float o3,
+                                                float *red) {
+    const int hp = static_cast<int>(head % t.H);
+    const float4 rk0 = __ldg(reinterpret_cast<const float4 *>(t.rk + hp * kN + row0));
+    const float4 rk1 = __ldg(reinterpret_cast<const float4 *>(t.rk + hp * kN + row0 + 4));
+    float bonus = 0.f;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        bonus = fmaf(rr[m] * kr[m], comp(rk0, m), bonus);
+        bonus = fmaf(rr[m + 4] * kr[m + 4], comp(rk1, m), bonus);
+    }
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) bonus += __shfl_xor_sync(0xffffffffu, bonus, off);
+    float s1 = (o0 + o1) + (o2 + o3);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+    if (lane == 0) red[warp] = s1;
+    __syncthreads();
+    const float mean = ((red[0] + red[1]) + (red[2] + red[3])) * (1.f / kN);
+    const float d0 = o0 - mean, d1 = o1 - mean, d2 = o2 - mean, d3 = o3 - mean;
+    float s2 = fmaf(d0, d0, fmaf(d1, d1, fmaf(d2, d2, d3 * d3)));
+    s2 += __shfl_xor_sync(0xffffffffu, s2, 1);
+    s2 += __shfl_xor_sync(0xffffffffu, s2, 2);
+    if (lane == 0) red[4 + warp] = s2;
+    __syncthreads();
+    const float var = ((red[4] + red[5]) + (red[6] + red[7])) * (1.f / kN);
+    const float rstd = rsqrtf(var + t.eps);
+    const float4 lw = __ldg(reinterpret_cast<const float4 *>(t.ln_w + hp * kN + col));
+    const float4 lb = __ldg(reinterpret_cast<const float4 *>(t.ln_b + hp * kN + col));
+    const float4 gg = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(t.g) + head * kN + col));
+    return make_float4((fmaf(d0 * rstd, lw.x, lb.x) + bonus * vv.x) * gg.x,
+                       (fmaf(d1 * rstd, lw.y, lb.y) + bonus * vv.y) * gg.y,
+                       (fmaf(d2 * rstd, lw.z, lb.z) + bonus * vv.z) * gg.z,
+                       (fmaf(d3 * rstd, lw.w, lb.w) + bonus * vv.w) * gg.w);
+}
+
+template <bool kTail>
 __global__ void __launch_bounds__(kThreads)
 wkv7_step_kernel(long long n_heads, const float *__restrict__ r, const float *__restrict__ w,
                  const float *__restrict__ k, const float *__restrict__ v,
                  const float *__restrict__ kk, const float *__restrict__ a,
-                 float *__restrict__ state, float *__restrict__ o, unsigned *status) {
+                 float *__restrict__ state, float *__restrict__ o, TailArgs tail, unsigned *status) {
     extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ float red[8];
     Stage *st = reinterpret_cast<Stage *>(smem);
     unsigned long long *full = reinterpret_cast<unsigned long long *>(smem + kStages * sizeof(Stage));
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -170,7 +217,13 @@ wkv7_step_kernel(long long n_heads, const float *__restrict__ r, const float *__
             o2 += __shfl_xor_sync(0xffffffffu, o2, off);
             o3 += __shfl_xor_sync(0xffffffffu, o3, off);
         }
-        if (rg == 0) *reinterpret_cast<float4 *>(o + head * kN + col) = make_float4(o0, o1, o2, o3);
+        if constexpr (kTail) {
+            const float4 y = tail_epilogue(tail, head, warp, lane, row0, col, rr, kr, vv, o0, o1, o2, o3, red);
+            if (rg == 0) *reinterpret_cast<float4 *>(tail.y + head * kN + col) = y;
+            if (o && rg == 0) *reinterpret_cast<float4 *>(o + head * kN + col) = make_float4(o0, o1, o2, o3);
+        } else {
+            if (rg == 0) *reinterpret_cast<float4 *>(o + head * kN + col) = make_float4(o0, o1, o2, o3);
+        }
 
         fence_proxy_async_smem();  // the new state in this stage -> visible to the bulk store
         __syncthreads();
@@ -206,11 +259,13 @@ wkv7_step_kernel(long long n_heads, const float *__restrict__ r, const float *__
 // and it avoids the per-head shared-memory round trip of the ring above.
 constexpr int kRegWarps = 4;
 
+template <bool kTail>
 __global__ void __launch_bounds__(kRegWarps * 32)
 wkv7_step_regs_kernel(long long n_units, const float *__restrict__ r, const float *__restrict__ w,
                       const float *__restrict__ k, const float *__restrict__ v,
                       const float *__restrict__ kk, const float *__restrict__ a,
-                      float *__restrict__ state, float *__restrict__ o) {
+                      float *__restrict__ state, float *__restrict__ o, TailArgs tail) {
+    __shared__ float red[8];  // a block is the four slices of one head
     grid_dep_wait();
     const int lane = threadIdx.x & 31;
     const long long unit = static_cast<long long>(blockIdx.x) * kRegWarps + (threadIdx.x >> 5);
@@ -277,14 +332,21 @@ wkv7_step_regs_kernel(long long n_units, const float *__restrict__ r, const floa
         o2 += __shfl_xor_sync(0xffffffffu, o2, off);
         o3 += __shfl_xor_sync(0xffffffffu, o3, off);
     }
-    if (rg == 0) *reinterpret_cast<float4 *>(o + head * kN + col) = make_float4(o0, o1, o2, o3);
+    if constexpr (kTail) {
+        const float4 y = tail_epilogue(tail, head, slice, lane, row0, col, rr, kr, vv, o0, o1, o2, o3, red);
+        if (rg == 0) *reinterpret_cast<float4 *>(tail.y + head * kN + col) = y;
+        if (o && rg == 0) *reinterpret_cast<float4 *>(o + head * kN + col) = make_float4(o0, o1, o2, o3);
+    } else {
+        if (rg == 0) *reinterpret_cast<float4 *>(o + head * kN + col) = make_float4(o0, o1, o2, o3);
+    }
 }
 
 // Head count from which the register form is used (several full waves).
 constexpr long long kRegsFromHeads = 8192;
 
 struct LaunchShape {
-    int grid_cap = 0;  // CTAs per wave (SMs x resident CTAs per SM)
+    int grid_cap = 0;       // CTAs per wave (SMs x resident CTAs per SM)
+    int grid_cap_tail = 0;  // the same for the form with the fused tail
 };
 
 LaunchShape shape_for_device() {
@@ -295,12 +357,18 @@ LaunchShape shape_for_device() {
     if (dev == cached_dev) return cached;
     LaunchShape s;
     int sms = 0, per_sm = 0;
-    if (cudaFuncSetAttribute(wkv7_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    int per_sm_tail = 0;
+    if (cudaFuncSetAttribute(wkv7_step_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes)) != cudaSuccess ||
+        cudaFuncSetAttribute(wkv7_step_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmemBytes)) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, wkv7_step_kernel, kThreads, kSmemBytes) !=
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, wkv7_step_kernel<false>, kThreads, kSmemBytes) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_tail, wkv7_step_kernel<true>, kThreads, kSmemBytes) !=
             cudaSuccess)
         return LaunchShape{};
+    s.grid_cap_tail = sms * (per_sm_tail > 0 ? per_sm_tail : 1);
     s.grid_cap = sms * (per_sm > 0 ? per_sm : 1);
     cached = s;
     cached_dev = dev;
@@ -311,7 +379,8 @@ LaunchShape shape_for_device() {
 
 cudaError_t launch_step(long long n_heads, const float *r, const float *w, const float *k,
                         const float *v, const float *kk, const float *a, float *state,
-                        float *o, unsigned *status, cudaStream_t stream) {
+                        float *o, const TailArgs *tail, unsigned *status, cudaStream_t stream) {
+    const TailArgs t = tail ? *tail : TailArgs{};
     if (n_heads <= 0) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
     cfg.stream = stream;
@@ -324,15 +393,18 @@ cudaError_t launch_step(long long n_heads, const float *r, const float *w, const
         const long long units = n_heads * 4;
         cfg.gridDim = dim3(static_cast<unsigned>((units + kRegWarps - 1) / kRegWarps));
         cfg.blockDim = dim3(kRegWarps * 32);
-        return cudaLaunchKernelEx(&cfg, wkv7_step_regs_kernel, units, r, w, k, v, kk, a, state, o);
+        if (tail) return cudaLaunchKernelEx(&cfg, wkv7_step_regs_kernel<true>, units, r, w, k, v, kk, a, state, o, t);
+        return cudaLaunchKernelEx(&cfg, wkv7_step_regs_kernel<false>, units, r, w, k, v, kk, a, state, o, t);
     }
     const LaunchShape shape = shape_for_device();
     if (shape.grid_cap <= 0) return cudaErrorInvalidDevice;
-    const long long grid = n_heads < shape.grid_cap ? n_heads : shape.grid_cap;
+    const long long cap = tail ? shape.grid_cap_tail : shape.grid_cap;
+    const long long grid = n_heads < cap ? n_heads : cap;
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
-    return cudaLaunchKernelEx(&cfg, wkv7_step_kernel, n_heads, r, w, k, v, kk, a, state, o, status);
+    if (tail) return cudaLaunchKernelEx(&cfg, wkv7_step_kernel<true>, n_heads, r, w, k, v, kk, a, state, o, t, status);
+    return cudaLaunchKernelEx(&cfg, wkv7_step_kernel<false>, n_heads, r, w, k, v, kk, a, state, o, t, status);
 }
 
 }  // namespace wkv7
