@@ -33,6 +33,10 @@ N_HEAD = 64
 STATE_BYTES = 2 * 4 * N_HEAD * N_HEAD           # state read + write per head-step
 STEP_BYTES = STATE_BYTES + 6 * 4 * N_HEAD + 4 * N_HEAD  # + six input vectors + o = 34,560
 PREFILL_BYTES_PER_TOKEN_HEAD = 5 * 2 * N_HEAD + 4 * N_HEAD + 4 * N_HEAD  # bf16 r,k,v,kk,a; fp32 w, o = 1,152
+# decode step with the fused time-mix tail: o not written, the gate g read, y written = 34,816
+TAIL_STEP_BYTES = STEP_BYTES - 4 * N_HEAD + 4 * N_HEAD + 4 * N_HEAD
+# the tail over packed rows, bf16 row inputs: o fp32 in, r, k, v, g bf16 in, y fp32 out = 1,024
+ROW_TAIL_BYTES_BF16 = 4 * N_HEAD + 4 * 2 * N_HEAD + 4 * N_HEAD
 PREFILL_FLOP_PER_TOKEN_HEAD = 26 * N_HEAD * N_HEAD  # chunked form, C = N = 64: 106,496
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 * 1024 * 1024
@@ -181,7 +185,7 @@ NAMES = ("r", "w", "k", "v", "kk", "a")
 class DecodeWorkload:
     """32 layer slabs of state, a pool of input sets per layer, per-layer o."""
 
-    def __init__(self, layers, B, H, pool, dev, seed):
+    def __init__(self, layers, B, H, pool, dev, seed, tail=False):
         import torch
 
         from rwkv_linear_attention_gb300 import inputs
@@ -193,12 +197,23 @@ class DecodeWorkload:
         self.pool = {n: x[n].contiguous() for n in NAMES}
         self.state = torch.zeros(layers, B, H, N_HEAD, N_HEAD, device=dev)
         self.o = torch.empty(layers, B, H, N_HEAD, device=dev)
+        self.tail = tail
+        if tail:  # the time-mix tail fused into the step: per-layer parameters, per-token gates, y out
+            gen = torch.Generator(device=dev).manual_seed(seed + 1)
+            self.rk, self.ln_w, self.ln_b = (torch.randn(layers, H, N_HEAD, generator=gen, device=dev)
+                                             for _ in range(3))
+            self.gate = torch.sigmoid(torch.randn(pool, layers, B, H, N_HEAD, generator=gen, device=dev))
+            self.y = torch.empty(layers, B, H, N_HEAD, device=dev)
 
     def launch_step(self, p, src=None):
         import rwkv_linear_attention_gb300 as wkv7
         src = src or {n: self.pool[n][p] for n in NAMES}
         for layer in range(self.layers):
-            wkv7.step(*(src[n][layer] for n in NAMES), self.state[layer], self.o[layer])
+            if self.tail:
+                wkv7.step_tail(*(src[n][layer] for n in NAMES), self.state[layer], self.rk[layer],
+                               self.ln_w[layer], self.ln_b[layer], self.gate[p][layer], 64e-5, y=self.y[layer])
+            else:
+                wkv7.step(*(src[n][layer] for n in NAMES), self.state[layer], self.o[layer])
 
     def warm(self, steps):
         for s in range(steps):
@@ -349,6 +364,37 @@ def run_configs(args, dev, peaks):
                           "achieved_gbs": round(gbs, 1), "frac": round(gbs / hbm, 4)}), flush=True)
         del graphs, wl
         torch.cuda.empty_cache()
+    # decode with the time-mix tail fused (o not written; g read, y written)
+    wl = DecodeWorkload(inputs.DECODE_2P9B["layers"], 32, inputs.DECODE_2P9B["H"], 4, dev, seed=7, tail=True)
+    graphs = wl.capture(stream)
+    steps = max(8, args.steps)
+    ms = time_graphs(graphs, steps, args.warmup, stream, 1) / steps
+    launch_us = ms * 1e3 / wl.layers
+    gbs = wl.B * wl.H * TAIL_STEP_BYTES / (launch_us * 1e-6) / 1e9
+    print(json.dumps({"workload": "decode 2.9B B=32 + fused time-mix tail", "us_per_launch": round(launch_us, 3),
+                      "achieved_gbs": round(gbs, 1), "frac": round(gbs / hbm, 4),
+                      "bytes_per_head_step": TAIL_STEP_BYTES}), flush=True)
+    del graphs, wl
+    torch.cuda.empty_cache()
+    # the time-mix tail over a prefill's outputs: 2.9B 8 x 4096 tokens, bf16 row inputs
+    rows, H = 8 * 4096, 40
+    gen = torch.Generator(device=dev).manual_seed(9)
+    o = torch.randn(rows, H, N_HEAD, generator=gen, device=dev)
+    r, k, v, gate = (torch.randn(rows, H, N_HEAD, generator=gen, device=dev).to(torch.bfloat16) for _ in range(4))
+    rk, ln_w, ln_b = (torch.randn(H, N_HEAD, generator=gen, device=dev) for _ in range(3))
+    y = torch.empty_like(o)
+
+    def tail_call():
+        wkv7.tmix_tail(o, r, k, v, gate, rk, ln_w, ln_b, 64e-5, y=y, stream=stream)
+    ms = time_stream(tail_call, 20, 3, stream)
+    wkv7.check_device_status(stream)
+    nbytes = rows * H * ROW_TAIL_BYTES_BF16
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    print(json.dumps({"workload": "time-mix tail over 2.9B prefill outputs (32768 x 40 rows, bf16 r,k,v,g)",
+                      "ms_per_call": round(ms, 4), "achieved_gbs": round(gbs, 1), "frac": round(gbs / hbm, 4),
+                      "bytes_per_row_head": ROW_TAIL_BYTES_BF16}), flush=True)
+    del o, r, k, v, gate, y
+    torch.cuda.empty_cache()
     # prefill: 2.9B 8 x 4096; 7.2B varlen (16 x U[1, 32768]); 7.2B single 32768
     v = inputs.VARLEN_7P2B
     cases = [("prefill 2.9B 8x4096", [4096] * 8, 40, False),

@@ -47,12 +47,18 @@ constexpr uint32_t kStateBytes = kN * kN * 4;  // 16 KB
 constexpr uint32_t kVecBytes = kN * 4;         // 256 B
 constexpr uint32_t kMaxPolls = 1u << 24;
 
+// One ring stage: a head's state and its vectors r, w, k, v, kk, a; with the fused
+// time-mix tail also its gate g and the head's r_k, ln_w, ln_b.
+template <bool kTail>
 struct Stage {
+    static constexpr int kVecs = kTail ? 10 : 6;
     float S[kN * kN];
-    float vec[6][kN];  // r, w, k, v, kk, a
+    float vec[kVecs][kN];
 };
-static_assert(sizeof(Stage) % 128 == 0, "stage size");
-constexpr size_t kSmemBytes = kStages * sizeof(Stage) + kStages * sizeof(unsigned long long);
+static_assert(sizeof(Stage<false>) % 128 == 0 && sizeof(Stage<true>) % 128 == 0, "stage size");
+template <bool kTail>
+constexpr size_t kSmemBytesT = kStages * sizeof(Stage<kTail>) + kStages * sizeof(unsigned long long);
+constexpr size_t kSmemBytes = kSmemBytesT<false>;
 
 __device__ __forceinline__ float comp(const float4 &x, int c) {
     return c == 0 ? x.x : c == 1 ? x.y : c == 2 ? x.z : x.w;
@@ -62,16 +68,14 @@ __device__ __forceinline__ float comp(const float4 &x, int c) {
 // key rows row0 .. row0+7 and value columns col .. col+3, and o0..o3 = o[col .. col+3],
 // the same in every row group):
 //   y = (GroupNorm_head(o) * ln_w + ln_b + (sum_i r_i k_i rk_i) v) * g
-// The mean and the variance (two passes) are summed within the warp by shuffles and
-// across the four warps through `red` (8 floats of shared memory, two block barriers;
-// every thread of the block takes part).
-__device__ __forceinline__ float4 tail_epilogue(const TailArgs &t, long long head, int warp, int lane, int row0,
-                                                int col, const float (&rr)[8], const float (&kr)[8],
-                                                const float4 &vv, float o0, float o1, float o2, float o3,
-                                                float *red) {
-    const int hp = static_cast<int>(head % t.H);
-    const float4 rk0 = __ldg(reinterpret_cast<const float4 *>(t.rk + hp * kN + row0));
-    const float4 rk1 = __ldg(reinterpret_cast<const float4 *>(t.rk + hp * kN + row0 + 4));
+// In two halves around a block barrier.  tail_stats: the bonus (rk0, rk1 = r_k at rows
+// row0 .. row0+7) by shuffles over the row groups, and this warp's mean and centred sum
+// of squares over its 16 columns into red[warp], red[4 + warp].  tail_apply, after the
+// barrier: the four merged (mean of means, plus 16 (m_w - m)^2 per warp), then y at
+// columns col .. col+3 from ln_w (w4), ln_b (b4) and the gate (g4).
+__device__ __forceinline__ float tail_stats(const float4 &rk0, const float4 &rk1, int warp, int lane,
+                                            const float (&rr)[8], const float (&kr)[8], float o0, float o1,
+                                            float o2, float o3, float *red) {
     float bonus = 0.f;
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
@@ -83,24 +87,31 @@ __device__ __forceinline__ float4 tail_epilogue(const TailArgs &t, long long hea
     float s1 = (o0 + o1) + (o2 + o3);
     s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
     s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
-    if (lane == 0) red[warp] = s1;
-    __syncthreads();
-    const float mean = ((red[0] + red[1]) + (red[2] + red[3])) * (1.f / kN);
+    const float mw = s1 * (1.f / 16);
+    const float e0 = o0 - mw, e1 = o1 - mw, e2 = o2 - mw, e3 = o3 - mw;
+    float q = fmaf(e0, e0, fmaf(e1, e1, fmaf(e2, e2, e3 * e3)));
+    q += __shfl_xor_sync(0xffffffffu, q, 1);
+    q += __shfl_xor_sync(0xffffffffu, q, 2);
+    if (lane == 0) {
+        red[warp] = mw;
+        red[4 + warp] = q;
+    }
+    return bonus;
+}
+
+__device__ __forceinline__ float4 tail_apply(const float *red, float eps, float bonus, const float4 &w4,
+                                             const float4 &b4, const float4 &g4, const float4 &vv, float o0,
+                                             float o1, float o2, float o3) {
+    const float m0 = red[0], m1 = red[1], m2 = red[2], m3 = red[3];
+    const float mean = ((m0 + m1) + (m2 + m3)) * 0.25f;
+    const float a0 = m0 - mean, a1 = m1 - mean, a2 = m2 - mean, a3 = m3 - mean;
+    const float M2 = ((red[4] + red[5]) + (red[6] + red[7])) + 16.f * fmaf(a0, a0, fmaf(a1, a1, fmaf(a2, a2, a3 * a3)));
+    const float rstd = rsqrtf(M2 * (1.f / kN) + eps);
     const float d0 = o0 - mean, d1 = o1 - mean, d2 = o2 - mean, d3 = o3 - mean;
-    float s2 = fmaf(d0, d0, fmaf(d1, d1, fmaf(d2, d2, d3 * d3)));
-    s2 += __shfl_xor_sync(0xffffffffu, s2, 1);
-    s2 += __shfl_xor_sync(0xffffffffu, s2, 2);
-    if (lane == 0) red[4 + warp] = s2;
-    __syncthreads();
-    const float var = ((red[4] + red[5]) + (red[6] + red[7])) * (1.f / kN);
-    const float rstd = rsqrtf(var + t.eps);
-    const float4 lw = __ldg(reinterpret_cast<const float4 *>(t.ln_w + hp * kN + col));
-    const float4 lb = __ldg(reinterpret_cast<const float4 *>(t.ln_b + hp * kN + col));
-    const float4 gg = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(t.g) + head * kN + col));
-    return make_float4((fmaf(d0 * rstd, lw.x, lb.x) + bonus * vv.x) * gg.x,
-                       (fmaf(d1 * rstd, lw.y, lb.y) + bonus * vv.y) * gg.y,
-                       (fmaf(d2 * rstd, lw.z, lb.z) + bonus * vv.z) * gg.z,
-                       (fmaf(d3 * rstd, lw.w, lb.w) + bonus * vv.w) * gg.w);
+    return make_float4((fmaf(d0 * rstd, w4.x, b4.x) + bonus * vv.x) * g4.x,
+                       (fmaf(d1 * rstd, w4.y, b4.y) + bonus * vv.y) * g4.y,
+                       (fmaf(d2 * rstd, w4.z, b4.z) + bonus * vv.z) * g4.z,
+                       (fmaf(d3 * rstd, w4.w, b4.w) + bonus * vv.w) * g4.w);
 }
 
 template <bool kTail>
@@ -110,9 +121,10 @@ wkv7_step_kernel(long long n_heads, const float *__restrict__ r, const float *__
                  const float *__restrict__ kk, const float *__restrict__ a,
                  float *__restrict__ state, float *__restrict__ o, TailArgs tail, unsigned *status) {
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ float red[8];
-    Stage *st = reinterpret_cast<Stage *>(smem);
-    unsigned long long *full = reinterpret_cast<unsigned long long *>(smem + kStages * sizeof(Stage));
+    __shared__ float red[2][8];  // the tail's statistics, double-buffered across heads
+    using StageX = Stage<kTail>;
+    StageX *st = reinterpret_cast<StageX *>(smem);
+    unsigned long long *full = reinterpret_cast<unsigned long long *>(smem + kStages * sizeof(StageX));
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     // Nothing in global memory is touched before the preceding grid is done.
@@ -125,10 +137,17 @@ wkv7_step_kernel(long long n_heads, const float *__restrict__ r, const float *__
         const long long head = first + idx * stride;
         const int s = static_cast<int>(idx % kStages);
         const uint32_t bar = smem_addr(&full[s]);
-        mbar_arrive_expect_tx(bar, kStateBytes + 6 * kVecBytes);
+        mbar_arrive_expect_tx(bar, kStateBytes + StageX::kVecs * kVecBytes);
         bulk_load(smem_addr(st[s].S), state + head * (kN * kN), kStateBytes, bar);
 #pragma unroll
         for (int i = 0; i < 6; ++i) bulk_load(smem_addr(st[s].vec[i]), vsrc[i] + head * kN, kVecBytes, bar);
+        if constexpr (kTail) {
+            const long long hp = head % tail.H;
+            bulk_load(smem_addr(st[s].vec[6]), static_cast<const float *>(tail.g) + head * kN, kVecBytes, bar);
+            bulk_load(smem_addr(st[s].vec[7]), tail.rk + hp * kN, kVecBytes, bar);
+            bulk_load(smem_addr(st[s].vec[8]), tail.ln_w + hp * kN, kVecBytes, bar);
+            bulk_load(smem_addr(st[s].vec[9]), tail.ln_b + hp * kN, kVecBytes, bar);
+        }
     };
     // thread 0 sets up the barriers and starts the first loads before the block syncs
     long long issued = 0;
@@ -153,7 +172,7 @@ wkv7_step_kernel(long long n_heads, const float *__restrict__ r, const float *__
             break;
         }
         const long long head = first + idx * stride;
-        Stage &S = st[s];
+        StageX &S = st[s];
 
         float4 x[8];
 #pragma unroll
@@ -217,16 +236,24 @@ wkv7_step_kernel(long long n_heads, const float *__restrict__ r, const float *__
             o2 += __shfl_xor_sync(0xffffffffu, o2, off);
             o3 += __shfl_xor_sync(0xffffffffu, o3, off);
         }
+        float bonus = 0.f;
         if constexpr (kTail) {
-            const float4 y = tail_epilogue(tail, head, warp, lane, row0, col, rr, kr, vv, o0, o1, o2, o3, red);
-            if (rg == 0) *reinterpret_cast<float4 *>(tail.y + head * kN + col) = y;
+            bonus = tail_stats(*reinterpret_cast<const float4 *>(&S.vec[7][row0]),
+                               *reinterpret_cast<const float4 *>(&S.vec[7][row0 + 4]), warp, lane, rr, kr, o0, o1,
+                               o2, o3, red[idx & 1]);
             if (o && rg == 0) *reinterpret_cast<float4 *>(o + head * kN + col) = make_float4(o0, o1, o2, o3);
         } else {
             if (rg == 0) *reinterpret_cast<float4 *>(o + head * kN + col) = make_float4(o0, o1, o2, o3);
         }
 
         fence_proxy_async_smem();  // the new state in this stage -> visible to the bulk store
-        __syncthreads();
+        __syncthreads();           // (and the tail's statistics of every warp)
+        if constexpr (kTail) {
+            const float4 y = tail_apply(red[idx & 1], tail.eps, bonus, *reinterpret_cast<const float4 *>(&S.vec[8][col]),
+                                        *reinterpret_cast<const float4 *>(&S.vec[9][col]),
+                                        *reinterpret_cast<const float4 *>(&S.vec[6][col]), vv, o0, o1, o2, o3);
+            if (rg == 0) *reinterpret_cast<float4 *>(tail.y + head * kN + col) = y;
+        }
         if (tid == 0) {
             bulk_store(state + head * (kN * kN), smem_addr(S.S), kStateBytes);
             bulk_commit();
@@ -286,6 +313,16 @@ wkv7_step_regs_kernel(long long n_units, const float *__restrict__ r, const floa
     const float4 kk0 = __ldg(reinterpret_cast<const float4 *>(kk + vb)), kk1 = __ldg(reinterpret_cast<const float4 *>(kk + vb + 4));
     const float4 a0 = __ldg(reinterpret_cast<const float4 *>(a + vb)), a1 = __ldg(reinterpret_cast<const float4 *>(a + vb + 4));
     const float4 vv = __ldg(reinterpret_cast<const float4 *>(v + head * kN + col));
+    // the tail's vectors, fetched now so that their latency hides behind the state math
+    float4 pre[5];
+    if constexpr (kTail) {
+        const long long hp = head % tail.H;
+        pre[0] = __ldg(reinterpret_cast<const float4 *>(tail.rk + hp * kN + row0));
+        pre[1] = __ldg(reinterpret_cast<const float4 *>(tail.rk + hp * kN + row0 + 4));
+        pre[2] = __ldg(reinterpret_cast<const float4 *>(tail.ln_w + hp * kN + col));
+        pre[3] = __ldg(reinterpret_cast<const float4 *>(tail.ln_b + hp * kN + col));
+        pre[4] = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(tail.g) + head * kN + col));
+    }
     float kkr[8], kr[8], rr[8], dr[8], cr[8];
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
@@ -333,7 +370,9 @@ wkv7_step_regs_kernel(long long n_units, const float *__restrict__ r, const floa
         o3 += __shfl_xor_sync(0xffffffffu, o3, off);
     }
     if constexpr (kTail) {
-        const float4 y = tail_epilogue(tail, head, slice, lane, row0, col, rr, kr, vv, o0, o1, o2, o3, red);
+        const float bonus = tail_stats(pre[0], pre[1], slice, lane, rr, kr, o0, o1, o2, o3, red);
+        __syncthreads();
+        const float4 y = tail_apply(red, tail.eps, bonus, pre[2], pre[3], pre[4], vv, o0, o1, o2, o3);
         if (rg == 0) *reinterpret_cast<float4 *>(tail.y + head * kN + col) = y;
         if (o && rg == 0) *reinterpret_cast<float4 *>(o + head * kN + col) = make_float4(o0, o1, o2, o3);
     } else {
@@ -361,12 +400,12 @@ LaunchShape shape_for_device() {
     if (cudaFuncSetAttribute(wkv7_step_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmemBytes)) != cudaSuccess ||
         cudaFuncSetAttribute(wkv7_step_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmemBytes)) != cudaSuccess ||
+                             static_cast<int>(kSmemBytesT<true>)) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, wkv7_step_kernel<false>, kThreads, kSmemBytes) !=
             cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_tail, wkv7_step_kernel<true>, kThreads, kSmemBytes) !=
-            cudaSuccess)
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_tail, wkv7_step_kernel<true>, kThreads,
+                                                      kSmemBytesT<true>) != cudaSuccess)
         return LaunchShape{};
     s.grid_cap_tail = sms * (per_sm_tail > 0 ? per_sm_tail : 1);
     s.grid_cap = sms * (per_sm > 0 ? per_sm : 1);
@@ -402,7 +441,7 @@ cudaError_t launch_step(long long n_heads, const float *r, const float *w, const
     const long long grid = n_heads < cap ? n_heads : cap;
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = tail ? kSmemBytesT<true> : kSmemBytes;
     if (tail) return cudaLaunchKernelEx(&cfg, wkv7_step_kernel<true>, n_heads, r, w, k, v, kk, a, state, o, t, status);
     return cudaLaunchKernelEx(&cfg, wkv7_step_kernel<false>, n_heads, r, w, k, v, kk, a, state, o, t, status);
 }
