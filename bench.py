@@ -35,6 +35,13 @@ STEP_BYTES = STATE_BYTES + 6 * 4 * N_HEAD + 4 * N_HEAD  # + six input vectors + 
 PREFILL_BYTES_PER_TOKEN_HEAD = 5 * 2 * N_HEAD + 4 * N_HEAD + 4 * N_HEAD  # bf16 r,k,v,kk,a; fp32 w, o = 1,152
 # decode step with the fused time-mix tail: o not written, the gate g read, y written = 34,816
 TAIL_STEP_BYTES = STEP_BYTES - 4 * N_HEAD + 4 * N_HEAD + 4 * N_HEAD
+# multi-token verify of T tokens: state read once, per position six input vectors, o and the
+# position's state written; the rollback reads the accepted state and writes the state
+def VERIFY_BYTES(T):
+    return 4 * N_HEAD * N_HEAD + T * (6 * 4 * N_HEAD + 4 * N_HEAD + 4 * N_HEAD * N_HEAD)
+
+
+COMMIT_BYTES = 2 * 4 * N_HEAD * N_HEAD
 # the tail over packed rows, bf16 row inputs: o fp32 in, r, k, v, g bf16 in, y fp32 out = 1,024
 ROW_TAIL_BYTES_BF16 = 4 * N_HEAD + 4 * 2 * N_HEAD + 4 * N_HEAD
 PREFILL_FLOP_PER_TOKEN_HEAD = 26 * N_HEAD * N_HEAD  # chunked form, C = N = 64: 106,496
@@ -376,6 +383,36 @@ def run_configs(args, dev, peaks):
                       "bytes_per_head_step": TAIL_STEP_BYTES}), flush=True)
     del graphs, wl
     torch.cuda.empty_cache()
+    # speculative verify + rollback (2.9B geometry, 32 layers): T = K + 1 tokens per row from
+    # the state, every position's state kept, then each row rolled to its accepted length
+    # (here all T: the largest commit).  3 drafts for <= 4 streams, 2 for <= 16.
+    for B, T in ((4, 4), (16, 3)):
+        H, L = inputs.DECODE_2P9B["H"], inputs.DECODE_2P9B["layers"]
+        x = inputs.draw_rwkkva((L, B, T, H, N_HEAD), seed=21, device=dev)
+        x = {n: x[n].contiguous() for n in NAMES}
+        state = torch.zeros(L, B, H, N_HEAD, N_HEAD, device=dev)
+        o = torch.empty(B, T, H, N_HEAD, device=dev)
+        states = torch.empty(T, B, H, N_HEAD, N_HEAD, device=dev)
+        acc = torch.full((B,), T, dtype=torch.int32, device=dev)
+
+        def verify_step():
+            for layer in range(L):
+                wkv7.verify(*(x[n][layer] for n in NAMES), state[layer], o=o, states=states, stream=stream)
+                wkv7.verify_commit(states, acc, state[layer], stream=stream)
+        g = torch.cuda.CUDAGraph()
+        verify_step()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            verify_step()
+        steps = max(8, args.steps // 8)
+        ms = time_graphs([g], steps, args.warmup, stream, 1) / steps
+        per_head = VERIFY_BYTES(T) + COMMIT_BYTES
+        gbs = L * B * H * per_head / (ms * 1e-3) / 1e9
+        print(json.dumps({"workload": f"verify 2.9B B={B} T={T} (+ rollback), 32 layers", "ms_per_step": round(ms, 4),
+                          "us_per_layer": round(ms * 1e3 / L, 3), "achieved_gbs": round(gbs, 1),
+                          "frac": round(gbs / hbm, 4), "bytes_per_head": per_head}), flush=True)
+        del g, x, state, o, states
+        torch.cuda.empty_cache()
     # the time-mix tail over a prefill's outputs: 2.9B 8 x 4096 tokens, bf16 row inputs
     rows, H = 8 * 4096, 40
     gen = torch.Generator(device=dev).manual_seed(9)

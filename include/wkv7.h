@@ -139,6 +139,38 @@ WKV7_API wkv7_status wkv7_tmix_tail(int n_rows, int H, int N, wkv7_dtype x_dtype
                       const float *ln_b, float eps, float *y, cudaStream_t stream);
 
 /*
+ * wkv7_verify -- the recurrence over T = K + 1 tokens per row from a read-only
+ * state, keeping every position's state: the WKV part of one speculative step
+ * of the RWKV-Infer-Next page ("Inference. One speculative step": the base
+ * model processes [t, d1 .. dK] in one forward, the sampler accepts the drafts
+ * up to the first mismatch, the recurrent state is rolled back to the accepted
+ * prefix).  For each row b, head h and position t = 0 .. T-1:
+ *     S_{-1} = state[b, h] ;  S_t = step(S_{t-1}, x[b, t, h]) ;  o[b, t, h] = S_t^T r[b, t, h]
+ *
+ *   T                  : 1 .. 8 tokens per row (K = T - 1 drafts)
+ *   r, w, k, v, kk, a  : fp32 [B, T, H, N]
+ *   state              : fp32 [B, H, N, N]     read only
+ *   o                  : fp32 [B, T, H, N]
+ *   states             : fp32 [T, B, H, N, N]  states[t] = S_t of every (row, head):
+ *                        states[t] has the layout of `state`, so a batch that
+ *                        accepts the same length everywhere can use it as is
+ * o and states overlap no input and not each other (WKV7_ERR_INVALID_ARG).
+ *
+ * wkv7_verify_commit -- the rollback: state[b] = states[accept_len[b] - 1][b]
+ * for every head, or unchanged when accept_len[b] = 0.  accept_len is a DEVICE
+ * int32 [B] (written by the sampler, so no host round trip is needed); a value
+ * outside 0 .. T leaves that row unchanged and is reported by
+ * wkv7_check_device_status (WKV7_ERR_DEVICE_BOUNDS).  The pages have no
+ * separate rollback call; it completes wkv7_verify's per-position states.
+ */
+WKV7_API wkv7_status wkv7_verify(int B, int T, int H, int N,
+                      const float *r, const float *w, const float *k,
+                      const float *v, const float *kk, const float *a,
+                      const float *state, float *o, float *states, cudaStream_t stream);
+WKV7_API wkv7_status wkv7_verify_commit(int B, int T, int H, int N, const float *states,
+                      const int32_t *accept_len, float *state, cudaStream_t stream);
+
+/*
  * wkv7_prefill_workspace_size -- bytes of device workspace with which
  * wkv7_prefill can use every schedule for this shape (may be 0; the result
  * depends only on the arguments).  It holds:

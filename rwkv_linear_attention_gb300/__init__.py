@@ -24,7 +24,7 @@ import torch
 from . import _lib
 from ._lib import WKV7Error  # noqa: F401
 
-__all__ = ["step", "step_tail", "tmix_tail", "prefill", "prefill_workspace_size", "check_device_status",
+__all__ = ["step", "step_tail", "tmix_tail", "verify", "verify_commit", "prefill", "prefill_workspace_size", "check_device_status",
            "WKV7Error", "HEAD_SIZE"]
 
 HEAD_SIZE = 64
@@ -122,6 +122,40 @@ def tmix_tail(o, r, k, v, g, r_k, ln_w, ln_b, eps, y=None, stream=None):
                             _stream(stream))
     _lib.check(st, "wkv7_tmix_tail")
     return y
+
+
+def verify(r, w, k, v, kk, a, state, o=None, states=None, stream=None):
+    """T tokens per row from a read-only state, keeping every position's state
+    (the WKV part of a speculative step).  Inputs fp32 [B, T, H, N] (T <= 8);
+    ``state`` fp32 [B, H, N, N] (not modified).  Returns ``(o [B, T, H, N],
+    states [T, B, H, N, N])``.  Roll back with :func:`verify_commit`."""
+    B, T, H, N = r.shape
+    for name, t in (("r", r), ("w", w), ("k", k), ("v", v), ("kk", kk), ("a", a)):
+        _need_cuda(name, t, torch.float32, (B, T, H, N))
+    _need_cuda("state", state, torch.float32, (B, H, N, N))
+    if o is None:
+        o = torch.empty((B, T, H, N), device=r.device, dtype=torch.float32)
+    if states is None:
+        states = torch.empty((T, B, H, N, N), device=r.device, dtype=torch.float32)
+    _need_cuda("o", o, torch.float32, (B, T, H, N))
+    _need_cuda("states", states, torch.float32, (T, B, H, N, N))
+    st = _lib.load().wkv7_verify(B, T, H, N, _ptr(r), _ptr(w), _ptr(k), _ptr(v), _ptr(kk), _ptr(a), _ptr(state),
+                                 _ptr(o), _ptr(states), _stream(stream))
+    _lib.check(st, "wkv7_verify")
+    return o, states
+
+
+def verify_commit(states, accept_len, state, stream=None):
+    """Roll ``state`` [B, H, N, N] forward to each row's accepted length:
+    ``state[b] = states[accept_len[b] - 1, b]`` (unchanged for 0).
+    ``accept_len``: int32 CUDA [B]."""
+    T, B, H, N, _ = states.shape
+    _need_cuda("states", states, torch.float32, (T, B, H, N, N))
+    _need_cuda("accept_len", accept_len, torch.int32, (B,))
+    _need_cuda("state", state, torch.float32, (B, H, N, N))
+    st = _lib.load().wkv7_verify_commit(B, T, H, N, _ptr(states), _ptr(accept_len), _ptr(state), _stream(stream))
+    _lib.check(st, "wkv7_verify_commit")
+    return state
 
 
 def prefill_workspace_size(num_seqs: int, T_total: int, H: int, N: int = HEAD_SIZE) -> int:

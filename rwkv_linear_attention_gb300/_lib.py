@@ -29,6 +29,8 @@ EXPORTS = (
     "wkv7_step",
     "wkv7_step_tail",
     "wkv7_tmix_tail",
+    "wkv7_verify",
+    "wkv7_verify_commit",
     "wkv7_prefill_workspace_size",
     "wkv7_prefill",
     "wkv7_prefill_noalloc",
@@ -55,6 +57,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     F = ctypes.c_float
     lib.wkv7_step_tail.restype = I
     lib.wkv7_step_tail.argtypes = [I, I, I, P, P, P, P, P, P, P, P, P, P, P, P, F, P, P]
+    lib.wkv7_verify.restype = I
+    lib.wkv7_verify.argtypes = [I, I, I, I, P, P, P, P, P, P, P, P, P, P]
+    lib.wkv7_verify_commit.restype = I
+    lib.wkv7_verify_commit.argtypes = [I, I, I, I, P, P, P, P]
     lib.wkv7_tmix_tail.restype = I
     lib.wkv7_tmix_tail.argtypes = [I, I, I, I, P, P, P, P, P, P, P, P, F, P, P]
     lib.wkv7_prefill_workspace_size.restype = S

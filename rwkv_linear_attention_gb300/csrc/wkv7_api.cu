@@ -143,6 +143,57 @@ wkv7_status wkv7_step_tail(int B, int H, int N, const float *r, const float *w, 
     return e == cudaSuccess ? WKV7_OK : cuda_fail(e);
 }
 
+wkv7_status wkv7_verify(int B, int T, int H, int N, const float *r, const float *w, const float *k, const float *v,
+                        const float *kk, const float *a, const float *state, float *o, float *states,
+                        cudaStream_t stream) {
+    if (N != wkv7::kN) return WKV7_ERR_UNSUPPORTED;
+    if (B < 0 || H <= 0 || T < 1 || T > wkv7::verify_max_tokens()) return WKV7_ERR_INVALID_ARG;
+    const long long heads = (long long)B * H;
+    if (heads * T > kMaxHeads) return WKV7_ERR_INVALID_ARG;
+    if (heads == 0) return WKV7_OK;
+    const void *ptrs[10] = {r, w, k, v, kk, a, state, o, states, nullptr};
+    for (int i = 0; i < 9; ++i)
+        if (!ptrs[i]) return WKV7_ERR_INVALID_ARG;
+    for (int i = 0; i < 9; ++i)
+        if (!aligned16(ptrs[i])) return WKV7_ERR_ALIGNMENT;
+    const size_t vec_bytes = (size_t)heads * T * N * sizeof(float);
+    const size_t state_bytes = (size_t)heads * N * N * sizeof(float);
+    const size_t states_bytes = state_bytes * T;
+    const void *ins[6] = {r, w, k, v, kk, a};
+    for (const void *p : ins) {
+        if (overlaps(o, vec_bytes, p, vec_bytes) || overlaps(states, states_bytes, p, vec_bytes))
+            return WKV7_ERR_INVALID_ARG;
+    }
+    if (overlaps(o, vec_bytes, state, state_bytes) || overlaps(states, states_bytes, state, state_bytes) ||
+        overlaps(o, vec_bytes, states, states_bytes))
+        return WKV7_ERR_INVALID_ARG;
+    unsigned *status = nullptr;
+    wkv7_status st = status_word(&status);
+    if (st != WKV7_OK) return st;
+    cudaError_t e = wkv7::launch_verify(B, T, H, r, w, k, v, kk, a, state, o, states, status, stream);
+    return e == cudaSuccess ? WKV7_OK : cuda_fail(e);
+}
+
+wkv7_status wkv7_verify_commit(int B, int T, int H, int N, const float *states, const int32_t *accept_len,
+                               float *state, cudaStream_t stream) {
+    if (N != wkv7::kN) return WKV7_ERR_UNSUPPORTED;
+    if (B < 0 || H <= 0 || T < 1 || T > wkv7::verify_max_tokens()) return WKV7_ERR_INVALID_ARG;
+    const long long heads = (long long)B * H;
+    if (heads * T > kMaxHeads) return WKV7_ERR_INVALID_ARG;
+    if (heads == 0) return WKV7_OK;
+    if (!states || !accept_len || !state) return WKV7_ERR_INVALID_ARG;
+    if (!aligned16(states) || !aligned16(state)) return WKV7_ERR_ALIGNMENT;
+    const size_t state_bytes = (size_t)heads * N * N * sizeof(float);
+    if (overlaps(state, state_bytes, states, state_bytes * T) ||
+        overlaps(state, state_bytes, accept_len, (size_t)B * sizeof(int32_t)))
+        return WKV7_ERR_INVALID_ARG;
+    unsigned *status = nullptr;
+    wkv7_status st = status_word(&status);
+    if (st != WKV7_OK) return st;
+    cudaError_t e = wkv7::launch_verify_commit(B, T, H, states, accept_len, state, status, stream);
+    return e == cudaSuccess ? WKV7_OK : cuda_fail(e);
+}
+
 wkv7_status wkv7_tmix_tail(int n_rows, int H, int N, wkv7_dtype x_dtype, const float *o, const void *r,
                            const void *k, const void *v, const void *g, const float *r_k, const float *ln_w,
                            const float *ln_b, float eps, float *y, cudaStream_t stream) {

@@ -41,6 +41,15 @@ cudaError_t launch_step(long long n_heads, const float *r, const float *w, const
                         const float *v, const float *kk, const float *a, float *state,
                         float *o, const TailArgs *tail, unsigned *status, cudaStream_t stream);
 
+// Multi-token verify (speculative decoding): T tokens per row from a read-only state,
+// every position's state kept; and the rollback to each row's accepted length.
+int verify_max_tokens();
+cudaError_t launch_verify(int B, int T, int H, const float *r, const float *w, const float *k, const float *v,
+                          const float *kk, const float *a, const float *state, float *o, float *states,
+                          unsigned *status, cudaStream_t stream);
+cudaError_t launch_verify_commit(int B, int T, int H, const float *states, const int32_t *accept_len, float *state,
+                                 unsigned *status, cudaStream_t stream);
+
 // The time-mix tail over packed rows: o fp32 [n_rows, H, 64]; r, k, v, g of x_dtype.
 cudaError_t launch_tmix_tail(long long n_rows, wkv7_dtype x_dtype, const float *o, const void *r,
                              const void *k, const void *v, const TailArgs &tail, cudaStream_t stream);
