@@ -242,6 +242,30 @@ WKV7_API wkv7_status wkv7_prefill(int num_seqs, int T_total, int H, int N,
                          cudaStream_t stream);
 
 /*
+ * wkv7_step_cast, wkv7_prefill_cast -- wkv7_step and wkv7_prefill with the output
+ * o in o_dtype: WKV7_F32, or WKV7_BF16 (each element of the fp32 result rounded
+ * to nearest even; o then holds 2 bytes per element and all its bounds and
+ * overlap rules use that size).  The SwiftRWKV inference page converts the WKV
+ * output to the model's compute type as soon as the recurrence has produced
+ * it, while the recurrent state itself stays fp32 (its
+ * castWKVOutputToComputeDType switch); the state stays fp32 here too.
+ * With a bf16 output the prefill does not take the tail split (its output
+ * correction would round twice).
+ */
+WKV7_API wkv7_status wkv7_step_cast(int B, int H, int N,
+                      const float *r, const float *w, const float *k,
+                      const float *v, const float *kk, const float *a,
+                      float *state, void *o, wkv7_dtype o_dtype, cudaStream_t stream);
+WKV7_API wkv7_status wkv7_prefill_cast(int num_seqs, int T_total, int H, int N,
+                         const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                         wkv7_dtype x_dtype,
+                         const void *r, const float *w, const void *k,
+                         const void *v, const void *kk, const void *a,
+                         const float *initial_state, float *final_state, void *o,
+                         wkv7_dtype o_dtype, void *workspace, size_t workspace_bytes,
+                         cudaStream_t stream);
+
+/*
  * wkv7_prefill_noalloc -- wkv7_prefill without a caller-supplied workspace.
  *
  * For callers that cannot allocate device memory when they run the prefill:

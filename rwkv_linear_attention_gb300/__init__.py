@@ -52,19 +52,29 @@ def _need_cuda(name, t, dtype, shape=None):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
 
 
-def step(r, w, k, v, kk, a, state, o=None, stream=None):
+def _out_code(dtype):
+    if dtype == torch.float32:
+        return _lib.F32
+    if dtype == torch.bfloat16:
+        return _lib.BF16
+    raise TypeError("out_dtype must be torch.float32 or torch.bfloat16")
+
+
+def step(r, w, k, v, kk, a, state, o=None, stream=None, out_dtype=torch.float32):
     """One decode token: inputs fp32 [B, H, N]; ``state`` fp32 [B, H, N, N]
-    updated in place.  Returns ``o`` fp32 [B, H, N] (allocated if None)."""
+    updated in place.  Returns ``o`` [B, H, N] in ``out_dtype`` (fp32, or bf16
+    rounded to nearest even; allocated if None)."""
     B, H, N = r.shape
+    code = _out_code(out_dtype)
     for name, t in (("r", r), ("w", w), ("k", k), ("v", v), ("kk", kk), ("a", a)):
         _need_cuda(name, t, torch.float32, (B, H, N))
     _need_cuda("state", state, torch.float32, (B, H, N, N))
     if o is None:
-        o = torch.empty((B, H, N), device=r.device, dtype=torch.float32)
-    _need_cuda("o", o, torch.float32, (B, H, N))
+        o = torch.empty((B, H, N), device=r.device, dtype=out_dtype)
+    _need_cuda("o", o, out_dtype, (B, H, N))
     lib = _lib.load()
-    st = lib.wkv7_step(B, H, N, _ptr(r), _ptr(w), _ptr(k), _ptr(v), _ptr(kk), _ptr(a),
-                       _ptr(state), _ptr(o), _stream(stream))
+    st = lib.wkv7_step_cast(B, H, N, _ptr(r), _ptr(w), _ptr(k), _ptr(v), _ptr(kk), _ptr(a),
+                            _ptr(state), _ptr(o), code, _stream(stream))
     _lib.check(st, "wkv7_step")
     return o
 
@@ -163,7 +173,7 @@ def prefill_workspace_size(num_seqs: int, T_total: int, H: int, N: int = HEAD_SI
 
 
 def prefill(r, w, k, v, kk, a, cu_seqlens, initial_state=None, final_state=None, o=None,
-            workspace=None, cu_seqlens_host=None, want_final_state=True, stream=None):
+            workspace=None, cu_seqlens_host=None, want_final_state=True, stream=None, out_dtype=torch.float32):
     """Packed varlen prefill.
 
     r, k, v, kk, a: [T_total, H, N] fp32 or bf16 (one dtype for all five);
@@ -175,7 +185,8 @@ def prefill(r, w, k, v, kk, a, cu_seqlens, initial_state=None, final_state=None,
     for scheduling).  ``workspace``: uint8 CUDA buffer; ``prefill_workspace_size``
     bytes enable every schedule, and a smaller one is accepted as long as it
     holds the sequence order (the tail split is then skipped); allocated when
-    None.  Returns ``(o, final_state)``.
+    None.  ``out_dtype``: the type of ``o`` (fp32, or bf16 rounded to nearest
+    even).  Returns ``(o, final_state)``.
     """
     T_total, H, N = r.shape
     xdt = r.dtype
@@ -192,9 +203,10 @@ def prefill(r, w, k, v, kk, a, cu_seqlens, initial_state=None, final_state=None,
         final_state = torch.empty((num_seqs, H, N, N), device=r.device, dtype=torch.float32)
     if final_state is not None:
         _need_cuda("final_state", final_state, torch.float32, (num_seqs, H, N, N))
+    code = _out_code(out_dtype)
     if o is None:
-        o = torch.empty((T_total, H, N), device=r.device, dtype=torch.float32)
-    _need_cuda("o", o, torch.float32, (T_total, H, N))
+        o = torch.empty((T_total, H, N), device=r.device, dtype=out_dtype)
+    _need_cuda("o", o, out_dtype, (T_total, H, N))
     host_ptr = None
     if cu_seqlens_host is not None:
         if cu_seqlens_host.device.type != "cpu" or cu_seqlens_host.dtype != torch.int32:
@@ -209,11 +221,11 @@ def prefill(r, w, k, v, kk, a, cu_seqlens, initial_state=None, final_state=None,
             workspace = torch.empty(need, device=r.device, dtype=torch.uint8)
         _need_cuda("workspace", workspace, torch.uint8)
         ws_bytes = workspace.numel()
-    st = lib.wkv7_prefill(num_seqs, T_total, H, N, _ptr(cu_seqlens), host_ptr,
-                          _lib.BF16 if xdt == torch.bfloat16 else _lib.F32,
-                          _ptr(r), _ptr(w), _ptr(k), _ptr(v), _ptr(kk), _ptr(a),
-                          _ptr(initial_state), _ptr(final_state), _ptr(o),
-                          _ptr(workspace) if need > 0 else None, ws_bytes, _stream(stream))
+    st = lib.wkv7_prefill_cast(num_seqs, T_total, H, N, _ptr(cu_seqlens), host_ptr,
+                               _lib.BF16 if xdt == torch.bfloat16 else _lib.F32,
+                               _ptr(r), _ptr(w), _ptr(k), _ptr(v), _ptr(kk), _ptr(a),
+                               _ptr(initial_state), _ptr(final_state), _ptr(o), code,
+                               _ptr(workspace) if need > 0 else None, ws_bytes, _stream(stream))
     _lib.check(st, "wkv7_prefill")
     return o, final_state
 

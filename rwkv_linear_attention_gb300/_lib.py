@@ -27,12 +27,14 @@ BF16 = 1
 
 EXPORTS = (
     "wkv7_step",
+    "wkv7_step_cast",
     "wkv7_step_tail",
     "wkv7_tmix_tail",
     "wkv7_verify",
     "wkv7_verify_commit",
     "wkv7_prefill_workspace_size",
     "wkv7_prefill",
+    "wkv7_prefill_cast",
     "wkv7_prefill_noalloc",
     "wkv7_status_string",
     "wkv7_check_device_status",
@@ -54,6 +56,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
     lib.wkv7_step.restype = I
     lib.wkv7_step.argtypes = [I, I, I, P, P, P, P, P, P, P, P, P]
+    lib.wkv7_step_cast.restype = I
+    lib.wkv7_step_cast.argtypes = [I, I, I, P, P, P, P, P, P, P, P, I, P]
+    lib.wkv7_prefill_cast.restype = I
+    lib.wkv7_prefill_cast.argtypes = [I, I, I, I, P, P, I, P, P, P, P, P, P, P, P, P, I, P, S, P]
     F = ctypes.c_float
     lib.wkv7_step_tail.restype = I
     lib.wkv7_step_tail.argtypes = [I, I, I, P, P, P, P, P, P, P, P, P, P, P, P, F, P, P]

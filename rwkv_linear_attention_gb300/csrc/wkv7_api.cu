@@ -77,10 +77,11 @@ const char *wkv7_status_string(wkv7_status s) {
     return "unknown status";
 }
 
-wkv7_status wkv7_step(int B, int H, int N, const float *r, const float *w, const float *k,
-                      const float *v, const float *kk, const float *a, float *state, float *o,
-                      cudaStream_t stream) {
+wkv7_status wkv7_step_cast(int B, int H, int N, const float *r, const float *w, const float *k,
+                           const float *v, const float *kk, const float *a, float *state, void *o,
+                           wkv7_dtype o_dtype, cudaStream_t stream) {
     if (N != wkv7::kN) return WKV7_ERR_UNSUPPORTED;
+    if (o_dtype != WKV7_F32 && o_dtype != WKV7_BF16) return WKV7_ERR_UNSUPPORTED;
     if (B < 0 || H <= 0) return WKV7_ERR_INVALID_ARG;
     const long long heads = (long long)B * H;
     if (heads > kMaxHeads) return WKV7_ERR_INVALID_ARG;
@@ -91,17 +92,25 @@ wkv7_status wkv7_step(int B, int H, int N, const float *r, const float *w, const
     for (const void *p : ptrs)
         if (!aligned16(p)) return WKV7_ERR_ALIGNMENT;
     const size_t vec_bytes = (size_t)heads * N * sizeof(float);
+    const size_t o_bytes = (size_t)heads * N * (o_dtype == WKV7_BF16 ? 2 : 4);
     const size_t state_bytes = vec_bytes * N;
-    const void *ins[7] = {r, w, k, v, kk, a, o};
+    const void *ins[6] = {r, w, k, v, kk, a};
     for (const void *p : ins)
         if (overlaps(state, state_bytes, p, vec_bytes)) return WKV7_ERR_INVALID_ARG;
+    if (overlaps(state, state_bytes, o, o_bytes)) return WKV7_ERR_INVALID_ARG;
     for (int i = 0; i < 6; ++i)
-        if (overlaps(o, vec_bytes, ins[i], vec_bytes)) return WKV7_ERR_INVALID_ARG;
+        if (overlaps(o, o_bytes, ins[i], vec_bytes)) return WKV7_ERR_INVALID_ARG;
     unsigned *status = nullptr;
     wkv7_status st = status_word(&status);
     if (st != WKV7_OK) return st;
-    cudaError_t e = wkv7::launch_step(heads, r, w, k, v, kk, a, state, o, nullptr, status, stream);
+    cudaError_t e = wkv7::launch_step(heads, r, w, k, v, kk, a, state, o, o_dtype, nullptr, status, stream);
     return e == cudaSuccess ? WKV7_OK : cuda_fail(e);
+}
+
+wkv7_status wkv7_step(int B, int H, int N, const float *r, const float *w, const float *k,
+                      const float *v, const float *kk, const float *a, float *state, float *o,
+                      cudaStream_t stream) {
+    return wkv7_step_cast(B, H, N, r, w, k, v, kk, a, state, o, WKV7_F32, stream);
 }
 
 wkv7_status wkv7_step_tail(int B, int H, int N, const float *r, const float *w, const float *k,
@@ -139,7 +148,7 @@ wkv7_status wkv7_step_tail(int B, int H, int N, const float *r, const float *w, 
     wkv7_status st = status_word(&status);
     if (st != WKV7_OK) return st;
     const wkv7::TailArgs tail{r_k, ln_w, ln_b, g, y, eps, H};
-    cudaError_t e = wkv7::launch_step(heads, r, w, k, v, kk, a, state, o, &tail, status, stream);
+    cudaError_t e = wkv7::launch_step(heads, r, w, k, v, kk, a, state, o, WKV7_F32, &tail, status, stream);
     return e == cudaSuccess ? WKV7_OK : cuda_fail(e);
 }
 
@@ -226,14 +235,15 @@ size_t wkv7_prefill_workspace_size(int num_seqs, int T_total, int H, int N) {
     return wkv7::prefill_workspace_bytes(num_seqs, T_total, H);
 }
 
-wkv7_status wkv7_prefill(int num_seqs, int T_total, int H, int N, const int32_t *cu_seqlens,
-                         const int32_t *cu_seqlens_host, wkv7_dtype x_dtype, const void *r,
-                         const float *w, const void *k, const void *v, const void *kk,
-                         const void *a, const float *initial_state, float *final_state,
-                         float *o, void *workspace, size_t workspace_bytes,
-                         cudaStream_t stream) {
+wkv7_status wkv7_prefill_cast(int num_seqs, int T_total, int H, int N, const int32_t *cu_seqlens,
+                              const int32_t *cu_seqlens_host, wkv7_dtype x_dtype, const void *r,
+                              const float *w, const void *k, const void *v, const void *kk,
+                              const void *a, const float *initial_state, float *final_state,
+                              void *o, wkv7_dtype o_dtype, void *workspace, size_t workspace_bytes,
+                              cudaStream_t stream) {
     if (N != wkv7::kN) return WKV7_ERR_UNSUPPORTED;
     if (x_dtype != WKV7_F32 && x_dtype != WKV7_BF16) return WKV7_ERR_UNSUPPORTED;
+    if (o_dtype != WKV7_F32 && o_dtype != WKV7_BF16) return WKV7_ERR_UNSUPPORTED;
     if (num_seqs < 0 || T_total < 0 || H <= 0) return WKV7_ERR_INVALID_ARG;
     if ((long long)num_seqs * H > kMaxHeads || (long long)T_total * H * N >= (1ll << 62))
         return WKV7_ERR_INVALID_ARG;
@@ -255,7 +265,7 @@ wkv7_status wkv7_prefill(int num_seqs, int T_total, int H, int N, const int32_t 
     const size_t x_elem = x_dtype == WKV7_BF16 ? 2 : 4;
     const size_t tok_elems = (size_t)T_total * H * N;
     const size_t state_bytes = (size_t)num_seqs * H * N * N * sizeof(float);
-    const size_t o_bytes = tok_elems * sizeof(float);
+    const size_t o_bytes = tok_elems * (o_dtype == WKV7_BF16 ? 2 : 4);
     // Outputs must not overlap inputs; final_state may equal initial_state
     // exactly but must not partially overlap it.
     const void *xins[5] = {r, k, v, kk, a};
@@ -304,6 +314,7 @@ wkv7_status wkv7_prefill(int num_seqs, int T_total, int H, int N, const int32_t 
     args.initial_state = initial_state;
     args.final_state = final_state;
     args.o = o;
+    args.o_dtype = o_dtype;
     args.status = status;
     cudaError_t e = cudaSuccess;
     if (need > 0 && wkv7::prefill_wants_order(args, cu_seqlens_host)) {
@@ -314,6 +325,16 @@ wkv7_status wkv7_prefill(int num_seqs, int T_total, int H, int N, const int32_t 
     }
     e = wkv7::launch_prefill(args, workspace, workspace_bytes, stream);
     return e == cudaSuccess ? WKV7_OK : cuda_fail(e);
+}
+
+wkv7_status wkv7_prefill(int num_seqs, int T_total, int H, int N, const int32_t *cu_seqlens,
+                         const int32_t *cu_seqlens_host, wkv7_dtype x_dtype, const void *r,
+                         const float *w, const void *k, const void *v, const void *kk,
+                         const void *a, const float *initial_state, float *final_state,
+                         float *o, void *workspace, size_t workspace_bytes,
+                         cudaStream_t stream) {
+    return wkv7_prefill_cast(num_seqs, T_total, H, N, cu_seqlens, cu_seqlens_host, x_dtype, r, w, k, v, kk, a,
+                             initial_state, final_state, o, WKV7_F32, workspace, workspace_bytes, stream);
 }
 
 wkv7_status wkv7_check_device_status(cudaStream_t stream) {

@@ -35,11 +35,12 @@ struct TailArgs {
     int H;
 };
 
-// Decode: one token for n_heads = B * H heads; with `tail` the time-mix tail is
-// fused into the epilogue (o may then be null).
+// Decode: one token for n_heads = B * H heads; o of o_dtype (fp32 or bf16); with
+// `tail` the time-mix tail is fused into the epilogue (o fp32, may then be null).
 cudaError_t launch_step(long long n_heads, const float *r, const float *w, const float *k,
                         const float *v, const float *kk, const float *a, float *state,
-                        float *o, const TailArgs *tail, unsigned *status, cudaStream_t stream);
+                        void *o, wkv7_dtype o_dtype, const TailArgs *tail, unsigned *status,
+                        cudaStream_t stream);
 
 // Multi-token verify (speculative decoding): T tokens per row from a read-only state,
 // every position's state kept; and the rollback to each row's accepted length.
@@ -70,7 +71,8 @@ struct PrefillArgs {
     const void *a;
     const float *initial_state;  // nullable
     float *final_state;          // nullable
-    float *o;
+    void *o;                     // [T_total, H, 64] of o_dtype
+    wkv7_dtype o_dtype;          // WKV7_F32, or WKV7_BF16 (rounded to nearest even)
     unsigned *status;            // device status word
 };
 

@@ -156,7 +156,7 @@ __device__ __forceinline__ int eidx(int t, int i) { return t * 64 + ((((i >> 2) 
 
 struct TensorMaps {
     CUtensorMap r, k, v, kk, a, w;
-    CUtensorMap o;     // fp32 output, 64 x 32 boxes in the 128-byte swizzle layout (stores)
+    CUtensorMap o;     // output: fp32 as 64 x 32 boxes, bf16 as 64 x 64 boxes, 128-byte swizzle (stores)
     CUtensorMap ohat;  // fp32 [rows, 64] carry-in readout of transfer items, same boxes
 };
 
@@ -279,6 +279,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
     }
     const int nchunks = c_end - c_begin;  // chunks of this item; loop indices below are relative to c_begin
     const long long tok_stride = static_cast<long long>(H) * 64;
+    const bool bf16_out = p.o_dtype == WKV7_BF16 && kind != kItemTransfer;
 
     // State: rows i = m - 64 (lanes 64..127), columns 16*cg .. 16*cg+15.
     const bool state_thread = q >= 2;
@@ -781,7 +782,31 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
             tmem_ld16(tmem + lane_off + kColD + 16 * cg, v);
             if (q < 2) {
                 const int t = m;
-                if (lc == kC) {
+                if (bf16_out) {
+                    // bf16 output: row t's 16 columns as two 16-byte words, staged (full chunk) in
+                    // one 64 x 64 box of T's scratch (128-byte swizzle) for one TMA store below
+                    uint4 wv[2];
+#pragma unroll
+                    for (int hw = 0; hw < 2; ++hw) {
+                        uint32_t pk[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * hw + 2 * j], v[8 * hw + 2 * j + 1]);
+                            pk[j] = *reinterpret_cast<const uint32_t *>(&b2);
+                        }
+                        wv[hw] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    }
+                    if (lc == kC) {
+                        unsigned char *row = sm + SM_TS + t * 128;
+                        *reinterpret_cast<uint4 *>(row + (((2 * cg) ^ (t & 7)) << 4)) = wv[0];
+                        *reinterpret_cast<uint4 *>(row + (((2 * cg + 1) ^ (t & 7)) << 4)) = wv[1];
+                    } else if (t < lc) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.o) + (t0 + t) * tok_stride +
+                                                               h * 64 + 16 * cg);
+                        dst[0] = wv[0];
+                        dst[1] = wv[1];
+                    }
+                } else if (lc == kC) {
                     // full chunk: stage row t in T's scratch as two 64 x 32 boxes (128-byte
                     // swizzle), written out below by two TMA stores
                     unsigned char *box = sm + SM_TS + (cg >> 1) * 8192 + t * 128;
@@ -792,7 +817,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
                 } else if (t < lc) {
                     float4 *dst = reinterpret_cast<float4 *>(
                         kind == kItemTransfer ? plan.ohat + (static_cast<long long>(ohat_row) + c * kC + t) * 64 + 16 * cg
-                                              : p.o + (t0 + t) * tok_stride + h * 64 + 16 * cg);
+                                              : static_cast<float *>(p.o) + (t0 + t) * tok_stride + h * 64 + 16 * cg);
 #pragma unroll
                     for (int j = 0; j < 4; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
                 }
@@ -811,6 +836,8 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
             if (kind == kItemTransfer) {
                 tma_store_2d(&maps.ohat, 0, ohat_row + c * kC, sbase + SM_TS);
                 tma_store_2d(&maps.ohat, 32, ohat_row + c * kC, sbase + SM_TS + 8192);
+            } else if (bf16_out) {
+                tma_store_2d(&maps.o, h * 64, t0, sbase + SM_TS);
             } else {
                 tma_store_2d(&maps.o, h * 64, t0, sbase + SM_TS);
                 tma_store_2d(&maps.o, h * 64 + 32, t0, sbase + SM_TS + 8192);
@@ -981,7 +1008,8 @@ wkv7_prefill_split_ofix_kernel(const __grid_constant__ FixPlan fp, PrefillArgs p
     for (int r = 0; r < 4; ++r) {
         const int t = 4 * tr + r;
         if (t < lc) {
-            float4 *dst = reinterpret_cast<float4 *>(p.o + (static_cast<long long>(t0) + t) * p.H * 64 + pr.h * 64 + 4 * tc);
+            float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.o) + (static_cast<long long>(t0) + t) * p.H * 64 +
+                                                     pr.h * 64 + 4 * tc);
             float4 v = *dst;
             v.x += acc[r][0];
             v.y += acc[r][1];
@@ -1030,15 +1058,18 @@ bool make_map(CUtensorMap *map, const void *base, bool bf16, int T_total, int H)
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// fp32 output [T_total, H*64] written as 64-row x 32-column boxes in the 128-byte swizzle layout.
-bool make_out_map(CUtensorMap *map, void *base, int T_total, int H) {
+// Output [T_total, H*64] written as 64-row boxes of 128 bytes in the 128-byte swizzle layout:
+// 32 fp32 or 64 bf16 columns.
+bool make_out_map(CUtensorMap *map, void *base, int T_total, int H, bool bf16) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
+    const cuuint64_t esz = bf16 ? 2 : 4;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(H) * 64, static_cast<cuuint64_t>(T_total)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(H) * 64 * 4};
-    cuuint32_t box[2] = {32, 64};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(H) * 64 * esz};
+    cuuint32_t box[2] = {bf16 ? 64u : 32u, 64};
     cuuint32_t estr[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    return enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
            CUDA_SUCCESS;
 }
@@ -1079,7 +1110,8 @@ bool plan_split(const PrefillArgs &a, unsigned char *split_ws, size_t split_byte
     plan.n_items = 0;
     plan.slots = plan.ohat = nullptr;
     fix.n_pairs = fix.n_blocks = 0;
-    if (!a.cu_seqlens_host || !split_ws || split_bytes < kSlotsBytes + 64 * 256) return false;
+    // the output correction adds into o, so only an fp32 output takes the split
+    if (!a.cu_seqlens_host || !split_ws || split_bytes < kSlotsBytes + 64 * 256 || a.o_dtype != WKV7_F32) return false;
     const long long rows_cap = static_cast<long long>((split_bytes - kSlotsBytes) / 256) & ~63ll;
     const int S = sm_count();
     if (S <= 0) return false;
@@ -1172,7 +1204,7 @@ cudaError_t launch_chunked(const PrefillArgs &args, unsigned char *split_ws, siz
         !make_map(&maps.v, args.v, true, args.T_total, args.H) ||
         !make_map(&maps.kk, args.kk, true, args.T_total, args.H) ||
         !make_map(&maps.a, args.a, true, args.T_total, args.H) ||
-        !make_map(&maps.w, args.w, false, args.T_total, args.H) || !make_out_map(&maps.o, args.o, args.T_total, args.H))
+        !make_map(&maps.w, args.w, false, args.T_total, args.H) || !make_out_map(&maps.o, args.o, args.T_total, args.H, args.o_dtype == WKV7_BF16))
         return cudaErrorInvalidValue;
     SplitPlan plan;
     FixPlan fix;

@@ -169,9 +169,18 @@ wkv7_prefill_scan_kernel(PrefillArgs p) {
             o2 += __shfl_xor_sync(0xffffffffu, o2, off);
             o3 += __shfl_xor_sync(0xffffffffu, o3, off);
         }
-        if (rg == 0)
-            *reinterpret_cast<float4 *>(p.o + t * tok_stride + h * kN + col) =
-                make_float4(o0, o1, o2, o3);
+        if (rg == 0) {
+            const long long at = t * tok_stride + h * kN + col;
+            if (p.o_dtype == WKV7_BF16) {
+                const __nv_bfloat162 lo = __floats2bfloat162_rn(o0, o1), hi = __floats2bfloat162_rn(o2, o3);
+                uint2 u;
+                u.x = *reinterpret_cast<const uint32_t *>(&lo);
+                u.y = *reinterpret_cast<const uint32_t *>(&hi);
+                *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p.o) + at) = u;
+            } else {
+                *reinterpret_cast<float4 *>(static_cast<float *>(p.o) + at) = make_float4(o0, o1, o2, o3);
+            }
+        }
         cur = nxt;
     }
 

@@ -31,6 +31,7 @@
 // preceding grid (griddepcontrol.wait) before it touches global memory, so
 // back-to-back calls on the same state stay ordered, while the launch and
 // block scheduling of the next call overlap the tail of this one.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "sm103_ptx.cuh"
@@ -62,6 +63,20 @@ constexpr size_t kSmemBytes = kSmemBytesT<false>;
 
 __device__ __forceinline__ float comp(const float4 &x, int c) {
     return c == 0 ? x.x : c == 1 ? x.y : c == 2 ? x.z : x.w;
+}
+
+// o[col .. col+3] of one head: fp32, or rounded to bf16 (to nearest even) when kBf16.
+template <bool kBf16>
+__device__ __forceinline__ void store_o4(void *o, long long idx, float o0, float o1, float o2, float o3) {
+    if constexpr (kBf16) {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(o0, o1), hi = __floats2bfloat162_rn(o2, o3);
+        uint2 u;
+        u.x = *reinterpret_cast<const uint32_t *>(&lo);
+        u.y = *reinterpret_cast<const uint32_t *>(&hi);
+        *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(o) + idx) = u;
+    } else {
+        *reinterpret_cast<float4 *>(static_cast<float *>(o) + idx) = make_float4(o0, o1, o2, o3);
+    }
 }
 
 // The time-mix tail of one head in the decode layout (four warps; lane L of warp w holds
@@ -114,12 +129,12 @@ __device__ __forceinline__ float4 tail_apply(const float *red, float eps, float 
                        (fmaf(d3 * rstd, w4.w, b4.w) + bonus * vv.w) * g4.w);
 }
 
-template <bool kTail>
+template <bool kTail, bool kBf16>
 __global__ void __launch_bounds__(kThreads)
 wkv7_step_kernel(long long n_heads, const float *__restrict__ r, const float *__restrict__ w,
                  const float *__restrict__ k, const float *__restrict__ v,
                  const float *__restrict__ kk, const float *__restrict__ a,
-                 float *__restrict__ state, float *__restrict__ o, TailArgs tail, unsigned *status) {
+                 float *__restrict__ state, void *__restrict__ o, TailArgs tail, unsigned *status) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float red[2][8];  // the tail's statistics, double-buffered across heads
     using StageX = Stage<kTail>;
@@ -241,9 +256,9 @@ wkv7_step_kernel(long long n_heads, const float *__restrict__ r, const float *__
             bonus = tail_stats(*reinterpret_cast<const float4 *>(&S.vec[7][row0]),
                                *reinterpret_cast<const float4 *>(&S.vec[7][row0 + 4]), warp, lane, rr, kr, o0, o1,
                                o2, o3, red[idx & 1]);
-            if (o && rg == 0) *reinterpret_cast<float4 *>(o + head * kN + col) = make_float4(o0, o1, o2, o3);
+            if (o && rg == 0) store_o4<kBf16>(o, head * kN + col, o0, o1, o2, o3);
         } else {
-            if (rg == 0) *reinterpret_cast<float4 *>(o + head * kN + col) = make_float4(o0, o1, o2, o3);
+            if (rg == 0) store_o4<kBf16>(o, head * kN + col, o0, o1, o2, o3);
         }
 
         fence_proxy_async_smem();  // the new state in this stage -> visible to the bulk store
@@ -286,12 +301,12 @@ wkv7_step_kernel(long long n_heads, const float *__restrict__ r, const float *__
 // and it avoids the per-head shared-memory round trip of the ring above.
 constexpr int kRegWarps = 4;
 
-template <bool kTail>
+template <bool kTail, bool kBf16>
 __global__ void __launch_bounds__(kRegWarps * 32)
 wkv7_step_regs_kernel(long long n_units, const float *__restrict__ r, const float *__restrict__ w,
                       const float *__restrict__ k, const float *__restrict__ v,
                       const float *__restrict__ kk, const float *__restrict__ a,
-                      float *__restrict__ state, float *__restrict__ o, TailArgs tail) {
+                      float *__restrict__ state, void *__restrict__ o, TailArgs tail) {
     __shared__ float red[8];  // a block is the four slices of one head
     grid_dep_wait();
     const int lane = threadIdx.x & 31;
@@ -374,9 +389,9 @@ wkv7_step_regs_kernel(long long n_units, const float *__restrict__ r, const floa
         __syncthreads();
         const float4 y = tail_apply(red, tail.eps, bonus, pre[2], pre[3], pre[4], vv, o0, o1, o2, o3);
         if (rg == 0) *reinterpret_cast<float4 *>(tail.y + head * kN + col) = y;
-        if (o && rg == 0) *reinterpret_cast<float4 *>(o + head * kN + col) = make_float4(o0, o1, o2, o3);
+        if (o && rg == 0) store_o4<kBf16>(o, head * kN + col, o0, o1, o2, o3);
     } else {
-        if (rg == 0) *reinterpret_cast<float4 *>(o + head * kN + col) = make_float4(o0, o1, o2, o3);
+        if (rg == 0) store_o4<kBf16>(o, head * kN + col, o0, o1, o2, o3);
     }
 }
 
@@ -397,14 +412,16 @@ LaunchShape shape_for_device() {
     LaunchShape s;
     int sms = 0, per_sm = 0;
     int per_sm_tail = 0;
-    if (cudaFuncSetAttribute(wkv7_step_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(wkv7_step_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmemBytes)) != cudaSuccess ||
-        cudaFuncSetAttribute(wkv7_step_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(wkv7_step_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmemBytesT<true>)) != cudaSuccess ||
+        cudaFuncSetAttribute(wkv7_step_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes)) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, wkv7_step_kernel<false>, kThreads, kSmemBytes) !=
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, wkv7_step_kernel<false, false>, kThreads, kSmemBytes) !=
             cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_tail, wkv7_step_kernel<true>, kThreads,
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_tail, wkv7_step_kernel<true, false>, kThreads,
                                                       kSmemBytesT<true>) != cudaSuccess)
         return LaunchShape{};
     s.grid_cap_tail = sms * (per_sm_tail > 0 ? per_sm_tail : 1);
@@ -418,7 +435,9 @@ LaunchShape shape_for_device() {
 
 cudaError_t launch_step(long long n_heads, const float *r, const float *w, const float *k,
                         const float *v, const float *kk, const float *a, float *state,
-                        float *o, const TailArgs *tail, unsigned *status, cudaStream_t stream) {
+                        void *o, wkv7_dtype o_dtype, const TailArgs *tail, unsigned *status,
+                        cudaStream_t stream) {
+    const bool bf16 = o_dtype == WKV7_BF16;
     const TailArgs t = tail ? *tail : TailArgs{};
     if (n_heads <= 0) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
@@ -432,8 +451,9 @@ cudaError_t launch_step(long long n_heads, const float *r, const float *w, const
         const long long units = n_heads * 4;
         cfg.gridDim = dim3(static_cast<unsigned>((units + kRegWarps - 1) / kRegWarps));
         cfg.blockDim = dim3(kRegWarps * 32);
-        if (tail) return cudaLaunchKernelEx(&cfg, wkv7_step_regs_kernel<true>, units, r, w, k, v, kk, a, state, o, t);
-        return cudaLaunchKernelEx(&cfg, wkv7_step_regs_kernel<false>, units, r, w, k, v, kk, a, state, o, t);
+        if (tail) return cudaLaunchKernelEx(&cfg, wkv7_step_regs_kernel<true, false>, units, r, w, k, v, kk, a, state, o, t);
+        if (bf16) return cudaLaunchKernelEx(&cfg, wkv7_step_regs_kernel<false, true>, units, r, w, k, v, kk, a, state, o, t);
+        return cudaLaunchKernelEx(&cfg, wkv7_step_regs_kernel<false, false>, units, r, w, k, v, kk, a, state, o, t);
     }
     const LaunchShape shape = shape_for_device();
     if (shape.grid_cap <= 0) return cudaErrorInvalidDevice;
@@ -442,8 +462,9 @@ cudaError_t launch_step(long long n_heads, const float *r, const float *w, const
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = tail ? kSmemBytesT<true> : kSmemBytes;
-    if (tail) return cudaLaunchKernelEx(&cfg, wkv7_step_kernel<true>, n_heads, r, w, k, v, kk, a, state, o, t, status);
-    return cudaLaunchKernelEx(&cfg, wkv7_step_kernel<false>, n_heads, r, w, k, v, kk, a, state, o, t, status);
+    if (tail) return cudaLaunchKernelEx(&cfg, wkv7_step_kernel<true, false>, n_heads, r, w, k, v, kk, a, state, o, t, status);
+    if (bf16) return cudaLaunchKernelEx(&cfg, wkv7_step_kernel<false, true>, n_heads, r, w, k, v, kk, a, state, o, t, status);
+    return cudaLaunchKernelEx(&cfg, wkv7_step_kernel<false, false>, n_heads, r, w, k, v, kk, a, state, o, t, status);
 }
 
 }  // namespace wkv7
