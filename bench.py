@@ -192,7 +192,7 @@ NAMES = ("r", "w", "k", "v", "kk", "a")
 class DecodeWorkload:
     """32 layer slabs of state, a pool of input sets per layer, per-layer o."""
 
-    def __init__(self, layers, B, H, pool, dev, seed, tail=False):
+    def __init__(self, layers, B, H, pool, dev, seed, tail=False, out_bf16=False):
         import torch
 
         from rwkv_linear_attention_gb300 import inputs
@@ -203,7 +203,8 @@ class DecodeWorkload:
         x = inputs.draw_rwkkva((pool, layers, B, H, N_HEAD), seed=seed, device=dev)
         self.pool = {n: x[n].contiguous() for n in NAMES}
         self.state = torch.zeros(layers, B, H, N_HEAD, N_HEAD, device=dev)
-        self.o = torch.empty(layers, B, H, N_HEAD, device=dev)
+        self.out_dtype = torch.bfloat16 if out_bf16 else torch.float32
+        self.o = torch.empty(layers, B, H, N_HEAD, device=dev, dtype=self.out_dtype)
         self.tail = tail
         if tail:  # the time-mix tail fused into the step: per-layer parameters, per-token gates, y out
             gen = torch.Generator(device=dev).manual_seed(seed + 1)
@@ -221,7 +222,7 @@ class DecodeWorkload:
                 wkv7.step_tail(*(src[n][layer] for n in NAMES), self.state[layer], self.rk[layer],
                                self.ln_w[layer], self.ln_b[layer], self.gate[p][layer], 64e-5, y=self.y[layer])
             else:
-                wkv7.step(*(src[n][layer] for n in NAMES), self.state[layer], out[layer])
+                wkv7.step(*(src[n][layer] for n in NAMES), self.state[layer], out[layer], out_dtype=self.out_dtype)
 
     def warm(self, steps):
         for s in range(steps):
@@ -415,6 +416,18 @@ def run_configs(args, dev, peaks):
                           "achieved_gbs": round(gbs, 1), "frac": round(gbs / hbm, 4)}), flush=True)
         del graphs, wl
         torch.cuda.empty_cache()
+    # decode with o cast to bf16 (34,432 B per head-step)
+    wl = DecodeWorkload(inputs.DECODE_2P9B["layers"], 32, inputs.DECODE_2P9B["H"], 4, dev, seed=7, out_bf16=True)
+    graphs = wl.capture(stream)
+    steps = max(8, args.steps)
+    ms = time_graphs(graphs, steps, args.warmup, stream, 1) / steps
+    launch_us = ms * 1e3 / wl.layers
+    gbs = wl.B * wl.H * (STEP_BYTES - 2 * N_HEAD) / (launch_us * 1e-6) / 1e9
+    print(json.dumps({"workload": "decode 2.9B B=32, o cast to bf16", "us_per_launch": round(launch_us, 3),
+                      "achieved_gbs": round(gbs, 1), "frac": round(gbs / hbm, 4),
+                      "bytes_per_head_step": STEP_BYTES - 2 * N_HEAD}), flush=True)
+    del graphs, wl
+    torch.cuda.empty_cache()
     # decode with the time-mix tail fused (o not written; g read, y written)
     wl = DecodeWorkload(inputs.DECODE_2P9B["layers"], 32, inputs.DECODE_2P9B["H"], 4, dev, seed=7, tail=True)
     graphs = wl.capture(stream)
@@ -479,25 +492,29 @@ def run_configs(args, dev, peaks):
     # prefill: 2.9B 8 x 4096; 7.2B varlen (16 x U[1, 32768]); 7.2B single 32768
     v = inputs.VARLEN_7P2B
     cases = [("prefill 2.9B 8x4096", [4096] * 8, 40, False),
+             ("prefill 2.9B 8x4096, o cast to bf16", [4096] * 8, 40, "bf16"),
              ("prefill 7.2B varlen 16 x U[1,32768]", inputs.seqlens_uniform(v["num_seqs"], v["lo"], v["hi"], 1004), 64, True),
              ("prefill 7.2B 1x32768", [v["single_T"]], 64, True)]
     for label, lens, H, with_s0 in cases:
+        out_dtype = torch.bfloat16 if with_s0 == "bf16" else torch.float32
+        with_s0 = with_s0 is True
         p = inputs.prefill_inputs(lens, H, 64, seed=11, device=dev)
         cu = p["cu_seqlens"]
         cu_dev = cu.to(dev)
         T = int(cu[-1])
         s0 = inputs.initial_state(len(lens), H, 64, seed=11, std=0.1, device=dev) if with_s0 else None
-        o = torch.empty(T, H, 64, device=dev)
+        o = torch.empty(T, H, 64, device=dev, dtype=out_dtype)
         sf = torch.empty(len(lens), H, 64, 64, device=dev)
         ws_n = wkv7.prefill_workspace_size(len(lens), T, H)
         ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=dev)
 
         def call():
             wkv7.prefill(p["r"], p["w"], p["k"], p["v"], p["kk"], p["a"], cu_dev, initial_state=s0, final_state=sf,
-                         o=o, workspace=ws if ws_n else None, cu_seqlens_host=cu, stream=stream)
+                         o=o, workspace=ws if ws_n else None, cu_seqlens_host=cu, stream=stream, out_dtype=out_dtype)
         ms = time_stream(call, max(3, args.prefill_steps // 4), 2, stream)
         wkv7.check_device_status(stream)
-        nbytes = T * H * PREFILL_BYTES_PER_TOKEN_HEAD + (2 if with_s0 else 1) * len(lens) * H * 16384
+        per_token_head = PREFILL_BYTES_PER_TOKEN_HEAD - (2 * N_HEAD if out_dtype == torch.bfloat16 else 0)
+        nbytes = T * H * per_token_head + (2 if with_s0 else 1) * len(lens) * H * 16384
         gbs = nbytes / (ms * 1e-3) / 1e9
         print(json.dumps({"workload": label, "tokens": T, "ms_per_call": round(ms, 4),
                           "tokens_per_s": round(T / (ms * 1e-3), 1), "achieved_gbs": round(gbs, 1),

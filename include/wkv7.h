@@ -249,8 +249,9 @@ WKV7_API wkv7_status wkv7_prefill(int num_seqs, int T_total, int H, int N,
  * output to the model's compute type as soon as the recurrence has produced
  * it, while the recurrent state itself stays fp32 (its
  * castWKVOutputToComputeDType switch); the state stays fp32 here too.
- * With a bf16 output the prefill does not take the tail split (its output
- * correction would round twice).
+ * With a bf16 output the tail split keeps its partial outputs in fp32
+ * scratch rows and rounds once, after the correction (it then needs twice
+ * the readout scratch; with less, every pair runs whole).
  */
 WKV7_API wkv7_status wkv7_step_cast(int B, int H, int N,
                       const float *r, const float *w, const float *k,

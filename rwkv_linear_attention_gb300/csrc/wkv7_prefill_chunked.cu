@@ -178,7 +178,8 @@ struct SplitItem {
     int16_t c0, c1;     // chunk range [c0, c1) of the pair
     int16_t kind;       // kItemWhole (segment 0 too), kItemPart, kItemTransfer
     int16_t slot;       // state slot for the final state (-1: the caller's final_state)
-    int32_t ohat_row;   // first scratch row of a transfer item's readout
+    int32_t ohat_row;   // first scratch row of a transfer item's readout, or (bf16 output)
+                        // of a part item's fp32 outputs
 };
 constexpr int kMaxSplitItems = 256;
 constexpr int kMaxSplitPairs = 80;
@@ -193,7 +194,8 @@ struct SplitPlan {
 struct FixSeg {
     int16_t c0, c1;
     int16_t slot_part, slot_transfer;  // slot_part of segment 0: its (true) final state
-    int32_t ohat_row;
+    int32_t ohat_row;                  // the transfer item's readout rows
+    int32_t opart_row;                 // with a bf16 output: the part item's fp32 output rows
 };
 struct FixPair {
     int32_t b, h, nseg;
@@ -279,7 +281,10 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
     }
     const int nchunks = c_end - c_begin;  // chunks of this item; loop indices below are relative to c_begin
     const long long tok_stride = static_cast<long long>(H) * 64;
-    const bool bf16_out = p.o_dtype == WKV7_BF16 && kind != kItemTransfer;
+    // outputs that go to fp32 scratch rows: a transfer item's readout, and a part item's
+    // partial outputs when o is bf16 (the correction is added before the one rounding)
+    const bool to_scratch = kind == kItemTransfer || (kind == kItemPart && p.o_dtype == WKV7_BF16);
+    const bool bf16_out = p.o_dtype == WKV7_BF16 && !to_scratch;
 
     // State: rows i = m - 64 (lanes 64..127), columns 16*cg .. 16*cg+15.
     const bool state_thread = q >= 2;
@@ -816,7 +821,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
                             make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
                 } else if (t < lc) {
                     float4 *dst = reinterpret_cast<float4 *>(
-                        kind == kItemTransfer ? plan.ohat + (static_cast<long long>(ohat_row) + c * kC + t) * 64 + 16 * cg
+                        to_scratch ? plan.ohat + (static_cast<long long>(ohat_row) + c * kC + t) * 64 + 16 * cg
                                               : static_cast<float *>(p.o) + (t0 + t) * tok_stride + h * 64 + 16 * cg);
 #pragma unroll
                     for (int j = 0; j < 4; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
@@ -833,7 +838,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
         }
         sync_for_mma();
         if (tid == 0 && lc == kC) {
-            if (kind == kItemTransfer) {
+            if (to_scratch) {
                 tma_store_2d(&maps.ohat, 0, ohat_row + c * kC, sbase + SM_TS);
                 tma_store_2d(&maps.ohat, 32, ohat_row + c * kC, sbase + SM_TS + 8192);
             } else if (bf16_out) {
@@ -1004,18 +1009,30 @@ wkv7_prefill_split_ofix_kernel(const __grid_constant__ FixPlan fp, PrefillArgs p
     const int bos = p.cu_seqlens[pr.b], eos = p.cu_seqlens[pr.b + 1];
     const int t0 = bos + chunk * 64;
     const int lc = min(64, eos - t0);
+    const bool bf16 = p.o_dtype == WKV7_BF16;
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
         const int t = 4 * tr + r;
         if (t < lc) {
-            float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.o) + (static_cast<long long>(t0) + t) * p.H * 64 +
-                                                     pr.h * 64 + 4 * tc);
-            float4 v = *dst;
+            const long long at = (static_cast<long long>(t0) + t) * p.H * 64 + pr.h * 64 + 4 * tc;
+            // the partial output: in o (fp32), or in the part item's fp32 rows (bf16 o)
+            const float4 *src = bf16 ? reinterpret_cast<const float4 *>(
+                                           fp.ohat + (static_cast<long long>(sg.opart_row) + (chunk - sg.c0) * 64 + t) * 64 + 4 * tc)
+                                     : reinterpret_cast<const float4 *>(static_cast<float *>(p.o) + at);
+            float4 v = *src;
             v.x += acc[r][0];
             v.y += acc[r][1];
             v.z += acc[r][2];
             v.w += acc[r][3];
-            *dst = v;
+            if (bf16) {
+                const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+                uint2 u;
+                u.x = *reinterpret_cast<const uint32_t *>(&lo);
+                u.y = *reinterpret_cast<const uint32_t *>(&hi);
+                *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p.o) + at) = u;
+            } else {
+                *reinterpret_cast<float4 *>(static_cast<float *>(p.o) + at) = v;
+            }
         }
     }
 }
@@ -1110,8 +1127,9 @@ bool plan_split(const PrefillArgs &a, unsigned char *split_ws, size_t split_byte
     plan.n_items = 0;
     plan.slots = plan.ohat = nullptr;
     fix.n_pairs = fix.n_blocks = 0;
-    // the output correction adds into o, so only an fp32 output takes the split
-    if (!a.cu_seqlens_host || !split_ws || split_bytes < kSlotsBytes + 64 * 256 || a.o_dtype != WKV7_F32) return false;
+    if (!a.cu_seqlens_host || !split_ws || split_bytes < kSlotsBytes + 64 * 256) return false;
+    // with a bf16 output the part items' outputs also go to fp32 scratch rows
+    const int rows_per = a.o_dtype == WKV7_BF16 ? 2 : 1;
     const long long rows_cap = static_cast<long long>((split_bytes - kSlotsBytes) / 256) & ~63ll;
     const int S = sm_count();
     if (S <= 0) return false;
@@ -1146,7 +1164,7 @@ bool plan_split(const PrefillArgs &a, unsigned char *split_ws, size_t split_byte
             }
             items += 2 * kp - 1;
             ++nsplit;
-            rows += static_cast<long long>(t.n - bound(t, kp, 1)) * 64;
+            rows += static_cast<long long>(t.n - bound(t, kp, 1)) * 64 * rows_per;
         }
         if (nsplit == 0 || items > kMaxSplitItems || (!two_to_one && items > S) || rows > rows_cap) continue;
         plan.main_items = static_cast<int>(P - r);
@@ -1171,6 +1189,7 @@ bool plan_split(const PrefillArgs &a, unsigned char *split_ws, size_t split_byte
             sg.slot_part = static_cast<int16_t>(slot);
             sg.slot_transfer = -1;
             sg.ohat_row = 0;
+            sg.opart_row = 0;
             plan.item[n++] = {pair, sg.c0, sg.c1, kItemWhole, static_cast<int16_t>(slot++), 0};
         }
         for (int f = 0; f < fix.n_pairs; ++f) {
@@ -1182,7 +1201,12 @@ bool plan_split(const PrefillArgs &a, unsigned char *split_ws, size_t split_byte
                 sg.c0 = static_cast<int16_t>(bound(t, fp.nseg, j));
                 sg.c1 = static_cast<int16_t>(bound(t, fp.nseg, j + 1));
                 sg.slot_part = static_cast<int16_t>(slot);
-                plan.item[n++] = {pair, sg.c0, sg.c1, kItemPart, static_cast<int16_t>(slot++), 0};
+                sg.opart_row = 0;
+                if (rows_per == 2) {
+                    sg.opart_row = static_cast<int32_t>(row);
+                    row += static_cast<long long>(sg.c1 - sg.c0) * 64;
+                }
+                plan.item[n++] = {pair, sg.c0, sg.c1, kItemPart, static_cast<int16_t>(slot++), sg.opart_row};
                 sg.slot_transfer = static_cast<int16_t>(slot);
                 sg.ohat_row = static_cast<int32_t>(row);
                 plan.item[n++] = {pair, sg.c0, sg.c1, kItemTransfer, static_cast<int16_t>(slot++), static_cast<int32_t>(row)};

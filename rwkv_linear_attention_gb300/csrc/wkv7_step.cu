@@ -65,18 +65,18 @@ __device__ __forceinline__ float comp(const float4 &x, int c) {
     return c == 0 ? x.x : c == 1 ? x.y : c == 2 ? x.z : x.w;
 }
 
-// o[col .. col+3] of one head: fp32, or rounded to bf16 (to nearest even) when kBf16.
-template <bool kBf16>
-__device__ __forceinline__ void store_o4(void *o, long long idx, float o0, float o1, float o2, float o3) {
-    if constexpr (kBf16) {
-        const __nv_bfloat162 lo = __floats2bfloat162_rn(o0, o1), hi = __floats2bfloat162_rn(o2, o3);
-        uint2 u;
-        u.x = *reinterpret_cast<const uint32_t *>(&lo);
-        u.y = *reinterpret_cast<const uint32_t *>(&hi);
-        *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(o) + idx) = u;
-    } else {
-        *reinterpret_cast<float4 *>(static_cast<float *>(o) + idx) = make_float4(o0, o1, o2, o3);
-    }
+// o[col .. col+3] of one head: fp32, or rounded to bf16 (to nearest even).
+__device__ __forceinline__ void store_o4(float *__restrict__ o, long long idx, float o0, float o1, float o2,
+                                         float o3) {
+    *reinterpret_cast<float4 *>(o + idx) = make_float4(o0, o1, o2, o3);
+}
+__device__ __forceinline__ void store_o4(__nv_bfloat16 *__restrict__ o, long long idx, float o0, float o1,
+                                         float o2, float o3) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(o0, o1), hi = __floats2bfloat162_rn(o2, o3);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t *>(&lo);
+    u.y = *reinterpret_cast<const uint32_t *>(&hi);
+    *reinterpret_cast<uint2 *>(o + idx) = u;
 }
 
 // The time-mix tail of one head in the decode layout (four warps; lane L of warp w holds
@@ -129,12 +129,12 @@ __device__ __forceinline__ float4 tail_apply(const float *red, float eps, float 
                        (fmaf(d3 * rstd, w4.w, b4.w) + bonus * vv.w) * g4.w);
 }
 
-template <bool kTail, bool kBf16>
+template <bool kTail, typename OutT>
 __global__ void __launch_bounds__(kThreads)
 wkv7_step_kernel(long long n_heads, const float *__restrict__ r, const float *__restrict__ w,
                  const float *__restrict__ k, const float *__restrict__ v,
                  const float *__restrict__ kk, const float *__restrict__ a,
-                 float *__restrict__ state, void *__restrict__ o, TailArgs tail, unsigned *status) {
+                 float *__restrict__ state, OutT *__restrict__ o, TailArgs tail, unsigned *status) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float red[2][8];  // the tail's statistics, double-buffered across heads
     using StageX = Stage<kTail>;
@@ -256,9 +256,13 @@ wkv7_step_kernel(long long n_heads, const float *__restrict__ r, const float *__
             bonus = tail_stats(*reinterpret_cast<const float4 *>(&S.vec[7][row0]),
                                *reinterpret_cast<const float4 *>(&S.vec[7][row0 + 4]), warp, lane, rr, kr, o0, o1,
                                o2, o3, red[idx & 1]);
-            if (o && rg == 0) store_o4<kBf16>(o, head * kN + col, o0, o1, o2, o3);
-        } else {
-            if (rg == 0) store_o4<kBf16>(o, head * kN + col, o0, o1, o2, o3);
+            if (o && rg == 0) store_o4(o, head * kN + col, o0, o1, o2, o3);
+        } else if (rg == 0) {
+            // the fp32 store written out here: through the helper this kernel ran 2.5% slower
+            if constexpr (sizeof(OutT) == 4)
+                *reinterpret_cast<float4 *>(o + head * kN + col) = make_float4(o0, o1, o2, o3);
+            else
+                store_o4(o, head * kN + col, o0, o1, o2, o3);
         }
 
         fence_proxy_async_smem();  // the new state in this stage -> visible to the bulk store
@@ -301,12 +305,12 @@ wkv7_step_kernel(long long n_heads, const float *__restrict__ r, const float *__
 // and it avoids the per-head shared-memory round trip of the ring above.
 constexpr int kRegWarps = 4;
 
-template <bool kTail, bool kBf16>
+template <bool kTail, typename OutT>
 __global__ void __launch_bounds__(kRegWarps * 32)
 wkv7_step_regs_kernel(long long n_units, const float *__restrict__ r, const float *__restrict__ w,
                       const float *__restrict__ k, const float *__restrict__ v,
                       const float *__restrict__ kk, const float *__restrict__ a,
-                      float *__restrict__ state, void *__restrict__ o, TailArgs tail) {
+                      float *__restrict__ state, OutT *__restrict__ o, TailArgs tail) {
     __shared__ float red[8];  // a block is the four slices of one head
     grid_dep_wait();
     const int lane = threadIdx.x & 31;
@@ -389,9 +393,9 @@ wkv7_step_regs_kernel(long long n_units, const float *__restrict__ r, const floa
         __syncthreads();
         const float4 y = tail_apply(red, tail.eps, bonus, pre[2], pre[3], pre[4], vv, o0, o1, o2, o3);
         if (rg == 0) *reinterpret_cast<float4 *>(tail.y + head * kN + col) = y;
-        if (o && rg == 0) store_o4<kBf16>(o, head * kN + col, o0, o1, o2, o3);
+        if (o && rg == 0) store_o4(o, head * kN + col, o0, o1, o2, o3);
     } else {
-        if (rg == 0) store_o4<kBf16>(o, head * kN + col, o0, o1, o2, o3);
+        if (rg == 0) store_o4(o, head * kN + col, o0, o1, o2, o3);
     }
 }
 
@@ -412,16 +416,16 @@ LaunchShape shape_for_device() {
     LaunchShape s;
     int sms = 0, per_sm = 0;
     int per_sm_tail = 0;
-    if (cudaFuncSetAttribute(wkv7_step_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(wkv7_step_kernel<false, float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmemBytes)) != cudaSuccess ||
-        cudaFuncSetAttribute(wkv7_step_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(wkv7_step_kernel<true, float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmemBytesT<true>)) != cudaSuccess ||
-        cudaFuncSetAttribute(wkv7_step_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(wkv7_step_kernel<false, __nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmemBytes)) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, wkv7_step_kernel<false, false>, kThreads, kSmemBytes) !=
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, wkv7_step_kernel<false, float>, kThreads, kSmemBytes) !=
             cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_tail, wkv7_step_kernel<true, false>, kThreads,
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_tail, wkv7_step_kernel<true, float>, kThreads,
                                                       kSmemBytesT<true>) != cudaSuccess)
         return LaunchShape{};
     s.grid_cap_tail = sms * (per_sm_tail > 0 ? per_sm_tail : 1);
@@ -451,9 +455,9 @@ cudaError_t launch_step(long long n_heads, const float *r, const float *w, const
         const long long units = n_heads * 4;
         cfg.gridDim = dim3(static_cast<unsigned>((units + kRegWarps - 1) / kRegWarps));
         cfg.blockDim = dim3(kRegWarps * 32);
-        if (tail) return cudaLaunchKernelEx(&cfg, wkv7_step_regs_kernel<true, false>, units, r, w, k, v, kk, a, state, o, t);
-        if (bf16) return cudaLaunchKernelEx(&cfg, wkv7_step_regs_kernel<false, true>, units, r, w, k, v, kk, a, state, o, t);
-        return cudaLaunchKernelEx(&cfg, wkv7_step_regs_kernel<false, false>, units, r, w, k, v, kk, a, state, o, t);
+        if (tail) return cudaLaunchKernelEx(&cfg, wkv7_step_regs_kernel<true, float>, units, r, w, k, v, kk, a, state, static_cast<float *>(o), t);
+        if (bf16) return cudaLaunchKernelEx(&cfg, wkv7_step_regs_kernel<false, __nv_bfloat16>, units, r, w, k, v, kk, a, state, static_cast<__nv_bfloat16 *>(o), t);
+        return cudaLaunchKernelEx(&cfg, wkv7_step_regs_kernel<false, float>, units, r, w, k, v, kk, a, state, static_cast<float *>(o), t);
     }
     const LaunchShape shape = shape_for_device();
     if (shape.grid_cap <= 0) return cudaErrorInvalidDevice;
@@ -462,9 +466,9 @@ cudaError_t launch_step(long long n_heads, const float *r, const float *w, const
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = tail ? kSmemBytesT<true> : kSmemBytes;
-    if (tail) return cudaLaunchKernelEx(&cfg, wkv7_step_kernel<true, false>, n_heads, r, w, k, v, kk, a, state, o, t, status);
-    if (bf16) return cudaLaunchKernelEx(&cfg, wkv7_step_kernel<false, true>, n_heads, r, w, k, v, kk, a, state, o, t, status);
-    return cudaLaunchKernelEx(&cfg, wkv7_step_kernel<false, false>, n_heads, r, w, k, v, kk, a, state, o, t, status);
+    if (tail) return cudaLaunchKernelEx(&cfg, wkv7_step_kernel<true, float>, n_heads, r, w, k, v, kk, a, state, static_cast<float *>(o), t, status);
+    if (bf16) return cudaLaunchKernelEx(&cfg, wkv7_step_kernel<false, __nv_bfloat16>, n_heads, r, w, k, v, kk, a, state, static_cast<__nv_bfloat16 *>(o), t, status);
+    return cudaLaunchKernelEx(&cfg, wkv7_step_kernel<false, float>, n_heads, r, w, k, v, kk, a, state, static_cast<float *>(o), t, status);
 }
 
 }  // namespace wkv7

@@ -62,16 +62,29 @@ def test_prefill_bf16_output_is_the_rounded_fp32_output(dev, lens, dtype):
         assert rel_err(o16.float(), o_ref) <= tol
 
 
-def test_prefill_bf16_output_with_the_full_workspace(dev):
-    """With the full workspace a bf16 output still runs every pair whole (the tail
-    split needs an fp32 output) and matches the oracle."""
-    lens, H = [3000], 8
+def test_prefill_bf16_output_with_the_tail_split(dev):
+    """With the full workspace a bf16 output takes the tail split when the plan's
+    scratch fits (the part items' outputs go to fp32 rows and are rounded once,
+    after the correction): it matches the oracle and the whole-pair bf16 result
+    within one bf16 rounding."""
+    lens, H = [1000] * 4, 40  # 160 pairs: on 152 SMs an 8-pair tail in 8 segments
     p = inputs.prefill_inputs(lens, H, 64, seed=170, device=dev)
-    s0 = inputs.initial_state(1, H, 64, seed=171, device=dev)
+    s0 = inputs.initial_state(len(lens), H, 64, seed=171, device=dev)
     cu = p["cu_seqlens"]
-    o16, f16 = wkv7.prefill(*(p[n] for n in NAMES), cu.to(dev), initial_state=s0, cu_seqlens_host=cu,
+    need = wkv7.prefill_workspace_size(len(lens), sum(lens), H)
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device=dev)
+    o16, f16 = wkv7.prefill(*(p[n] for n in NAMES), cu.to(dev), initial_state=s0, cu_seqlens_host=cu, workspace=ws,
                             out_dtype=torch.bfloat16)
+    small = torch.empty(256, dtype=torch.uint8, device=dev)
+    o_whole, f_whole = wkv7.prefill(*(p[n] for n in NAMES), cu.to(dev), initial_state=s0, cu_seqlens_host=cu,
+                                    workspace=small, out_dtype=torch.bfloat16)
     wkv7.check_device_status()
+    S = torch.cuda.get_device_properties(0).multi_processor_count
+    if 0 < (len(lens) * H) % S <= min(S // 2, 80):
+        # the split ran: its state slots (after the 256-byte sequence order) were written
+        assert bool((ws[256:256 + 16384] != 0xFF).any())
     o_ref, s_ref = oracle_prefill(p, cu, s0=s0)
     assert rel_err(o16.float(), o_ref) <= 2e-3 + BF16_ROUND
     assert rel_err(f16, s_ref) <= 2e-3
+    assert rel_err(o16.float(), o_whole.float()) <= 2e-3 + BF16_ROUND
+    assert rel_err(f16, f_whole) <= 2e-3
