@@ -267,6 +267,31 @@ WKV7_API wkv7_status wkv7_prefill_cast(int num_seqs, int T_total, int H, int N,
                          cudaStream_t stream);
 
 /*
+ * wkv7_prefill_padded -- wkv7_prefill_cast over a right-padded batch: row b of
+ * the [B, T_max, H, N] inputs holds lens[b] real tokens followed by padding.
+ * The SwiftRWKV inference page feeds its batched prefill this way (right
+ * padding, each row ending on its last real token).  The result for row b is
+ * that of a packed sequence of its lens[b] tokens; positions past lens[b] of o
+ * are not written.
+ *
+ *   lens      : DEVICE int32 [B], 0 <= lens[b] <= T_max (a value outside is
+ *               reported by wkv7_check_device_status and that row is skipped)
+ *   lens_host : optional HOST copy of lens (validated; used for scheduling)
+ *   r, k, v, kk, a : x_dtype [B, T_max, H, N];  w : fp32 [B, T_max, H, N]
+ *   o         : o_dtype [B, T_max, H, N]
+ *   initial_state, final_state : fp32 [B, H, N, N], as wkv7_prefill
+ *   workspace : as wkv7_prefill with num_seqs = B, T_total = B * T_max
+ */
+WKV7_API wkv7_status wkv7_prefill_padded(int B, int T_max, int H, int N,
+                         const int32_t *lens, const int32_t *lens_host,
+                         wkv7_dtype x_dtype,
+                         const void *r, const float *w, const void *k,
+                         const void *v, const void *kk, const void *a,
+                         const float *initial_state, float *final_state, void *o,
+                         wkv7_dtype o_dtype, void *workspace, size_t workspace_bytes,
+                         cudaStream_t stream);
+
+/*
  * wkv7_prefill_noalloc -- wkv7_prefill without a caller-supplied workspace.
  *
  * For callers that cannot allocate device memory when they run the prefill:

@@ -24,7 +24,7 @@ import torch
 from . import _lib
 from ._lib import WKV7Error  # noqa: F401
 
-__all__ = ["step", "step_tail", "tmix_tail", "verify", "verify_commit", "prefill", "prefill_workspace_size", "check_device_status",
+__all__ = ["step", "step_tail", "tmix_tail", "verify", "verify_commit", "prefill", "prefill_padded", "prefill_workspace_size", "check_device_status",
            "WKV7Error", "HEAD_SIZE"]
 
 HEAD_SIZE = 64
@@ -227,6 +227,53 @@ def prefill(r, w, k, v, kk, a, cu_seqlens, initial_state=None, final_state=None,
                                _ptr(initial_state), _ptr(final_state), _ptr(o), code,
                                _ptr(workspace) if need > 0 else None, ws_bytes, _stream(stream))
     _lib.check(st, "wkv7_prefill")
+    return o, final_state
+
+
+def prefill_padded(r, w, k, v, kk, a, lens, initial_state=None, final_state=None, o=None, workspace=None,
+                   lens_host=None, want_final_state=True, stream=None, out_dtype=torch.float32):
+    """Prefill over a right-padded batch: inputs [B, T_max, H, N] (r, k, v, kk, a
+    fp32 or bf16, w fp32); row b holds ``lens[b]`` real tokens (``lens`` int32
+    CUDA [B]; ``lens_host`` an optional CPU copy, used for scheduling).  Returns
+    ``(o [B, T_max, H, N] in out_dtype, final_state)``; o past each row's length
+    is left as it was."""
+    B, T_max, H, N = r.shape
+    xdt = r.dtype
+    if xdt not in (torch.float32, torch.bfloat16):
+        raise TypeError("r, k, v, kk, a must be float32 or bfloat16")
+    for name, t in (("r", r), ("k", k), ("v", v), ("kk", kk), ("a", a)):
+        _need_cuda(name, t, xdt, (B, T_max, H, N))
+    _need_cuda("w", w, torch.float32, (B, T_max, H, N))
+    _need_cuda("lens", lens, torch.int32, (B,))
+    if initial_state is not None:
+        _need_cuda("initial_state", initial_state, torch.float32, (B, H, N, N))
+    if final_state is None and want_final_state:
+        final_state = torch.empty((B, H, N, N), device=r.device, dtype=torch.float32)
+    if final_state is not None:
+        _need_cuda("final_state", final_state, torch.float32, (B, H, N, N))
+    code = _out_code(out_dtype)
+    if o is None:
+        o = torch.zeros((B, T_max, H, N), device=r.device, dtype=out_dtype)
+    _need_cuda("o", o, out_dtype, (B, T_max, H, N))
+    host_ptr = None
+    if lens_host is not None:
+        if lens_host.device.type != "cpu" or lens_host.dtype != torch.int32:
+            raise TypeError("lens_host must be a CPU int32 tensor")
+        lens_host = lens_host.contiguous()
+        host_ptr = _ptr(lens_host)
+    lib = _lib.load()
+    need = int(lib.wkv7_prefill_workspace_size(B, B * T_max, H, N))
+    ws_bytes = 0
+    if need > 0:
+        if workspace is None:
+            workspace = torch.empty(need, device=r.device, dtype=torch.uint8)
+        _need_cuda("workspace", workspace, torch.uint8)
+        ws_bytes = workspace.numel()
+    st = lib.wkv7_prefill_padded(B, T_max, H, N, _ptr(lens), host_ptr, _lib.BF16 if xdt == torch.bfloat16 else _lib.F32,
+                                 _ptr(r), _ptr(w), _ptr(k), _ptr(v), _ptr(kk), _ptr(a), _ptr(initial_state),
+                                 _ptr(final_state), _ptr(o), code, _ptr(workspace) if need > 0 else None, ws_bytes,
+                                 _stream(stream))
+    _lib.check(st, "wkv7_prefill_padded")
     return o, final_state
 
 

@@ -35,6 +35,7 @@ EXPORTS = (
     "wkv7_prefill_workspace_size",
     "wkv7_prefill",
     "wkv7_prefill_cast",
+    "wkv7_prefill_padded",
     "wkv7_prefill_noalloc",
     "wkv7_status_string",
     "wkv7_check_device_status",
@@ -58,6 +59,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.wkv7_step.argtypes = [I, I, I, P, P, P, P, P, P, P, P, P]
     lib.wkv7_step_cast.restype = I
     lib.wkv7_step_cast.argtypes = [I, I, I, P, P, P, P, P, P, P, P, I, P]
+    lib.wkv7_prefill_padded.restype = I
+    lib.wkv7_prefill_padded.argtypes = [I, I, I, I, P, P, I, P, P, P, P, P, P, P, P, P, I, P, S, P]
     lib.wkv7_prefill_cast.restype = I
     lib.wkv7_prefill_cast.argtypes = [I, I, I, I, P, P, I, P, P, P, P, P, P, P, P, P, I, P, S, P]
     F = ctypes.c_float

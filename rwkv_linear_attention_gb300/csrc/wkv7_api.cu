@@ -307,6 +307,9 @@ wkv7_status wkv7_prefill_cast(int num_seqs, int T_total, int H, int N, const int
     args.T_total = T_total;
     args.H = H;
     args.cu_seqlens = cu_seqlens;
+    args.lens = nullptr;
+    args.lens_host = nullptr;
+    args.row_stride = 0;
     args.order = nullptr;
     args.cu_seqlens_host = cu_seqlens_host;
     args.x_dtype = x_dtype;
@@ -317,9 +320,91 @@ wkv7_status wkv7_prefill_cast(int num_seqs, int T_total, int H, int N, const int
     args.o_dtype = o_dtype;
     args.status = status;
     cudaError_t e = cudaSuccess;
-    if (need > 0 && wkv7::prefill_wants_order(args, cu_seqlens_host)) {
+    if (need > 0 && wkv7::prefill_wants_order(args)) {
         int32_t *order = static_cast<int32_t *>(workspace);
-        e = wkv7::launch_prefill_order(cu_seqlens, num_seqs, order, stream);
+        e = wkv7::launch_prefill_order(args, order, stream);
+        if (e != cudaSuccess) return cuda_fail(e);
+        args.order = order;
+    }
+    e = wkv7::launch_prefill(args, workspace, workspace_bytes, stream);
+    return e == cudaSuccess ? WKV7_OK : cuda_fail(e);
+}
+
+wkv7_status wkv7_prefill_padded(int B, int T_max, int H, int N, const int32_t *lens, const int32_t *lens_host,
+                                wkv7_dtype x_dtype, const void *r, const float *w, const void *k, const void *v,
+                                const void *kk, const void *a, const float *initial_state, float *final_state,
+                                void *o, wkv7_dtype o_dtype, void *workspace, size_t workspace_bytes,
+                                cudaStream_t stream) {
+    if (N != wkv7::kN) return WKV7_ERR_UNSUPPORTED;
+    if (x_dtype != WKV7_F32 && x_dtype != WKV7_BF16) return WKV7_ERR_UNSUPPORTED;
+    if (o_dtype != WKV7_F32 && o_dtype != WKV7_BF16) return WKV7_ERR_UNSUPPORTED;
+    if (B < 0 || T_max < 0 || H <= 0) return WKV7_ERR_INVALID_ARG;
+    if ((long long)B * H > kMaxHeads || (long long)B * T_max >= kMaxTokens ||
+        (long long)B * T_max * H * N >= (1ll << 62))
+        return WKV7_ERR_INVALID_ARG;
+    if (B == 0) return WKV7_OK;
+    const int T_total = B * T_max;
+    if (!lens) return WKV7_ERR_INVALID_ARG;
+    if (T_total > 0 && (!r || !w || !k || !v || !kk || !a || !o)) return WKV7_ERR_INVALID_ARG;
+    const void *ptrs[10] = {r, w, k, v, kk, a, initial_state, final_state, o, lens};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return WKV7_ERR_ALIGNMENT;
+    if (lens_host)
+        for (int b = 0; b < B; ++b)
+            if (lens_host[b] < 0 || lens_host[b] > T_max) return WKV7_ERR_INVALID_ARG;
+    const size_t x_elem = x_dtype == WKV7_BF16 ? 2 : 4;
+    const size_t tok_elems = (size_t)T_total * H * N;
+    const size_t state_bytes = (size_t)B * H * N * N * sizeof(float);
+    const size_t o_bytes = tok_elems * (o_dtype == WKV7_BF16 ? 2 : 4);
+    const void *xins[5] = {r, k, v, kk, a};
+    for (const void *p : xins) {
+        if (overlaps(o, o_bytes, p, tok_elems * x_elem)) return WKV7_ERR_INVALID_ARG;
+        if (overlaps(final_state, state_bytes, p, tok_elems * x_elem)) return WKV7_ERR_INVALID_ARG;
+    }
+    if (overlaps(o, o_bytes, w, tok_elems * 4) || overlaps(final_state, state_bytes, w, tok_elems * 4))
+        return WKV7_ERR_INVALID_ARG;
+    if (overlaps(o, o_bytes, final_state, state_bytes) || overlaps(o, o_bytes, initial_state, state_bytes))
+        return WKV7_ERR_INVALID_ARG;
+    if (final_state != initial_state && overlaps(final_state, state_bytes, initial_state, state_bytes))
+        return WKV7_ERR_INVALID_ARG;
+    if (overlaps(o, o_bytes, lens, (size_t)B * 4) || overlaps(final_state, state_bytes, lens, (size_t)B * 4))
+        return WKV7_ERR_INVALID_ARG;
+    const size_t need = wkv7::prefill_workspace_min_bytes(B);
+    if (need > 0 && (!workspace || workspace_bytes < need)) return WKV7_ERR_WORKSPACE;
+    if (!workspace) workspace_bytes = 0;
+    if (workspace_bytes > 0) {
+        if (!aligned16(workspace)) return WKV7_ERR_ALIGNMENT;
+        const void *others[10] = {o, final_state, initial_state, r, w, k, v, kk, a, lens};
+        const size_t sizes[10] = {o_bytes, state_bytes, state_bytes, tok_elems * x_elem, tok_elems * 4,
+                                  tok_elems * x_elem, tok_elems * x_elem, tok_elems * x_elem, tok_elems * x_elem,
+                                  (size_t)B * 4};
+        for (int i = 0; i < 10; ++i)
+            if (overlaps(workspace, workspace_bytes, others[i], sizes[i])) return WKV7_ERR_INVALID_ARG;
+    }
+    unsigned *status = nullptr;
+    wkv7_status st = status_word(&status);
+    if (st != WKV7_OK) return st;
+    wkv7::PrefillArgs args;
+    args.num_seqs = B;
+    args.T_total = T_total;
+    args.H = H;
+    args.cu_seqlens = nullptr;
+    args.lens = lens;
+    args.lens_host = lens_host;
+    args.row_stride = T_max;
+    args.order = nullptr;
+    args.cu_seqlens_host = nullptr;
+    args.x_dtype = x_dtype;
+    args.r = r; args.w = w; args.k = k; args.v = v; args.kk = kk; args.a = a;
+    args.initial_state = initial_state;
+    args.final_state = final_state;
+    args.o = o;
+    args.o_dtype = o_dtype;
+    args.status = status;
+    cudaError_t e = cudaSuccess;
+    if (need > 0 && wkv7::prefill_wants_order(args)) {
+        int32_t *order = static_cast<int32_t *>(workspace);
+        e = wkv7::launch_prefill_order(args, order, stream);
         if (e != cudaSuccess) return cuda_fail(e);
         args.order = order;
     }

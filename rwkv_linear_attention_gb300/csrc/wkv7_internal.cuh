@@ -59,7 +59,10 @@ struct PrefillArgs {
     int num_seqs;
     int T_total;
     int H;
-    const int32_t *cu_seqlens;   // device [num_seqs + 1]
+    const int32_t *cu_seqlens;   // device [num_seqs + 1], or nullptr with `lens`
+    const int32_t *lens;         // padded layout: device [num_seqs]; sequence b owns tokens
+    const int32_t *lens_host;    //   b * row_stride .. b * row_stride + lens[b] - 1 (host copy or nullptr)
+    int row_stride;
     const int32_t *order;        // device [num_seqs] schedule (longest first) or nullptr
     const int32_t *cu_seqlens_host;  // host copy of cu_seqlens or nullptr (scheduling only)
     wkv7_dtype x_dtype;
@@ -76,6 +79,28 @@ struct PrefillArgs {
     unsigned *status;            // device status word
 };
 
+// Token range [bos, eos) of sequence b: packed (cu_seqlens) or padded (lens, row_stride).
+__device__ __forceinline__ void seq_bounds(const PrefillArgs &p, int b, int &bos, int &eos) {
+    if (p.lens) {
+        bos = b * p.row_stride;
+        eos = bos + p.lens[b];
+    } else {
+        bos = p.cu_seqlens[b];
+        eos = p.cu_seqlens[b + 1];
+    }
+}
+// The same on the host from the host copy (cu_seqlens_host or lens_host); false if absent.
+inline bool host_seq_len(const PrefillArgs &p, int b, int &len) {
+    if (p.lens) {
+        if (!p.lens_host) return false;
+        len = p.lens_host[b];
+        return true;
+    }
+    if (!p.cu_seqlens_host) return false;
+    len = p.cu_seqlens_host[b + 1] - p.cu_seqlens_host[b];
+    return true;
+}
+
 // Prefill, token-serial form (one warp per 16-column slice, tokens in order).
 cudaError_t launch_prefill_scan(const PrefillArgs &args, cudaStream_t stream);
 
@@ -86,7 +111,7 @@ size_t prefill_workspace_bytes(int num_seqs, int T_total, int H);  // for the fa
 size_t prefill_workspace_min_bytes(int num_seqs);                 // required (the sequence order)
 // Whether this batch is worth a longest-first schedule, and the kernel that
 // writes it (order[rank] = sequence index) into device memory.
-bool prefill_wants_order(const PrefillArgs &args, const int32_t *cu_seqlens_host);
-cudaError_t launch_prefill_order(const int32_t *cu_seqlens, int num_seqs, int32_t *order, cudaStream_t stream);
+bool prefill_wants_order(const PrefillArgs &args);
+cudaError_t launch_prefill_order(const PrefillArgs &args, int32_t *order, cudaStream_t stream);
 
 }  // namespace wkv7

@@ -268,8 +268,9 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
         if (tid == 0) report(p.status, kDevBounds);
         return;
     }
-    const int bos = p.cu_seqlens[b], eos = p.cu_seqlens[b + 1];
-    if (bos < 0 || eos < bos || eos > p.T_total) {
+    int bos, eos;
+    seq_bounds(p, b, bos, eos);
+    if (bos < 0 || eos < bos || eos > p.T_total || (p.lens && eos - bos > p.row_stride)) {
         if (tid == 0) report(p.status, kDevBadSeqlens);
         return;
     }
@@ -879,14 +880,15 @@ constexpr int kOrderThreads = 1024;
 constexpr int kMaxOrdered = 4096;  // sequences sorted on the device; more keep input order
 
 __global__ void __launch_bounds__(kOrderThreads)
-wkv7_prefill_order_kernel(const int32_t *__restrict__ cu, int num_seqs, int32_t *__restrict__ order) {
+wkv7_prefill_order_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ lens, int num_seqs,
+                          int32_t *__restrict__ order) {
     __shared__ unsigned long long key[kMaxOrdered];
     int n2 = 1;
     while (n2 < num_seqs) n2 <<= 1;
     for (int i = threadIdx.x; i < n2; i += kOrderThreads) {
         unsigned long long k = ~0ull;  // padding sorts last
         if (i < num_seqs) {
-            const int len = max(0, cu[i + 1] - cu[i]);
+            const int len = max(0, lens ? lens[i] : cu[i + 1] - cu[i]);
             // ascending sort of (~len, index) = descending length, then index
             k = (static_cast<unsigned long long>(0x7fffffff - len) << 32) | static_cast<unsigned>(i);
         }
@@ -1006,7 +1008,8 @@ wkv7_prefill_split_ofix_kernel(const __grid_constant__ FixPlan fp, PrefillArgs p
 #pragma unroll
         for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
     mm64_tile(oht, sin_, tr, tc, acc);
-    const int bos = p.cu_seqlens[pr.b], eos = p.cu_seqlens[pr.b + 1];
+    int bos, eos;
+    seq_bounds(p, pr.b, bos, eos);
     const int t0 = bos + chunk * 64;
     const int lc = min(64, eos - t0);
     const bool bf16 = p.o_dtype == WKV7_BF16;
@@ -1127,7 +1130,8 @@ bool plan_split(const PrefillArgs &a, unsigned char *split_ws, size_t split_byte
     plan.n_items = 0;
     plan.slots = plan.ohat = nullptr;
     fix.n_pairs = fix.n_blocks = 0;
-    if (!a.cu_seqlens_host || !split_ws || split_bytes < kSlotsBytes + 64 * 256) return false;
+    int len0 = 0;
+    if (!host_seq_len(a, 0, len0) || !split_ws || split_bytes < kSlotsBytes + 64 * 256) return false;
     // with a bf16 output the part items' outputs also go to fp32 scratch rows
     const int rows_per = a.o_dtype == WKV7_BF16 ? 2 : 1;
     const long long rows_cap = static_cast<long long>((split_bytes - kSlotsBytes) / 256) & ~63ll;
@@ -1136,7 +1140,11 @@ bool plan_split(const PrefillArgs &a, unsigned char *split_ws, size_t split_byte
     const long long r = P % S;
     if (r == 0 || 2 * r > S || r > kMaxSplitPairs) return false;
     const bool two_to_one = 3 * r > S;
-    auto len = [&](int b) { return a.cu_seqlens_host[b + 1] - a.cu_seqlens_host[b]; };
+    auto len = [&](int b) {
+        int l = 0;
+        host_seq_len(a, b, l);
+        return l;
+    };
     // the schedule's sequence order: the device order kernel's (descending length, ties by index)
     std::vector<int> ord(a.num_seqs);
     std::iota(ord.begin(), ord.end(), 0);
@@ -1276,17 +1284,17 @@ size_t prefill_workspace_bytes(int num_seqs, int T_total, int H) {
     return bytes;
 }
 
-bool prefill_wants_order(const PrefillArgs &args, const int32_t *cu_seqlens_host) {
+bool prefill_wants_order(const PrefillArgs &args) {
     if (args.num_seqs < 2 || args.num_seqs > kMaxOrdered || args.x_dtype != WKV7_BF16) return false;
-    if (!cu_seqlens_host) return true;  // lengths unknown on the host: sort on the device
-    const int32_t len0 = cu_seqlens_host[1] - cu_seqlens_host[0];
+    int len0 = 0, len = 0;
+    if (!host_seq_len(args, 0, len0)) return true;  // lengths unknown on the host: sort on the device
     for (int b = 1; b < args.num_seqs; ++b)
-        if (cu_seqlens_host[b + 1] - cu_seqlens_host[b] != len0) return true;
+        if (host_seq_len(args, b, len) && len != len0) return true;
     return false;  // all lengths equal: the input order is already longest-first
 }
 
-cudaError_t launch_prefill_order(const int32_t *cu_seqlens, int num_seqs, int32_t *order, cudaStream_t stream) {
-    wkv7_prefill_order_kernel<<<1, kOrderThreads, 0, stream>>>(cu_seqlens, num_seqs, order);
+cudaError_t launch_prefill_order(const PrefillArgs &args, int32_t *order, cudaStream_t stream) {
+    wkv7_prefill_order_kernel<<<1, kOrderThreads, 0, stream>>>(args.cu_seqlens, args.lens, args.num_seqs, order);
     return cudaGetLastError();
 }
 

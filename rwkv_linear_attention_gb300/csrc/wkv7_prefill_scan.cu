@@ -90,9 +90,9 @@ wkv7_prefill_scan_kernel(PrefillArgs p) {
         if (threadIdx.x == 0) report(p.status, kDevBounds);
         return;
     }
-    const int bos = p.cu_seqlens[b];
-    const int eos = p.cu_seqlens[b + 1];
-    if (bos < 0 || eos < bos || eos > p.T_total) {
+    int bos, eos;
+    seq_bounds(p, b, bos, eos);
+    if (bos < 0 || eos < bos || eos > p.T_total || (p.lens && eos - bos > p.row_stride)) {
         if (threadIdx.x == 0) report(p.status, kDevBadSeqlens);
         return;
     }
