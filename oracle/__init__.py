@@ -55,6 +55,9 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     t = lib.wkv7_oracle_tail
     t.restype = ctypes.c_int
     t.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int, P, P, P, P, P, P, P, P, ctypes.c_double, P]
+    b = lib.wkv7_oracle_backward
+    b.restype = ctypes.c_int
+    b.argtypes = [ctypes.c_int, P, ctypes.c_int, ctypes.c_int] + [P] * 6 + [P] * 3 + [P] * 7 + [ctypes.c_int]
     return lib
 
 
@@ -123,6 +126,49 @@ def run(r, w, k, v, kk, a, cu_seqlens=None, s0=None, nthreads: int | None = None
     if rc != 0:
         raise ValueError(f"wkv7_oracle_run failed with code {rc}")
     return o, s_final
+
+
+def _as_f64(x) -> np.ndarray:
+    if hasattr(x, "detach"):
+        x = x.detach().cpu().double().numpy()
+    return np.ascontiguousarray(x, dtype=np.float64)
+
+
+def backward(r, w, k, v, kk, a, d_o, cu_seqlens=None, s0=None, d_sfinal=None,
+             nthreads: int | None = None, lib=None):
+    """Reverse-mode derivative of ``run`` for L = <d_o, o> + <d_sfinal, s_final>.
+
+    Inputs as for ``run``; ``d_o`` [T_total, H, N] and ``d_sfinal``
+    [num_seqs, H, N, N] (None = zeros) are taken in double.  Returns
+    ``(dr, dw, dk, dv, dkk, da, d_s0)``, all float64: the first six
+    [T_total, H, N], d_s0 [num_seqs, H, N, N].
+    """
+    lib = lib or load()
+    arrs = [_as_f32(x) for x in (r, w, k, v, kk, a)]
+    T_total, H, N = arrs[0].shape
+    for x in arrs:
+        if x.shape != (T_total, H, N):
+            raise ValueError(f"input shape {x.shape} != {(T_total, H, N)}")
+    if cu_seqlens is None:
+        cu = np.array([0, T_total], dtype=np.int64)
+    else:
+        if hasattr(cu_seqlens, "detach"):
+            cu_seqlens = cu_seqlens.detach().cpu().numpy()
+        cu = np.ascontiguousarray(cu_seqlens, dtype=np.int64)
+    num_seqs = cu.shape[0] - 1
+    if num_seqs < 0 or cu[-1] != T_total:
+        raise ValueError("cu_seqlens must end at T_total")
+    dod = _as_f64(d_o).reshape(T_total, H, N)
+    s0d = None if s0 is None else _as_f64(s0).reshape(num_seqs, H, N, N)
+    dsf = None if d_sfinal is None else _as_f64(d_sfinal).reshape(num_seqs, H, N, N)
+    outs = [np.zeros((T_total, H, N), dtype=np.float64) for _ in range(6)]
+    d_s0 = np.zeros((num_seqs, H, N, N), dtype=np.float64)
+    rc = lib.wkv7_oracle_backward(num_seqs, _ptr(cu), H, N, *[_ptr(x) for x in arrs],
+                                  _ptr(s0d), _ptr(dod), _ptr(dsf), *[_ptr(x) for x in outs], _ptr(d_s0),
+                                  int(nthreads or default_threads()))
+    if rc != 0:
+        raise ValueError(f"wkv7_oracle_backward failed with code {rc}")
+    return (*outs, d_s0)
 
 
 def step(r, w, k, v, kk, a, state, nthreads: int | None = None, lib=None):

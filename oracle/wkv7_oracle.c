@@ -249,3 +249,228 @@ int wkv7_oracle_tail(int64_t n_rows, int H, int N, const double *o, const float 
     }
     return 0;
 }
+
+/*
+ * wkv7_oracle_backward -- the reverse-mode derivative of wkv7_oracle_run, in
+ * double, one token at a time.
+ *
+ * It differentiates the same per-head recurrence (Core AI model zoo,
+ * "Recurrent / linear-attention LLMs on Core AI", section 1) for the scalar
+ * loss  L = sum_t do_t . o_t + sum dS_final .* S_final  and returns dL with
+ * respect to every input.  Written as the chain rule taken backwards through
+ * each token's three statements (no identities, no chunking), with
+ * G = dL/dS for the state after the token being undone, c = kk .* a and
+ * z = kk^T S_old from the forward pass:
+ *
+ *     G    += r do^T                              (the read-out o = S^T r)
+ *     dr    = S_new do
+ *     dv    = G^T k ,          dk = G v
+ *     dw_i  = exp(w_i) sum_j G[i][j] S_old[i][j]
+ *     dc    = -G z ,           u  = G^T c
+ *     dkk   = -S_old u + a .* dc ,   da = kk .* dc
+ *     G     = diag(exp w) G - kk u^T              (dL/dS_old)
+ *
+ * and dL/dS_initial is G after the first token.  The forward states of the
+ * pair are kept (len + 1 matrices) so that S_old and S_new are exact.
+ *
+ *   cu_seqlens, r .. a, s0 : as for wkv7_oracle_run
+ *   d_o      : double [T_total, H, N]             upstream gradient of o
+ *   d_sfinal : double [num_seqs, H, N, N] or NULL upstream gradient of S_final
+ *   dr, dw, dk, dv, dkk, da : double [T_total, H, N]  (written)
+ *   d_s0     : double [num_seqs, H, N, N] or NULL    (written when given)
+ * Returns 0, -1 on a malformed argument, -2 if memory or threads fail.
+ */
+typedef struct {
+    int num_seqs, H, N, nthreads, tid;
+    const int64_t *cu;
+    const float *r, *w, *k, *v, *kk, *a;
+    const double *s0, *d_o, *d_sf;
+    double *dr, *dw, *dk, *dv, *dkk, *da, *d_s0;
+    int failed;
+} oracle_bwd_job;
+
+static void oracle_pair_backward(const oracle_bwd_job *job, int b, int h, double *hist, double *zs,
+                                 double *G, double *u, double *dc)
+{
+    const int H = job->H, N = job->N;
+    const size_t NN = (size_t)N * (size_t)N;
+    const size_t slot = (size_t)b * (size_t)H + (size_t)h;
+    const int64_t t0 = job->cu[b], t1 = job->cu[b + 1];
+    int64_t t;
+    int i, j;
+
+    /* forward: hist[s] is the state before local token s; hist[len] the final state */
+    if (job->s0)
+        memcpy(hist, job->s0 + slot * NN, sizeof(double) * NN);
+    else
+        memset(hist, 0, sizeof(double) * NN);
+    for (t = t0; t < t1; ++t) {
+        const size_t base = ((size_t)t * (size_t)H + (size_t)h) * (size_t)N;
+        const double *S = hist + (size_t)(t - t0) * NN;
+        double *Sn = hist + (size_t)(t - t0 + 1) * NN;
+        double *z = zs + (size_t)(t - t0) * (size_t)N;
+        for (j = 0; j < N; ++j) {
+            double acc = 0.0;
+            for (i = 0; i < N; ++i)
+                acc += (double)job->kk[base + i] * S[(size_t)i * N + j];
+            z[j] = acc;
+        }
+        for (i = 0; i < N; ++i) {
+            const double decay = exp((double)job->w[base + i]);
+            const double c = (double)job->kk[base + i] * (double)job->a[base + i];
+            for (j = 0; j < N; ++j)
+                Sn[(size_t)i * N + j] = decay * S[(size_t)i * N + j] - c * z[j]
+                                        + (double)job->k[base + i] * (double)job->v[base + j];
+        }
+    }
+
+    /* backward */
+    if (job->d_sf)
+        memcpy(G, job->d_sf + slot * NN, sizeof(double) * NN);
+    else
+        memset(G, 0, sizeof(double) * NN);
+    for (t = t1 - 1; t >= t0; --t) {
+        const size_t base = ((size_t)t * (size_t)H + (size_t)h) * (size_t)N;
+        const double *S_old = hist + (size_t)(t - t0) * NN;
+        const double *S_new = hist + (size_t)(t - t0 + 1) * NN;
+        const double *z = zs + (size_t)(t - t0) * (size_t)N;
+        const double *dot = job->d_o + base;
+
+        for (i = 0; i < N; ++i)
+            for (j = 0; j < N; ++j)
+                G[(size_t)i * N + j] += (double)job->r[base + i] * dot[j];
+        for (i = 0; i < N; ++i) {
+            double acc_r = 0.0, acc_k = 0.0, acc_d = 0.0, acc_c = 0.0;
+            for (j = 0; j < N; ++j) {
+                acc_r += S_new[(size_t)i * N + j] * dot[j];
+                acc_k += G[(size_t)i * N + j] * (double)job->v[base + j];
+                acc_d += G[(size_t)i * N + j] * S_old[(size_t)i * N + j];
+                acc_c += G[(size_t)i * N + j] * z[j];
+            }
+            job->dr[base + i] = acc_r;
+            job->dk[base + i] = acc_k;
+            job->dw[base + i] = exp((double)job->w[base + i]) * acc_d;
+            dc[i] = -acc_c;
+        }
+        for (j = 0; j < N; ++j) {
+            double acc_v = 0.0, acc_u = 0.0;
+            for (i = 0; i < N; ++i) {
+                acc_v += G[(size_t)i * N + j] * (double)job->k[base + i];
+                acc_u += G[(size_t)i * N + j] * (double)job->kk[base + i] * (double)job->a[base + i];
+            }
+            job->dv[base + j] = acc_v;
+            u[j] = acc_u;
+        }
+        for (i = 0; i < N; ++i) {
+            double acc = 0.0;
+            for (j = 0; j < N; ++j)
+                acc += S_old[(size_t)i * N + j] * u[j];
+            job->dkk[base + i] = -acc + (double)job->a[base + i] * dc[i];
+            job->da[base + i] = (double)job->kk[base + i] * dc[i];
+        }
+        for (i = 0; i < N; ++i) {
+            const double decay = exp((double)job->w[base + i]);
+            for (j = 0; j < N; ++j)
+                G[(size_t)i * N + j] = decay * G[(size_t)i * N + j] - (double)job->kk[base + i] * u[j];
+        }
+    }
+    if (job->d_s0)
+        memcpy(job->d_s0 + slot * NN, G, sizeof(double) * NN);
+}
+
+static void *oracle_bwd_worker(void *arg)
+{
+    oracle_bwd_job *job = (oracle_bwd_job *)arg;
+    const size_t N = (size_t)job->N, NN = N * N;
+    const int64_t pairs = (int64_t)job->num_seqs * job->H;
+    int64_t p, max_len = 0;
+    int b;
+    double *hist, *zs, *G, *u, *dc;
+    for (b = 0; b < job->num_seqs; ++b)
+        if (job->cu[b + 1] - job->cu[b] > max_len)
+            max_len = job->cu[b + 1] - job->cu[b];
+    hist = (double *)malloc(sizeof(double) * NN * (size_t)(max_len + 1));
+    zs = (double *)malloc(sizeof(double) * N * (size_t)(max_len + 1));
+    G = (double *)malloc(sizeof(double) * NN);
+    u = (double *)malloc(sizeof(double) * N);
+    dc = (double *)malloc(sizeof(double) * N);
+    if (!hist || !zs || !G || !u || !dc) {
+        job->failed = 1;
+    } else {
+        for (p = job->tid; p < pairs; p += job->nthreads)
+            oracle_pair_backward(job, (int)(p / job->H), (int)(p % job->H), hist, zs, G, u, dc);
+    }
+    free(hist);
+    free(zs);
+    free(G);
+    free(u);
+    free(dc);
+    return NULL;
+}
+
+int wkv7_oracle_backward(int num_seqs, const int64_t *cu_seqlens, int H, int N,
+                         const float *r, const float *w, const float *k,
+                         const float *v, const float *kk, const float *a,
+                         const double *s0, const double *d_o, const double *d_sfinal,
+                         double *dr, double *dw, double *dk, double *dv, double *dkk, double *da,
+                         double *d_s0, int nthreads)
+{
+    int b, t;
+    oracle_bwd_job *jobs;
+    pthread_t *threads;
+    int rc = 0;
+
+    if (num_seqs < 0 || H <= 0 || N <= 0 || !cu_seqlens)
+        return -1;
+    if (cu_seqlens[0] != 0)
+        return -1;
+    for (b = 0; b < num_seqs; ++b)
+        if (cu_seqlens[b + 1] < cu_seqlens[b])
+            return -1;
+    if (cu_seqlens[num_seqs] > 0 &&
+        (!r || !w || !k || !v || !kk || !a || !d_o || !dr || !dw || !dk || !dv || !dkk || !da))
+        return -1;
+    if (nthreads <= 0)
+        nthreads = 1;
+    if ((int64_t)nthreads > (int64_t)num_seqs * H)
+        nthreads = (int)((int64_t)num_seqs * H);
+    if (nthreads < 1)
+        return 0;
+
+    jobs = (oracle_bwd_job *)calloc((size_t)nthreads, sizeof(oracle_bwd_job));
+    threads = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !threads) {
+        free(jobs);
+        free(threads);
+        return -2;
+    }
+    for (t = 0; t < nthreads; ++t) {
+        oracle_bwd_job *j = &jobs[t];
+        j->num_seqs = num_seqs; j->H = H; j->N = N;
+        j->nthreads = nthreads; j->tid = t;
+        j->cu = cu_seqlens;
+        j->r = r; j->w = w; j->k = k; j->v = v; j->kk = kk; j->a = a;
+        j->s0 = s0; j->d_o = d_o; j->d_sf = d_sfinal;
+        j->dr = dr; j->dw = dw; j->dk = dk; j->dv = dv; j->dkk = dkk; j->da = da; j->d_s0 = d_s0;
+    }
+    if (nthreads == 1) {
+        oracle_bwd_worker(&jobs[0]);
+    } else {
+        int started = 0;
+        for (t = 0; t < nthreads; ++t) {
+            if (pthread_create(&threads[t], NULL, oracle_bwd_worker, &jobs[t]) != 0)
+                break;
+            ++started;
+        }
+        for (t = 0; t < started; ++t)
+            pthread_join(threads[t], NULL);
+        if (started != nthreads)
+            rc = -2;
+    }
+    for (t = 0; t < nthreads; ++t)
+        if (jobs[t].failed)
+            rc = -2;
+    free(jobs);
+    free(threads);
+    return rc;
+}

@@ -414,6 +414,171 @@ def pin_tail_heads_use_their_parameters(lib):
     _close(yp, y[:, perm], 0.0, "head permutation")
 
 
+# --------------------------------------------------------------------------
+# (f) the backward: reverse-mode derivative of the recurrence for
+#     L = <dO, o> + <dS_T, S_T>, pinned to the forward oracle (itself pinned
+#     above) by finite differences, to a scalar closed form, to Euler's
+#     identity for inputs the loss is homogeneous in, and to chaining.
+
+
+def _bwd(lib, r, w, k, v, kk, a, d_o, cu=None, s0=None, dsf=None):
+    return oracle.backward(r, w, k, v, kk, a, d_o, cu_seqlens=cu, s0=s0, d_sfinal=dsf, nthreads=2, lib=lib)
+
+
+def _loss(lib, xs, d_o, cu, s0, dsf):
+    o, s = _run(lib, *xs, cu=cu, s0=s0)
+    return float(np.sum(o * d_o) + np.sum(s * dsf))
+
+
+def pin_bwd_finite_differences(lib):
+    """Every gradient equals the central difference of the forward loss.
+
+    Two packed sequences (3 and 4 tokens), N = 4, random S0, dO and dS_T.  The
+    step is 2^-10 on the fp32 inputs (the difference of the two rounded fp32
+    points is used as the step) and 2^-10 on S0; the truncation error is
+    O(step^2), far below the tolerance, and a dropped term, a sign or a
+    transposed operand gives O(1) errors.
+    """
+    H, N = 2, 4
+    cu = np.array([0, 3, 7])
+    T = 7
+    xs = list(_draw(T, H, N, seed=40))
+    g = _rng(41)
+    s0 = g.standard_normal((2, H, N, N))
+    d_o = g.standard_normal((T, H, N))
+    dsf = g.standard_normal((2, H, N, N))
+    grads = _bwd(lib, *xs, d_o, cu=cu, s0=s0, dsf=dsf)
+    h = 2.0 ** -10
+    names = ["r", "w", "k", "v", "kk", "a"]
+    for q, name in enumerate(names):
+        fd = np.zeros((T, H, N))
+        for idx in np.ndindex(T, H, N):
+            x0 = xs[q][idx]
+            xp = np.float32(float(x0) + h)
+            xm = np.float32(float(x0) - h)
+            xs[q][idx] = xp
+            lp = _loss(lib, xs, d_o, cu, s0, dsf)
+            xs[q][idx] = xm
+            lm = _loss(lib, xs, d_o, cu, s0, dsf)
+            xs[q][idx] = x0
+            fd[idx] = (lp - lm) / (float(xp) - float(xm))
+        _close(grads[q], fd, 1e-5, f"d{name} against finite differences")
+    fd = np.zeros_like(s0)
+    for idx in np.ndindex(*s0.shape):
+        x0 = s0[idx]
+        s0[idx] = x0 + h
+        lp = _loss(lib, xs, d_o, cu, s0, dsf)
+        s0[idx] = x0 - h
+        lm = _loss(lib, xs, d_o, cu, s0, dsf)
+        s0[idx] = x0
+        fd[idx] = (lp - lm) / (2 * h)
+    _close(grads[6], fd, 1e-5, "dS0 against finite differences")
+
+
+def pin_bwd_scalar_n1(lib):
+    """N = 1: s_t = g_t s_{t-1} + k_t v_t with g_t = e^{w_t} - a_t kk_t^2, o_t = r_t s_t.
+
+    With the adjoint lam_t = r_t do_t + g_{t+1} lam_{t+1} (lam_T = r_T do_T + dS_T):
+    dr = s_t do_t, dk = lam_t v_t, dv = lam_t k_t, dw = lam_t e^{w_t} s_{t-1},
+    dkk = -2 lam_t a_t kk_t s_{t-1}, da = -lam_t kk_t^2 s_{t-1}, dS0 = g_1 lam_1.
+    """
+    T = 9
+    g = _rng(42)
+    r, k, v, d_o = (g.standard_normal((T, 1, 1)) for _ in range(4))
+    r, k, v = _f32(r), _f32(k), _f32(v)
+    w = _f32(-0.6 * g.random((T, 1, 1)))
+    kk = _f32(np.where(g.random((T, 1, 1)) < 0.5, -1.0, 1.0) * g.random((T, 1, 1)))
+    a = _f32(g.random((T, 1, 1)))
+    s0, dsf = 0.625, -1.5
+    dr, dw, dk, dv, dkk, da, ds0 = _bwd(lib, r, w, k, v, kk, a, d_o, s0=np.full((1, 1, 1, 1), s0),
+                                        dsf=np.full((1, 1, 1, 1), dsf))
+    f = lambda x: x[:, 0, 0].astype(np.float64)  # noqa: E731
+    r, w, k, v, kk, a, d_o = map(f, (r, w, k, v, kk, a, d_o))
+    gm = np.exp(w) - a * kk * kk
+    s = np.zeros(T + 1)
+    s[0] = s0
+    for t in range(T):
+        s[t + 1] = gm[t] * s[t] + k[t] * v[t]
+    lam = np.zeros(T)
+    nxt = dsf
+    for t in range(T - 1, -1, -1):
+        lam[t] = r[t] * d_o[t] + nxt
+        nxt = gm[t] * lam[t]
+    _close(dr[:, 0, 0], s[1:] * d_o, 1e-12, "dr")
+    _close(dk[:, 0, 0], lam * v, 1e-12, "dk")
+    _close(dv[:, 0, 0], lam * k, 1e-12, "dv")
+    _close(dw[:, 0, 0], lam * np.exp(w) * s[:-1], 1e-12, "dw")
+    _close(dkk[:, 0, 0], -2.0 * lam * a * kk * s[:-1], 1e-12, "dkk")
+    _close(da[:, 0, 0], -lam * kk * kk * s[:-1], 1e-12, "da")
+    _close(ds0[0, 0, 0, 0], gm[0] * lam[0], 1e-12, "dS0")
+
+
+def pin_bwd_euler_identities(lib):
+    """The loss is linear in r, and homogeneous of degree one in (S0, v) and
+    in (S0, k) jointly, so <r, dr> = <dO, o> and
+    <S0, dS0> + <v, dv> = <S0, dS0> + <k, dk> = L."""
+    H, N = 3, 8
+    cu = np.array([0, 5, 5, 19])
+    T = 19
+    r, w, k, v, kk, a = _draw(T, H, N, seed=43)
+    g = _rng(44)
+    s0 = g.standard_normal((3, H, N, N))
+    d_o = g.standard_normal((T, H, N))
+    dsf = g.standard_normal((3, H, N, N))
+    o, s = _run(lib, r, w, k, v, kk, a, cu=cu, s0=s0)
+    lo = float(np.sum(o * d_o))
+    L = lo + float(np.sum(s * dsf))
+    dr, dw, dk, dv, dkk, da, ds0 = _bwd(lib, r, w, k, v, kk, a, d_o, cu=cu, s0=s0, dsf=dsf)
+    f = lambda x: x.astype(np.float64)  # noqa: E731
+    _close(np.sum(f(r) * dr), lo, 1e-12, "<r, dr> = <dO, o>")
+    _close(np.sum(s0 * ds0) + np.sum(f(v) * dv), L, 1e-12, "<S0, dS0> + <v, dv> = L")
+    _close(np.sum(s0 * ds0) + np.sum(f(k) * dk), L, 1e-12, "<S0, dS0> + <k, dk> = L")
+
+
+def pin_bwd_split_invariance(lib):
+    """The backward of [0, T) equals the backward of [T1, T) (from the carried
+    state) followed by that of [0, T1) with dS_T1 = the second part's dS0."""
+    T, H, N = 21, 2, 8
+    r, w, k, v, kk, a = _draw(T, H, N, seed=45)
+    g = _rng(46)
+    s0 = g.standard_normal((1, H, N, N))
+    d_o = g.standard_normal((T, H, N))
+    dsf = g.standard_normal((1, H, N, N))
+    whole = _bwd(lib, r, w, k, v, kk, a, d_o, s0=s0, dsf=dsf)
+    xs = (r, w, k, v, kk, a)
+    for T1 in (1, 8, 20):
+        _, s_mid = _run(lib, *(x[:T1] for x in xs), s0=s0)
+        second = _bwd(lib, *(x[T1:] for x in xs), d_o[T1:], s0=s_mid, dsf=dsf)
+        first = _bwd(lib, *(x[:T1] for x in xs), d_o[:T1], s0=s0, dsf=second[6])
+        for q in range(6):
+            _close(np.concatenate([first[q], second[q]]), whole[q], 1e-12, f"grad {q} split at {T1}")
+        _close(first[6], whole[6], 1e-12, f"dS0 split at {T1}")
+
+
+def pin_bwd_packing_and_zero_length(lib):
+    """A packed backward equals per-sequence backwards; a 0-token sequence
+    passes dS_T through as dS0 (zeros when none given)."""
+    H, N = 2, 4
+    lens = [3, 0, 6]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    T = sum(lens)
+    r, w, k, v, kk, a = _draw(T, H, N, seed=47)
+    g = _rng(48)
+    s0 = g.standard_normal((3, H, N, N))
+    d_o = g.standard_normal((T, H, N))
+    dsf = g.standard_normal((3, H, N, N))
+    packed = _bwd(lib, r, w, k, v, kk, a, d_o, cu=cu, s0=s0, dsf=dsf)
+    for b, n in enumerate(lens):
+        sl = slice(cu[b], cu[b + 1])
+        one = _bwd(lib, *(x[sl] for x in (r, w, k, v, kk, a)), d_o[sl], s0=s0[b:b + 1], dsf=dsf[b:b + 1])
+        for q in range(6):
+            _close(packed[q][sl], one[q], 0.0, f"packed grad {q} seq {b}")
+        _close(packed[6][b], one[6][0], 0.0, f"packed dS0 seq {b}")
+    _close(packed[6][1], dsf[1], 0.0, "zero-length passes dS_T")
+    none = _bwd(lib, r, w, k, v, kk, a, d_o, cu=cu, s0=s0)
+    _close(none[6][1], np.zeros((H, N, N)), 0.0, "zero-length without dS_T")
+
+
 ALL_PINS = [
     pin_golden_hand_n2,
     pin_t1_zero_state,
@@ -434,4 +599,9 @@ ALL_PINS = [
     pin_tail_bonus_unit_vectors,
     pin_tail_constant_head,
     pin_tail_heads_use_their_parameters,
+    pin_bwd_finite_differences,
+    pin_bwd_scalar_n1,
+    pin_bwd_euler_identities,
+    pin_bwd_split_invariance,
+    pin_bwd_packing_and_zero_length,
 ]

@@ -43,6 +43,30 @@ MUTANTS = [
      "bonus += (double)r[base + i] * (double)k[base + i];"),
     ("tail_bonus_times_wrong_v", "bonus * (double)v[base + j]", "bonus * (double)v[base + (N - 1 - j)]"),
     ("tail_parameters_of_head_zero", "const size_t pbase = (size_t)h * (size_t)N;", "const size_t pbase = 0;"),
+    # the backward
+    ("bwd_dr_from_old_state", "acc_r += S_new[(size_t)i * N + j] * dot[j];",
+     "acc_r += S_old[(size_t)i * N + j] * dot[j];"),
+    ("bwd_dw_without_decay_factor", "job->dw[base + i] = exp((double)job->w[base + i]) * acc_d;",
+     "job->dw[base + i] = acc_d;"),
+    ("bwd_dw_on_new_state", "acc_d += G[(size_t)i * N + j] * S_old[(size_t)i * N + j];",
+     "acc_d += G[(size_t)i * N + j] * S_new[(size_t)i * N + j];"),
+    ("bwd_u_with_kk_not_c", "acc_u += G[(size_t)i * N + j] * (double)job->kk[base + i] * (double)job->a[base + i];",
+     "acc_u += G[(size_t)i * N + j] * (double)job->kk[base + i];"),
+    ("bwd_dkk_without_c_chain", "job->dkk[base + i] = -acc + (double)job->a[base + i] * dc[i];",
+     "job->dkk[base + i] = -acc;"),
+    ("bwd_da_without_kk", "job->da[base + i] = (double)job->kk[base + i] * dc[i];", "job->da[base + i] = dc[i];"),
+    ("bwd_dc_sign", "dc[i] = -acc_c;", "dc[i] = acc_c;"),
+    ("bwd_removal_sign_in_adjoint", "decay * G[(size_t)i * N + j] - (double)job->kk[base + i] * u[j];",
+     "decay * G[(size_t)i * N + j] + (double)job->kk[base + i] * u[j];"),
+    ("bwd_adjoint_not_decayed", "decay * G[(size_t)i * N + j] - (double)job->kk[base + i] * u[j];",
+     "G[(size_t)i * N + j] - (double)job->kk[base + i] * u[j];"),
+    ("bwd_readout_outer_transposed", "G[(size_t)i * N + j] += (double)job->r[base + i] * dot[j];",
+     "G[(size_t)i * N + j] += (double)job->r[base + j] * dot[i];"),
+    ("bwd_dk_transposed", "acc_k += G[(size_t)i * N + j] * (double)job->v[base + j];",
+     "acc_k += G[(size_t)j * N + i] * (double)job->v[base + j];"),
+    ("bwd_dv_with_kk", "acc_v += G[(size_t)i * N + j] * (double)job->k[base + i];",
+     "acc_v += G[(size_t)i * N + j] * (double)job->kk[base + i];"),
+    ("bwd_final_state_gradient_ignored", "if (job->d_sf)\n        memcpy(G,", "if (0)\n        memcpy(G,"),
 ]
 
 
