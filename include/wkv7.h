@@ -323,6 +323,51 @@ WKV7_API wkv7_status wkv7_prefill_noalloc(int num_seqs, int T_total, int H, int 
                          const float *initial_state, float *final_state, float *o,
                          cudaStream_t stream);
 
+/*
+ * wkv7_prefill_backward -- gradients of a wkv7_prefill call, for training.
+ *
+ * The Pantheon RWKV-X page lists training (a forward with callbacks) among the
+ * Foundry engine's features, and the SwiftRWKV inference page notes that a
+ * fused kernel is opaque to autograd; this call is the written-out derivative
+ * of the recurrence of wkv7_step (Core AI model zoo, section 1) for the loss
+ *     L = sum_t <d_o_t, o_t> + sum_b <d_final_state_b, S_final_b>,
+ * i.e. the vector-Jacobian product of (o, final_state) with (d_o,
+ * d_final_state).  It recomputes the states itself from the inputs: it needs no
+ * saved forward activations beyond the inputs of the wkv7_prefill call.
+ *
+ *   num_seqs .. a    : exactly the arguments of the wkv7_prefill call being
+ *                      differentiated (same layouts, dtypes and sequence
+ *                      rules; cu_seqlens_host optional and validated)
+ *   initial_state    : fp32 [num_seqs, H, N, N] or NULL (= zeros), as given
+ *                      to wkv7_prefill
+ *   d_o              : fp32 [T_total, H, N]     gradient of the loss w.r.t. o
+ *   d_final_state    : fp32 [num_seqs, H, N, N] or NULL (= zeros)
+ *   dr, dw, dk, dv, dkk, da : fp32 [T_total, H, N]  (written; dw is the
+ *                      gradient w.r.t. the log-decay w)
+ *   d_initial_state  : fp32 [num_seqs, H, N, N] or NULL (not written)
+ *   workspace        : device memory, 16-byte aligned, of at least
+ *                      wkv7_prefill_backward_workspace_size(num_seqs, T_total,
+ *                      H, N) bytes (about 1 KB per token and head: the state
+ *                      at every 64-token boundary plus three 64 x 64 chunk
+ *                      summaries); contents need not be initialised.
+ *
+ * Every written range must not overlap any other argument.  Zero-length
+ * sequences give d_initial_state = d_final_state.  Same precondition on w as
+ * wkv7_prefill (w >= -2.5).  Stream-ordered, no synchronisation; a malformed
+ * device cu_seqlens (when no host copy is given) is reported by
+ * wkv7_check_device_status and leaves the token gradients unwritten.
+ */
+WKV7_API size_t wkv7_prefill_backward_workspace_size(int num_seqs, int T_total, int H, int N);
+WKV7_API wkv7_status wkv7_prefill_backward(int num_seqs, int T_total, int H, int N,
+                         const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                         wkv7_dtype x_dtype,
+                         const void *r, const float *w, const void *k,
+                         const void *v, const void *kk, const void *a,
+                         const float *initial_state, const float *d_o, const float *d_final_state,
+                         float *dr, float *dw, float *dk, float *dv, float *dkk, float *da,
+                         float *d_initial_state, void *workspace, size_t workspace_bytes,
+                         cudaStream_t stream);
+
 /* Static English text for a status code (never NULL). */
 WKV7_API const char *wkv7_status_string(wkv7_status status);
 

@@ -24,7 +24,8 @@ import torch
 from . import _lib
 from ._lib import WKV7Error  # noqa: F401
 
-__all__ = ["step", "step_tail", "tmix_tail", "verify", "verify_commit", "prefill", "prefill_padded", "prefill_workspace_size", "check_device_status",
+__all__ = ["step", "step_tail", "tmix_tail", "verify", "verify_commit", "prefill", "prefill_padded", "prefill_workspace_size",
+           "prefill_backward", "prefill_backward_workspace_size", "check_device_status",
            "WKV7Error", "HEAD_SIZE"]
 
 HEAD_SIZE = 64
@@ -228,6 +229,63 @@ def prefill(r, w, k, v, kk, a, cu_seqlens, initial_state=None, final_state=None,
                                _ptr(workspace) if need > 0 else None, ws_bytes, _stream(stream))
     _lib.check(st, "wkv7_prefill")
     return o, final_state
+
+
+def prefill_backward_workspace_size(num_seqs: int, T_total: int, H: int, N: int = HEAD_SIZE) -> int:
+    return int(_lib.load().wkv7_prefill_backward_workspace_size(num_seqs, T_total, H, N))
+
+
+def prefill_backward(r, w, k, v, kk, a, cu_seqlens, d_o, initial_state=None, d_final_state=None,
+                     want_d_initial_state=True, grads=None, workspace=None, cu_seqlens_host=None, stream=None):
+    """Gradients of a :func:`prefill` call for L = <d_o, o> + <d_final_state, final_state>.
+
+    The first seven arguments and ``initial_state`` are those of the forward
+    call; ``d_o``: fp32 [T_total, H, N]; ``d_final_state``: fp32
+    [num_seqs, H, N, N] or None (zeros).  ``grads``: optional tuple of six fp32
+    [T_total, H, N] output buffers (dr, dw, dk, dv, dkk, da); ``workspace``:
+    uint8 CUDA buffer of ``prefill_backward_workspace_size`` bytes (allocated
+    when None).  Returns ``(dr, dw, dk, dv, dkk, da, d_initial_state)``
+    (the last None unless ``want_d_initial_state``).
+    """
+    T_total, H, N = r.shape
+    xdt = r.dtype
+    if xdt not in (torch.float32, torch.bfloat16):
+        raise TypeError("r, k, v, kk, a must be float32 or bfloat16")
+    for name, t in (("r", r), ("k", k), ("v", v), ("kk", kk), ("a", a)):
+        _need_cuda(name, t, xdt, (T_total, H, N))
+    _need_cuda("w", w, torch.float32, (T_total, H, N))
+    _need_cuda("d_o", d_o, torch.float32, (T_total, H, N))
+    _need_cuda("cu_seqlens", cu_seqlens, torch.int32)
+    num_seqs = cu_seqlens.shape[0] - 1
+    for name, t in (("initial_state", initial_state), ("d_final_state", d_final_state)):
+        if t is not None:
+            _need_cuda(name, t, torch.float32, (num_seqs, H, N, N))
+    if grads is None:
+        grads = tuple(torch.empty((T_total, H, N), device=r.device, dtype=torch.float32) for _ in range(6))
+    if len(grads) != 6:
+        raise ValueError("grads must hold six tensors")
+    for name, t in zip(("dr", "dw", "dk", "dv", "dkk", "da"), grads):
+        _need_cuda(name, t, torch.float32, (T_total, H, N))
+    ds0 = torch.empty((num_seqs, H, N, N), device=r.device, dtype=torch.float32) if want_d_initial_state else None
+    host_ptr = None
+    if cu_seqlens_host is not None:
+        if cu_seqlens_host.device.type != "cpu" or cu_seqlens_host.dtype != torch.int32:
+            raise TypeError("cu_seqlens_host must be a CPU int32 tensor")
+        cu_seqlens_host = cu_seqlens_host.contiguous()
+        host_ptr = _ptr(cu_seqlens_host)
+    lib = _lib.load()
+    need = int(lib.wkv7_prefill_backward_workspace_size(num_seqs, T_total, H, N))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=r.device, dtype=torch.uint8)
+    _need_cuda("workspace", workspace, torch.uint8)
+    st = lib.wkv7_prefill_backward(num_seqs, T_total, H, N, _ptr(cu_seqlens), host_ptr,
+                                   _lib.BF16 if xdt == torch.bfloat16 else _lib.F32,
+                                   _ptr(r), _ptr(w), _ptr(k), _ptr(v), _ptr(kk), _ptr(a),
+                                   _ptr(initial_state), _ptr(d_o), _ptr(d_final_state),
+                                   *[_ptr(t) for t in grads], _ptr(ds0),
+                                   _ptr(workspace), workspace.numel(), _stream(stream))
+    _lib.check(st, "wkv7_prefill_backward")
+    return (*grads, ds0)
 
 
 def prefill_padded(r, w, k, v, kk, a, lens, initial_state=None, final_state=None, o=None, workspace=None,

@@ -422,6 +422,79 @@ wkv7_status wkv7_prefill(int num_seqs, int T_total, int H, int N, const int32_t 
                              initial_state, final_state, o, WKV7_F32, workspace, workspace_bytes, stream);
 }
 
+size_t wkv7_prefill_backward_workspace_size(int num_seqs, int T_total, int H, int N) {
+    if (N != wkv7::kN || num_seqs < 0 || T_total < 0 || H <= 0) return 0;
+    if ((long long)num_seqs * H > kMaxHeads || (long long)T_total >= kMaxTokens) return 0;
+    return wkv7::prefill_backward_workspace_bytes(num_seqs, T_total, H);
+}
+
+wkv7_status wkv7_prefill_backward(int num_seqs, int T_total, int H, int N, const int32_t *cu_seqlens,
+                                  const int32_t *cu_seqlens_host, wkv7_dtype x_dtype, const void *r,
+                                  const float *w, const void *k, const void *v, const void *kk, const void *a,
+                                  const float *initial_state, const float *d_o, const float *d_final_state,
+                                  float *dr, float *dw, float *dk, float *dv, float *dkk, float *da,
+                                  float *d_initial_state, void *workspace, size_t workspace_bytes,
+                                  cudaStream_t stream) {
+    if (N != wkv7::kN) return WKV7_ERR_UNSUPPORTED;
+    if (x_dtype != WKV7_F32 && x_dtype != WKV7_BF16) return WKV7_ERR_UNSUPPORTED;
+    if (num_seqs < 0 || T_total < 0 || H <= 0) return WKV7_ERR_INVALID_ARG;
+    if ((long long)num_seqs * H > kMaxHeads || (long long)T_total >= kMaxTokens) return WKV7_ERR_INVALID_ARG;
+    if (H > 65535) return WKV7_ERR_INVALID_ARG;  // grid y
+    if (num_seqs == 0) return T_total == 0 ? WKV7_OK : WKV7_ERR_INVALID_ARG;
+    if (!cu_seqlens) return WKV7_ERR_INVALID_ARG;
+    if (T_total > 0 && (!r || !w || !k || !v || !kk || !a || !d_o || !dr || !dw || !dk || !dv || !dkk || !da))
+        return WKV7_ERR_INVALID_ARG;
+    const void *ptrs[17] = {cu_seqlens, r, w, k, v, kk, a, initial_state, d_o, d_final_state,
+                            dr, dw, dk, dv, dkk, da, d_initial_state};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return WKV7_ERR_ALIGNMENT;
+    if (cu_seqlens_host) {
+        if (cu_seqlens_host[0] != 0 || cu_seqlens_host[num_seqs] != T_total) return WKV7_ERR_INVALID_ARG;
+        for (int b = 0; b < num_seqs; ++b)
+            if (cu_seqlens_host[b + 1] < cu_seqlens_host[b]) return WKV7_ERR_INVALID_ARG;
+    }
+    const size_t need = wkv7::prefill_backward_workspace_bytes(num_seqs, T_total, H);
+    if (!workspace || workspace_bytes < need) return WKV7_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return WKV7_ERR_ALIGNMENT;
+
+    // Every written range (the six gradients, d_initial_state, the workspace)
+    // must not overlap any other argument.
+    const size_t x_elem = x_dtype == WKV7_BF16 ? 2 : 4;
+    const size_t tok = (size_t)T_total * H * N;
+    const size_t st_bytes = (size_t)num_seqs * H * N * N * sizeof(float);
+    const void *outs[8] = {dr, dw, dk, dv, dkk, da, d_initial_state, workspace};
+    const size_t out_sizes[8] = {tok * 4, tok * 4, tok * 4, tok * 4, tok * 4, tok * 4, st_bytes, workspace_bytes};
+    const void *all[17] = {r, k, v, kk, a, w, d_o, initial_state, d_final_state, cu_seqlens,
+                           dr, dw, dk, dv, dkk, da, d_initial_state};
+    const size_t all_sizes[17] = {tok * x_elem, tok * x_elem, tok * x_elem, tok * x_elem, tok * x_elem, tok * 4,
+                                  tok * 4, st_bytes, st_bytes, (size_t)(num_seqs + 1) * 4,
+                                  tok * 4, tok * 4, tok * 4, tok * 4, tok * 4, tok * 4, st_bytes};
+    for (int i = 0; i < 8; ++i)
+        for (int j = 0; j < 17; ++j) {
+            if (j >= 10 && j - 10 == i) continue;  // itself
+            if (overlaps(outs[i], out_sizes[i], all[j], all_sizes[j])) return WKV7_ERR_INVALID_ARG;
+        }
+
+    unsigned *status = nullptr;
+    wkv7_status st = status_word(&status);
+    if (st != WKV7_OK) return st;
+    wkv7::BackwardArgs b;
+    b.num_seqs = num_seqs;
+    b.T_total = T_total;
+    b.H = H;
+    b.cu_seqlens = cu_seqlens;
+    b.x_dtype = x_dtype;
+    b.r = r; b.w = w; b.k = k; b.v = v; b.kk = kk; b.a = a;
+    b.initial_state = initial_state;
+    b.d_o = d_o;
+    b.d_final_state = d_final_state;
+    b.dr = dr; b.dw = dw; b.dk = dk; b.dv = dv; b.dkk = dkk; b.da = da;
+    b.d_initial_state = d_initial_state;
+    b.status = status;
+    cudaError_t e = wkv7::launch_prefill_backward(b, workspace, stream);
+    return e == cudaSuccess ? WKV7_OK : cuda_fail(e);
+}
+
 wkv7_status wkv7_check_device_status(cudaStream_t stream) {
     cudaError_t e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return cuda_fail(e);

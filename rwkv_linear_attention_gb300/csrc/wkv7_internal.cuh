@@ -114,4 +114,27 @@ size_t prefill_workspace_min_bytes(int num_seqs);                 // required (t
 bool prefill_wants_order(const PrefillArgs &args);
 cudaError_t launch_prefill_order(const PrefillArgs &args, int32_t *order, cudaStream_t stream);
 
+// Backward of the packed prefill (chunked; see wkv7_prefill_backward.cu).
+struct BackwardArgs {
+    int num_seqs;
+    int T_total;
+    int H;
+    const int32_t *cu_seqlens;  // device [num_seqs + 1]
+    wkv7_dtype x_dtype;
+    const void *r;
+    const float *w;
+    const void *k;
+    const void *v;
+    const void *kk;
+    const void *a;
+    const float *initial_state;  // nullable
+    const float *d_o;            // [T_total, H, 64]
+    const float *d_final_state;  // nullable
+    float *dr, *dw, *dk, *dv, *dkk, *da;  // [T_total, H, 64]
+    float *d_initial_state;               // nullable
+    unsigned *status;                     // device status word
+};
+size_t prefill_backward_workspace_bytes(int num_seqs, int T_total, int H);
+cudaError_t launch_prefill_backward(const BackwardArgs &args, void *workspace, cudaStream_t stream);
+
 }  // namespace wkv7

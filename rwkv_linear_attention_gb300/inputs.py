@@ -104,6 +104,17 @@ def prefill_inputs(seqlens, H: int, N: int = 64, seed: int = 1002, device="cpu",
     return out
 
 
+def upstream_gradients(T_total: int, num_seqs: int, H: int, N: int = 64, seed: int = 1005, device="cpu",
+                       state_std: float = 0.1):
+    """Seeded upstream gradients for a prefill backward: d_o ~ N(0, 1) fp32
+    [T_total, H, N] and d_final_state ~ N(0, state_std) fp32 [num_seqs, H, N, N]."""
+    device = torch.device(device)
+    g = _gen(seed + 15485863, device)
+    d_o = _normal((T_total, H, N), g, device)
+    d_sf = _normal((num_seqs, H, N, N), g, device) * state_std
+    return d_o, d_sf
+
+
 # Workload shapes of the five named configurations.
 DECODE_2P9B = dict(layers=32, H=40, N=64, batches=(1, 8, 32), warm_tokens=256, pool=16, steps=1024)
 PREFILL_2P9B = dict(num_seqs=8, T=4096, H=40, N=64)
