@@ -44,6 +44,8 @@ def VERIFY_BYTES(T):
 COMMIT_BYTES = 2 * 4 * N_HEAD * N_HEAD
 # the tail over packed rows, bf16 row inputs: o fp32 in, r, k, v, g bf16 in, y fp32 out = 1,024
 ROW_TAIL_BYTES_BF16 = 4 * N_HEAD + 4 * 2 * N_HEAD + 4 * N_HEAD
+# prefill backward: bf16 r,k,v,kk,a, fp32 w and dO in; six fp32 gradients out = 2,688
+BACKWARD_BYTES_PER_TOKEN_HEAD = 5 * 2 * N_HEAD + 4 * N_HEAD + 4 * N_HEAD + 6 * 4 * N_HEAD
 PREFILL_FLOP_PER_TOKEN_HEAD = 26 * N_HEAD * N_HEAD  # chunked form, C = N = 64: 106,496
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 * 1024 * 1024
@@ -520,6 +522,31 @@ def run_configs(args, dev, peaks):
                           "tokens_per_s": round(T / (ms * 1e-3), 1), "achieved_gbs": round(gbs, 1),
                           "frac": round(gbs / hbm, 4), "roofline_ms": round(nbytes / hbm / 1e6, 4)}), flush=True)
         del p, o, sf, ws
+        torch.cuda.empty_cache()
+    # prefill backward (dr, dw, dk, dv, dkk, da and dS0 from dO and dS_final)
+    for label, lens, H, with_s0 in [("prefill backward 2.9B 8x4096", [4096] * 8, 40, False),
+                                    ("prefill backward 7.2B 1x32768", [v["single_T"]], 64, True)]:
+        p = inputs.prefill_inputs(lens, H, 64, seed=12, device=dev)
+        cu = p["cu_seqlens"]
+        cu_dev = cu.to(dev)
+        T = int(cu[-1])
+        s0 = inputs.initial_state(len(lens), H, 64, seed=12, std=0.1, device=dev) if with_s0 else None
+        d_o, dsf = inputs.upstream_gradients(T, len(lens), H, 64, seed=12, device=dev)
+        grads = tuple(torch.empty(T, H, 64, device=dev) for _ in range(6))
+        ws = torch.empty(wkv7.prefill_backward_workspace_size(len(lens), T, H), dtype=torch.uint8, device=dev)
+
+        def bcall():
+            wkv7.prefill_backward(p["r"], p["w"], p["k"], p["v"], p["kk"], p["a"], cu_dev, d_o, initial_state=s0,
+                                  d_final_state=dsf, grads=grads, workspace=ws, cu_seqlens_host=cu, stream=stream)
+        ms = time_stream(bcall, max(3, args.prefill_steps // 4), 2, stream)
+        wkv7.check_device_status(stream)
+        nbytes = T * H * BACKWARD_BYTES_PER_TOKEN_HEAD + (3 if with_s0 else 2) * len(lens) * H * 16384
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        print(json.dumps({"workload": label, "tokens": T, "ms_per_call": round(ms, 4),
+                          "tokens_per_s": round(T / (ms * 1e-3), 1), "achieved_gbs": round(gbs, 1),
+                          "frac": round(gbs / hbm, 4), "roofline_ms": round(nbytes / hbm / 1e6, 4),
+                          "bytes_per_token_head": BACKWARD_BYTES_PER_TOKEN_HEAD}), flush=True)
+        del p, d_o, dsf, grads, ws
         torch.cuda.empty_cache()
 
 

@@ -46,10 +46,13 @@
 
 #include <cstdint>
 
+#include "sm103_ptx.cuh"
 #include "wkv7_internal.cuh"
 
 namespace wkv7 {
 namespace {
+
+using namespace ptx;
 
 constexpr int kC = 64;            // tokens per chunk
 constexpr int kLD = 68;           // shared-memory row stride in floats (16-B rows, staggered banks)
@@ -58,9 +61,7 @@ constexpr int kThreads = 256;
 constexpr size_t kMatBytes = (size_t)kMat * sizeof(float);
 constexpr size_t kStateElems = (size_t)kN * kN;
 constexpr int kSummaryBufs = 11;
-constexpr int kGradBufs = 13;
 constexpr size_t kSummarySmem = kSummaryBufs * kMatBytes + 2 * kN * sizeof(float);
-constexpr size_t kGradSmem = kGradBufs * kMatBytes + 3 * kN * sizeof(float);
 constexpr size_t kChainSmem = 3 * kMatBytes;
 
 struct BwdArgs {
@@ -80,6 +81,7 @@ struct BwdArgs {
     float *Ack;  // [n_chunks, H, 64, 64]
     float *Fck;  // [n_chunks, H, 64, 64]
     float *Eck;  // [n_chunks, H, 64, 64]; E, then overwritten by the adjoint at the chunk end
+    unsigned *status;  // device status word
 };
 
 // ---------------------------------------------------------------------------
@@ -120,13 +122,15 @@ __device__ __forceinline__ void mm(float (&acc)[4][4], const float *__restrict__
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const float4 b = *reinterpret_cast<const float4 *>(B + (k + q) * kLD + n0);
+            const float2 b01 = make_float2(b.x, b.y), b23 = make_float2(b.z, b.w);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const float x = kNeg ? -a[i][q] : a[i][q];
-                acc[i][0] = fmaf(x, b.x, acc[i][0]);
-                acc[i][1] = fmaf(x, b.y, acc[i][1]);
-                acc[i][2] = fmaf(x, b.z, acc[i][2]);
-                acc[i][3] = fmaf(x, b.w, acc[i][3]);
+                const float2 xx = make_float2(x, x);
+                const float2 c01 = __ffma2_rn(xx, b01, make_float2(acc[i][0], acc[i][1]));
+                const float2 c23 = __ffma2_rn(xx, b23, make_float2(acc[i][2], acc[i][3]));
+                acc[i][0] = c01.x; acc[i][1] = c01.y;
+                acc[i][2] = c23.x; acc[i][3] = c23.y;
             }
         }
     }
@@ -362,8 +366,12 @@ __device__ void unit_lower_inverse(const float *Lc, float *T, float *tmp) {
         const int np = 4 - d;
         for (int e = tid; e < np * 256; e += kThreads) {
             const int J = e >> 8, rr = (e >> 4) & 15, cc = e & 15, I = J + d;
+            const float *lrow = Lc + (I * 16 + rr) * kLD;
             float acc = 0.f;
-            for (int kq = J * 16; kq < I * 16; ++kq) acc = fmaf(Lc[(I * 16 + rr) * kLD + kq], T[kq * kLD + J * 16 + cc], acc);
+            for (int kb = J; kb < I; ++kb) {
+#pragma unroll
+                for (int q = 0; q < 16; ++q) acc = fmaf(lrow[kb * 16 + q], T[(kb * 16 + q) * kLD + J * 16 + cc], acc);
+            }
             tmp[e] = acc;
         }
         __syncthreads();
@@ -524,15 +532,34 @@ __global__ void __launch_bounds__(kThreads) bwd_chain_kernel(BwdArgs p) {
     const int c0 = p.chunk_base[s], nch = p.chunk_base[s + 1] - c0;
     const size_t pair = ((size_t)s * p.H + h) * kStateElems;
     const float *init = adjoint ? (p.dsf ? p.dsf + pair : nullptr) : (p.s0 ? p.s0 + pair : nullptr);
+    const float *X = adjoint ? p.Eck : p.Fck;
     load_state(Sm, init);
     __syncthreads();
     if (!adjoint) store_state(p.Sck + ((size_t)(c0 + s) * p.H + h) * kStateElems, Sm);
+    // The next step's A and F (or E) are fetched into registers while this step multiplies.
+    float4 pa[4], px[4];
+    const auto fetch = [&](int step) {
+        const int ci = adjoint ? nch - 1 - step : step;
+        const size_t cidx = ((size_t)(c0 + ci) * p.H + h) * kStateElems;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int e = threadIdx.x + q * kThreads, row = e >> 4, c4 = (e & 15) * 4;
+            pa[q] = __ldg(reinterpret_cast<const float4 *>(p.Ack + cidx + row * kN + c4));
+            px[q] = __ldg(reinterpret_cast<const float4 *>(X + cidx + row * kN + c4));
+        }
+    };
+    if (nch > 0) fetch(0);
     for (int step = 0; step < nch; ++step) {
         const int ci = adjoint ? nch - 1 - step : step;
         const size_t cidx = ((size_t)(c0 + ci) * p.H + h) * kStateElems;
-        load_state(Am, p.Ack + cidx);
-        load_state(Xm, (adjoint ? p.Eck : p.Fck) + cidx);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int e = threadIdx.x + q * kThreads, row = e >> 4, c4 = (e & 15) * 4;
+            *reinterpret_cast<float4 *>(Am + row * kLD + c4) = pa[q];
+            *reinterpret_cast<float4 *>(Xm + row * kLD + c4) = px[q];
+        }
         __syncthreads();
+        if (step + 1 < nch) fetch(step + 1);
         float acc[4][4];
         const int m0 = tile_row(), n0 = tile_col();
 #pragma unroll
@@ -555,220 +582,504 @@ __global__ void __launch_bounds__(kThreads) bwd_chain_kernel(BwdArgs p) {
 }
 
 // ---------------------------------------------------------------------------
-// 4. per-chunk gradients
+// 4. per-chunk gradients, on the tensor cores (tcgen05, tf32 operands, fp32
+// accumulation in tensor memory).
+//
+// Every product is one M = 128 MMA whose A operand sits in tensor memory (row m
+// in lane m) and whose B operand is a K-major 128-byte-swizzled tile in shared
+// memory (D = A B^T).  Two 64-row matrices share one MMA by taking the two
+// halves of the lanes: either the same B serves both (stacked rows), or two
+// MMAs with different B read the same A columns and each keeps one half.
+// Thread (warp w, lane l) owns TMEM lane L = 32 (w mod 4) + l, i.e. row
+// t = L mod 64 of the top (L < 64) or bottom matrix, and the 32 columns of half
+// w / 4 of every 64-column block.  Transposed operands come from a second MMA
+// (C^T = B A^T) or from transposed stores into the B tile, never from moving
+// data between lanes.
+//
+// Rounds (each: operands written -> one thread issues -> commit -> all wait):
+//   1  G1 = [Q; Cm] x [Cm; K; R]^T -> Lc, Lk (top), Mc^T (bottom);
+//      G2 = K x [R; Q]^T            -> Mk^T, Lk^T (top)
+//   2  Y  = [Q | Lk] x [S0'^T | V^c]^T (top);  Y2 = [Cm | Mc^T] x [G'^T | dO^c]^T (bottom)
+//   3  U  = T^T Y2 (top), Z = T Y (bottom), from one A holding T^T / T
+//   4  dV = [K | Mk^T | -Lk^T] x [G'^T | dO^c | U^c]^T;  P = [V; Z] x [dO; U]^T
+//   5  Pt = [U; dO] x [V; Z]^T                           (the transposed P blocks)
+//   6  [dK; dC]  = [V | P1 | -P2 ; Z | P3 | -P4] x [G' | R^c | Q^c]^T
+//      [dKr; dR] = [U | P2^T | -P4^T ; dO | P1^T | -P3^T] x [S0' | K^c | Cm^T]^T
+// then the epilogue scales by the decay factors and forms dr, dk, dkk, da, dw.
 
-__global__ void __launch_bounds__(kThreads, 1) bwd_grad_kernel(BwdArgs p) {
-    extern __shared__ __align__(16) float sm[];
-    Chunk c;
-    if (!locate(p, blockIdx.x, c)) return;
-    const int h = blockIdx.y;
-    float *Gm = sm, *R = sm + 1 * kMat, *Q = sm + 2 * kMat, *K = sm + 3 * kMat, *Cm = sm + 4 * kMat;
-    float *V = sm + 5 * kMat, *dO = sm + 6 * kMat, *B7 = sm + 7 * kMat, *B8 = sm + 8 * kMat;
-    float *B9 = sm + 9 * kMat, *B10 = sm + 10 * kMat, *B11 = sm + 11 * kMat, *B12 = sm + 12 * kMat;
-    float *rho = sm + kGradBufs * kMat, *gC = rho + kN, *carry = gC + kN;
+namespace tcg {
+// shared memory (bytes from a 1024-aligned base)
+constexpr uint32_t kBG = 0;           // [Cm; K; R; Q], 256 rows x K 64 (64 KB), round 1
+constexpr uint32_t kBY = 0;           // [S0'^T | V^c] 64 x 128 (32 KB), round 2; then Y^c, Y2^c; then B_P
+constexpr uint32_t kBF3 = 32768;      // [G'^T | dO^c | U^c] 64 x 192 (48 KB), rounds 2 and 4
+constexpr uint32_t kBF1 = 81920;      // [G' | R^c | Q^c] 64 x 192 (48 KB), round 6
+constexpr uint32_t kBF2 = 131072;     // [S0' | K^c | Cm^c] 64 x 192 (48 KB), round 6
+constexpr uint32_t kPlain0 = 180224;  // fp32 64 x 68: the cumulative decay, then T; then (with kPlain1) B_Pt
+constexpr uint32_t kPlain1 = 197632;  // fp32 64 x 68: Lc
+constexpr uint32_t kVec = 215040;     // rho[64], gC[64], carry halves [2][64]
+constexpr uint32_t kBar = 216064;     // mbarrier, TMEM base slot
+constexpr uint32_t kBytes = 216080;
+constexpr uint32_t kAlloc = kBytes + 1024;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kMaxPolls = 1u << 24;
+constexpr uint32_t kAtom64 = 64 * 128, kAtom128 = 128 * 128, kAtom256 = 256 * 128;
+}  // namespace tcg
 
-    build_operands(p, c, h, Gm, R, Q, K, Cm, B7, B8, V, dO, rho, gC);
-    const int m0 = tile_row(), n0 = tile_col();
-    const size_t cidx = ((size_t)blockIdx.x * p.H + h) * kStateElems;
-    const size_t b0 = ((size_t)(blockIdx.x + c.seq) * p.H + h) * kStateElems;  // S at the chunk start
-    const size_t b1 = b0 + (size_t)p.H * kStateElems;                            // S at the chunk end
-    float acc[4][4], dv[4][4];
+__device__ __forceinline__ uint32_t tf32r(float x) { return __float_as_uint(x) + 0x1000u; }
 
-    // Grams: Lc -> B9, Lk -> B10, Mc -> B11, Mk -> B12
-    gram<kStrictLower>(B9, Q, B8);
-    gram<kStrictLower>(B10, Q, B7);
-    gram<kLower>(B11, R, B8);
-    gram<kLower>(B12, R, B7);
-    __syncthreads();
-    float *T = B7, *Lk = B10, *Mc = B11;
-    unit_lower_inverse(B9, T, B8);
-    // dV starts with Mk^T dO; Mk (B12) is then free
-    tile_zero(dv);
-    mm<true, false>(dv, B12, dO, from_diag(), kC);
-
-    // S0' = e^{rho} S0 -> B8
-    {
-        const int row = threadIdx.x >> 2, c16 = (threadIdx.x & 3) * 16;
-        const float sc = expf(rho[row]);
-        const float *src = p.Sck + b0 + row * kN + c16;
+// 32 consecutive values of one packed token row, widened to fp32.
+__device__ __forceinline__ void load32(float (&v)[32], const void *src, bool bf16, size_t off) {
+    if (bf16) {
+        const uint4 *p = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(src) + off);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const float4 x = __ldg(reinterpret_cast<const float4 *>(src) + q);
-            *reinterpret_cast<float4 *>(B8 + row * kLD + c16 + 4 * q) = make_float4(sc * x.x, sc * x.y, sc * x.z, sc * x.w);
-        }
-    }
-    __syncthreads();
-    // Y = Q S0' + Lk V -> Z = T Y, both in B9 (Lc done)
-    tile_zero(acc);
-    mm<false, false>(acc, Q, B8, 0, kC);
-    mm<false, false>(acc, Lk, V, 0, upto_diag());
-    tile_store(B9, acc);
-    __syncthreads();
-    tile_zero(acc);
-    mm<false, false>(acc, T, B9, 0, upto_diag());
-    __syncthreads();
-    tile_store(B9, acc);
-    float *Z = B9;
-    // G' = e^{gC-rho} Ghat -> B12, and the carry rowsum(Ghat .* S_C)
-    {
-        const int row = threadIdx.x >> 2, c16 = (threadIdx.x & 3) * 16;
-        const float sc = expf(gC[row] - rho[row]);
-        const float *g = p.Eck + cidx + row * kN + c16;
-        const float *sC = p.Sck + b1 + row * kN + c16;
-        float part = 0.f;
+            const uint4 u = __ldg(p + q);
+            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float4 x = __ldg(reinterpret_cast<const float4 *>(g) + q);
-            const float4 y = __ldg(reinterpret_cast<const float4 *>(sC) + q);
-            part += x.x * y.x + x.y * y.y + x.z * y.z + x.w * y.w;
-            *reinterpret_cast<float4 *>(B12 + row * kLD + c16 + 4 * q) = make_float4(sc * x.x, sc * x.y, sc * x.z, sc * x.w);
-        }
-        part += __shfl_xor_sync(0xffffffffu, part, 1);
-        part += __shfl_xor_sync(0xffffffffu, part, 2);
-        if ((threadIdx.x & 3) == 0) carry[row] = part;
-    }
-    __syncthreads();
-    float *Gp = B12;
-    // Y2 = Cm G' + Mc^T dO -> B11 ; U = T^T Y2 -> B7 (T done)
-    tile_zero(acc);
-    mm<false, false>(acc, Cm, Gp, 0, kC);
-    mm<true, false>(acc, Mc, dO, from_diag(), kC);
-    __syncthreads();
-    tile_store(B11, acc);
-    __syncthreads();
-    tile_zero(acc);
-    mm<true, false>(acc, T, B11, from_diag(), kC);
-    __syncthreads();
-    tile_store(B7, acc);
-    __syncthreads();
-    float *U = B7;
-    // dV += K G' - Lk^T U
-    mm<false, false>(dv, K, Gp, 0, kC);
-    mm<true, true>(dv, Lk, U, from_diag(), kC);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int t = m0 + i;
-        if (t < c.len)
-            *reinterpret_cast<float4 *>(p.dv + ((size_t)(c.tb + t) * p.H + h) * kN + n0) =
-                make_float4(dv[i][0], dv[i][1], dv[i][2], dv[i][3]);
-    }
-    // G'^T -> B10 (Lk done), S0'^T -> B11
-    __syncthreads();
-    transpose(B10, Gp);
-    transpose(B11, B8);
-    __syncthreads();
-    float dK[4][4], dC[4][4], dR[4][4], dKr[4][4];
-    tile_zero(dK);
-    tile_zero(dC);
-    tile_zero(dR);
-    tile_zero(dKr);
-    mm<false, false>(dK, V, B10, 0, kC);
-    mm<false, false>(dC, Z, B10, 0, kC);
-    mm<false, false>(dR, dO, B11, 0, kC);
-    mm<false, false>(dKr, U, B11, 0, kC);
-    __syncthreads();
-    // dO^T -> B8, U^T -> B10 ; P1 = triu0(V dO^T) -> B11, P3 = triu0(Z dO^T) -> B12
-    transpose(B8, dO);
-    transpose(B10, U);
-    __syncthreads();
-    gram<kUpper>(B11, V, B8);
-    gram<kUpper>(B12, Z, B8);
-    __syncthreads();
-    mm<false, false>(dK, B11, R, from_diag(), kC);
-    mm<false, false>(dC, B12, R, from_diag(), kC);
-    mm<true, false>(dR, B11, K, 0, upto_diag());
-    mm<true, true>(dR, B12, Cm, 0, upto_diag());
-    __syncthreads();
-    // P2 = triu1(V U^T) -> B11, P4 = triu1(Z U^T) -> B12
-    gram<kStrictUpper>(B11, V, B10);
-    gram<kStrictUpper>(B12, Z, B10);
-    __syncthreads();
-    mm<false, true>(dK, B11, Q, from_diag(), kC);
-    mm<false, true>(dC, B12, Q, from_diag(), kC);
-    mm<true, false>(dKr, B11, K, 0, upto_diag());
-    mm<true, true>(dKr, B12, Cm, 0, upto_diag());
-
-    // epilogue: scale, combine with the raw inputs, write; dw through a reverse
-    // cumulative sum over the chunk (in B8) plus the carry.
-    float Y[4][4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int t = m0 + i;
-        const bool valid = t < c.len;
-        const size_t off = ((size_t)(c.tb + (valid ? t : 0)) * p.H + h) * kN + n0;
-        float rr[4], kv[4], kkv[4], av[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) rr[j] = kv[j] = kkv[j] = av[j] = 0.f;
-        if (valid) {
-            if (p.x_bf16) {
-                const auto ld4 = [&](const void *src, float (&o)[4]) {
-                    const uint2 u = __ldg(reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(src) + off));
-                    o[0] = __uint_as_float(u.x << 16); o[1] = __uint_as_float(u.x & 0xffff0000u);
-                    o[2] = __uint_as_float(u.y << 16); o[3] = __uint_as_float(u.y & 0xffff0000u);
-                };
-                ld4(p.r, rr); ld4(p.k, kv); ld4(p.kk, kkv); ld4(p.a, av);
-            } else {
-                const auto ld4 = [&](const void *src, float (&o)[4]) {
-                    const float4 x = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(src) + off));
-                    o[0] = x.x; o[1] = x.y; o[2] = x.z; o[3] = x.w;
-                };
-                ld4(p.r, rr); ld4(p.k, kv); ld4(p.kk, kkv); ld4(p.a, av);
+            for (int e = 0; e < 4; ++e) {
+                v[8 * q + 2 * e] = __uint_as_float(w4[e] << 16);
+                v[8 * q + 2 * e + 1] = __uint_as_float(w4[e] & 0xffff0000u);
             }
         }
-        float odr[4], odk[4], odkk[4], oda[4], wsum[4];
+    } else {
+        const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(src) + off);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int ch = n0 + j;
-            const float g = Gm[t * kLD + ch], gx = t > 0 ? Gm[(t - 1) * kLD + ch] : 0.f, rh = rho[ch];
-            const float up = expf(g - rh), dn = expf(rh - g), upx = expf(gx - rh);
-            const float vr = dR[i][j] * up, vk = dK[i][j] * dn, vc = -dC[i][j] * dn, vkr = -dKr[i][j] * upx;
-            const float cv = kkv[j] * av[j];
-            odr[j] = vr;
-            odk[j] = vk;
-            odkk[j] = vkr + av[j] * vc;
-            oda[j] = kkv[j] * vc;
-            Y[i][j] = kkv[j] * vkr;
-            wsum[j] = rr[j] * vr - kv[j] * vk - cv * vc + Y[i][j];
-        }
-        *reinterpret_cast<float4 *>(B8 + t * kLD + n0) = make_float4(wsum[0], wsum[1], wsum[2], wsum[3]);
-        if (valid) {
-            const size_t go = ((size_t)(c.tb + t) * p.H + h) * kN + n0;
-            *reinterpret_cast<float4 *>(p.dr + go) = make_float4(odr[0], odr[1], odr[2], odr[3]);
-            *reinterpret_cast<float4 *>(p.dk + go) = make_float4(odk[0], odk[1], odk[2], odk[3]);
-            *reinterpret_cast<float4 *>(p.dkk + go) = make_float4(odkk[0], odkk[1], odkk[2], odkk[3]);
-            *reinterpret_cast<float4 *>(p.da + go) = make_float4(oda[0], oda[1], oda[2], oda[3]);
-        }
-    }
-    __syncthreads();
-    {
-        // reverse inclusive cumulative sum over tokens, per channel (4 threads x 16 tokens)
-        const int ch = threadIdx.x & 63, qt = threadIdx.x >> 6;
-        float run = 0.f;
-        float part[16];
-#pragma unroll
-        for (int u = 15; u >= 0; --u) {
-            run += B8[(qt * 16 + u) * kLD + ch];
-            part[u] = run;
-        }
-        B9[qt * kLD + ch] = run;  // quarter totals (Z is done)
-        __syncthreads();
-        float base = carry[ch];
-        for (int q = qt + 1; q < 4; ++q) base += B9[q * kLD + ch];
-#pragma unroll
-        for (int u = 0; u < 16; ++u) B8[(qt * 16 + u) * kLD + ch] = part[u] + base;
-        __syncthreads();
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int t = m0 + i;
-        if (t < c.len) {
-            const float4 x = *reinterpret_cast<const float4 *>(B8 + t * kLD + n0);
-            *reinterpret_cast<float4 *>(p.dw + ((size_t)(c.tb + t) * p.H + h) * kN + n0) =
-                make_float4(x.x - Y[i][0], x.y - Y[i][1], x.z - Y[i][2], x.w - Y[i][3]);
+        for (int q = 0; q < 8; ++q) {
+            const float4 x = __ldg(p + q);
+            v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
         }
     }
 }
+__device__ __forceinline__ void zero32(float (&v)[32]) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = 0.f;
+}
+// 32 values of row `row` of a plain [64][kLD] buffer from column c0 (float4 reads).
+__device__ __forceinline__ void plain_row(float (&v)[32], const float *buf, int row, int c0) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float4 x = *reinterpret_cast<const float4 *>(buf + row * kLD + c0 + 4 * q);
+        v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
+    }
+}
+__device__ __forceinline__ void plain_row_store(float *buf, int row, int c0, const float (&v)[32]) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<float4 *>(buf + row * kLD + c0 + 4 * q) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+}
+// Row `row`, K = kofs .. kofs + 31 of a K-major 128B-swizzled tile with `rows` rows.
+__device__ __forceinline__ void b_row(unsigned char *tile, int rows, int row, int kofs, const float (&v)[32]) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<uint4 *>(tile + sw128_off(row, kofs + 4 * q, rows)) =
+            make_uint4(tf32r(v[4 * q]), tf32r(v[4 * q + 1]), tf32r(v[4 * q + 2]), tf32r(v[4 * q + 3]));
+}
+// Column k of the tile, rows n0 .. n0 + 31 (a transposed store of this thread's row).
+__device__ __forceinline__ void b_col(unsigned char *tile, int rows, int k, int n0, const float (&v)[32]) {
+#pragma unroll
+    for (int c = 0; c < 32; ++c) *reinterpret_cast<uint32_t *>(tile + sw128_off(n0 + c, k, rows)) = tf32r(v[c]);
+}
+// This thread's TMEM lane, 32 columns from taddr: tf32 operand values / raw reads.
+__device__ __forceinline__ void a_row(uint32_t taddr, const float (&v)[32]) {
+    uint32_t r[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] = tf32r(v[i]);
+    tmem_st32u(taddr, r);
+}
 
+// Keep entries of row `row`, columns c0 .. c0 + 31, whose column passes the mask; optionally negate.
+template <Mask M, bool kNegate>
+__device__ __forceinline__ void mask32(float (&v)[32], int row, int c0) {
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+        const float x = kNegate ? -v[c] : v[c];
+        v[c] = keep<M>(row, c0 + c) ? x : 0.f;
+    }
+}
+
+// D[dcol..] = A[tmem acol..] x B^T with B a K-major tile at bsaddr (atom_bytes per 32 K).
+__device__ __forceinline__ void mma_group(uint32_t tmem, uint32_t dcol, uint32_t acol, uint32_t bsaddr,
+                                          uint32_t atom_bytes, int n, int k) {
+    const uint32_t idesc = idesc_tf32(128, n);
+    for (int kq = 0; kq < k / 8; ++kq)
+        mma_tf32_tmem_a(tmem + dcol, tmem + acol + 8 * kq,
+                        sdesc_sw128(bsaddr + (kq >> 2) * atom_bytes + (kq & 3) * 32), idesc, kq > 0 ? 1u : 0u);
+}
+
+// Operands written -> thread 0 issues and commits -> every thread waits (bounded).
+// The outcome is uniform over the CTA; false after a timeout (reported).
+template <class F>
+__device__ __forceinline__ bool mma_round(uint32_t bar, uint32_t &phase, unsigned *status, F issue) {
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        tc_fence_after_sync();
+        issue();
+        mma_commit(bar);
+    }
+    const bool ok = mbar_wait_bounded(bar, phase, tcg::kMaxPolls);
+    phase ^= 1u;
+    const int all_ok = __syncthreads_and(ok ? 1 : 0);
+    tc_fence_after_sync();
+    if (!all_ok && threadIdx.x == 0) report(status, kDevTimeout);
+    return all_ok != 0;
+}
+
+// Inclusive cumulative sum of w over the chunk into Gm ([64][kLD]); scratch: 4 rows of kLD.
+__device__ void decay_cumsum(const BwdArgs &p, const Chunk &c, int h, float *Gm, float *scratch) {
+    {
+        const int t = threadIdx.x >> 2, cc = (threadIdx.x & 3) * 16;
+        const bool valid = t < c.len;
+        float x[16];
+        load16(x, p.w, false, ((size_t)(c.tb + (valid ? t : 0)) * p.H + h) * kN + cc, valid);
+        store16(Gm + t * kLD + cc, x);
+    }
+    __syncthreads();
+    const int ch = threadIdx.x & 63, qt = threadIdx.x >> 6;
+    float run = 0.f;
+    float part[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+        run += Gm[(qt * 16 + u) * kLD + ch];
+        part[u] = run;
+    }
+    scratch[qt * kLD + ch] = run;
+    __syncthreads();
+    float base = 0.f;
+    for (int q = 0; q < qt; ++q) base += scratch[q * kLD + ch];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) Gm[(qt * 16 + u) * kLD + ch] = part[u] + base;
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *sm = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    Chunk c;
+    if (!locate(p, blockIdx.x, c)) return;
+    const int h = blockIdx.y;
+    const uint32_t sbase = smem_addr(sm);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, hh = warp >> 2;
+    const int L = 32 * quad + lane, t = L & 63, c0 = 32 * hh;
+    const bool top = L < 64;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
+    float *rho = reinterpret_cast<float *>(sm + tcg::kVec), *gC = rho + 64, *carry = gC + 64;  // carry[2][64]
+    float *P0 = reinterpret_cast<float *>(sm + tcg::kPlain0), *P1p = reinterpret_cast<float *>(sm + tcg::kPlain1);
+    const uint32_t bar = sbase + tcg::kBar;
+    const size_t cidx = ((size_t)blockIdx.x * p.H + h) * kStateElems;
+    const size_t b0 = ((size_t)(blockIdx.x + c.seq) * p.H + h) * kStateElems;
+    const size_t b1 = b0 + (size_t)p.H * kStateElems;
+    const bool row_valid = t < c.len;
+    const size_t roff = ((size_t)(c.tb + (row_valid ? t : 0)) * p.H + h) * kN + c0;  // this thread's token row, half
+
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(sbase + tcg::kBar + 8, tcg::kTmemCols);
+    decay_cumsum(p, c, h, P0, P1p);  // ends with a barrier
+    if (tid < 64) {
+        rho[tid] = P0[31 * kLD + tid];
+        gC[tid] = P0[63 * kLD + tid];
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm + tcg::kBar + 8);
+    const uint32_t tl = tmem + lane_off + c0;  // this thread's lane, column half
+    uint32_t phase = 0;
+    bool ok = true;
+    float v[32], x[32];
+
+    // ---- scaled operands: top rows Q, K; bottom rows Cm, R
+    {
+        float g[32], gx[32], kk[32];
+        plain_row(g, P0, t, c0);
+        if (t > 0) plain_row(gx, P0, t - 1, c0); else zero32(gx);
+        if (row_valid) load32(kk, p.kk, p.x_bf16, roff); else zero32(kk);
+        if (top) {
+            if (row_valid) load32(x, p.k, p.x_bf16, roff); else zero32(x);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float rh = rho[c0 + i];
+                v[i] = kk[i] * __expf(gx[i] - rh);     // Q
+                x[i] = x[i] * __expf(rh - g[i]);       // K
+            }
+            a_row(tl + 0, v);
+            a_row(tl + 256, x);
+            b_row(sm + tcg::kBG, 256, 64 + t, c0, x);
+            b_row(sm + tcg::kBG, 256, 192 + t, c0, v);
+            b_col(sm + tcg::kBF1, 64, 128 + t, c0, v);  // Q^c
+            b_col(sm + tcg::kBF2, 64, 64 + t, c0, x);   // K^c
+        } else {
+            float a[32];
+            if (row_valid) { load32(a, p.a, p.x_bf16, roff); load32(x, p.r, p.x_bf16, roff); }
+            else { zero32(a); zero32(x); }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float rh = rho[c0 + i];
+                v[i] = kk[i] * a[i] * __expf(rh - g[i]);  // Cm
+                x[i] = x[i] * __expf(g[i] - rh);          // R
+            }
+            a_row(tl + 0, v);
+            b_row(sm + tcg::kBG, 256, t, c0, v);
+            b_row(sm + tcg::kBG, 256, 128 + t, c0, x);
+            b_col(sm + tcg::kBF1, 64, 64 + t, c0, x);   // R^c
+            b_col(sm + tcg::kBF2, 64, 128 + t, c0, v);  // Cm^c
+        }
+    }
+    ok = mma_round(bar, phase, p.status, [&] {
+        mma_group(tmem, 64, 0, sbase + tcg::kBG, tcg::kAtom256, 192, 64);
+        mma_group(tmem, 320, 256, sbase + tcg::kBG + 128 * 128, tcg::kAtom256, 128, 64);
+    });
+
+    if (ok) {
+        // ---- Grams out: Lc -> plain; A_YY2 = [Q | Lk] (top), [Cm | Mc^T] (bottom); A_F3 = [K | Mk^T | -Lk^T]
+        if (top) {
+            tmem_ld32(tl + 64, v);
+            mask32<kStrictLower, false>(v, t, c0);
+            plain_row_store(P1p, t, c0, v);
+            tmem_ld32(tl + 128, v);
+            mask32<kStrictLower, false>(v, t, c0);
+            a_row(tl + 64, v);
+            tmem_ld32(tl + 320, v);
+            mask32<kUpper, false>(v, t, c0);
+            a_row(tl + 320, v);
+            tmem_ld32(tl + 384, v);
+            mask32<kStrictUpper, true>(v, t, c0);
+            a_row(tl + 384, v);
+        } else {
+            tmem_ld32(tl + 192, v);
+            mask32<kUpper, false>(v, t, c0);
+            a_row(tl + 64, v);
+        }
+        __syncthreads();  // Lc complete; B_G no longer read
+
+        // ---- B tiles from the states, V and dO; the carry rowsum(Ghat .* S_C)
+        if (top) {
+            float gh[32], sc[32];
+            const float *s0row = p.Sck + b0 + t * kN + c0;
+            const float *ghrow = p.Eck + cidx + t * kN + c0;
+            const float *scrow = p.Sck + b1 + t * kN + c0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 a4 = __ldg(reinterpret_cast<const float4 *>(s0row) + q);
+                const float4 g4 = __ldg(reinterpret_cast<const float4 *>(ghrow) + q);
+                const float4 s4 = __ldg(reinterpret_cast<const float4 *>(scrow) + q);
+                v[4 * q] = a4.x; v[4 * q + 1] = a4.y; v[4 * q + 2] = a4.z; v[4 * q + 3] = a4.w;
+                gh[4 * q] = g4.x; gh[4 * q + 1] = g4.y; gh[4 * q + 2] = g4.z; gh[4 * q + 3] = g4.w;
+                sc[4 * q] = s4.x; sc[4 * q + 1] = s4.y; sc[4 * q + 2] = s4.z; sc[4 * q + 3] = s4.w;
+            }
+            float part = 0.f;
+            const float s0s = __expf(rho[t]), gs = __expf(gC[t] - rho[t]);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                part = fmaf(gh[i], sc[i], part);
+                v[i] *= s0s;   // S0'
+                gh[i] *= gs;   // G'
+            }
+            carry[hh * 64 + t] = part;
+            b_col(sm + tcg::kBY, 64, t, c0, v);         // S0'^T
+            b_row(sm + tcg::kBF2, 64, t, c0, v);        // S0'
+            b_col(sm + tcg::kBF3, 64, t, c0, gh);       // G'^T
+            b_row(sm + tcg::kBF1, 64, t, c0, gh);       // G'
+        } else {
+            if (row_valid) load32(v, p.v, p.x_bf16, roff); else zero32(v);
+            b_col(sm + tcg::kBY, 64, 64 + t, c0, v);    // V^c
+            if (row_valid) load32(v, p.d_o, false, roff); else zero32(v);
+            b_col(sm + tcg::kBF3, 64, 64 + t, c0, v);   // dO^c
+        }
+        unit_lower_inverse(P1p, P0, reinterpret_cast<float *>(sm + tcg::kBF3 + 32768));
+        ok = mma_round(bar, phase, p.status, [&] {
+            mma_group(tmem, 128, 0, sbase + tcg::kBY, tcg::kAtom64, 64, 128);
+            mma_group(tmem, 192, 0, sbase + tcg::kBF3, tcg::kAtom64, 64, 128);
+        });
+    }
+
+    if (ok) {
+        // ---- Y -> Y^c, Y2 -> Y2^c; T rows (cols 0..63) and T^T rows (64..127) in the top lanes
+        if (top) {
+            tmem_ld32(tl + 128, v);
+            b_col(sm + tcg::kBY, 64, t, c0, v);
+            plain_row(x, P0, t, c0);
+            a_row(tl + 0, x);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) x[i] = P0[(c0 + i) * kLD + t];
+            a_row(tl + 64, x);
+        } else {
+            tmem_ld32(tl + 192, v);
+            b_col(sm + tcg::kBY + 16384, 64, t, c0, v);
+        }
+        ok = mma_round(bar, phase, p.status, [&] {
+            mma_group(tmem, 128, 0, sbase + tcg::kBY, tcg::kAtom64, 64, 64);           // Z = T Y (top)
+            mma_group(tmem, 192, 64, sbase + tcg::kBY + 16384, tcg::kAtom64, 64, 64);  // U = T^T Y2 (top)
+        });
+    }
+
+    if (ok) {
+        // ---- Z and U out; A_P = [Z; V], A_Pt = [U; dO], B_P = [dO; U], B_Pt = [V; Z], U^c into B_F3
+        unsigned char *bp = sm + tcg::kBY, *bpt = sm + tcg::kPlain0;
+        if (top) {
+            tmem_ld32(tl + 128, v);  // Z row t
+            tmem_ld32(tl + 192, x);  // U row t
+            a_row(tl + 0, v);
+            b_row(bpt, 128, 64 + t, c0, v);
+            b_col(sm + tcg::kBF3, 64, 128 + t, c0, x);
+            b_row(bp, 128, 64 + t, c0, x);
+            a_row(tl + 448, x);
+        } else {
+            if (row_valid) load32(v, p.v, p.x_bf16, roff); else zero32(v);
+            if (row_valid) load32(x, p.d_o, false, roff); else zero32(x);
+            a_row(tl + 0, v);
+            b_row(bpt, 128, t, c0, v);
+            b_row(bp, 128, t, c0, x);
+            a_row(tl + 448, x);
+        }
+        ok = mma_round(bar, phase, p.status, [&] {
+            mma_group(tmem, 192, 256, sbase + tcg::kBF3, tcg::kAtom64, 64, 192);  // dV (top)
+            mma_group(tmem, 64, 0, sbase + tcg::kBY, tcg::kAtom128, 128, 64);      // P
+        });
+    }
+
+    if (ok) {
+        if (top) {
+            tmem_ld32(tl + 192, v);  // dV row t
+            if (row_valid) {
+                float *dst = p.dv + ((size_t)(c.tb + t) * p.H + h) * kN + c0;
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    reinterpret_cast<float4 *>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            }
+        }
+        ok = mma_round(bar, phase, p.status, [&] {
+            mma_group(tmem, 320, 448, sbase + tcg::kPlain0, tcg::kAtom128, 128, 64);  // Pt
+        });
+    }
+
+    if (ok) {
+        // ---- masks in place: A_F1 = [Z | P3 | -P4 ; V | P1 | -P2] at 0, A_F2 = [U | P2^T | -P4^T ; dO | P1^T | -P3^T] at 256
+        tmem_ld32(tl + 64, v);
+        mask32<kUpper, false>(v, t, c0);
+        a_row(tl + 64, v);
+        tmem_ld32(tl + 128, v);
+        mask32<kStrictUpper, true>(v, t, c0);
+        a_row(tl + 128, v);
+        if (top) {
+            tmem_ld32(tl + 320, v);
+            mask32<kStrictLower, false>(v, t, c0);
+            a_row(tl + 320, v);
+            tmem_ld32(tl + 384, v);
+            mask32<kStrictLower, true>(v, t, c0);
+            a_row(tl + 384, v);
+        } else {
+            tmem_ld32(tl + 320, v);
+            mask32<kLower, false>(v, t, c0);
+            a_row(tl + 320, v);
+            tmem_ld32(tl + 384, v);
+            mask32<kLower, true>(v, t, c0);
+            a_row(tl + 384, v);
+        }
+        tmem_ld32(tl + 448, v);
+        a_row(tl + 256, v);
+        ok = mma_round(bar, phase, p.status, [&] {
+            mma_group(tmem, 192, 0, sbase + tcg::kBF1, tcg::kAtom64, 64, 192);    // [dC; dK]
+            mma_group(tmem, 448, 256, sbase + tcg::kBF2, tcg::kAtom64, 64, 192);  // [dKr; dR]
+        });
+    }
+
+    if (ok) {
+        // ---- epilogue: top rows hold dC, dKr; bottom rows dK, dR.  Each half writes its
+        // part of W = r dr - k dk - c dC + kk dKr; the reverse cumulative sum adds them.
+        float *Gm = reinterpret_cast<float *>(sm + 0);
+        float *PW = reinterpret_cast<float *>(sm + 17408);  // top part, then the cumulative sum
+        float *PB = reinterpret_cast<float *>(sm + 34816);  // bottom part
+        decay_cumsum(p, c, h, Gm, reinterpret_cast<float *>(sm + 52224));
+        float g[32], acc1[32], acc2[32];
+        plain_row(g, Gm, t, c0);
+        tmem_ld32(tl + 192, acc1);  // top dC, bottom dK
+        tmem_ld32(tl + 448, acc2);  // top dKr, bottom dR
+        const size_t go = ((size_t)(c.tb + t) * p.H + h) * kN + c0;
+        float Y[32];
+        if (top) {
+            float gx[32], kk[32], a[32];
+            if (t > 0) plain_row(gx, Gm, t - 1, c0); else zero32(gx);
+            if (row_valid) { load32(kk, p.kk, p.x_bf16, roff); load32(a, p.a, p.x_bf16, roff); }
+            else { zero32(kk); zero32(a); }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float rh = rho[c0 + i];
+                const float dC = -acc1[i] * __expf(rh - g[i]);
+                const float dKr = -acc2[i] * __expf(gx[i] - rh);
+                Y[i] = kk[i] * dKr;
+                x[i] = Y[i] - kk[i] * a[i] * dC;  // - c dC + kk dKr
+                acc1[i] = kk[i] * dC;             // da
+                acc2[i] = dKr + a[i] * dC;        // dkk
+            }
+            plain_row_store(PW, t, c0, x);
+            if (row_valid) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    reinterpret_cast<float4 *>(p.da + go)[q] = make_float4(acc1[4 * q], acc1[4 * q + 1], acc1[4 * q + 2], acc1[4 * q + 3]);
+                    reinterpret_cast<float4 *>(p.dkk + go)[q] = make_float4(acc2[4 * q], acc2[4 * q + 1], acc2[4 * q + 2], acc2[4 * q + 3]);
+                }
+            }
+        } else {
+            float rr[32], kv[32];
+            if (row_valid) { load32(rr, p.r, p.x_bf16, roff); load32(kv, p.k, p.x_bf16, roff); }
+            else { zero32(rr); zero32(kv); }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float rh = rho[c0 + i];
+                const float dK = acc1[i] * __expf(rh - g[i]);
+                const float dR = acc2[i] * __expf(g[i] - rh);
+                x[i] = rr[i] * dR - kv[i] * dK;  // r dr - k dk
+                acc1[i] = dK;
+                acc2[i] = dR;
+            }
+            plain_row_store(PB, t, c0, x);
+            if (row_valid) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    reinterpret_cast<float4 *>(p.dk + go)[q] = make_float4(acc1[4 * q], acc1[4 * q + 1], acc1[4 * q + 2], acc1[4 * q + 3]);
+                    reinterpret_cast<float4 *>(p.dr + go)[q] = make_float4(acc2[4 * q], acc2[4 * q + 1], acc2[4 * q + 2], acc2[4 * q + 3]);
+                }
+            }
+        }
+        __syncthreads();
+        {
+            // reverse inclusive cumulative sum over tokens per channel, plus the carry
+            float *scratch = reinterpret_cast<float *>(sm + 52224);
+            const int ch = tid & 63, qt = tid >> 6;
+            float run = 0.f;
+            float part[16];
+#pragma unroll
+            for (int u = 15; u >= 0; --u) {
+                run += PW[(qt * 16 + u) * kLD + ch] + PB[(qt * 16 + u) * kLD + ch];
+                part[u] = run;
+            }
+            scratch[qt * kLD + ch] = run;
+            __syncthreads();
+            float base = carry[ch] + carry[64 + ch];
+            for (int q = qt + 1; q < 4; ++q) base += scratch[q * kLD + ch];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) PW[(qt * 16 + u) * kLD + ch] = part[u] + base;
+            __syncthreads();
+        }
+        if (top && row_valid) {
+            plain_row(v, PW, t, c0);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                reinterpret_cast<float4 *>(p.dw + go)[q] = make_float4(v[4 * q] - Y[4 * q], v[4 * q + 1] - Y[4 * q + 1],
+                                                                       v[4 * q + 2] - Y[4 * q + 2], v[4 * q + 3] - Y[4 * q + 3]);
+        }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, tcg::kTmemCols);
+}
 }  // namespace
 
 // Upper bound on the chunks of any packing of T_total tokens into num_seqs sequences.
@@ -789,7 +1100,7 @@ cudaError_t launch_prefill_backward(const BackwardArgs &b, void *workspace, cuda
     if (attr_dev != dev) {
         e = cudaFuncSetAttribute(bwd_summary_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSummarySmem);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(bwd_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGradSmem);
+            e = cudaFuncSetAttribute(bwd_grad_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tcg::kAlloc);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(bwd_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kChainSmem);
         if (e != cudaSuccess) return e;
@@ -810,6 +1121,7 @@ cudaError_t launch_prefill_backward(const BackwardArgs &b, void *workspace, cuda
     p.dsf = b.d_final_state;
     p.dr = b.dr; p.dw = b.dw; p.dk = b.dk; p.dv = b.dv; p.dkk = b.dkk; p.da = b.da;
     p.ds0 = b.d_initial_state;
+    p.status = b.status;
     p.chunk_base = reinterpret_cast<int32_t *>(ws);
     p.Sck = reinterpret_cast<float *>(ws + table);
     p.Ack = p.Sck + (size_t)(nc + b.num_seqs) * plane;
@@ -830,7 +1142,7 @@ cudaError_t launch_prefill_backward(const BackwardArgs &b, void *workspace, cuda
     if (e != cudaSuccess) return e;
     if (nc > 0) {
         const dim3 grid((unsigned)nc, (unsigned)b.H);
-        bwd_grad_kernel<<<grid, kThreads, kGradSmem, stream>>>(p);
+        bwd_grad_tc_kernel<<<grid, kThreads, tcg::kAlloc, stream>>>(p);
         e = cudaGetLastError();
     }
     return e;

