@@ -40,8 +40,10 @@
 //   3. chains (one CTA per sequence, head and direction): the states at every
 //      chunk boundary forward, the adjoints at every chunk end backward.
 //   4. gradients (one CTA per chunk and head, all in parallel).
-// The products are 64 x 64 x 64 fp32 on the CUDA cores (4 x 4 register tiles,
-// operands in shared memory); only the two chains are sequential.
+// The summary and the chains multiply in fp32 on the CUDA cores (4 x 4 register
+// tiles, operands in shared memory), so the carried states and adjoints keep
+// fp32 accuracy; the gradient pass runs its products on the tensor cores (tf32
+// operands, fp32 accumulation).  Only the two chains are sequential.
 #include <cuda_bf16.h>
 
 #include <cstdint>

@@ -5,13 +5,15 @@ The oracle is the token-serial reverse-mode derivative of the recurrence
 sees exactly the values the GPU sees (bf16 inputs widened exactly; d_o and the
 states in fp32).
 
-Bound: max|gpu - oracle| / max|oracle| <= 1e-4 per gradient tensor.  The
-backward computes in fp32 throughout (64 x 64 x 64 products on the CUDA cores,
-the 64 x 64 unit-lower-triangular inverse, the two chunk chains), so its error
-is fp32 rounding grown by the chunk algebra's products and chains: the
-products have length 64 and the decay factors are taken relative to the
-chunk's 32nd token, which keeps the operand scales within e^{+-20} for the
-drawn w; the measured errors at every size below stay under 2e-5.
+Bound: max|gpu - oracle| / max|oracle| <= 2e-3 per gradient tensor.  The
+chunk summaries and the two chains (the carried states and adjoints) are fp32
+on the CUDA cores; the per-chunk gradient products run on the tensor cores with
+tf32 operands (each rounded to 11 significant bits, relative error <= 2^-12)
+and fp32 accumulation.  A gradient passes through at most four such rounded
+products (Gram -> Y -> Z -> P -> final), so its error is a few times 2^-12 of
+the largest term: about 1e-3, the same order as the bf16-input forward bound;
+the measured maximum over every case below, the 2.9B full-size sample included,
+is 9.4e-4, and d_initial_state (chains only) stays under 1e-6.
 """
 import numpy as np
 import pytest
