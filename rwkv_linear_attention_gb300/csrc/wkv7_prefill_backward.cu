@@ -40,10 +40,10 @@
 //   3. chains (one CTA per sequence, head and direction): the states at every
 //      chunk boundary forward, the adjoints at every chunk end backward.
 //   4. gradients (one CTA per chunk and head, all in parallel).
-// The summary and the chains multiply in fp32 on the CUDA cores (4 x 4 register
-// tiles, operands in shared memory), so the carried states and adjoints keep
-// fp32 accuracy; the gradient pass runs its products on the tensor cores (tf32
-// operands, fp32 accumulation).  Only the two chains are sequential.
+// The summary and gradient passes run their products on the tensor cores
+// (tcgen05, tf32 operands, fp32 accumulation in tensor memory); the chains
+// multiply in fp32 on the CUDA cores (4 x 4 register tiles, operands in shared
+// memory).  Only the two chains are sequential.
 #include <cuda_bf16.h>
 
 #include <cstdint>
@@ -62,8 +62,6 @@ constexpr int kMat = kC * kLD;    // floats per 64 x 64 buffer
 constexpr int kThreads = 256;
 constexpr size_t kMatBytes = (size_t)kMat * sizeof(float);
 constexpr size_t kStateElems = (size_t)kN * kN;
-constexpr int kSummaryBufs = 11;
-constexpr size_t kSummarySmem = kSummaryBufs * kMatBytes + 2 * kN * sizeof(float);
 constexpr size_t kChainSmem = 3 * kMatBytes;
 
 struct BwdArgs {
@@ -91,13 +89,6 @@ struct BwdArgs {
 
 __device__ __forceinline__ int tile_row() { return (threadIdx.x >> 4) * 4; }
 __device__ __forceinline__ int tile_col() { return (threadIdx.x & 15) * 4; }
-
-__device__ __forceinline__ void tile_zero(float (&acc)[4][4]) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-}
 
 // acc[i][j] += (or -=) sum_{k in [k0, k1)} opA(m0 + i, k) * B[k][n0 + j], with
 // opA(m, k) = A[m][k] (kTA = false) or A[k][m] (kTA = true); k0, k1 multiples of 4.
@@ -138,10 +129,6 @@ __device__ __forceinline__ void mm(float (&acc)[4][4], const float *__restrict__
     }
 }
 
-// k ranges that skip the zero half of a triangular left operand for this thread's rows.
-__device__ __forceinline__ int upto_diag() { return tile_row() + 4; }  // opA lower: k <= m
-__device__ __forceinline__ int from_diag() { return tile_row(); }      // opA upper: k >= m
-
 __device__ __forceinline__ void tile_store(float *dst, const float (&acc)[4][4]) {
     const int m0 = tile_row(), n0 = tile_col();
 #pragma unroll
@@ -158,26 +145,6 @@ __device__ __forceinline__ bool keep(int row, int col) {
     if (M == kUpper) return col >= row;
     return col > row;
 }
-// Whether this thread's whole 4 x 4 tile is masked out.
-template <Mask M>
-__device__ __forceinline__ bool tile_empty() {
-    const int m0 = tile_row(), n0 = tile_col();
-    if (M == kStrictLower) return n0 >= m0 + 3;
-    if (M == kLower) return n0 > m0 + 3;
-    if (M == kUpper) return n0 + 3 < m0;
-    return n0 + 3 <= m0;
-}
-template <Mask M>
-__device__ __forceinline__ void tile_store_masked(float *dst, float (&acc)[4][4]) {
-    const int m0 = tile_row(), n0 = tile_col();
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            if (!keep<M>(m0 + i, n0 + j)) acc[i][j] = 0.f;
-    tile_store(dst, acc);
-}
-
 // Global [64][64] fp32 (row-major, 256 B rows) <-> shared [64][kLD]; nullptr loads zeros.
 __device__ __forceinline__ void load_state(float *dst, const float *src) {
 #pragma unroll
@@ -193,20 +160,6 @@ __device__ __forceinline__ void store_state(float *dst, const float *src) {
         const int e = threadIdx.x + q * kThreads, row = e >> 4, c4 = (e & 15) * 4;
         *reinterpret_cast<float4 *>(dst + row * kN + c4) = *reinterpret_cast<const float4 *>(src + row * kLD + c4);
     }
-}
-
-// dst[j][i] = src[i][j] for a 64 x 64 buffer (4 x 4 blocks per thread).
-__device__ __forceinline__ void transpose(float *dst, const float *src) {
-    const int m0 = tile_row(), n0 = tile_col();
-    float x[4][4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float4 v = *reinterpret_cast<const float4 *>(src + (m0 + i) * kLD + n0);
-        x[i][0] = v.x; x[i][1] = v.y; x[i][2] = v.z; x[i][3] = v.w;
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-        *reinterpret_cast<float4 *>(dst + (n0 + j) * kLD + m0) = make_float4(x[0][j], x[1][j], x[2][j], x[3][j]);
 }
 
 // One token row (64 channels) of a packed [T_total, H, 64] input: 16 values
@@ -267,77 +220,6 @@ __device__ __forceinline__ bool locate(const BwdArgs &p, int g, Chunk &c) {
     return true;
 }
 
-// Loads the chunk and builds the scaled operands.  On return (after a barrier):
-//   Gm = g (inclusive cumulative log-decay), R, Q, K, Cm token-major, Kc, Cc
-//   channel-major (K^T, Cm^T), V, dO; rho[i] = g[31][i], gC[i] = g[63][i].
-__device__ void build_operands(const BwdArgs &p, const Chunk &c, int h, float *Gm, float *R, float *Q, float *K,
-                               float *Cm, float *Kc, float *Cc, float *V, float *dO, float *rho, float *gC) {
-    const int t = threadIdx.x >> 2, c0 = (threadIdx.x & 3) * 16;
-    const bool valid = t < c.len;
-    const size_t off = ((size_t)(c.tb + (valid ? t : 0)) * p.H + h) * kN + c0;
-    float x[16];
-    load16(x, p.w, false, off, valid);
-    store16(Gm + t * kLD + c0, x);
-    load16(x, p.r, p.x_bf16, off, valid);
-    store16(R + t * kLD + c0, x);
-    load16(x, p.k, p.x_bf16, off, valid);
-    store16(K + t * kLD + c0, x);
-    load16(x, p.kk, p.x_bf16, off, valid);
-    store16(Q + t * kLD + c0, x);
-    load16(x, p.a, p.x_bf16, off, valid);
-    store16(Cm + t * kLD + c0, x);
-    load16(x, p.v, p.x_bf16, off, valid);
-    store16(V + t * kLD + c0, x);
-    load16(x, p.d_o, false, off, valid);
-    store16(dO + t * kLD + c0, x);
-    __syncthreads();
-
-    // inclusive cumulative sum of w over the chunk, per channel: 4 threads per
-    // channel, 16 tokens each, then the earlier quarters' totals.
-    {
-        const int ch = threadIdx.x & 63, qt = threadIdx.x >> 6;
-        float run = 0.f;
-        float part[16];
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            run += Gm[(qt * 16 + u) * kLD + ch];
-            part[u] = run;
-        }
-        // quarter totals through Kc's first rows (free until the scaling pass)
-        Kc[qt * kLD + ch] = run;
-        __syncthreads();
-        float base = 0.f;
-        for (int q = 0; q < qt; ++q) base += Kc[q * kLD + ch];
-#pragma unroll
-        for (int u = 0; u < 16; ++u) Gm[(qt * 16 + u) * kLD + ch] = part[u] + base;
-        __syncthreads();
-    }
-    if (threadIdx.x < kN) {
-        rho[threadIdx.x] = Gm[31 * kLD + threadIdx.x];
-        gC[threadIdx.x] = Gm[63 * kLD + threadIdx.x];
-    }
-    __syncthreads();
-
-    // scaled operands and the channel-major copies of K and Cm
-#pragma unroll 4
-    for (int q = 0; q < 16; ++q) {
-        const int e = threadIdx.x + q * kThreads, tt = e >> 6, ch = e & 63;
-        const float g = Gm[tt * kLD + ch];
-        const float gx = tt > 0 ? Gm[(tt - 1) * kLD + ch] : 0.f;
-        const float rh = rho[ch];
-        const float up = expf(g - rh), dn = expf(rh - g), upx = expf(gx - rh);
-        const float kkv = Q[tt * kLD + ch], av = Cm[tt * kLD + ch];
-        R[tt * kLD + ch] *= up;
-        Q[tt * kLD + ch] = kkv * upx;
-        const float kv = K[tt * kLD + ch] * dn, cv = kkv * av * dn;
-        K[tt * kLD + ch] = kv;
-        Cm[tt * kLD + ch] = cv;
-        Kc[ch * kLD + tt] = kv;
-        Cc[ch * kLD + tt] = cv;
-    }
-    __syncthreads();
-}
-
 // T = (I + Lc)^{-1} for the strictly lower Lc: the four 16 x 16 diagonal blocks by
 // forward substitution (one thread per column), then the blocks below them by
 // T_IJ = -T_II sum_{K=J}^{I-1} Lc_IK T_KJ, one block diagonal at a time.
@@ -388,15 +270,6 @@ __device__ void unit_lower_inverse(const float *Lc, float *T, float *tmp) {
     }
 }
 
-// Masked Gram product out = mask(A B) with B channel-major (so out[t][s] = A_t . X_s).
-template <Mask M>
-__device__ __forceinline__ void gram(float *out, const float *A, const float *Bc) {
-    float acc[4][4];
-    tile_zero(acc);
-    if (!tile_empty<M>()) mm<false, false>(acc, A, Bc, 0, kC);
-    tile_store_masked<M>(out, acc);
-}
-
 // ---------------------------------------------------------------------------
 // 1. chunk table: chunk_base[s] = sum_{s' < s} ceil(len_s' / 64).  A malformed
 // cu_seqlens (not starting at 0, decreasing, or not ending at T_total) is
@@ -438,176 +311,7 @@ __global__ void __launch_bounds__(1024) bwd_chunk_table_kernel(const int32_t *cu
 }
 
 // ---------------------------------------------------------------------------
-// 2. per-chunk summary: A, F (forward transition) and E (adjoint input)
-
-__global__ void __launch_bounds__(kThreads, 1) bwd_summary_kernel(BwdArgs p) {
-    extern __shared__ __align__(16) float sm[];
-    Chunk c;
-    if (!locate(p, blockIdx.x, c)) return;
-    const int h = blockIdx.y;
-    float *B0 = sm, *R = sm + 1 * kMat, *Q = sm + 2 * kMat, *K = sm + 3 * kMat, *Cm = sm + 4 * kMat;
-    float *V = sm + 5 * kMat, *dO = sm + 6 * kMat, *B7 = sm + 7 * kMat, *B8 = sm + 8 * kMat;
-    float *B9 = sm + 9 * kMat, *B10 = sm + 10 * kMat;
-    float *rho = sm + kSummaryBufs * kMat, *gC = rho + kN;
-
-    build_operands(p, c, h, B0, R, Q, K, Cm, B7, B8, V, dO, rho, gC);
-    // Grams: Lc -> B0 (the cumulative decay is no longer needed), Lk -> B9, Mc -> B10
-    gram<kStrictLower>(B0, Q, B8);
-    gram<kStrictLower>(B9, Q, B7);
-    gram<kLower>(B10, R, B8);
-    __syncthreads();
-    float *T = B7, *Lc = B0, *Lk = B9, *Mc = B10;
-    unit_lower_inverse(Lc, T, B8);
-
-    const int m0 = tile_row(), n0 = tile_col();
-    const size_t cidx = ((size_t)blockIdx.x * p.H + h) * kStateElems;
-    float acc[4][4];
-
-    // W1t = T^T Cm  ([t][i]; W1 = Cm^T T)
-    tile_zero(acc);
-    mm<true, false>(acc, T, Cm, from_diag(), kC);
-    tile_store(B8, acc);
-    __syncthreads();
-    // A = diag(e^{gC-rho}) (I - W1 Q) diag(e^{rho})
-    tile_zero(acc);
-    mm<true, false>(acc, B8, Q, 0, kC);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int row = m0 + i;
-        const float sr = expf(gC[row] - rho[row]);
-        float o[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int col = n0 + j;
-            o[j] = sr * ((row == col ? 1.f : 0.f) - acc[i][j]) * expf(rho[col]);
-        }
-        *reinterpret_cast<float4 *>(p.Ack + cidx + row * kN + n0) = make_float4(o[0], o[1], o[2], o[3]);
-    }
-    // LkV = Lk V -> B0 (Lc done)
-    tile_zero(acc);
-    mm<false, false>(acc, Lk, V, 0, upto_diag());
-    tile_store(B0, acc);
-    __syncthreads();
-    // F = diag(e^{gC-rho}) (K^T V - W1 LkV)
-    tile_zero(acc);
-    mm<true, false>(acc, K, V, 0, kC);
-    mm<true, true>(acc, B8, B0, 0, kC);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int row = m0 + i;
-        const float sr = expf(gC[row] - rho[row]);
-        *reinterpret_cast<float4 *>(p.Fck + cidx + row * kN + n0) =
-            make_float4(sr * acc[i][0], sr * acc[i][1], sr * acc[i][2], sr * acc[i][3]);
-    }
-    __syncthreads();  // B0 (LkV) and Lk reads done
-    // McdO = Mc^T dO -> B0 ; TQ = T Q -> B9
-    tile_zero(acc);
-    mm<true, false>(acc, Mc, dO, from_diag(), kC);
-    tile_store(B0, acc);
-    tile_zero(acc);
-    mm<false, false>(acc, T, Q, 0, upto_diag());
-    tile_store(B9, acc);
-    __syncthreads();
-    // E = diag(e^{rho}) (R^T dO - TQ^T McdO)
-    tile_zero(acc);
-    mm<true, false>(acc, R, dO, 0, kC);
-    mm<true, true>(acc, B9, B0, 0, kC);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int row = m0 + i;
-        const float sr = expf(rho[row]);
-        *reinterpret_cast<float4 *>(p.Eck + cidx + row * kN + n0) =
-            make_float4(sr * acc[i][0], sr * acc[i][1], sr * acc[i][2], sr * acc[i][3]);
-    }
-}
-
-// ---------------------------------------------------------------------------
-// 3. chains over the chunks of one (sequence, head): blockIdx.z = 0 runs the
-// states forward (S_{c+1} = A_c S_c + F_c, every boundary stored), 1 runs the
-// adjoint backward (Ghat_{c-1} = A_c^T Ghat_c + E_c; Ghat_c stored over E_c).
-
-__global__ void __launch_bounds__(kThreads) bwd_chain_kernel(BwdArgs p) {
-    extern __shared__ __align__(16) float sm[];
-    float *Am = sm, *Xm = sm + kMat, *Sm = sm + 2 * kMat;
-    const int s = blockIdx.x, h = blockIdx.y;
-    const bool adjoint = blockIdx.z == 1;
-    const int c0 = p.chunk_base[s], nch = p.chunk_base[s + 1] - c0;
-    const size_t pair = ((size_t)s * p.H + h) * kStateElems;
-    const float *init = adjoint ? (p.dsf ? p.dsf + pair : nullptr) : (p.s0 ? p.s0 + pair : nullptr);
-    const float *X = adjoint ? p.Eck : p.Fck;
-    load_state(Sm, init);
-    __syncthreads();
-    if (!adjoint) store_state(p.Sck + ((size_t)(c0 + s) * p.H + h) * kStateElems, Sm);
-    // The next step's A and F (or E) are fetched into registers while this step multiplies.
-    float4 pa[4], px[4];
-    const auto fetch = [&](int step) {
-        const int ci = adjoint ? nch - 1 - step : step;
-        const size_t cidx = ((size_t)(c0 + ci) * p.H + h) * kStateElems;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int e = threadIdx.x + q * kThreads, row = e >> 4, c4 = (e & 15) * 4;
-            pa[q] = __ldg(reinterpret_cast<const float4 *>(p.Ack + cidx + row * kN + c4));
-            px[q] = __ldg(reinterpret_cast<const float4 *>(X + cidx + row * kN + c4));
-        }
-    };
-    if (nch > 0) fetch(0);
-    for (int step = 0; step < nch; ++step) {
-        const int ci = adjoint ? nch - 1 - step : step;
-        const size_t cidx = ((size_t)(c0 + ci) * p.H + h) * kStateElems;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int e = threadIdx.x + q * kThreads, row = e >> 4, c4 = (e & 15) * 4;
-            *reinterpret_cast<float4 *>(Am + row * kLD + c4) = pa[q];
-            *reinterpret_cast<float4 *>(Xm + row * kLD + c4) = px[q];
-        }
-        __syncthreads();
-        if (step + 1 < nch) fetch(step + 1);
-        float acc[4][4];
-        const int m0 = tile_row(), n0 = tile_col();
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float4 x = *reinterpret_cast<const float4 *>(Xm + (m0 + i) * kLD + n0);
-            acc[i][0] = x.x; acc[i][1] = x.y; acc[i][2] = x.z; acc[i][3] = x.w;
-        }
-        if (adjoint) {
-            mm<true, false>(acc, Am, Sm, 0, kC);
-            store_state(p.Eck + cidx, Sm);  // the adjoint at this chunk's end (E already read)
-        } else {
-            mm<false, false>(acc, Am, Sm, 0, kC);
-        }
-        __syncthreads();
-        tile_store(Sm, acc);
-        __syncthreads();
-        if (!adjoint) store_state(p.Sck + ((size_t)(c0 + s + ci + 1) * p.H + h) * kStateElems, Sm);
-    }
-    if (adjoint && p.ds0) store_state(p.ds0 + pair, Sm);
-}
-
-// ---------------------------------------------------------------------------
-// 4. per-chunk gradients, on the tensor cores (tcgen05, tf32 operands, fp32
-// accumulation in tensor memory).
-//
-// Every product is one M = 128 MMA whose A operand sits in tensor memory (row m
-// in lane m) and whose B operand is a K-major 128-byte-swizzled tile in shared
-// memory (D = A B^T).  Two 64-row matrices share one MMA by taking the two
-// halves of the lanes: either the same B serves both (stacked rows), or two
-// MMAs with different B read the same A columns and each keeps one half.
-// Thread (warp w, lane l) owns TMEM lane L = 32 (w mod 4) + l, i.e. row
-// t = L mod 64 of the top (L < 64) or bottom matrix, and the 32 columns of half
-// w / 4 of every 64-column block.  Transposed operands come from a second MMA
-// (C^T = B A^T) or from transposed stores into the B tile, never from moving
-// data between lanes.
-//
-// Rounds (each: operands written -> one thread issues -> commit -> all wait):
-//   1  G1 = [Q; Cm] x [Cm; K; R]^T -> Lc, Lk (top), Mc^T (bottom);
-//      G2 = K x [R; Q]^T            -> Mk^T, Lk^T (top)
-//   2  Y  = [Q | Lk] x [S0'^T | V^c]^T (top);  Y2 = [Cm | Mc^T] x [G'^T | dO^c]^T (bottom)
-//   3  U  = T^T Y2 (top), Z = T Y (bottom), from one A holding T^T / T
-//   4  dV = [K | Mk^T | -Lk^T] x [G'^T | dO^c | U^c]^T;  P = [V; Z] x [dO; U]^T
-//   5  Pt = [U; dO] x [V; Z]^T                           (the transposed P blocks)
-//   6  [dK; dC]  = [V | P1 | -P2 ; Z | P3 | -P4] x [G' | R^c | Q^c]^T
-//      [dKr; dR] = [U | P2^T | -P4^T ; dO | P1^T | -P3^T] x [S0' | K^c | Cm^T]^T
-// then the epilogue scales by the decay factors and forms dr, dk, dkk, da, dw.
+// tensor-core helpers shared by the summary and gradient passes
 
 namespace tcg {
 // shared memory (bytes from a 1024-aligned base)
@@ -708,6 +412,16 @@ __device__ __forceinline__ void mma_group(uint32_t tmem, uint32_t dcol, uint32_t
                         sdesc_sw128(bsaddr + (kq >> 2) * atom_bytes + (kq & 3) * 32), idesc, kq > 0 ? 1u : 0u);
 }
 
+// As mma_group, with the A operand negated and/or accumulating onto D from the first step.
+__device__ __forceinline__ void mma_group_acc(uint32_t tmem, uint32_t dcol, uint32_t acol, uint32_t bsaddr,
+                                              uint32_t atom_bytes, int n, int k, bool negate, bool accumulate) {
+    const uint32_t idesc = idesc_tf32(128, n) | (negate ? kIdescNegateA : 0u);
+    for (int kq = 0; kq < k / 8; ++kq)
+        mma_tf32_tmem_a(tmem + dcol, tmem + acol + 8 * kq,
+                        sdesc_sw128(bsaddr + (kq >> 2) * atom_bytes + (kq & 3) * 32), idesc,
+                        (accumulate || kq > 0) ? 1u : 0u);
+}
+
 // Operands written -> thread 0 issues and commits -> every thread waits (bounded).
 // The outcome is uniform over the CTA; false after a timeout (reported).
 template <class F>
@@ -754,6 +468,301 @@ __device__ void decay_cumsum(const BwdArgs &p, const Chunk &c, int h, float *Gm,
     for (int u = 0; u < 16; ++u) Gm[(qt * 16 + u) * kLD + ch] = part[u] + base;
     __syncthreads();
 }
+
+// ---------------------------------------------------------------------------
+// 2. per-chunk summary on the tensor cores: A, F (forward transition) and E
+// (adjoint input).  Their products contract over tokens, so their left
+// operands have channels for rows: those come from identity products
+// ([I 0; 0 I] x [X | Y]^T puts X^T in the top lanes and Y^T in the bottom ones)
+// and from products whose own left operand already has channels for rows.
+// Rounds:
+//   1  G1 = [Q; Cm] x [Cm; K; R]^T -> Lc, Lk (top), Mc^T (bottom);
+//      [Cm^T; Q^T] and [K^T; R^T] by identity products
+//   2  Lk V (top), Mc^T dO (bottom); W1 = Cm^T T (top), W2 = Q^T T^T (bottom)
+//   3  F* = K^T V - W1 (Lk V) (top), E* = R^T dO - W2 (Mc^T dO) (bottom), A* = W1 Q (top)
+// then A = diag(e^{gC-rho})(I - A*)diag(e^{rho}), F = diag(e^{gC-rho}) F*, E = diag(e^{rho}) E*.
+
+namespace tcs {
+constexpr uint32_t kBG = 0;           // [Cm; K; R; Q], 256 rows x K 64 (64 KB), round 1; then round-2 tiles
+constexpr uint32_t kBVc = 0;          // V^c (16 KB), rounds 2 and 3
+constexpr uint32_t kBdOc = 16384;     // dO^c (16 KB), rounds 2 and 3
+constexpr uint32_t kBTt = 32768;      // rows t: T[s][t] (16 KB), round 2
+constexpr uint32_t kBTn = 49152;      // rows t: T[t][s] (16 KB), round 2
+constexpr uint32_t kBT1 = 65536;      // [Cm | Q] 64 x K 128 (32 KB), round 1; then (Lk V)^c, (Mc^T dO)^c
+constexpr uint32_t kBT2 = 98304;      // [K | R] 64 x K 128 (32 KB), round 1
+constexpr uint32_t kBQc = 131072;     // Q^c (16 KB), round 3
+constexpr uint32_t kPlain0 = 147456;  // fp32 64 x 68: the cumulative decay, then T
+constexpr uint32_t kPlain1 = 164864;  // fp32 64 x 68: Lc
+constexpr uint32_t kVec = 182272;     // rho[64], gC[64]
+constexpr uint32_t kBar = 182784;     // mbarrier, TMEM base slot
+constexpr uint32_t kBytes = 182800;
+constexpr uint32_t kAlloc = kBytes + 1024;
+}  // namespace tcs
+
+__global__ void __launch_bounds__(kThreads, 1) bwd_summary_tc_kernel(BwdArgs p) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *sm = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    Chunk c;
+    if (!locate(p, blockIdx.x, c)) return;
+    const int h = blockIdx.y;
+    const uint32_t sbase = smem_addr(sm);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, hh = warp >> 2;
+    const int L = 32 * quad + lane, t = L & 63, c0 = 32 * hh;
+    const bool top = L < 64;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
+    float *rho = reinterpret_cast<float *>(sm + tcs::kVec), *gC = rho + 64;
+    float *P0 = reinterpret_cast<float *>(sm + tcs::kPlain0), *P1p = reinterpret_cast<float *>(sm + tcs::kPlain1);
+    const uint32_t bar = sbase + tcs::kBar;
+    const size_t cidx = ((size_t)blockIdx.x * p.H + h) * kStateElems;
+    const bool row_valid = t < c.len;
+    const size_t roff = ((size_t)(c.tb + (row_valid ? t : 0)) * p.H + h) * kN + c0;
+
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(sbase + tcs::kBar + 8, tcg::kTmemCols);
+    decay_cumsum(p, c, h, P0, P1p);
+    if (tid < 64) {
+        rho[tid] = P0[31 * kLD + tid];
+        gC[tid] = P0[63 * kLD + tid];
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm + tcs::kBar + 8);
+    const uint32_t tl = tmem + lane_off + c0;
+    uint32_t phase = 0;
+    bool ok = true;
+    float v[32], x[32];
+
+    // ---- scaled operands (top rows Q, K; bottom rows Cm, R) and the identity [I 0; 0 I] at 256..383
+    {
+        float g[32], gx[32], kk[32];
+        plain_row(g, P0, t, c0);
+        if (t > 0) plain_row(gx, P0, t - 1, c0); else zero32(gx);
+        if (row_valid) load32(kk, p.kk, p.x_bf16, roff); else zero32(kk);
+        if (top) {
+            if (row_valid) load32(x, p.k, p.x_bf16, roff); else zero32(x);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float rh = rho[c0 + i];
+                v[i] = kk[i] * __expf(gx[i] - rh);  // Q
+                x[i] = x[i] * __expf(rh - g[i]);    // K
+            }
+            a_row(tl + 0, v);
+            b_row(sm + tcs::kBG, 256, 64 + t, c0, x);
+            b_row(sm + tcs::kBG, 256, 192 + t, c0, v);
+            b_row(sm + tcs::kBT1, 64, t, 64 + c0, v);
+            b_row(sm + tcs::kBT2, 64, t, c0, x);
+            b_col(sm + tcs::kBQc, 64, t, c0, v);
+        } else {
+            float a[32];
+            if (row_valid) { load32(a, p.a, p.x_bf16, roff); load32(x, p.r, p.x_bf16, roff); }
+            else { zero32(a); zero32(x); }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float rh = rho[c0 + i];
+                v[i] = kk[i] * a[i] * __expf(rh - g[i]);  // Cm
+                x[i] = x[i] * __expf(g[i] - rh);          // R
+            }
+            a_row(tl + 0, v);
+            b_row(sm + tcs::kBG, 256, t, c0, v);
+            b_row(sm + tcs::kBG, 256, 128 + t, c0, x);
+            b_row(sm + tcs::kBT1, 64, t, c0, v);
+            b_row(sm + tcs::kBT2, 64, t, 64 + c0, x);
+        }
+        uint32_t id[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) id[i] = (top && c0 + i == t) ? 0x3f800000u : 0u;
+        tmem_st32u(tl + 256, id);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) id[i] = (!top && c0 + i == t) ? 0x3f800000u : 0u;
+        tmem_st32u(tl + 320, id);
+    }
+    ok = mma_round(bar, phase, p.status, [&] {
+        mma_group(tmem, 64, 0, sbase + tcs::kBG, tcg::kAtom256, 192, 64);         // G1
+        mma_group(tmem, 384, 256, sbase + tcs::kBT1, tcg::kAtom64, 64, 128);      // [Cm^T; Q^T]
+        mma_group(tmem, 448, 256, sbase + tcs::kBT2, tcg::kAtom64, 64, 128);      // [K^T; R^T]
+    });
+
+    if (ok) {
+        // ---- Lc -> plain; A_L = [Lk (top); Mc^T (bottom)] at 64
+        if (top) {
+            tmem_ld32(tl + 64, v);
+            mask32<kStrictLower, false>(v, t, c0);
+            plain_row_store(P1p, t, c0, v);
+            tmem_ld32(tl + 128, v);
+            mask32<kStrictLower, false>(v, t, c0);
+            a_row(tl + 64, v);
+        } else {
+            tmem_ld32(tl + 192, v);
+            mask32<kUpper, false>(v, t, c0);
+            a_row(tl + 64, v);
+            if (row_valid) load32(v, p.v, p.x_bf16, roff); else zero32(v);
+            b_col(sm + tcs::kBVc, 64, t, c0, v);
+            if (row_valid) load32(v, p.d_o, false, roff); else zero32(v);
+            b_col(sm + tcs::kBdOc, 64, t, c0, v);
+        }
+        __syncthreads();
+        unit_lower_inverse(P1p, P0, reinterpret_cast<float *>(sm + tcs::kBTt));
+        if (top) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) x[i] = P0[(c0 + i) * kLD + t];
+            b_row(sm + tcs::kBTt, 64, t, c0, x);  // rows t: T[s][t]
+        } else {
+            plain_row(x, P0, t, c0);
+            b_row(sm + tcs::kBTn, 64, t, c0, x);  // rows t: T[t][s]
+        }
+        ok = mma_round(bar, phase, p.status, [&] {
+            mma_group(tmem, 128, 64, sbase + tcs::kBVc, tcg::kAtom64, 64, 64);    // Lk V (top)
+            mma_group(tmem, 192, 64, sbase + tcs::kBdOc, tcg::kAtom64, 64, 64);   // Mc^T dO (bottom)
+            mma_group(tmem, 0, 384, sbase + tcs::kBTt, tcg::kAtom64, 64, 64);     // W1 = Cm^T T (top)
+            mma_group(tmem, 256, 384, sbase + tcs::kBTn, tcg::kAtom64, 64, 64);   // W2 = Q^T T^T (bottom)
+        });
+    }
+
+    if (ok) {
+        // ---- (Lk V)^c, (Mc^T dO)^c; W1, W2 rounded to tf32 in place
+        if (top) {
+            tmem_ld32(tl + 128, v);
+            b_col(sm + tcs::kBT1, 64, t, c0, v);
+            tmem_ld32(tl + 0, v);
+            a_row(tl + 0, v);
+        } else {
+            tmem_ld32(tl + 192, v);
+            b_col(sm + tcs::kBT1 + 16384, 64, t, c0, v);
+            tmem_ld32(tl + 256, v);
+            a_row(tl + 256, v);
+        }
+        ok = mma_round(bar, phase, p.status, [&] {
+            mma_group_acc(tmem, 64, 448, sbase + tcs::kBVc, tcg::kAtom64, 64, 64, false, false);         // K^T V
+            mma_group_acc(tmem, 64, 0, sbase + tcs::kBT1, tcg::kAtom64, 64, 64, true, true);             // - W1 (Lk V)
+            mma_group_acc(tmem, 128, 448, sbase + tcs::kBdOc, tcg::kAtom64, 64, 64, false, false);       // R^T dO
+            mma_group_acc(tmem, 128, 256, sbase + tcs::kBT1 + 16384, tcg::kAtom64, 64, 64, true, true);  // - W2 (Mc^T dO)
+            mma_group(tmem, 192, 0, sbase + tcs::kBQc, tcg::kAtom64, 64, 64);                            // W1 Q
+        });
+    }
+
+    if (ok) {
+        // ---- out: row i = t of A and F (top), of E (bottom)
+        const int i = t;
+        if (top) {
+            const float sr = __expf(gC[i] - rho[i]);
+            tmem_ld32(tl + 64, v);
+            float *dst = p.Fck + cidx + i * kN + c0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                reinterpret_cast<float4 *>(dst)[q] = make_float4(sr * v[4 * q], sr * v[4 * q + 1], sr * v[4 * q + 2], sr * v[4 * q + 3]);
+            tmem_ld32(tl + 192, v);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = sr * ((c0 + j == i ? 1.f : 0.f) - v[j]) * __expf(rho[c0 + j]);
+            dst = p.Ack + cidx + i * kN + c0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                reinterpret_cast<float4 *>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        } else {
+            const float sr = __expf(rho[i]);
+            tmem_ld32(tl + 128, v);
+            float *dst = p.Eck + cidx + i * kN + c0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                reinterpret_cast<float4 *>(dst)[q] = make_float4(sr * v[4 * q], sr * v[4 * q + 1], sr * v[4 * q + 2], sr * v[4 * q + 3]);
+        }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, tcg::kTmemCols);
+}
+// ---------------------------------------------------------------------------
+// 3. chains over the chunks of one (sequence, head): blockIdx.z = 0 runs the
+// states forward (S_{c+1} = A_c S_c + F_c, every boundary stored), 1 runs the
+// adjoint backward (Ghat_{c-1} = A_c^T Ghat_c + E_c; Ghat_c stored over E_c).
+
+__global__ void __launch_bounds__(kThreads) bwd_chain_kernel(BwdArgs p) {
+    extern __shared__ __align__(16) float sm[];
+    float *Am = sm, *Xm = sm + kMat, *Sm = sm + 2 * kMat;
+    const int s = blockIdx.x, h = blockIdx.y;
+    const bool adjoint = blockIdx.z == 1;
+    const int c0 = p.chunk_base[s], nch = p.chunk_base[s + 1] - c0;
+    const size_t pair = ((size_t)s * p.H + h) * kStateElems;
+    const float *init = adjoint ? (p.dsf ? p.dsf + pair : nullptr) : (p.s0 ? p.s0 + pair : nullptr);
+    const float *X = adjoint ? p.Eck : p.Fck;
+    load_state(Sm, init);
+    __syncthreads();
+    if (!adjoint) store_state(p.Sck + ((size_t)(c0 + s) * p.H + h) * kStateElems, Sm);
+    // The next step's A and F (or E) are fetched into registers while this step multiplies.
+    float4 pa[4], px[4];
+    const auto fetch = [&](int step) {
+        const int ci = adjoint ? nch - 1 - step : step;
+        const size_t cidx = ((size_t)(c0 + ci) * p.H + h) * kStateElems;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int e = threadIdx.x + q * kThreads, row = e >> 4, c4 = (e & 15) * 4;
+            pa[q] = __ldg(reinterpret_cast<const float4 *>(p.Ack + cidx + row * kN + c4));
+            px[q] = __ldg(reinterpret_cast<const float4 *>(X + cidx + row * kN + c4));
+        }
+    };
+    if (nch > 0) fetch(0);
+    for (int step = 0; step < nch; ++step) {
+        const int ci = adjoint ? nch - 1 - step : step;
+        const size_t cidx = ((size_t)(c0 + ci) * p.H + h) * kStateElems;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int e = threadIdx.x + q * kThreads, row = e >> 4, c4 = (e & 15) * 4;
+            *reinterpret_cast<float4 *>(Am + row * kLD + c4) = pa[q];
+            *reinterpret_cast<float4 *>(Xm + row * kLD + c4) = px[q];
+        }
+        __syncthreads();
+        if (step + 1 < nch) fetch(step + 1);
+        float acc[4][4];
+        const int m0 = tile_row(), n0 = tile_col();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float4 x = *reinterpret_cast<const float4 *>(Xm + (m0 + i) * kLD + n0);
+            acc[i][0] = x.x; acc[i][1] = x.y; acc[i][2] = x.z; acc[i][3] = x.w;
+        }
+        if (adjoint) {
+            mm<true, false>(acc, Am, Sm, 0, kC);
+            store_state(p.Eck + cidx, Sm);  // the adjoint at this chunk's end (E already read)
+        } else {
+            mm<false, false>(acc, Am, Sm, 0, kC);
+        }
+        __syncthreads();
+        tile_store(Sm, acc);
+        __syncthreads();
+        if (!adjoint) store_state(p.Sck + ((size_t)(c0 + s + ci + 1) * p.H + h) * kStateElems, Sm);
+    }
+    if (adjoint && p.ds0) store_state(p.ds0 + pair, Sm);
+}
+
+// ---------------------------------------------------------------------------
+// 4. per-chunk gradients, on the tensor cores (tcgen05, tf32 operands, fp32
+// accumulation in tensor memory).
+//
+// Every product is one M = 128 MMA whose A operand sits in tensor memory (row m
+// in lane m) and whose B operand is a K-major 128-byte-swizzled tile in shared
+// memory (D = A B^T).  Two 64-row matrices share one MMA by taking the two
+// halves of the lanes: either the same B serves both (stacked rows), or two
+// MMAs with different B read the same A columns and each keeps one half.
+// Thread (warp w, lane l) owns TMEM lane L = 32 (w mod 4) + l, i.e. row
+// t = L mod 64 of the top (L < 64) or bottom matrix, and the 32 columns of half
+// w / 4 of every 64-column block.  Transposed operands come from a second MMA
+// (C^T = B A^T) or from transposed stores into the B tile, never from moving
+// data between lanes.
+//
+// Rounds (each: operands written -> one thread issues -> commit -> all wait):
+//   1  G1 = [Q; Cm] x [Cm; K; R]^T -> Lc, Lk (top), Mc^T (bottom);
+//      G2 = K x [R; Q]^T            -> Mk^T, Lk^T (top)
+//   2  Y  = [Q | Lk] x [S0'^T | V^c]^T (top);  Y2 = [Cm | Mc^T] x [G'^T | dO^c]^T (bottom)
+//   3  U  = T^T Y2 (top), Z = T Y (bottom), from one A holding T^T / T
+//   4  dV = [K | Mk^T | -Lk^T] x [G'^T | dO^c | U^c]^T;  P = [V; Z] x [dO; U]^T
+//   5  Pt = [U; dO] x [V; Z]^T                           (the transposed P blocks)
+//   6  [dK; dC]  = [V | P1 | -P2 ; Z | P3 | -P4] x [G' | R^c | Q^c]^T
+//      [dKr; dR] = [U | P2^T | -P4^T ; dO | P1^T | -P3^T] x [S0' | K^c | Cm^T]^T
+// then the epilogue scales by the decay factors and forms dr, dk, dkk, da, dw.
 
 __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
     extern __shared__ unsigned char smem_raw[];
@@ -1082,6 +1091,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, tcg::kTmemCols);
 }
+
 }  // namespace
 
 // Upper bound on the chunks of any packing of T_total tokens into num_seqs sequences.
@@ -1100,7 +1110,7 @@ cudaError_t launch_prefill_backward(const BackwardArgs &b, void *workspace, cuda
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (attr_dev != dev) {
-        e = cudaFuncSetAttribute(bwd_summary_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSummarySmem);
+        e = cudaFuncSetAttribute(bwd_summary_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tcs::kAlloc);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(bwd_grad_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tcg::kAlloc);
         if (e == cudaSuccess)
@@ -1135,7 +1145,7 @@ cudaError_t launch_prefill_backward(const BackwardArgs &b, void *workspace, cuda
     if (e != cudaSuccess) return e;
     if (nc > 0) {
         const dim3 grid((unsigned)nc, (unsigned)b.H);
-        bwd_summary_kernel<<<grid, kThreads, kSummarySmem, stream>>>(p);
+        bwd_summary_tc_kernel<<<grid, kThreads, tcs::kAlloc, stream>>>(p);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
