@@ -442,15 +442,17 @@ __device__ __forceinline__ bool mma_round(uint32_t bar, uint32_t &phase, unsigne
     return all_ok != 0;
 }
 
-// Inclusive cumulative sum of w over the chunk into Gm ([64][kLD]); scratch: 4 rows of kLD.
-__device__ void decay_cumsum(const BwdArgs &p, const Chunk &c, int h, float *Gm, float *scratch) {
-    {
-        const int t = threadIdx.x >> 2, cc = (threadIdx.x & 3) * 16;
-        const bool valid = t < c.len;
-        float x[16];
-        load16(x, p.w, false, ((size_t)(c.tb + (valid ? t : 0)) * p.H + h) * kN + cc, valid);
-        store16(Gm + t * kLD + cc, x);
-    }
+// This thread's 16 values of w for the cumulative sum (row tid / 4, channels 16 (tid mod 4) ..).
+__device__ __forceinline__ void load_w16(float (&x)[16], const BwdArgs &p, const Chunk &c, int h) {
+    const int t = threadIdx.x >> 2, cc = (threadIdx.x & 3) * 16;
+    const bool valid = t < c.len;
+    load16(x, p.w, false, ((size_t)(c.tb + (valid ? t : 0)) * p.H + h) * kN + cc, valid);
+}
+
+// Inclusive cumulative sum of w over the chunk into Gm ([64][kLD]) from the values
+// of load_w16; scratch: 4 rows of kLD.  Ends with a barrier.
+__device__ void decay_cumsum_from(const float (&x)[16], float *Gm, float *scratch) {
+    store16(Gm + (threadIdx.x >> 2) * kLD + (threadIdx.x & 3) * 16, x);
     __syncthreads();
     const int ch = threadIdx.x & 63, qt = threadIdx.x >> 6;
     float run = 0.f;
@@ -467,6 +469,21 @@ __device__ void decay_cumsum(const BwdArgs &p, const Chunk &c, int h, float *Gm,
 #pragma unroll
     for (int u = 0; u < 16; ++u) Gm[(qt * 16 + u) * kLD + ch] = part[u] + base;
     __syncthreads();
+}
+
+__device__ void decay_cumsum(const BwdArgs &p, const Chunk &c, int h, float *Gm, float *scratch) {
+    float x[16];
+    load_w16(x, p, c, h);
+    decay_cumsum_from(x, Gm, scratch);
+}
+
+// 32 values of a 64 x 64 fp32 state row (global), or zeros.
+__device__ __forceinline__ void load_state32(float (&v)[32], const float *src) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float4 a4 = __ldg(reinterpret_cast<const float4 *>(src) + q);
+        v[4 * q] = a4.x; v[4 * q + 1] = a4.y; v[4 * q + 2] = a4.z; v[4 * q + 3] = a4.w;
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -524,6 +541,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_summary_tc_kernel(BwdArgs p) 
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(sbase + tcs::kBar + 8, tcg::kTmemCols);
+    float kk[32], ra[32], rb[32];  // top: kk, k; bottom: kk, a, r (fetched before the cumulative sum)
+    if (row_valid) {
+        load32(kk, p.kk, p.x_bf16, roff);
+        load32(ra, top ? p.k : p.a, p.x_bf16, roff);
+        if (!top) load32(rb, p.r, p.x_bf16, roff);
+    } else {
+        zero32(kk); zero32(ra); zero32(rb);
+    }
     decay_cumsum(p, c, h, P0, P1p);
     if (tid < 64) {
         rho[tid] = P0[31 * kLD + tid];
@@ -540,17 +565,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_summary_tc_kernel(BwdArgs p) 
 
     // ---- scaled operands (top rows Q, K; bottom rows Cm, R) and the identity [I 0; 0 I] at 256..383
     {
-        float g[32], gx[32], kk[32];
+        float g[32], gx[32];
         plain_row(g, P0, t, c0);
         if (t > 0) plain_row(gx, P0, t - 1, c0); else zero32(gx);
-        if (row_valid) load32(kk, p.kk, p.x_bf16, roff); else zero32(kk);
         if (top) {
-            if (row_valid) load32(x, p.k, p.x_bf16, roff); else zero32(x);
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 const float rh = rho[c0 + i];
                 v[i] = kk[i] * __expf(gx[i] - rh);  // Q
-                x[i] = x[i] * __expf(rh - g[i]);    // K
+                x[i] = ra[i] * __expf(rh - g[i]);   // K
             }
             a_row(tl + 0, v);
             b_row(sm + tcs::kBG, 256, 64 + t, c0, x);
@@ -559,14 +582,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_summary_tc_kernel(BwdArgs p) 
             b_row(sm + tcs::kBT2, 64, t, c0, x);
             b_col(sm + tcs::kBQc, 64, t, c0, v);
         } else {
-            float a[32];
-            if (row_valid) { load32(a, p.a, p.x_bf16, roff); load32(x, p.r, p.x_bf16, roff); }
-            else { zero32(a); zero32(x); }
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 const float rh = rho[c0 + i];
-                v[i] = kk[i] * a[i] * __expf(rh - g[i]);  // Cm
-                x[i] = x[i] * __expf(g[i] - rh);          // R
+                v[i] = kk[i] * ra[i] * __expf(rh - g[i]);  // Cm
+                x[i] = rb[i] * __expf(g[i] - rh);          // R
             }
             a_row(tl + 0, v);
             b_row(sm + tcs::kBG, 256, t, c0, v);
@@ -581,6 +601,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_summary_tc_kernel(BwdArgs p) 
 #pragma unroll
         for (int i = 0; i < 32; ++i) id[i] = (!top && c0 + i == t) ? 0x3f800000u : 0u;
         tmem_st32u(tl + 320, id);
+    }
+    if (!top) {  // V and dO rows, in flight during the first products
+        if (row_valid) { load32(kk, p.v, p.x_bf16, roff); load32(ra, p.d_o, false, roff); }
+        else { zero32(kk); zero32(ra); }
     }
     ok = mma_round(bar, phase, p.status, [&] {
         mma_group(tmem, 64, 0, sbase + tcs::kBG, tcg::kAtom256, 192, 64);         // G1
@@ -601,10 +625,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_summary_tc_kernel(BwdArgs p) 
             tmem_ld32(tl + 192, v);
             mask32<kUpper, false>(v, t, c0);
             a_row(tl + 64, v);
-            if (row_valid) load32(v, p.v, p.x_bf16, roff); else zero32(v);
-            b_col(sm + tcs::kBVc, 64, t, c0, v);
-            if (row_valid) load32(v, p.d_o, false, roff); else zero32(v);
-            b_col(sm + tcs::kBdOc, 64, t, c0, v);
+            b_col(sm + tcs::kBVc, 64, t, c0, kk);
+            b_col(sm + tcs::kBdOc, 64, t, c0, ra);
         }
         __syncthreads();
         unit_lower_inverse(P1p, P0, reinterpret_cast<float *>(sm + tcs::kBTt));
@@ -791,6 +813,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(sbase + tcg::kBar + 8, tcg::kTmemCols);
+    // raw rows for the scaled operands, fetched before the cumulative sum needs w
+    float kk[32], ra[32], rb[32];  // top: kk, k; bottom: kk, a, r
+    if (row_valid) {
+        load32(kk, p.kk, p.x_bf16, roff);
+        load32(ra, top ? p.k : p.a, p.x_bf16, roff);
+        if (!top) load32(rb, p.r, p.x_bf16, roff);
+    } else {
+        zero32(kk); zero32(ra); zero32(rb);
+    }
     decay_cumsum(p, c, h, P0, P1p);  // ends with a barrier
     if (tid < 64) {
         rho[tid] = P0[31 * kLD + tid];
@@ -807,17 +838,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
 
     // ---- scaled operands: top rows Q, K; bottom rows Cm, R
     {
-        float g[32], gx[32], kk[32];
+        float g[32], gx[32];
         plain_row(g, P0, t, c0);
         if (t > 0) plain_row(gx, P0, t - 1, c0); else zero32(gx);
-        if (row_valid) load32(kk, p.kk, p.x_bf16, roff); else zero32(kk);
         if (top) {
-            if (row_valid) load32(x, p.k, p.x_bf16, roff); else zero32(x);
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 const float rh = rho[c0 + i];
                 v[i] = kk[i] * __expf(gx[i] - rh);     // Q
-                x[i] = x[i] * __expf(rh - g[i]);       // K
+                x[i] = ra[i] * __expf(rh - g[i]);      // K
             }
             a_row(tl + 0, v);
             a_row(tl + 256, x);
@@ -826,14 +855,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
             b_col(sm + tcg::kBF1, 64, 128 + t, c0, v);  // Q^c
             b_col(sm + tcg::kBF2, 64, 64 + t, c0, x);   // K^c
         } else {
-            float a[32];
-            if (row_valid) { load32(a, p.a, p.x_bf16, roff); load32(x, p.r, p.x_bf16, roff); }
-            else { zero32(a); zero32(x); }
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 const float rh = rho[c0 + i];
-                v[i] = kk[i] * a[i] * __expf(rh - g[i]);  // Cm
-                x[i] = x[i] * __expf(g[i] - rh);          // R
+                v[i] = kk[i] * ra[i] * __expf(rh - g[i]);  // Cm
+                x[i] = rb[i] * __expf(g[i] - rh);          // R
             }
             a_row(tl + 0, v);
             b_row(sm + tcg::kBG, 256, t, c0, v);
@@ -841,6 +867,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
             b_col(sm + tcg::kBF1, 64, 64 + t, c0, x);   // R^c
             b_col(sm + tcg::kBF2, 64, 128 + t, c0, v);  // Cm^c
         }
+    }
+    // the next phase's rows, in flight during the Gram products: top S0, Ghat, S_C; bottom V, dO
+    if (top) {
+        load_state32(kk, p.Sck + b0 + t * kN + c0);
+        load_state32(ra, p.Eck + cidx + t * kN + c0);
+        load_state32(rb, p.Sck + b1 + t * kN + c0);
+    } else if (row_valid) {
+        load32(kk, p.v, p.x_bf16, roff);
+        load32(ra, p.d_o, false, roff);
+    } else {
+        zero32(kk); zero32(ra);
     }
     ok = mma_round(bar, phase, p.status, [&] {
         mma_group(tmem, 64, 0, sbase + tcg::kBG, tcg::kAtom256, 192, 64);
@@ -871,37 +908,22 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
 
         // ---- B tiles from the states, V and dO; the carry rowsum(Ghat .* S_C)
         if (top) {
-            float gh[32], sc[32];
-            const float *s0row = p.Sck + b0 + t * kN + c0;
-            const float *ghrow = p.Eck + cidx + t * kN + c0;
-            const float *scrow = p.Sck + b1 + t * kN + c0;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float4 a4 = __ldg(reinterpret_cast<const float4 *>(s0row) + q);
-                const float4 g4 = __ldg(reinterpret_cast<const float4 *>(ghrow) + q);
-                const float4 s4 = __ldg(reinterpret_cast<const float4 *>(scrow) + q);
-                v[4 * q] = a4.x; v[4 * q + 1] = a4.y; v[4 * q + 2] = a4.z; v[4 * q + 3] = a4.w;
-                gh[4 * q] = g4.x; gh[4 * q + 1] = g4.y; gh[4 * q + 2] = g4.z; gh[4 * q + 3] = g4.w;
-                sc[4 * q] = s4.x; sc[4 * q + 1] = s4.y; sc[4 * q + 2] = s4.z; sc[4 * q + 3] = s4.w;
-            }
             float part = 0.f;
             const float s0s = __expf(rho[t]), gs = __expf(gC[t] - rho[t]);
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-                part = fmaf(gh[i], sc[i], part);
-                v[i] *= s0s;   // S0'
-                gh[i] *= gs;   // G'
+                part = fmaf(ra[i], rb[i], part);
+                kk[i] *= s0s;  // S0'
+                ra[i] *= gs;   // G'
             }
             carry[hh * 64 + t] = part;
-            b_col(sm + tcg::kBY, 64, t, c0, v);         // S0'^T
-            b_row(sm + tcg::kBF2, 64, t, c0, v);        // S0'
-            b_col(sm + tcg::kBF3, 64, t, c0, gh);       // G'^T
-            b_row(sm + tcg::kBF1, 64, t, c0, gh);       // G'
+            b_col(sm + tcg::kBY, 64, t, c0, kk);         // S0'^T
+            b_row(sm + tcg::kBF2, 64, t, c0, kk);        // S0'
+            b_col(sm + tcg::kBF3, 64, t, c0, ra);        // G'^T
+            b_row(sm + tcg::kBF1, 64, t, c0, ra);        // G'
         } else {
-            if (row_valid) load32(v, p.v, p.x_bf16, roff); else zero32(v);
-            b_col(sm + tcg::kBY, 64, 64 + t, c0, v);    // V^c
-            if (row_valid) load32(v, p.d_o, false, roff); else zero32(v);
-            b_col(sm + tcg::kBF3, 64, 64 + t, c0, v);   // dO^c
+            b_col(sm + tcg::kBY, 64, 64 + t, c0, kk);    // V^c
+            b_col(sm + tcg::kBF3, 64, 64 + t, c0, ra);   // dO^c
         }
         unit_lower_inverse(P1p, P0, reinterpret_cast<float *>(sm + tcg::kBF3 + 32768));
         ok = mma_round(bar, phase, p.status, [&] {
@@ -923,6 +945,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
         } else {
             tmem_ld32(tl + 192, v);
             b_col(sm + tcg::kBY + 16384, 64, t, c0, v);
+            if (row_valid) { load32(kk, p.v, p.x_bf16, roff); load32(ra, p.d_o, false, roff); }
+            else { zero32(kk); zero32(ra); }
         }
         ok = mma_round(bar, phase, p.status, [&] {
             mma_group(tmem, 128, 0, sbase + tcg::kBY, tcg::kAtom64, 64, 64);           // Z = T Y (top)
@@ -942,12 +966,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
             b_row(bp, 128, 64 + t, c0, x);
             a_row(tl + 448, x);
         } else {
-            if (row_valid) load32(v, p.v, p.x_bf16, roff); else zero32(v);
-            if (row_valid) load32(x, p.d_o, false, roff); else zero32(x);
-            a_row(tl + 0, v);
-            b_row(bpt, 128, t, c0, v);
-            b_row(bp, 128, t, c0, x);
-            a_row(tl + 448, x);
+            a_row(tl + 0, kk);           // V
+            b_row(bpt, 128, t, c0, kk);
+            b_row(bp, 128, t, c0, ra);   // dO
+            a_row(tl + 448, ra);
         }
         ok = mma_round(bar, phase, p.status, [&] {
             mma_group(tmem, 192, 256, sbase + tcg::kBF3, tcg::kAtom64, 64, 192);  // dV (top)
@@ -995,6 +1017,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
         }
         tmem_ld32(tl + 448, v);
         a_row(tl + 256, v);
+    }
+    float wq[16];
+    if (ok) {
+        // the epilogue's rows (top kk, a; bottom r, k) and w, in flight during the last products
+        if (row_valid) {
+            load32(kk, top ? p.kk : p.r, p.x_bf16, roff);
+            load32(ra, top ? p.a : p.k, p.x_bf16, roff);
+        } else {
+            zero32(kk); zero32(ra);
+        }
+        load_w16(wq, p, c, h);
         ok = mma_round(bar, phase, p.status, [&] {
             mma_group(tmem, 192, 0, sbase + tcg::kBF1, tcg::kAtom64, 64, 192);    // [dC; dK]
             mma_group(tmem, 448, 256, sbase + tcg::kBF2, tcg::kAtom64, 64, 192);  // [dKr; dR]
@@ -1007,7 +1040,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
         float *Gm = reinterpret_cast<float *>(sm + 0);
         float *PW = reinterpret_cast<float *>(sm + 17408);  // top part, then the cumulative sum
         float *PB = reinterpret_cast<float *>(sm + 34816);  // bottom part
-        decay_cumsum(p, c, h, Gm, reinterpret_cast<float *>(sm + 52224));
+        decay_cumsum_from(wq, Gm, reinterpret_cast<float *>(sm + 52224));
         float g[32], acc1[32], acc2[32];
         plain_row(g, Gm, t, c0);
         tmem_ld32(tl + 192, acc1);  // top dC, bottom dK
@@ -1015,19 +1048,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
         const size_t go = ((size_t)(c.tb + t) * p.H + h) * kN + c0;
         float Y[32];
         if (top) {
-            float gx[32], kk[32], a[32];
+            float gx[32];
             if (t > 0) plain_row(gx, Gm, t - 1, c0); else zero32(gx);
-            if (row_valid) { load32(kk, p.kk, p.x_bf16, roff); load32(a, p.a, p.x_bf16, roff); }
-            else { zero32(kk); zero32(a); }
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 const float rh = rho[c0 + i];
                 const float dC = -acc1[i] * __expf(rh - g[i]);
                 const float dKr = -acc2[i] * __expf(gx[i] - rh);
                 Y[i] = kk[i] * dKr;
-                x[i] = Y[i] - kk[i] * a[i] * dC;  // - c dC + kk dKr
-                acc1[i] = kk[i] * dC;             // da
-                acc2[i] = dKr + a[i] * dC;        // dkk
+                x[i] = Y[i] - kk[i] * ra[i] * dC;  // - c dC + kk dKr
+                acc1[i] = kk[i] * dC;              // da
+                acc2[i] = dKr + ra[i] * dC;        // dkk
             }
             plain_row_store(PW, t, c0, x);
             if (row_valid) {
@@ -1038,15 +1069,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
                 }
             }
         } else {
-            float rr[32], kv[32];
-            if (row_valid) { load32(rr, p.r, p.x_bf16, roff); load32(kv, p.k, p.x_bf16, roff); }
-            else { zero32(rr); zero32(kv); }
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 const float rh = rho[c0 + i];
                 const float dK = acc1[i] * __expf(rh - g[i]);
                 const float dR = acc2[i] * __expf(g[i] - rh);
-                x[i] = rr[i] * dR - kv[i] * dK;  // r dr - k dk
+                x[i] = kk[i] * dR - ra[i] * dK;  // r dr - k dk
                 acc1[i] = dK;
                 acc2[i] = dR;
             }
