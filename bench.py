@@ -524,30 +524,38 @@ def run_configs(args, dev, peaks):
         del p, o, sf, ws
         torch.cuda.empty_cache()
     # prefill backward (dr, dw, dk, dv, dkk, da and dS0 from dO and dS_final)
-    for label, lens, H, with_s0 in [("prefill backward 2.9B 8x4096", [4096] * 8, 40, False),
-                                    ("prefill backward 7.2B 1x32768", [v["single_T"]], 64, True)]:
-        p = inputs.prefill_inputs(lens, H, 64, seed=12, device=dev)
-        cu = p["cu_seqlens"]
-        cu_dev = cu.to(dev)
-        T = int(cu[-1])
-        s0 = inputs.initial_state(len(lens), H, 64, seed=12, std=0.1, device=dev) if with_s0 else None
-        d_o, dsf = inputs.upstream_gradients(T, len(lens), H, 64, seed=12, device=dev)
-        grads = tuple(torch.empty(T, H, 64, device=dev) for _ in range(6))
-        ws = torch.empty(wkv7.prefill_backward_workspace_size(len(lens), T, H), dtype=torch.uint8, device=dev)
+    backward_line(args, dev, peaks, "prefill backward 2.9B 8x4096", [4096] * 8, 40, False, stream)
+    backward_line(args, dev, peaks, "prefill backward 7.2B 1x32768", [v["single_T"]], 64, True, stream)
 
-        def bcall():
-            wkv7.prefill_backward(p["r"], p["w"], p["k"], p["v"], p["kk"], p["a"], cu_dev, d_o, initial_state=s0,
-                                  d_final_state=dsf, grads=grads, workspace=ws, cu_seqlens_host=cu, stream=stream)
-        ms = time_stream(bcall, max(3, args.prefill_steps // 4), 2, stream)
-        wkv7.check_device_status(stream)
-        nbytes = T * H * BACKWARD_BYTES_PER_TOKEN_HEAD + (3 if with_s0 else 2) * len(lens) * H * 16384
-        gbs = nbytes / (ms * 1e-3) / 1e9
-        print(json.dumps({"workload": label, "tokens": T, "ms_per_call": round(ms, 4),
-                          "tokens_per_s": round(T / (ms * 1e-3), 1), "achieved_gbs": round(gbs, 1),
-                          "frac": round(gbs / hbm, 4), "roofline_ms": round(nbytes / hbm / 1e6, 4),
-                          "bytes_per_token_head": BACKWARD_BYTES_PER_TOKEN_HEAD}), flush=True)
-        del p, d_o, dsf, grads, ws
-        torch.cuda.empty_cache()
+
+def backward_line(args, dev, peaks, label, lens, H, with_s0, stream):
+    """Time wkv7_prefill_backward on one workload and print its JSON line."""
+    import torch
+
+    import rwkv_linear_attention_gb300 as wkv7
+    from rwkv_linear_attention_gb300 import inputs
+    p = inputs.prefill_inputs(lens, H, 64, seed=12, device=dev)
+    cu = p["cu_seqlens"]
+    cu_dev = cu.to(dev)
+    T = int(cu[-1])
+    s0 = inputs.initial_state(len(lens), H, 64, seed=12, std=0.1, device=dev) if with_s0 else None
+    d_o, dsf = inputs.upstream_gradients(T, len(lens), H, 64, seed=12, device=dev)
+    grads = tuple(torch.empty(T, H, 64, device=dev) for _ in range(6))
+    ws = torch.empty(wkv7.prefill_backward_workspace_size(len(lens), T, H), dtype=torch.uint8, device=dev)
+
+    def bcall():
+        wkv7.prefill_backward(p["r"], p["w"], p["k"], p["v"], p["kk"], p["a"], cu_dev, d_o, initial_state=s0,
+                              d_final_state=dsf, grads=grads, workspace=ws, cu_seqlens_host=cu, stream=stream)
+    ms = time_stream(bcall, max(3, args.prefill_steps // 4), args.warmup, stream)
+    wkv7.check_device_status(stream)
+    nbytes = T * H * BACKWARD_BYTES_PER_TOKEN_HEAD + (3 if with_s0 else 2) * len(lens) * H * 16384
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    print(json.dumps({"workload": label, "tokens": T, "ms_per_call": round(ms, 4),
+                      "tokens_per_s": round(T / (ms * 1e-3), 1), "achieved_gbs": round(gbs, 1),
+                      "frac": round(gbs / peaks["hbm_gbs"], 4), "roofline_ms": round(nbytes / peaks["hbm_gbs"] / 1e6, 4),
+                      "bytes_per_token_head": BACKWARD_BYTES_PER_TOKEN_HEAD}), flush=True)
+    del p, d_o, dsf, grads, ws
+    torch.cuda.empty_cache()
 
 
 def cpu_baseline_decode(B, H, layers, budget_s=15.0):
@@ -596,6 +604,12 @@ def run_ours(args):
     if args.workload == "configs":
         if rank == 0:
             run_configs(args, dev, peaks)
+        return
+    if args.workload == "backward":
+        if rank == 0:
+            n = args.backward_seqs
+            backward_line(args, dev, peaks, f"prefill backward 2.9B {n}x4096", [4096] * n, 40, False,
+                          torch.cuda.Stream(device=dev))
         return
     if args.workload == "prefill":
         pre = prefill_bench(dev, args.prefill_steps, args.warmup, world)
@@ -762,9 +776,10 @@ def main(argv=None):
     ap.add_argument("--prefill-steps", type=int, default=20)
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=("all", "decode", "prefill", "configs"), default="all",
+    ap.add_argument("--backward-seqs", type=int, default=8, help="sequences of 4096 tokens for --workload backward")
+    ap.add_argument("--workload", choices=("all", "decode", "prefill", "configs", "backward"), default="all",
                     help="all (the contract line); decode or prefill alone, for profiling; "
-                         "configs: one line per named workload")
+                         "configs: one line per named workload; backward: the prefill backward alone")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
