@@ -13,8 +13,9 @@ gradient passes through at most four rounded products (Gram -> Y -> Z -> P ->
 final), and the carried states and adjoints through one rounded transition
 per chunk in a contracting chain, so the error is a few times 2^-12 of the
 largest term: about 1e-3, the same order as the bf16-input forward bound.  The
-measured maximum over every case below, the 2.9B full-size sample included,
-is 1.07e-3 (dw); d_initial_state stays near 5e-4.
+measured maximum over every case below, the 2.9B and 7.2B full-size samples
+included (512 chained chunks in the 32768-token sequence), is 1.07e-3 (dw);
+d_initial_state stays near 5e-4.
 """
 import numpy as np
 import pytest
@@ -136,6 +137,27 @@ def test_backward_full_size_2p9b_sampled(dev):
         ref = _oracle(sub, cu1, d_o[t0:t1], dsf[b:b + 1], None, heads=heads)
         part = tuple(g[t0:t1] for g in got[:6]) + (got[6][b:b + 1],)
         _compare(part, ref, heads=heads)
+
+
+def test_backward_full_size_7p2b_single_32768_sampled(dev):
+    """The longest chain: one sequence of 32768 tokens (512 chunks), 64 heads,
+    bf16 inputs, random initial states; the oracle checks heads 0 and 63."""
+    cfg = inputs.VARLEN_7P2B
+    p, cu, d_o, dsf, s0 = _case([cfg["single_T"]], cfg["H"], torch.bfloat16, dev, seed=inputs.CONFIG_SEEDS[4])
+    got = _gpu(p, cu, d_o, dsf, s0, dev)
+    heads = [0, cfg["H"] - 1]
+    _compare(got, _oracle(p, cu, d_o, dsf, s0, heads=heads), heads=heads)
+
+
+def test_backward_full_size_7p2b_varlen_sampled(dev):
+    """16 sequences of U[1, 32768] tokens (seeded), 64 heads, bf16, random
+    initial states; the oracle checks every sequence of head 17."""
+    cfg = inputs.VARLEN_7P2B
+    lens = inputs.seqlens_uniform(cfg["num_seqs"], cfg["lo"], cfg["hi"], seed=1004)
+    p, cu, d_o, dsf, s0 = _case(lens, cfg["H"], torch.bfloat16, dev, seed=1004)
+    got = _gpu(p, cu, d_o, dsf, s0, dev)
+    heads = [17]
+    _compare(got, _oracle(p, cu, d_o, dsf, s0, heads=heads), heads=heads)
 
 
 def test_rejects_bad_arguments(dev):
