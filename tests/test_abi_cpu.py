@@ -149,6 +149,71 @@ def test_workspace_size_is_pure(lib):
     assert lib.wkv7_prefill_workspace_size(8, 32768, 40, 32) == 0
 
 
+def _backward(lib, num_seqs=2, T=10, H=2, N=64, cu_host=None, dtype=_lib.BF16, ptrs=None, ws_bytes=None):
+    """wkv7_prefill_backward with fake, never-dereferenced device pointers.
+
+    ptrs: cu, r, w, k, v, kk, a, s0, d_o, dsf, dr, dw, dk, dv, dkk, da, ds0, workspace."""
+    P = ctypes.c_void_p
+    base = ptrs or [FAKE + i * (1 << 26) for i in range(18)]
+    host = None
+    if cu_host is not None:
+        arr = (ctypes.c_int32 * len(cu_host))(*cu_host)
+        host = ctypes.cast(arr, P)
+    need = lib.wkv7_prefill_backward_workspace_size(num_seqs, T, H, N)
+    wsb = need if ws_bytes is None else ws_bytes
+    return lib.wkv7_prefill_backward(num_seqs, T, H, N, P(base[0]), host, dtype, *[P(x) for x in base[1:17]],
+                                     P(base[17]), wsb, P(0))
+
+
+def test_backward_rejects_unsupported(lib):
+    assert _backward(lib, N=32) == _lib.ERR_UNSUPPORTED
+    assert _backward(lib, dtype=5) == _lib.ERR_UNSUPPORTED
+
+
+def test_backward_rejects_bad_sizes_and_host_cu_seqlens(lib):
+    assert _backward(lib, num_seqs=-1) == _lib.ERR_INVALID_ARG
+    assert _backward(lib, H=0) == _lib.ERR_INVALID_ARG
+    assert _backward(lib, num_seqs=0, T=0) == _lib.OK
+    assert _backward(lib, num_seqs=0, T=4) == _lib.ERR_INVALID_ARG
+    assert _backward(lib, cu_host=[0, 6, 4]) == _lib.ERR_INVALID_ARG
+    assert _backward(lib, cu_host=[0, 4, 9]) == _lib.ERR_INVALID_ARG
+
+
+def test_backward_rejects_nulls_and_misalignment(lib):
+    good = [FAKE + i * (1 << 26) for i in range(18)]
+    required = [0, 1, 2, 3, 4, 5, 6, 8, 10, 11, 12, 13, 14, 15]  # cu, inputs, d_o, the six gradients
+    for i in required:
+        bad = list(good)
+        bad[i] = 0
+        assert _backward(lib, ptrs=bad) == _lib.ERR_INVALID_ARG, i
+    for i in range(17):
+        bad = list(good)
+        bad[i] += 4
+        assert _backward(lib, ptrs=bad, cu_host=[0, 4, 10]) == _lib.ERR_ALIGNMENT, i
+
+
+def test_backward_rejects_small_workspace_and_overlaps(lib):
+    need = lib.wkv7_prefill_backward_workspace_size(2, 10, 2, 64)
+    assert need > 0
+    assert _backward(lib, ws_bytes=need - 16) == _lib.ERR_WORKSPACE
+    ptrs = [FAKE + i * (1 << 26) for i in range(18)]
+    over = list(ptrs)
+    over[10] = ptrs[1]  # dr over r
+    assert _backward(lib, ptrs=over, cu_host=[0, 4, 10]) == _lib.ERR_INVALID_ARG
+    over = list(ptrs)
+    over[17] = ptrs[12]  # workspace over dk
+    assert _backward(lib, ptrs=over, cu_host=[0, 4, 10]) == _lib.ERR_INVALID_ARG
+
+
+def test_backward_workspace_size(lib):
+    # the state at every 64-token boundary plus A, F, E per chunk: (4 chunks + seqs) 16 KB planes
+    n, T, H = 8, 32768, 40
+    nc = T // 64 + n
+    table = ((n + 1) * 4 + 255) // 256 * 256
+    assert lib.wkv7_prefill_backward_workspace_size(n, T, H, 64) == table + (4 * nc + n) * H * 16384
+    assert lib.wkv7_prefill_backward_workspace_size(n, T, H, 32) == 0
+
+
 def test_product_package_does_not_import_the_oracle():
     pkg = os.path.join(ROOT, "rwkv_linear_attention_gb300")
     for dirpath, _, files in os.walk(pkg):
