@@ -23,9 +23,11 @@
 // +3 of that slice; the two reductions over key rows (kk^T S and S'^T r) are
 // a per-lane sum over eight rows and three xor-shuffles.
 //
-// From 8192 heads per launch (many full waves) a register-resident form of
-// the same computation is used instead (below), which streams at ~94% of
-// measured bandwidth there.
+// A register-resident form of the same computation (below) is used instead
+// from 8192 heads per launch (many full waves: ~94% of measured bandwidth
+// there) and when the launch fits in one wave of it (at most SMs x 6 heads:
+// 912 on a GB300; 1.79 vs 2.11 us at 40 heads, 5.95 vs 6.89 us at 640).
+// In between (e.g. 1280 heads: 9.25 vs 10.03 us) the ring is faster.
 //
 // Launch order: programmatic dependent launch.  The kernel waits for the
 // preceding grid (griddepcontrol.wait) before it touches global memory, so
@@ -405,6 +407,7 @@ constexpr long long kRegsFromHeads = 8192;
 struct LaunchShape {
     int grid_cap = 0;       // CTAs per wave (SMs x resident CTAs per SM)
     int grid_cap_tail = 0;  // the same for the form with the fused tail
+    long long regs_wave = 0;  // heads the register-resident form runs in one wave
 };
 
 LaunchShape shape_for_device() {
@@ -428,6 +431,11 @@ LaunchShape shape_for_device() {
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_tail, wkv7_step_kernel<true, float>, kThreads,
                                                       kSmemBytesT<true>) != cudaSuccess)
         return LaunchShape{};
+    int per_sm_regs = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_regs, wkv7_step_regs_kernel<false, float>, kRegWarps * 32, 0) !=
+        cudaSuccess)
+        return LaunchShape{};
+    s.regs_wave = static_cast<long long>(sms) * (per_sm_regs > 0 ? per_sm_regs : 1);
     s.grid_cap_tail = sms * (per_sm_tail > 0 ? per_sm_tail : 1);
     s.grid_cap = sms * (per_sm > 0 ? per_sm : 1);
     cached = s;
@@ -451,7 +459,11 @@ cudaError_t launch_step(long long n_heads, const float *r, const float *w, const
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (n_heads >= kRegsFromHeads) {
+    const LaunchShape shape = shape_for_device();
+    if (shape.grid_cap <= 0) return cudaErrorInvalidDevice;
+    // The register-resident form whenever the launch is one wave of it (a head per
+    // 4-warp block: no ring to fill, every head's loads issued at once) or many waves.
+    if (n_heads >= kRegsFromHeads || n_heads <= shape.regs_wave) {
         const long long units = n_heads * 4;
         cfg.gridDim = dim3(static_cast<unsigned>((units + kRegWarps - 1) / kRegWarps));
         cfg.blockDim = dim3(kRegWarps * 32);
@@ -459,8 +471,6 @@ cudaError_t launch_step(long long n_heads, const float *r, const float *w, const
         if (bf16) return cudaLaunchKernelEx(&cfg, wkv7_step_regs_kernel<false, __nv_bfloat16>, units, r, w, k, v, kk, a, state, static_cast<__nv_bfloat16 *>(o), t);
         return cudaLaunchKernelEx(&cfg, wkv7_step_regs_kernel<false, float>, units, r, w, k, v, kk, a, state, static_cast<float *>(o), t);
     }
-    const LaunchShape shape = shape_for_device();
-    if (shape.grid_cap <= 0) return cudaErrorInvalidDevice;
     const long long cap = tail ? shape.grid_cap_tail : shape.grid_cap;
     const long long grid = n_heads < cap ? n_heads : cap;
     cfg.gridDim = dim3(static_cast<unsigned>(grid));

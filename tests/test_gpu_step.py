@@ -199,10 +199,12 @@ def test_step_rejects_bad_arguments_on_gpu(dev):
     assert e.value.status == wkv7._lib.ERR_ALIGNMENT
 
 
-@pytest.mark.parametrize("B,H", [(8191, 1), (128, 64)], ids=["8191-heads", "8192-heads"])
+@pytest.mark.parametrize("B,H", [(24, 38), (1, 913), (8191, 1), (128, 64)],
+                         ids=["912-heads", "913-heads", "8191-heads", "8192-heads"])
 def test_step_either_side_of_the_large_batch_form(dev, B, H):
-    """Both decode forms (shared-memory ring below 8192 heads, register form from
-    8192 heads) against the oracle, from a random state."""
+    """Both decode forms against the oracle, from a random state, either side of
+    each switch: the register form up to one wave of it (912 heads on a GB300)
+    and from 8192 heads, the shared-memory ring in between."""
     N = 64
     x = inputs.decode_inputs(B, H, N, steps=1, seed=B + H, device=dev)
     x = {n: t[0].contiguous() for n, t in x.items()}
