@@ -315,11 +315,11 @@ __global__ void __launch_bounds__(1024) bwd_chunk_table_kernel(const int32_t *cu
 
 namespace tcg {
 // shared memory (bytes from a 1024-aligned base)
-constexpr uint32_t kBG = 0;           // [Cm; K; R; Q], 256 rows x K 64 (64 KB), round 1
-constexpr uint32_t kBY = 0;           // [S0'^T | V^c] 64 x 128 (32 KB), round 2; then Y^c, Y2^c; then B_P
-constexpr uint32_t kBF3 = 32768;      // [G'^T | dO^c | U^c] 64 x 192 (48 KB), rounds 2 and 4
-constexpr uint32_t kBF1 = 81920;      // [G' | R^c | Q^c] 64 x 192 (48 KB), round 6
-constexpr uint32_t kBF2 = 131072;     // [S0' | K^c | Cm^c] 64 x 192 (48 KB), round 6
+constexpr uint32_t kBG = 0;           // [Cm; K; R; Q], 256 rows x K 64 (64 KB), stage 1
+constexpr uint32_t kBY = 0;           // [S0'^T | V^c] 64 x 128 (32 KB), stage 2; then Y^c, Y2^c; then B_P
+constexpr uint32_t kBF3 = 32768;      // [G'^T | dO^c | U^c] 64 x 192 (48 KB), stages 2 and 4
+constexpr uint32_t kBF1 = 81920;      // [G' | R^c | Q^c] 64 x 192 (48 KB), stage 6
+constexpr uint32_t kBF2 = 131072;     // [S0' | K^c | Cm^c] 64 x 192 (48 KB), stage 6
 constexpr uint32_t kPlain0 = 180224;  // fp32 64 x 68: the cumulative decay, then T; then (with kPlain1) B_Pt
 constexpr uint32_t kPlain1 = 197632;  // fp32 64 x 68: Lc
 constexpr uint32_t kVec = 215040;     // rho[64], gC[64], carry halves [2][64]
@@ -425,7 +425,7 @@ __device__ __forceinline__ void mma_group_acc(uint32_t tmem, uint32_t dcol, uint
 // Operands written -> thread 0 issues and commits -> every thread waits (bounded).
 // The outcome is uniform over the CTA; false after a timeout (reported).
 template <class F>
-__device__ __forceinline__ bool mma_round(uint32_t bar, uint32_t &phase, unsigned *status, F issue) {
+__device__ __forceinline__ bool mma_stage(uint32_t bar, uint32_t &phase, unsigned *status, F issue) {
     fence_proxy_async_smem();
     tc_fence_before_sync();
     __syncthreads();
@@ -492,7 +492,7 @@ __device__ __forceinline__ void load_state32(float (&v)[32], const float *src) {
 // operands have channels for rows: those come from identity products
 // ([I 0; 0 I] x [X | Y]^T puts X^T in the top lanes and Y^T in the bottom ones)
 // and from products whose own left operand already has channels for rows.
-// Rounds:
+// Stages:
 //   1  G1 = [Q; Cm] x [Cm; K; R]^T -> Lc, Lk (top), Mc^T (bottom);
 //      [Cm^T; Q^T] and [K^T; R^T] by identity products
 //   2  Lk V (top), Mc^T dO (bottom); W1 = Cm^T T (top), W2 = Q^T T^T (bottom)
@@ -500,14 +500,14 @@ __device__ __forceinline__ void load_state32(float (&v)[32], const float *src) {
 // then A = diag(e^{gC-rho})(I - A*)diag(e^{rho}), F = diag(e^{gC-rho}) F*, E = diag(e^{rho}) E*.
 
 namespace tcs {
-constexpr uint32_t kBG = 0;           // [Cm; K; R; Q], 256 rows x K 64 (64 KB), round 1; then round-2 tiles
-constexpr uint32_t kBVc = 0;          // V^c (16 KB), rounds 2 and 3
-constexpr uint32_t kBdOc = 16384;     // dO^c (16 KB), rounds 2 and 3
-constexpr uint32_t kBTt = 32768;      // rows t: T[s][t] (16 KB), round 2
-constexpr uint32_t kBTn = 49152;      // rows t: T[t][s] (16 KB), round 2
-constexpr uint32_t kBT1 = 65536;      // [Cm | Q] 64 x K 128 (32 KB), round 1; then (Lk V)^c, (Mc^T dO)^c
-constexpr uint32_t kBT2 = 98304;      // [K | R] 64 x K 128 (32 KB), round 1
-constexpr uint32_t kBQc = 131072;     // Q^c (16 KB), round 3
+constexpr uint32_t kBG = 0;           // [Cm; K; R; Q], 256 rows x K 64 (64 KB), stage 1; then stage-2 tiles
+constexpr uint32_t kBVc = 0;          // V^c (16 KB), stages 2 and 3
+constexpr uint32_t kBdOc = 16384;     // dO^c (16 KB), stages 2 and 3
+constexpr uint32_t kBTt = 32768;      // rows t: T[s][t] (16 KB), stage 2
+constexpr uint32_t kBTn = 49152;      // rows t: T[t][s] (16 KB), stage 2
+constexpr uint32_t kBT1 = 65536;      // [Cm | Q] 64 x K 128 (32 KB), stage 1; then (Lk V)^c, (Mc^T dO)^c
+constexpr uint32_t kBT2 = 98304;      // [K | R] 64 x K 128 (32 KB), stage 1
+constexpr uint32_t kBQc = 131072;     // Q^c (16 KB), stage 3
 constexpr uint32_t kPlain0 = 147456;  // fp32 64 x 68: the cumulative decay, then T
 constexpr uint32_t kPlain1 = 164864;  // fp32 64 x 68: Lc
 constexpr uint32_t kVec = 182272;     // rho[64], gC[64]
@@ -606,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_summary_tc_kernel(BwdArgs p) 
         if (row_valid) { load32(kk, p.v, p.x_bf16, roff); load32(ra, p.d_o, false, roff); }
         else { zero32(kk); zero32(ra); }
     }
-    ok = mma_round(bar, phase, p.status, [&] {
+    ok = mma_stage(bar, phase, p.status, [&] {
         mma_group(tmem, 64, 0, sbase + tcs::kBG, tcg::kAtom256, 192, 64);         // G1
         mma_group(tmem, 384, 256, sbase + tcs::kBT1, tcg::kAtom64, 64, 128);      // [Cm^T; Q^T]
         mma_group(tmem, 448, 256, sbase + tcs::kBT2, tcg::kAtom64, 64, 128);      // [K^T; R^T]
@@ -638,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_summary_tc_kernel(BwdArgs p) 
             plain_row(x, P0, t, c0);
             b_row(sm + tcs::kBTn, 64, t, c0, x);  // rows t: T[t][s]
         }
-        ok = mma_round(bar, phase, p.status, [&] {
+        ok = mma_stage(bar, phase, p.status, [&] {
             mma_group(tmem, 128, 64, sbase + tcs::kBVc, tcg::kAtom64, 64, 64);    // Lk V (top)
             mma_group(tmem, 192, 64, sbase + tcs::kBdOc, tcg::kAtom64, 64, 64);   // Mc^T dO (bottom)
             mma_group(tmem, 0, 384, sbase + tcs::kBTt, tcg::kAtom64, 64, 64);     // W1 = Cm^T T (top)
@@ -659,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_summary_tc_kernel(BwdArgs p) 
             tmem_ld32(tl + 256, v);
             a_row(tl + 256, v);
         }
-        ok = mma_round(bar, phase, p.status, [&] {
+        ok = mma_stage(bar, phase, p.status, [&] {
             mma_group_acc(tmem, 64, 448, sbase + tcs::kBVc, tcg::kAtom64, 64, 64, false, false);         // K^T V
             mma_group_acc(tmem, 64, 0, sbase + tcs::kBT1, tcg::kAtom64, 64, 64, true, true);             // - W1 (Lk V)
             mma_group_acc(tmem, 128, 448, sbase + tcs::kBdOc, tcg::kAtom64, 64, 64, false, false);       // R^T dO
@@ -775,7 +775,7 @@ __global__ void __launch_bounds__(kThreads) bwd_chain_kernel(BwdArgs p) {
 // (C^T = B A^T) or from transposed stores into the B tile, never from moving
 // data between lanes.
 //
-// Rounds (each: operands written -> one thread issues -> commit -> all wait):
+// Stages (each: operands written -> one thread issues -> commit -> all wait):
 //   1  G1 = [Q; Cm] x [Cm; K; R]^T -> Lc, Lk (top), Mc^T (bottom);
 //      G2 = K x [R; Q]^T            -> Mk^T, Lk^T (top)
 //   2  Y  = [Q | Lk] x [S0'^T | V^c]^T (top);  Y2 = [Cm | Mc^T] x [G'^T | dO^c]^T (bottom)
@@ -879,7 +879,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
     } else {
         zero32(kk); zero32(ra);
     }
-    ok = mma_round(bar, phase, p.status, [&] {
+    ok = mma_stage(bar, phase, p.status, [&] {
         mma_group(tmem, 64, 0, sbase + tcg::kBG, tcg::kAtom256, 192, 64);
         mma_group(tmem, 320, 256, sbase + tcg::kBG + 128 * 128, tcg::kAtom256, 128, 64);
     });
@@ -926,7 +926,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
             b_col(sm + tcg::kBF3, 64, 64 + t, c0, ra);   // dO^c
         }
         unit_lower_inverse(P1p, P0, reinterpret_cast<float *>(sm + tcg::kBF3 + 32768));
-        ok = mma_round(bar, phase, p.status, [&] {
+        ok = mma_stage(bar, phase, p.status, [&] {
             mma_group(tmem, 128, 0, sbase + tcg::kBY, tcg::kAtom64, 64, 128);
             mma_group(tmem, 192, 0, sbase + tcg::kBF3, tcg::kAtom64, 64, 128);
         });
@@ -948,7 +948,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
             if (row_valid) { load32(kk, p.v, p.x_bf16, roff); load32(ra, p.d_o, false, roff); }
             else { zero32(kk); zero32(ra); }
         }
-        ok = mma_round(bar, phase, p.status, [&] {
+        ok = mma_stage(bar, phase, p.status, [&] {
             mma_group(tmem, 128, 0, sbase + tcg::kBY, tcg::kAtom64, 64, 64);           // Z = T Y (top)
             mma_group(tmem, 192, 64, sbase + tcg::kBY + 16384, tcg::kAtom64, 64, 64);  // U = T^T Y2 (top)
         });
@@ -971,7 +971,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
             b_row(bp, 128, t, c0, ra);   // dO
             a_row(tl + 448, ra);
         }
-        ok = mma_round(bar, phase, p.status, [&] {
+        ok = mma_stage(bar, phase, p.status, [&] {
             mma_group(tmem, 192, 256, sbase + tcg::kBF3, tcg::kAtom64, 64, 192);  // dV (top)
             mma_group(tmem, 64, 0, sbase + tcg::kBY, tcg::kAtom128, 128, 64);      // P
         });
@@ -987,7 +987,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
                     reinterpret_cast<float4 *>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
             }
         }
-        ok = mma_round(bar, phase, p.status, [&] {
+        ok = mma_stage(bar, phase, p.status, [&] {
             mma_group(tmem, 320, 448, sbase + tcg::kPlain0, tcg::kAtom128, 128, 64);  // Pt
         });
     }
@@ -1028,7 +1028,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
             zero32(kk); zero32(ra);
         }
         load_w16(wq, p, c, h);
-        ok = mma_round(bar, phase, p.status, [&] {
+        ok = mma_stage(bar, phase, p.status, [&] {
             mma_group(tmem, 192, 0, sbase + tcg::kBF1, tcg::kAtom64, 64, 192);    // [dC; dK]
             mma_group(tmem, 448, 256, sbase + tcg::kBF2, tcg::kAtom64, 64, 192);  // [dKr; dR]
         });
