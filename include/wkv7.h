@@ -368,6 +368,19 @@ WKV7_API wkv7_status wkv7_prefill_backward(int num_seqs, int T_total, int H, int
                          float *d_initial_state, void *workspace, size_t workspace_bytes,
                          cudaStream_t stream);
 
+/*
+ * wkv7_diag_bounded_wait -- a diagnostic of the timeout path.  Launches one
+ * device-side wait on a barrier that nothing completes, through the same
+ * bounded wait (global-timer limit plus a poll count) and status report the
+ * kernels use for every mbarrier wait.  After timeout_us (1 .. 2,000,000) the
+ * device gives up and sets the timeout bit of the status word, exactly as an
+ * expired wait inside a kernel would; wkv7_check_device_status then returns
+ * WKV7_ERR_TIMEOUT (and clears it) and the context stays usable.  No fault and
+ * no hang: the wait always ends.  Stream-ordered; returns WKV7_ERR_INVALID_ARG
+ * for a timeout outside the range, WKV7_ERR_CUDA if the launch fails.
+ */
+WKV7_API wkv7_status wkv7_diag_bounded_wait(unsigned timeout_us, cudaStream_t stream);
+
 /* Static English text for a status code (never NULL). */
 WKV7_API const char *wkv7_status_string(wkv7_status status);
 

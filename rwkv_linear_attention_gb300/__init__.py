@@ -25,7 +25,7 @@ from . import _lib
 from ._lib import WKV7Error  # noqa: F401
 
 __all__ = ["step", "step_tail", "tmix_tail", "verify", "verify_commit", "prefill", "prefill_padded", "prefill_workspace_size",
-           "prefill_backward", "prefill_backward_workspace_size", "check_device_status",
+           "prefill_backward", "prefill_backward_workspace_size", "check_device_status", "diag_bounded_wait",
            "WKV7Error", "HEAD_SIZE"]
 
 HEAD_SIZE = 64
@@ -333,6 +333,13 @@ def prefill_padded(r, w, k, v, kk, a, lens, initial_state=None, final_state=None
                                  _stream(stream))
     _lib.check(st, "wkv7_prefill_padded")
     return o, final_state
+
+
+def diag_bounded_wait(timeout_us: int = 20000, stream=None) -> None:
+    """Run one device-side wait that nothing completes, bounded by ``timeout_us``;
+    the device reports the expiry through the status word, so the next
+    :func:`check_device_status` raises ``WKV7Error`` with the timeout status."""
+    _lib.check(_lib.load().wkv7_diag_bounded_wait(int(timeout_us), _stream(stream)), "wkv7_diag_bounded_wait")
 
 
 def check_device_status(stream=None) -> None:

@@ -39,6 +39,7 @@ EXPORTS = (
     "wkv7_prefill_noalloc",
     "wkv7_prefill_backward_workspace_size",
     "wkv7_prefill_backward",
+    "wkv7_diag_bounded_wait",
     "wkv7_status_string",
     "wkv7_check_device_status",
     "wkv7_last_cuda_error",
@@ -84,6 +85,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.wkv7_prefill_backward_workspace_size.argtypes = [I, I, I, I]
     lib.wkv7_prefill_backward.restype = I
     lib.wkv7_prefill_backward.argtypes = [I, I, I, I, P, P, I] + [P] * 6 + [P] * 3 + [P] * 7 + [P, S, P]
+    lib.wkv7_diag_bounded_wait.restype = I
+    lib.wkv7_diag_bounded_wait.argtypes = [ctypes.c_uint, P]
     lib.wkv7_status_string.restype = ctypes.c_char_p
     lib.wkv7_status_string.argtypes = [I]
     lib.wkv7_check_device_status.restype = I

@@ -6,6 +6,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "sm103_ptx.cuh"
 #include "wkv7_internal.cuh"
 
 namespace {
@@ -50,6 +51,18 @@ bool overlaps(const void *p, size_t n, const void *q, size_t m) {
     if (!p || !q || n == 0 || m == 0) return false;
     const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(q);
     return a < b + m && b < a + n;
+}
+
+// One wait that nothing completes, through the same bounded-wait helper and
+// status report as the kernels' mbarrier waits: the device gives up after
+// timeout_ns and reports kDevTimeout.
+__global__ void wkv7_bounded_wait_probe_kernel(unsigned *status, unsigned long long timeout_ns) {
+    __shared__ alignas(8) unsigned long long bar;
+    if (threadIdx.x != 0) return;
+    const uint32_t b = wkv7::ptx::smem_addr(&bar);
+    wkv7::ptx::mbar_init(b, 1);
+    wkv7::ptx::fence_mbar_init();
+    if (!wkv7::ptx::mbar_wait_bounded(b, 0, 1u << 24, timeout_ns)) wkv7::report(status, wkv7::kDevTimeout);
 }
 
 constexpr long long kMaxHeads = 1ll << 30;   // B*H (or num_seqs*H) limit
@@ -492,6 +505,16 @@ wkv7_status wkv7_prefill_backward(int num_seqs, int T_total, int H, int N, const
     b.d_initial_state = d_initial_state;
     b.status = status;
     cudaError_t e = wkv7::launch_prefill_backward(b, workspace, stream);
+    return e == cudaSuccess ? WKV7_OK : cuda_fail(e);
+}
+
+wkv7_status wkv7_diag_bounded_wait(unsigned timeout_us, cudaStream_t stream) {
+    if (timeout_us == 0 || timeout_us > 2000000u) return WKV7_ERR_INVALID_ARG;
+    unsigned *status = nullptr;
+    wkv7_status st = status_word(&status);
+    if (st != WKV7_OK) return st;
+    wkv7_bounded_wait_probe_kernel<<<1, 32, 0, stream>>>(status, 1000ull * timeout_us);
+    const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? WKV7_OK : cuda_fail(e);
 }
 

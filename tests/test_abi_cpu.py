@@ -214,6 +214,11 @@ def test_backward_workspace_size(lib):
     assert lib.wkv7_prefill_backward_workspace_size(n, T, H, 32) == 0
 
 
+def test_diag_bounded_wait_rejects_out_of_range_bound(lib):
+    assert lib.wkv7_diag_bounded_wait(0, ctypes.c_void_p(0)) == _lib.ERR_INVALID_ARG
+    assert lib.wkv7_diag_bounded_wait(2000001, ctypes.c_void_p(0)) == _lib.ERR_INVALID_ARG
+
+
 def test_product_package_does_not_import_the_oracle():
     pkg = os.path.join(ROOT, "rwkv_linear_attention_gb300")
     for dirpath, _, files in os.walk(pkg):
