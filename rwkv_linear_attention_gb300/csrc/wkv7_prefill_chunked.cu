@@ -26,13 +26,17 @@
 // with [Mt ; Ct] = [M_c ; Cb^T] T.  Every row i of the lower half carries the
 // factor e^{g_C - g_ref}[i] (Cb^T = diag(e^{g_C - g_ref}) C^T, likewise Kb^T);
 // the kernel keeps the lower half without it and applies it to the state rows
-// of the product.  Per chunk these tf32 MMAs run, all with M = 128, fp32
-// accumulators in tensor memory and the A operand read from tensor memory:
+// of the product.  Every S0 column i of A_chain carries the factor e^{g_ref}[i]
+// (Ra = R diag(e^{g_ref}), Qa = Q diag(e^{g_ref}), with R and Q the Gram
+// operands below); the kernel keeps those columns without it and scales the
+// rows of the state operand instead, S0' = diag(e^{g_ref}) S0.  Per chunk these
+// tf32 MMAs run, all with M = 128, fp32 accumulators in tensor memory and the A
+// operand read from tensor memory:
 //   G       = [R ; Q] [C ; K]^T                 (the four Gram blocks; 128x128x64)
 //   [. ; C^T | K^T] = [0 ; I] [C ; K]^T          (the transposes, no SIMT transposition)
 //   X       = [M_c ; C^T] T                      (three small products, see phase 4)
-//   A_chain = base - X [Qa | L_k]                (accumulated onto base = [Ra | M_k ; 0 | K^T]; 128x128x64)
-//   D       = A_chain [S0 ; V]                   (128x64x128)
+//   A_chain = base - X [Q | L_k]                 (accumulated onto base = [R | M_k ; 0 | K^T]; 128x128x64)
+//   D       = A_chain [S0' ; V]                  (128x64x128)
 // The SIMT work (cumulative decay, exponentials, masks, the blocked 64x64
 // unit-lower-triangular inverse, operand staging) is software-pipelined with
 // the MMAs: the next chunk's decay and Gram operands are built while this
@@ -42,7 +46,8 @@
 // in registers between chunks.  Inputs arrive by TMA as 2-D tiles of
 // 64 tokens x 64 channels of the packed [T, H, 64] arrays (bf16 tiles in the
 // 128-byte swizzled layout, so both row- and column-wise reads are free of
-// bank conflicts).
+// bank conflicts); a chunk's tiles are requested as soon as the previous
+// chunk's are consumed, a full chunk before they are needed.
 //
 // Inputs r, k, v, kk, a are bf16 (w fp32); fp32-input prefill is served by
 // the token-serial kernel instead.
@@ -89,12 +94,12 @@ constexpr int kTile = 64 * 64 * 2;  // one bf16 raw tile
 constexpr int SM_R = 0, SM_K = SM_R + kTile, SM_KK = SM_K + kTile, SM_A = SM_KK + kTile, SM_V = SM_A + kTile;
 constexpr int SM_W = SM_V + kTile;         // fp32 w tile -> E = e^{g - g_ref} (swizzled)
 constexpr int SM_BG = SM_W + 16384;        // B operand of G: [C ; K]  (128 x K64)
-constexpr int SM_BY = SM_BG + 32768;       // B operand of A_chain: [Qa^T ; L_k^T] (128 x K64)
+constexpr int SM_BY = SM_BG + 32768;       // B operand of A_chain: [Q^T ; L_k^T] (128 x K64)
 constexpr int SM_BX = SM_BY + 32768;       // B operand of X: T^T (64 x K64)
-constexpr int SM_BC = SM_BX + 16384;       // B operand of D: [S0^T | V^T] (64 x K128)
-constexpr int SM_LC = SM_BC + 32768;       // fp32 L_c [64][kLd]
-constexpr int SM_TS = SM_LC + 64 * kLd * 4;  // fp32 T [64][kLd]
-constexpr int SM_XS = SM_TS + 64 * kLd * 4;  // fp32 32 x 32 scratch
+constexpr int SM_BC = SM_BX + 16384;       // B operand of D: [S0'^T | V^T] (64 x K128)
+constexpr int SM_LC = SM_BC + 32768;       // fp32 L_c^T [64][kLd]
+constexpr int SM_TS = SM_LC + 64 * kLd * 4;  // output staging for the TMA stores
+constexpr int SM_XS = SM_TS + 64 * kLd * 4;  // fp32 2 x 16 x 16 scratch (T_11 of each half)
 constexpr int SM_TOT = SM_XS + 4096;       // 16 x 64 cumsum partials
 constexpr int SM_GREF = SM_TOT + 4096;     // 64: g_ref
 constexpr int SM_EREF = SM_GREF + 256;     // 2 x 64: e^{g_ref} (double-buffered across chunks)
@@ -346,12 +351,6 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(sbase + SM_SLOT, kTmemCols);
-    // B_chain rows j, K 0..63 <- S0[i][j]
-    if (state_thread) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-            *reinterpret_cast<uint32_t *>(sm + SM_BC + sw128_off(16 * cg + j, si, 64)) = to_tf32(s[j]);
-    }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
@@ -571,7 +570,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
                     mma_tf32_tmem_a(tmem + kColX, tmem + kColAC + 8 * kq, sdesc_sw128(sbase + SM_BX + 8192 + kq * 32),
                                     idesc_tf32(128, 32), kq > 0);
                 mma_commit(bar_x);
-                // A_chain -= X [Qa | L_k]  (negated A, accumulating onto the base [Ra | M_k ; 0 | Kb^T])
+                // A_chain -= X [Q | L_k]  (negated A, accumulating onto the base [R | M_k ; 0 | K^T])
                 if (!(ok = ready(rdy_y, par))) break;
 #pragma unroll
                 for (int kq = 0; kq < 8; ++kq)
@@ -615,9 +614,17 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
     if (alive) {
         phase1(chunk_len(0), 0);
         wsync();
+        // B_chain rows j, K 0..63 <- e^{g_ref}[i] S0[i][j]
+        if (state_thread) {
+            const float er = EREF[si];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                *reinterpret_cast<uint32_t *>(sm + SM_BC + sw128_off(16 * cg + j, si, 64)) = to_tf32(s[j] * er);
+        }
         phase2(chunk_len(0), EREF);
         write_vt(chunk_len(0));
         handoff(rdy_g);
+        if (tid == 0 && nchunks > 1) issue_tma(1);  // chunk 0's tiles are no longer read
         alive = wait_uniform(bar_g, 0, p.status);
         tc_fence_after_sync();
     }
@@ -627,7 +634,6 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
         const int lc = chunk_len(c);
         const bool has_next = c + 1 < nchunks;
         const uint32_t par = static_cast<uint32_t>(c & 1);
-        const float *erc = EREF + (c & 1) * 64;  // e^{g_ref} of this chunk
 
         // ---- phase 3: read G.  M_c (masked) -> A_chain columns 0..63 of rows t, which with
         // the transposing product's Cb^T below them form A_X = [M_c ; Cb^T]; M_k (masked) ->
@@ -648,12 +654,9 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
             const int t = m - 64, s0 = 16 * cg;
             float v[16];
             tmem_ld16(tmem + lane_off + kColG + s0, v);
-            float *LCw = reinterpret_cast<float *>(sm + SM_LC);
+            float *LTw = reinterpret_cast<float *>(sm + SM_LC);  // L_c^T: LT[s][t] = L_c[t][s]
 #pragma unroll
-            for (int j = 0; j < 16; j += 4)
-                *reinterpret_cast<float4 *>(LCw + t * kLd + s0 + j) =
-                    make_float4(s0 + j < t ? v[j] : 0.f, s0 + j + 1 < t ? v[j + 1] : 0.f,
-                                s0 + j + 2 < t ? v[j + 2] : 0.f, s0 + j + 3 < t ? v[j + 3] : 0.f);
+            for (int j = 0; j < 16; ++j) LTw[(s0 + j) * kLd + t] = s0 + j < t ? v[j] : 0.f;
             tmem_ld16(tmem + lane_off + kColG + 64 + s0, v);
             unsigned char *BY = sm + SM_BY;
 #pragma unroll
@@ -662,90 +665,109 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
         }
         sync_for_mma();
 
-        // ---- phase 4: the two 32x32 diagonal halves of T = (I + L_c)^{-1}, in fp32:
-        // T_A = (I + L_AA)^{-1}, T_B = (I + L_BB)^{-1} (16x16 diagonal blocks by right-looking
-        // substitution in registers, then T_10 = -T_11 L_10 T_00 and T_32 likewise).  The
-        // off-diagonal half T_BA = -T_B L_BA T_A is never formed: with [M_c ; Cb^T] = [B_L | B_R],
+        // ---- phase 4: the two 32x32 diagonal halves of T = (I + L_c)^{-1}, in fp32, one warp
+        // each: T_A = (I + L_AA)^{-1} (warp 0), T_B = (I + L_BB)^{-1} (warp 1).  Within a half
+        // [T_00 0 ; T_10 T_11]: the 16x16 diagonal blocks by right-looking substitution (lane
+        // = column; lanes 0..15 the first block, 16..31 the second), then T_10 = -T_11 (L_10 T_00)
+        // with rows split between the two half-warps.  The off-diagonal half
+        // T_BA = -T_B L_BA T_A is never formed: with [M_c ; Cb^T] = [B_L | B_R],
         //   X_R = B_R T_B,   X_L = (B_L - X_R L_BA) T_A
-        // are three small MMAs.  Their B operands T_B^T, L_BA^T, T_A^T go to B_X.
+        // are three small MMAs.  Their B operands T_B^T, L_BA^T, T_A^T go to B_X
+        // (B[n][k] = M[k][n]); the warps of the other two sub-partitions (warp % 4 = 2, 3)
+        // stage L_BA^T and Q^T meanwhile, so the two inverse warps issue unhindered.
         {
-            const float *LC = reinterpret_cast<const float *>(sm + SM_LC);
-            float *TS = reinterpret_cast<float *>(sm + SM_TS);
-            float *XS = reinterpret_cast<float *>(sm + SM_XS);
-            if (tid < 64) {
-                const int bb = tid >> 4, j = tid & 15, o = 16 * bb;
-                float x[16];
+            const float *LT = reinterpret_cast<const float *>(sm + SM_LC);
+            if (warp < 2) {
+                const int o = 32 * warp, hb = lane >> 4, j = lane & 15, ob = o + 16 * hb;
+                float x[16];  // column j of this lane's diagonal block of T
 #pragma unroll
                 for (int t = 0; t < 16; ++t) x[t] = (t == j) ? 1.f : 0.f;
 #pragma unroll
                 for (int u = 0; u < 15; ++u) {
+                    const float *lrow = LT + (ob + u) * kLd + ob;  // L[ob + t][ob + u], t = 0..15
 #pragma unroll
-                    for (int t = u + 1; t < 16; ++t) x[t] = fmaf(-LC[(o + t) * kLd + o + u], x[u], x[t]);
-                }
-#pragma unroll
-                for (int t = 0; t < 16; ++t)
-                    if (t >= j) TS[(o + t) * kLd + o + j] = x[t];
-            } else {
-                // the other warps meanwhile: Qa^T into B_Y rows 0..63, Qa[t][i] = kk e^{g_{t-1}}
-                // (task: channels i, i+1 of tokens tb .. tb+3; row order alternated as in write_vt)
-                for (int task = tid - 64; task < 512; task += kThreads - 64) {
-                    const int i = 2 * (task & 31), tb = 4 * (task >> 5);
-                    const float2 er = *reinterpret_cast<const float2 *>(erc + i);
-                    float x0[4], x1[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int t = tb + e;
-                        const float2 f = t == 0 ? make_float2(1.f, 1.f)
-                                                : *reinterpret_cast<const float2 *>(E + eidx(t - 1, i));
-                        const float2 kv = t < lc ? raw2(rkk, t, i) : make_float2(0.f, 0.f);
-                        x0[e] = t == 0 ? kv.x : kv.x * f.x * er.x;
-                        x1[e] = t == 0 ? kv.y : kv.y * f.y * er.y;
-                    }
-                    const bool odd_first = (task >> 2) & 1;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const bool odd = (h == 0) == odd_first;
-                        st_tf32x4(sm + SM_BY + sw128_off(i + (odd ? 1 : 0), tb, 128), odd ? x1[0] : x0[0],
-                                  odd ? x1[1] : x0[1], odd ? x1[2] : x0[2], odd ? x1[3] : x0[3]);
+                    for (int t4 = (u + 1) & ~3; t4 < 16; t4 += 4) {
+                        const float4 l = *reinterpret_cast<const float4 *>(lrow + t4);
+                        if (t4 + 0 > u) x[t4 + 0] = fmaf(-l.x, x[u], x[t4 + 0]);
+                        if (t4 + 1 > u) x[t4 + 1] = fmaf(-l.y, x[u], x[t4 + 1]);
+                        if (t4 + 2 > u) x[t4 + 2] = fmaf(-l.z, x[u], x[t4 + 2]);
+                        if (t4 + 3 > u) x[t4 + 3] = fmaf(-l.w, x[u], x[t4 + 3]);
                     }
                 }
-            }
-            wsync();
-            // The raw tiles and E are no longer read for this chunk: fetch the next one.
-            if (tid == 0 && has_next) issue_tma(c + 1);
-            {   // Y1 = L_10 T_00 -> XS[0..255], Y3 = L_32 T_22 -> XS[256..511]
-                const int blk = tid >> 8, r = (tid >> 4) & 15, cc = tid & 15, o = 32 * blk;
-                float y = 0.f;
+                // Y = L_10 T_00, column j, rows 8 hb .. 8 hb + 7 (L_10[r][u] = L[o + 16 + r][o + u])
+                float y[8];
 #pragma unroll
-                for (int u = 0; u < 16; ++u)
-                    y = fmaf(LC[(o + 16 + r) * kLd + o + u], u >= cc ? TS[(o + u) * kLd + o + cc] : 0.f, y);
-                XS[blk * 256 + r * 16 + cc] = y;
-            }
-            wsync();
-            {   // T_10 = -T_11 Y1, T_32 = -T_33 Y3
-                const int blk = tid >> 8, r = (tid >> 4) & 15, cc = tid & 15, o = 32 * blk;
-                float t_ = 0.f;
+                for (int r = 0; r < 8; ++r) y[r] = 0.f;
 #pragma unroll
-                for (int u = 0; u < 16; ++u)
-                    t_ = fmaf(u <= r ? TS[(o + 16 + r) * kLd + o + 16 + u] : 0.f, XS[blk * 256 + u * 16 + cc], t_);
-                TS[(o + 16 + r) * kLd + o + cc] = -t_;
-            }
-            wsync();
-            // B_X: [T_B^T | L_BA^T | T_A^T], each 32 rows x K 32 (B[n][k] = M[k][n])
+                for (int u = 0; u < 16; ++u) {
+                    const float xa = __shfl_sync(0xffffffffu, x[u], j);  // T_00[u][j]
+                    const float *lr = LT + (o + u) * kLd + o + 16 + 8 * hb;
+                    const float4 l0 = *reinterpret_cast<const float4 *>(lr);
+                    const float4 l1 = *reinterpret_cast<const float4 *>(lr + 4);
+                    y[0] = fmaf(l0.x, xa, y[0]); y[1] = fmaf(l0.y, xa, y[1]);
+                    y[2] = fmaf(l0.z, xa, y[2]); y[3] = fmaf(l0.w, xa, y[3]);
+                    y[4] = fmaf(l1.x, xa, y[4]); y[5] = fmaf(l1.y, xa, y[5]);
+                    y[6] = fmaf(l1.z, xa, y[6]); y[7] = fmaf(l1.w, xa, y[7]);
+                }
+                // T_10 = -T_11 Y, column j, rows 8 hb .. 8 hb + 7.  T_11 goes through this warp's
+                // scratch (row-major 16 x 16, exact zeros above the diagonal).
+                float *T11 = reinterpret_cast<float *>(sm + SM_XS) + warp * 256;
+                if (hb) {
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int task = tid + kThreads * u;
-                if (task < 768) {
-                    const int op = task >> 8, n = (task >> 3) & 31, k0 = 4 * (task & 7);
-                    float e[4];
+                    for (int r = 0; r < 16; ++r) T11[r * 16 + j] = x[r];
+                }
+                float yv[16];  // Y[v][j], v = 0..15 (rows 8..15 are only needed, and only read, by hb = 1)
 #pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) {
-                        const int k = k0 + jj;
-                        if (op == 0)      e[jj] = k >= n ? TS[(32 + k) * kLd + 32 + n] : 0.f;
-                        else if (op == 1) e[jj] = LC[(32 + k) * kLd + n];
-                        else              e[jj] = k >= n ? TS[k * kLd + n] : 0.f;
+                for (int v = 0; v < 8; ++v) {
+                    yv[v] = __shfl_sync(0xffffffffu, y[v], j);
+                    yv[8 + v] = y[v];
+                }
+                __syncwarp();
+                float z[8];
+#pragma unroll
+                for (int rr = 0; rr < 8; ++rr) {
+                    const float *tr = T11 + (8 * hb + rr) * 16;
+                    float acc = 0.f;
+#pragma unroll
+                    for (int v4 = 0; v4 < 16; v4 += 4) {
+                        const float4 tv = *reinterpret_cast<const float4 *>(tr + v4);
+                        acc = fmaf(tv.x, yv[v4], acc);
+                        acc = fmaf(tv.y, yv[v4 + 1], acc);
+                        acc = fmaf(tv.z, yv[v4 + 2], acc);
+                        acc = fmaf(tv.w, yv[v4 + 3], acc);
                     }
-                    st_tf32x4(sm + SM_BX + op * 4096 + sw128_off(n, k0, 32), e[0], e[1], e[2], e[3]);
+                    z[rr] = -acc;
+                }
+                // B_X rows: row n = column n of the half's T
+                unsigned char *dst = sm + SM_BX + (warp == 0 ? 8192 : 0);
+                if (hb == 0) {
+#pragma unroll
+                    for (int k0 = 0; k0 < 16; k0 += 4) st_tf32x4(dst + sw128_off(j, k0, 32), x[k0], x[k0 + 1], x[k0 + 2], x[k0 + 3]);
+                    st_tf32x4(dst + sw128_off(j, 16, 32), z[0], z[1], z[2], z[3]);
+                    st_tf32x4(dst + sw128_off(j, 20, 32), z[4], z[5], z[6], z[7]);
+                } else {
+                    st_tf32x4(dst + sw128_off(j, 24, 32), z[0], z[1], z[2], z[3]);
+                    st_tf32x4(dst + sw128_off(j, 28, 32), z[4], z[5], z[6], z[7]);
+#pragma unroll
+                    for (int k0 = 0; k0 < 16; k0 += 4) {
+                        *reinterpret_cast<uint4 *>(dst + sw128_off(16 + j, k0, 32)) = make_uint4(0u, 0u, 0u, 0u);
+                        st_tf32x4(dst + sw128_off(16 + j, 16 + k0, 32), x[k0], x[k0 + 1], x[k0 + 2], x[k0 + 3]);
+                    }
+                }
+            } else if (warp & 2) {
+                const int sidx = (((warp >> 2) << 1) | (warp & 1)) * 32 + lane;
+                {   // Q^T into B_Y rows 0..63: B[i][t] = Q[t][i], the tf32 words of the Gram A operand's lower half
+                    const int t = m - 64;
+                    float v[16];
+                    tmem_ld16(tmem + lane_off + kColAG + 16 * cg, v);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        *reinterpret_cast<uint32_t *>(sm + SM_BY + sw128_off(16 * cg + j, t, 128)) = __float_as_uint(v[j]);
+                }
+                {   // L_BA^T: B[n][k] = L_c[32 + k][n] = LT[n][32 + k]
+                    const int n = sidx >> 3, k0 = 4 * (sidx & 7);
+                    const float4 l = *reinterpret_cast<const float4 *>(LT + n * kLd + 32 + k0);
+                    st_tf32x4(sm + SM_BX + 4096 + sw128_off(n, k0, 32), l.x, l.y, l.z, l.w);
                 }
             }
         }
@@ -758,21 +780,22 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
         }
         if (!wait_uniform(bar_x, par, p.status)) { alive = false; break; }
         tc_fence_after_sync();
-        // A_chain columns 0..63 (A_X, now consumed) <- base [Ra ; 0], Ra[t][i] = R[t][i] e^{g_ref}[i]
+        // A_chain columns 0..63 (A_X, now consumed) <- base [R ; 0] (the factor e^{g_ref} of the
+        // S0 columns rides on the state operand's rows)
         {
             float v[16];
             uint32_t wds[16];
             if (q < 2) {
                 tmem_ld16(tmem + lane_off + kColAG + 16 * cg, v);  // R (this chunk's Gram A operand)
 #pragma unroll
-                for (int j = 0; j < 16; ++j) wds[j] = to_tf32(v[j] * erc[16 * cg + j]);
+                for (int j = 0; j < 16; ++j) wds[j] = __float_as_uint(v[j]);
             } else {
 #pragma unroll
                 for (int j = 0; j < 16; ++j) wds[j] = 0u;
             }
             tmem_st16(tmem + lane_off + kColAC + 16 * cg, wds);
         }
-        handoff(rdy_y);  // -> A_chain -= X [Qa | L_k], then D = A_chain [S0 ; V]
+        handoff(rdy_y);  // -> A_chain -= X [Q | L_k], then D = A_chain [S0' ; V]
 
         // ---- next chunk, phase 2 (overlaps the A_chain and D products)
         if (has_next) {
@@ -829,10 +852,11 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
                 }
             } else {
                 const float decay = GC[(c & 1) * 64 + si], rowf = E63[(c & 1) * 64 + si];
+                const float ern = has_next ? EREF[((c + 1) & 1) * 64 + si] : 1.f;  // e^{g_ref} of the next chunk
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     s[j] = fmaf(decay, s[j], rowf * v[j]);
-                    *reinterpret_cast<uint32_t *>(sm + SM_BC + sw128_off(16 * cg + j, si, 64)) = to_tf32(s[j]);
+                    *reinterpret_cast<uint32_t *>(sm + SM_BC + sw128_off(16 * cg + j, si, 64)) = to_tf32(s[j] * ern);
                 }
             }
             if (has_next) write_vt(chunk_len(c + 1));
@@ -850,6 +874,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
             }
             bulk_commit();
         }
+        if (tid == 0 && c + 2 < nchunks) issue_tma(c + 2);  // chunk c + 1's tiles are no longer read
         if (has_next) {
             if (!wait_uniform(bar_g, static_cast<uint32_t>((c + 1) & 1), p.status)) { alive = false; break; }
             tc_fence_after_sync();
