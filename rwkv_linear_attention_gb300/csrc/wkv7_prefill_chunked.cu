@@ -33,15 +33,18 @@
 // tf32 MMAs run, all with M = 128, fp32 accumulators in tensor memory and the A
 // operand read from tensor memory:
 //   G       = [R ; Q] [C ; K]^T                 (the four Gram blocks; 128x128x64)
-//   [. ; C^T | K^T] = [0 ; I] [C ; K]^T          (the transposes, no SIMT transposition)
 //   X       = [M_c ; C^T] T                      (three small products, see phase 4)
 //   A_chain = base - X [Q | L_k]                 (accumulated onto base = [R | M_k ; 0 | K^T]; 128x128x64)
 //   D       = A_chain [S0' ; V]                  (128x64x128)
+// C^T and K^T (the lower lanes of A_X and of the base) are copied from the Gram
+// B operand [C ; K] in shared memory into tensor memory by threads.
 // The SIMT work (cumulative decay, exponentials, masks, the blocked 64x64
 // unit-lower-triangular inverse, operand staging) is software-pipelined with
 // the MMAs: the next chunk's decay and Gram operands are built while this
 // chunk's X and A_chain products run, and the next chunk's Gram product runs
-// while this chunk's outputs are written.  One CTA (512 threads) owns one
+// while this chunk's outputs are written.  A dedicated warp issues every MMA and
+// every TMA copy (input tiles a chunk ahead, output stores), so no worker
+// thread stalls on an issue queue.  One CTA (512 threads) owns one
 // (sequence, head) pair and walks its chunks in order; the fp32 state lives
 // in registers between chunks.  Inputs arrive by TMA as 2-D tiles of
 // 64 tokens x 64 channels of the packed [T, H, 64] arrays (bf16 tiles in the
@@ -75,19 +78,18 @@ using namespace ptx;
 
 constexpr int kC = 64;          // chunk length
 constexpr int kThreads = 512;   // worker warps w < 16: TMEM lane quarter w % 4, column group w / 4
-constexpr int kBlock = kThreads + 32;  // + one warp that issues every MMA
+constexpr int kBlock = kThreads + 32;  // + one warp that issues every MMA and TMA copy
 constexpr uint32_t kMaxPolls = 1u << 24;
 
-// TMEM columns
+// TMEM columns (448 used; the allocation is a power of two)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColG = 0;     // G
 constexpr uint32_t kColX = 128;   // X = [Mt ; Ct]
 constexpr uint32_t kColAC = 192;  // A_chain (128 columns)
 constexpr uint32_t kColD = 320;   // D = [O ; S_C - e^{g_C} S0]
 constexpr uint32_t kColAG = 384;  // A operand of G = [R ; Q] (for the next chunk)
-constexpr uint32_t kColAT = 448;  // constant A operand [0 ; I] of the transposing product
 
-constexpr int kLd = 68;  // padded row stride (floats) of the fp32 L_c / T scratch
+constexpr int kLd = 68;  // padded row stride (floats) of the fp32 L_c^T scratch
 
 // Shared memory map (bytes from a 1024-aligned base)
 constexpr int kTile = 64 * 64 * 2;  // one bf16 raw tile
@@ -336,7 +338,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
     // waiter never misses a phase.
     const uint32_t bar_tma = sbase + SM_BAR, bar_g = bar_tma + 8, bar_x = bar_tma + 16, bar_y = bar_tma + 24,
                    bar_d = bar_tma + 32, bar_i = bar_tma + 40;
-    const uint32_t rdy_x = bar_tma + 48, rdy_y = bar_tma + 56, rdy_g = bar_tma + 64;
+    const uint32_t rdy_x = bar_tma + 48, rdy_y = bar_tma + 56, rdy_g = bar_tma + 64, rdy_t = bar_tma + 72;
 
     if (tid == 0) {
         mbar_init(bar_tma, 1);
@@ -348,6 +350,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
         mbar_init(rdy_x, 1);
         mbar_init(rdy_y, 1);
         mbar_init(rdy_g, 1);
+        mbar_init(rdy_t, 1);
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(sbase + SM_SLOT, kTmemCols);
@@ -502,11 +505,10 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
         }
     };
 
-    // Gram product G = [R ; Q] [C ; K]^T, and the transposing product
-    // [0 ; I] [C ; K]^T, whose lower half is [C^T | K^T] -- Cb^T and Kb^T without their
-    // row factor e^{g_C - g_ref}[i] (Cb^T[i][s] = e^{g_C - g_ref}[i] C[s][i]).  That factor
-    // multiplies every row of the lower half of A_chain, so it is applied to the
-    // state rows of D instead.
+    // Gram product G = [R ; Q] [C ; K]^T.  The lower half of A_chain takes [C^T | K^T]
+    // (copied in phase 4): Cb^T and Kb^T without their row factor e^{g_C - g_ref}[i]
+    // (Cb^T[i][s] = e^{g_C - g_ref}[i] C[s][i]).  That factor multiplies every row of the
+    // lower half of A_chain, so it is applied to the state rows of D instead.
     auto issue_gram = [&]() {
 #pragma unroll
         for (int kq = 0; kq < 8; ++kq)
@@ -514,21 +516,15 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
                             sdesc_sw128(sbase + SM_BG + (kq >> 2) * 128 * 128 + (kq & 3) * 32),
                             idesc_tf32(128, 128), kq > 0);
     };
-    auto issue_transpose = [&]() {
-#pragma unroll
-        for (int kq = 0; kq < 8; ++kq)
-            mma_tf32_tmem_a(tmem + kColAC, tmem + kColAT + 8 * kq,
-                            sdesc_sw128(sbase + SM_BG + (kq >> 2) * 128 * 128 + (kq & 3) * 32),
-                            idesc_tf32(128, 128), kq > 0);
-    };
 
     bool alive = true;
     if (warp == kThreads / 32) {
         // ======== the MMA warp: one lane issues every tensor-core product, in
-        // the order the workers hand the operands over, so operand staging never
-        // waits for MMA issue.
+        // the order the workers hand the operands over, and every TMA copy, so
+        // operand staging never waits for an issue.
         if (lane == 0) {
             uint32_t ip = 0;
+            int last_load = nchunks > 1 ? 1 : 0;  // the last chunk whose tiles were requested
             auto ready = [&](uint32_t rdy, uint32_t parity) {
                 const bool ok = mbar_wait_bounded(rdy, parity, kMaxPolls);
                 tc_fence_after_sync();
@@ -543,7 +539,6 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
             bool ok = ready(rdy_g, 0);  // chunk 0: Gram operands
             if (ok) {
                 issue_gram();
-                issue_transpose();
                 mma_commit(bar_g);
             }
             for (int c = 0; c < nchunks && ok; ++c) {
@@ -586,29 +581,43 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
                     mma_tf32_tmem_a(tmem + kColD, tmem + kColAC + 8 * kq,
                                     sdesc_sw128(sbase + SM_BC + (kq >> 2) * 64 * 128 + (kq & 3) * 32),
                                     idesc_tf32(128, 64), kq > 0);
+                // the previous chunk's output stores have read the staging tile, so D's completion
+                // also tells the workers that they may stage this chunk's outputs
+                bulk_wait_read<0>();
                 mma_commit(bar_d);
-                if (has_next) {
-                    // the next chunk's Gram products; the transposing one overwrites A_chain,
-                    // so it waits for D to complete
+                if (has_next) {  // the next chunk's Gram product
                     if (!(ok = ready(rdy_g, static_cast<uint32_t>((c + 1) & 1)))) break;
                     issue_gram();
-                    if (!(ok = mbar_wait_bounded(bar_d, par, kMaxPolls))) break;
-                    tc_fence_after_sync();
-                    issue_transpose();
                     mma_commit(bar_g);
+                }
+                // the workers have staged this chunk's outputs and consumed chunk c + 1's tiles
+                if (!(ok = ready(rdy_t, par))) break;
+                if (chunk_len(c) == kC) {
+                    const int t0 = bos + (c_begin + c) * kC;
+                    if (to_scratch) {
+                        tma_store_2d(&maps.ohat, 0, ohat_row + c * kC, sbase + SM_TS);
+                        tma_store_2d(&maps.ohat, 32, ohat_row + c * kC, sbase + SM_TS + 8192);
+                    } else if (bf16_out) {
+                        tma_store_2d(&maps.o, h * 64, t0, sbase + SM_TS);
+                    } else {
+                        tma_store_2d(&maps.o, h * 64, t0, sbase + SM_TS);
+                        tma_store_2d(&maps.o, h * 64 + 32, t0, sbase + SM_TS + 8192);
+                    }
+                    bulk_commit();
+                }
+                if (c + 2 < nchunks) {
+                    issue_tma(c + 2);
+                    last_load = c + 2;
                 }
             }
             if (!ok) report(p.status, kDevTimeout);
+            bulk_wait<0>();  // every output store has completed
+            // the last input load has landed before the CTA's shared memory goes away
+            mbar_wait_bounded(bar_tma, static_cast<uint32_t>(last_load & 1), kMaxPolls);
         }
     } else {
     // ======== the 512 worker threads
-    // ---- prologue: the constant A_T = [0 ; I]; chunk 0 up to its Gram products
-    {
-        uint32_t wds[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) wds[j] = (m >= 64 && 16 * cg + j == m - 64) ? 0x3f800000u : 0u;
-        tmem_st16(tmem + lane_off + kColAT + 16 * cg, wds);
-    }
+    // ---- prologue: chunk 0 up to its Gram product
     if (tid == 0) issue_tma(0);
     alive = wait_uniform(bar_tma, 0, p.status);
     if (alive) {
@@ -636,8 +645,8 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
         const uint32_t par = static_cast<uint32_t>(c & 1);
 
         // ---- phase 3: read G.  M_c (masked) -> A_chain columns 0..63 of rows t, which with
-        // the transposing product's Cb^T below them form A_X = [M_c ; Cb^T]; M_k (masked) ->
-        // A_chain rows t, K 64..; L_c -> LC; L_k^T -> B_Y (16 + 16 columns per lower-lane warp).
+        // Cb^T below them (phase 4) form A_X = [M_c ; Cb^T]; M_k (masked) -> A_chain rows t,
+        // K 64..; L_c^T -> LT; L_k^T -> B_Y (16 + 16 columns per lower-lane warp).
         if (q < 2) {
             uint32_t wds[32];
             const int gcol = (cg < 2 ? 0 : 64) + 32 * (cg & 1);  // M_c | M_k
@@ -649,7 +658,6 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
             for (int j = 0; j < 32; ++j) wds[j] = to_tf32(s0 + j <= t ? v[j] : 0.f);
             tmem_st32_issue(tmem + lane_off + kColAC + gcol, wds);
             tmem_wait_st();
-            if (tid == 0) bulk_wait_read<0>();  // the previous chunk's O stores have read T's scratch
         } else {
             const int t = m - 64, s0 = 16 * cg;
             float v[16];
@@ -674,7 +682,8 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
         //   X_R = B_R T_B,   X_L = (B_L - X_R L_BA) T_A
         // are three small MMAs.  Their B operands T_B^T, L_BA^T, T_A^T go to B_X
         // (B[n][k] = M[k][n]); the warps of the other two sub-partitions (warp % 4 = 2, 3)
-        // stage L_BA^T and Q^T meanwhile, so the two inverse warps issue unhindered.
+        // meanwhile copy Q^T and [C^T | K^T] and stage L_BA^T, so the two inverse warps
+        // issue unhindered.
         {
             const float *LT = reinterpret_cast<const float *>(sm + SM_LC);
             if (warp < 2) {
@@ -763,6 +772,20 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
                         *reinterpret_cast<uint32_t *>(sm + SM_BY + sw128_off(16 * cg + j, t, 128)) = __float_as_uint(v[j]);
+                }
+                {   // [C^T | K^T] into A_chain lanes 64..127 (row i = m - 64, columns s = 16 cg ..):
+                    // the tf32 words of B_G with the rounding bits cleared, i.e. exactly the
+                    // product of the identity with B_G
+                    const int i = m - 64;
+                    uint32_t cw[16], kw[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int s_ = 16 * cg + j;
+                        cw[j] = *reinterpret_cast<const uint32_t *>(sm + SM_BG + sw128_off(s_, i, 128)) & 0xffffe000u;
+                        kw[j] = *reinterpret_cast<const uint32_t *>(sm + SM_BG + sw128_off(64 + s_, i, 128)) & 0xffffe000u;
+                    }
+                    tmem_st16(tmem + lane_off + kColAC + 16 * cg, cw);
+                    tmem_st16(tmem + lane_off + kColAC + 64 + 16 * cg, kw);
                 }
                 {   // L_BA^T: B[n][k] = L_c[32 + k][n] = LT[n][32 + k]
                     const int n = sidx >> 3, k0 = 4 * (sidx & 7);
@@ -862,19 +885,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
             if (has_next) write_vt(chunk_len(c + 1));
         }
         sync_for_mma();
-        if (tid == 0 && lc == kC) {
-            if (to_scratch) {
-                tma_store_2d(&maps.ohat, 0, ohat_row + c * kC, sbase + SM_TS);
-                tma_store_2d(&maps.ohat, 32, ohat_row + c * kC, sbase + SM_TS + 8192);
-            } else if (bf16_out) {
-                tma_store_2d(&maps.o, h * 64, t0, sbase + SM_TS);
-            } else {
-                tma_store_2d(&maps.o, h * 64, t0, sbase + SM_TS);
-                tma_store_2d(&maps.o, h * 64 + 32, t0, sbase + SM_TS + 8192);
-            }
-            bulk_commit();
-        }
-        if (tid == 0 && c + 2 < nchunks) issue_tma(c + 2);  // chunk c + 1's tiles are no longer read
+        if (tid == 0) mbar_arrive(rdy_t);  // -> the output stores and the tiles of chunk c + 2
         if (has_next) {
             if (!wait_uniform(bar_g, static_cast<uint32_t>((c + 1) & 1), p.status)) { alive = false; break; }
             tc_fence_after_sync();
@@ -887,7 +898,6 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
 #pragma unroll
         for (int j = 0; j < 4; ++j) dst[j] = make_float4(s[4 * j], s[4 * j + 1], s[4 * j + 2], s[4 * j + 3]);
     }
-    if (tid == 0) bulk_wait<0>();  // every O store has completed
     }  // workers
     tc_fence_before_sync();
     __syncthreads();
