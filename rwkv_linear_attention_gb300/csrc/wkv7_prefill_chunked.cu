@@ -107,7 +107,7 @@ constexpr int SM_GREF = SM_TOT + 4096;     // 64: g_ref
 constexpr int SM_EREF = SM_GREF + 256;     // 2 x 64: e^{g_ref} (double-buffered across chunks)
 constexpr int SM_E63 = SM_EREF + 512;      // 2 x 64: e^{g_C - g_ref} (double-buffered across chunks)
 constexpr int SM_GC = SM_E63 + 512;        // 2 x 64: e^{g_C} (double-buffered across chunks)
-constexpr int SM_BAR = SM_GC + 512;        // 9 mbarriers
+constexpr int SM_BAR = SM_GC + 512;        // 10 mbarriers
 constexpr int SM_SLOT = SM_BAR + 128;
 constexpr int kSmemBytes = SM_SLOT + 64;
 constexpr int kSmemAlloc = kSmemBytes + 1024;
@@ -573,7 +573,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
                                     sdesc_sw128(sbase + SM_BY + (kq >> 2) * 128 * 128 + (kq & 3) * 32),
                                     idesc_tf32(128, 128) | kIdescNegateA, 1);
                 mma_commit(bar_y);
-                // D = A_chain [S0 ; V]
+                // D = A_chain [S0' ; V]
                 if (!(ok = mbar_wait_bounded(bar_y, par, kMaxPolls))) break;
                 tc_fence_after_sync();
 #pragma unroll
