@@ -37,7 +37,8 @@
 //   A_chain = base - X [Q | L_k]                 (accumulated onto base = [R | M_k ; 0 | K^T]; 128x128x64)
 //   D       = A_chain [S0' ; V]                  (128x64x128)
 // C^T and K^T (the lower lanes of A_X and of the base) are copied from the Gram
-// B operand [C ; K] in shared memory into tensor memory by threads.
+// B operand [C ; K] in shared memory into tensor memory by threads, and R (the
+// base's upper left block) from the Gram A operand.
 // The SIMT work (cumulative decay, exponentials, masks, the blocked 64x64
 // unit-lower-triangular inverse, operand staging) is software-pipelined with
 // the MMAs: the next chunk's decay and Gram operands are built while this
@@ -81,13 +82,16 @@ constexpr int kThreads = 512;   // worker warps w < 16: TMEM lane quarter w % 4,
 constexpr int kBlock = kThreads + 32;  // + one warp that issues every MMA and TMA copy
 constexpr uint32_t kMaxPolls = 1u << 24;
 
-// TMEM columns (448 used; the allocation is a power of two)
+// TMEM columns.  A_X and A_chain are apart, so A_chain's whole base can be
+// written before the X products (which consume A_X) run, and X, A_chain and D
+// follow one another on the tensor core without a handoff from the workers.
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColG = 0;     // G
 constexpr uint32_t kColX = 128;   // X = [Mt ; Ct]
-constexpr uint32_t kColAC = 192;  // A_chain (128 columns)
-constexpr uint32_t kColD = 320;   // D = [O ; S_C - e^{g_C} S0]
+constexpr uint32_t kColAX = 192;  // A_X = [M_c ; C^T], the A operand of X (64 columns)
+constexpr uint32_t kColAC = 256;  // A_chain (128 columns: the S0 block, then the V block)
 constexpr uint32_t kColAG = 384;  // A operand of G = [R ; Q] (for the next chunk)
+constexpr uint32_t kColD = 448;   // D = [O ; S_C - e^{g_C} S0]
 
 constexpr int kLd = 68;  // padded row stride (floats) of the fp32 L_c^T scratch
 
@@ -107,7 +111,7 @@ constexpr int SM_GREF = SM_TOT + 4096;     // 64: g_ref
 constexpr int SM_EREF = SM_GREF + 256;     // 2 x 64: e^{g_ref} (double-buffered across chunks)
 constexpr int SM_E63 = SM_EREF + 512;      // 2 x 64: e^{g_C - g_ref} (double-buffered across chunks)
 constexpr int SM_GC = SM_E63 + 512;        // 2 x 64: e^{g_C} (double-buffered across chunks)
-constexpr int SM_BAR = SM_GC + 512;        // 10 mbarriers
+constexpr int SM_BAR = SM_GC + 512;        // 7 mbarriers
 constexpr int SM_SLOT = SM_BAR + 128;
 constexpr int kSmemBytes = SM_SLOT + 64;
 constexpr int kSmemAlloc = kSmemBytes + 1024;
@@ -336,19 +340,15 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
     // chunk and the workers cannot reach the same handoff of the next chunk before the MMA
     // warp has consumed this one (they first wait on a product it issues after it), so a
     // waiter never misses a phase.
-    const uint32_t bar_tma = sbase + SM_BAR, bar_g = bar_tma + 8, bar_x = bar_tma + 16, bar_y = bar_tma + 24,
-                   bar_d = bar_tma + 32, bar_i = bar_tma + 40;
-    const uint32_t rdy_x = bar_tma + 48, rdy_y = bar_tma + 56, rdy_g = bar_tma + 64, rdy_t = bar_tma + 72;
+    const uint32_t bar_tma = sbase + SM_BAR, bar_g = bar_tma + 8, bar_d = bar_tma + 16, bar_i = bar_tma + 24;
+    const uint32_t rdy_x = bar_tma + 32, rdy_g = bar_tma + 40, rdy_t = bar_tma + 48;
 
     if (tid == 0) {
         mbar_init(bar_tma, 1);
         mbar_init(bar_g, 1);
-        mbar_init(bar_x, 1);
-        mbar_init(bar_y, 1);
         mbar_init(bar_d, 1);
         mbar_init(bar_i, 1);
         mbar_init(rdy_x, 1);
-        mbar_init(rdy_y, 1);
         mbar_init(rdy_g, 1);
         mbar_init(rdy_t, 1);
         fence_mbar_init();
@@ -549,33 +549,32 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
                 if (!(ok = ready(rdy_x, par))) break;
 #pragma unroll
                 for (int kq = 0; kq < 4; ++kq)
-                    mma_tf32_tmem_a(tmem + kColX + 32, tmem + kColAC + 32 + 8 * kq,
+                    mma_tf32_tmem_a(tmem + kColX + 32, tmem + kColAX + 32 + 8 * kq,
                                     sdesc_sw128(sbase + SM_BX + kq * 32), idesc_tf32(128, 32), kq > 0);
                 mma_commit(bar_i);
                 if (!(ok = wait_own())) break;
 #pragma unroll
                 for (int kq = 0; kq < 4; ++kq)
-                    mma_tf32_tmem_a(tmem + kColAC, tmem + kColX + 32 + 8 * kq,
+                    mma_tf32_tmem_a(tmem + kColAX, tmem + kColX + 32 + 8 * kq,
                                     sdesc_sw128(sbase + SM_BX + 4096 + kq * 32),
                                     idesc_tf32(128, 32) | kIdescNegateA, 1);
                 mma_commit(bar_i);
                 if (!(ok = wait_own())) break;
 #pragma unroll
                 for (int kq = 0; kq < 4; ++kq)
-                    mma_tf32_tmem_a(tmem + kColX, tmem + kColAC + 8 * kq, sdesc_sw128(sbase + SM_BX + 8192 + kq * 32),
+                    mma_tf32_tmem_a(tmem + kColX, tmem + kColAX + 8 * kq, sdesc_sw128(sbase + SM_BX + 8192 + kq * 32),
                                     idesc_tf32(128, 32), kq > 0);
-                mma_commit(bar_x);
+                mma_commit(bar_i);
+                if (!(ok = wait_own())) break;
                 // A_chain -= X [Q | L_k]  (negated A, accumulating onto the base [R | M_k ; 0 | K^T])
-                if (!(ok = ready(rdy_y, par))) break;
 #pragma unroll
                 for (int kq = 0; kq < 8; ++kq)
                     mma_tf32_tmem_a(tmem + kColAC, tmem + kColX + 8 * kq,
                                     sdesc_sw128(sbase + SM_BY + (kq >> 2) * 128 * 128 + (kq & 3) * 32),
                                     idesc_tf32(128, 128) | kIdescNegateA, 1);
-                mma_commit(bar_y);
+                mma_commit(bar_i);
+                if (!(ok = wait_own())) break;
                 // D = A_chain [S0' ; V]
-                if (!(ok = mbar_wait_bounded(bar_y, par, kMaxPolls))) break;
-                tc_fence_after_sync();
 #pragma unroll
                 for (int kq = 0; kq < 16; ++kq)
                     mma_tf32_tmem_a(tmem + kColD, tmem + kColAC + 8 * kq,
@@ -656,7 +655,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
             tmem_ld32(tmem + lane_off + kColG + gcol, v);
 #pragma unroll
             for (int j = 0; j < 32; ++j) wds[j] = to_tf32(s0 + j <= t ? v[j] : 0.f);
-            tmem_st32_issue(tmem + lane_off + kColAC + gcol, wds);
+            tmem_st32_issue(tmem + lane_off + (gcol < 64 ? kColAX : kColAC) + gcol, wds);
             tmem_wait_st();
         } else {
             const int t = m - 64, s0 = 16 * cg;
@@ -683,7 +682,10 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
         // are three small MMAs.  Their B operands T_B^T, L_BA^T, T_A^T go to B_X
         // (B[n][k] = M[k][n]); the warps of the other two sub-partitions (warp % 4 = 2, 3)
         // meanwhile copy Q^T and [C^T | K^T] and stage L_BA^T, so the two inverse warps
-        // issue unhindered.
+        // issue unhindered, and warps 4, 5, 8, 9 copy R into A_chain's S0 block.  With
+        // that, every operand of X, A_chain and D is in place at the end of this phase: the
+        // MMA warp runs the three without another handoff while the workers go on to the
+        // next chunk.
         {
             const float *LT = reinterpret_cast<const float *>(sm + SM_LC);
             if (warp < 2) {
@@ -763,7 +765,20 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
                         st_tf32x4(dst + sw128_off(16 + j, 16 + k0, 32), x[k0], x[k0 + 1], x[k0 + 2], x[k0 + 3]);
                     }
                 }
-            } else if (warp & 2) {
+            } else if (!(warp & 2)) {
+                // warps 4, 5 and 8, 9: the base's R block (this chunk's Gram A operand, upper
+                // lanes) into A_chain's S0 columns
+                if (cg < 3) {
+                    const int c0 = 32 * (cg - 1);
+                    float v[32];
+                    uint32_t wds[32];
+                    tmem_ld32(tmem + lane_off + kColAG + c0, v);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) wds[j] = __float_as_uint(v[j]);
+                    tmem_st32_issue(tmem + lane_off + kColAC + c0, wds);
+                    tmem_wait_st();
+                }
+            } else {
                 const int sidx = (((warp >> 2) << 1) | (warp & 1)) * 32 + lane;
                 {   // Q^T into B_Y rows 0..63: B[i][t] = Q[t][i], the tf32 words of the Gram A operand's lower half
                     const int t = m - 64;
@@ -784,8 +799,14 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
                         cw[j] = *reinterpret_cast<const uint32_t *>(sm + SM_BG + sw128_off(s_, i, 128)) & 0xffffe000u;
                         kw[j] = *reinterpret_cast<const uint32_t *>(sm + SM_BG + sw128_off(64 + s_, i, 128)) & 0xffffe000u;
                     }
-                    tmem_st16(tmem + lane_off + kColAC + 16 * cg, cw);
+                    tmem_st16(tmem + lane_off + kColAX + 16 * cg, cw);
                     tmem_st16(tmem + lane_off + kColAC + 64 + 16 * cg, kw);
+                }
+                {   // the base's zero block below R
+                    uint32_t z[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) z[j] = 0u;
+                    tmem_st16(tmem + lane_off + kColAC + 16 * cg, z);
                 }
                 {   // L_BA^T: B[n][k] = L_c[32 + k][n] = LT[n][32 + k]
                     const int n = sidx >> 3, k0 = 4 * (sidx & 7);
@@ -796,32 +817,11 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
         }
         handoff(rdy_x);  // -> X = [M_c ; Cb^T] T
 
-        // ---- next chunk, phase 1 (overlaps X_L)
+        // ---- next chunk, phases 1 and 2 (overlap the X, A_chain and D products)
         if (has_next) {
             if (!wait_uniform(bar_tma, static_cast<uint32_t>((c + 1) & 1), p.status)) { alive = false; break; }
             phase1(chunk_len(c + 1), (c + 1) & 1);
-        }
-        if (!wait_uniform(bar_x, par, p.status)) { alive = false; break; }
-        tc_fence_after_sync();
-        // A_chain columns 0..63 (A_X, now consumed) <- base [R ; 0] (the factor e^{g_ref} of the
-        // S0 columns rides on the state operand's rows)
-        {
-            float v[16];
-            uint32_t wds[16];
-            if (q < 2) {
-                tmem_ld16(tmem + lane_off + kColAG + 16 * cg, v);  // R (this chunk's Gram A operand)
-#pragma unroll
-                for (int j = 0; j < 16; ++j) wds[j] = __float_as_uint(v[j]);
-            } else {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) wds[j] = 0u;
-            }
-            tmem_st16(tmem + lane_off + kColAC + 16 * cg, wds);
-        }
-        handoff(rdy_y);  // -> A_chain -= X [Q | L_k], then D = A_chain [S0' ; V]
-
-        // ---- next chunk, phase 2 (overlaps the A_chain and D products)
-        if (has_next) {
+            wsync();
             phase2(chunk_len(c + 1), EREF + ((c + 1) & 1) * 64);
             handoff(rdy_g);  // -> the next chunk's Gram products
         }
