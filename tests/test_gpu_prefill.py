@@ -56,7 +56,8 @@ def test_small_0p1b_fp32_inputs(dev):
     _check(p, o, sf)
 
 
-EDGE_LENGTHS = [[1], [63], [64], [65], [128], [1, 63, 64, 65, 0, 127, 200], [0, 0, 5], [0], [3, 0]]
+EDGE_LENGTHS = [[1], [63], [64], [65], [128], [192], [130, 3, 191], [1, 63, 64, 65, 0, 127, 200], [0, 0, 5], [0],
+                [3, 0]]
 
 
 @pytest.mark.parametrize("lens", EDGE_LENGTHS, ids=lambda x: "-".join(map(str, x)))
@@ -73,6 +74,16 @@ def test_varlen_edges(dev, lens, dtype, with_s0):
         if n == 0:
             ref = s0[b] if s0 is not None else torch.zeros_like(sf[b])
             assert torch.equal(sf[b], ref)
+
+
+def test_many_short_sequences(dev):
+    """Hundreds of short sequences (seeded lengths 1..200, several waves of pairs, most
+    chunks partial) with initial states, against the oracle."""
+    lens = inputs.seqlens_uniform(300, 1, 200, seed=31)
+    p = inputs.prefill_inputs(lens, 2, 64, seed=31, device=dev)
+    s0 = inputs.initial_state(len(lens), 2, 64, seed=31, device=dev)
+    o, sf = _run(p, dev, s0=s0)
+    _check(p, o, sf, s0=s0)
 
 
 def test_no_host_cu_seqlens(dev):
