@@ -92,6 +92,9 @@ constexpr uint32_t kColAX = 192;  // A_X = [M_c ; C^T], the A operand of X (64 c
 constexpr uint32_t kColAC = 256;  // A_chain (128 columns: the S0 block, then the V block)
 constexpr uint32_t kColAG = 384;  // A operand of G = [R ; Q] (for the next chunk)
 constexpr uint32_t kColD = 448;   // D = [O ; S_C - e^{g_C} S0]
+static_assert(kColX == kColG + 128 && kColAX == kColX + 64 && kColAC == kColAX + 64 && kColAG == kColAC + 128 &&
+                  kColD == kColAG + 64 && kColD + 64 <= kTmemCols,
+              "tensor-memory regions must tile the allocation without overlap");
 
 constexpr int kLd = 68;  // padded row stride (floats) of the fp32 L_c^T scratch
 
@@ -113,6 +116,7 @@ constexpr int SM_E63 = SM_EREF + 512;      // 2 x 64: e^{g_C - g_ref} (double-bu
 constexpr int SM_GC = SM_E63 + 512;        // 2 x 64: e^{g_C} (double-buffered across chunks)
 constexpr int SM_BAR = SM_GC + 512;        // 7 mbarriers
 constexpr int SM_SLOT = SM_BAR + 128;
+static_assert(7 * 8 <= SM_SLOT - SM_BAR, "mbarriers exceed their space");
 constexpr int kSmemBytes = SM_SLOT + 64;
 constexpr int kSmemAlloc = kSmemBytes + 1024;
 static_assert(kSmemAlloc <= 232448, "shared memory layout too large");
