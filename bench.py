@@ -164,6 +164,91 @@ class ClockSampler:
         return summarize_clocks(self.lines)
 
 
+class NvmlClockSampler:
+    """Clock and throttle-reason sampling through NVML (read-only queries), about
+    every ``period_ms`` in a background thread, so that even a timed region of a few
+    milliseconds carries samples.  ``start()`` returns None when NVML cannot be
+    loaded (the caller then falls back to nvidia-smi)."""
+
+    # NVML clocks-event reason bits (nvml.h)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, gpu_index: str, period_ms: float = 0.25):
+        self.gpu_index = gpu_index
+        self.period = period_ms / 1000.0
+        self.samples: list[tuple[int, int, int]] = []
+        self._stop = threading.Event()
+        self._thread = None
+
+    def start(self):
+        import ctypes
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return None
+            handle = ctypes.c_void_p()
+            if self.gpu_index.startswith("GPU-") or self.gpu_index.startswith("MIG-"):
+                rc = nv.nvmlDeviceGetHandleByUUID(self.gpu_index.encode(), ctypes.byref(handle))
+            else:
+                rc = nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(int(self.gpu_index)), ctypes.byref(handle))
+            if rc != 0:
+                return None
+            reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        except (OSError, AttributeError, ValueError):
+            return None
+        self._nv, self._handle, self._reasons_fn = nv, handle, reasons_fn
+        mx = ctypes.c_uint(0)
+        nv.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx))  # NVML_CLOCK_SM = 1
+        self.max_mhz = int(mx.value)
+
+        def loop():
+            clk, rs = ctypes.c_uint(0), ctypes.c_ulonglong(0)
+            while not self._stop.is_set():
+                if nv.nvmlDeviceGetClockInfo(handle, 1, ctypes.byref(clk)) == 0 and \
+                        reasons_fn(handle, ctypes.byref(rs)) == 0:
+                    self.samples.append((int(clk.value), self.max_mhz, int(rs.value)))
+                time.sleep(self.period)
+        self._thread = threading.Thread(target=loop, daemon=True)
+        self._thread.start()
+        return self
+
+    def stop(self) -> dict:
+        self._stop.set()
+        if self._thread:
+            self._thread.join(timeout=2)
+        return summarize_nvml(self.samples, self.REASONS)
+
+
+def summarize_nvml(samples, reason_bits) -> dict:
+    if not samples:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": "nvml"}
+    reasons = set()
+    for _, _, bits in samples:
+        for bit, name in reason_bits.items():
+            if bits & bit:
+                reasons.add(name)
+    return {"sm_mhz": statistics.median(s[0] for s in samples), "sm_max_mhz": max(s[1] for s in samples),
+            "reasons": sorted(reasons), "samples": len(samples), "source": "nvml"}
+
+
+class Clocks:
+    """Samples clocks during a timed region: NVML every ~0.25 ms where it loads,
+    else nvidia-smi every 50 ms."""
+
+    def __init__(self, gpu_index: str):
+        self.gpu_index = gpu_index
+        self.impl = None
+
+    def __enter__(self):
+        self.impl = NvmlClockSampler(self.gpu_index).start() or ClockSampler(self.gpu_index).start()
+        return self
+
+    def __exit__(self, *exc):
+        self.result = self.impl.stop()
+        return False
+
+
 def summarize_clocks(lines) -> dict:
     sm, smax, reasons = [], [], set()
     names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
@@ -194,7 +279,7 @@ NAMES = ("r", "w", "k", "v", "kk", "a")
 class DecodeWorkload:
     """32 layer slabs of state, a pool of input sets per layer, per-layer o."""
 
-    def __init__(self, layers, B, H, pool, dev, seed, tail=False, out_bf16=False):
+    def __init__(self, layers, B, H, pool, dev, seed, tail=False, out_bf16=False, state_std=None):
         import torch
 
         from rwkv_linear_attention_gb300 import inputs
@@ -204,7 +289,11 @@ class DecodeWorkload:
         # layers are one contiguous block (one host->device copy per input)
         x = inputs.draw_rwkkva((pool, layers, B, H, N_HEAD), seed=seed, device=dev)
         self.pool = {n: x[n].contiguous() for n in NAMES}
-        self.state = torch.zeros(layers, B, H, N_HEAD, N_HEAD, device=dev)
+        if state_std is None:
+            self.state = torch.zeros(layers, B, H, N_HEAD, N_HEAD, device=dev)
+        else:  # seeded N(0, state_std) fill, one slab per layer
+            self.state = inputs.initial_state(layers * B, H, N_HEAD, seed=seed, std=state_std,
+                                              device=dev).view(layers, B, H, N_HEAD, N_HEAD)
         self.out_dtype = torch.bfloat16 if out_bf16 else torch.float32
         self.o = torch.empty(layers, B, H, N_HEAD, device=dev, dtype=self.out_dtype)
         self.tail = tail
@@ -230,6 +319,15 @@ class DecodeWorkload:
         for s in range(steps):
             self.launch_step(s % self.P)
 
+    def warm_fresh(self, tokens, seed):
+        """Run ``tokens`` distinct seeded random tokens through every layer (each
+        token's inputs drawn like the pool's), e.g. from the zero state to the
+        state after 256 random tokens that the 2.9B decode workload starts from."""
+        from rwkv_linear_attention_gb300 import inputs
+        for t in range(tokens):
+            x = inputs.draw_rwkkva((self.layers, self.B, self.H, N_HEAD), seed=seed * 100003 + t, device=self.dev)
+            self.launch_step(0, src=x)
+
     def capture(self, stream):
         import torch
         graphs = []
@@ -247,13 +345,17 @@ class DecodeWorkload:
         return self.layers * self.B * self.H * STATE_BYTES
 
 
-def time_graphs(graphs, steps, warmup, stream, world):
+def time_graphs(graphs, steps, warmup, stream, world, clocks=None):
+    """CUDA-event time (ms) of ``steps`` graph replays after ``warmup`` untimed
+    ones; ``clocks`` (a Clocks) samples only the timed region."""
     import torch
     for s in range(warmup):
         graphs[s % len(graphs)].replay()
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
+    if clocks is not None:
+        clocks.__enter__()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         start.record(stream)
@@ -261,6 +363,8 @@ def time_graphs(graphs, steps, warmup, stream, world):
             graphs[s % len(graphs)].replay()
         end.record(stream)
     torch.cuda.synchronize()
+    if clocks is not None:
+        clocks.__exit__(None, None, None)
     barrier(world)
     torch.cuda.synchronize()
     return start.elapsed_time(end)
@@ -334,49 +438,257 @@ def decode_e2e(wl, steps, warmup, stream, world):
     return ms, h2d, d2h
 
 
-def prefill_bench(dev, steps, warmup, world):
+def decode_e2e_api(wl, steps, warmup, stream, world):
+    """The decode metric through the public API with host buffers and no CUDA
+    graph: every step copies that step's inputs (all 32 layers) from pinned host
+    memory, makes the 32 ``wkv7.step`` calls (ctypes marshalling, the C ABI's host
+    checks and the launch are all inside the timed region) and reads o back into
+    pinned host memory.  Inputs and outputs are double-buffered and the copies run
+    on two more streams, so step s+1's copy-in and step s-1's copy-out overlap
+    step s's calls, as a serving loop would run them."""
+    import torch
+    host_pool = {n: wl.pool[n].cpu().pin_memory() for n in NAMES}
+    dev_in = [{n: torch.empty_like(wl.pool[n][0]) for n in NAMES} for _ in range(2)]
+    o_dev = [torch.empty_like(wl.o) for _ in range(2)]
+    o_host = [torch.empty(wl.o.shape, dtype=wl.o.dtype).pin_memory() for _ in range(2)]
+    cin, cout = torch.cuda.Stream(device=wl.dev), torch.cuda.Stream(device=wl.dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_free = [torch.cuda.Event() for _ in range(2)]
+
+    def run(n_steps):
+        for s in range(n_steps):
+            i, p = s & 1, s % wl.P
+            with torch.cuda.stream(cin):
+                if s >= 2:
+                    cin.wait_event(ev_done[i])
+                for n in NAMES:
+                    dev_in[i][n].copy_(host_pool[n][p], non_blocking=True)
+                ev_in[i].record(cin)
+            stream.wait_event(ev_in[i])
+            if s >= 2:
+                stream.wait_event(ev_free[i])
+            with torch.cuda.stream(stream):
+                wl.launch_step(p, src=dev_in[i], out=o_dev[i])
+            ev_done[i].record(stream)
+            with torch.cuda.stream(cout):
+                cout.wait_event(ev_done[i])
+                o_host[i].copy_(o_dev[i], non_blocking=True)
+                ev_free[i].record(cout)
+
+    run(max(warmup, 2))
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(cin)
+    stream.wait_stream(cin)
+    cout.wait_stream(cin)
+    run(steps)
+    cout.wait_stream(stream)
+    cout.wait_stream(cin)
+    end.record(cout)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end)
+    h2d = sum(dev_in[0][n].numel() * 4 for n in NAMES)
+    d2h = o_host[0].numel() * o_host[0].element_size()
+    return ms, h2d, d2h
+
+
+def prefill_case(lens, H, seed, dev, with_s0=False, x_dtype=None):
+    """Inputs, outputs and workspace of one prefill workload, on the device."""
     import torch
 
     import rwkv_linear_attention_gb300 as wkv7
     from rwkv_linear_attention_gb300 import inputs
-    cfg = inputs.PREFILL_2P9B
-    lens = [cfg["T"]] * cfg["num_seqs"]
-    p = inputs.prefill_inputs(lens, cfg["H"], cfg["N"], seed=1002, device=dev)
+    x_dtype = x_dtype or torch.bfloat16
+    p = inputs.prefill_inputs(lens, H, N_HEAD, seed=seed, device=dev, x_dtype=x_dtype)
     cu = p["cu_seqlens"]
-    cu_dev = cu.to(dev)
-    T_total = int(cu[-1])
-    o = torch.empty(T_total, cfg["H"], N_HEAD, device=dev)
-    sf = torch.empty(len(lens), cfg["H"], N_HEAD, N_HEAD, device=dev)
-    ws_bytes = wkv7.prefill_workspace_size(len(lens), T_total, cfg["H"])
-    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
-    stream = torch.cuda.Stream(device=dev)
+    T = int(cu[-1])
+    c = {"p": p, "cu": cu, "cu_dev": cu.to(dev), "T": T, "H": H, "num_seqs": len(lens),
+         "s0": inputs.initial_state(len(lens), H, N_HEAD, seed=seed, std=0.1, device=dev) if with_s0 else None,
+         "o": torch.empty(T, H, N_HEAD, device=dev),
+         "sf": torch.empty(len(lens), H, N_HEAD, N_HEAD, device=dev)}
+    ws_n = wkv7.prefill_workspace_size(len(lens), T, H)
+    c["ws"] = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=dev) if ws_n else None
+    x_bytes = 2 if x_dtype == torch.bfloat16 else 4
+    per_th = 5 * x_bytes * N_HEAD + 4 * N_HEAD + 4 * N_HEAD
+    # algorithmic bytes: the token inputs and o, plus the final state (and the initial one when given)
+    c["bytes"] = T * H * per_th + (2 if with_s0 else 1) * len(lens) * H * 4 * N_HEAD * N_HEAD
+    c["flop"] = T * H * PREFILL_FLOP_PER_TOKEN_HEAD
+    return c
 
-    def call():
-        wkv7.prefill(p["r"], p["w"], p["k"], p["v"], p["kk"], p["a"], cu_dev, final_state=sf, o=o,
-                     workspace=ws if ws_bytes else None, cu_seqlens_host=cu, stream=stream)
+
+def prefill_call(c, stream, src=None, o=None, sf=None):
+    import rwkv_linear_attention_gb300 as wkv7
+    p = src or c["p"]
+    wkv7.prefill(p["r"], p["w"], p["k"], p["v"], p["kk"], p["a"], c["cu_dev"], initial_state=c["s0"],
+                 final_state=c["sf"] if sf is None else sf, o=c["o"] if o is None else o, workspace=c["ws"],
+                 cu_seqlens_host=c["cu"], stream=stream)
+
+
+def prefill_e2e(c, calls, warmup, stream, world):
+    """The prefill metric through the public API with host buffers: every call
+    copies its inputs (r, k, v, kk, a, w; and the initial states when the workload
+    has them) from pinned host memory, runs ``wkv7.prefill`` and copies o and the
+    final states back into pinned host memory.  Double-buffered over copy-in and
+    copy-out streams, so call i+1's copy-in and call i-1's copy-out overlap call
+    i; timed from the first copy-in to the last copy-out."""
+    import torch
+    names = NAMES + (("s0",) if c["s0"] is not None else ())
+    srcs = dict(c["p"], s0=c["s0"])
+    host = {n: srcs[n].cpu().pin_memory() for n in names}
+    dev_in = [{n: torch.empty_like(srcs[n]) for n in names} for _ in range(2)]
+    o_dev = [torch.empty_like(c["o"]) for _ in range(2)]
+    sf_dev = [torch.empty_like(c["sf"]) for _ in range(2)]
+    o_host = [torch.empty(c["o"].shape, dtype=c["o"].dtype).pin_memory() for _ in range(2)]
+    sf_host = [torch.empty(c["sf"].shape, dtype=c["sf"].dtype).pin_memory() for _ in range(2)]
+    cin, cout = torch.cuda.Stream(device=c["o"].device), torch.cuda.Stream(device=c["o"].device)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_free = [torch.cuda.Event() for _ in range(2)]
+
+    def run(n):
+        import rwkv_linear_attention_gb300 as wkv7
+        for s in range(n):
+            i = s & 1
+            with torch.cuda.stream(cin):
+                if s >= 2:
+                    cin.wait_event(ev_done[i])
+                for nm in names:
+                    dev_in[i][nm].copy_(host[nm], non_blocking=True)
+                ev_in[i].record(cin)
+            stream.wait_event(ev_in[i])
+            if s >= 2:
+                stream.wait_event(ev_free[i])
+            d = dev_in[i]
+            wkv7.prefill(d["r"], d["w"], d["k"], d["v"], d["kk"], d["a"], c["cu_dev"], initial_state=d.get("s0"),
+                         final_state=sf_dev[i], o=o_dev[i], workspace=c["ws"], cu_seqlens_host=c["cu"],
+                         stream=stream)
+            ev_done[i].record(stream)
+            with torch.cuda.stream(cout):
+                cout.wait_event(ev_done[i])
+                o_host[i].copy_(o_dev[i], non_blocking=True)
+                sf_host[i].copy_(sf_dev[i], non_blocking=True)
+                ev_free[i].record(cout)
+
+    run(max(warmup, 2))
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(cin)
+    stream.wait_stream(cin)
+    cout.wait_stream(cin)
+    run(calls)
+    cout.wait_stream(stream)
+    cout.wait_stream(cin)
+    end.record(cout)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(start.elapsed_time(end), world, c["o"].device)
+    h2d = sum(dev_in[0][n].numel() * dev_in[0][n].element_size() for n in names)
+    d2h = o_host[0].numel() * o_host[0].element_size() + sf_host[0].numel() * 4
+    del dev_in, o_dev, sf_dev
+    return ms, h2d, d2h
+
+
+def oracle_rate(fn, units, budget_s, threads):
+    """Time ``fn(n, threads)`` (n units of work) on the host: n grows until one run
+    takes about ``budget_s``; when all ``units`` take less, the full run is repeated
+    until the budget is spent.  Returns (units per second, units timed, seconds)."""
+    n = 1
+    while True:
+        t0 = time.perf_counter()
+        fn(n, threads)
+        dt = time.perf_counter() - t0
+        if dt >= budget_s:
+            return n / dt, n, dt
+        if n >= units:
+            reps = max(1, int(budget_s / max(dt, 1e-6)))
+            t0 = time.perf_counter()
+            for _ in range(reps):
+                fn(n, threads)
+            dt = time.perf_counter() - t0
+            return reps * n / dt, reps * n, dt
+        n = min(units, max(n + 1, int(n * min(8.0, 1.5 * budget_s / max(dt, 1e-4)))))
+
+
+def cpu_baseline_prefill(lens, H, budget_s):
+    """The oracle, as it stands, on the host cores over a bounded sample of a
+    prefill workload (whole sequences of a subset of its heads), once on one core
+    and once on all cores; tokens/s scaled to the workload's H heads."""
+    import oracle
+    from rwkv_linear_attention_gb300 import inputs
+    T = sum(lens)
+    p = inputs.prefill_inputs(lens, H, N_HEAD, seed=5, device="cpu")
+    cu = p["cu_seqlens"].numpy()
+    arrs = {n: p[n].float().numpy() for n in NAMES}
+    all_cores = oracle.default_threads()
+
+    def fn(n_heads, threads):
+        oracle.run(*(arrs[n][:, :n_heads] for n in NAMES), cu_seqlens=cu, nthreads=threads)
+    out = {}
+    for label, threads in (("one_core", 1), ("all_cores", all_cores)):
+        rate, n, dt = oracle_rate(fn, H, budget_s / 2, threads)
+        out[label] = {"value": round(rate * T / H, 1), "unit": "tokens/s", "cores": threads,
+                      "sample": f"{n} head-passes of {H} heads over all {len(lens)} sequences ({T} tokens), "
+                                f"{dt:.2f} s"}
+    return {"value": out["all_cores"]["value"], "unit": "tokens/s", "cores": all_cores, "kind": "oracle",
+            "sample": out["all_cores"]["sample"], "one_core": out["one_core"]}
+
+
+def cpu_baseline_decode_cfg(B, H, budget_s, state_std=None):
+    """The oracle on one decode layer-step of B x H heads (a subset of the heads
+    when one layer-step would exceed the budget), one core and all cores; GB/s of
+    state traffic."""
+    import oracle
+    from rwkv_linear_attention_gb300 import inputs
+    x = inputs.draw_rwkkva((B, H, N_HEAD), seed=3, device="cpu")
+    arrs = {n: x[n].reshape(B * H, 1, N_HEAD).numpy() for n in NAMES}
+    s0 = inputs.initial_state(B * H, 1, N_HEAD, seed=3, std=state_std or 0.1).double().numpy()
+
+    def fn(n_heads, threads):
+        oracle.step(*(arrs[n][:n_heads] for n in NAMES), state=s0[:n_heads], nthreads=threads)
+    out = {}
+    for label, threads in (("one_core", 1), ("all_cores", oracle.default_threads())):
+        rate, n, dt = oracle_rate(fn, B * H, budget_s / 2, threads)
+        out[label] = {"value": round(rate * STATE_BYTES / 1e9, 4), "unit": "GB/s", "cores": threads,
+                      "sample": f"{n} head-steps (layer-steps of {B * H} heads), {dt:.2f} s"}
+    return {"value": out["all_cores"]["value"], "unit": "GB/s", "cores": out["all_cores"]["cores"],
+            "kind": "oracle", "sample": out["all_cores"]["sample"], "one_core": out["one_core"]}
+
+
+def prefill_bench(c, steps, warmup, world, clocks=None):
+    """CUDA-event time per call of the prefill workload ``c`` (see prefill_case)."""
+    import torch
+
+    import rwkv_linear_attention_gb300 as wkv7
+    dev = c["o"].device
+    stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
         for _ in range(warmup):
-            call()
+            prefill_call(c, stream)
     torch.cuda.synchronize()
     wkv7.check_device_status(stream)
     barrier(world)
     torch.cuda.synchronize()
+    if clocks is not None:
+        clocks.__enter__()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         start.record(stream)
         for _ in range(steps):
-            call()
+            prefill_call(c, stream)
         end.record(stream)
     torch.cuda.synchronize()
+    if clocks is not None:
+        clocks.__exit__(None, None, None)
     barrier(world)
-    ms = max_over_ranks(start.elapsed_time(end), world, dev) / steps
-    token_heads = T_total * cfg["H"]
-    return {
-        "tokens": T_total, "token_heads": token_heads, "ms_per_call": ms,
-        "algorithmic_bytes": token_heads * PREFILL_BYTES_PER_TOKEN_HEAD,
-        "algorithmic_flop": token_heads * PREFILL_FLOP_PER_TOKEN_HEAD,
-        "input_bytes_gt_l2": token_heads * PREFILL_BYTES_PER_TOKEN_HEAD > L2_BYTES,
-    }
+    return max_over_ranks(start.elapsed_time(end), world, dev) / steps
 
 
 def time_stream(fn, steps, warmup, stream):
@@ -582,6 +894,102 @@ def cpu_baseline_decode(B, H, layers, budget_s=15.0):
             "sample": f"{n_layer_steps} layer-steps of B={B} x H={H} heads (fp64, {dt:.1f} s)"}
 
 
+def roofline_obj(nbytes, ms, peaks, peak_kind, **extra):
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    d = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+         "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_kind": f"{peak_kind} (copy bandwidth)"}
+    d.update(extra)
+    return d
+
+
+def config_lines(args, dev, peaks, peak_kind, world, gpu_index, cpu_budget):
+    """One object per remaining named workload (the 0.1B case, 2.9B decode at B = 1
+    and 8, 7.2B decode at B = 256, the two 7.2B prefill runs), each timed in its own
+    region with CUDA events, its roofline fraction, its clocks and (rank 0, unless
+    disabled) the oracle on a bounded sample of the same workload."""
+    import torch
+
+    import rwkv_linear_attention_gb300 as wkv7
+    from rwkv_linear_attention_gb300 import inputs
+    rank = dist_env()[0]
+    stream = torch.cuda.Stream(device=dev)
+    want_cpu = rank == 0 and cpu_budget > 0
+    out = []
+
+    # 0.1B: B=1, T=64, H=12, fp32 inputs: the prefill (token-serial kernel) and the
+    # 64-step decode loop from the zero state
+    c0 = inputs.SMALL_0P1B
+    c = prefill_case([c0["T"]], c0["H"], 1000, dev, x_dtype=torch.float32)
+    with Clocks(gpu_index) as clk:
+        ms = time_stream(lambda: prefill_call(c, stream), max(args.steps, 8), args.warmup, stream)
+    wkv7.check_device_status(stream)
+    x = inputs.draw_rwkkva((c0["T"], 1, c0["H"], N_HEAD), seed=1000, device=dev)
+    st = torch.zeros(1, c0["H"], N_HEAD, N_HEAD, device=dev)
+    o1 = torch.empty(1, c0["H"], N_HEAD, device=dev)
+
+    def loop():
+        for t in range(c0["T"]):
+            wkv7.step(*(x[n][t] for n in NAMES), st, o1, stream=stream)
+    ms_loop = time_stream(loop, max(args.steps // 4, 4), args.warmup, stream)
+    obj = {"config": 0, "workload": "0.1B geometry, B=1, T=64, H=12, fp32 inputs, zero initial state",
+           "metric": "prefill tokens/s", "value": round(world * c0["T"] / (ms * 1e-3), 1), "unit": "tokens/s",
+           "prefill_ms": round(ms, 5),
+           "decode_loop_ms": round(ms_loop, 5), "clocks": clk.result,
+           "roofline": roofline_obj(c["bytes"], ms, peaks, peak_kind, kernel="wkv7_prefill_scan_kernel",
+                                    note="launch-bound: 0.4 MB per call")}
+    if want_cpu:
+        obj["cpu_baseline"] = cpu_baseline_prefill([c0["T"]], c0["H"], cpu_budget)
+    out.append(obj)
+    del c, x, st
+    torch.cuda.empty_cache()
+
+    # 2.9B decode at B = 1 and 8, from the state after 256 random tokens; 7.2B at B = 256
+    # from a seeded N(0, 0.1) state
+    for cfg_id, cfg, B, std in ((1, inputs.DECODE_2P9B, 1, None), (1, inputs.DECODE_2P9B, 8, None),
+                                (3, inputs.DECODE_7P2B, inputs.DECODE_7P2B["B"], inputs.DECODE_7P2B["state_std"])):
+        wl = DecodeWorkload(cfg["layers"], B, cfg["H"], 4, dev, seed=1000 + cfg_id, state_std=std)
+        if std is None:
+            wl.warm_fresh(cfg["warm_tokens"], seed=1000 + cfg_id)
+        graphs = wl.capture(stream)
+        steps = max(args.steps, 8)
+        clk = Clocks(gpu_index)
+        ms = max_over_ranks(time_graphs(graphs, steps, args.warmup, stream, world, clocks=clk), world, dev) / steps
+        launch_us = ms * 1e3 / wl.layers
+        obj = {"config": cfg_id, "workload": f"decode, {'2.9B' if cfg_id == 1 else '7.2B'} geometry: "
+                                             f"{wl.layers} layers x H={wl.H}, B={B}, CUDA-graph replay",
+               "metric": "state-GB/s", "value": round(world * wl.state_bytes_per_step() / (ms * 1e-3) / 1e9, 2),
+               "unit": "GB/s", "ms_per_step": round(ms, 5), "us_per_launch": round(launch_us, 3), "steps": steps,
+               "clocks": clk.result,
+               "roofline": roofline_obj(B * wl.H * STEP_BYTES, launch_us * 1e-3, peaks, peak_kind,
+                                        kernel="wkv7_step_kernel", algorithmic_bytes_per_launch=B * wl.H * STEP_BYTES)}
+        if want_cpu:
+            obj["cpu_baseline"] = cpu_baseline_decode_cfg(B, wl.H, cpu_budget, state_std=std)
+        out.append(obj)
+        del graphs, wl
+        torch.cuda.empty_cache()
+
+    # 7.2B prefill: 16 sequences of U[1, 32768] tokens, and one 32768-token sequence,
+    # both with N(0, 0.1) initial states
+    v = inputs.VARLEN_7P2B
+    for label, lens in (("7.2B varlen, 16 x U[1, 32768]", inputs.seqlens_uniform(v["num_seqs"], v["lo"], v["hi"], 1004)),
+                        ("7.2B, 1 x 32768", [v["single_T"]])):
+        c = prefill_case(lens, v["H"], 1004, dev, with_s0=True)
+        calls = max(3, args.prefill_steps // 4)
+        clk = Clocks(gpu_index)
+        ms = prefill_bench(c, calls, 2, world, clocks=clk)
+        obj = {"config": 4, "workload": f"prefill, {label}, H=64, bf16 inputs, initial and final states",
+               "metric": "tokens/s", "value": round(world * c["T"] / (ms * 1e-3), 1), "unit": "tokens/s",
+               "ms_per_call": round(ms, 4), "tokens": c["T"], "calls": calls, "clocks": clk.result,
+               "roofline": roofline_obj(c["bytes"], ms, peaks, peak_kind, kernel="wkv7_prefill_chunked_kernel",
+                                        algorithmic_bytes_per_launch=c["bytes"])}
+        if want_cpu:
+            obj["cpu_baseline"] = cpu_baseline_prefill(lens, v["H"], cpu_budget)
+        out.append(obj)
+        del c
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import torch
 
@@ -601,6 +1009,7 @@ def run_ours(args):
 
     from rwkv_linear_attention_gb300 import inputs
     peaks, peak_kind = load_peaks()
+    gpu_index = smi_index(local)
     if args.workload == "configs":
         if rank == 0:
             run_configs(args, dev, peaks)
@@ -611,25 +1020,26 @@ def run_ours(args):
             backward_line(args, dev, peaks, f"prefill backward 2.9B {n}x4096", [4096] * n, 40, False,
                           torch.cuda.Stream(device=dev))
         return
+    pcfg = inputs.PREFILL_2P9B
     if args.workload == "prefill":
-        pre = prefill_bench(dev, args.prefill_steps, args.warmup, world)
+        c = prefill_case([pcfg["T"]] * pcfg["num_seqs"], pcfg["H"], 1002, dev)
+        ms = prefill_bench(c, args.prefill_steps, args.warmup, world)
         if rank == 0:
-            gbs = pre["algorithmic_bytes"] / (pre["ms_per_call"] / 1e3) / 1e9
-            print(json.dumps({"workload": "prefill 2.9B (8 x 4096, H=40, bf16)", "ms_per_call": pre["ms_per_call"],
-                              "tokens_per_s": world * pre["tokens"] / (pre["ms_per_call"] / 1e3),
+            gbs = c["bytes"] / (ms / 1e3) / 1e9
+            print(json.dumps({"workload": "prefill 2.9B (8 x 4096, H=40, bf16)", "ms_per_call": ms,
+                              "tokens_per_s": world * c["T"] / (ms / 1e3),
                               "achieved_gbs": gbs, "frac": gbs / peaks["hbm_gbs"]}), flush=True)
         return
     cfg = inputs.DECODE_2P9B
     B = args.batch
     wl = DecodeWorkload(cfg["layers"], B, cfg["H"], cfg["pool"], dev, seed=1001 + rank)
-    wl.warm(min(cfg["warm_tokens"], 64))
+    wl.warm_fresh(cfg["warm_tokens"], seed=1001 + rank)  # the state after 256 random tokens
     stream = torch.cuda.Stream(device=dev)
     graphs = wl.capture(stream)
 
-    sampler = ClockSampler(smi_index(local))
-    sampler.start()
-    ms = time_graphs(graphs, args.steps, args.warmup, stream, world)
-    clocks = sampler.stop()
+    clk = Clocks(gpu_index)
+    ms = time_graphs(graphs, args.steps, args.warmup, stream, world, clocks=clk)
+    clocks = clk.result
     ms = max_over_ranks(ms, world, dev)
     ms_step = ms / args.steps
     launches = wl.layers * args.steps
@@ -641,7 +1051,6 @@ def run_ours(args):
     step_src = [os.path.join(csrc, "wkv7_step.cu")] + shared
     prefill_src = [os.path.join(csrc, "wkv7_prefill_chunked.cu")] + shared
     traffic = kernel_traffic("wkv7_step_kernel", f"B={B},H={cfg['H']}", step_src)
-    del graphs
 
     if args.workload == "decode":
         if rank == 0:
@@ -649,17 +1058,49 @@ def run_ours(args):
                               "achieved_gbs": achieved, "frac": achieved / peaks["hbm_gbs"], "clocks": clocks}),
                   flush=True)
         return
-    e2e_ms, h2d, d2h = decode_e2e(wl, max(args.steps // 4, 8), args.warmup, stream, world)
+    e2e_steps = max(args.steps, 8)
+    g_ms, g_h2d, g_d2h = decode_e2e(wl, e2e_steps, args.warmup, stream, world)
+    g_ms = max_over_ranks(g_ms, world, dev)
+    del graphs
+    e2e_ms, h2d, d2h = decode_e2e_api(wl, e2e_steps, args.warmup, stream, world)
     e2e_ms = max_over_ranks(e2e_ms, world, dev)
-    e2e_steps = max(args.steps // 4, 8)
     e2e_value = world * wl.state_bytes_per_step() * e2e_steps / (e2e_ms / 1e3) / 1e9
+    g_value = world * wl.state_bytes_per_step() * e2e_steps / (g_ms / 1e3) / 1e9
     del wl
     torch.cuda.empty_cache()
 
-    pre = prefill_bench(dev, args.prefill_steps, max(args.warmup, 3), world)
-    pre_tokens_s = world * pre["tokens"] / (pre["ms_per_call"] / 1e3)
-    pre_gbs = pre["algorithmic_bytes"] / (pre["ms_per_call"] / 1e3) / 1e9
-    pre_tflops = pre["algorithmic_flop"] / (pre["ms_per_call"] / 1e3) / 1e12
+    c = prefill_case([pcfg["T"]] * pcfg["num_seqs"], pcfg["H"], 1002, dev)
+    pclk = Clocks(gpu_index)
+    pms = prefill_bench(c, args.prefill_steps, max(args.warmup, 3), world, clocks=pclk)
+    pre_tokens_s = world * c["T"] / (pms / 1e3)
+    pre_tflops = c["flop"] / (pms / 1e3) / 1e12
+    pe_calls = max(args.prefill_steps // 4, 4)
+    pe_ms, pe_h2d, pe_d2h = prefill_e2e(c, pe_calls, 2, torch.cuda.Stream(device=dev), world)
+    pre_e2e = world * c["T"] * pe_calls / (pe_ms / 1e3)
+    prefill = {
+        "metric": "prefill tokens/s", "value": round(pre_tokens_s, 1), "unit": "tokens/s",
+        "ms_per_call": round(pms, 4), "calls": args.prefill_steps,
+        "config": {"workload": "WKV-7 chunked prefill, 2.9B geometry: 8 x 4096 tokens, H=40, N=64, "
+                               "bf16 r,k,v,kk,a, fp32 w, zero initial state, final state out",
+                   "l2": "inputs larger than L2"},
+        "clocks": pclk.result,
+        "roofline": roofline_obj(c["bytes"], pms, peaks, peak_kind,
+                                 traffic=kernel_traffic("wkv7_prefill_chunked_kernel", "2.9B 8x4096 H=40", prefill_src),
+                                 kernel="wkv7_prefill_chunked_kernel", algorithmic_bytes_per_launch=c["bytes"],
+                                 tensor_tflops=round(pre_tflops, 2),
+                                 tensor_frac_of_bf16=round(pre_tflops / peaks["bf16_tflops"], 4)),
+        "e2e": {"value": round(pre_e2e, 1), "unit": "tokens/s", "h2d_bytes_per_step": pe_h2d,
+                "d2h_bytes_per_step": pe_d2h, "steps": pe_calls,
+                "how": "per call: pinned H2D of r, k, v, kk, a, w, one wkv7.prefill call through the binding, "
+                       "D2H of o and the final states; double-buffered over copy-in and copy-out streams; timed "
+                       "from the first copy-in to the last copy-out"},
+    }
+    del c
+    torch.cuda.empty_cache()
+    budget = 0.0 if args.no_cpu_baseline else args.cpu_budget
+    if rank == 0 and budget > 0:
+        prefill["cpu_baseline"] = cpu_baseline_prefill([pcfg["T"]] * pcfg["num_seqs"], pcfg["H"], budget / 2)
+    configs = config_lines(args, dev, peaks, peak_kind, world, gpu_index, budget / 4)
 
     line = {
         "metric": METRIC,
@@ -675,8 +1116,9 @@ def run_ours(args):
         "dtype": "f32",
         "data": "synthetic (seeded; r,k,v~N(0,1), k/sqrt(N), w=-0.606531*sigmoid(N(0,1)), unit kk, a=sigmoid(N(0,1)))",
         "config": {
-            "workload": f"WKV-7 decode, 2.9B geometry: 32 layers x H=40 x N=64, B={B}, fp32 state in place, "
-                        "one token per step (32 launches), 16 input sets per layer cycled, CUDA-graph replay",
+            "workload": f"WKV-7 decode, 2.9B geometry: 32 layers x H=40 x N=64, B={B}, fp32 state in place "
+                        "(starting from the state after 256 random tokens), one token per step (32 launches), "
+                        "16 input sets per layer cycled, CUDA-graph replay",
             "layers": cfg["layers"], "B": B, "H": cfg["H"], "N": N_HEAD,
             "state_bytes_per_step": cfg["layers"] * B * cfg["H"] * STATE_BYTES,
             "l2": "inputs larger than L2 (state touched per step = "
@@ -692,29 +1134,20 @@ def run_ours(args):
         },
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "how": "per step: pinned H2D of all 32 layers' inputs, 32 wkv7_step calls (one CUDA graph), D2H of o; "
-                       "double-buffered and pipelined over copy-in and copy-out streams (step s+1's copy-in and "
-                       "step s-1's copy-out overlap step s's calls); timed from the first copy-in to the last "
-                       "copy-out"},
+                "how": "per step: pinned H2D of all 32 layers' inputs, 32 wkv7.step calls through the binding "
+                       "(ctypes, the C ABI's host checks and each launch inside the timed region; no CUDA graph), "
+                       "D2H of o; double-buffered over copy-in and copy-out streams; timed from the first "
+                       "copy-in to the last copy-out"},
+        "e2e_graph": {"value": round(g_value, 2), "unit": "GB/s", "h2d_bytes_per_step": g_h2d,
+                      "d2h_bytes_per_step": g_d2h, "steps": e2e_steps,
+                      "how": "as e2e, with each step's 32 calls captured once in a CUDA graph and replayed"},
         "gpu_launches": launches,
         "clocks": clocks,
-        "prefill": {
-            "metric": "prefill tokens/s", "value": round(pre_tokens_s, 1), "unit": "tokens/s",
-            "ms_per_call": round(pre["ms_per_call"], 4), "calls": args.prefill_steps,
-            "config": {"workload": "WKV-7 chunked prefill, 2.9B geometry: 8 x 4096 tokens, H=40, N=64, "
-                                   "bf16 r,k,v,kk,a, fp32 w, zero initial state, final state out",
-                       "l2": "inputs larger than L2"},
-            "roofline": {"bound": "hbm", "achieved": round(pre_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": round(pre_gbs / peaks["hbm_gbs"], 4),
-                         "traffic": kernel_traffic("wkv7_prefill_chunked_kernel", "2.9B 8x4096 H=40", prefill_src),
-                         "kernel": "wkv7_prefill_chunked_kernel",
-                         "algorithmic_bytes_per_launch": pre["algorithmic_bytes"],
-                         "tensor_tflops": round(pre_tflops, 2),
-                         "tensor_frac_of_bf16": round(pre_tflops / peaks["bf16_tflops"], 4)},
-        },
+        "prefill": prefill,
+        "configs": configs,
     }
-    if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_decode(B, cfg["H"], cfg["layers"], budget_s=args.cpu_budget)
+    if rank == 0 and budget > 0:
+        line["cpu_baseline"] = cpu_baseline_decode(B, cfg["H"], cfg["layers"], budget_s=budget / 4)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

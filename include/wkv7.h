@@ -227,10 +227,17 @@ WKV7_API size_t wkv7_prefill_workspace_size(int num_seqs, int T_total, int H, in
  *                     any other argument.  Calls that overlap on the GPU must
  *                     use distinct workspaces.
  *
- * Precondition for the chunked formulation: w >= -2.5 elementwise (every
- * RWKV-7 model has w in (-0.6066, 0)).  The chunked kernel takes a chunk's
- * decay factors relative to its 32nd token, so for such w every factor lies
- * within e^{+-80}, finite in fp32.
+ * Domain of the chunked formulation (bf16 inputs): w >= -1 elementwise
+ * (every RWKV-7 model has w in (-0.6066, 0)).  The chunked kernel takes a
+ * chunk's decay factors relative to its 32nd token, so each scaled operand
+ * carries a factor within e^{+-32} and the chunk's removal block, where one
+ * channel's growing factor meets another's through the UT transform, within
+ * e^{64}: finite in fp32 with a wide margin.  (At w = -2.5 on some channels
+ * and 0 on others that block overflows.)  The kernel checks the domain on the
+ * device: a w below -1 (or -inf) is reported by wkv7_check_device_status as
+ * WKV7_ERR_INVALID_ARG, and the outputs of that call are then unspecified
+ * (they may hold inf or NaN).  fp32 inputs take a token-serial kernel that
+ * has no such limit.
  */
 WKV7_API wkv7_status wkv7_prefill(int num_seqs, int T_total, int H, int N,
                          const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
@@ -352,8 +359,10 @@ WKV7_API wkv7_status wkv7_prefill_noalloc(int num_seqs, int T_total, int H, int 
  *                      summaries); contents need not be initialised.
  *
  * Every written range must not overlap any other argument.  Zero-length
- * sequences give d_initial_state = d_final_state.  Same precondition on w as
- * wkv7_prefill (w >= -2.5).  Stream-ordered, no synchronisation; a malformed
+ * sequences give d_initial_state = d_final_state.  Same domain as the chunked
+ * wkv7_prefill (w >= -1, for either input type), checked on the device the
+ * same way: a w below it is reported by wkv7_check_device_status as
+ * WKV7_ERR_INVALID_ARG.  Stream-ordered, no synchronisation; a malformed
  * device cu_seqlens (when no host copy is given) is reported by
  * wkv7_check_device_status and leaves the token gradients unwritten.
  */
@@ -387,8 +396,15 @@ WKV7_API const char *wkv7_status_string(wkv7_status status);
 /*
  * wkv7_check_device_status -- synchronise `stream`, then read and clear the
  * current device's status word.  Returns WKV7_OK, WKV7_ERR_TIMEOUT,
- * WKV7_ERR_DEVICE_BOUNDS, WKV7_ERR_INVALID_ARG (malformed device cu_seqlens)
- * or WKV7_ERR_CUDA (the synchronisation itself failed).
+ * WKV7_ERR_DEVICE_BOUNDS, WKV7_ERR_INVALID_ARG (malformed device cu_seqlens,
+ * or a w below the chunked kernels' domain) or WKV7_ERR_CUDA (the
+ * synchronisation itself failed).
+ *
+ * The library looks up the device address of this status word (and of the
+ * fixed scratch of wkv7_prefill_noalloc) once per device and keeps it for the
+ * life of the process.  After cudaDeviceReset, or any other teardown of a
+ * device's primary context, those cached addresses are stale: do not call the
+ * library on that device again in the same process.
  */
 WKV7_API wkv7_status wkv7_check_device_status(cudaStream_t stream);
 

@@ -531,7 +531,7 @@ wkv7_status wkv7_check_device_status(cudaStream_t stream) {
     }
     if (host & wkv7::kDevTimeout) return WKV7_ERR_TIMEOUT;
     if (host & wkv7::kDevBounds) return WKV7_ERR_DEVICE_BOUNDS;
-    if (host & wkv7::kDevBadSeqlens) return WKV7_ERR_INVALID_ARG;
+    if (host & (wkv7::kDevBadSeqlens | wkv7::kDevDomain)) return WKV7_ERR_INVALID_ARG;
     return WKV7_OK;
 }
 

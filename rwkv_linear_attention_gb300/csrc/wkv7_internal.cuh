@@ -17,7 +17,16 @@ enum : unsigned {
     kDevTimeout = 1u,     // a bounded wait expired
     kDevBounds = 2u,      // an index was out of range
     kDevBadSeqlens = 4u,  // device cu_seqlens malformed
+    kDevDomain = 8u,      // an input lies outside a kernel's stated domain (w < kMinLogDecay)
 };
+
+// Smallest log-decay the chunked kernels (prefill and its backward) accept.  They
+// take a chunk's decay factors relative to its 32nd token, so each scaled operand
+// carries a factor within e^{+-32|w|max}; a product of two of them (the removal
+// block C^T T Q of the chunk transition, where one channel's growth meets
+// another's through T) reaches e^{64|w|max}, which must stay well inside fp32
+// (e^{88.7}).  With w >= -1 that is e^{64}.  RWKV-7 models have w in (-0.6066, 0).
+constexpr float kMinLogDecay = -1.0f;
 
 __device__ __forceinline__ void report(unsigned *status, unsigned bit) {
     if (status) atomicOr(status, bit);

@@ -447,6 +447,10 @@ __device__ __forceinline__ void load_w16(float (&x)[16], const BwdArgs &p, const
     const int t = threadIdx.x >> 2, cc = (threadIdx.x & 3) * 16;
     const bool valid = t < c.len;
     load16(x, p.w, false, ((size_t)(c.tb + (valid ? t : 0)) * p.H + h) * kN + cc, valid);
+    float wmin = 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) wmin = fminf(wmin, x[j]);
+    if (valid && wmin < kMinLogDecay) report(p.status, kDevDomain);  // outside the domain: reported
 }
 
 // Inclusive cumulative sum of w over the chunk into Gm ([64][kLD]) from the values

@@ -61,7 +61,8 @@
 // tensor memory (the hardware reads them at tf32 precision); accumulation is
 // fp32 and the state carried between chunks is fp32.  The decay factors of
 // the Gram operands are taken relative to the chunk's 32nd token, so for
-// w >= -2.5 every factor lies within e^{+-80} (finite in fp32).
+// w >= -1 every factor lies within e^{+-32} and every product of two within
+// e^{+-64} (finite in fp32); phase 1 reports a w below -1.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -382,6 +383,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
         const int ch = 2 * (tid & 31), seg = tid >> 5;
         float2 g[4];
         float2 acc = make_float2(0.f, 0.f);
+        float wmin = 0.f;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int t = 4 * seg + u;
@@ -389,9 +391,11 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
                 const float2 wv = *reinterpret_cast<const float2 *>(E + t * 64 + ch);
                 acc.x += wv.x;
                 acc.y += wv.y;
+                wmin = fminf(wmin, fminf(wv.x, wv.y));
             }
             g[u] = acc;
         }
+        if (wmin < kMinLogDecay) report(p.status, kDevDomain);  // outside the domain: reported, not trapped
         *reinterpret_cast<float2 *>(TOT + seg * 64 + ch) = acc;
         wsync();
         float2 pre = make_float2(0.f, 0.f);

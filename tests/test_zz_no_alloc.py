@@ -1,13 +1,17 @@
 """wkv7_prefill_noalloc, the prefill for callers that cannot allocate device
 memory (a memory plan fixed up front, code recorded during stream capture, a
 host that only holds pointers to someone else's buffers), against the
-regular wkv7_prefill.
+regular wkv7_prefill and against the fp64 oracle.
 
 It runs the same kernels with its scratch in a fixed device array instead of
 a caller workspace, so its outputs must match the regular entry point's
 within the prefill tolerance -- on two calls in a row, the second reusing the
-scratch the first one left behind.  Called through the C ABI.  This file is
-named to be collected last.
+scratch the first one left behind -- and, since both share those kernels,
+each call is also held to the oracle on its own.  The batches cover the
+longest-first schedule (unequal lengths: the order is written into the fixed
+array and read back) and the two cases that write no order at all (one
+sequence; equal lengths).  Called through the C ABI.  This file is named to be
+collected last.
 """
 import ctypes
 
@@ -16,7 +20,7 @@ import torch
 
 import rwkv_linear_attention_gb300 as wkv7
 from rwkv_linear_attention_gb300 import _lib, inputs
-from tests.gpu_util import rel_err
+from tests.gpu_util import oracle_prefill, rel_err
 
 pytestmark = pytest.mark.gpu
 
@@ -48,12 +52,15 @@ def _noalloc(p, s0, sf, o):
     return o, sf
 
 
+# Two unequal-length batches (the longest-first order is written into the fixed
+# array and read back on each call), one single-sequence batch and one batch of
+# equal lengths (neither writes an order).
+CASES = [([300, 5, 129, 64, 0, 700], 3, 31), ([17, 640, 2, 255], 2, 32), ([1000], 4, 33), ([130, 130, 130], 2, 34)]
+
+
 @pytest.mark.parametrize("call", [0, 1])
 def test_noalloc_matches_prefill_two_calls_in_a_row(dev, call):
-    # two different unequal-length batches, so the longest-first schedule in the
-    # static scratch is written and read on each call
-    cases = [([300, 5, 129, 64, 0, 700], 3, 31), ([17, 640, 2, 255], 2, 32)]
-    for lens, H, seed in cases:
+    for lens, H, seed in CASES:
         p = inputs.prefill_inputs(lens, H, 64, seed=seed + call, device=dev)
         s0 = inputs.initial_state(len(lens), H, 64, seed=seed, device=dev)
         o_ref, sf_ref = wkv7.prefill(p["r"], p["w"], p["k"], p["v"], p["kk"], p["a"], p["cu_seqlens"].to(dev),
@@ -64,6 +71,10 @@ def test_noalloc_matches_prefill_two_calls_in_a_row(dev, call):
         _noalloc(p, s0, sf, o)
         assert rel_err(o, o_ref) <= TOL
         assert rel_err(sf, sf_ref) <= TOL
+        # both entry points run the same kernels, so hold this one to the oracle too
+        o_or, s_or = oracle_prefill(p, p["cu_seqlens"], s0=s0)
+        assert rel_err(o, o_or) <= TOL, lens
+        assert rel_err(sf, s_or) <= TOL, lens
 
 
 def test_noalloc_rejects_batches_beyond_its_scratch(dev):
