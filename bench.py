@@ -279,7 +279,7 @@ NAMES = ("r", "w", "k", "v", "kk", "a")
 class DecodeWorkload:
     """32 layer slabs of state, a pool of input sets per layer, per-layer o."""
 
-    def __init__(self, layers, B, H, pool, dev, seed, tail=False, out_bf16=False, state_std=None):
+    def __init__(self, layers, B, H, pool, dev, seed, tail=False, out_bf16=False, state_std=None, state_dtype=None):
         import torch
 
         from rwkv_linear_attention_gb300 import inputs
@@ -294,6 +294,9 @@ class DecodeWorkload:
         else:  # seeded N(0, state_std) fill, one slab per layer
             self.state = inputs.initial_state(layers * B, H, N_HEAD, seed=seed, std=state_std,
                                               device=dev).view(layers, B, H, N_HEAD, N_HEAD)
+        if state_dtype is not None and state_dtype != torch.float32:  # a 16-bit state cache
+            self.state = self.state.to(state_dtype)
+        self.state_elem = self.state.element_size()
         self.out_dtype = torch.bfloat16 if out_bf16 else torch.float32
         self.o = torch.empty(layers, B, H, N_HEAD, device=dev, dtype=self.out_dtype)
         self.tail = tail
@@ -338,11 +341,16 @@ class DecodeWorkload:
             graphs.append(g)
         return graphs
 
+    def head_step_bytes(self):
+        """Algorithmic bytes per head-step: the state read and written (in its own
+        type) plus the six input vectors and o."""
+        return STEP_BYTES - STATE_BYTES + 2 * self.state_elem * N_HEAD * N_HEAD
+
     def bytes_per_step(self):
-        return self.layers * self.B * self.H * STEP_BYTES
+        return self.layers * self.B * self.H * self.head_step_bytes()
 
     def state_bytes_per_step(self):
-        return self.layers * self.B * self.H * STATE_BYTES
+        return self.layers * self.B * self.H * 2 * self.state_elem * N_HEAD * N_HEAD
 
 
 def time_graphs(graphs, steps, warmup, stream, world, clocks=None):
@@ -945,9 +953,12 @@ def config_lines(args, dev, peaks, peak_kind, world, gpu_index, cpu_budget):
 
     # 2.9B decode at B = 1 and 8, from the state after 256 random tokens; 7.2B at B = 256
     # from a seeded N(0, 0.1) state
-    for cfg_id, cfg, B, std in ((1, inputs.DECODE_2P9B, 1, None), (1, inputs.DECODE_2P9B, 8, None),
-                                (3, inputs.DECODE_7P2B, inputs.DECODE_7P2B["B"], inputs.DECODE_7P2B["state_std"])):
-        wl = DecodeWorkload(cfg["layers"], B, cfg["H"], 4, dev, seed=1000 + cfg_id, state_std=std)
+    for cfg_id, cfg, B, std, sdt in ((1, inputs.DECODE_2P9B, 1, None, None), (1, inputs.DECODE_2P9B, 8, None, None),
+                                     (3, inputs.DECODE_7P2B, inputs.DECODE_7P2B["B"], inputs.DECODE_7P2B["state_std"], None),
+                                     (1, inputs.DECODE_2P9B, 32, None, torch.float16),
+                                     (3, inputs.DECODE_7P2B, inputs.DECODE_7P2B["B"], inputs.DECODE_7P2B["state_std"],
+                                      torch.float16)):
+        wl = DecodeWorkload(cfg["layers"], B, cfg["H"], 4, dev, seed=1000 + cfg_id, state_std=std, state_dtype=sdt)
         if std is None:
             wl.warm_fresh(cfg["warm_tokens"], seed=1000 + cfg_id)
         graphs = wl.capture(stream)
@@ -955,14 +966,17 @@ def config_lines(args, dev, peaks, peak_kind, world, gpu_index, cpu_budget):
         clk = Clocks(gpu_index)
         ms = max_over_ranks(time_graphs(graphs, steps, args.warmup, stream, world, clocks=clk), world, dev) / steps
         launch_us = ms * 1e3 / wl.layers
+        per_launch = B * wl.H * wl.head_step_bytes()
+        kern = "wkv7_step_kernel" if sdt is None else "wkv7_step_state16_kernel"
         obj = {"config": cfg_id, "workload": f"decode, {'2.9B' if cfg_id == 1 else '7.2B'} geometry: "
-                                             f"{wl.layers} layers x H={wl.H}, B={B}, CUDA-graph replay",
+                                             f"{wl.layers} layers x H={wl.H}, B={B}, "
+                                             f"{'fp32' if sdt is None else 'fp16'} state, CUDA-graph replay",
                "metric": "state-GB/s", "value": round(world * wl.state_bytes_per_step() / (ms * 1e-3) / 1e9, 2),
                "unit": "GB/s", "ms_per_step": round(ms, 5), "us_per_launch": round(launch_us, 3), "steps": steps,
-               "clocks": clk.result,
-               "roofline": roofline_obj(B * wl.H * STEP_BYTES, launch_us * 1e-3, peaks, peak_kind,
-                                        kernel="wkv7_step_kernel", algorithmic_bytes_per_launch=B * wl.H * STEP_BYTES)}
-        if want_cpu:
+               "bytes_per_head_step": wl.head_step_bytes(), "clocks": clk.result,
+               "roofline": roofline_obj(per_launch, launch_us * 1e-3, peaks, peak_kind, kernel=kern,
+                                        algorithmic_bytes_per_launch=per_launch)}
+        if want_cpu and sdt is None:
             obj["cpu_baseline"] = cpu_baseline_decode_cfg(B, wl.H, cpu_budget, state_std=std)
         out.append(obj)
         del graphs, wl

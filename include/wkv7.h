@@ -63,7 +63,8 @@ typedef enum {
 
 typedef enum {
     WKV7_F32 = 0,
-    WKV7_BF16 = 1
+    WKV7_BF16 = 1,
+    WKV7_F16 = 2   /* IEEE half precision; accepted only where a call says so */
 } wkv7_dtype;
 
 #define WKV7_HEAD_SIZE 64
@@ -86,6 +87,31 @@ WKV7_API wkv7_status wkv7_step(int B, int H, int N,
                       const float *r, const float *w, const float *k,
                       const float *v, const float *kk, const float *a,
                       float *state, float *o, cudaStream_t stream);
+
+/*
+ * wkv7_step_state -- wkv7_step with the state stored in state_dtype: WKV7_F32
+ * (exactly wkv7_step_cast), WKV7_F16 or WKV7_BF16.  A 16-bit state is widened
+ * to fp32 on load, the update and the read-out run in fp32 as in wkv7_step,
+ * and the new state is rounded to nearest even when it is stored back in
+ * place.  The Core AI model zoo note (section 5, "Parity gate + tokenizer")
+ * runs an fp16 export with fp16 state arrays; a 16-bit state halves the state
+ * traffic, which is 95% of a decode step's bytes.  Each step rounds the state
+ * once, so over many steps it drifts from an fp32-state run by about one
+ * 16-bit rounding per step (relative 2^-11 for fp16, 2^-8 for bf16), damped by
+ * the decay.
+ *
+ *   r, w, k, v, kk, a : fp32 [B, H, N]
+ *   state             : state_dtype [B, H, N, N], read and overwritten
+ *   o                 : o_dtype [B, H, N] (WKV7_F32 or WKV7_BF16)
+ *
+ * Same rules as wkv7_step (sizes, alignment, no overlap of state with any
+ * other argument) with the byte sizes of the chosen types.
+ */
+WKV7_API wkv7_status wkv7_step_state(int B, int H, int N,
+                      const float *r, const float *w, const float *k,
+                      const float *v, const float *kk, const float *a,
+                      void *state, wkv7_dtype state_dtype, void *o, wkv7_dtype o_dtype,
+                      cudaStream_t stream);
 
 /*
  * The time-mix tail after WKV, per row and head of N channels:
@@ -271,6 +297,24 @@ WKV7_API wkv7_status wkv7_prefill_cast(int num_seqs, int T_total, int H, int N,
                          const void *v, const void *kk, const void *a,
                          const float *initial_state, float *final_state, void *o,
                          wkv7_dtype o_dtype, void *workspace, size_t workspace_bytes,
+                         cudaStream_t stream);
+
+/*
+ * wkv7_prefill_state -- wkv7_prefill_cast with initial_state and final_state
+ * in state_dtype: WKV7_F32, WKV7_F16 or WKV7_BF16 (both the same type).  A
+ * 16-bit initial state is widened to fp32 exactly, the whole prefill runs with
+ * the fp32 state of wkv7_prefill, and the final state is rounded to nearest
+ * even once, when it is stored.  The counterpart of wkv7_step_state for the
+ * prompt that fills a 16-bit state cache; all other rules as wkv7_prefill_cast,
+ * with the byte sizes of the chosen state type.
+ */
+WKV7_API wkv7_status wkv7_prefill_state(int num_seqs, int T_total, int H, int N,
+                         const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                         wkv7_dtype x_dtype,
+                         const void *r, const float *w, const void *k,
+                         const void *v, const void *kk, const void *a,
+                         const void *initial_state, void *final_state, wkv7_dtype state_dtype,
+                         void *o, wkv7_dtype o_dtype, void *workspace, size_t workspace_bytes,
                          cudaStream_t stream);
 
 /*

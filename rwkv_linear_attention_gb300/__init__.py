@@ -61,21 +61,31 @@ def _out_code(dtype):
     raise TypeError("out_dtype must be torch.float32 or torch.bfloat16")
 
 
+_STATE_CODES = {torch.float32: _lib.F32, torch.float16: _lib.F16, torch.bfloat16: _lib.BF16}
+
+
 def step(r, w, k, v, kk, a, state, o=None, stream=None, out_dtype=torch.float32):
-    """One decode token: inputs fp32 [B, H, N]; ``state`` fp32 [B, H, N, N]
-    updated in place.  Returns ``o`` [B, H, N] in ``out_dtype`` (fp32, or bf16
-    rounded to nearest even; allocated if None)."""
+    """One decode token: inputs fp32 [B, H, N]; ``state`` [B, H, N, N] updated
+    in place, fp32 or a 16-bit type (fp16 / bf16: widened to fp32 for the
+    update, rounded to nearest even on store).  Returns ``o`` [B, H, N] in
+    ``out_dtype`` (fp32, or bf16 rounded to nearest even; allocated if None)."""
     B, H, N = r.shape
     code = _out_code(out_dtype)
     for name, t in (("r", r), ("w", w), ("k", k), ("v", v), ("kk", kk), ("a", a)):
         _need_cuda(name, t, torch.float32, (B, H, N))
-    _need_cuda("state", state, torch.float32, (B, H, N, N))
+    if state.dtype not in _STATE_CODES:
+        raise TypeError("state must be float32, float16 or bfloat16")
+    _need_cuda("state", state, state.dtype, (B, H, N, N))
     if o is None:
         o = torch.empty((B, H, N), device=r.device, dtype=out_dtype)
     _need_cuda("o", o, out_dtype, (B, H, N))
     lib = _lib.load()
-    st = lib.wkv7_step_cast(B, H, N, _ptr(r), _ptr(w), _ptr(k), _ptr(v), _ptr(kk), _ptr(a),
-                            _ptr(state), _ptr(o), code, _stream(stream))
+    if state.dtype == torch.float32:
+        st = lib.wkv7_step_cast(B, H, N, _ptr(r), _ptr(w), _ptr(k), _ptr(v), _ptr(kk), _ptr(a),
+                                _ptr(state), _ptr(o), code, _stream(stream))
+    else:
+        st = lib.wkv7_step_state(B, H, N, _ptr(r), _ptr(w), _ptr(k), _ptr(v), _ptr(kk), _ptr(a),
+                                 _ptr(state), _STATE_CODES[state.dtype], _ptr(o), code, _stream(stream))
     _lib.check(st, "wkv7_step")
     return o
 
@@ -174,7 +184,8 @@ def prefill_workspace_size(num_seqs: int, T_total: int, H: int, N: int = HEAD_SI
 
 
 def prefill(r, w, k, v, kk, a, cu_seqlens, initial_state=None, final_state=None, o=None,
-            workspace=None, cu_seqlens_host=None, want_final_state=True, stream=None, out_dtype=torch.float32):
+            workspace=None, cu_seqlens_host=None, want_final_state=True, stream=None, out_dtype=torch.float32,
+            state_dtype=None):
     """Packed varlen prefill.
 
     r, k, v, kk, a: [T_total, H, N] fp32 or bf16 (one dtype for all five);
@@ -187,7 +198,10 @@ def prefill(r, w, k, v, kk, a, cu_seqlens, initial_state=None, final_state=None,
     bytes enable every schedule, and a smaller one is accepted as long as it
     holds the sequence order (the tail split is then skipped); allocated when
     None.  ``out_dtype``: the type of ``o`` (fp32, or bf16 rounded to nearest
-    even).  Returns ``(o, final_state)``.
+    even).  ``state_dtype``: the type of both states (fp32, fp16 or bf16; by
+    default that of ``initial_state`` or ``final_state``, else fp32); a 16-bit
+    final state is rounded to nearest even once, when it is stored.  Returns
+    ``(o, final_state)``.
     """
     T_total, H, N = r.shape
     xdt = r.dtype
@@ -198,12 +212,17 @@ def prefill(r, w, k, v, kk, a, cu_seqlens, initial_state=None, final_state=None,
     _need_cuda("w", w, torch.float32, (T_total, H, N))
     _need_cuda("cu_seqlens", cu_seqlens, torch.int32)
     num_seqs = cu_seqlens.shape[0] - 1
+    if state_dtype is None:
+        state_dtype = (initial_state if initial_state is not None else
+                       final_state if final_state is not None else torch.zeros(0)).dtype
+    if state_dtype not in _STATE_CODES:
+        raise TypeError("states must be float32, float16 or bfloat16")
     if initial_state is not None:
-        _need_cuda("initial_state", initial_state, torch.float32, (num_seqs, H, N, N))
+        _need_cuda("initial_state", initial_state, state_dtype, (num_seqs, H, N, N))
     if final_state is None and want_final_state:
-        final_state = torch.empty((num_seqs, H, N, N), device=r.device, dtype=torch.float32)
+        final_state = torch.empty((num_seqs, H, N, N), device=r.device, dtype=state_dtype)
     if final_state is not None:
-        _need_cuda("final_state", final_state, torch.float32, (num_seqs, H, N, N))
+        _need_cuda("final_state", final_state, state_dtype, (num_seqs, H, N, N))
     code = _out_code(out_dtype)
     if o is None:
         o = torch.empty((T_total, H, N), device=r.device, dtype=out_dtype)
@@ -222,11 +241,11 @@ def prefill(r, w, k, v, kk, a, cu_seqlens, initial_state=None, final_state=None,
             workspace = torch.empty(need, device=r.device, dtype=torch.uint8)
         _need_cuda("workspace", workspace, torch.uint8)
         ws_bytes = workspace.numel()
-    st = lib.wkv7_prefill_cast(num_seqs, T_total, H, N, _ptr(cu_seqlens), host_ptr,
-                               _lib.BF16 if xdt == torch.bfloat16 else _lib.F32,
-                               _ptr(r), _ptr(w), _ptr(k), _ptr(v), _ptr(kk), _ptr(a),
-                               _ptr(initial_state), _ptr(final_state), _ptr(o), code,
-                               _ptr(workspace) if need > 0 else None, ws_bytes, _stream(stream))
+    st = lib.wkv7_prefill_state(num_seqs, T_total, H, N, _ptr(cu_seqlens), host_ptr,
+                                _lib.BF16 if xdt == torch.bfloat16 else _lib.F32,
+                                _ptr(r), _ptr(w), _ptr(k), _ptr(v), _ptr(kk), _ptr(a),
+                                _ptr(initial_state), _ptr(final_state), _STATE_CODES[state_dtype], _ptr(o), code,
+                                _ptr(workspace) if need > 0 else None, ws_bytes, _stream(stream))
     _lib.check(st, "wkv7_prefill")
     return o, final_state
 

@@ -24,10 +24,12 @@ ERR_DEVICE_BOUNDS = 7
 
 F32 = 0
 BF16 = 1
+F16 = 2
 
 EXPORTS = (
     "wkv7_step",
     "wkv7_step_cast",
+    "wkv7_step_state",
     "wkv7_step_tail",
     "wkv7_tmix_tail",
     "wkv7_verify",
@@ -35,6 +37,7 @@ EXPORTS = (
     "wkv7_prefill_workspace_size",
     "wkv7_prefill",
     "wkv7_prefill_cast",
+    "wkv7_prefill_state",
     "wkv7_prefill_padded",
     "wkv7_prefill_noalloc",
     "wkv7_prefill_backward_workspace_size",
@@ -62,10 +65,14 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.wkv7_step.argtypes = [I, I, I, P, P, P, P, P, P, P, P, P]
     lib.wkv7_step_cast.restype = I
     lib.wkv7_step_cast.argtypes = [I, I, I, P, P, P, P, P, P, P, P, I, P]
+    lib.wkv7_step_state.restype = I
+    lib.wkv7_step_state.argtypes = [I, I, I, P, P, P, P, P, P, P, I, P, I, P]
     lib.wkv7_prefill_padded.restype = I
     lib.wkv7_prefill_padded.argtypes = [I, I, I, I, P, P, I, P, P, P, P, P, P, P, P, P, I, P, S, P]
     lib.wkv7_prefill_cast.restype = I
     lib.wkv7_prefill_cast.argtypes = [I, I, I, I, P, P, I, P, P, P, P, P, P, P, P, P, I, P, S, P]
+    lib.wkv7_prefill_state.restype = I
+    lib.wkv7_prefill_state.argtypes = [I, I, I, I, P, P, I, P, P, P, P, P, P, P, P, I, P, I, P, S, P]
     F = ctypes.c_float
     lib.wkv7_step_tail.restype = I
     lib.wkv7_step_tail.argtypes = [I, I, I, P, P, P, P, P, P, P, P, P, P, P, P, F, P, P]

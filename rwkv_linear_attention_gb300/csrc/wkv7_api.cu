@@ -120,6 +120,36 @@ wkv7_status wkv7_step_cast(int B, int H, int N, const float *r, const float *w, 
     return e == cudaSuccess ? WKV7_OK : cuda_fail(e);
 }
 
+wkv7_status wkv7_step_state(int B, int H, int N, const float *r, const float *w, const float *k, const float *v,
+                            const float *kk, const float *a, void *state, wkv7_dtype state_dtype, void *o,
+                            wkv7_dtype o_dtype, cudaStream_t stream) {
+    if (state_dtype == WKV7_F32)
+        return wkv7_step_cast(B, H, N, r, w, k, v, kk, a, static_cast<float *>(state), o, o_dtype, stream);
+    if (N != wkv7::kN) return WKV7_ERR_UNSUPPORTED;
+    if (state_dtype != WKV7_F16 && state_dtype != WKV7_BF16) return WKV7_ERR_UNSUPPORTED;
+    if (o_dtype != WKV7_F32 && o_dtype != WKV7_BF16) return WKV7_ERR_UNSUPPORTED;
+    if (B < 0 || H <= 0) return WKV7_ERR_INVALID_ARG;
+    const long long heads = (long long)B * H;
+    if (heads > kMaxHeads) return WKV7_ERR_INVALID_ARG;
+    if (heads == 0) return WKV7_OK;
+    const void *ptrs[8] = {r, w, k, v, kk, a, state, o};
+    for (const void *p : ptrs)
+        if (!p) return WKV7_ERR_INVALID_ARG;
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return WKV7_ERR_ALIGNMENT;
+    const size_t vec_bytes = (size_t)heads * N * sizeof(float);
+    const size_t o_bytes = (size_t)heads * N * (o_dtype == WKV7_BF16 ? 2 : 4);
+    const size_t state_bytes = (size_t)heads * N * N * 2;
+    const void *ins[6] = {r, w, k, v, kk, a};
+    for (const void *p : ins)
+        if (overlaps(state, state_bytes, p, vec_bytes)) return WKV7_ERR_INVALID_ARG;
+    if (overlaps(state, state_bytes, o, o_bytes)) return WKV7_ERR_INVALID_ARG;
+    for (int i = 0; i < 6; ++i)
+        if (overlaps(o, o_bytes, ins[i], vec_bytes)) return WKV7_ERR_INVALID_ARG;
+    cudaError_t e = wkv7::launch_step_state16(heads, r, w, k, v, kk, a, state, state_dtype, o, o_dtype, stream);
+    return e == cudaSuccess ? WKV7_OK : cuda_fail(e);
+}
+
 wkv7_status wkv7_step(int B, int H, int N, const float *r, const float *w, const float *k,
                       const float *v, const float *kk, const float *a, float *state, float *o,
                       cudaStream_t stream) {
@@ -248,15 +278,16 @@ size_t wkv7_prefill_workspace_size(int num_seqs, int T_total, int H, int N) {
     return wkv7::prefill_workspace_bytes(num_seqs, T_total, H);
 }
 
-wkv7_status wkv7_prefill_cast(int num_seqs, int T_total, int H, int N, const int32_t *cu_seqlens,
-                              const int32_t *cu_seqlens_host, wkv7_dtype x_dtype, const void *r,
-                              const float *w, const void *k, const void *v, const void *kk,
-                              const void *a, const float *initial_state, float *final_state,
-                              void *o, wkv7_dtype o_dtype, void *workspace, size_t workspace_bytes,
-                              cudaStream_t stream) {
+wkv7_status wkv7_prefill_state(int num_seqs, int T_total, int H, int N, const int32_t *cu_seqlens,
+                               const int32_t *cu_seqlens_host, wkv7_dtype x_dtype, const void *r,
+                               const float *w, const void *k, const void *v, const void *kk,
+                               const void *a, const void *initial_state, void *final_state,
+                               wkv7_dtype state_dtype, void *o, wkv7_dtype o_dtype, void *workspace,
+                               size_t workspace_bytes, cudaStream_t stream) {
     if (N != wkv7::kN) return WKV7_ERR_UNSUPPORTED;
     if (x_dtype != WKV7_F32 && x_dtype != WKV7_BF16) return WKV7_ERR_UNSUPPORTED;
     if (o_dtype != WKV7_F32 && o_dtype != WKV7_BF16) return WKV7_ERR_UNSUPPORTED;
+    if (state_dtype != WKV7_F32 && state_dtype != WKV7_F16 && state_dtype != WKV7_BF16) return WKV7_ERR_UNSUPPORTED;
     if (num_seqs < 0 || T_total < 0 || H <= 0) return WKV7_ERR_INVALID_ARG;
     if ((long long)num_seqs * H > kMaxHeads || (long long)T_total * H * N >= (1ll << 62))
         return WKV7_ERR_INVALID_ARG;
@@ -277,7 +308,7 @@ wkv7_status wkv7_prefill_cast(int num_seqs, int T_total, int H, int N, const int
 
     const size_t x_elem = x_dtype == WKV7_BF16 ? 2 : 4;
     const size_t tok_elems = (size_t)T_total * H * N;
-    const size_t state_bytes = (size_t)num_seqs * H * N * N * sizeof(float);
+    const size_t state_bytes = (size_t)num_seqs * H * N * N * wkv7::state_elem_bytes(state_dtype);
     const size_t o_bytes = tok_elems * (o_dtype == WKV7_BF16 ? 2 : 4);
     // Outputs must not overlap inputs; final_state may equal initial_state
     // exactly but must not partially overlap it.
@@ -331,6 +362,7 @@ wkv7_status wkv7_prefill_cast(int num_seqs, int T_total, int H, int N, const int
     args.final_state = final_state;
     args.o = o;
     args.o_dtype = o_dtype;
+    args.state_dtype = state_dtype;
     args.status = status;
     cudaError_t e = cudaSuccess;
     if (need > 0 && wkv7::prefill_wants_order(args)) {
@@ -341,6 +373,16 @@ wkv7_status wkv7_prefill_cast(int num_seqs, int T_total, int H, int N, const int
     }
     e = wkv7::launch_prefill(args, workspace, workspace_bytes, stream);
     return e == cudaSuccess ? WKV7_OK : cuda_fail(e);
+}
+
+wkv7_status wkv7_prefill_cast(int num_seqs, int T_total, int H, int N, const int32_t *cu_seqlens,
+                              const int32_t *cu_seqlens_host, wkv7_dtype x_dtype, const void *r,
+                              const float *w, const void *k, const void *v, const void *kk,
+                              const void *a, const float *initial_state, float *final_state,
+                              void *o, wkv7_dtype o_dtype, void *workspace, size_t workspace_bytes,
+                              cudaStream_t stream) {
+    return wkv7_prefill_state(num_seqs, T_total, H, N, cu_seqlens, cu_seqlens_host, x_dtype, r, w, k, v, kk, a,
+                              initial_state, final_state, WKV7_F32, o, o_dtype, workspace, workspace_bytes, stream);
 }
 
 wkv7_status wkv7_prefill_padded(int B, int T_max, int H, int N, const int32_t *lens, const int32_t *lens_host,
@@ -413,6 +455,7 @@ wkv7_status wkv7_prefill_padded(int B, int T_max, int H, int N, const int32_t *l
     args.final_state = final_state;
     args.o = o;
     args.o_dtype = o_dtype;
+    args.state_dtype = WKV7_F32;
     args.status = status;
     cudaError_t e = cudaSuccess;
     if (need > 0 && wkv7::prefill_wants_order(args)) {

@@ -2,6 +2,8 @@
 // units.  Not part of the C ABI (that is include/wkv7.h).
 #pragma once
 
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
@@ -51,6 +53,12 @@ cudaError_t launch_step(long long n_heads, const float *r, const float *w, const
                         void *o, wkv7_dtype o_dtype, const TailArgs *tail, unsigned *status,
                         cudaStream_t stream);
 
+// Decode with the state stored in 16 bits (state_dtype WKV7_F16 or WKV7_BF16): widened
+// to fp32 on load, rounded to nearest even on store; o of o_dtype (fp32 or bf16).
+cudaError_t launch_step_state16(long long n_heads, const float *r, const float *w, const float *k, const float *v,
+                                const float *kk, const float *a, void *state, wkv7_dtype state_dtype, void *o,
+                                wkv7_dtype o_dtype, cudaStream_t stream);
+
 // Multi-token verify (speculative decoding): T tokens per row from a read-only state,
 // every position's state kept; and the rollback to each row's accepted length.
 int verify_max_tokens();
@@ -81,12 +89,44 @@ struct PrefillArgs {
     const void *v;
     const void *kk;
     const void *a;
-    const float *initial_state;  // nullable
-    float *final_state;          // nullable
+    const void *initial_state;   // nullable, [num_seqs, H, 64, 64] of state_dtype
+    void *final_state;           // nullable, same type
     void *o;                     // [T_total, H, 64] of o_dtype
     wkv7_dtype o_dtype;          // WKV7_F32, or WKV7_BF16 (rounded to nearest even)
+    wkv7_dtype state_dtype;      // WKV7_F32, WKV7_F16 or WKV7_BF16 (16-bit: rounded to nearest even)
     unsigned *status;            // device status word
 };
+
+// Four consecutive state elements at element index idx of a state array of type dt,
+// widened to fp32; and the rounded store (to nearest even for the 16-bit types).
+__device__ __forceinline__ float4 load_state4(const void *base, wkv7_dtype dt, long long idx) {
+    if (dt == WKV7_F32) return *reinterpret_cast<const float4 *>(static_cast<const float *>(base) + idx);
+    const uint2 u = *reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(base) + idx);
+    if (dt == WKV7_BF16)
+        return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u), __uint_as_float(u.y << 16),
+                           __uint_as_float(u.y & 0xffff0000u));
+    const float2 lo = __half22float2(*reinterpret_cast<const __half2 *>(&u.x));
+    const float2 hi = __half22float2(*reinterpret_cast<const __half2 *>(&u.y));
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+__device__ __forceinline__ void store_state4(void *base, wkv7_dtype dt, long long idx, float4 v) {
+    if (dt == WKV7_F32) {
+        *reinterpret_cast<float4 *>(static_cast<float *>(base) + idx) = v;
+        return;
+    }
+    uint2 u;
+    if (dt == WKV7_BF16) {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+        u.x = *reinterpret_cast<const uint32_t *>(&lo);
+        u.y = *reinterpret_cast<const uint32_t *>(&hi);
+    } else {
+        const __half2 lo = __floats2half2_rn(v.x, v.y), hi = __floats2half2_rn(v.z, v.w);
+        u.x = *reinterpret_cast<const uint32_t *>(&lo);
+        u.y = *reinterpret_cast<const uint32_t *>(&hi);
+    }
+    *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(base) + idx) = u;
+}
+inline size_t state_elem_bytes(wkv7_dtype dt) { return dt == WKV7_F32 ? 4 : 2; }
 
 // Token range [bos, eos) of sequence b: packed (cu_seqlens) or padded (lens, row_stride).
 __device__ __forceinline__ void seq_bounds(const PrefillArgs &p, int b, int &bos, int &eos) {

@@ -313,10 +313,9 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
 #pragma unroll
             for (int j = 0; j < 16; ++j) s[j] = (16 * cg + j == si) ? 1.f : 0.f;
         } else if (kind == kItemWhole && p.initial_state) {
-            const float4 *src = reinterpret_cast<const float4 *>(p.initial_state + sslot + si * 64 + 16 * cg);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const float4 x = src[j];
+                const float4 x = load_state4(p.initial_state, p.state_dtype, sslot + si * 64 + 16 * cg + 4 * j);
                 s[4 * j] = x.x; s[4 * j + 1] = x.y; s[4 * j + 2] = x.z; s[4 * j + 3] = x.w;
             }
         } else {
@@ -326,9 +325,10 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
     }
     if (nchunks == 0) {
         if (state_thread && p.final_state) {
-            float4 *dst = reinterpret_cast<float4 *>(p.final_state + sslot + si * 64 + 16 * cg);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) dst[j] = make_float4(s[4 * j], s[4 * j + 1], s[4 * j + 2], s[4 * j + 3]);
+            for (int j = 0; j < 4; ++j)
+                store_state4(p.final_state, p.state_dtype, sslot + si * 64 + 16 * cg + 4 * j,
+                             make_float4(s[4 * j], s[4 * j + 1], s[4 * j + 2], s[4 * j + 3]));
         }
         return;
     }
@@ -900,11 +900,14 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
         }
     }
 
-    float *fdst = slot >= 0 ? plan.slots + static_cast<long long>(slot) * 4096 : p.final_state ? p.final_state + sslot : nullptr;
-    if (alive && state_thread && fdst) {
-        float4 *dst = reinterpret_cast<float4 *>(fdst + si * 64 + 16 * cg);
+    // the final state: into a tail-split slot (fp32) or the caller's final_state (state_dtype)
+    if (alive && state_thread && (slot >= 0 || p.final_state)) {
+        void *fdst = slot >= 0 ? static_cast<void *>(plan.slots + static_cast<long long>(slot) * 4096) : p.final_state;
+        const wkv7_dtype fdt = slot >= 0 ? WKV7_F32 : p.state_dtype;
+        const long long fbase = (slot >= 0 ? 0 : sslot) + si * 64 + 16 * cg;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) dst[j] = make_float4(s[4 * j], s[4 * j + 1], s[4 * j + 2], s[4 * j + 3]);
+        for (int j = 0; j < 4; ++j)
+            store_state4(fdst, fdt, fbase + 4 * j, make_float4(s[4 * j], s[4 * j + 1], s[4 * j + 2], s[4 * j + 3]));
     }
     }  // workers
     tc_fence_before_sync();
@@ -993,7 +996,7 @@ __device__ __forceinline__ void load_t64(float *dst, const float *src) {
 // S_in(j+1) = P(j) S_in(j) + S_part(j), written over S_part(j)'s slot; the
 // last one is the pair's final state.
 __global__ void __launch_bounds__(kFixThreads)
-wkv7_prefill_split_chain_kernel(const __grid_constant__ FixPlan fp, float *final_state, int H) {
+wkv7_prefill_split_chain_kernel(const __grid_constant__ FixPlan fp, void *final_state, wkv7_dtype state_dtype, int H) {
     __shared__ __align__(16) float sin_[64 * 64];
     __shared__ __align__(16) float pt[64 * kLdT];  // P(j) transposed
     const FixPair &pr = fp.pair[blockIdx.x];
@@ -1021,8 +1024,9 @@ wkv7_prefill_split_chain_kernel(const __grid_constant__ FixPlan fp, float *final
     }
     __syncthreads();
     if (final_state) {
-        float4 *dst = reinterpret_cast<float4 *>(final_state + (static_cast<long long>(pr.b) * H + pr.h) * 4096);
-        for (int e = tid; e < 1024; e += kFixThreads) dst[e] = reinterpret_cast<const float4 *>(sin_)[e];
+        const long long base = (static_cast<long long>(pr.b) * H + pr.h) * 4096;
+        for (int e = tid; e < 1024; e += kFixThreads)
+            store_state4(final_state, state_dtype, base + 4 * e, reinterpret_cast<const float4 *>(sin_)[e]);
     }
 }
 
@@ -1300,7 +1304,8 @@ cudaError_t launch_chunked(const PrefillArgs &args, unsigned char *split_ws, siz
         args, maps, plan);
     e = cudaGetLastError();
     if (e != cudaSuccess || !split) return e;
-    wkv7_prefill_split_chain_kernel<<<fix.n_pairs, kFixThreads, 0, stream>>>(fix, args.final_state, args.H);
+    wkv7_prefill_split_chain_kernel<<<fix.n_pairs, kFixThreads, 0, stream>>>(fix, args.final_state, args.state_dtype,
+                                                                              args.H);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     wkv7_prefill_split_ofix_kernel<<<dim3(fix.n_blocks, fix.n_pairs), kFixThreads, 0, stream>>>(fix, args);
@@ -1344,7 +1349,7 @@ cudaError_t launch_prefill_order(const PrefillArgs &args, int32_t *order, cudaSt
 cudaError_t launch_prefill(const PrefillArgs &args, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
     const long long pairs = static_cast<long long>(args.num_seqs) * args.H;
     if (pairs <= 0) return cudaSuccess;
-    const size_t state_bytes = static_cast<size_t>(pairs) * 4096 * sizeof(float);
+    const size_t state_bytes = static_cast<size_t>(pairs) * 4096 * state_elem_bytes(args.state_dtype);
     if (args.T_total == 0) {  // every sequence is empty: final = initial (or zeros)
         if (!args.final_state) return cudaSuccess;
         if (!args.initial_state) return cudaMemsetAsync(args.final_state, 0, state_bytes, stream);

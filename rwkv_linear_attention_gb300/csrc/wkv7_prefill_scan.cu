@@ -105,8 +105,7 @@ wkv7_prefill_scan_kernel(PrefillArgs p) {
     float4 s[8];
     if (p.initial_state) {
 #pragma unroll
-        for (int m = 0; m < 8; ++m)
-            s[m] = *reinterpret_cast<const float4 *>(p.initial_state + slot + m * kN);
+        for (int m = 0; m < 8; ++m) s[m] = load_state4(p.initial_state, p.state_dtype, slot + m * kN);
     } else {
 #pragma unroll
         for (int m = 0; m < 8; ++m) s[m] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -186,8 +185,7 @@ wkv7_prefill_scan_kernel(PrefillArgs p) {
 
     if (p.final_state) {
 #pragma unroll
-        for (int m = 0; m < 8; ++m)
-            *reinterpret_cast<float4 *>(p.final_state + slot + m * kN) = s[m];
+        for (int m = 0; m < 8; ++m) store_state4(p.final_state, p.state_dtype, slot + m * kN, s[m]);
     }
 }
 

@@ -34,6 +34,7 @@
 // back-to-back calls on the same state stay ordered, while the launch and
 // block scheduling of the next call overlap the tail of this one.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "sm103_ptx.cuh"
@@ -401,6 +402,133 @@ wkv7_step_regs_kernel(long long n_units, const float *__restrict__ r, const floa
     }
 }
 
+// ---------------------------------------------------------------- 16-bit state
+//
+// The same step with the state stored in fp16 or bf16: each element is widened
+// to fp32 on load, the whole update and read-out run in fp32, and the new state
+// is rounded to nearest even on store.  The Core AI model zoo note (section 5,
+// "Parity gate + tokenizer") runs an fp16 export with fp16 state arrays; the
+// state traffic, 95% of a decode step's bytes, halves.
+//
+// Register-resident, two warps per head: warp `half` owns value columns
+// 32*half .. +31; lane L holds key rows 8*(L>>2) .. +7 and columns 8*(L&3) .. +7
+// of that slice, so every state access is one 16-byte load or store per row.
+// The reductions over key rows are a per-lane sum over eight rows and three
+// xor-shuffles, as in the fp32 forms.
+constexpr int kHalfWarps = 4;  // two heads per block
+
+__device__ __forceinline__ void unpack8(const uint4 &u, float (&f)[8], const __half *) {
+    const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float2 p = __half22float2(*reinterpret_cast<const __half2 *>(&wv[j]));
+        f[2 * j] = p.x;
+        f[2 * j + 1] = p.y;
+    }
+}
+__device__ __forceinline__ void unpack8(const uint4 &u, float (&f)[8], const __nv_bfloat16 *) {
+    const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        f[2 * j] = __uint_as_float(wv[j] << 16);
+        f[2 * j + 1] = __uint_as_float(wv[j] & 0xffff0000u);
+    }
+}
+__device__ __forceinline__ uint4 pack8(const float (&f)[8], const __half *) {
+    uint32_t wv[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const __half2 h = __floats2half2_rn(f[2 * j], f[2 * j + 1]);
+        wv[j] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    return make_uint4(wv[0], wv[1], wv[2], wv[3]);
+}
+__device__ __forceinline__ uint4 pack8(const float (&f)[8], const __nv_bfloat16 *) {
+    uint32_t wv[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * j], f[2 * j + 1]);
+        wv[j] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    return make_uint4(wv[0], wv[1], wv[2], wv[3]);
+}
+
+template <typename ST, typename OutT>
+__global__ void __launch_bounds__(kHalfWarps * 32)
+wkv7_step_state16_kernel(long long n_heads, const float *__restrict__ r, const float *__restrict__ w,
+                         const float *__restrict__ k, const float *__restrict__ v,
+                         const float *__restrict__ kk, const float *__restrict__ a,
+                         ST *__restrict__ state, OutT *__restrict__ o) {
+    grid_dep_wait();
+    const int lane = threadIdx.x & 31;
+    const long long unit = static_cast<long long>(blockIdx.x) * kHalfWarps + (threadIdx.x >> 5);
+    if (unit >= 2 * n_heads) return;
+    const long long head = unit >> 1;
+    const int half = static_cast<int>(unit & 1);
+    const int rg = lane >> 2, row0 = rg * 8;
+    const int col = half * 32 + (lane & 3) * 8;
+    ST *S = state + head * (kN * kN) + static_cast<long long>(row0) * kN + col;
+    uint4 raw[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) raw[m] = *reinterpret_cast<const uint4 *>(S + m * kN);
+    grid_dep_launch();
+    const long long vb = head * kN + row0;
+    const float4 r0 = __ldg(reinterpret_cast<const float4 *>(r + vb)), r1 = __ldg(reinterpret_cast<const float4 *>(r + vb + 4));
+    const float4 w0 = __ldg(reinterpret_cast<const float4 *>(w + vb)), w1 = __ldg(reinterpret_cast<const float4 *>(w + vb + 4));
+    const float4 k0 = __ldg(reinterpret_cast<const float4 *>(k + vb)), k1 = __ldg(reinterpret_cast<const float4 *>(k + vb + 4));
+    const float4 kk0 = __ldg(reinterpret_cast<const float4 *>(kk + vb)), kk1 = __ldg(reinterpret_cast<const float4 *>(kk + vb + 4));
+    const float4 a0 = __ldg(reinterpret_cast<const float4 *>(a + vb)), a1 = __ldg(reinterpret_cast<const float4 *>(a + vb + 4));
+    const float4 v0 = __ldg(reinterpret_cast<const float4 *>(v + head * kN + col));
+    const float4 v1 = __ldg(reinterpret_cast<const float4 *>(v + head * kN + col + 4));
+    const float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    float kkr[8], kr[8], rr[8], dr[8], cr[8];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        kkr[m] = comp(kk0, m); kkr[m + 4] = comp(kk1, m);
+        kr[m] = comp(k0, m);   kr[m + 4] = comp(k1, m);
+        rr[m] = comp(r0, m);   rr[m + 4] = comp(r1, m);
+        dr[m] = expf(comp(w0, m)); dr[m + 4] = expf(comp(w1, m));
+        cr[m] = comp(kk0, m) * comp(a0, m); cr[m + 4] = comp(kk1, m) * comp(a1, m);
+    }
+    float z[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) z[c] = 0.f;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        float x[8];
+        unpack8(raw[m], x, static_cast<const ST *>(nullptr));
+#pragma unroll
+        for (int c = 0; c < 8; ++c) z[c] = fmaf(kkr[m], x[c], z[c]);
+    }
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) z[c] += __shfl_xor_sync(0xffffffffu, z[c], off);
+    float oc[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) oc[c] = 0.f;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        float x[8];
+        unpack8(raw[m], x, static_cast<const ST *>(nullptr));
+        const float d = dr[m], cm = cr[m], kv = kr[m];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            x[c] = fmaf(d, x[c], fmaf(-cm, z[c], kv * vv[c]));
+            oc[c] = fmaf(rr[m], x[c], oc[c]);
+        }
+        *reinterpret_cast<uint4 *>(S + m * kN) = pack8(x, static_cast<const ST *>(nullptr));
+    }
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) oc[c] += __shfl_xor_sync(0xffffffffu, oc[c], off);
+    if (rg == 0) {
+        store_o4(o, head * kN + col, oc[0], oc[1], oc[2], oc[3]);
+        store_o4(o, head * kN + col + 4, oc[4], oc[5], oc[6], oc[7]);
+    }
+}
+
 // Head count from which the register form is used (several full waves).
 constexpr long long kRegsFromHeads = 8192;
 
@@ -444,6 +572,29 @@ LaunchShape shape_for_device() {
 }
 
 }  // namespace
+
+cudaError_t launch_step_state16(long long n_heads, const float *r, const float *w, const float *k, const float *v,
+                                const float *kk, const float *a, void *state, wkv7_dtype state_dtype, void *o,
+                                wkv7_dtype o_dtype, cudaStream_t stream) {
+    if (n_heads <= 0) return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const long long units = 2 * n_heads;
+    cfg.gridDim = dim3(static_cast<unsigned>((units + kHalfWarps - 1) / kHalfWarps));
+    cfg.blockDim = dim3(kHalfWarps * 32);
+    const bool ob = o_dtype == WKV7_BF16;
+    if (state_dtype == WKV7_F16) {
+        if (ob) return cudaLaunchKernelEx(&cfg, wkv7_step_state16_kernel<__half, __nv_bfloat16>, n_heads, r, w, k, v, kk, a, static_cast<__half *>(state), static_cast<__nv_bfloat16 *>(o));
+        return cudaLaunchKernelEx(&cfg, wkv7_step_state16_kernel<__half, float>, n_heads, r, w, k, v, kk, a, static_cast<__half *>(state), static_cast<float *>(o));
+    }
+    if (ob) return cudaLaunchKernelEx(&cfg, wkv7_step_state16_kernel<__nv_bfloat16, __nv_bfloat16>, n_heads, r, w, k, v, kk, a, static_cast<__nv_bfloat16 *>(state), static_cast<__nv_bfloat16 *>(o));
+    return cudaLaunchKernelEx(&cfg, wkv7_step_state16_kernel<__nv_bfloat16, float>, n_heads, r, w, k, v, kk, a, static_cast<__nv_bfloat16 *>(state), static_cast<float *>(o));
+}
 
 cudaError_t launch_step(long long n_heads, const float *r, const float *w, const float *k,
                         const float *v, const float *kk, const float *a, float *state,
