@@ -146,7 +146,10 @@ wkv7_status wkv7_step_state(int B, int H, int N, const float *r, const float *w,
     if (overlaps(state, state_bytes, o, o_bytes)) return WKV7_ERR_INVALID_ARG;
     for (int i = 0; i < 6; ++i)
         if (overlaps(o, o_bytes, ins[i], vec_bytes)) return WKV7_ERR_INVALID_ARG;
-    cudaError_t e = wkv7::launch_step_state16(heads, r, w, k, v, kk, a, state, state_dtype, o, o_dtype, stream);
+    unsigned *status = nullptr;
+    wkv7_status st = status_word(&status);
+    if (st != WKV7_OK) return st;
+    cudaError_t e = wkv7::launch_step_state16(heads, r, w, k, v, kk, a, state, state_dtype, o, o_dtype, status, stream);
     return e == cudaSuccess ? WKV7_OK : cuda_fail(e);
 }
 

@@ -57,7 +57,7 @@ cudaError_t launch_step(long long n_heads, const float *r, const float *w, const
 // to fp32 on load, rounded to nearest even on store; o of o_dtype (fp32 or bf16).
 cudaError_t launch_step_state16(long long n_heads, const float *r, const float *w, const float *k, const float *v,
                                 const float *kk, const float *a, void *state, wkv7_dtype state_dtype, void *o,
-                                wkv7_dtype o_dtype, cudaStream_t stream);
+                                wkv7_dtype o_dtype, unsigned *status, cudaStream_t stream);
 
 // Multi-token verify (speculative decoding): T tokens per row from a read-only state,
 // every position's state kept; and the rollback to each row's accepted length.

@@ -53,16 +53,42 @@ constexpr uint32_t kMaxPolls = 1u << 24;
 
 // One ring stage: a head's state and its vectors r, w, k, v, kk, a; with the fused
 // time-mix tail also its gate g and the head's r_k, ln_w, ln_b.
-template <bool kTail>
+template <bool kTail, typename ST = float>
 struct Stage {
     static constexpr int kVecs = kTail ? 10 : 6;
-    float S[kN * kN];
+    ST S[kN * kN];
     float vec[kVecs][kN];
 };
-static_assert(sizeof(Stage<false>) % 128 == 0 && sizeof(Stage<true>) % 128 == 0, "stage size");
-template <bool kTail>
-constexpr size_t kSmemBytesT = kStages * sizeof(Stage<kTail>) + kStages * sizeof(unsigned long long);
+static_assert(sizeof(Stage<false>) % 128 == 0 && sizeof(Stage<true>) % 128 == 0 &&
+                  sizeof(Stage<false, __half>) % 128 == 0, "stage size");
+template <bool kTail, typename ST = float>
+constexpr size_t kSmemBytesT = kStages * sizeof(Stage<kTail, ST>) + kStages * sizeof(unsigned long long);
 constexpr size_t kSmemBytes = kSmemBytesT<false>;
+constexpr size_t kSmemBytes16 = kSmemBytesT<false, __half>;
+
+// Four state elements (columns col .. col+3 of one row) of a ring stage, widened to
+// fp32; and the store back, rounded to nearest even for the 16-bit types.
+__device__ __forceinline__ float4 ld_state4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ float4 ld_state4(const __half *p) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(p);
+    const float2 lo = __half22float2(*reinterpret_cast<const __half2 *>(&u.x));
+    const float2 hi = __half22float2(*reinterpret_cast<const __half2 *>(&u.y));
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+__device__ __forceinline__ float4 ld_state4(const __nv_bfloat16 *p) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(p);
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u), __uint_as_float(u.y << 16),
+                       __uint_as_float(u.y & 0xffff0000u));
+}
+__device__ __forceinline__ void st_state4(float *p, const float4 &x) { *reinterpret_cast<float4 *>(p) = x; }
+__device__ __forceinline__ void st_state4(__half *p, const float4 &x) {
+    const __half2 lo = __floats2half2_rn(x.x, x.y), hi = __floats2half2_rn(x.z, x.w);
+    *reinterpret_cast<uint2 *>(p) = make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
+}
+__device__ __forceinline__ void st_state4(__nv_bfloat16 *p, const float4 &x) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y), hi = __floats2bfloat162_rn(x.z, x.w);
+    *reinterpret_cast<uint2 *>(p) = make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
+}
 
 __device__ __forceinline__ float comp(const float4 &x, int c) {
     return c == 0 ? x.x : c == 1 ? x.y : c == 2 ? x.z : x.w;
@@ -132,15 +158,16 @@ __device__ __forceinline__ float4 tail_apply(const float *red, float eps, float 
                        (fmaf(d3 * rstd, w4.w, b4.w) + bonus * vv.w) * g4.w);
 }
 
-template <bool kTail, typename OutT>
+template <bool kTail, typename OutT, typename ST = float>
 __global__ void __launch_bounds__(kThreads)
 wkv7_step_kernel(long long n_heads, const float *__restrict__ r, const float *__restrict__ w,
                  const float *__restrict__ k, const float *__restrict__ v,
                  const float *__restrict__ kk, const float *__restrict__ a,
-                 float *__restrict__ state, OutT *__restrict__ o, TailArgs tail, unsigned *status) {
+                 ST *__restrict__ state, OutT *__restrict__ o, TailArgs tail, unsigned *status) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float red[2][8];  // the tail's statistics, double-buffered across heads
-    using StageX = Stage<kTail>;
+    using StageX = Stage<kTail, ST>;
+    constexpr uint32_t kStBytes = kN * kN * sizeof(ST);
     StageX *st = reinterpret_cast<StageX *>(smem);
     unsigned long long *full = reinterpret_cast<unsigned long long *>(smem + kStages * sizeof(StageX));
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -155,8 +182,8 @@ wkv7_step_kernel(long long n_heads, const float *__restrict__ r, const float *__
         const long long head = first + idx * stride;
         const int s = static_cast<int>(idx % kStages);
         const uint32_t bar = smem_addr(&full[s]);
-        mbar_arrive_expect_tx(bar, kStateBytes + StageX::kVecs * kVecBytes);
-        bulk_load(smem_addr(st[s].S), state + head * (kN * kN), kStateBytes, bar);
+        mbar_arrive_expect_tx(bar, kStBytes + StageX::kVecs * kVecBytes);
+        bulk_load(smem_addr(st[s].S), state + head * (kN * kN), kStBytes, bar);
 #pragma unroll
         for (int i = 0; i < 6; ++i) bulk_load(smem_addr(st[s].vec[i]), vsrc[i] + head * kN, kVecBytes, bar);
         if constexpr (kTail) {
@@ -194,7 +221,7 @@ wkv7_step_kernel(long long n_heads, const float *__restrict__ r, const float *__
 
         float4 x[8];
 #pragma unroll
-        for (int m = 0; m < 8; ++m) x[m] = *reinterpret_cast<const float4 *>(&S.S[(row0 + m) * kN + col]);
+        for (int m = 0; m < 8; ++m) x[m] = ld_state4(&S.S[(row0 + m) * kN + col]);
         const float4 r0 = *reinterpret_cast<const float4 *>(&S.vec[0][row0]);
         const float4 r1 = *reinterpret_cast<const float4 *>(&S.vec[0][row0 + 4]);
         const float4 w0 = *reinterpret_cast<const float4 *>(&S.vec[1][row0]);
@@ -245,7 +272,7 @@ wkv7_step_kernel(long long n_heads, const float *__restrict__ r, const float *__
             o1 = fmaf(rr[m], x[m].y, o1);
             o2 = fmaf(rr[m], x[m].z, o2);
             o3 = fmaf(rr[m], x[m].w, o3);
-            *reinterpret_cast<float4 *>(&S.S[(row0 + m) * kN + col]) = x[m];
+            st_state4(&S.S[(row0 + m) * kN + col], x[m]);
         }
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
@@ -277,7 +304,7 @@ wkv7_step_kernel(long long n_heads, const float *__restrict__ r, const float *__
             if (rg == 0) *reinterpret_cast<float4 *>(tail.y + head * kN + col) = y;
         }
         if (tid == 0) {
-            bulk_store(state + head * (kN * kN), smem_addr(S.S), kStateBytes);
+            bulk_store(state + head * (kN * kN), smem_addr(S.S), kStBytes);
             bulk_commit();
             // refill the previous stage once its store has read it
             if (idx >= 1 && issued < count) {
@@ -404,130 +431,16 @@ wkv7_step_regs_kernel(long long n_units, const float *__restrict__ r, const floa
 
 // ---------------------------------------------------------------- 16-bit state
 //
-// The same step with the state stored in fp16 or bf16: each element is widened
-// to fp32 on load, the whole update and read-out run in fp32, and the new state
-// is rounded to nearest even on store.  The Core AI model zoo note (section 5,
-// "Parity gate + tokenizer") runs an fp16 export with fp16 state arrays; the
-// state traffic, 95% of a decode step's bytes, halves.
-//
-// Register-resident, two warps per head: warp `half` owns value columns
-// 32*half .. +31; lane L holds key rows 8*(L>>2) .. +7 and columns 8*(L&3) .. +7
-// of that slice, so every state access is one 16-byte load or store per row.
-// The reductions over key rows are a per-lane sum over eight rows and three
-// xor-shuffles, as in the fp32 forms.
-constexpr int kHalfWarps = 4;  // two heads per block
-
-__device__ __forceinline__ void unpack8(const uint4 &u, float (&f)[8], const __half *) {
-    const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const float2 p = __half22float2(*reinterpret_cast<const __half2 *>(&wv[j]));
-        f[2 * j] = p.x;
-        f[2 * j + 1] = p.y;
-    }
-}
-__device__ __forceinline__ void unpack8(const uint4 &u, float (&f)[8], const __nv_bfloat16 *) {
-    const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        f[2 * j] = __uint_as_float(wv[j] << 16);
-        f[2 * j + 1] = __uint_as_float(wv[j] & 0xffff0000u);
-    }
-}
-__device__ __forceinline__ uint4 pack8(const float (&f)[8], const __half *) {
-    uint32_t wv[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const __half2 h = __floats2half2_rn(f[2 * j], f[2 * j + 1]);
-        wv[j] = *reinterpret_cast<const uint32_t *>(&h);
-    }
-    return make_uint4(wv[0], wv[1], wv[2], wv[3]);
-}
-__device__ __forceinline__ uint4 pack8(const float (&f)[8], const __nv_bfloat16 *) {
-    uint32_t wv[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * j], f[2 * j + 1]);
-        wv[j] = *reinterpret_cast<const uint32_t *>(&h);
-    }
-    return make_uint4(wv[0], wv[1], wv[2], wv[3]);
-}
-
-template <typename ST, typename OutT>
-__global__ void __launch_bounds__(kHalfWarps * 32)
-wkv7_step_state16_kernel(long long n_heads, const float *__restrict__ r, const float *__restrict__ w,
-                         const float *__restrict__ k, const float *__restrict__ v,
-                         const float *__restrict__ kk, const float *__restrict__ a,
-                         ST *__restrict__ state, OutT *__restrict__ o) {
-    grid_dep_wait();
-    const int lane = threadIdx.x & 31;
-    const long long unit = static_cast<long long>(blockIdx.x) * kHalfWarps + (threadIdx.x >> 5);
-    if (unit >= 2 * n_heads) return;
-    const long long head = unit >> 1;
-    const int half = static_cast<int>(unit & 1);
-    const int rg = lane >> 2, row0 = rg * 8;
-    const int col = half * 32 + (lane & 3) * 8;
-    ST *S = state + head * (kN * kN) + static_cast<long long>(row0) * kN + col;
-    uint4 raw[8];
-#pragma unroll
-    for (int m = 0; m < 8; ++m) raw[m] = *reinterpret_cast<const uint4 *>(S + m * kN);
-    grid_dep_launch();
-    const long long vb = head * kN + row0;
-    const float4 r0 = __ldg(reinterpret_cast<const float4 *>(r + vb)), r1 = __ldg(reinterpret_cast<const float4 *>(r + vb + 4));
-    const float4 w0 = __ldg(reinterpret_cast<const float4 *>(w + vb)), w1 = __ldg(reinterpret_cast<const float4 *>(w + vb + 4));
-    const float4 k0 = __ldg(reinterpret_cast<const float4 *>(k + vb)), k1 = __ldg(reinterpret_cast<const float4 *>(k + vb + 4));
-    const float4 kk0 = __ldg(reinterpret_cast<const float4 *>(kk + vb)), kk1 = __ldg(reinterpret_cast<const float4 *>(kk + vb + 4));
-    const float4 a0 = __ldg(reinterpret_cast<const float4 *>(a + vb)), a1 = __ldg(reinterpret_cast<const float4 *>(a + vb + 4));
-    const float4 v0 = __ldg(reinterpret_cast<const float4 *>(v + head * kN + col));
-    const float4 v1 = __ldg(reinterpret_cast<const float4 *>(v + head * kN + col + 4));
-    const float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    float kkr[8], kr[8], rr[8], dr[8], cr[8];
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        kkr[m] = comp(kk0, m); kkr[m + 4] = comp(kk1, m);
-        kr[m] = comp(k0, m);   kr[m + 4] = comp(k1, m);
-        rr[m] = comp(r0, m);   rr[m + 4] = comp(r1, m);
-        dr[m] = expf(comp(w0, m)); dr[m + 4] = expf(comp(w1, m));
-        cr[m] = comp(kk0, m) * comp(a0, m); cr[m + 4] = comp(kk1, m) * comp(a1, m);
-    }
-    float z[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) z[c] = 0.f;
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-        float x[8];
-        unpack8(raw[m], x, static_cast<const ST *>(nullptr));
-#pragma unroll
-        for (int c = 0; c < 8; ++c) z[c] = fmaf(kkr[m], x[c], z[c]);
-    }
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1)
-#pragma unroll
-        for (int c = 0; c < 8; ++c) z[c] += __shfl_xor_sync(0xffffffffu, z[c], off);
-    float oc[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) oc[c] = 0.f;
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-        float x[8];
-        unpack8(raw[m], x, static_cast<const ST *>(nullptr));
-        const float d = dr[m], cm = cr[m], kv = kr[m];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            x[c] = fmaf(d, x[c], fmaf(-cm, z[c], kv * vv[c]));
-            oc[c] = fmaf(rr[m], x[c], oc[c]);
-        }
-        *reinterpret_cast<uint4 *>(S + m * kN) = pack8(x, static_cast<const ST *>(nullptr));
-    }
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1)
-#pragma unroll
-        for (int c = 0; c < 8; ++c) oc[c] += __shfl_xor_sync(0xffffffffu, oc[c], off);
-    if (rg == 0) {
-        store_o4(o, head * kN + col, oc[0], oc[1], oc[2], oc[3]);
-        store_o4(o, head * kN + col + 4, oc[4], oc[5], oc[6], oc[7]);
-    }
-}
+// The same step with the state stored in fp16 or bf16 (wkv7_step_kernel with
+// ST = __half or __nv_bfloat16): the bulk copies move 8 KB per head instead of
+// 16 KB, each element is widened to fp32 when it is read from the ring stage,
+// the whole update and read-out run in fp32, and the new state is rounded to
+// nearest even when it is written back into the stage, from where the bulk
+// store takes it.  The Core AI model zoo note (section 5, "Parity gate +
+// tokenizer") runs an fp16 export with fp16 state arrays; the state traffic,
+// 95% of a decode step's bytes, halves.  The ring is used for every head count:
+// staged in shared memory, a stage's bytes in flight do not depend on registers,
+// which hold only half as many state bytes in 16 bits.
 
 // Head count from which the register form is used (several full waves).
 constexpr long long kRegsFromHeads = 8192;
@@ -575,8 +488,30 @@ LaunchShape shape_for_device() {
 
 cudaError_t launch_step_state16(long long n_heads, const float *r, const float *w, const float *k, const float *v,
                                 const float *kk, const float *a, void *state, wkv7_dtype state_dtype, void *o,
-                                wkv7_dtype o_dtype, cudaStream_t stream) {
+                                wkv7_dtype o_dtype, unsigned *status, cudaStream_t stream) {
     if (n_heads <= 0) return cudaSuccess;
+    static int cached_dev = -1, cap = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev != cached_dev) {
+        int sms = 0, per_sm = 0;
+        const void *fns[4] = {reinterpret_cast<const void *>(wkv7_step_kernel<false, float, __half>),
+                              reinterpret_cast<const void *>(wkv7_step_kernel<false, __nv_bfloat16, __half>),
+                              reinterpret_cast<const void *>(wkv7_step_kernel<false, float, __nv_bfloat16>),
+                              reinterpret_cast<const void *>(wkv7_step_kernel<false, __nv_bfloat16, __nv_bfloat16>)};
+        for (const void *f : fns) {
+            e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes16));
+            if (e != cudaSuccess) return e;
+        }
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, wkv7_step_kernel<false, float, __half>, kThreads,
+                                                          kSmemBytes16);
+        if (e != cudaSuccess) return e;
+        cap = sms * (per_sm > 0 ? per_sm : 1);
+        cached_dev = dev;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -584,16 +519,17 @@ cudaError_t launch_step_state16(long long n_heads, const float *r, const float *
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const long long units = 2 * n_heads;
-    cfg.gridDim = dim3(static_cast<unsigned>((units + kHalfWarps - 1) / kHalfWarps));
-    cfg.blockDim = dim3(kHalfWarps * 32);
+    cfg.gridDim = dim3(static_cast<unsigned>(n_heads < cap ? n_heads : cap));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes16;
+    const TailArgs t{};
     const bool ob = o_dtype == WKV7_BF16;
     if (state_dtype == WKV7_F16) {
-        if (ob) return cudaLaunchKernelEx(&cfg, wkv7_step_state16_kernel<__half, __nv_bfloat16>, n_heads, r, w, k, v, kk, a, static_cast<__half *>(state), static_cast<__nv_bfloat16 *>(o));
-        return cudaLaunchKernelEx(&cfg, wkv7_step_state16_kernel<__half, float>, n_heads, r, w, k, v, kk, a, static_cast<__half *>(state), static_cast<float *>(o));
+        if (ob) return cudaLaunchKernelEx(&cfg, wkv7_step_kernel<false, __nv_bfloat16, __half>, n_heads, r, w, k, v, kk, a, static_cast<__half *>(state), static_cast<__nv_bfloat16 *>(o), t, status);
+        return cudaLaunchKernelEx(&cfg, wkv7_step_kernel<false, float, __half>, n_heads, r, w, k, v, kk, a, static_cast<__half *>(state), static_cast<float *>(o), t, status);
     }
-    if (ob) return cudaLaunchKernelEx(&cfg, wkv7_step_state16_kernel<__nv_bfloat16, __nv_bfloat16>, n_heads, r, w, k, v, kk, a, static_cast<__nv_bfloat16 *>(state), static_cast<__nv_bfloat16 *>(o));
-    return cudaLaunchKernelEx(&cfg, wkv7_step_state16_kernel<__nv_bfloat16, float>, n_heads, r, w, k, v, kk, a, static_cast<__nv_bfloat16 *>(state), static_cast<float *>(o));
+    if (ob) return cudaLaunchKernelEx(&cfg, wkv7_step_kernel<false, __nv_bfloat16, __nv_bfloat16>, n_heads, r, w, k, v, kk, a, static_cast<__nv_bfloat16 *>(state), static_cast<__nv_bfloat16 *>(o), t, status);
+    return cudaLaunchKernelEx(&cfg, wkv7_step_kernel<false, float, __nv_bfloat16>, n_heads, r, w, k, v, kk, a, static_cast<__nv_bfloat16 *>(state), static_cast<float *>(o), t, status);
 }
 
 cudaError_t launch_step(long long n_heads, const float *r, const float *w, const float *k,
