@@ -73,6 +73,12 @@ template <int ID, int COUNT>
 __device__ __forceinline__ void named_sync() {
     asm volatile("bar.sync %0, %1;" ::"n"(ID), "n"(COUNT) : "memory");
 }
+// Arrive on named barrier `id` (of `count` threads in all) without waiting: the
+// producer side of a producer / consumer barrier whose consumers use named_sync.
+template <int ID, int COUNT>
+__device__ __forceinline__ void named_arrive() {
+    asm volatile("bar.arrive %0, %1;" ::"n"(ID), "n"(COUNT) : "memory");
+}
 // Named barrier with an OR-reduction of `pred` over the participating threads.
 template <int ID, int COUNT>
 __device__ __forceinline__ int named_sync_or(int pred) {

@@ -653,18 +653,28 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
 
         // ---- phase 3: read G.  M_c (masked) -> A_chain columns 0..63 of rows t, which with
         // Cb^T below them (phase 4) form A_X = [M_c ; Cb^T]; M_k (masked) -> A_chain rows t,
-        // K 64..; L_c^T -> LT; L_k^T -> B_Y (16 + 16 columns per lower-lane warp).
+        // K 64..; L_c^T -> LT; L_k^T -> B_Y (16 + 16 columns per lower-lane warp).  The two
+        // warps that compute the T halves (0, 1) take no part: the lower-lane warps signal them
+        // as soon as L_c^T is written (named barrier 2: 256 arrivals + their 64), so the
+        // inverse starts while the rest of this phase runs, and warps 12, 13 take their share
+        // of M_c.  The others finish the phase on named barrier 3 (448 threads).
         if (q < 2) {
-            uint32_t wds[32];
-            const int gcol = (cg < 2 ? 0 : 64) + 32 * (cg & 1);  // M_c | M_k
-            const int s0 = 32 * (cg & 1);
-            const int t = m;
-            float v[32];
-            tmem_ld32(tmem + lane_off + kColG + gcol, v);
+            if (warp >= 2) {
+#pragma unroll 1
+                for (int pass = 0; pass < (cg == 3 ? 2 : 1); ++pass) {
+                    const int g = pass ? 0 : cg;  // warps 12, 13: M_k columns 32..63, then M_c 0..31
+                    uint32_t wds[32];
+                    const int gcol = (g < 2 ? 0 : 64) + 32 * (g & 1);  // M_c | M_k
+                    const int s0 = 32 * (g & 1);
+                    const int t = m;
+                    float v[32];
+                    tmem_ld32(tmem + lane_off + kColG + gcol, v);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) wds[j] = to_tf32(s0 + j <= t ? v[j] : 0.f);
-            tmem_st32_issue(tmem + lane_off + (gcol < 64 ? kColAX : kColAC) + gcol, wds);
-            tmem_wait_st();
+                    for (int j = 0; j < 32; ++j) wds[j] = to_tf32(s0 + j <= t ? v[j] : 0.f);
+                    tmem_st32_issue(tmem + lane_off + (gcol < 64 ? kColAX : kColAC) + gcol, wds);
+                    tmem_wait_st();
+                }
+            }
         } else {
             const int t = m - 64, s0 = 16 * cg;
             float v[16];
@@ -672,13 +682,21 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
             float *LTw = reinterpret_cast<float *>(sm + SM_LC);  // L_c^T: LT[s][t] = L_c[t][s]
 #pragma unroll
             for (int j = 0; j < 16; ++j) LTw[(s0 + j) * kLd + t] = s0 + j < t ? v[j] : 0.f;
+            named_arrive<2, 256 + 64>();  // -> the T halves
             tmem_ld16(tmem + lane_off + kColG + 64 + s0, v);
             unsigned char *BY = sm + SM_BY;
 #pragma unroll
             for (int j = 0; j < 16; ++j)
                 *reinterpret_cast<uint32_t *>(BY + sw128_off(64 + s0 + j, t, 128)) = to_tf32(s0 + j < t ? v[j] : 0.f);
         }
-        sync_for_mma();
+        if (warp < 2) {
+            named_sync<2, 256 + 64>();  // L_c^T written
+        } else {
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            named_sync<3, kThreads - 64>();
+            tc_fence_after_sync();
+        }
 
         // ---- phase 4: the two 32x32 diagonal halves of T = (I + L_c)^{-1}, in fp32, one warp
         // each: T_A = (I + L_AA)^{-1} (warp 0), T_B = (I + L_BB)^{-1} (warp 1).  Within a half
