@@ -1046,7 +1046,10 @@ def run_ours(args):
         return
     cfg = inputs.DECODE_2P9B
     B = args.batch
-    wl = DecodeWorkload(cfg["layers"], B, cfg["H"], cfg["pool"], dev, seed=1001 + rank)
+    sdt = {"f32": None, "f16": torch.float16, "bf16": torch.bfloat16}[args.state_dtype]
+    if sdt is not None and args.workload != "decode":
+        raise SystemExit("--state-dtype applies to --workload decode")
+    wl = DecodeWorkload(cfg["layers"], B, cfg["H"], cfg["pool"], dev, seed=1001 + rank, state_dtype=sdt)
     wl.warm_fresh(cfg["warm_tokens"], seed=1001 + rank)  # the state after 256 random tokens
     stream = torch.cuda.Stream(device=dev)
     graphs = wl.capture(stream)
@@ -1059,7 +1062,7 @@ def run_ours(args):
     launches = wl.layers * args.steps
     value = world * wl.state_bytes_per_step() * args.steps / (ms / 1e3) / 1e9
     launch_s = ms / 1e3 / launches
-    achieved = wl.B * wl.H * STEP_BYTES / launch_s / 1e9
+    achieved = wl.B * wl.H * wl.head_step_bytes() / launch_s / 1e9
     csrc = os.path.join(ROOT, "rwkv_linear_attention_gb300", "csrc")
     shared = [os.path.join(csrc, "sm103_ptx.cuh"), os.path.join(csrc, "wkv7_internal.cuh")]
     step_src = [os.path.join(csrc, "wkv7_step.cu")] + shared
@@ -1220,6 +1223,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--batch", type=int, default=32, help="decode batch B (2.9B geometry: 1, 8 or 32)")
+    ap.add_argument("--state-dtype", choices=("f32", "f16", "bf16"), default="f32",
+                    help="state type of --workload decode (the contract line is fp32)")
     ap.add_argument("--prefill-steps", type=int, default=20)
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
