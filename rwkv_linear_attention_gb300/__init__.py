@@ -35,9 +35,21 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream=None):
     s = stream if stream is not None else torch.cuda.current_stream()
     return ctypes.c_void_p(s.cuda_stream)
+
+
+def _stream_handle(stream, device):
+    """The cudaStream_t of ``stream`` (or of the current stream of ``device``) as an int."""
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None:
+        return _raw_stream(device.index if device.index is not None else torch.cuda.current_device())
+    return torch.cuda.current_stream(device).cuda_stream
 
 
 def _need_cuda(name, t, dtype, shape=None):
@@ -62,31 +74,44 @@ def _out_code(dtype):
 
 
 _STATE_CODES = {torch.float32: _lib.F32, torch.float16: _lib.F16, torch.bfloat16: _lib.BF16}
+_STEP_IN = ("r", "w", "k", "v", "kk", "a")
 
 
 def step(r, w, k, v, kk, a, state, o=None, stream=None, out_dtype=torch.float32):
     """One decode token: inputs fp32 [B, H, N]; ``state`` [B, H, N, N] updated
     in place, fp32 or a 16-bit type (fp16 / bf16: widened to fp32 for the
     update, rounded to nearest even on store).  Returns ``o`` [B, H, N] in
-    ``out_dtype`` (fp32, or bf16 rounded to nearest even; allocated if None)."""
-    B, H, N = r.shape
-    code = _out_code(out_dtype)
-    for name, t in (("r", r), ("w", w), ("k", k), ("v", v), ("kk", kk), ("a", a)):
-        _need_cuda(name, t, torch.float32, (B, H, N))
-    if state.dtype not in _STATE_CODES:
+    ``out_dtype`` (fp32, or bf16 rounded to nearest even; allocated if None).
+
+    This is the per-token call of a decode loop, so the checks are one cheap
+    pass (the C ABI validates sizes, alignment and overlaps again); a tensor that
+    fails it is re-checked field by field for a precise error."""
+    B, H, N = shp = r.shape
+    ins = (r, w, k, v, kk, a)
+    for t in ins:
+        if not (t.is_cuda and t.dtype is torch.float32 and t.shape == shp and t.is_contiguous()):
+            for name, u in zip(_STEP_IN, ins):
+                _need_cuda(name, u, torch.float32, (B, H, N))
+    scode = _STATE_CODES.get(state.dtype)
+    if scode is None:
         raise TypeError("state must be float32, float16 or bfloat16")
-    _need_cuda("state", state, state.dtype, (B, H, N, N))
+    if not (state.is_cuda and state.shape == (B, H, N, N) and state.is_contiguous()):
+        _need_cuda("state", state, state.dtype, (B, H, N, N))
+    code = _out_code(out_dtype)
     if o is None:
         o = torch.empty((B, H, N), device=r.device, dtype=out_dtype)
-    _need_cuda("o", o, out_dtype, (B, H, N))
-    lib = _lib.load()
-    if state.dtype == torch.float32:
-        st = lib.wkv7_step_cast(B, H, N, _ptr(r), _ptr(w), _ptr(k), _ptr(v), _ptr(kk), _ptr(a),
-                                _ptr(state), _ptr(o), code, _stream(stream))
+    elif not (o.is_cuda and o.dtype is out_dtype and o.shape == shp and o.is_contiguous()):
+        _need_cuda("o", o, out_dtype, (B, H, N))
+    lib = _lib._lib or _lib.load()
+    sh = _stream_handle(stream, r.device)
+    if scode == _lib.F32:
+        st = lib.wkv7_step_cast(B, H, N, r.data_ptr(), w.data_ptr(), k.data_ptr(), v.data_ptr(), kk.data_ptr(),
+                                a.data_ptr(), state.data_ptr(), o.data_ptr(), code, sh)
     else:
-        st = lib.wkv7_step_state(B, H, N, _ptr(r), _ptr(w), _ptr(k), _ptr(v), _ptr(kk), _ptr(a),
-                                 _ptr(state), _STATE_CODES[state.dtype], _ptr(o), code, _stream(stream))
-    _lib.check(st, "wkv7_step")
+        st = lib.wkv7_step_state(B, H, N, r.data_ptr(), w.data_ptr(), k.data_ptr(), v.data_ptr(), kk.data_ptr(),
+                                 a.data_ptr(), state.data_ptr(), scode, o.data_ptr(), code, sh)
+    if st:
+        _lib.check(st, "wkv7_step")
     return o
 
 
