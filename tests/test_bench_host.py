@@ -78,3 +78,36 @@ def test_byte_and_flop_constants():
 def test_warmup_floor():
     with pytest.raises(SystemExit):
         bench.main(["--warmup", "2"])
+
+
+def test_summarize_nvml_reasons_and_median():
+    bits = bench.NvmlClockSampler.REASONS
+    samples = [(2070, 2070, 0), (2055, 2070, 0x4), (1995, 2070, 0x4 | 0x1), (2070, 2070, 0x40)]
+    c = bench.summarize_nvml(samples, bits)
+    assert c["samples"] == 4 and c["sm_max_mhz"] == 2070 and c["source"] == "nvml"
+    assert c["sm_mhz"] == (2055 + 2070) / 2
+    assert c["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]  # the idle bit (0x1) is not a throttle
+    assert bench.summarize_nvml([], bits)["samples"] == 0
+
+
+def test_oracle_rate_repeats_when_the_units_run_out():
+    calls = []
+
+    def fn(n, threads):
+        calls.append(n)
+        import time
+        time.sleep(0.002 * n)
+
+    rate, n, dt = bench.oracle_rate(fn, units=3, budget_s=0.05, threads=1)
+    # 3 units take ~6 ms < 50 ms: the full run is repeated until the budget is spent
+    assert n % 3 == 0 and n >= 6 and dt >= 0.04
+    assert abs(rate - n / dt) < 1e-9
+
+
+def test_oracle_rate_grows_the_sample_to_the_budget():
+    def fn(n, threads):
+        import time
+        time.sleep(0.001 * n)
+
+    rate, n, dt = bench.oracle_rate(fn, units=10 ** 6, budget_s=0.03, threads=4)
+    assert dt >= 0.03 and n < 10 ** 6
