@@ -986,16 +986,32 @@ constexpr int kFixThreads = 256;
 // 4 tc..): acc += A B with A held transposed (At[k][row], stride kLdT) and B row-major
 // (stride 64), both in shared memory; per k one 16-byte load of each gives 16 FMAs.
 constexpr int kLdT = 68;
+// The inner product runs on paired fp32 FMAs (two lanes of a float2 per instruction;
+// each element is the same single fmaf as before).
 __device__ __forceinline__ void mm64_tile(const float *At, const float *B, int tr, int tc, float (&acc)[4][4]) {
+    float2 acc2[4][2];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        acc2[r][0] = make_float2(acc[r][0], acc[r][1]);
+        acc2[r][1] = make_float2(acc[r][2], acc[r][3]);
+    }
 #pragma unroll 8
     for (int k = 0; k < 64; ++k) {
         const float4 a = *reinterpret_cast<const float4 *>(At + k * kLdT + 4 * tr);
         const float4 b = *reinterpret_cast<const float4 *>(B + k * 64 + 4 * tc);
-        const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+        const float av[4] = {a.x, a.y, a.z, a.w};
+        const float2 b01 = make_float2(b.x, b.y), b23 = make_float2(b.z, b.w);
 #pragma unroll
-        for (int r = 0; r < 4; ++r)
+        for (int r = 0; r < 4; ++r) {
+            const float2 ar = make_float2(av[r], av[r]);
+            acc2[r][0] = __ffma2_rn(ar, b01, acc2[r][0]);
+            acc2[r][1] = __ffma2_rn(ar, b23, acc2[r][1]);
+        }
+    }
 #pragma unroll
-            for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(av[r], bv[c], acc[r][c]);
+    for (int r = 0; r < 4; ++r) {
+        acc[r][0] = acc2[r][0].x; acc[r][1] = acc2[r][0].y;
+        acc[r][2] = acc2[r][1].x; acc[r][3] = acc2[r][1].y;
     }
 }
 // global row-major 64x64 fp32 -> shared, transposed (dst[k][row], stride kLdT)
@@ -1012,39 +1028,59 @@ __device__ __forceinline__ void load_t64(float *dst, const float *src) {
 
 // One CTA per split pair: the true state at every segment boundary, in order,
 // S_in(j+1) = P(j) S_in(j) + S_part(j), written over S_part(j)'s slot; the
-// last one is the pair's final state.
-__global__ void __launch_bounds__(kFixThreads)
+// last one is the pair's final state.  The products are a dependent chain, so
+// the CTA is large (1024 threads, a 2 x 2 output tile each: rows 2 tr .., columns
+// 2 tc ..) to keep each product short.
+constexpr int kChainThreads = 1024;
+
+__global__ void __launch_bounds__(kChainThreads)
 wkv7_prefill_split_chain_kernel(const __grid_constant__ FixPlan fp, void *final_state, wkv7_dtype state_dtype, int H) {
     __shared__ __align__(16) float sin_[64 * 64];
     __shared__ __align__(16) float pt[64 * kLdT];  // P(j) transposed
     const FixPair &pr = fp.pair[blockIdx.x];
-    const int tid = threadIdx.x, tr = tid >> 4, tc = tid & 15;
+    const int tid = threadIdx.x, tr = tid >> 5, tc = tid & 31;
     const float4 *s0 = reinterpret_cast<const float4 *>(fp.slots + static_cast<long long>(pr.seg[0].slot_part) * 4096);
-    for (int e = tid; e < 1024; e += kFixThreads) reinterpret_cast<float4 *>(sin_)[e] = s0[e];
-    for (int j = 1; j < pr.nseg; ++j) {
-        load_t64(pt, fp.slots + static_cast<long long>(pr.seg[j].slot_transfer) * 4096);
-        float *Sp = fp.slots + static_cast<long long>(pr.seg[j].slot_part) * 4096;
-        float acc[4][4];
+    reinterpret_cast<float4 *>(sin_)[tid] = s0[tid];  // 1024 float4 = the 64 x 64 state
+    // this thread's float4 of P(j) and 2 x 2 tile of S_part(j), fetched one segment ahead
+    auto fetch = [&](int j, float4 &x, float2 (&sp)[2]) {
+        x = reinterpret_cast<const float4 *>(fp.slots + static_cast<long long>(pr.seg[j].slot_transfer) * 4096)[tid];
+        const float *Sp = fp.slots + static_cast<long long>(pr.seg[j].slot_part) * 4096;
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const float4 v = *reinterpret_cast<const float4 *>(Sp + (4 * tr + r) * 64 + 4 * tc);
-            acc[r][0] = v.x; acc[r][1] = v.y; acc[r][2] = v.z; acc[r][3] = v.w;
+        for (int r = 0; r < 2; ++r) sp[r] = *reinterpret_cast<const float2 *>(Sp + (2 * tr + r) * 64 + 2 * tc);
+    };
+    float4 xn;
+    float2 spn[2];
+    if (pr.nseg > 1) fetch(1, xn, spn);
+    for (int j = 1; j < pr.nseg; ++j) {
+        {   // P(j) transposed into pt[k][row]: one float4 of a row per thread
+            const int row = tid >> 4, k0 = 4 * (tid & 15);
+            pt[(k0 + 0) * kLdT + row] = xn.x;
+            pt[(k0 + 1) * kLdT + row] = xn.y;
+            pt[(k0 + 2) * kLdT + row] = xn.z;
+            pt[(k0 + 3) * kLdT + row] = xn.w;
         }
+        float *Sp = fp.slots + static_cast<long long>(pr.seg[j].slot_part) * 4096;
+        float2 acc[2] = {spn[0], spn[1]};
+        if (j + 1 < pr.nseg) fetch(j + 1, xn, spn);  // lands during this product
         __syncthreads();  // P(j)^T and S_in(j) in shared memory
-        mm64_tile(pt, sin_, tr, tc, acc);
+#pragma unroll 8
+        for (int k = 0; k < 64; ++k) {
+            const float2 a = *reinterpret_cast<const float2 *>(pt + k * kLdT + 2 * tr);
+            const float2 bv = *reinterpret_cast<const float2 *>(sin_ + k * 64 + 2 * tc);
+            acc[0] = __ffma2_rn(make_float2(a.x, a.x), bv, acc[0]);
+            acc[1] = __ffma2_rn(make_float2(a.y, a.y), bv, acc[1]);
+        }
         __syncthreads();  // every thread has read S_in(j) and P(j)
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const float4 v = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
-            *reinterpret_cast<float4 *>(sin_ + (4 * tr + r) * 64 + 4 * tc) = v;
-            *reinterpret_cast<float4 *>(Sp + (4 * tr + r) * 64 + 4 * tc) = v;
+        for (int r = 0; r < 2; ++r) {
+            *reinterpret_cast<float2 *>(sin_ + (2 * tr + r) * 64 + 2 * tc) = acc[r];
+            *reinterpret_cast<float2 *>(Sp + (2 * tr + r) * 64 + 2 * tc) = acc[r];
         }
     }
     __syncthreads();
     if (final_state) {
         const long long base = (static_cast<long long>(pr.b) * H + pr.h) * 4096;
-        for (int e = tid; e < 1024; e += kFixThreads)
-            store_state4(final_state, state_dtype, base + 4 * e, reinterpret_cast<const float4 *>(sin_)[e]);
+        store_state4(final_state, state_dtype, base + 4 * tid, reinterpret_cast<const float4 *>(sin_)[tid]);
     }
 }
 
@@ -1066,6 +1102,25 @@ wkv7_prefill_split_ofix_kernel(const __grid_constant__ FixPlan fp, PrefillArgs p
     const float4 *Sin = reinterpret_cast<const float4 *>(fp.slots + static_cast<long long>(pr.seg[j - 1].slot_part) * 4096);
     for (int e = tid; e < 1024; e += kFixThreads) reinterpret_cast<float4 *>(sin_)[e] = Sin[e];
     load_t64(oht, fp.ohat + (static_cast<long long>(sg.ohat_row) + (chunk - sg.c0) * 64) * 64);
+    int bos, eos;
+    seq_bounds(p, pr.b, bos, eos);
+    const int t0 = bos + chunk * 64;
+    const int lc = min(64, eos - t0);
+    const bool bf16 = p.o_dtype == WKV7_BF16;
+    // the partial outputs this thread corrects (in o, fp32; or in the part item's fp32 rows when
+    // o is bf16), fetched before the product so that their latency overlaps it
+    float4 part[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int t = 4 * tr + r;
+        part[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (t < lc) {
+            const long long at = (static_cast<long long>(t0) + t) * p.H * 64 + pr.h * 64 + 4 * tc;
+            part[r] = bf16 ? *reinterpret_cast<const float4 *>(
+                                 fp.ohat + (static_cast<long long>(sg.opart_row) + (chunk - sg.c0) * 64 + t) * 64 + 4 * tc)
+                           : *reinterpret_cast<const float4 *>(static_cast<float *>(p.o) + at);
+        }
+    }
     __syncthreads();
     float acc[4][4];
 #pragma unroll
@@ -1073,21 +1128,12 @@ wkv7_prefill_split_ofix_kernel(const __grid_constant__ FixPlan fp, PrefillArgs p
 #pragma unroll
         for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
     mm64_tile(oht, sin_, tr, tc, acc);
-    int bos, eos;
-    seq_bounds(p, pr.b, bos, eos);
-    const int t0 = bos + chunk * 64;
-    const int lc = min(64, eos - t0);
-    const bool bf16 = p.o_dtype == WKV7_BF16;
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
         const int t = 4 * tr + r;
         if (t < lc) {
             const long long at = (static_cast<long long>(t0) + t) * p.H * 64 + pr.h * 64 + 4 * tc;
-            // the partial output: in o (fp32), or in the part item's fp32 rows (bf16 o)
-            const float4 *src = bf16 ? reinterpret_cast<const float4 *>(
-                                           fp.ohat + (static_cast<long long>(sg.opart_row) + (chunk - sg.c0) * 64 + t) * 64 + 4 * tc)
-                                     : reinterpret_cast<const float4 *>(static_cast<float *>(p.o) + at);
-            float4 v = *src;
+            float4 v = part[r];
             v.x += acc[r][0];
             v.y += acc[r][1];
             v.z += acc[r][2];
@@ -1322,8 +1368,8 @@ cudaError_t launch_chunked(const PrefillArgs &args, unsigned char *split_ws, siz
         args, maps, plan);
     e = cudaGetLastError();
     if (e != cudaSuccess || !split) return e;
-    wkv7_prefill_split_chain_kernel<<<fix.n_pairs, kFixThreads, 0, stream>>>(fix, args.final_state, args.state_dtype,
-                                                                              args.H);
+    wkv7_prefill_split_chain_kernel<<<fix.n_pairs, kChainThreads, 0, stream>>>(fix, args.final_state, args.state_dtype,
+                                                                                args.H);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     wkv7_prefill_split_ofix_kernel<<<dim3(fix.n_blocks, fix.n_pairs), kFixThreads, 0, stream>>>(fix, args);
