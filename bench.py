@@ -513,8 +513,9 @@ def decode_e2e_api(wl, steps, warmup, stream, world):
     return ms, h2d, d2h
 
 
-def prefill_case(lens, H, seed, dev, with_s0=False, x_dtype=None):
-    """Inputs, outputs and workspace of one prefill workload, on the device."""
+def prefill_case(lens, H, seed, dev, with_s0=False, x_dtype=None, tf32=False):
+    """Inputs, outputs and workspace of one prefill workload, on the device (``tf32``:
+    fp32 inputs through the chunked tensor-core kernel)."""
     import torch
 
     import rwkv_linear_attention_gb300 as wkv7
@@ -523,7 +524,7 @@ def prefill_case(lens, H, seed, dev, with_s0=False, x_dtype=None):
     p = inputs.prefill_inputs(lens, H, N_HEAD, seed=seed, device=dev, x_dtype=x_dtype)
     cu = p["cu_seqlens"]
     T = int(cu[-1])
-    c = {"p": p, "cu": cu, "cu_dev": cu.to(dev), "T": T, "H": H, "num_seqs": len(lens),
+    c = {"p": p, "cu": cu, "cu_dev": cu.to(dev), "T": T, "H": H, "num_seqs": len(lens), "tf32": tf32,
          "s0": inputs.initial_state(len(lens), H, N_HEAD, seed=seed, std=0.1, device=dev) if with_s0 else None,
          "o": torch.empty(T, H, N_HEAD, device=dev),
          "sf": torch.empty(len(lens), H, N_HEAD, N_HEAD, device=dev)}
@@ -542,7 +543,7 @@ def prefill_call(c, stream, src=None, o=None, sf=None):
     p = src or c["p"]
     wkv7.prefill(p["r"], p["w"], p["k"], p["v"], p["kk"], p["a"], c["cu_dev"], initial_state=c["s0"],
                  final_state=c["sf"] if sf is None else sf, o=c["o"] if o is None else o, workspace=c["ws"],
-                 cu_seqlens_host=c["cu"], stream=stream)
+                 cu_seqlens_host=c["cu"], stream=stream, tf32=c["tf32"])
 
 
 def prefill_e2e(c, calls, warmup, stream, world):
@@ -938,12 +939,15 @@ def config_lines(args, dev, peaks, peak_kind, world, gpu_index, cpu_budget):
     want_cpu = rank == 0 and cpu_budget > 0
     out = []
 
-    # 0.1B: B=1, T=64, H=12, fp32 inputs: the prefill (token-serial kernel) and the
-    # 64-step decode loop from the zero state
+    # 0.1B: B=1, T=64, H=12, fp32 inputs: the prefill through the chunked tensor-core
+    # kernel (tf32 contraction) and through the exact token-serial kernel, and the 64-step
+    # decode loop from the zero state
     c0 = inputs.SMALL_0P1B
-    c = prefill_case([c0["T"]], c0["H"], 1000, dev, x_dtype=torch.float32)
+    c = prefill_case([c0["T"]], c0["H"], 1000, dev, x_dtype=torch.float32, tf32=True)
     with Clocks(gpu_index) as clk:
         ms = time_stream(lambda: prefill_call(c, stream), max(args.steps, 8), args.warmup, stream)
+    c["tf32"] = False
+    ms_serial = time_stream(lambda: prefill_call(c, stream), max(args.steps, 8), args.warmup, stream)
     wkv7.check_device_status(stream)
     x = inputs.draw_rwkkva((c0["T"], 1, c0["H"], N_HEAD), seed=1000, device=dev)
     st = torch.zeros(1, c0["H"], N_HEAD, N_HEAD, device=dev)
@@ -955,9 +959,9 @@ def config_lines(args, dev, peaks, peak_kind, world, gpu_index, cpu_budget):
     ms_loop = time_stream(loop, max(args.steps // 4, 4), args.warmup, stream)
     obj = {"config": 0, "workload": "0.1B geometry, B=1, T=64, H=12, fp32 inputs, zero initial state",
            "metric": "prefill tokens/s", "value": round(world * c0["T"] / (ms * 1e-3), 1), "unit": "tokens/s",
-           "prefill_ms": round(ms, 5),
+           "prefill_ms": round(ms, 5), "prefill_token_serial_ms": round(ms_serial, 5),
            "decode_loop_ms": round(ms_loop, 5), "clocks": clk.result,
-           "roofline": roofline_obj(c["bytes"], ms, peaks, peak_kind, kernel="wkv7_prefill_scan_kernel",
+           "roofline": roofline_obj(c["bytes"], ms, peaks, peak_kind, kernel="wkv7_prefill_chunked_kernel",
                                     note="launch-bound: 0.4 MB per call")}
     if want_cpu:
         obj["cpu_baseline"] = cpu_baseline_prefill([c0["T"]], c0["H"], cpu_budget)
@@ -995,6 +999,21 @@ def config_lines(args, dev, peaks, peak_kind, world, gpu_index, cpu_budget):
         out.append(obj)
         del graphs, wl
         torch.cuda.empty_cache()
+
+    # the 2.9B prefill batch with fp32 inputs through the chunked kernel (tf32 contraction)
+    pc = inputs.PREFILL_2P9B
+    c = prefill_case([pc["T"]] * pc["num_seqs"], pc["H"], 1002, dev, x_dtype=torch.float32, tf32=True)
+    calls = max(3, args.prefill_steps // 4)
+    clk = Clocks(gpu_index)
+    ms = prefill_bench(c, calls, 2, world, clocks=clk)
+    out.append({"config": 2, "workload": "prefill, 2.9B 8 x 4096, H=40, fp32 inputs contracted at tf32 "
+                                         "(the chunked kernel), zero initial state",
+                "metric": "tokens/s", "value": round(world * c["T"] / (ms * 1e-3), 1), "unit": "tokens/s",
+                "ms_per_call": round(ms, 4), "tokens": c["T"], "calls": calls, "clocks": clk.result,
+                "roofline": roofline_obj(c["bytes"], ms, peaks, peak_kind, kernel="wkv7_prefill_chunked_kernel",
+                                         algorithmic_bytes_per_launch=c["bytes"])})
+    del c
+    torch.cuda.empty_cache()
 
     # 7.2B prefill: 16 sequences of U[1, 32768] tokens, and one 32768-token sequence,
     # both with N(0, 0.1) initial states
@@ -1050,11 +1069,13 @@ def run_ours(args):
         return
     pcfg = inputs.PREFILL_2P9B
     if args.workload == "prefill":
-        c = prefill_case([pcfg["T"]] * pcfg["num_seqs"], pcfg["H"], 1002, dev)
+        c = prefill_case([pcfg["T"]] * pcfg["num_seqs"], pcfg["H"], 1002, dev,
+                         x_dtype=torch.float32 if args.prefill_tf32 else None, tf32=args.prefill_tf32)
         ms = prefill_bench(c, args.prefill_steps, args.warmup, world)
         if rank == 0:
             gbs = c["bytes"] / (ms / 1e3) / 1e9
-            print(json.dumps({"workload": "prefill 2.9B (8 x 4096, H=40, bf16)", "ms_per_call": ms,
+            xs = "fp32 inputs, tf32 contraction" if args.prefill_tf32 else "bf16"
+            print(json.dumps({"workload": f"prefill 2.9B (8 x 4096, H=40, {xs})", "ms_per_call": ms,
                               "tokens_per_s": world * c["T"] / (ms / 1e3),
                               "achieved_gbs": gbs, "frac": gbs / peaks["hbm_gbs"]}), flush=True)
         return
@@ -1240,6 +1261,8 @@ def main(argv=None):
     ap.add_argument("--state-dtype", choices=("f32", "f16", "bf16"), default="f32",
                     help="state type of --workload decode (the contract line is fp32)")
     ap.add_argument("--prefill-steps", type=int, default=20)
+    ap.add_argument("--prefill-tf32", action="store_true",
+                    help="--workload prefill: fp32 inputs through the chunked kernel (tf32 contraction)")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--backward-seqs", type=int, default=8, help="sequences of 4096 tokens for --workload backward")

@@ -64,7 +64,9 @@ typedef enum {
 typedef enum {
     WKV7_F32 = 0,
     WKV7_BF16 = 1,
-    WKV7_F16 = 2   /* IEEE half precision; accepted only where a call says so */
+    WKV7_F16 = 2,  /* IEEE half precision; accepted only where a call says so */
+    WKV7_TF32 = 3  /* fp32 storage contracted at tf32 precision on the tensor cores;
+                      accepted only where a call says so (the prefill inputs) */
 } wkv7_dtype;
 
 #define WKV7_HEAD_SIZE 64
@@ -237,7 +239,14 @@ WKV7_API size_t wkv7_prefill_workspace_size(int num_seqs, int T_total, int H, in
  *                     split; it must equal the device array.  When NULL the
  *                     device validates cu_seqlens and a malformed array is
  *                     reported by wkv7_check_device_status.
- *   x_dtype         : WKV7_F32 or WKV7_BF16, the type of r, k, v, kk, a
+ *   x_dtype         : the type of r, k, v, kk, a, and the kernel that runs:
+ *                     WKV7_BF16 -- bf16, the chunked tensor-core kernel (the
+ *                       WY/UT form, contractions at tf32 with fp32 accumulation);
+ *                     WKV7_TF32 -- fp32 inputs through the same chunked kernel
+ *                       (read at full precision, contracted at tf32: the same
+ *                       error bound and domain as bf16 inputs);
+ *                     WKV7_F32 -- fp32 inputs through an exact token-serial
+ *                       kernel (fp32 arithmetic throughout, no domain limit)
  *   r, k, v, kk, a  : x_dtype [T_total, H, N]  (token-major)
  *   w               : fp32 [T_total, H, N]     log-decay
  *   initial_state   : fp32 [num_seqs, H, N, N] or NULL (= zeros)
@@ -253,7 +262,7 @@ WKV7_API size_t wkv7_prefill_workspace_size(int num_seqs, int T_total, int H, in
  *                     any other argument.  Calls that overlap on the GPU must
  *                     use distinct workspaces.
  *
- * Domain of the chunked formulation (bf16 inputs): w >= -1 elementwise
+ * Domain of the chunked formulation (WKV7_BF16, WKV7_TF32): w >= -1 elementwise
  * (every RWKV-7 model has w in (-0.6066, 0)).  The chunked kernel takes a
  * chunk's decay factors relative to its 32nd token, so each scaled operand
  * carries a factor within e^{+-32} and the chunk's removal block, where one
@@ -262,8 +271,8 @@ WKV7_API size_t wkv7_prefill_workspace_size(int num_seqs, int T_total, int H, in
  * and 0 on others that block overflows.)  The kernel checks the domain on the
  * device: a w below -1 (or -inf) is reported by wkv7_check_device_status as
  * WKV7_ERR_INVALID_ARG, and the outputs of that call are then unspecified
- * (they may hold inf or NaN).  fp32 inputs take a token-serial kernel that
- * has no such limit.
+ * (they may hold inf or NaN).  WKV7_F32 inputs take the token-serial kernel,
+ * which has no such limit.
  */
 WKV7_API wkv7_status wkv7_prefill(int num_seqs, int T_total, int H, int N,
                          const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
@@ -388,7 +397,8 @@ WKV7_API wkv7_status wkv7_prefill_noalloc(int num_seqs, int T_total, int H, int 
  *
  *   num_seqs .. a    : exactly the arguments of the wkv7_prefill call being
  *                      differentiated (same layouts, dtypes and sequence
- *                      rules; cu_seqlens_host optional and validated)
+ *                      rules; cu_seqlens_host optional and validated;
+ *                      WKV7_TF32 and WKV7_F32 both mean fp32 inputs here)
  *   initial_state    : fp32 [num_seqs, H, N, N] or NULL (= zeros), as given
  *                      to wkv7_prefill
  *   d_o              : fp32 [T_total, H, N]     gradient of the loss w.r.t. o

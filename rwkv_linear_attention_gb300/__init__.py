@@ -74,6 +74,14 @@ def _out_code(dtype):
 
 
 _STATE_CODES = {torch.float32: _lib.F32, torch.float16: _lib.F16, torch.bfloat16: _lib.BF16}
+
+
+def _x_code(xdt, tf32):
+    """The prefill input code: bf16; fp32 contracted at tf32 by the chunked kernel
+    (``tf32``); or fp32 through the exact token-serial kernel."""
+    if xdt == torch.bfloat16:
+        return _lib.BF16
+    return _lib.TF32 if tf32 else _lib.F32
 _STEP_IN = ("r", "w", "k", "v", "kk", "a")
 
 
@@ -210,10 +218,13 @@ def prefill_workspace_size(num_seqs: int, T_total: int, H: int, N: int = HEAD_SI
 
 def prefill(r, w, k, v, kk, a, cu_seqlens, initial_state=None, final_state=None, o=None,
             workspace=None, cu_seqlens_host=None, want_final_state=True, stream=None, out_dtype=torch.float32,
-            state_dtype=None):
+            state_dtype=None, tf32=False):
     """Packed varlen prefill.
 
     r, k, v, kk, a: [T_total, H, N] fp32 or bf16 (one dtype for all five);
+    bf16 inputs run the chunked tensor-core kernel, fp32 inputs the exact
+    token-serial kernel, or with ``tf32`` the chunked kernel (fp32 read in full,
+    contracted at tf32: the bf16 inputs' error bound and domain w >= -1);
     w: fp32 [T_total, H, N]; ``cu_seqlens``: int32 CUDA [num_seqs + 1].
     ``initial_state``: fp32 [num_seqs, H, N, N] or None (zeros).
     ``final_state``: output buffer (may be ``initial_state`` for an in-place
@@ -266,8 +277,7 @@ def prefill(r, w, k, v, kk, a, cu_seqlens, initial_state=None, final_state=None,
             workspace = torch.empty(need, device=r.device, dtype=torch.uint8)
         _need_cuda("workspace", workspace, torch.uint8)
         ws_bytes = workspace.numel()
-    st = lib.wkv7_prefill_state(num_seqs, T_total, H, N, _ptr(cu_seqlens), host_ptr,
-                                _lib.BF16 if xdt == torch.bfloat16 else _lib.F32,
+    st = lib.wkv7_prefill_state(num_seqs, T_total, H, N, _ptr(cu_seqlens), host_ptr, _x_code(xdt, tf32),
                                 _ptr(r), _ptr(w), _ptr(k), _ptr(v), _ptr(kk), _ptr(a),
                                 _ptr(initial_state), _ptr(final_state), _STATE_CODES[state_dtype], _ptr(o), code,
                                 _ptr(workspace) if need > 0 else None, ws_bytes, _stream(stream))
@@ -280,7 +290,8 @@ def prefill_backward_workspace_size(num_seqs: int, T_total: int, H: int, N: int 
 
 
 def prefill_backward(r, w, k, v, kk, a, cu_seqlens, d_o, initial_state=None, d_final_state=None,
-                     want_d_initial_state=True, grads=None, workspace=None, cu_seqlens_host=None, stream=None):
+                     want_d_initial_state=True, grads=None, workspace=None, cu_seqlens_host=None, stream=None,
+                     tf32=False):
     """Gradients of a :func:`prefill` call for L = <d_o, o> + <d_final_state, final_state>.
 
     The first seven arguments and ``initial_state`` are those of the forward
@@ -322,8 +333,7 @@ def prefill_backward(r, w, k, v, kk, a, cu_seqlens, d_o, initial_state=None, d_f
     if workspace is None:
         workspace = torch.empty(max(need, 16), device=r.device, dtype=torch.uint8)
     _need_cuda("workspace", workspace, torch.uint8)
-    st = lib.wkv7_prefill_backward(num_seqs, T_total, H, N, _ptr(cu_seqlens), host_ptr,
-                                   _lib.BF16 if xdt == torch.bfloat16 else _lib.F32,
+    st = lib.wkv7_prefill_backward(num_seqs, T_total, H, N, _ptr(cu_seqlens), host_ptr, _x_code(xdt, tf32),
                                    _ptr(r), _ptr(w), _ptr(k), _ptr(v), _ptr(kk), _ptr(a),
                                    _ptr(initial_state), _ptr(d_o), _ptr(d_final_state),
                                    *[_ptr(t) for t in grads], _ptr(ds0),
@@ -333,9 +343,9 @@ def prefill_backward(r, w, k, v, kk, a, cu_seqlens, d_o, initial_state=None, d_f
 
 
 def prefill_padded(r, w, k, v, kk, a, lens, initial_state=None, final_state=None, o=None, workspace=None,
-                   lens_host=None, want_final_state=True, stream=None, out_dtype=torch.float32):
+                   lens_host=None, want_final_state=True, stream=None, out_dtype=torch.float32, tf32=False):
     """Prefill over a right-padded batch: inputs [B, T_max, H, N] (r, k, v, kk, a
-    fp32 or bf16, w fp32); row b holds ``lens[b]`` real tokens (``lens`` int32
+    fp32 or bf16, w fp32; ``tf32`` as in :func:`prefill`); row b holds ``lens[b]`` real tokens (``lens`` int32
     CUDA [B]; ``lens_host`` an optional CPU copy, used for scheduling).  Returns
     ``(o [B, T_max, H, N] in out_dtype, final_state)``; o past each row's length
     is left as it was."""
@@ -371,7 +381,7 @@ def prefill_padded(r, w, k, v, kk, a, lens, initial_state=None, final_state=None
             workspace = torch.empty(need, device=r.device, dtype=torch.uint8)
         _need_cuda("workspace", workspace, torch.uint8)
         ws_bytes = workspace.numel()
-    st = lib.wkv7_prefill_padded(B, T_max, H, N, _ptr(lens), host_ptr, _lib.BF16 if xdt == torch.bfloat16 else _lib.F32,
+    st = lib.wkv7_prefill_padded(B, T_max, H, N, _ptr(lens), host_ptr, _x_code(xdt, tf32),
                                  _ptr(r), _ptr(w), _ptr(k), _ptr(v), _ptr(kk), _ptr(a), _ptr(initial_state),
                                  _ptr(final_state), _ptr(o), code, _ptr(workspace) if need > 0 else None, ws_bytes,
                                  _stream(stream))

@@ -25,6 +25,7 @@ ERR_DEVICE_BOUNDS = 7
 F32 = 0
 BF16 = 1
 F16 = 2
+TF32 = 3
 
 EXPORTS = (
     "wkv7_step",

@@ -288,7 +288,7 @@ wkv7_status wkv7_prefill_state(int num_seqs, int T_total, int H, int N, const in
                                wkv7_dtype state_dtype, void *o, wkv7_dtype o_dtype, void *workspace,
                                size_t workspace_bytes, cudaStream_t stream) {
     if (N != wkv7::kN) return WKV7_ERR_UNSUPPORTED;
-    if (x_dtype != WKV7_F32 && x_dtype != WKV7_BF16) return WKV7_ERR_UNSUPPORTED;
+    if (x_dtype != WKV7_F32 && x_dtype != WKV7_BF16 && x_dtype != WKV7_TF32) return WKV7_ERR_UNSUPPORTED;
     if (o_dtype != WKV7_F32 && o_dtype != WKV7_BF16) return WKV7_ERR_UNSUPPORTED;
     if (state_dtype != WKV7_F32 && state_dtype != WKV7_F16 && state_dtype != WKV7_BF16) return WKV7_ERR_UNSUPPORTED;
     if (num_seqs < 0 || T_total < 0 || H <= 0) return WKV7_ERR_INVALID_ARG;
@@ -394,7 +394,7 @@ wkv7_status wkv7_prefill_padded(int B, int T_max, int H, int N, const int32_t *l
                                 void *o, wkv7_dtype o_dtype, void *workspace, size_t workspace_bytes,
                                 cudaStream_t stream) {
     if (N != wkv7::kN) return WKV7_ERR_UNSUPPORTED;
-    if (x_dtype != WKV7_F32 && x_dtype != WKV7_BF16) return WKV7_ERR_UNSUPPORTED;
+    if (x_dtype != WKV7_F32 && x_dtype != WKV7_BF16 && x_dtype != WKV7_TF32) return WKV7_ERR_UNSUPPORTED;
     if (o_dtype != WKV7_F32 && o_dtype != WKV7_BF16) return WKV7_ERR_UNSUPPORTED;
     if (B < 0 || T_max < 0 || H <= 0) return WKV7_ERR_INVALID_ARG;
     if ((long long)B * H > kMaxHeads || (long long)B * T_max >= kMaxTokens ||
@@ -495,7 +495,7 @@ wkv7_status wkv7_prefill_backward(int num_seqs, int T_total, int H, int N, const
                                   float *d_initial_state, void *workspace, size_t workspace_bytes,
                                   cudaStream_t stream) {
     if (N != wkv7::kN) return WKV7_ERR_UNSUPPORTED;
-    if (x_dtype != WKV7_F32 && x_dtype != WKV7_BF16) return WKV7_ERR_UNSUPPORTED;
+    if (x_dtype != WKV7_F32 && x_dtype != WKV7_BF16 && x_dtype != WKV7_TF32) return WKV7_ERR_UNSUPPORTED;
     if (num_seqs < 0 || T_total < 0 || H <= 0) return WKV7_ERR_INVALID_ARG;
     if ((long long)num_seqs * H > kMaxHeads || (long long)T_total >= kMaxTokens) return WKV7_ERR_INVALID_ARG;
     if (H > 65535) return WKV7_ERR_INVALID_ARG;  // grid y
@@ -542,7 +542,7 @@ wkv7_status wkv7_prefill_backward(int num_seqs, int T_total, int H, int N, const
     b.T_total = T_total;
     b.H = H;
     b.cu_seqlens = cu_seqlens;
-    b.x_dtype = x_dtype;
+    b.x_dtype = x_dtype == WKV7_TF32 ? WKV7_F32 : x_dtype;
     b.r = r; b.w = w; b.k = k; b.v = v; b.kk = kk; b.a = a;
     b.initial_state = initial_state;
     b.d_o = d_o;

@@ -252,6 +252,11 @@ __device__ __forceinline__ void handoff(uint32_t rdy) {
     if (threadIdx.x == 0) mbar_arrive(rdy);
 }
 
+// kF32In: r, k, v, kk, a are fp32 (contracted at tf32 like the rest).  Their tiles are twice
+// the size of bf16 tiles and do not fit beside the operand buffers, so only w is staged by TMA;
+// the other five are prefetched into L2 when w is requested and read from global memory where
+// the bf16 form reads its swizzled tiles.
+template <bool kF32In>
 __global__ void __launch_bounds__(kBlock, 1)
 wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps maps,
                             const __grid_constant__ SplitPlan plan) {
@@ -366,13 +371,45 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
 
     auto issue_tma = [&](int chunk) {
         const int y = bos + (c_begin + chunk) * kC, x = h * 64;
-        mbar_arrive_expect_tx(bar_tma, kTmaBytes);
-        tma_load_2d(sbase + SM_R, &maps.r, x, y, bar_tma);
-        tma_load_2d(sbase + SM_K, &maps.k, x, y, bar_tma);
-        tma_load_2d(sbase + SM_KK, &maps.kk, x, y, bar_tma);
-        tma_load_2d(sbase + SM_A, &maps.a, x, y, bar_tma);
-        tma_load_2d(sbase + SM_V, &maps.v, x, y, bar_tma);
+        if constexpr (kF32In) {
+            mbar_arrive_expect_tx(bar_tma, 16384u);
+            tma_prefetch_2d(&maps.r, x, y);
+            tma_prefetch_2d(&maps.k, x, y);
+            tma_prefetch_2d(&maps.kk, x, y);
+            tma_prefetch_2d(&maps.a, x, y);
+            tma_prefetch_2d(&maps.v, x, y);
+        } else {
+            mbar_arrive_expect_tx(bar_tma, kTmaBytes);
+            tma_load_2d(sbase + SM_R, &maps.r, x, y, bar_tma);
+            tma_load_2d(sbase + SM_K, &maps.k, x, y, bar_tma);
+            tma_load_2d(sbase + SM_KK, &maps.kk, x, y, bar_tma);
+            tma_load_2d(sbase + SM_A, &maps.a, x, y, bar_tma);
+            tma_load_2d(sbase + SM_V, &maps.v, x, y, bar_tma);
+        }
         tma_load_2d(sbase + SM_W, &maps.w, x, y, bar_tma);
+    };
+    // Channels i .. of row t of chunk `chunk` of an input: from its staged bf16 tile, or (fp32
+    // inputs) from global memory.
+    auto xrow = [&](const void *x, int chunk, int t) {
+        return static_cast<const float *>(x) + (static_cast<long long>(bos + (c_begin + chunk) * kC + t) * H + h) * 64;
+    };
+    auto in2 = [&](const unsigned char *tile, const void *x, int chunk, int t, int i) -> float2 {
+        if constexpr (kF32In) return __ldg(reinterpret_cast<const float2 *>(xrow(x, chunk, t) + i));
+        else return raw2(tile, t, i);
+    };
+    auto in4 = [&](const unsigned char *tile, const void *x, int chunk, int t, int i) -> float4 {
+        if constexpr (kF32In) return __ldg(reinterpret_cast<const float4 *>(xrow(x, chunk, t) + i));
+        else return raw4(tile, t, i);
+    };
+    auto in8 = [&](const unsigned char *tile, const void *x, int chunk, int t, int i, float *f) {
+        if constexpr (kF32In) {
+            const float4 *src = reinterpret_cast<const float4 *>(xrow(x, chunk, t) + i);
+            const float4 u0 = __ldg(src), u1 = __ldg(src + 1);
+            f[0] = u0.x; f[1] = u0.y; f[2] = u0.z; f[3] = u0.w;
+            f[4] = u1.x; f[5] = u1.y; f[6] = u1.z; f[7] = u1.w;
+        } else {
+            raw8(tile, t, i, f);
+        }
     };
     auto chunk_len = [&](int chunk) { return min(kC, eos - (bos + (c_begin + chunk) * kC)); };
 
@@ -427,7 +464,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
     // ---- phase 2: A_G = [R ; Q] into TMEM; the Gram B operand B_G = [C ; K] (rows s, 64 + s),
     // C[s][i] = kk a e^{g_ref - g_s}, K[s][i] = k e^{g_ref - g_s}, with e^{g_ref - g_s} = 1 / E[s][i].
     // Rows past the chunk's end are zero.
-    auto phase2 = [&](int lc, const float *eref) {
+    auto phase2 = [&](int chunk, int lc, const float *eref) {
         {   // B_G: thread = row t, channels 4 cq .. 4 cq + 3 and 32 + 4 cq .. 32 + 4 cq + 3, so that
             // each 8- or 16-byte access of a quarter-warp (one row) covers 8 distinct bank groups
             const int t = tid >> 3, cq = tid & 7;
@@ -437,7 +474,8 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int c4 = 4 * cq + 32 * h;
-                    const float4 kkv = raw4(rkk, t, c4), av = raw4(ra, t, c4), kv = raw4(rk, t, c4);
+                    const float4 kkv = in4(rkk, p.kk, chunk, t, c4), av = in4(ra, p.a, chunk, t, c4),
+                                 kv = in4(rk, p.k, chunk, t, c4);
                     const float4 e = *reinterpret_cast<const float4 *>(E + eidx(t, c4));
                     const float2 e0 = make_float2(rcp(e.x), rcp(e.y)), e1 = make_float2(rcp(e.z), rcp(e.w));
                     const float2 c0 = __fmul2_rn(__fmul2_rn(make_float2(kkv.x, kkv.y), make_float2(av.x, av.y)), e0);
@@ -463,8 +501,8 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
             uint32_t wds[16];
             if (t < lc) {
                 float x[16];
-                raw8(rrow ? rr : rkk, t, i0, x);
-                raw8(rrow ? rr : rkk, t, i0 + 8, x + 8);
+                in8(rrow ? rr : rkk, rrow ? p.r : p.kk, chunk, t, i0, x);
+                in8(rrow ? rr : rkk, rrow ? p.r : p.kk, chunk, t, i0 + 8, x + 8);
 #pragma unroll
                 for (int j = 0; j < 16; j += 4) {
                     float4 e;
@@ -494,13 +532,13 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
     // V^T into B_chain (K 64..127)
     // Thread: columns j, j+1 (j even) of tokens s0 .. s0+3.  Half the lanes store row j first,
     // half row j+1, so each quarter-warp's 16-byte stores land in 8 distinct bank groups.
-    auto write_vt = [&](int lc) {
+    auto write_vt = [&](int chunk, int lc) {
         if (kind == kItemTransfer) lc = 0;  // v = 0
         const int j = 2 * (tid & 31), s0 = 4 * (tid >> 5);
         float a0[4], a1[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const float2 x = s0 + e < lc ? raw2(rv, s0 + e, j) : make_float2(0.f, 0.f);
+            const float2 x = s0 + e < lc ? in2(rv, p.v, chunk, s0 + e, j) : make_float2(0.f, 0.f);
             a0[e] = x.x;
             a1[e] = x.y;
         }
@@ -637,8 +675,8 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
             for (int j = 0; j < 16; ++j)
                 *reinterpret_cast<uint32_t *>(sm + SM_BC + sw128_off(16 * cg + j, si, 64)) = to_tf32(s[j] * er);
         }
-        phase2(chunk_len(0), EREF);
-        write_vt(chunk_len(0));
+        phase2(0, chunk_len(0), EREF);
+        write_vt(0, chunk_len(0));
         handoff(rdy_g);
         if (tid == 0 && nchunks > 1) issue_tma(1);  // chunk 0's tiles are no longer read
         alive = wait_uniform(bar_g, 0, p.status);
@@ -848,7 +886,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
             if (!wait_uniform(bar_tma, static_cast<uint32_t>((c + 1) & 1), p.status)) { alive = false; break; }
             phase1(chunk_len(c + 1), (c + 1) & 1);
             wsync();
-            phase2(chunk_len(c + 1), EREF + ((c + 1) & 1) * 64);
+            phase2(c + 1, chunk_len(c + 1), EREF + ((c + 1) & 1) * 64);
             handoff(rdy_g);  // -> the next chunk's Gram products
         }
         if (!wait_uniform(bar_d, par, p.status)) { alive = false; break; }
@@ -908,7 +946,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
                     *reinterpret_cast<uint32_t *>(sm + SM_BC + sw128_off(16 * cg + j, si, 64)) = to_tf32(s[j] * ern);
                 }
             }
-            if (has_next) write_vt(chunk_len(c + 1));
+            if (has_next) write_vt(c + 1, chunk_len(c + 1));
         }
         sync_for_mma();
         if (tid == 0) mbar_arrive(rdy_t);  // -> the output stores and the tiles of chunk c + 2
@@ -1342,11 +1380,14 @@ bool plan_split(const PrefillArgs &a, unsigned char *split_ws, size_t split_byte
 
 cudaError_t launch_chunked(const PrefillArgs &args, unsigned char *split_ws, size_t split_bytes, cudaStream_t stream) {
     TensorMaps maps;
-    if (!make_map(&maps.r, args.r, true, args.T_total, args.H) ||
-        !make_map(&maps.k, args.k, true, args.T_total, args.H) ||
-        !make_map(&maps.v, args.v, true, args.T_total, args.H) ||
-        !make_map(&maps.kk, args.kk, true, args.T_total, args.H) ||
-        !make_map(&maps.a, args.a, true, args.T_total, args.H) ||
+    // bf16 inputs: swizzled 64 x 64 boxes staged in shared memory; fp32 inputs: plain 64 x 64
+    // fp32 boxes, used only for the L2 prefetch
+    const bool bf16_in = args.x_dtype == WKV7_BF16;
+    if (!make_map(&maps.r, args.r, bf16_in, args.T_total, args.H) ||
+        !make_map(&maps.k, args.k, bf16_in, args.T_total, args.H) ||
+        !make_map(&maps.v, args.v, bf16_in, args.T_total, args.H) ||
+        !make_map(&maps.kk, args.kk, bf16_in, args.T_total, args.H) ||
+        !make_map(&maps.a, args.a, bf16_in, args.T_total, args.H) ||
         !make_map(&maps.w, args.w, false, args.T_total, args.H) || !make_out_map(&maps.o, args.o, args.T_total, args.H, args.o_dtype == WKV7_BF16))
         return cudaErrorInvalidValue;
     SplitPlan plan;
@@ -1354,18 +1395,21 @@ cudaError_t launch_chunked(const PrefillArgs &args, unsigned char *split_ws, siz
     const bool split = plan_split(args, split_ws, split_bytes, plan, fix);
     if (split && !make_ohat_map(&maps.ohat, plan.ohat, static_cast<long long>((split_bytes - kSlotsBytes) / 256) & ~63ll))
         return cudaErrorInvalidValue;
-    static int attr_dev = -1;
+    static int attr_dev[2] = {-1, -1};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (attr_dev != dev) {
-        e = cudaFuncSetAttribute(wkv7_prefill_chunked_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemAlloc);
+    if (attr_dev[bf16_in] != dev) {
+        e = cudaFuncSetAttribute(bf16_in ? wkv7_prefill_chunked_kernel<false> : wkv7_prefill_chunked_kernel<true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
         if (e != cudaSuccess) return e;
-        attr_dev = dev;
+        attr_dev[bf16_in] = dev;
     }
-    wkv7_prefill_chunked_kernel<<<static_cast<unsigned>(plan.main_items + plan.n_items), kBlock, kSmemAlloc, stream>>>(
-        args, maps, plan);
+    const unsigned grid = static_cast<unsigned>(plan.main_items + plan.n_items);
+    if (bf16_in)
+        wkv7_prefill_chunked_kernel<false><<<grid, kBlock, kSmemAlloc, stream>>>(args, maps, plan);
+    else
+        wkv7_prefill_chunked_kernel<true><<<grid, kBlock, kSmemAlloc, stream>>>(args, maps, plan);
     e = cudaGetLastError();
     if (e != cudaSuccess || !split) return e;
     wkv7_prefill_split_chain_kernel<<<fix.n_pairs, kChainThreads, 0, stream>>>(fix, args.final_state, args.state_dtype,
@@ -1397,7 +1441,7 @@ size_t prefill_workspace_bytes(int num_seqs, int T_total, int H) {
 }
 
 bool prefill_wants_order(const PrefillArgs &args) {
-    if (args.num_seqs < 2 || args.num_seqs > kMaxOrdered || args.x_dtype != WKV7_BF16) return false;
+    if (args.num_seqs < 2 || args.num_seqs > kMaxOrdered || args.x_dtype == WKV7_F32) return false;
     int len0 = 0, len = 0;
     if (!host_seq_len(args, 0, len0)) return true;  // lengths unknown on the host: sort on the device
     for (int b = 1; b < args.num_seqs; ++b)
@@ -1420,9 +1464,9 @@ cudaError_t launch_prefill(const PrefillArgs &args, void *workspace, size_t work
         if (args.initial_state == args.final_state) return cudaSuccess;
         return cudaMemcpyAsync(args.final_state, args.initial_state, state_bytes, cudaMemcpyDeviceToDevice, stream);
     }
-    // bf16 inputs (the prefill format) take the chunked tensor-core kernel;
-    // fp32 inputs take the exact token-serial kernel.
-    if (args.x_dtype == WKV7_BF16) {
+    // bf16 inputs (the prefill format) and fp32 inputs marked for tf32 contraction take the
+    // chunked tensor-core kernel; plain fp32 inputs take the exact token-serial kernel.
+    if (args.x_dtype == WKV7_BF16 || args.x_dtype == WKV7_TF32) {
         const size_t head = prefill_workspace_min_bytes(args.num_seqs);
         unsigned char *split_ws = workspace && workspace_bytes > head ? static_cast<unsigned char *>(workspace) + head : nullptr;
         return launch_chunked(args, split_ws, split_ws ? workspace_bytes - head : 0, stream);

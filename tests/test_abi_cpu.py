@@ -106,6 +106,22 @@ def _prefill(lib, num_seqs=2, T=10, H=2, N=64, cu_host=None, dtype=_lib.BF16, pt
 def test_prefill_rejects_unsupported(lib):
     assert _prefill(lib, N=48) == _lib.ERR_UNSUPPORTED
     assert _prefill(lib, dtype=7) == _lib.ERR_UNSUPPORTED
+    assert _prefill(lib, dtype=_lib.F16) == _lib.ERR_UNSUPPORTED  # 16-bit inputs are bf16 only
+
+
+def test_prefill_tf32_inputs_are_four_bytes(lib):
+    """x_dtype WKV7_TF32 (fp32 inputs through the chunked kernel) passes the host
+    checks with 4-byte elements: an output placed right after a bf16-sized r
+    overlaps an fp32 r."""
+    T, H = 10, 2
+    ptrs = [FAKE + i * (1 << 26) for i in range(8)]
+    ptrs[7] = ptrs[1] + T * H * 64 * 2  # o right after r's first T*H*64*2 bytes
+    assert _prefill(lib, T=T, H=H, ptrs=ptrs, cu_host=[0, 4, 10], dtype=_lib.TF32) == _lib.ERR_INVALID_ARG
+    assert _prefill(lib, T=T, H=H, ptrs=ptrs, cu_host=[0, 4, 10], dtype=_lib.F32) == _lib.ERR_INVALID_ARG
+    assert _prefill(lib, T=T, H=H, ptrs=ptrs, cu_host=[0, 4, 10], dtype=_lib.BF16) != _lib.ERR_INVALID_ARG
+    bad = [FAKE + i * (1 << 26) for i in range(8)]
+    bad[3] += 4
+    assert _prefill(lib, ptrs=bad, cu_host=[0, 4, 10], dtype=_lib.TF32) == _lib.ERR_ALIGNMENT
 
 
 def test_prefill_rejects_malformed_host_cu_seqlens(lib):
