@@ -30,9 +30,13 @@
 // In between (e.g. 1280 heads: 9.25 vs 10.03 us) the ring is faster.
 //
 // Launch order: programmatic dependent launch.  The kernel waits for the
-// preceding grid (griddepcontrol.wait) before it touches global memory, so
-// back-to-back calls on the same state stay ordered, while the launch and
-// block scheduling of the next call overlap the tail of this one.
+// preceding grid (griddepcontrol.wait) before it loads anything from global
+// memory, so back-to-back calls on the same state stay ordered, while the
+// launch and block scheduling of the next call overlap the tail of this one.
+// Before the wait a block only issues L2 prefetches of the heads it will load
+// first: they start the HBM reads during the preceding grid's tail, and since
+// L2 is the point of coherence the loads after the wait still see every write
+// of that grid.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -172,12 +176,22 @@ wkv7_step_kernel(long long n_heads, const float *__restrict__ r, const float *__
     unsigned long long *full = reinterpret_cast<unsigned long long *>(smem + kStages * sizeof(StageX));
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-    // Nothing in global memory is touched before the preceding grid is done.
-    grid_dep_wait();
-
     const long long first = blockIdx.x, stride = gridDim.x;
     const long long count = n_heads > first ? (n_heads - 1 - first) / stride + 1 : 0;
     const float *const vsrc[6] = {r, w, k, v, kk, a};
+
+    // While the preceding grid finishes, its tail overlaps with L2 prefetches of the heads
+    // this block loads first (prefetches read nothing into the block and L2 is coherent
+    // with that grid's writes).  Nothing is loaded before the preceding grid is done.
+    if (tid == 0) {
+        for (long long idx = 0; idx < count && idx < kStages; ++idx) {
+            const long long head = first + idx * stride;
+            bulk_prefetch_l2(state + head * (kN * kN), kStBytes);
+#pragma unroll
+            for (int i = 0; i < 6; ++i) bulk_prefetch_l2(vsrc[i] + head * kN, kVecBytes);
+        }
+    }
+    grid_dep_wait();
     auto issue = [&](long long idx) {
         const long long head = first + idx * stride;
         const int s = static_cast<int>(idx % kStages);
@@ -342,9 +356,17 @@ wkv7_step_regs_kernel(long long n_units, const float *__restrict__ r, const floa
                       const float *__restrict__ kk, const float *__restrict__ a,
                       float *__restrict__ state, OutT *__restrict__ o, TailArgs tail) {
     __shared__ float red[8];  // a block is the four slices of one head
-    grid_dep_wait();
     const int lane = threadIdx.x & 31;
     const long long unit = static_cast<long long>(blockIdx.x) * kRegWarps + (threadIdx.x >> 5);
+    // L2 prefetch of this block's head while the preceding grid finishes (as in the ring form)
+    if (threadIdx.x == 0 && unit < n_units) {
+        const long long hd = unit >> 2;
+        bulk_prefetch_l2(state + hd * (kN * kN), kN * kN * 4);
+        const float *const vsrc[6] = {r, w, k, v, kk, a};
+#pragma unroll
+        for (int i = 0; i < 6; ++i) bulk_prefetch_l2(vsrc[i] + hd * kN, kVecBytes);
+    }
+    grid_dep_wait();
     if (unit >= n_units) return;
     const long long head = unit >> 2;
     const int slice = static_cast<int>(unit & 3);
@@ -354,6 +376,8 @@ wkv7_step_regs_kernel(long long n_units, const float *__restrict__ r, const floa
     float4 x[8];
 #pragma unroll
     for (int m = 0; m < 8; ++m) x[m] = *reinterpret_cast<const float4 *>(S + m * kN);
+    // the next grid may be scheduled once every block has its state (triggering at the
+    // start instead: B = 8 on the 2.9B geometry 3.10 -> 3.93 us)
     grid_dep_launch();
     const long long vb = head * kN + row0;
     const float4 r0 = __ldg(reinterpret_cast<const float4 *>(r + vb)), r1 = __ldg(reinterpret_cast<const float4 *>(r + vb + 4));
