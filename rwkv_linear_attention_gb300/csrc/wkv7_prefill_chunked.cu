@@ -17,32 +17,35 @@
 //   O = Ra S0 + M_k V - M_c Z,               Ra[t,i] = r_t[i] e^{g_t[i]}
 //   S_C = diag(e^{g_C}) S0 + Kb^T V - Cb^T Z,   Kb[s,i] = k_s[i] e^{g_C[i]-g_s[i]}, Cb likewise
 //
-// Substituting Z and folding every state-independent product gives one
-// matrix product per chunk on the state's critical path:
+// In block form, with W = Qa S0 + L_k V (= T^{-1} Z, which needs no inverse):
 //
-//   [ O                  ]   [ Ra - Mt Qa | M_k - Mt L_k  ]   [ S0 ]
-//   [ S_C - e^{g_C} * S0 ] = [ -Ct Qa     | Kb^T - Ct L_k ] . [ V  ]      (A_chain)
+//   [ O                  ]   [ Ra | M_k  ]   [ S0 ]   [ M_c  ]
+//   [ S_C - e^{g_C} * S0 ] = [ 0  | Kb^T ] . [ V  ] - [ Cb^T ] . T W
 //
-// with [Mt ; Ct] = [M_c ; Cb^T] T.  Every row i of the lower half carries the
-// factor e^{g_C - g_ref}[i] (Cb^T = diag(e^{g_C - g_ref}) C^T, likewise Kb^T);
-// the kernel keeps the lower half without it and applies it to the state rows
-// of the product.  Every S0 column i of A_chain carries the factor e^{g_ref}[i]
-// (Ra = R diag(e^{g_ref}), Qa = Q diag(e^{g_ref}), with R and Q the Gram
-// operands below); the kernel keeps those columns without it and scales the
-// rows of the state operand instead, S0' = diag(e^{g_ref}) S0.  Per chunk these
-// tf32 MMAs run, all with M = 128, fp32 accumulators in tensor memory and the A
-// operand read from tensor memory:
-//   G       = [R ; Q] [C ; K]^T                 (the four Gram blocks; 128x128x64)
-//   X       = [M_c ; C^T] T                      (three small products, see phase 4)
-//   A_chain = base - X [Q | L_k]                 (accumulated onto base = [R | M_k ; 0 | K^T]; 128x128x64)
-//   D       = A_chain [S0' ; V]                  (128x64x128)
+// Every row i of the lower half carries the factor e^{g_C - g_ref}[i]
+// (Cb^T = diag(e^{g_C - g_ref}) C^T, likewise Kb^T); the kernel keeps the lower
+// half without it and applies it to the state rows of the product.  Every S0
+// column i carries the factor e^{g_ref}[i] (Ra = R diag(e^{g_ref}),
+// Qa = Q diag(e^{g_ref}), with R and Q the Gram operands below); the kernel
+// keeps those columns without it and scales the rows of the state operand
+// instead, S0' = diag(e^{g_ref}) S0.  Per chunk these tf32 MMAs run, all with
+// M = 128, fp32 accumulators in tensor memory and the A operand read from
+// tensor memory:
+//   G = [R ; Q] [C ; K]^T                (the four Gram blocks; 128x128x64)
+//   W = [R | M_k ; Q | L_k] [S0' ; V]    (rows 64..127 are W, rows 0..63 are not used,
+//                                         their M_k unmasked; 128x64x128, needs no T)
+//   X = [M_c ; C^T] T                    (three small products, see phase 4)
+//   D = [R | M_k ; 0 | K^T] [S0' ; V] - X W   (128x64x128, then 128x64x64)
+// so after the T halves only X and the last K = 64 product remain on the
+// critical path, and no intermediate carries the e^{64|w|} of the chunk's
+// removal block C^T T Q (which the transition contains but no product forms).
 // C^T and K^T (the lower lanes of A_X and of the base) are copied from the Gram
 // B operand [C ; K] in shared memory into tensor memory by threads, and R (the
 // base's upper left block) from the Gram A operand.
 // The SIMT work (cumulative decay, exponentials, masks, the blocked 64x64
 // unit-lower-triangular inverse, operand staging) is software-pipelined with
 // the MMAs: the next chunk's decay and Gram operands are built while this
-// chunk's X and A_chain products run, and the next chunk's Gram product runs
+// chunk's X and D products run, and the next chunk's Gram product runs
 // while this chunk's outputs are written.  A dedicated warp issues every MMA and
 // every TMA copy (input tiles a chunk ahead, output stores), so no worker
 // thread stalls on an issue queue.  One CTA (512 threads) owns one
@@ -53,8 +56,8 @@
 // bank conflicts); a chunk's tiles are requested as soon as the previous
 // chunk's are consumed, a full chunk before they are needed.
 //
-// Inputs r, k, v, kk, a are bf16 (w fp32); fp32-input prefill is served by
-// the token-serial kernel instead.
+// Inputs r, k, v, kk, a are bf16, or fp32 (then read from global memory after
+// an L2 prefetch, see kF32In); w is fp32.
 //
 // Precision: inputs are used exactly; operands staged by threads are rounded
 // to tf32 (to nearest); operands that one MMA hands to the next stay in
@@ -83,14 +86,17 @@ constexpr int kThreads = 512;   // worker warps w < 16: TMEM lane quarter w % 4,
 constexpr int kBlock = kThreads + 32;  // + one warp that issues every MMA and TMA copy
 constexpr uint32_t kMaxPolls = 1u << 24;
 
-// TMEM columns.  A_X and A_chain are apart, so A_chain's whole base can be
-// written before the X products (which consume A_X) run, and X, A_chain and D
-// follow one another on the tensor core without a handoff from the workers.
+// TMEM columns.  The chunk's outputs and state increment are
+//   D = base [S0' ; V] - X W,   base = [R | M_k ; 0 | K^T],  X = [M_c ; Cb^T] T,
+//   W = [Q | L_k] [S0' ; V]  (= Q S0' + L_k V, rows 64..127 of an M = 128 product),
+// so W needs no T and runs while the T halves are formed; after them only X and
+// one K = 64 product remain on the tensor core.  W is written over G's first 64
+// columns once they are read, with L_k masked in place beside it as its A operand.
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColG = 0;     // G
+constexpr uint32_t kColG = 0;     // G; then W in its columns 0..63 (A operand [Q | L_k]: A_G, G 64..127)
 constexpr uint32_t kColX = 128;   // X = [Mt ; Ct]
 constexpr uint32_t kColAX = 192;  // A_X = [M_c ; C^T], the A operand of X (64 columns)
-constexpr uint32_t kColAC = 256;  // A_chain (128 columns: the S0 block, then the V block)
+constexpr uint32_t kColAC = 256;  // the base [R | M_k ; 0 | K^T] (128 columns: the S0 block, then the V block)
 constexpr uint32_t kColAG = 384;  // A operand of G = [R ; Q] (for the next chunk)
 constexpr uint32_t kColD = 448;   // D = [O ; S_C - e^{g_C} S0]
 static_assert(kColX == kColG + 128 && kColAX == kColX + 64 && kColAC == kColAX + 64 && kColAG == kColAC + 128 &&
@@ -104,7 +110,7 @@ constexpr int kTile = 64 * 64 * 2;  // one bf16 raw tile
 constexpr int SM_R = 0, SM_K = SM_R + kTile, SM_KK = SM_K + kTile, SM_A = SM_KK + kTile, SM_V = SM_A + kTile;
 constexpr int SM_W = SM_V + kTile;         // fp32 w tile -> E = e^{g - g_ref} (swizzled)
 constexpr int SM_BG = SM_W + 16384;        // B operand of G: [C ; K]  (128 x K64)
-constexpr int SM_BY = SM_BG + 32768;       // B operand of A_chain: [Q^T ; L_k^T] (128 x K64)
+constexpr int SM_BY = SM_BG + 32768;       // B operand of the last product: W^T (64 x K64; 32 KB reserved)
 constexpr int SM_BX = SM_BY + 32768;       // B operand of X: T^T (64 x K64)
 constexpr int SM_BC = SM_BX + 16384;       // B operand of D: [S0'^T | V^T] (64 x K128)
 constexpr int SM_LC = SM_BC + 32768;       // fp32 L_c^T [64][kLd]
@@ -352,6 +358,8 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
     // waiter never misses a phase.
     const uint32_t bar_tma = sbase + SM_BAR, bar_g = bar_tma + 8, bar_d = bar_tma + 16, bar_i = bar_tma + 24;
     const uint32_t rdy_x = bar_tma + 32, rdy_g = bar_tma + 40, rdy_t = bar_tma + 48;
+    const uint32_t rdy_w = bar_tma + 56, bar_w = bar_tma + 64;  // W's operands ready; W complete
+    const uint32_t rdy_b = bar_tma + 72;                        // the base [R | M_k ; 0 | K^T] ready
 
     if (tid == 0) {
         mbar_init(bar_tma, 1);
@@ -361,6 +369,9 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
         mbar_init(rdy_x, 1);
         mbar_init(rdy_g, 1);
         mbar_init(rdy_t, 1);
+        mbar_init(rdy_w, 1);
+        mbar_init(bar_w, 1);
+        mbar_init(rdy_b, 1);
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(sbase + SM_SLOT, kTmemCols);
@@ -436,10 +447,13 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
         *reinterpret_cast<float2 *>(TOT + seg * 64 + ch) = acc;
         wsync();
         float2 pre = make_float2(0.f, 0.f);
-        for (int u = 0; u < seg; ++u) {
-            const float2 tv = *reinterpret_cast<const float2 *>(TOT + u * 64 + ch);
-            pre.x += tv.x;
-            pre.y += tv.y;
+#pragma unroll
+        for (int u = 0; u < 15; ++u) {  // unrolled, so that the loads issue back to back
+            if (u < seg) {
+                const float2 tv = *reinterpret_cast<const float2 *>(TOT + u * 64 + ch);
+                pre.x += tv.x;
+                pre.y += tv.y;
+            }
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -551,10 +565,10 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
         }
     };
 
-    // Gram product G = [R ; Q] [C ; K]^T.  The lower half of A_chain takes [C^T | K^T]
-    // (copied in phase 4): Cb^T and Kb^T without their row factor e^{g_C - g_ref}[i]
-    // (Cb^T[i][s] = e^{g_C - g_ref}[i] C[s][i]).  That factor multiplies every row of the
-    // lower half of A_chain, so it is applied to the state rows of D instead.
+    // Gram product G = [R ; Q] [C ; K]^T.  The lower halves of A_X and of the base take
+    // [C^T | K^T] (copied in phase 4): Cb^T and Kb^T without their row factor
+    // e^{g_C - g_ref}[i] (Cb^T[i][s] = e^{g_C - g_ref}[i] C[s][i]).  That factor multiplies
+    // every lower row of D's operands, so it is applied to the state rows of D instead.
     auto issue_gram = [&]() {
 #pragma unroll
         for (int kq = 0; kq < 8; ++kq)
@@ -590,7 +604,24 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
             for (int c = 0; c < nchunks && ok; ++c) {
                 const bool has_next = c + 1 < nchunks;
                 const uint32_t par = static_cast<uint32_t>(c & 1);
-                // X = [M_c ; Cb^T] T in three products (A_X lives in A_chain's columns 0..63):
+                // W = [Q | L_k] [S0' ; V] over G's columns 0..63 (rows 0..63 of that product are
+                // not used): as soon as G is read and L_k masked in place
+                if (!(ok = ready(rdy_w, par))) break;
+#pragma unroll
+                for (int kq = 0; kq < 16; ++kq)
+                    mma_tf32_tmem_a(tmem + kColG, tmem + (kq < 8 ? kColAG + 8 * kq : kColG + 64 + 8 * (kq - 8)),
+                                    sdesc_sw128(sbase + SM_BC + (kq >> 2) * 64 * 128 + (kq & 3) * 32),
+                                    idesc_tf32(128, 64), kq > 0);
+                mma_commit(bar_w);
+                // D = base [S0' ; V] as soon as the base is written (it needs no T either), so that
+                // only X and D -= X W follow the T halves on the tensor core
+                if (!(ok = ready(rdy_b, par))) break;
+#pragma unroll
+                for (int kq = 0; kq < 16; ++kq)
+                    mma_tf32_tmem_a(tmem + kColD, tmem + kColAC + 8 * kq,
+                                    sdesc_sw128(sbase + SM_BC + (kq >> 2) * 64 * 128 + (kq & 3) * 32),
+                                    idesc_tf32(128, 64), kq > 0);
+                // X = [M_c ; Cb^T] T in three products:
                 //   X_R = B_R T_B -> X[:, 32:64);  B_L -= X_R L_BA (in place);  X_L = B_L T_A -> X[:, 0:32)
                 if (!(ok = ready(rdy_x, par))) break;
 #pragma unroll
@@ -612,20 +643,12 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
                                     idesc_tf32(128, 32), kq > 0);
                 mma_commit(bar_i);
                 if (!(ok = wait_own())) break;
-                // A_chain -= X [Q | L_k]  (negated A, accumulating onto the base [R | M_k ; 0 | K^T])
+                // D -= X W  (negated A, accumulating onto base [S0' ; V])
 #pragma unroll
                 for (int kq = 0; kq < 8; ++kq)
-                    mma_tf32_tmem_a(tmem + kColAC, tmem + kColX + 8 * kq,
-                                    sdesc_sw128(sbase + SM_BY + (kq >> 2) * 128 * 128 + (kq & 3) * 32),
-                                    idesc_tf32(128, 128) | kIdescNegateA, 1);
-                mma_commit(bar_i);
-                if (!(ok = wait_own())) break;
-                // D = A_chain [S0' ; V]
-#pragma unroll
-                for (int kq = 0; kq < 16; ++kq)
-                    mma_tf32_tmem_a(tmem + kColD, tmem + kColAC + 8 * kq,
-                                    sdesc_sw128(sbase + SM_BC + (kq >> 2) * 64 * 128 + (kq & 3) * 32),
-                                    idesc_tf32(128, 64), kq > 0);
+                    mma_tf32_tmem_a(tmem + kColD, tmem + kColX + 8 * kq,
+                                    sdesc_sw128(sbase + SM_BY + (kq >> 2) * 64 * 128 + (kq & 3) * 32),
+                                    idesc_tf32(128, 64) | kIdescNegateA, 1);
                 // the previous chunk's output stores have read the staging tile, so D's completion
                 // also tells the workers that they may stage this chunk's outputs
                 bulk_wait_read<0>();
@@ -689,13 +712,14 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
         const bool has_next = c + 1 < nchunks;
         const uint32_t par = static_cast<uint32_t>(c & 1);
 
-        // ---- phase 3: read G.  M_c (masked) -> A_chain columns 0..63 of rows t, which with
-        // Cb^T below them (phase 4) form A_X = [M_c ; Cb^T]; M_k (masked) -> A_chain rows t,
-        // K 64..; L_c^T -> LT; L_k^T -> B_Y (16 + 16 columns per lower-lane warp).  The two
-        // warps that compute the T halves (0, 1) take no part: the lower-lane warps signal them
-        // as soon as L_c^T is written (named barrier 2: 256 arrivals + their 64), so the
-        // inverse starts while the rest of this phase runs, and warps 12, 13 take their share
-        // of M_c.  The others finish the phase on named barrier 3 (448 threads).
+        // ---- phase 3: read G.  M_c (masked) -> A_X rows t, which with Cb^T below them
+        // (phase 4) form A_X = [M_c ; Cb^T]; M_k (masked) -> the base's rows t, K 64..;
+        // L_c^T -> LT; L_k masked in place (G columns 64..127, rows 64..127: W's A operand
+        // beside A_G's Q), 16 + 16 columns per lower-lane warp.  The two warps that compute
+        // the T halves (0, 1) take no part: the lower-lane warps signal them as soon as L_c^T
+        // is written (named barrier 2: 256 arrivals + their 64), so the inverse starts while
+        // the rest of this phase runs, and warps 12, 13 take their share of M_c.  The others
+        // finish the phase on named barrier 3 (448 threads) and hand W's operands over.
         if (q < 2) {
             if (warp >= 2) {
 #pragma unroll 1
@@ -722,10 +746,10 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
             for (int j = 0; j < 16; ++j) LTw[(s0 + j) * kLd + t] = s0 + j < t ? v[j] : 0.f;
             named_arrive<2, 256 + 64>();  // -> the T halves
             tmem_ld16(tmem + lane_off + kColG + 64 + s0, v);
-            unsigned char *BY = sm + SM_BY;
+            uint32_t lw[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-                *reinterpret_cast<uint32_t *>(BY + sw128_off(64 + s0 + j, t, 128)) = to_tf32(s0 + j < t ? v[j] : 0.f);
+            for (int j = 0; j < 16; ++j) lw[j] = to_tf32(s0 + j < t ? v[j] : 0.f);
+            tmem_st16(tmem + lane_off + kColG + 64 + s0, lw);
         }
         if (warp < 2) {
             named_sync<2, 256 + 64>();  // L_c^T written
@@ -734,6 +758,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
             tc_fence_before_sync();
             named_sync<3, kThreads - 64>();
             tc_fence_after_sync();
+            if (tid == 64) mbar_arrive(rdy_w);  // -> W = [Q | L_k] [S0' ; V]
         }
 
         // ---- phase 4: the two 32x32 diagonal halves of T = (I + L_c)^{-1}, in fp32, one warp
@@ -745,11 +770,11 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
         //   X_R = B_R T_B,   X_L = (B_L - X_R L_BA) T_A
         // are three small MMAs.  Their B operands T_B^T, L_BA^T, T_A^T go to B_X
         // (B[n][k] = M[k][n]); the warps of the other two sub-partitions (warp % 4 = 2, 3)
-        // meanwhile copy Q^T and [C^T | K^T] and stage L_BA^T, so the two inverse warps
-        // issue unhindered, and warps 4, 5, 8, 9 copy R into A_chain's S0 block.  With
-        // that, every operand of X, A_chain and D is in place at the end of this phase: the
-        // MMA warp runs the three without another handoff while the workers go on to the
-        // next chunk.
+        // meanwhile copy [C^T | K^T], stage L_BA^T and, once W is complete, W^T, so the two
+        // inverse warps issue unhindered, and warps 4, 5, 8, 9 copy R into the base's S0
+        // block.  With that, every operand of X, D = base [S0' ; V] and D -= X W is in place
+        // at the end of this phase: the MMA warp runs them without another handoff while the
+        // workers go on to the next chunk.
         {
             const float *LT = reinterpret_cast<const float *>(sm + SM_LC);
             if (warp < 2) {
@@ -831,7 +856,7 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
                 }
             } else if (!(warp & 2)) {
                 // warps 4, 5 and 8, 9: the base's R block (this chunk's Gram A operand, upper
-                // lanes) into A_chain's S0 columns
+                // lanes) into the base's S0 columns
                 if (cg < 3) {
                     const int c0 = 32 * (cg - 1);
                     float v[32];
@@ -842,17 +867,11 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
                     tmem_st32_issue(tmem + lane_off + kColAC + c0, wds);
                     tmem_wait_st();
                 }
+                tc_fence_before_sync();
+                named_sync<3, kThreads - 64>();  // the base is written
             } else {
                 const int sidx = (((warp >> 2) << 1) | (warp & 1)) * 32 + lane;
-                {   // Q^T into B_Y rows 0..63: B[i][t] = Q[t][i], the tf32 words of the Gram A operand's lower half
-                    const int t = m - 64;
-                    float v[16];
-                    tmem_ld16(tmem + lane_off + kColAG + 16 * cg, v);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        *reinterpret_cast<uint32_t *>(sm + SM_BY + sw128_off(16 * cg + j, t, 128)) = __float_as_uint(v[j]);
-                }
-                {   // [C^T | K^T] into A_chain lanes 64..127 (row i = m - 64, columns s = 16 cg ..):
+                {   // [C^T | K^T] into A_X and base lanes 64..127 (row i = m - 64, columns s = 16 cg ..):
                     // the tf32 words of B_G with the rounding bits cleared, i.e. exactly the
                     // product of the identity with B_G
                     const int i = m - 64;
@@ -872,16 +891,33 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
                     for (int j = 0; j < 16; ++j) z[j] = 0u;
                     tmem_st16(tmem + lane_off + kColAC + 16 * cg, z);
                 }
+                tc_fence_before_sync();
+                named_sync<3, kThreads - 64>();  // the base is written
+                if (tid == 64) {
+                    tc_fence_after_sync();
+                    mbar_arrive(rdy_b);  // -> D = base [S0' ; V]
+                }
                 {   // L_BA^T: B[n][k] = L_c[32 + k][n] = LT[n][32 + k]
                     const int n = sidx >> 3, k0 = 4 * (sidx & 7);
                     const float4 l = *reinterpret_cast<const float4 *>(LT + n * kLd + 32 + k0);
                     st_tf32x4(sm + SM_BX + 4096 + sw128_off(n, k0, 32), l.x, l.y, l.z, l.w);
                 }
+                {   // W^T into B_Y (B[n][t] = W[t][n]) once the product is complete.  A wait that
+                    // runs out is reported; the block then stops at its next uniform wait.
+                    if (!mbar_wait_bounded(bar_w, par, kMaxPolls)) report(p.status, kDevTimeout);
+                    tc_fence_after_sync();
+                    const int t = m - 64;
+                    float v[16];
+                    tmem_ld16(tmem + lane_off + kColG + 16 * cg, v);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        *reinterpret_cast<uint32_t *>(sm + SM_BY + sw128_off(16 * cg + j, t, 64)) = to_tf32(v[j]);
+                }
             }
         }
         handoff(rdy_x);  // -> X = [M_c ; Cb^T] T
 
-        // ---- next chunk, phases 1 and 2 (overlap the X, A_chain and D products)
+        // ---- next chunk, phases 1 and 2 (overlap the X and D products)
         if (has_next) {
             if (!wait_uniform(bar_tma, static_cast<uint32_t>((c + 1) & 1), p.status)) { alive = false; break; }
             phase1(chunk_len(c + 1), (c + 1) & 1);

@@ -50,6 +50,9 @@ wkv7_verify_kernel(int B, int T, int H, const float *__restrict__ r, const float
     const long long head = blockIdx.x;  // b * H + h
     const long long b = head / H, h = head % H;
 
+    // L2 prefetch of the head's state while the preceding grid finishes (L2 is coherent with
+    // that grid's writes); nothing is loaded before it is done
+    if (tid == 0) bulk_prefetch_l2(state + head * (kN * kN), kN * kN * 4);
     grid_dep_wait();
     if (tid == 0) {
         mbar_init(smem_addr(bar), 1);
