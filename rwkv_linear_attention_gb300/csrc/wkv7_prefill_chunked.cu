@@ -480,8 +480,12 @@ wkv7_prefill_chunked_kernel(PrefillArgs p, const __grid_constant__ TensorMaps ma
     // Rows past the chunk's end are zero.
     auto phase2 = [&](int chunk, int lc, const float *eref) {
         {   // B_G: thread = row t, channels 4 cq .. 4 cq + 3 and 32 + 4 cq .. 32 + 4 cq + 3, so that
-            // each 8- or 16-byte access of a quarter-warp (one row) covers 8 distinct bank groups
-            const int t = tid >> 3, cq = tid & 7;
+            // each 16-byte access of a quarter-warp (one row) covers 8 distinct bank groups.  A
+            // warp takes rows b, b + 4, b + 1, b + 5 in its four quarters: the two rows of a
+            // half-warp (its 8-byte tile reads) differ by 4, so their 64 bytes each lie in the
+            // two complementary halves of the 128-byte swizzle pattern.
+            const int wq = tid >> 5, jq = (tid >> 3) & 3;
+            const int t = 8 * (wq >> 1) + 2 * (wq & 1) + 4 * (jq & 1) + (jq >> 1), cq = tid & 7;
             unsigned char *BG = sm + SM_BG;
             uint4 cw[2], kw[2];
             if (t < lc) {
