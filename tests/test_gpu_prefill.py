@@ -291,3 +291,41 @@ def test_host_rejects_malformed_cu_seqlens(dev):
     with pytest.raises(wkv7.WKV7Error) as e:
         wkv7.prefill(p["r"], p["w"], p["k"], p["v"], p["kk"], p["a"], bad.to(dev), cu_seqlens_host=bad)
     assert e.value.status == wkv7._lib.ERR_INVALID_ARG
+
+
+def test_concurrent_calls_on_two_streams(dev):
+    """Two calls with distinct workspaces, outputs and states, issued on two streams
+    so that they overlap on the GPU (one of them tail-split, so its fix-up kernels and
+    scratch are in flight too): each result is bit-identical to the same call run
+    alone (the kernels are deterministic), and within the bound of the oracle."""
+    cases = [([3000], 8, 91), ([64, 101, 0, 7, 700], 3, 92)]
+    runs = []
+    for lens, H, seed in cases:
+        p = inputs.prefill_inputs(lens, H, 64, seed=seed, device=dev)
+        s0 = inputs.initial_state(len(lens), H, 64, seed=seed, device=dev)
+        cu = p["cu_seqlens"]
+        ws = torch.empty(max(wkv7.prefill_workspace_size(len(lens), int(cu[-1]), H), 16), dtype=torch.uint8,
+                         device=dev)
+        o, sf = wkv7.prefill(p["r"], p["w"], p["k"], p["v"], p["kk"], p["a"], cu.to(dev), initial_state=s0,
+                             cu_seqlens_host=cu, workspace=ws)
+        runs.append((p, s0, cu, ws, o.clone(), sf.clone()))
+    torch.cuda.synchronize()
+    wkv7.check_device_status()
+    streams = [torch.cuda.Stream(device=dev) for _ in runs]
+    for _ in range(4):
+        outs = []
+        for (p, s0, cu, ws, o_ref, sf_ref), st in zip(runs, streams):
+            o = torch.full_like(o_ref, float("nan"))
+            sf = torch.full_like(sf_ref, float("nan"))
+            st.wait_stream(torch.cuda.current_stream(dev))
+            with torch.cuda.stream(st):
+                wkv7.prefill(p["r"], p["w"], p["k"], p["v"], p["kk"], p["a"], cu.to(dev), initial_state=s0,
+                             final_state=sf, o=o, cu_seqlens_host=cu, workspace=ws, stream=st)
+            outs.append((o, sf))
+        torch.cuda.synchronize()
+        wkv7.check_device_status()
+        for (o, sf), (_, _, _, _, o_ref, sf_ref) in zip(outs, runs):
+            assert torch.equal(o, o_ref)
+            assert torch.equal(sf, sf_ref)
+    for p, s0, cu, _, o_ref, sf_ref in runs:
+        _check(p, o_ref, sf_ref, s0=s0)
