@@ -205,17 +205,18 @@ WKV7_API wkv7_status wkv7_verify_commit(int B, int T, int H, int N, const float 
  *   - the longest-first order of the sequences, 4 bytes per sequence rounded
  *     up to 256, for 2 <= num_seqs <= 4096 (required: a smaller workspace
  *     returns WKV7_ERR_WORKSPACE);
- *   - for T_total >= 1024, scratch for the tail split (optional): 256 state
+ *   - for T_total >= 1024, scratch for the tail split (optional): 512 state
  *     slots of 16 KB, then 256 bytes per token-head for up to
  *     min(T_total * H, 2^20) token-heads.  When the (sequence, head)
- *     pairs do not fill the last wave of CTAs (P mod SMs <= SMs / 3), the
- *     pairs of that wave are cut into chunk-aligned segments that run
- *     concurrently; a segment after the first runs from a zero state and once
- *     more from the identity state with v = 0, and two small kernels chain
- *     the true boundary states and add the carried-in state's contribution
- *     to the outputs (exact up to rounding: the recurrence is linear in the
- *     state).  This needs cu_seqlens_host; with less scratch than a plan
- *     needs, or without the host copy, every pair runs whole.
+ *     pairs do not fill the last wave of CTAs (0 < P mod SMs <= SMs / 2, at
+ *     most 80 pairs), the pairs of that wave are cut into chunk-aligned
+ *     segments that run concurrently; a segment after the first runs from a
+ *     zero state and once more from the identity state with v = 0, and two
+ *     small kernels chain the true boundary states and add the carried-in
+ *     state's contribution to the outputs (exact up to rounding: the
+ *     recurrence is linear in the state).  This needs cu_seqlens_host; with
+ *     less scratch than a plan needs, or without the host copy, every pair
+ *     runs whole.
  */
 WKV7_API size_t wkv7_prefill_workspace_size(int num_seqs, int T_total, int H, int N);
 

@@ -203,7 +203,7 @@ struct SplitItem {
     int32_t ohat_row;   // first scratch row of a transfer item's readout, or (bf16 output)
                         // of a part item's fp32 outputs
 };
-constexpr int kMaxSplitItems = 256;
+constexpr int kMaxSplitItems = 512;
 constexpr int kMaxSplitPairs = 80;
 constexpr int kMaxSegs = 16;
 struct SplitPlan {
@@ -1307,12 +1307,16 @@ int sm_count() {
 
 // The tail-split schedule (see SplitItem).  With P pairs on S SMs (one CTA per SM),
 // the last r = P mod S pairs in schedule order (the shortest) would run alone in a
-// last wave.  When r <= S/3 each is cut into k equal segments (2k - 1 items, all
-// running at once) with k as large as the SMs, kMaxSegs and the scratch allow.
-// When S/3 < r <= S/2 each is cut in two, 2:1: the long first segments and S - r
-// of the short items start together, the other short items follow as the first
-// short ones finish, so the tail takes about 2/3 of a pair.  Needs the host copy
-// of cu_seqlens; returns false (whole pairs only) otherwise.
+// last wave (split when 0 < r <= S/2 and r <= kMaxSplitPairs).  Each is cut into k
+// segments, the first of about f0 of its chunks and the others equal (2k - 1
+// items: the first segment, then a part and a transfer item per later segment).
+// Items start in launch order as SMs free up, so (k, f0) is chosen from a model of that
+// list schedule (a few integer operations per candidate, no search on the host's
+// critical path): when 2k - 1 items per pair fit on the SMs at once the best is k equal
+// segments; when they do not, a longer first segment lets the short items run in rounds
+// beside it (r = 64 pairs of 512 chunks: k = 3, a first segment of 307 chunks, against
+// 512 whole and 342 for a 2:1 cut).  Needs the
+// host copy of cu_seqlens; returns false (whole pairs only) otherwise.
 bool plan_split(const PrefillArgs &a, unsigned char *split_ws, size_t split_bytes, SplitPlan &plan, FixPlan &fix) {
     const long long P = static_cast<long long>(a.num_seqs) * a.H;
     plan.main_items = static_cast<int>(P);
@@ -1328,7 +1332,6 @@ bool plan_split(const PrefillArgs &a, unsigned char *split_ws, size_t split_byte
     if (S <= 0) return false;
     const long long r = P % S;
     if (r == 0 || 2 * r > S || r > kMaxSplitPairs) return false;
-    const bool two_to_one = 3 * r > S;
     auto len = [&](int b) {
         int l = 0;
         host_seq_len(a, b, l);
@@ -1344,26 +1347,70 @@ bool plan_split(const PrefillArgs &a, unsigned char *split_ws, size_t split_byte
         const int b = ord[bi / a.H];
         tail.push_back({b, static_cast<int>(bi % a.H), (len(b) + kC - 1) / kC});
     }
-    // segment j of a pair of n chunks cut into kp segments: [bound(j), bound(j + 1))
+    // segment j of a pair of n chunks cut into kp segments, the first of about f0 / 1000 of
+    // them, the others equal: [bound(j), bound(j + 1)), every segment at least one chunk
     auto segs = [&](const Tail &t, int k) { return t.n > 32767 || t.n < 3 ? 1 : std::min(k, t.n / 2); };
-    auto bound = [&](const Tail &t, int kp, int j) {
-        if (two_to_one) return j == 0 ? 0 : j == 1 ? (2 * t.n + 2) / 3 : t.n;
-        return j * t.n / kp;
+    auto bound = [&](const Tail &t, int kp, int f0, int j) {
+        if (j <= 0) return 0;
+        if (j >= kp) return t.n;
+        const int l0 = std::min(t.n - (kp - 1), std::max(1, (f0 * t.n + 500) / 1000));
+        return l0 + (j - 1) * (t.n - l0) / (kp - 1);
     };
-    const int k_hi = two_to_one ? 2 : static_cast<int>(std::min<long long>(kMaxSegs, (S / r + 1) / 2));
-    for (int k = k_hi; k >= 2; --k) {
+    // Candidates k = 2 .. kMaxSegs, each with the first-segment share f0 (per mille) that
+    // balances the list schedule, and its length in chunks (-1: does not fit).  When every
+    // item starts at once the segments are equal and the tail takes the longest one.  When
+    // not, the first segments hold r SMs and the 2 (k - 1) r short items run in rounds on
+    // the other S - r (a model of the longest pair: rounds x short = first segment).
+    int nmax = 0;
+    for (const Tail &t : tail) nmax = std::max(nmax, t.n);
+    auto candidate = [&](int k, int &f0) -> long long {
         long long items = 0, rows = 0, nsplit = 0;
+        for (const Tail &t : tail) items += segs(t, k) < 2 ? 1 : 2 * segs(t, k) - 1;
+        if (items <= S) {
+            f0 = 1000 / k;
+        } else {
+            const long long rounds = (items - r + (S - r) - 1) / (S - r);
+            f0 = static_cast<int>((1000 * rounds) / (rounds + k - 1));
+        }
+        long long span = 0;
         for (const Tail &t : tail) {
             const int kp = segs(t, k);
             if (kp < 2) {
-                items += 1;
+                span = std::max<long long>(span, t.n);
                 continue;
             }
-            items += 2 * kp - 1;
             ++nsplit;
-            rows += static_cast<long long>(t.n - bound(t, kp, 1)) * 64 * rows_per;
+            rows += static_cast<long long>(t.n - bound(t, kp, f0, 1)) * 64 * rows_per;
+            span = std::max<long long>(span, bound(t, kp, f0, 1));
+            if (items <= S)
+                for (int j = 1; j < kp; ++j) span = std::max<long long>(span, bound(t, kp, f0, j + 1) - bound(t, kp, f0, j));
         }
-        if (nsplit == 0 || items > kMaxSplitItems || (!two_to_one && items > S) || rows > rows_cap) continue;
+        if (nsplit == 0 || items > kMaxSplitItems || rows > rows_cap) return -1;
+        if (items > S) {  // the short items' rounds beside the first segments (longest pair)
+            const Tail lp{0, 0, nmax};
+            const int kp = segs(lp, k);
+            if (kp >= 2) {
+                const long long rounds = (items - r + (S - r) - 1) / (S - r);
+                const long long short_len = (nmax - bound(lp, kp, f0, 1) + kp - 2) / (kp - 1);
+                span = std::max(span, rounds * short_len);
+            }
+        }
+        return span;
+    };
+    int best_k = 0, best_f = 0;
+    long long best = -1;
+    for (int k = 2; k <= kMaxSegs; ++k) {
+        int f0 = 0;
+        const long long m = candidate(k, f0);
+        if (m >= 0 && (best < 0 || m < best)) {
+            best = m;
+            best_k = k;
+            best_f = f0;
+        }
+    }
+    if (best < 0) return false;
+    {
+        const int k = best_k, f0 = best_f;
         plan.main_items = static_cast<int>(P - r);
         plan.slots = fix.slots = reinterpret_cast<float *>(split_ws);
         plan.ohat = fix.ohat = reinterpret_cast<float *>(split_ws + kSlotsBytes);
@@ -1382,7 +1429,7 @@ bool plan_split(const PrefillArgs &a, unsigned char *split_ws, size_t split_byte
             fp.nseg = kp;
             FixSeg &sg = fp.seg[0];
             sg.c0 = 0;
-            sg.c1 = static_cast<int16_t>(bound(t, kp, 1));
+            sg.c1 = static_cast<int16_t>(bound(t, kp, f0, 1));
             sg.slot_part = static_cast<int16_t>(slot);
             sg.slot_transfer = -1;
             sg.ohat_row = 0;
@@ -1395,8 +1442,8 @@ bool plan_split(const PrefillArgs &a, unsigned char *split_ws, size_t split_byte
             const int pair = fp.b * a.H + fp.h;
             for (int j = 1; j < fp.nseg; ++j) {
                 FixSeg &sg = fp.seg[j];
-                sg.c0 = static_cast<int16_t>(bound(t, fp.nseg, j));
-                sg.c1 = static_cast<int16_t>(bound(t, fp.nseg, j + 1));
+                sg.c0 = static_cast<int16_t>(bound(t, fp.nseg, f0, j));
+                sg.c1 = static_cast<int16_t>(bound(t, fp.nseg, f0, j + 1));
                 sg.slot_part = static_cast<int16_t>(slot);
                 sg.opart_row = 0;
                 if (rows_per == 2) {
@@ -1413,9 +1460,8 @@ bool plan_split(const PrefillArgs &a, unsigned char *split_ws, size_t split_byte
         }
         plan.n_items = n;
         fix.n_blocks = blk;
-        return true;
     }
-    return false;
+    return true;
 }
 
 cudaError_t launch_chunked(const PrefillArgs &args, unsigned char *split_ws, size_t split_bytes, cudaStream_t stream) {

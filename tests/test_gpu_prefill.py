@@ -178,13 +178,14 @@ def test_prefill_7p2b_single_32768(dev):
 
 
 # Tail split: with P (sequence, head) pairs on S SMs, the last r = P mod S pairs are
-# cut into segments when 0 < r <= S/2 (and r <= 80): k equal segments for r <= S/3,
-# two segments 2:1 above.  These shapes split on a GB300 (S = 152): one ragged
-# sequence of 8 heads (10 segments per pair), three unequal sequences of 10 heads
-# (the schedule's longest-first order, 3 segments), one sequence of 64 heads and two
-# unequal sequences of 30 heads (2:1).
+# cut into segments when 0 < r <= S/2 (and r <= 80), k of them with a first segment
+# of a chosen length (the host's list schedule).  These shapes split on a GB300
+# (S = 152): one ragged sequence of 8 heads (10 equal segments per pair), three
+# unequal sequences of 10 heads (the schedule's longest-first order), one sequence of
+# 64 heads and two unequal sequences of 30 heads (more items than SMs: a longer first
+# segment, the short items in rounds).
 SPLIT_CASES = [([3000], 8, 21), ([2000, 1500, 700], 10, 22), ([2500], 64, 24), ([1500, 900], 30, 25)]
-SPLIT_IDS = ["1x3000-H8", "unequal-H10", "1x2500-H64-2to1", "unequal-H30-2to1"]
+SPLIT_IDS = ["1x3000-H8", "unequal-H10", "1x2500-H64-rounds", "unequal-H30-rounds"]
 
 
 def _expect_split(num_seqs, H):

@@ -113,7 +113,7 @@ def test_bf16_values_bit_identical(dev, lens, H):
 
 
 @pytest.mark.parametrize("lens,H,seed", [([3000], 8, 71), ([2000, 1500, 700], 10, 72), ([2500], 64, 74)],
-                         ids=["1x3000-H8", "unequal-H10", "1x2500-H64-2to1"])
+                         ids=["1x3000-H8", "unequal-H10", "1x2500-H64-rounds"])
 def test_tail_split_against_oracle(dev, lens, H, seed):
     p = inputs.prefill_inputs(lens, H, 64, seed=seed, device=dev, x_dtype=torch.float32)
     s0 = inputs.initial_state(len(lens), H, 64, seed=seed, device=dev)
