@@ -88,3 +88,23 @@ def test_prefill_bf16_output_with_the_tail_split(dev):
     assert rel_err(f16, s_ref) <= 2e-3
     assert rel_err(o16.float(), o_whole.float()) <= 2e-3 + BF16_ROUND
     assert rel_err(f16, f_whole) <= 2e-3
+
+
+def test_prefill_bf16_output_with_a_rounds_split(dev):
+    """A tail of 64 pairs (one sequence of 64 heads) is cut into more items than SMs:
+    a longer first segment with the short part and transfer items in rounds.  With a
+    bf16 output the part items' fp32 rows sit beside the transfer rows in the
+    scratch; the result matches the oracle and the fp32-output call rounded once."""
+    lens, H = [2500], 64
+    p = inputs.prefill_inputs(lens, H, 64, seed=172, device=dev)
+    s0 = inputs.initial_state(1, H, 64, seed=173, device=dev)
+    cu = p["cu_seqlens"]
+    o16, f16 = wkv7.prefill(*(p[n] for n in NAMES), cu.to(dev), initial_state=s0, cu_seqlens_host=cu,
+                            out_dtype=torch.bfloat16)
+    o32, f32 = wkv7.prefill(*(p[n] for n in NAMES), cu.to(dev), initial_state=s0, cu_seqlens_host=cu)
+    wkv7.check_device_status()
+    assert torch.equal(o16, o32.to(torch.bfloat16))
+    assert torch.equal(f16, f32)
+    o_ref, s_ref = oracle_prefill(p, cu, s0=s0)
+    assert rel_err(o16.float(), o_ref) <= 2e-3 + BF16_ROUND
+    assert rel_err(f16, s_ref) <= 2e-3
