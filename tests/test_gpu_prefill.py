@@ -330,3 +330,36 @@ def test_concurrent_calls_on_two_streams(dev):
             assert torch.equal(sf, sf_ref)
     for p, s0, cu, _, o_ref, sf_ref in runs:
         _check(p, o_ref, sf_ref, s0=s0)
+
+
+# Randomised schedules: batches whose last wave of pairs is split in many different
+# ways (equal segments, a longer first segment with the short items in rounds, pairs
+# too short to split beside long ones), each checked on sampled heads against the
+# oracle and against the same call with every pair whole.  Heads H - 1 and H - 2
+# belong to the last sequence in the schedule, whose pairs form the tail.
+RANDOM_SCHEDULES = [
+    (1, 8, 9001), (1, 40, 9002), (1, 64, 9003), (2, 30, 9004), (2, 38, 9005), (3, 13, 9006),
+    (3, 25, 9007), (4, 19, 9008), (5, 7, 9009), (6, 12, 9010), (1, 76, 9011), (2, 76, 9012),
+]
+
+
+@pytest.mark.parametrize("num_seqs,H,seed", RANDOM_SCHEDULES, ids=lambda x: str(x))
+def test_random_split_schedules(dev, num_seqs, H, seed):
+    g = torch.Generator().manual_seed(seed)
+    lens = (torch.randint(3, 5000, (num_seqs,), generator=g)).tolist()
+    if sum(lens) < 1024:  # the split needs at least 1024 tokens of scratch
+        lens[0] += 1024
+    p = inputs.prefill_inputs(lens, H, 64, seed=seed, device=dev)
+    s0 = inputs.initial_state(num_seqs, H, 64, seed=seed, device=dev)
+    cu = p["cu_seqlens"]
+    o, sf = wkv7.prefill(p["r"], p["w"], p["k"], p["v"], p["kk"], p["a"], cu.to(dev), initial_state=s0,
+                         cu_seqlens_host=cu)
+    small = torch.empty(max(256, wkv7.prefill_workspace_size(num_seqs, 0, H)), dtype=torch.uint8, device=dev)
+    o_w, sf_w = wkv7.prefill(p["r"], p["w"], p["k"], p["v"], p["kk"], p["a"], cu.to(dev), initial_state=s0,
+                             cu_seqlens_host=cu, workspace=small)
+    wkv7.check_device_status()
+    assert rel_err(o, o_w) <= TOL and rel_err(sf, sf_w) <= TOL
+    heads = sorted({0, H - 2, H - 1})
+    o_ref, s_ref = oracle_prefill(p, cu, s0=s0, heads=heads)
+    e_o, e_s = rel_err(o[:, heads], o_ref), rel_err(sf[:, heads], s_ref)
+    assert e_o <= TOL and e_s <= TOL, f"o {e_o:.3e}, state {e_s:.3e}"
