@@ -243,3 +243,15 @@ def test_product_package_does_not_import_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "wkv7_oracle" not in text, f
+
+
+def test_binding_input_codes():
+    """The binding's prefill input code: bf16 always takes the chunked kernel; fp32 the
+    exact token-serial kernel unless tf32 contraction is asked for."""
+    import torch
+    import rwkv_linear_attention_gb300 as wkv7
+    assert wkv7._x_code(torch.bfloat16, False) == _lib.BF16
+    assert wkv7._x_code(torch.bfloat16, True) == _lib.BF16
+    assert wkv7._x_code(torch.float32, False) == _lib.F32
+    assert wkv7._x_code(torch.float32, True) == _lib.TF32
+    assert (_lib.F32, _lib.BF16, _lib.F16, _lib.TF32) == (0, 1, 2, 3)
