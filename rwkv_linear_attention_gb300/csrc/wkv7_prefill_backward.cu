@@ -422,6 +422,19 @@ __device__ __forceinline__ void mma_group_acc(uint32_t tmem, uint32_t dcol, uint
                         (accumulate || kq > 0) ? 1u : 0u);
 }
 
+// Operands written -> thread 0 issues, without a commit: the products run while the
+// threads go on, and the next mma_stage's commit and wait cover them too.
+template <class F>
+__device__ __forceinline__ void mma_issue(F issue) {
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        tc_fence_after_sync();
+        issue();
+    }
+}
+
 // Operands written -> thread 0 issues and commits -> every thread waits (bounded).
 // The outcome is uniform over the CTA; false after a timeout (reported).
 template <class F>
@@ -632,7 +645,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_summary_tc_kernel(BwdArgs p) 
             b_col(sm + tcs::kBVc, 64, t, c0, kk);
             b_col(sm + tcs::kBdOc, 64, t, c0, ra);
         }
-        __syncthreads();
+        // Lk V and Mc^T dO need no T: they run while the threads form it (the inverse's
+        // scratch is the T tiles' space, which these products do not read)
+        mma_issue([&] {
+            mma_group(tmem, 128, 64, sbase + tcs::kBVc, tcg::kAtom64, 64, 64);    // Lk V (top)
+            mma_group(tmem, 192, 64, sbase + tcs::kBdOc, tcg::kAtom64, 64, 64);   // Mc^T dO (bottom)
+        });
         unit_lower_inverse(P1p, P0, reinterpret_cast<float *>(sm + tcs::kBTt));
         if (top) {
 #pragma unroll
@@ -643,8 +661,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_summary_tc_kernel(BwdArgs p) 
             b_row(sm + tcs::kBTn, 64, t, c0, x);  // rows t: T[t][s]
         }
         ok = mma_stage(bar, phase, p.status, [&] {
-            mma_group(tmem, 128, 64, sbase + tcs::kBVc, tcg::kAtom64, 64, 64);    // Lk V (top)
-            mma_group(tmem, 192, 64, sbase + tcs::kBdOc, tcg::kAtom64, 64, 64);   // Mc^T dO (bottom)
             mma_group(tmem, 0, 384, sbase + tcs::kBTt, tcg::kAtom64, 64, 64);     // W1 = Cm^T T (top)
             mma_group(tmem, 256, 384, sbase + tcs::kBTn, tcg::kAtom64, 64, 64);   // W2 = Q^T T^T (bottom)
         });
@@ -929,11 +945,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
             b_col(sm + tcg::kBY, 64, 64 + t, c0, kk);    // V^c
             b_col(sm + tcg::kBF3, 64, 64 + t, c0, ra);   // dO^c
         }
-        unit_lower_inverse(P1p, P0, reinterpret_cast<float *>(sm + tcg::kBF3 + 32768));
-        ok = mma_stage(bar, phase, p.status, [&] {
+        // Y and Y2 need no T: they run while the threads form it (the inverse's scratch lies
+        // past the part of B_F3 these products read)
+        mma_issue([&] {
             mma_group(tmem, 128, 0, sbase + tcg::kBY, tcg::kAtom64, 64, 128);
             mma_group(tmem, 192, 0, sbase + tcg::kBF3, tcg::kAtom64, 64, 128);
         });
+        unit_lower_inverse(P1p, P0, reinterpret_cast<float *>(sm + tcg::kBF3 + 32768));
+        ok = mma_stage(bar, phase, p.status, [] {});
     }
 
     if (ok) {
