@@ -60,6 +60,9 @@ constexpr int kC = 64;            // tokens per chunk
 constexpr int kLD = 68;           // shared-memory row stride in floats (16-B rows, staggered banks)
 constexpr int kMat = kC * kLD;    // floats per 64 x 64 buffer
 constexpr int kThreads = 256;
+// The gradient pass runs 16 warps: a 128 x 64 operand row (TMEM lane) is split over four
+// threads of kGW = 16 columns (kGroups = 4 column groups), the other passes over two of 32.
+constexpr int kGradThreads = 512, kGW = 16, kGroups = 4;
 constexpr size_t kMatBytes = (size_t)kMat * sizeof(float);
 constexpr size_t kStateElems = (size_t)kN * kN;
 constexpr size_t kChainSmem = 3 * kMatBytes;
@@ -223,12 +226,13 @@ __device__ __forceinline__ bool locate(const BwdArgs &p, int g, Chunk &c) {
 // T = (I + Lc)^{-1} for the strictly lower Lc: the four 16 x 16 diagonal blocks by
 // forward substitution (one thread per column), then the blocks below them by
 // T_IJ = -T_II sum_{K=J}^{I-1} Lc_IK T_KJ, one block diagonal at a time.
-// tmp holds at least 3 * 256 floats.  Ends with a barrier.
+// tmp holds at least 3 * 256 floats.  NT threads.  Ends with a barrier.
+template <int NT>
 __device__ void unit_lower_inverse(const float *Lc, float *T, float *tmp) {
     const int tid = threadIdx.x;
 #pragma unroll 4
-    for (int q = 0; q < 16; ++q) {
-        const int e = tid + q * kThreads;
+    for (int q = 0; q < 4096 / NT; ++q) {
+        const int e = tid + q * NT;
         T[(e >> 6) * kLD + (e & 63)] = 0.f;
     }
     __syncthreads();
@@ -248,7 +252,7 @@ __device__ void unit_lower_inverse(const float *Lc, float *T, float *tmp) {
     __syncthreads();
     for (int d = 1; d < 4; ++d) {
         const int np = 4 - d;
-        for (int e = tid; e < np * 256; e += kThreads) {
+        for (int e = tid; e < np * 256; e += NT) {
             const int J = e >> 8, rr = (e >> 4) & 15, cc = e & 15, I = J + d;
             const float *lrow = Lc + (I * 16 + rr) * kLD;
             float acc = 0.f;
@@ -259,7 +263,7 @@ __device__ void unit_lower_inverse(const float *Lc, float *T, float *tmp) {
             tmp[e] = acc;
         }
         __syncthreads();
-        for (int e = tid; e < np * 256; e += kThreads) {
+        for (int e = tid; e < np * 256; e += NT) {
             const int J = e >> 8, rr = (e >> 4) & 15, cc = e & 15, I = J + d;
             float acc = 0.f;
 #pragma unroll
@@ -322,9 +326,9 @@ constexpr uint32_t kBF1 = 81920;      // [G' | R^c | Q^c] 64 x 192 (48 KB), stag
 constexpr uint32_t kBF2 = 131072;     // [S0' | K^c | Cm^c] 64 x 192 (48 KB), stage 6
 constexpr uint32_t kPlain0 = 180224;  // fp32 64 x 68: the cumulative decay, then T; then (with kPlain1) B_Pt
 constexpr uint32_t kPlain1 = 197632;  // fp32 64 x 68: Lc
-constexpr uint32_t kVec = 215040;     // rho[64], gC[64], carry halves [2][64]
-constexpr uint32_t kBar = 216064;     // mbarrier, TMEM base slot
-constexpr uint32_t kBytes = 216080;
+constexpr uint32_t kVec = 215040;     // rho[64], gC[64], carry parts [4][64]
+constexpr uint32_t kBar = 216576;     // mbarrier, TMEM base slot
+constexpr uint32_t kBytes = 216592;
 constexpr uint32_t kAlloc = kBytes + 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kMaxPolls = 1u << 24;
@@ -333,12 +337,13 @@ constexpr uint32_t kAtom64 = 64 * 128, kAtom128 = 128 * 128, kAtom256 = 256 * 12
 
 __device__ __forceinline__ uint32_t tf32r(float x) { return __float_as_uint(x) + 0x1000u; }
 
-// 32 consecutive values of one packed token row, widened to fp32.
-__device__ __forceinline__ void load32(float (&v)[32], const void *src, bool bf16, size_t off) {
+// W (16 or 32) consecutive values of one packed token row, widened to fp32.
+template <int W>
+__device__ __forceinline__ void load_row(float (&v)[W], const void *src, bool bf16, size_t off) {
     if (bf16) {
         const uint4 *p = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(src) + off);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < W / 8; ++q) {
             const uint4 u = __ldg(p + q);
             const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -350,54 +355,66 @@ __device__ __forceinline__ void load32(float (&v)[32], const void *src, bool bf1
     } else {
         const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(src) + off);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
+        for (int q = 0; q < W / 4; ++q) {
             const float4 x = __ldg(p + q);
             v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
         }
     }
 }
-__device__ __forceinline__ void zero32(float (&v)[32]) {
+template <int W>
+__device__ __forceinline__ void zero_row(float (&v)[W]) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = 0.f;
+    for (int i = 0; i < W; ++i) v[i] = 0.f;
 }
-// 32 values of row `row` of a plain [64][kLD] buffer from column c0 (float4 reads).
-__device__ __forceinline__ void plain_row(float (&v)[32], const float *buf, int row, int c0) {
+// W values of row `row` of a plain [64][kLD] buffer from column c0 (float4 reads).
+template <int W>
+__device__ __forceinline__ void plain_row(float (&v)[W], const float *buf, int row, int c0) {
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
+    for (int q = 0; q < W / 4; ++q) {
         const float4 x = *reinterpret_cast<const float4 *>(buf + row * kLD + c0 + 4 * q);
         v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
     }
 }
-__device__ __forceinline__ void plain_row_store(float *buf, int row, int c0, const float (&v)[32]) {
+template <int W>
+__device__ __forceinline__ void plain_row_store(float *buf, int row, int c0, const float (&v)[W]) {
 #pragma unroll
-    for (int q = 0; q < 8; ++q)
+    for (int q = 0; q < W / 4; ++q)
         *reinterpret_cast<float4 *>(buf + row * kLD + c0 + 4 * q) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
 }
-// Row `row`, K = kofs .. kofs + 31 of a K-major 128B-swizzled tile with `rows` rows.
-__device__ __forceinline__ void b_row(unsigned char *tile, int rows, int row, int kofs, const float (&v)[32]) {
+// Row `row`, K = kofs .. kofs + W - 1 of a K-major 128B-swizzled tile with `rows` rows.
+template <int W>
+__device__ __forceinline__ void b_row(unsigned char *tile, int rows, int row, int kofs, const float (&v)[W]) {
 #pragma unroll
-    for (int q = 0; q < 8; ++q)
+    for (int q = 0; q < W / 4; ++q)
         *reinterpret_cast<uint4 *>(tile + sw128_off(row, kofs + 4 * q, rows)) =
             make_uint4(tf32r(v[4 * q]), tf32r(v[4 * q + 1]), tf32r(v[4 * q + 2]), tf32r(v[4 * q + 3]));
 }
-// Column k of the tile, rows n0 .. n0 + 31 (a transposed store of this thread's row).
-__device__ __forceinline__ void b_col(unsigned char *tile, int rows, int k, int n0, const float (&v)[32]) {
+// Column k of the tile, rows n0 .. n0 + W - 1 (a transposed store of this thread's row).
+template <int W>
+__device__ __forceinline__ void b_col(unsigned char *tile, int rows, int k, int n0, const float (&v)[W]) {
 #pragma unroll
-    for (int c = 0; c < 32; ++c) *reinterpret_cast<uint32_t *>(tile + sw128_off(n0 + c, k, rows)) = tf32r(v[c]);
+    for (int c = 0; c < W; ++c) *reinterpret_cast<uint32_t *>(tile + sw128_off(n0 + c, k, rows)) = tf32r(v[c]);
 }
-// This thread's TMEM lane, 32 columns from taddr: tf32 operand values / raw reads.
-__device__ __forceinline__ void a_row(uint32_t taddr, const float (&v)[32]) {
-    uint32_t r[32];
+// This thread's TMEM lane, W columns from taddr: tf32 operand values / raw reads.
+template <int W>
+__device__ __forceinline__ void a_row(uint32_t taddr, const float (&v)[W]) {
+    uint32_t r[W];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) r[i] = tf32r(v[i]);
-    tmem_st32u(taddr, r);
+    for (int i = 0; i < W; ++i) r[i] = tf32r(v[i]);
+    if constexpr (W == 32) tmem_st32u(taddr, r);
+    else tmem_st16(taddr, r);
+}
+template <int W>
+__device__ __forceinline__ void tmem_ld_row(uint32_t taddr, float (&v)[W]) {
+    if constexpr (W == 32) tmem_ld32(taddr, v);
+    else tmem_ld16(taddr, v);
 }
 
-// Keep entries of row `row`, columns c0 .. c0 + 31, whose column passes the mask; optionally negate.
-template <Mask M, bool kNegate>
-__device__ __forceinline__ void mask32(float (&v)[32], int row, int c0) {
+// Keep entries of row `row`, columns c0 .. c0 + W - 1, whose column passes the mask; optionally negate.
+template <Mask M, bool kNegate, int W>
+__device__ __forceinline__ void mask_row(float (&v)[W], int row, int c0) {
 #pragma unroll
-    for (int c = 0; c < 32; ++c) {
+    for (int c = 0; c < W; ++c) {
         const float x = kNegate ? -v[c] : v[c];
         v[c] = keep<M>(row, c0 + c) ? x : 0.f;
     }
@@ -455,28 +472,47 @@ __device__ __forceinline__ bool mma_stage(uint32_t bar, uint32_t &phase, unsigne
     return all_ok != 0;
 }
 
-// This thread's 16 values of w for the cumulative sum (row tid / 4, channels 16 (tid mod 4) ..).
-__device__ __forceinline__ void load_w16(float (&x)[16], const BwdArgs &p, const Chunk &c, int h) {
-    const int t = threadIdx.x >> 2, cc = (threadIdx.x & 3) * 16;
+// This thread's 4096 / NT values of w for the cumulative sum (row tid / (NT / 64), the
+// consecutive channels from (tid mod (NT / 64)) x 4096 / NT) with NT threads.
+template <int NT>
+__device__ __forceinline__ void load_w(float (&x)[4096 / NT], const BwdArgs &p, const Chunk &c, int h) {
+    constexpr int kPer = 4096 / NT;
+    const int t = threadIdx.x / (NT / 64), cc = (threadIdx.x % (NT / 64)) * kPer;
     const bool valid = t < c.len;
-    load16(x, p.w, false, ((size_t)(c.tb + (valid ? t : 0)) * p.H + h) * kN + cc, valid);
+    if (valid) {
+        const float4 *src = reinterpret_cast<const float4 *>(p.w + ((size_t)(c.tb + t) * p.H + h) * kN + cc);
+#pragma unroll
+        for (int q = 0; q < kPer / 4; ++q) {
+            const float4 w4 = __ldg(src + q);
+            x[4 * q] = w4.x; x[4 * q + 1] = w4.y; x[4 * q + 2] = w4.z; x[4 * q + 3] = w4.w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) x[j] = 0.f;
+    }
     float wmin = 0.f;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) wmin = fminf(wmin, x[j]);
+    for (int j = 0; j < kPer; ++j) wmin = fminf(wmin, x[j]);
     if (valid && wmin < kMinLogDecay) report(p.status, kDevDomain);  // outside the domain: reported
 }
 
 // Inclusive cumulative sum of w over the chunk into Gm ([64][kLD]) from the values
-// of load_w16; scratch: 4 rows of kLD.  Ends with a barrier.
-__device__ void decay_cumsum_from(const float (&x)[16], float *Gm, float *scratch) {
-    store16(Gm + (threadIdx.x >> 2) * kLD + (threadIdx.x & 3) * 16, x);
+// of load_w, with NT threads (NT / 64 row segments of 4096 / NT rows); scratch: NT / 64
+// rows of kLD.  Ends with a barrier.
+template <int NT>
+__device__ void decay_cumsum_from(const float (&x)[4096 / NT], float *Gm, float *scratch) {
+    constexpr int kPer = 4096 / NT;
+    float *dst = Gm + (threadIdx.x / (NT / 64)) * kLD + (threadIdx.x % (NT / 64)) * kPer;
+#pragma unroll
+    for (int q = 0; q < kPer / 4; ++q)
+        *reinterpret_cast<float4 *>(dst + 4 * q) = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
     __syncthreads();
     const int ch = threadIdx.x & 63, qt = threadIdx.x >> 6;
     float run = 0.f;
-    float part[16];
+    float part[kPer];
 #pragma unroll
-    for (int u = 0; u < 16; ++u) {
-        run += Gm[(qt * 16 + u) * kLD + ch];
+    for (int u = 0; u < kPer; ++u) {
+        run += Gm[(qt * kPer + u) * kLD + ch];
         part[u] = run;
     }
     scratch[qt * kLD + ch] = run;
@@ -484,20 +520,22 @@ __device__ void decay_cumsum_from(const float (&x)[16], float *Gm, float *scratc
     float base = 0.f;
     for (int q = 0; q < qt; ++q) base += scratch[q * kLD + ch];
 #pragma unroll
-    for (int u = 0; u < 16; ++u) Gm[(qt * 16 + u) * kLD + ch] = part[u] + base;
+    for (int u = 0; u < kPer; ++u) Gm[(qt * kPer + u) * kLD + ch] = part[u] + base;
     __syncthreads();
 }
 
+template <int NT>
 __device__ void decay_cumsum(const BwdArgs &p, const Chunk &c, int h, float *Gm, float *scratch) {
-    float x[16];
-    load_w16(x, p, c, h);
-    decay_cumsum_from(x, Gm, scratch);
+    float x[4096 / NT];
+    load_w<NT>(x, p, c, h);
+    decay_cumsum_from<NT>(x, Gm, scratch);
 }
 
-// 32 values of a 64 x 64 fp32 state row (global), or zeros.
-__device__ __forceinline__ void load_state32(float (&v)[32], const float *src) {
+// W values of a 64 x 64 fp32 state row (global).
+template <int W>
+__device__ __forceinline__ void load_state_row(float (&v)[W], const float *src) {
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
+    for (int q = 0; q < W / 4; ++q) {
         const float4 a4 = __ldg(reinterpret_cast<const float4 *>(src) + q);
         v[4 * q] = a4.x; v[4 * q + 1] = a4.y; v[4 * q + 2] = a4.z; v[4 * q + 3] = a4.w;
     }
@@ -560,13 +598,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_summary_tc_kernel(BwdArgs p) 
     if (warp == 0) tmem_alloc(sbase + tcs::kBar + 8, tcg::kTmemCols);
     float kk[32], ra[32], rb[32];  // top: kk, k; bottom: kk, a, r (fetched before the cumulative sum)
     if (row_valid) {
-        load32(kk, p.kk, p.x_bf16, roff);
-        load32(ra, top ? p.k : p.a, p.x_bf16, roff);
-        if (!top) load32(rb, p.r, p.x_bf16, roff);
+        load_row(kk, p.kk, p.x_bf16, roff);
+        load_row(ra, top ? p.k : p.a, p.x_bf16, roff);
+        if (!top) load_row(rb, p.r, p.x_bf16, roff);
     } else {
-        zero32(kk); zero32(ra); zero32(rb);
+        zero_row(kk); zero_row(ra); zero_row(rb);
     }
-    decay_cumsum(p, c, h, P0, P1p);
+    decay_cumsum<kThreads>(p, c, h, P0, P1p);
     if (tid < 64) {
         rho[tid] = P0[31 * kLD + tid];
         gC[tid] = P0[63 * kLD + tid];
@@ -584,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_summary_tc_kernel(BwdArgs p) 
     {
         float g[32], gx[32];
         plain_row(g, P0, t, c0);
-        if (t > 0) plain_row(gx, P0, t - 1, c0); else zero32(gx);
+        if (t > 0) plain_row(gx, P0, t - 1, c0); else zero_row(gx);
         if (top) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
@@ -620,8 +658,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_summary_tc_kernel(BwdArgs p) 
         tmem_st32u(tl + 320, id);
     }
     if (!top) {  // V and dO rows, in flight during the first products
-        if (row_valid) { load32(kk, p.v, p.x_bf16, roff); load32(ra, p.d_o, false, roff); }
-        else { zero32(kk); zero32(ra); }
+        if (row_valid) { load_row(kk, p.v, p.x_bf16, roff); load_row(ra, p.d_o, false, roff); }
+        else { zero_row(kk); zero_row(ra); }
     }
     ok = mma_stage(bar, phase, p.status, [&] {
         mma_group(tmem, 64, 0, sbase + tcs::kBG, tcg::kAtom256, 192, 64);         // G1
@@ -632,15 +670,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_summary_tc_kernel(BwdArgs p) 
     if (ok) {
         // ---- Lc -> plain; A_L = [Lk (top); Mc^T (bottom)] at 64
         if (top) {
-            tmem_ld32(tl + 64, v);
-            mask32<kStrictLower, false>(v, t, c0);
+            tmem_ld_row(tl + 64, v);
+            mask_row<kStrictLower, false>(v, t, c0);
             plain_row_store(P1p, t, c0, v);
-            tmem_ld32(tl + 128, v);
-            mask32<kStrictLower, false>(v, t, c0);
+            tmem_ld_row(tl + 128, v);
+            mask_row<kStrictLower, false>(v, t, c0);
             a_row(tl + 64, v);
         } else {
-            tmem_ld32(tl + 192, v);
-            mask32<kUpper, false>(v, t, c0);
+            tmem_ld_row(tl + 192, v);
+            mask_row<kUpper, false>(v, t, c0);
             a_row(tl + 64, v);
             b_col(sm + tcs::kBVc, 64, t, c0, kk);
             b_col(sm + tcs::kBdOc, 64, t, c0, ra);
@@ -651,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_summary_tc_kernel(BwdArgs p) 
             mma_group(tmem, 128, 64, sbase + tcs::kBVc, tcg::kAtom64, 64, 64);    // Lk V (top)
             mma_group(tmem, 192, 64, sbase + tcs::kBdOc, tcg::kAtom64, 64, 64);   // Mc^T dO (bottom)
         });
-        unit_lower_inverse(P1p, P0, reinterpret_cast<float *>(sm + tcs::kBTt));
+        unit_lower_inverse<kThreads>(P1p, P0, reinterpret_cast<float *>(sm + tcs::kBTt));
         if (top) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) x[i] = P0[(c0 + i) * kLD + t];
@@ -669,14 +707,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_summary_tc_kernel(BwdArgs p) 
     if (ok) {
         // ---- (Lk V)^c, (Mc^T dO)^c; W1, W2 rounded to tf32 in place
         if (top) {
-            tmem_ld32(tl + 128, v);
+            tmem_ld_row(tl + 128, v);
             b_col(sm + tcs::kBT1, 64, t, c0, v);
-            tmem_ld32(tl + 0, v);
+            tmem_ld_row(tl + 0, v);
             a_row(tl + 0, v);
         } else {
-            tmem_ld32(tl + 192, v);
+            tmem_ld_row(tl + 192, v);
             b_col(sm + tcs::kBT1 + 16384, 64, t, c0, v);
-            tmem_ld32(tl + 256, v);
+            tmem_ld_row(tl + 256, v);
             a_row(tl + 256, v);
         }
         ok = mma_stage(bar, phase, p.status, [&] {
@@ -693,12 +731,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_summary_tc_kernel(BwdArgs p) 
         const int i = t;
         if (top) {
             const float sr = __expf(gC[i] - rho[i]);
-            tmem_ld32(tl + 64, v);
+            tmem_ld_row(tl + 64, v);
             float *dst = p.Fck + cidx + i * kN + c0;
 #pragma unroll
             for (int q = 0; q < 8; ++q)
                 reinterpret_cast<float4 *>(dst)[q] = make_float4(sr * v[4 * q], sr * v[4 * q + 1], sr * v[4 * q + 2], sr * v[4 * q + 3]);
-            tmem_ld32(tl + 192, v);
+            tmem_ld_row(tl + 192, v);
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = sr * ((c0 + j == i ? 1.f : 0.f) - v[j]) * __expf(rho[c0 + j]);
             dst = p.Ack + cidx + i * kN + c0;
@@ -707,7 +745,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_summary_tc_kernel(BwdArgs p) 
                 reinterpret_cast<float4 *>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         } else {
             const float sr = __expf(rho[i]);
-            tmem_ld32(tl + 128, v);
+            tmem_ld_row(tl + 128, v);
             float *dst = p.Eck + cidx + i * kN + c0;
 #pragma unroll
             for (int q = 0; q < 8; ++q)
@@ -806,7 +844,7 @@ __global__ void __launch_bounds__(kThreads) bwd_chain_kernel(BwdArgs p) {
 //      [dKr; dR] = [U | P2^T | -P4^T ; dO | P1^T | -P3^T] x [S0' | K^c | Cm^T]^T
 // then the epilogue scales by the decay factors and forms dr, dk, dkk, da, dw.
 
-__global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
+__global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -816,10 +854,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
     const uint32_t sbase = smem_addr(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3, hh = warp >> 2;
-    const int L = 32 * quad + lane, t = L & 63, c0 = 32 * hh;
+    const int L = 32 * quad + lane, t = L & 63, c0 = kGW * hh;
     const bool top = L < 64;
     const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
-    float *rho = reinterpret_cast<float *>(sm + tcg::kVec), *gC = rho + 64, *carry = gC + 64;  // carry[2][64]
+    float *rho = reinterpret_cast<float *>(sm + tcg::kVec), *gC = rho + 64, *carry = gC + 64;  // carry[kGroups][64]
     float *P0 = reinterpret_cast<float *>(sm + tcg::kPlain0), *P1p = reinterpret_cast<float *>(sm + tcg::kPlain1);
     const uint32_t bar = sbase + tcg::kBar;
     const size_t cidx = ((size_t)blockIdx.x * p.H + h) * kStateElems;
@@ -834,15 +872,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
     }
     if (warp == 0) tmem_alloc(sbase + tcg::kBar + 8, tcg::kTmemCols);
     // raw rows for the scaled operands, fetched before the cumulative sum needs w
-    float kk[32], ra[32], rb[32];  // top: kk, k; bottom: kk, a, r
+    float kk[kGW], ra[kGW], rb[kGW];  // top: kk, k; bottom: kk, a, r
     if (row_valid) {
-        load32(kk, p.kk, p.x_bf16, roff);
-        load32(ra, top ? p.k : p.a, p.x_bf16, roff);
-        if (!top) load32(rb, p.r, p.x_bf16, roff);
+        load_row(kk, p.kk, p.x_bf16, roff);
+        load_row(ra, top ? p.k : p.a, p.x_bf16, roff);
+        if (!top) load_row(rb, p.r, p.x_bf16, roff);
     } else {
-        zero32(kk); zero32(ra); zero32(rb);
+        zero_row(kk); zero_row(ra); zero_row(rb);
     }
-    decay_cumsum(p, c, h, P0, P1p);  // ends with a barrier
+    decay_cumsum<kGradThreads>(p, c, h, P0, P1p);  // ends with a barrier
     if (tid < 64) {
         rho[tid] = P0[31 * kLD + tid];
         gC[tid] = P0[63 * kLD + tid];
@@ -854,16 +892,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
     const uint32_t tl = tmem + lane_off + c0;  // this thread's lane, column half
     uint32_t phase = 0;
     bool ok = true;
-    float v[32], x[32];
+    float v[kGW], x[kGW];
 
     // ---- scaled operands: top rows Q, K; bottom rows Cm, R
     {
-        float g[32], gx[32];
+        float g[kGW], gx[kGW];
         plain_row(g, P0, t, c0);
-        if (t > 0) plain_row(gx, P0, t - 1, c0); else zero32(gx);
+        if (t > 0) plain_row(gx, P0, t - 1, c0); else zero_row(gx);
         if (top) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
+            for (int i = 0; i < kGW; ++i) {
                 const float rh = rho[c0 + i];
                 v[i] = kk[i] * __expf(gx[i] - rh);     // Q
                 x[i] = ra[i] * __expf(rh - g[i]);      // K
@@ -876,7 +914,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
             b_col(sm + tcg::kBF2, 64, 64 + t, c0, x);   // K^c
         } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
+            for (int i = 0; i < kGW; ++i) {
                 const float rh = rho[c0 + i];
                 v[i] = kk[i] * ra[i] * __expf(rh - g[i]);  // Cm
                 x[i] = rb[i] * __expf(g[i] - rh);          // R
@@ -890,14 +928,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
     }
     // the next phase's rows, in flight during the Gram products: top S0, Ghat, S_C; bottom V, dO
     if (top) {
-        load_state32(kk, p.Sck + b0 + t * kN + c0);
-        load_state32(ra, p.Eck + cidx + t * kN + c0);
-        load_state32(rb, p.Sck + b1 + t * kN + c0);
+        load_state_row(kk, p.Sck + b0 + t * kN + c0);
+        load_state_row(ra, p.Eck + cidx + t * kN + c0);
+        load_state_row(rb, p.Sck + b1 + t * kN + c0);
     } else if (row_valid) {
-        load32(kk, p.v, p.x_bf16, roff);
-        load32(ra, p.d_o, false, roff);
+        load_row(kk, p.v, p.x_bf16, roff);
+        load_row(ra, p.d_o, false, roff);
     } else {
-        zero32(kk); zero32(ra);
+        zero_row(kk); zero_row(ra);
     }
     ok = mma_stage(bar, phase, p.status, [&] {
         mma_group(tmem, 64, 0, sbase + tcg::kBG, tcg::kAtom256, 192, 64);
@@ -907,21 +945,21 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
     if (ok) {
         // ---- Grams out: Lc -> plain; A_YY2 = [Q | Lk] (top), [Cm | Mc^T] (bottom); A_F3 = [K | Mk^T | -Lk^T]
         if (top) {
-            tmem_ld32(tl + 64, v);
-            mask32<kStrictLower, false>(v, t, c0);
+            tmem_ld_row(tl + 64, v);
+            mask_row<kStrictLower, false>(v, t, c0);
             plain_row_store(P1p, t, c0, v);
-            tmem_ld32(tl + 128, v);
-            mask32<kStrictLower, false>(v, t, c0);
+            tmem_ld_row(tl + 128, v);
+            mask_row<kStrictLower, false>(v, t, c0);
             a_row(tl + 64, v);
-            tmem_ld32(tl + 320, v);
-            mask32<kUpper, false>(v, t, c0);
+            tmem_ld_row(tl + 320, v);
+            mask_row<kUpper, false>(v, t, c0);
             a_row(tl + 320, v);
-            tmem_ld32(tl + 384, v);
-            mask32<kStrictUpper, true>(v, t, c0);
+            tmem_ld_row(tl + 384, v);
+            mask_row<kStrictUpper, true>(v, t, c0);
             a_row(tl + 384, v);
         } else {
-            tmem_ld32(tl + 192, v);
-            mask32<kUpper, false>(v, t, c0);
+            tmem_ld_row(tl + 192, v);
+            mask_row<kUpper, false>(v, t, c0);
             a_row(tl + 64, v);
         }
         __syncthreads();  // Lc complete; B_G no longer read
@@ -931,7 +969,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
             float part = 0.f;
             const float s0s = __expf(rho[t]), gs = __expf(gC[t] - rho[t]);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
+            for (int i = 0; i < kGW; ++i) {
                 part = fmaf(ra[i], rb[i], part);
                 kk[i] *= s0s;  // S0'
                 ra[i] *= gs;   // G'
@@ -951,25 +989,25 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
             mma_group(tmem, 128, 0, sbase + tcg::kBY, tcg::kAtom64, 64, 128);
             mma_group(tmem, 192, 0, sbase + tcg::kBF3, tcg::kAtom64, 64, 128);
         });
-        unit_lower_inverse(P1p, P0, reinterpret_cast<float *>(sm + tcg::kBF3 + 32768));
+        unit_lower_inverse<kGradThreads>(P1p, P0, reinterpret_cast<float *>(sm + tcg::kBF3 + 32768));
         ok = mma_stage(bar, phase, p.status, [] {});
     }
 
     if (ok) {
         // ---- Y -> Y^c, Y2 -> Y2^c; T rows (cols 0..63) and T^T rows (64..127) in the top lanes
         if (top) {
-            tmem_ld32(tl + 128, v);
+            tmem_ld_row(tl + 128, v);
             b_col(sm + tcg::kBY, 64, t, c0, v);
             plain_row(x, P0, t, c0);
             a_row(tl + 0, x);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) x[i] = P0[(c0 + i) * kLD + t];
+            for (int i = 0; i < kGW; ++i) x[i] = P0[(c0 + i) * kLD + t];
             a_row(tl + 64, x);
         } else {
-            tmem_ld32(tl + 192, v);
+            tmem_ld_row(tl + 192, v);
             b_col(sm + tcg::kBY + 16384, 64, t, c0, v);
-            if (row_valid) { load32(kk, p.v, p.x_bf16, roff); load32(ra, p.d_o, false, roff); }
-            else { zero32(kk); zero32(ra); }
+            if (row_valid) { load_row(kk, p.v, p.x_bf16, roff); load_row(ra, p.d_o, false, roff); }
+            else { zero_row(kk); zero_row(ra); }
         }
         ok = mma_stage(bar, phase, p.status, [&] {
             mma_group(tmem, 128, 0, sbase + tcg::kBY, tcg::kAtom64, 64, 64);           // Z = T Y (top)
@@ -981,8 +1019,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
         // ---- Z and U out; A_P = [Z; V], A_Pt = [U; dO], B_P = [dO; U], B_Pt = [V; Z], U^c into B_F3
         unsigned char *bp = sm + tcg::kBY, *bpt = sm + tcg::kPlain0;
         if (top) {
-            tmem_ld32(tl + 128, v);  // Z row t
-            tmem_ld32(tl + 192, x);  // U row t
+            tmem_ld_row(tl + 128, v);  // Z row t
+            tmem_ld_row(tl + 192, x);  // U row t
             a_row(tl + 0, v);
             b_row(bpt, 128, 64 + t, c0, v);
             b_col(sm + tcg::kBF3, 64, 128 + t, c0, x);
@@ -1002,11 +1040,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
 
     if (ok) {
         if (top) {
-            tmem_ld32(tl + 192, v);  // dV row t
+            tmem_ld_row(tl + 192, v);  // dV row t
             if (row_valid) {
                 float *dst = p.dv + ((size_t)(c.tb + t) * p.H + h) * kN + c0;
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
+                for (int q = 0; q < kGW / 4; ++q)
                     reinterpret_cast<float4 *>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
             }
         }
@@ -1017,40 +1055,40 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
 
     if (ok) {
         // ---- masks in place: A_F1 = [Z | P3 | -P4 ; V | P1 | -P2] at 0, A_F2 = [U | P2^T | -P4^T ; dO | P1^T | -P3^T] at 256
-        tmem_ld32(tl + 64, v);
-        mask32<kUpper, false>(v, t, c0);
+        tmem_ld_row(tl + 64, v);
+        mask_row<kUpper, false>(v, t, c0);
         a_row(tl + 64, v);
-        tmem_ld32(tl + 128, v);
-        mask32<kStrictUpper, true>(v, t, c0);
+        tmem_ld_row(tl + 128, v);
+        mask_row<kStrictUpper, true>(v, t, c0);
         a_row(tl + 128, v);
         if (top) {
-            tmem_ld32(tl + 320, v);
-            mask32<kStrictLower, false>(v, t, c0);
+            tmem_ld_row(tl + 320, v);
+            mask_row<kStrictLower, false>(v, t, c0);
             a_row(tl + 320, v);
-            tmem_ld32(tl + 384, v);
-            mask32<kStrictLower, true>(v, t, c0);
+            tmem_ld_row(tl + 384, v);
+            mask_row<kStrictLower, true>(v, t, c0);
             a_row(tl + 384, v);
         } else {
-            tmem_ld32(tl + 320, v);
-            mask32<kLower, false>(v, t, c0);
+            tmem_ld_row(tl + 320, v);
+            mask_row<kLower, false>(v, t, c0);
             a_row(tl + 320, v);
-            tmem_ld32(tl + 384, v);
-            mask32<kLower, true>(v, t, c0);
+            tmem_ld_row(tl + 384, v);
+            mask_row<kLower, true>(v, t, c0);
             a_row(tl + 384, v);
         }
-        tmem_ld32(tl + 448, v);
+        tmem_ld_row(tl + 448, v);
         a_row(tl + 256, v);
     }
-    float wq[16];
+    float wq[4096 / kGradThreads];
     if (ok) {
         // the epilogue's rows (top kk, a; bottom r, k) and w, in flight during the last products
         if (row_valid) {
-            load32(kk, top ? p.kk : p.r, p.x_bf16, roff);
-            load32(ra, top ? p.a : p.k, p.x_bf16, roff);
+            load_row(kk, top ? p.kk : p.r, p.x_bf16, roff);
+            load_row(ra, top ? p.a : p.k, p.x_bf16, roff);
         } else {
-            zero32(kk); zero32(ra);
+            zero_row(kk); zero_row(ra);
         }
-        load_w16(wq, p, c, h);
+        load_w<kGradThreads>(wq, p, c, h);
         ok = mma_stage(bar, phase, p.status, [&] {
             mma_group(tmem, 192, 0, sbase + tcg::kBF1, tcg::kAtom64, 64, 192);    // [dC; dK]
             mma_group(tmem, 448, 256, sbase + tcg::kBF2, tcg::kAtom64, 64, 192);  // [dKr; dR]
@@ -1063,18 +1101,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
         float *Gm = reinterpret_cast<float *>(sm + 0);
         float *PW = reinterpret_cast<float *>(sm + 17408);  // top part, then the cumulative sum
         float *PB = reinterpret_cast<float *>(sm + 34816);  // bottom part
-        decay_cumsum_from(wq, Gm, reinterpret_cast<float *>(sm + 52224));
-        float g[32], acc1[32], acc2[32];
+        decay_cumsum_from<kGradThreads>(wq, Gm, reinterpret_cast<float *>(sm + 52224));
+        float g[kGW], acc1[kGW], acc2[kGW];
         plain_row(g, Gm, t, c0);
-        tmem_ld32(tl + 192, acc1);  // top dC, bottom dK
-        tmem_ld32(tl + 448, acc2);  // top dKr, bottom dR
+        tmem_ld_row(tl + 192, acc1);  // top dC, bottom dK
+        tmem_ld_row(tl + 448, acc2);  // top dKr, bottom dR
         const size_t go = ((size_t)(c.tb + t) * p.H + h) * kN + c0;
-        float Y[32];
+        float Y[kGW];
         if (top) {
-            float gx[32];
-            if (t > 0) plain_row(gx, Gm, t - 1, c0); else zero32(gx);
+            float gx[kGW];
+            if (t > 0) plain_row(gx, Gm, t - 1, c0); else zero_row(gx);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
+            for (int i = 0; i < kGW; ++i) {
                 const float rh = rho[c0 + i];
                 const float dC = -acc1[i] * __expf(rh - g[i]);
                 const float dKr = -acc2[i] * __expf(gx[i] - rh);
@@ -1086,14 +1124,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
             plain_row_store(PW, t, c0, x);
             if (row_valid) {
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
+                for (int q = 0; q < kGW / 4; ++q) {
                     reinterpret_cast<float4 *>(p.da + go)[q] = make_float4(acc1[4 * q], acc1[4 * q + 1], acc1[4 * q + 2], acc1[4 * q + 3]);
                     reinterpret_cast<float4 *>(p.dkk + go)[q] = make_float4(acc2[4 * q], acc2[4 * q + 1], acc2[4 * q + 2], acc2[4 * q + 3]);
                 }
             }
         } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
+            for (int i = 0; i < kGW; ++i) {
                 const float rh = rho[c0 + i];
                 const float dK = acc1[i] * __expf(rh - g[i]);
                 const float dR = acc2[i] * __expf(g[i] - rh);
@@ -1104,7 +1142,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
             plain_row_store(PB, t, c0, x);
             if (row_valid) {
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
+                for (int q = 0; q < kGW / 4; ++q) {
                     reinterpret_cast<float4 *>(p.dk + go)[q] = make_float4(acc1[4 * q], acc1[4 * q + 1], acc1[4 * q + 2], acc1[4 * q + 3]);
                     reinterpret_cast<float4 *>(p.dr + go)[q] = make_float4(acc2[4 * q], acc2[4 * q + 1], acc2[4 * q + 2], acc2[4 * q + 3]);
                 }
@@ -1114,26 +1152,29 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
         {
             // reverse inclusive cumulative sum over tokens per channel, plus the carry
             float *scratch = reinterpret_cast<float *>(sm + 52224);
+            constexpr int kSeg = kGradThreads / 64, kRows = 64 / kSeg;  // row segments of the sum
             const int ch = tid & 63, qt = tid >> 6;
             float run = 0.f;
-            float part[16];
+            float part[kRows];
 #pragma unroll
-            for (int u = 15; u >= 0; --u) {
-                run += PW[(qt * 16 + u) * kLD + ch] + PB[(qt * 16 + u) * kLD + ch];
+            for (int u = kRows - 1; u >= 0; --u) {
+                run += PW[(qt * kRows + u) * kLD + ch] + PB[(qt * kRows + u) * kLD + ch];
                 part[u] = run;
             }
             scratch[qt * kLD + ch] = run;
             __syncthreads();
-            float base = carry[ch] + carry[64 + ch];
-            for (int q = qt + 1; q < 4; ++q) base += scratch[q * kLD + ch];
+            float base = 0.f;
 #pragma unroll
-            for (int u = 0; u < 16; ++u) PW[(qt * 16 + u) * kLD + ch] = part[u] + base;
+            for (int q = 0; q < kGroups; ++q) base += carry[q * 64 + ch];
+            for (int q = qt + 1; q < kSeg; ++q) base += scratch[q * kLD + ch];
+#pragma unroll
+            for (int u = 0; u < kRows; ++u) PW[(qt * kRows + u) * kLD + ch] = part[u] + base;
             __syncthreads();
         }
         if (top && row_valid) {
             plain_row(v, PW, t, c0);
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
+            for (int q = 0; q < kGW / 4; ++q)
                 reinterpret_cast<float4 *>(p.dw + go)[q] = make_float4(v[4 * q] - Y[4 * q], v[4 * q + 1] - Y[4 * q + 1],
                                                                        v[4 * q + 2] - Y[4 * q + 2], v[4 * q + 3] - Y[4 * q + 3]);
         }
@@ -1205,7 +1246,7 @@ cudaError_t launch_prefill_backward(const BackwardArgs &b, void *workspace, cuda
     if (e != cudaSuccess) return e;
     if (nc > 0) {
         const dim3 grid((unsigned)nc, (unsigned)b.H);
-        bwd_grad_tc_kernel<<<grid, kThreads, tcg::kAlloc, stream>>>(p);
+        bwd_grad_tc_kernel<<<grid, kGradThreads, tcg::kAlloc, stream>>>(p);
         e = cudaGetLastError();
     }
     return e;
