@@ -60,8 +60,8 @@ constexpr int kC = 64;            // tokens per chunk
 constexpr int kLD = 68;           // shared-memory row stride in floats (16-B rows, staggered banks)
 constexpr int kMat = kC * kLD;    // floats per 64 x 64 buffer
 constexpr int kThreads = 256;
-// The gradient pass runs 16 warps: a 128 x 64 operand row (TMEM lane) is split over four
-// threads of kGW = 16 columns (kGroups = 4 column groups), the other passes over two of 32.
+// The summary and gradient passes run 16 warps: a 128 x 64 operand row (TMEM lane) is split
+// over four threads of kGW = 16 columns (kGroups = 4 column groups); the chains run 8 warps.
 constexpr int kGradThreads = 512, kGW = 16, kGroups = 4;
 constexpr size_t kMatBytes = (size_t)kMat * sizeof(float);
 constexpr size_t kStateElems = (size_t)kN * kN;
@@ -405,6 +405,11 @@ __device__ __forceinline__ void a_row(uint32_t taddr, const float (&v)[W]) {
     else tmem_st16(taddr, r);
 }
 template <int W>
+__device__ __forceinline__ void tmem_st_row(uint32_t taddr, const uint32_t (&r)[W]) {
+    if constexpr (W == 32) tmem_st32u(taddr, r);
+    else tmem_st16(taddr, r);
+}
+template <int W>
 __device__ __forceinline__ void tmem_ld_row(uint32_t taddr, float (&v)[W]) {
     if constexpr (W == 32) tmem_ld32(taddr, v);
     else tmem_ld16(taddr, v);
@@ -571,7 +576,7 @@ constexpr uint32_t kBytes = 182800;
 constexpr uint32_t kAlloc = kBytes + 1024;
 }  // namespace tcs
 
-__global__ void __launch_bounds__(kThreads, 1) bwd_summary_tc_kernel(BwdArgs p) {
+__global__ void __launch_bounds__(kGradThreads, 1) bwd_summary_tc_kernel(BwdArgs p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -581,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_summary_tc_kernel(BwdArgs p) 
     const uint32_t sbase = smem_addr(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3, hh = warp >> 2;
-    const int L = 32 * quad + lane, t = L & 63, c0 = 32 * hh;
+    const int L = 32 * quad + lane, t = L & 63, c0 = kGW * hh;
     const bool top = L < 64;
     const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
     float *rho = reinterpret_cast<float *>(sm + tcs::kVec), *gC = rho + 64;
@@ -596,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_summary_tc_kernel(BwdArgs p) 
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(sbase + tcs::kBar + 8, tcg::kTmemCols);
-    float kk[32], ra[32], rb[32];  // top: kk, k; bottom: kk, a, r (fetched before the cumulative sum)
+    float kk[kGW], ra[kGW], rb[kGW];  // top: kk, k; bottom: kk, a, r (fetched before the cumulative sum)
     if (row_valid) {
         load_row(kk, p.kk, p.x_bf16, roff);
         load_row(ra, top ? p.k : p.a, p.x_bf16, roff);
@@ -604,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_summary_tc_kernel(BwdArgs p) 
     } else {
         zero_row(kk); zero_row(ra); zero_row(rb);
     }
-    decay_cumsum<kThreads>(p, c, h, P0, P1p);
+    decay_cumsum<kGradThreads>(p, c, h, P0, P1p);
     if (tid < 64) {
         rho[tid] = P0[31 * kLD + tid];
         gC[tid] = P0[63 * kLD + tid];
@@ -616,16 +621,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_summary_tc_kernel(BwdArgs p) 
     const uint32_t tl = tmem + lane_off + c0;
     uint32_t phase = 0;
     bool ok = true;
-    float v[32], x[32];
+    float v[kGW], x[kGW];
 
     // ---- scaled operands (top rows Q, K; bottom rows Cm, R) and the identity [I 0; 0 I] at 256..383
     {
-        float g[32], gx[32];
+        float g[kGW], gx[kGW];
         plain_row(g, P0, t, c0);
         if (t > 0) plain_row(gx, P0, t - 1, c0); else zero_row(gx);
         if (top) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
+            for (int i = 0; i < kGW; ++i) {
                 const float rh = rho[c0 + i];
                 v[i] = kk[i] * __expf(gx[i] - rh);  // Q
                 x[i] = ra[i] * __expf(rh - g[i]);   // K
@@ -638,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_summary_tc_kernel(BwdArgs p) 
             b_col(sm + tcs::kBQc, 64, t, c0, v);
         } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
+            for (int i = 0; i < kGW; ++i) {
                 const float rh = rho[c0 + i];
                 v[i] = kk[i] * ra[i] * __expf(rh - g[i]);  // Cm
                 x[i] = rb[i] * __expf(g[i] - rh);          // R
@@ -649,13 +654,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_summary_tc_kernel(BwdArgs p) 
             b_row(sm + tcs::kBT1, 64, t, c0, v);
             b_row(sm + tcs::kBT2, 64, t, 64 + c0, x);
         }
-        uint32_t id[32];
+        uint32_t id[kGW];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) id[i] = (top && c0 + i == t) ? 0x3f800000u : 0u;
-        tmem_st32u(tl + 256, id);
+        for (int i = 0; i < kGW; ++i) id[i] = (top && c0 + i == t) ? 0x3f800000u : 0u;
+        tmem_st_row(tl + 256, id);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) id[i] = (!top && c0 + i == t) ? 0x3f800000u : 0u;
-        tmem_st32u(tl + 320, id);
+        for (int i = 0; i < kGW; ++i) id[i] = (!top && c0 + i == t) ? 0x3f800000u : 0u;
+        tmem_st_row(tl + 320, id);
     }
     if (!top) {  // V and dO rows, in flight during the first products
         if (row_valid) { load_row(kk, p.v, p.x_bf16, roff); load_row(ra, p.d_o, false, roff); }
@@ -689,10 +694,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_summary_tc_kernel(BwdArgs p) 
             mma_group(tmem, 128, 64, sbase + tcs::kBVc, tcg::kAtom64, 64, 64);    // Lk V (top)
             mma_group(tmem, 192, 64, sbase + tcs::kBdOc, tcg::kAtom64, 64, 64);   // Mc^T dO (bottom)
         });
-        unit_lower_inverse<kThreads>(P1p, P0, reinterpret_cast<float *>(sm + tcs::kBTt));
+        unit_lower_inverse<kGradThreads>(P1p, P0, reinterpret_cast<float *>(sm + tcs::kBTt));
         if (top) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) x[i] = P0[(c0 + i) * kLD + t];
+            for (int i = 0; i < kGW; ++i) x[i] = P0[(c0 + i) * kLD + t];
             b_row(sm + tcs::kBTt, 64, t, c0, x);  // rows t: T[s][t]
         } else {
             plain_row(x, P0, t, c0);
@@ -734,21 +739,21 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_summary_tc_kernel(BwdArgs p) 
             tmem_ld_row(tl + 64, v);
             float *dst = p.Fck + cidx + i * kN + c0;
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
+            for (int q = 0; q < kGW / 4; ++q)
                 reinterpret_cast<float4 *>(dst)[q] = make_float4(sr * v[4 * q], sr * v[4 * q + 1], sr * v[4 * q + 2], sr * v[4 * q + 3]);
             tmem_ld_row(tl + 192, v);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = sr * ((c0 + j == i ? 1.f : 0.f) - v[j]) * __expf(rho[c0 + j]);
+            for (int j = 0; j < kGW; ++j) v[j] = sr * ((c0 + j == i ? 1.f : 0.f) - v[j]) * __expf(rho[c0 + j]);
             dst = p.Ack + cidx + i * kN + c0;
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
+            for (int q = 0; q < kGW / 4; ++q)
                 reinterpret_cast<float4 *>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         } else {
             const float sr = __expf(rho[i]);
             tmem_ld_row(tl + 128, v);
             float *dst = p.Eck + cidx + i * kN + c0;
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
+            for (int q = 0; q < kGW / 4; ++q)
                 reinterpret_cast<float4 *>(dst)[q] = make_float4(sr * v[4 * q], sr * v[4 * q + 1], sr * v[4 * q + 2], sr * v[4 * q + 3]);
         }
     }
@@ -1237,7 +1242,7 @@ cudaError_t launch_prefill_backward(const BackwardArgs &b, void *workspace, cuda
     if (e != cudaSuccess) return e;
     if (nc > 0) {
         const dim3 grid((unsigned)nc, (unsigned)b.H);
-        bwd_summary_tc_kernel<<<grid, kThreads, tcs::kAlloc, stream>>>(p);
+        bwd_summary_tc_kernel<<<grid, kGradThreads, tcs::kAlloc, stream>>>(p);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
