@@ -165,41 +165,6 @@ __device__ __forceinline__ void store_state(float *dst, const float *src) {
     }
 }
 
-// One token row (64 channels) of a packed [T_total, H, 64] input: 16 values
-// from channel c0 for this thread, widened to fp32; zeros past the chunk's end.
-__device__ __forceinline__ void load16(float (&v)[16], const void *src, bool bf16, size_t off, bool valid) {
-    if (!valid) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = 0.f;
-        return;
-    }
-    if (bf16) {
-        const uint4 *p = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(src) + off);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const uint4 u = __ldg(p + h);
-            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                v[h * 8 + 2 * q] = __uint_as_float(w4[q] << 16);
-                v[h * 8 + 2 * q + 1] = __uint_as_float(w4[q] & 0xffff0000u);
-            }
-        }
-    } else {
-        const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(src) + off);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float4 x = __ldg(p + q);
-            v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
-        }
-    }
-}
-__device__ __forceinline__ void store16(float *dst, const float (&v)[16]) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-        *reinterpret_cast<float4 *>(dst + 4 * q) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-}
-
 // The largest s with chunk_base[s] <= g (the sequence that owns global chunk g).
 __device__ __forceinline__ int owner(const int32_t *cb, int num_seqs, int g) {
     int lo = 0, hi = num_seqs;
@@ -324,6 +289,7 @@ constexpr uint32_t kBY = 0;           // [S0'^T | V^c] 64 x 128 (32 KB), stage 2
 constexpr uint32_t kBF3 = 32768;      // [G'^T | dO^c | U^c] 64 x 192 (48 KB), stages 2 and 4
 constexpr uint32_t kBF1 = 81920;      // [G' | R^c | Q^c] 64 x 192 (48 KB), stage 6
 constexpr uint32_t kBF2 = 131072;     // [S0' | K^c | Cm^c] 64 x 192 (48 KB), stage 6
+constexpr uint32_t kStage = 81920;    // epilogue (B_F1, B_F2 done): fp32 64 x 68 tiles of da, dkk, dk, dr, dw
 constexpr uint32_t kPlain0 = 180224;  // fp32 64 x 68: the cumulative decay, then T; then (with kPlain1) B_Pt
 constexpr uint32_t kPlain1 = 197632;  // fp32 64 x 68: Lc
 constexpr uint32_t kVec = 215040;     // rho[64], gC[64], carry parts [4][64]
@@ -333,6 +299,8 @@ constexpr uint32_t kAlloc = kBytes + 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kMaxPolls = 1u << 24;
 constexpr uint32_t kAtom64 = 64 * 128, kAtom128 = 128 * 128, kAtom256 = 256 * 128;
+static_assert(kStage + 5 * kMatBytes <= kPlain0, "gradient staging tiles overlap the plain buffers");
+static_assert((kLD * sizeof(float)) % 16 == 0, "staged rows must start on 16-byte boundaries for the bulk stores");
 }  // namespace tcg
 
 __device__ __forceinline__ uint32_t tf32r(float x) { return __float_as_uint(x) + 0x1000u; }
@@ -1106,12 +1074,12 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
         float *Gm = reinterpret_cast<float *>(sm + 0);
         float *PW = reinterpret_cast<float *>(sm + 17408);  // top part, then the cumulative sum
         float *PB = reinterpret_cast<float *>(sm + 34816);  // bottom part
+        float *const stage = reinterpret_cast<float *>(sm + tcg::kStage);
         decay_cumsum_from<kGradThreads>(wq, Gm, reinterpret_cast<float *>(sm + 52224));
         float g[kGW], acc1[kGW], acc2[kGW];
         plain_row(g, Gm, t, c0);
         tmem_ld_row(tl + 192, acc1);  // top dC, bottom dK
         tmem_ld_row(tl + 448, acc2);  // top dKr, bottom dR
-        const size_t go = ((size_t)(c.tb + t) * p.H + h) * kN + c0;
         float Y[kGW];
         if (top) {
             float gx[kGW];
@@ -1127,13 +1095,8 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
                 acc2[i] = dKr + ra[i] * dC;        // dkk
             }
             plain_row_store(PW, t, c0, x);
-            if (row_valid) {
-#pragma unroll
-                for (int q = 0; q < kGW / 4; ++q) {
-                    reinterpret_cast<float4 *>(p.da + go)[q] = make_float4(acc1[4 * q], acc1[4 * q + 1], acc1[4 * q + 2], acc1[4 * q + 3]);
-                    reinterpret_cast<float4 *>(p.dkk + go)[q] = make_float4(acc2[4 * q], acc2[4 * q + 1], acc2[4 * q + 2], acc2[4 * q + 3]);
-                }
-            }
+            plain_row_store(stage + 0 * kMat, t, c0, acc1);
+            plain_row_store(stage + 1 * kMat, t, c0, acc2);
         } else {
 #pragma unroll
             for (int i = 0; i < kGW; ++i) {
@@ -1145,13 +1108,8 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
                 acc2[i] = dR;
             }
             plain_row_store(PB, t, c0, x);
-            if (row_valid) {
-#pragma unroll
-                for (int q = 0; q < kGW / 4; ++q) {
-                    reinterpret_cast<float4 *>(p.dk + go)[q] = make_float4(acc1[4 * q], acc1[4 * q + 1], acc1[4 * q + 2], acc1[4 * q + 3]);
-                    reinterpret_cast<float4 *>(p.dr + go)[q] = make_float4(acc2[4 * q], acc2[4 * q + 1], acc2[4 * q + 2], acc2[4 * q + 3]);
-                }
-            }
+            plain_row_store(stage + 2 * kMat, t, c0, acc1);
+            plain_row_store(stage + 3 * kMat, t, c0, acc2);
         }
         __syncthreads();
         {
@@ -1176,13 +1134,25 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
             for (int u = 0; u < kRows; ++u) PW[(qt * kRows + u) * kLD + ch] = part[u] + base;
             __syncthreads();
         }
-        if (top && row_valid) {
+        if (top) {
             plain_row(v, PW, t, c0);
 #pragma unroll
-            for (int q = 0; q < kGW / 4; ++q)
-                reinterpret_cast<float4 *>(p.dw + go)[q] = make_float4(v[4 * q] - Y[4 * q], v[4 * q + 1] - Y[4 * q + 1],
-                                                                       v[4 * q + 2] - Y[4 * q + 2], v[4 * q + 3] - Y[4 * q + 3]);
+            for (int i = 0; i < kGW; ++i) v[i] -= Y[i];
+            plain_row_store(stage + 4 * kMat, t, c0, v);
         }
+        // every valid row of the five tiles leaves by one 256-byte bulk copy (a warp's own
+        // stores would touch 32 rows each)
+        fence_proxy_async_smem();
+        __syncthreads();
+        for (int i = tid; i < 5 * kC; i += kGradThreads) {
+            const int gi = i / kC, row = i % kC;
+            float *const dst = gi == 0 ? p.da : gi == 1 ? p.dkk : gi == 2 ? p.dk : gi == 3 ? p.dr : p.dw;
+            if (row < c.len)
+                bulk_store(dst + ((size_t)(c.tb + row) * p.H + h) * kN,
+                           sbase + tcg::kStage + (uint32_t)((gi * kMat + row * kLD) * sizeof(float)), kN * sizeof(float));
+        }
+        bulk_commit();
+        bulk_wait_read<0>();
     }
     tc_fence_before_sync();
     __syncthreads();
