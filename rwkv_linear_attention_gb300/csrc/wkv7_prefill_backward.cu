@@ -290,6 +290,7 @@ constexpr uint32_t kBF3 = 32768;      // [G'^T | dO^c | U^c] 64 x 192 (48 KB), s
 constexpr uint32_t kBF1 = 81920;      // [G' | R^c | Q^c] 64 x 192 (48 KB), stage 6
 constexpr uint32_t kBF2 = 131072;     // [S0' | K^c | Cm^c] 64 x 192 (48 KB), stage 6
 constexpr uint32_t kStage = 81920;    // epilogue (B_F1, B_F2 done): fp32 64 x 68 tiles of da, dkk, dk, dr, dw
+constexpr uint32_t kDv = 32768;       // after stage 4 (B_F3 done) to stage 6: fp32 64 x 68 tile of dV
 constexpr uint32_t kPlain0 = 180224;  // fp32 64 x 68: the cumulative decay, then T; then (with kPlain1) B_Pt
 constexpr uint32_t kPlain1 = 197632;  // fp32 64 x 68: Lc
 constexpr uint32_t kVec = 215040;     // rho[64], gC[64], carry parts [4][64]
@@ -300,6 +301,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kMaxPolls = 1u << 24;
 constexpr uint32_t kAtom64 = 64 * 128, kAtom128 = 128 * 128, kAtom256 = 256 * 128;
 static_assert(kStage + 5 * kMatBytes <= kPlain0, "gradient staging tiles overlap the plain buffers");
+static_assert(kDv >= kBF3 && kDv + kMatBytes <= kBF1, "the dV tile lies outside B_F3");
 static_assert((kLD * sizeof(float)) % 16 == 0, "staged rows must start on 16-byte boundaries for the bulk stores");
 }  // namespace tcg
 
@@ -538,6 +540,8 @@ constexpr uint32_t kBT2 = 98304;      // [K | R] 64 x K 128 (32 KB), stage 1
 constexpr uint32_t kBQc = 131072;     // Q^c (16 KB), stage 3
 constexpr uint32_t kPlain0 = 147456;  // fp32 64 x 68: the cumulative decay, then T
 constexpr uint32_t kPlain1 = 164864;  // fp32 64 x 68: Lc
+constexpr uint32_t kStage = 0;        // after stage 3: fp32 64 x 68 tiles of F, A, E for the bulk row stores
+static_assert(kStage + 3 * kMatBytes <= kPlain0, "output staging tiles overlap the plain buffers");
 constexpr uint32_t kVec = 182272;     // rho[64], gC[64]
 constexpr uint32_t kBar = 182784;     // mbarrier, TMEM base slot
 constexpr uint32_t kBytes = 182800;
@@ -700,30 +704,37 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_summary_tc_kernel(BwdArgs
     }
 
     if (ok) {
-        // ---- out: row i = t of A and F (top), of E (bottom)
+        // ---- out: row i = t of F and A (top), of E (bottom), staged in shared memory (the
+        // stage-3 operands are consumed) and written by one 256-byte bulk copy per row
+        float *const stage = reinterpret_cast<float *>(sm + tcs::kStage);
         const int i = t;
         if (top) {
             const float sr = __expf(gC[i] - rho[i]);
             tmem_ld_row(tl + 64, v);
-            float *dst = p.Fck + cidx + i * kN + c0;
 #pragma unroll
-            for (int q = 0; q < kGW / 4; ++q)
-                reinterpret_cast<float4 *>(dst)[q] = make_float4(sr * v[4 * q], sr * v[4 * q + 1], sr * v[4 * q + 2], sr * v[4 * q + 3]);
+            for (int j = 0; j < kGW; ++j) v[j] *= sr;
+            plain_row_store(stage + 0 * kMat, i, c0, v);
             tmem_ld_row(tl + 192, v);
 #pragma unroll
             for (int j = 0; j < kGW; ++j) v[j] = sr * ((c0 + j == i ? 1.f : 0.f) - v[j]) * __expf(rho[c0 + j]);
-            dst = p.Ack + cidx + i * kN + c0;
-#pragma unroll
-            for (int q = 0; q < kGW / 4; ++q)
-                reinterpret_cast<float4 *>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            plain_row_store(stage + 1 * kMat, i, c0, v);
         } else {
             const float sr = __expf(rho[i]);
             tmem_ld_row(tl + 128, v);
-            float *dst = p.Eck + cidx + i * kN + c0;
 #pragma unroll
-            for (int q = 0; q < kGW / 4; ++q)
-                reinterpret_cast<float4 *>(dst)[q] = make_float4(sr * v[4 * q], sr * v[4 * q + 1], sr * v[4 * q + 2], sr * v[4 * q + 3]);
+            for (int j = 0; j < kGW; ++j) v[j] *= sr;
+            plain_row_store(stage + 2 * kMat, i, c0, v);
         }
+        fence_proxy_async_smem();
+        __syncthreads();
+        for (int j = tid; j < 3 * kN; j += kGradThreads) {
+            const int gi = j / kN, row = j % kN;
+            float *const dst = gi == 0 ? p.Fck : gi == 1 ? p.Ack : p.Eck;
+            bulk_store(dst + cidx + row * kN, sbase + tcs::kStage + (uint32_t)((gi * kMat + row * kLD) * sizeof(float)),
+                       kN * sizeof(float));
+        }
+        bulk_commit();
+        bulk_wait_read<0>();
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -1012,18 +1023,19 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
     }
 
     if (ok) {
+        // dV row t into B_F3 (consumed by stage 4); the stage's barrier and proxy fence
+        // publish it, and one bulk copy per row writes it out beside the masks below
         if (top) {
             tmem_ld_row(tl + 192, v);  // dV row t
-            if (row_valid) {
-                float *dst = p.dv + ((size_t)(c.tb + t) * p.H + h) * kN + c0;
-#pragma unroll
-                for (int q = 0; q < kGW / 4; ++q)
-                    reinterpret_cast<float4 *>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-            }
+            plain_row_store(reinterpret_cast<float *>(sm + tcg::kDv), t, c0, v);
         }
         ok = mma_stage(bar, phase, p.status, [&] {
             mma_group(tmem, 320, 448, sbase + tcg::kPlain0, tcg::kAtom128, 128, 64);  // Pt
         });
+        if (tid < c.len)
+            bulk_store(p.dv + ((size_t)(c.tb + tid) * p.H + h) * kN,
+                       sbase + tcg::kDv + (uint32_t)(tid * kLD * sizeof(float)), kN * sizeof(float));
+        bulk_commit();
     }
 
     if (ok) {
@@ -1062,6 +1074,7 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
             zero_row(kk); zero_row(ra);
         }
         load_w<kGradThreads>(wq, p, c, h);
+        bulk_wait_read<0>();  // dV's tile is read before the epilogue writes over it
         ok = mma_stage(bar, phase, p.status, [&] {
             mma_group(tmem, 192, 0, sbase + tcg::kBF1, tcg::kAtom64, 64, 192);    // [dC; dK]
             mma_group(tmem, 448, 256, sbase + tcg::kBF2, tcg::kAtom64, 64, 192);  // [dKr; dR]
@@ -1152,8 +1165,8 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
                            sbase + tcg::kStage + (uint32_t)((gi * kMat + row * kLD) * sizeof(float)), kN * sizeof(float));
         }
         bulk_commit();
-        bulk_wait_read<0>();
     }
+    bulk_wait_read<0>();  // every row copy has read its tile (also after a timeout)
     tc_fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, tcg::kTmemCols);
