@@ -294,14 +294,20 @@ constexpr uint32_t kDv = 32768;       // after stage 4 (B_F3 done) to stage 6: f
 constexpr uint32_t kPlain0 = 180224;  // fp32 64 x 68: the cumulative decay, then T; then (with kPlain1) B_Pt
 constexpr uint32_t kPlain1 = 197632;  // fp32 64 x 68: Lc
 constexpr uint32_t kVec = 215040;     // rho[64], gC[64], carry parts [4][64]
-constexpr uint32_t kBar = 216576;     // mbarrier, TMEM base slot
-constexpr uint32_t kBytes = 216592;
+constexpr uint32_t kBar = 216576;     // mbarrier, TMEM base slot, the staged states' mbarrier
+constexpr uint32_t kBytes = 216600;
+// S0, Ghat and S_C (16 KB each, unpadded) arrive by bulk copies at the CTA's start and are
+// read in the B-tile step: places no operand uses before then (B_F3's U^c part, B_F1's and
+// B_F2's first K = 64, written in that step after a barrier)
+constexpr uint32_t kSt0 = 65536, kSt1 = 81920, kSt2 = 131072;
 constexpr uint32_t kAlloc = kBytes + 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kMaxPolls = 1u << 24;
 constexpr uint32_t kAtom64 = 64 * 128, kAtom128 = 128 * 128, kAtom256 = 256 * 128;
 static_assert(kStage + 5 * kMatBytes <= kPlain0, "gradient staging tiles overlap the plain buffers");
 static_assert(kDv >= kBF3 && kDv + kMatBytes <= kBF1, "the dV tile lies outside B_F3");
+static_assert(kSt0 >= kBG + 256 * 256 && kSt0 + 16384 <= kBF1 && kSt1 == kBF1 && kSt2 == kBF2,
+              "a staged state overlaps an operand in use before the B-tile step");
 static_assert((kLD * sizeof(float)) % 16 == 0, "staged rows must start on 16-byte boundaries for the bulk stores");
 }  // namespace tcg
 
@@ -506,13 +512,19 @@ __device__ void decay_cumsum(const BwdArgs &p, const Chunk &c, int h, float *Gm,
     decay_cumsum_from<NT>(x, Gm, scratch);
 }
 
-// W values of a 64 x 64 fp32 state row (global).
-template <int W>
-__device__ __forceinline__ void load_state_row(float (&v)[W], const float *src) {
+// Row `row`, columns c0 .. c0 + 15 of an unpadded 64 x 64 fp32 matrix in shared memory.
+// A warp's 32 rows start in one bank, so each lane reads its four 16-byte words in an
+// order rotated by its row (four bank groups per access instead of one).
+__device__ __forceinline__ void staged_row16(float (&v)[16], const float *m, int row, int c0) {
+    const int r = row & 3;
+    float4 w[4];
 #pragma unroll
-    for (int q = 0; q < W / 4; ++q) {
-        const float4 a4 = __ldg(reinterpret_cast<const float4 *>(src) + q);
-        v[4 * q] = a4.x; v[4 * q + 1] = a4.y; v[4 * q + 2] = a4.z; v[4 * q + 3] = a4.w;
+    for (int k = 0; k < 4; ++k) w[k] = *reinterpret_cast<const float4 *>(m + row * kN + c0 + 4 * ((k + r) & 3));
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {  // word q was read at step (q - r) mod 4
+        const int k = (q - r) & 3;
+        const float4 x = k == 0 ? w[0] : k == 1 ? w[1] : k == 2 ? w[2] : w[3];
+        v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
     }
 }
 
@@ -843,7 +855,7 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
     const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
     float *rho = reinterpret_cast<float *>(sm + tcg::kVec), *gC = rho + 64, *carry = gC + 64;  // carry[kGroups][64]
     float *P0 = reinterpret_cast<float *>(sm + tcg::kPlain0), *P1p = reinterpret_cast<float *>(sm + tcg::kPlain1);
-    const uint32_t bar = sbase + tcg::kBar;
+    const uint32_t bar = sbase + tcg::kBar, bar_st = sbase + tcg::kBar + 16;
     const size_t cidx = ((size_t)blockIdx.x * p.H + h) * kStateElems;
     const size_t b0 = ((size_t)(blockIdx.x + c.seq) * p.H + h) * kStateElems;
     const size_t b1 = b0 + (size_t)p.H * kStateElems;
@@ -852,7 +864,12 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
 
     if (tid == 0) {
         mbar_init(bar, 1);
+        mbar_init(bar_st, 1);
         fence_mbar_init();
+        mbar_arrive_expect_tx(bar_st, 3 * kStateElems * sizeof(float));
+        bulk_load(sbase + tcg::kSt0, p.Sck + b0, kStateElems * sizeof(float), bar_st);
+        bulk_load(sbase + tcg::kSt1, p.Eck + cidx, kStateElems * sizeof(float), bar_st);
+        bulk_load(sbase + tcg::kSt2, p.Sck + b1, kStateElems * sizeof(float), bar_st);
     }
     if (warp == 0) tmem_alloc(sbase + tcg::kBar + 8, tcg::kTmemCols);
     // raw rows for the scaled operands, fetched before the cumulative sum needs w
@@ -910,16 +927,15 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
             b_col(sm + tcg::kBF2, 64, 128 + t, c0, v);  // Cm^c
         }
     }
-    // the next phase's rows, in flight during the Gram products: top S0, Ghat, S_C; bottom V, dO
-    if (top) {
-        load_state_row(kk, p.Sck + b0 + t * kN + c0);
-        load_state_row(ra, p.Eck + cidx + t * kN + c0);
-        load_state_row(rb, p.Sck + b1 + t * kN + c0);
-    } else if (row_valid) {
-        load_row(kk, p.v, p.x_bf16, roff);
-        load_row(ra, p.d_o, false, roff);
-    } else {
-        zero_row(kk); zero_row(ra);
+    // the next phase's rows, in flight during the Gram products: bottom V, dO (the top
+    // rows' states come by bulk copy)
+    if (!top) {
+        if (row_valid) {
+            load_row(kk, p.v, p.x_bf16, roff);
+            load_row(ra, p.d_o, false, roff);
+        } else {
+            zero_row(kk); zero_row(ra);
+        }
     }
     ok = mma_stage(bar, phase, p.status, [&] {
         mma_group(tmem, 64, 0, sbase + tcg::kBG, tcg::kAtom256, 192, 64);
@@ -946,8 +962,20 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
             mask_row<kUpper, false>(v, t, c0);
             a_row(tl + 64, v);
         }
-        __syncthreads();  // Lc complete; B_G no longer read
-
+        bool got = true;
+        if (top) {  // this row of S0, Ghat and S_C
+            got = mbar_wait_bounded(bar_st, 0, tcg::kMaxPolls);
+            staged_row16(kk, reinterpret_cast<const float *>(sm + tcg::kSt0), t, c0);
+            staged_row16(ra, reinterpret_cast<const float *>(sm + tcg::kSt1), t, c0);
+            staged_row16(rb, reinterpret_cast<const float *>(sm + tcg::kSt2), t, c0);
+        }
+        // Lc complete; B_G no longer read; the staged states read (B_F1 and B_F2 go over them)
+        if (!__syncthreads_and(got ? 1 : 0)) {
+            if (tid == 0) report(p.status, kDevTimeout);
+            ok = false;
+        }
+    }
+    if (ok) {
         // ---- B tiles from the states, V and dO; the carry rowsum(Ghat .* S_C)
         if (top) {
             float part = 0.f;
@@ -1167,6 +1195,7 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
         bulk_commit();
     }
     bulk_wait_read<0>();  // every row copy has read its tile (also after a timeout)
+    if (tid == 0) mbar_wait_bounded(bar_st, 0, tcg::kMaxPolls);  // the staged states have landed
     tc_fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, tcg::kTmemCols);
