@@ -380,6 +380,13 @@ __device__ __forceinline__ void a_row(uint32_t taddr, const float (&v)[W]) {
     if constexpr (W == 32) tmem_st32u(taddr, r);
     else tmem_st16(taddr, r);
 }
+// As a_row for 16 columns, without the wait (tmem_wait_st before an MMA reads them).
+__device__ __forceinline__ void a_row_issue(uint32_t taddr, const float (&v)[16]) {
+    uint32_t r[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) r[i] = tf32r(v[i]);
+    tmem_st16_issue(taddr, r);
+}
 template <int W>
 __device__ __forceinline__ void tmem_st_row(uint32_t taddr, const uint32_t (&r)[W]) {
     if constexpr (W == 32) tmem_st32u(taddr, r);
@@ -945,23 +952,22 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
     if (ok) {
         // ---- Grams out: Lc -> plain; A_YY2 = [Q | Lk] (top), [Cm | Mc^T] (bottom); A_F3 = [K | Mk^T | -Lk^T]
         if (top) {
-            tmem_ld_row(tl + 64, v);
+            tmem_ld16x2(tl + 64, tl + 128, v, x);
             mask_row<kStrictLower, false>(v, t, c0);
             plain_row_store(P1p, t, c0, v);
-            tmem_ld_row(tl + 128, v);
-            mask_row<kStrictLower, false>(v, t, c0);
-            a_row(tl + 64, v);
-            tmem_ld_row(tl + 320, v);
+            mask_row<kStrictLower, false>(x, t, c0);
+            a_row_issue(tl + 64, x);
+            tmem_ld16x2(tl + 320, tl + 384, v, x);
             mask_row<kUpper, false>(v, t, c0);
-            a_row(tl + 320, v);
-            tmem_ld_row(tl + 384, v);
-            mask_row<kStrictUpper, true>(v, t, c0);
-            a_row(tl + 384, v);
+            a_row_issue(tl + 320, v);
+            mask_row<kStrictUpper, true>(x, t, c0);
+            a_row_issue(tl + 384, x);
         } else {
             tmem_ld_row(tl + 192, v);
             mask_row<kUpper, false>(v, t, c0);
-            a_row(tl + 64, v);
+            a_row_issue(tl + 64, v);
         }
+        tmem_wait_st();
         bool got = true;
         if (top) {  // this row of S0, Ghat and S_C
             got = mbar_wait_bounded(bar_st, 0, tcg::kMaxPolls);
@@ -1068,29 +1074,24 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
 
     if (ok) {
         // ---- masks in place: A_F1 = [Z | P3 | -P4 ; V | P1 | -P2] at 0, A_F2 = [U | P2^T | -P4^T ; dO | P1^T | -P3^T] at 256
-        tmem_ld_row(tl + 64, v);
+        tmem_ld16x2(tl + 64, tl + 128, v, x);
         mask_row<kUpper, false>(v, t, c0);
-        a_row(tl + 64, v);
-        tmem_ld_row(tl + 128, v);
-        mask_row<kStrictUpper, true>(v, t, c0);
-        a_row(tl + 128, v);
+        a_row_issue(tl + 64, v);
+        mask_row<kStrictUpper, true>(x, t, c0);
+        a_row_issue(tl + 128, x);
+        float g3[kGW];
+        tmem_ld16x3(tl + 320, tl + 384, tl + 448, v, x, g3);
         if (top) {
-            tmem_ld_row(tl + 320, v);
             mask_row<kStrictLower, false>(v, t, c0);
-            a_row(tl + 320, v);
-            tmem_ld_row(tl + 384, v);
-            mask_row<kStrictLower, true>(v, t, c0);
-            a_row(tl + 384, v);
+            mask_row<kStrictLower, true>(x, t, c0);
         } else {
-            tmem_ld_row(tl + 320, v);
             mask_row<kLower, false>(v, t, c0);
-            a_row(tl + 320, v);
-            tmem_ld_row(tl + 384, v);
-            mask_row<kLower, true>(v, t, c0);
-            a_row(tl + 384, v);
+            mask_row<kLower, true>(x, t, c0);
         }
-        tmem_ld_row(tl + 448, v);
-        a_row(tl + 256, v);
+        a_row_issue(tl + 320, v);
+        a_row_issue(tl + 384, x);
+        a_row_issue(tl + 256, g3);
+        tmem_wait_st();
     }
     float wq[4096 / kGradThreads];
     if (ok) {
