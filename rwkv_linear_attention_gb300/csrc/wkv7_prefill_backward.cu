@@ -1067,8 +1067,6 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
         } else {
             tmem_ld_row(tl + 192, v);
             b_col(sm + tcg::kBY + 16384, 64, t, c0, v);
-            if (row_valid) { load_row(kk, p.v, p.x_bf16, roff); load_row(ra, p.d_o, false, roff); }
-            else { zero_row(kk); zero_row(ra); }
         }
         ok = mma_stage(bar, phase, p.status, [&] {
             mma_group(tmem, 128, 0, sbase + tcg::kBY, tcg::kAtom64, 64, 64);           // Z = T Y (top)
