@@ -470,29 +470,41 @@ __device__ __forceinline__ void mma_group_acc(uint32_t tmem, uint32_t dcol, uint
                         (accumulate || kq > 0) ? 1u : 0u);
 }
 
-// Operands written -> thread 0 issues, without a commit: the products run while the
-// threads go on, and the next mma_stage's commit and wait cover them too.
+// The products of a stage are issued by two threads, lane 0 of warps 0 and 1 (issuer 0
+// and 1), each taking its own independent groups (a group and whatever accumulates onto
+// its D stay with one issuer, so they keep their order): an issuing thread is held for
+// ~70 cycles per instruction, and every barrier after it waits for its warp.
+constexpr int kIssuers = 2;
+__device__ __forceinline__ int issuer_id() {
+    return (threadIdx.x & 31) == 0 && threadIdx.x < 32 * kIssuers ? static_cast<int>(threadIdx.x >> 5) : -1;
+}
+
+// Operands written -> the issuers issue, without a commit: the products run while the
+// threads go on, and the next mma_stage's commits and wait cover them too.
 template <class F>
 __device__ __forceinline__ void mma_issue(F issue) {
     fence_proxy_async_smem();
     tc_fence_before_sync();
     __syncthreads();
-    if (threadIdx.x == 0) {
+    const int who = issuer_id();
+    if (who >= 0) {
         tc_fence_after_sync();
-        issue();
+        issue(who);
     }
 }
 
-// Operands written -> thread 0 issues and commits -> every thread waits (bounded).
-// The outcome is uniform over the CTA; false after a timeout (reported).
+// Operands written -> the issuers issue and each commits (the mbarrier counts kIssuers
+// arrivals) -> every thread waits (bounded).  The outcome is uniform over the CTA; false
+// after a timeout (reported).
 template <class F>
 __device__ __forceinline__ bool mma_stage(uint32_t bar, uint32_t &phase, unsigned *status, F issue) {
     fence_proxy_async_smem();
     tc_fence_before_sync();
     __syncthreads();
-    if (threadIdx.x == 0) {
+    const int who = issuer_id();
+    if (who >= 0) {
         tc_fence_after_sync();
-        issue();
+        issue(who);
         mma_commit(bar);
     }
     const bool ok = mbar_wait_bounded(bar, phase, tcg::kMaxPolls);
@@ -631,7 +643,7 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_summary_tc_kernel(BwdArgs
     const size_t roff = ((size_t)(c.tb + (row_valid ? t : 0)) * p.H + h) * kN + c0;
 
     if (tid == 0) {
-        mbar_init(bar, 1);
+        mbar_init(bar, kIssuers);
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(sbase + tcs::kBar + 8, tcg::kTmemCols);
@@ -700,10 +712,13 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_summary_tc_kernel(BwdArgs
         if (row_valid) { load_row(kk, p.v, p.x_bf16, roff); load_row(ra, p.d_o, false, roff); }
         else { zero_row(kk); zero_row(ra); }
     }
-    ok = mma_stage(bar, phase, p.status, [&] {
-        mma_group(tmem, 64, 0, sbase + tcs::kBG, tcg::kAtom256, 192, 64);         // G1
-        mma_group(tmem, 384, 256, sbase + tcs::kBT1, tcg::kAtom64, 64, 128);      // [Cm^T; Q^T]
-        mma_group(tmem, 448, 256, sbase + tcs::kBT2, tcg::kAtom64, 64, 128);      // [K^T; R^T]
+    ok = mma_stage(bar, phase, p.status, [&](int who) {
+        if (who == 0) {
+            mma_group(tmem, 64, 0, sbase + tcs::kBG, tcg::kAtom256, 192, 64);     // G1
+            mma_group(tmem, 384, 256, sbase + tcs::kBT1, tcg::kAtom64, 64, 128);  // [Cm^T; Q^T]
+        } else {
+            mma_group(tmem, 448, 256, sbase + tcs::kBT2, tcg::kAtom64, 64, 128);  // [K^T; R^T]
+        }
     });
 
     if (ok) {
@@ -724,9 +739,9 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_summary_tc_kernel(BwdArgs
         }
         // Lk V and Mc^T dO need no T: they run while the threads form it (the inverse's
         // scratch is the T tiles' space, which these products do not read)
-        mma_issue([&] {
-            mma_group(tmem, 128, 64, sbase + tcs::kBVc, tcg::kAtom64, 64, 64);    // Lk V (top)
-            mma_group(tmem, 192, 64, sbase + tcs::kBdOc, tcg::kAtom64, 64, 64);   // Mc^T dO (bottom)
+        mma_issue([&](int who) {
+            if (who == 0) mma_group(tmem, 128, 64, sbase + tcs::kBVc, tcg::kAtom64, 64, 64);   // Lk V (top)
+            else mma_group(tmem, 192, 64, sbase + tcs::kBdOc, tcg::kAtom64, 64, 64);           // Mc^T dO (bottom)
         });
         unit_lower_inverse<kGradThreads>(P1p, P0, reinterpret_cast<float *>(sm + tcs::kBTt));
         if (top) {
@@ -737,9 +752,9 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_summary_tc_kernel(BwdArgs
             plain_row(x, P0, t, c0);
             b_row(sm + tcs::kBTn, 64, t, c0, x);  // rows t: T[t][s]
         }
-        ok = mma_stage(bar, phase, p.status, [&] {
-            mma_group(tmem, 0, 384, sbase + tcs::kBTt, tcg::kAtom64, 64, 64);     // W1 = Cm^T T (top)
-            mma_group(tmem, 256, 384, sbase + tcs::kBTn, tcg::kAtom64, 64, 64);   // W2 = Q^T T^T (bottom)
+        ok = mma_stage(bar, phase, p.status, [&](int who) {
+            if (who == 0) mma_group(tmem, 0, 384, sbase + tcs::kBTt, tcg::kAtom64, 64, 64);  // W1 = Cm^T T (top)
+            else mma_group(tmem, 256, 384, sbase + tcs::kBTn, tcg::kAtom64, 64, 64);         // W2 = Q^T T^T (bottom)
         });
     }
 
@@ -756,12 +771,16 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_summary_tc_kernel(BwdArgs
             tmem_ld_row(tl + 256, v);
             a_row(tl + 256, v);
         }
-        ok = mma_stage(bar, phase, p.status, [&] {
-            mma_group_acc(tmem, 64, 448, sbase + tcs::kBVc, tcg::kAtom64, 64, 64, false, false);         // K^T V
-            mma_group_acc(tmem, 64, 0, sbase + tcs::kBT1, tcg::kAtom64, 64, 64, true, true);             // - W1 (Lk V)
-            mma_group_acc(tmem, 128, 448, sbase + tcs::kBdOc, tcg::kAtom64, 64, 64, false, false);       // R^T dO
-            mma_group_acc(tmem, 128, 256, sbase + tcs::kBT1 + 16384, tcg::kAtom64, 64, 64, true, true);  // - W2 (Mc^T dO)
-            mma_group(tmem, 192, 0, sbase + tcs::kBQc, tcg::kAtom64, 64, 64);                            // W1 Q
+        ok = mma_stage(bar, phase, p.status, [&](int who) {
+            if (who == 0) {
+                mma_group_acc(tmem, 64, 448, sbase + tcs::kBVc, tcg::kAtom64, 64, 64, false, false);    // K^T V
+                mma_group_acc(tmem, 64, 0, sbase + tcs::kBT1, tcg::kAtom64, 64, 64, true, true);        // - W1 (Lk V)
+                mma_group(tmem, 192, 0, sbase + tcs::kBQc, tcg::kAtom64, 64, 64);                       // W1 Q
+            } else {
+                mma_group_acc(tmem, 128, 448, sbase + tcs::kBdOc, tcg::kAtom64, 64, 64, false, false);  // R^T dO
+                mma_group_acc(tmem, 128, 256, sbase + tcs::kBT1 + 16384, tcg::kAtom64, 64, 64, true,
+                              true);                                                                    // - W2 (Mc^T dO)
+            }
         });
     }
 
@@ -913,7 +932,7 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
     const size_t roff = ((size_t)(c.tb + (row_valid ? t : 0)) * p.H + h) * kN + c0;  // this thread's token row, half
 
     if (tid == 0) {
-        mbar_init(bar, 1);
+        mbar_init(bar, kIssuers);
         mbar_init(bar_st, 1);
         fence_mbar_init();
         mbar_arrive_expect_tx(bar_st, 3 * kStateElems * sizeof(float));
@@ -987,9 +1006,9 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
             zero_row(kk); zero_row(ra);
         }
     }
-    ok = mma_stage(bar, phase, p.status, [&] {
-        mma_group(tmem, 64, 0, sbase + tcg::kBG, tcg::kAtom256, 192, 64);
-        mma_group(tmem, 320, 256, sbase + tcg::kBG + 128 * 128, tcg::kAtom256, 128, 64);
+    ok = mma_stage(bar, phase, p.status, [&](int who) {
+        if (who == 0) mma_group(tmem, 64, 0, sbase + tcg::kBG, tcg::kAtom256, 192, 64);
+        else mma_group(tmem, 320, 256, sbase + tcg::kBG + 128 * 128, tcg::kAtom256, 128, 64);
     });
 
     if (ok) {
@@ -1046,12 +1065,12 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
         }
         // Y and Y2 need no T: they run while the threads form it (the inverse's scratch lies
         // past the part of B_F3 these products read)
-        mma_issue([&] {
-            mma_group(tmem, 128, 0, sbase + tcg::kBY, tcg::kAtom64, 64, 128);
-            mma_group(tmem, 192, 0, sbase + tcg::kBF3, tcg::kAtom64, 64, 128);
+        mma_issue([&](int who) {
+            if (who == 0) mma_group(tmem, 128, 0, sbase + tcg::kBY, tcg::kAtom64, 64, 128);
+            else mma_group(tmem, 192, 0, sbase + tcg::kBF3, tcg::kAtom64, 64, 128);
         });
         unit_lower_inverse<kGradThreads>(P1p, P0, reinterpret_cast<float *>(sm + tcg::kBF3 + 32768));
-        ok = mma_stage(bar, phase, p.status, [] {});
+        ok = mma_stage(bar, phase, p.status, [](int) {});
     }
 
     if (ok) {
@@ -1068,9 +1087,9 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
             tmem_ld_row(tl + 192, v);
             b_col(sm + tcg::kBY + 16384, 64, t, c0, v);
         }
-        ok = mma_stage(bar, phase, p.status, [&] {
-            mma_group(tmem, 128, 0, sbase + tcg::kBY, tcg::kAtom64, 64, 64);           // Z = T Y (top)
-            mma_group(tmem, 192, 64, sbase + tcg::kBY + 16384, tcg::kAtom64, 64, 64);  // U = T^T Y2 (top)
+        ok = mma_stage(bar, phase, p.status, [&](int who) {
+            if (who == 0) mma_group(tmem, 128, 0, sbase + tcg::kBY, tcg::kAtom64, 64, 64);  // Z = T Y (top)
+            else mma_group(tmem, 192, 64, sbase + tcg::kBY + 16384, tcg::kAtom64, 64, 64);  // U = T^T Y2 (top)
         });
     }
 
@@ -1091,9 +1110,9 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
             b_row(bp, 128, t, c0, ra);   // dO
             a_row(tl + 448, ra);
         }
-        ok = mma_stage(bar, phase, p.status, [&] {
-            mma_group(tmem, 192, 256, sbase + tcg::kBF3, tcg::kAtom64, 64, 192);  // dV (top)
-            mma_group(tmem, 64, 0, sbase + tcg::kBY, tcg::kAtom128, 128, 64);      // P
+        ok = mma_stage(bar, phase, p.status, [&](int who) {
+            if (who == 0) mma_group(tmem, 192, 256, sbase + tcg::kBF3, tcg::kAtom64, 64, 192);  // dV (top)
+            else mma_group(tmem, 64, 0, sbase + tcg::kBY, tcg::kAtom128, 128, 64);              // P
         });
     }
 
@@ -1104,8 +1123,8 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
             tmem_ld_row(tl + 192, v);  // dV row t
             plain_row_store(reinterpret_cast<float *>(sm + tcg::kDv), t, c0, v);
         }
-        ok = mma_stage(bar, phase, p.status, [&] {
-            mma_group(tmem, 320, 448, sbase + tcg::kPlain0, tcg::kAtom128, 128, 64);  // Pt
+        ok = mma_stage(bar, phase, p.status, [&](int who) {
+            if (who == 0) mma_group(tmem, 320, 448, sbase + tcg::kPlain0, tcg::kAtom128, 128, 64);  // Pt
         });
         if (tid < c.len)
             bulk_store(p.dv + ((size_t)(c.tb + tid) * p.H + h) * kN,
@@ -1145,9 +1164,9 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
         }
         load_w<kGradThreads>(wq, p, c, h);
         bulk_wait_read<0>();  // dV's tile is read before the epilogue writes over it
-        ok = mma_stage(bar, phase, p.status, [&] {
-            mma_group(tmem, 192, 0, sbase + tcg::kBF1, tcg::kAtom64, 64, 192);    // [dC; dK]
-            mma_group(tmem, 448, 256, sbase + tcg::kBF2, tcg::kAtom64, 64, 192);  // [dKr; dR]
+        ok = mma_stage(bar, phase, p.status, [&](int who) {
+            if (who == 0) mma_group(tmem, 192, 0, sbase + tcg::kBF1, tcg::kAtom64, 64, 192);  // [dC; dK]
+            else mma_group(tmem, 448, 256, sbase + tcg::kBF2, tcg::kAtom64, 64, 192);         // [dKr; dR]
         });
     }
 
