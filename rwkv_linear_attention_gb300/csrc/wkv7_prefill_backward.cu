@@ -898,7 +898,7 @@ __global__ void __launch_bounds__(kThreads) bwd_chain_kernel(BwdArgs p) {
 // (C^T = B A^T) or from transposed stores into the B tile, never from moving
 // data between lanes.
 //
-// Stages (each: operands written -> one thread issues -> commit -> all wait):
+// Stages (each: operands written -> two threads issue their groups -> each commits -> all wait):
 //   1  G1 = [Q; Cm] x [Cm; K; R]^T -> Lc, Lk (top), Mc^T (bottom);
 //      G2 = K x [R; Q]^T            -> Mk^T, Lk^T (top)
 //   2  Y  = [Q | Lk] x [S0'^T | V^c]^T (top);  Y2 = [Cm | Mc^T] x [G'^T | dO^c]^T (bottom)
