@@ -84,6 +84,7 @@ struct BwdArgs {
     float *Ack;  // [n_chunks, H, 64, 64]
     float *Fck;  // [n_chunks, H, 64, 64]
     float *Eck;  // [n_chunks, H, 64, 64]; E, then overwritten by the adjoint at the chunk end
+    float *Tck;  // [n_chunks, H, 64, 64] T = (I + L_c)^{-1}, from the summary pass to the gradient pass
     unsigned *status;  // device status word
 };
 
@@ -294,8 +295,8 @@ constexpr uint32_t kDv = 32768;       // after stage 4 (B_F3 done) to stage 6: f
 constexpr uint32_t kPlain0 = 180224;  // fp32 64 x 68: the cumulative decay, then T; then (with kPlain1) B_Pt
 constexpr uint32_t kPlain1 = 197632;  // fp32 64 x 68: Lc
 constexpr uint32_t kVec = 215040;     // rho[64], gC[64], carry parts [4][64]
-constexpr uint32_t kBar = 216576;     // mbarrier, TMEM base slot, the staged states' mbarrier
-constexpr uint32_t kBytes = 216600;
+constexpr uint32_t kBar = 216576;     // mbarrier, TMEM base slot, the staged states' and T's mbarriers
+constexpr uint32_t kBytes = 216608;
 // S0, Ghat and S_C (16 KB each, unpadded) arrive by bulk copies at the CTA's start and are
 // read in the B-tile step: places no operand uses before then (B_F3's U^c part, B_F1's and
 // B_F2's first K = 64, written in that step after a barrier)
@@ -756,6 +757,12 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_summary_tc_kernel(BwdArgs
             if (who == 0) mma_group(tmem, 0, 384, sbase + tcs::kBTt, tcg::kAtom64, 64, 64);  // W1 = Cm^T T (top)
             else mma_group(tmem, 256, 384, sbase + tcs::kBTn, tcg::kAtom64, 64, 64);         // W2 = Q^T T^T (bottom)
         });
+        // T for the gradient pass, one 256-byte bulk copy per row (the stage's barrier and
+        // proxy fence published it; nothing writes the plain buffer again)
+        if (tid < kC)
+            bulk_store(p.Tck + cidx + tid * kN, sbase + tcs::kPlain0 + (uint32_t)(tid * kLD * sizeof(float)),
+                       kN * sizeof(float));
+        bulk_commit();
     }
 
     if (ok) {
@@ -815,8 +822,8 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_summary_tc_kernel(BwdArgs
                        kN * sizeof(float));
         }
         bulk_commit();
-        bulk_wait_read<0>();
     }
+    bulk_wait_read<0>();  // T's and the outputs' row copies have read their tiles (also after a timeout)
     tc_fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, tcg::kTmemCols);
@@ -924,7 +931,7 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
     const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
     float *rho = reinterpret_cast<float *>(sm + tcg::kVec), *gC = rho + 64, *carry = gC + 64;  // carry[kGroups][64]
     float *P0 = reinterpret_cast<float *>(sm + tcg::kPlain0), *P1p = reinterpret_cast<float *>(sm + tcg::kPlain1);
-    const uint32_t bar = sbase + tcg::kBar, bar_st = sbase + tcg::kBar + 16;
+    const uint32_t bar = sbase + tcg::kBar, bar_st = sbase + tcg::kBar + 16, bar_t = sbase + tcg::kBar + 24;
     const size_t cidx = ((size_t)blockIdx.x * p.H + h) * kStateElems;
     const size_t b0 = ((size_t)(blockIdx.x + c.seq) * p.H + h) * kStateElems;
     const size_t b1 = b0 + (size_t)p.H * kStateElems;
@@ -934,6 +941,7 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
     if (tid == 0) {
         mbar_init(bar, kIssuers);
         mbar_init(bar_st, 1);
+        mbar_init(bar_t, 1);
         fence_mbar_init();
         mbar_arrive_expect_tx(bar_st, 3 * kStateElems * sizeof(float));
         bulk_load(sbase + tcg::kSt0, p.Sck + b0, kStateElems * sizeof(float), bar_st);
@@ -1010,18 +1018,24 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
         if (who == 0) mma_group(tmem, 64, 0, sbase + tcg::kBG, tcg::kAtom256, 192, 64);
         else mma_group(tmem, 320, 256, sbase + tcg::kBG + 128 * 128, tcg::kAtom256, 128, 64);
     });
+    // T from the summary pass into the plain buffer (the cumulative decay there has been
+    // read), unpadded, in flight during the Gram readout and the B tiles
+    bool t_issued = false;
+    if (ok && tid == 0) {
+        mbar_arrive_expect_tx(bar_t, kStateElems * sizeof(float));
+        bulk_load(sbase + tcg::kPlain0, p.Tck + cidx, kStateElems * sizeof(float), bar_t);
+        t_issued = true;
+    }
 
     if (ok) {
         // ---- Grams out: Lc -> plain; A_YY2 = [Q | Lk] (top), [Cm | Mc^T] (bottom); A_F3 = [K | Mk^T | -Lk^T]
-        if (top) {
-            tmem_ld16x2(tl + 64, tl + 128, v, x);
-            mask_row<kStrictLower, false>(v, t, c0);
-            plain_row_store(P1p, t, c0, v);
+        if (top) {  // (L_c, in columns 64.., is not needed here: T comes from the summary pass)
+            tmem_ld16x2(tl + 128, tl + 320, x, v);
             mask_row<kStrictLower, false>(x, t, c0);
             a_row_issue(tl + 64, x);
-            tmem_ld16x2(tl + 320, tl + 384, v, x);
             mask_row<kUpper, false>(v, t, c0);
             a_row_issue(tl + 320, v);
+            tmem_ld_row(tl + 384, x);
             mask_row<kStrictUpper, true>(x, t, c0);
             a_row_issue(tl + 384, x);
         } else {
@@ -1063,14 +1077,10 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
             b_col(sm + tcg::kBY, 64, 64 + t, c0, kk);    // V^c
             b_col(sm + tcg::kBF3, 64, 64 + t, c0, ra);   // dO^c
         }
-        // Y and Y2 need no T: they run while the threads form it (the inverse's scratch lies
-        // past the part of B_F3 these products read)
-        mma_issue([&](int who) {
-            if (who == 0) mma_group(tmem, 128, 0, sbase + tcg::kBY, tcg::kAtom64, 64, 128);
-            else mma_group(tmem, 192, 0, sbase + tcg::kBF3, tcg::kAtom64, 64, 128);
+        ok = mma_stage(bar, phase, p.status, [&](int who) {
+            if (who == 0) mma_group(tmem, 128, 0, sbase + tcg::kBY, tcg::kAtom64, 64, 128);  // Y
+            else mma_group(tmem, 192, 0, sbase + tcg::kBF3, tcg::kAtom64, 64, 128);          // Y2
         });
-        unit_lower_inverse<kGradThreads>(P1p, P0, reinterpret_cast<float *>(sm + tcg::kBF3 + 32768));
-        ok = mma_stage(bar, phase, p.status, [](int) {});
     }
 
     if (ok) {
@@ -1078,10 +1088,11 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
         if (top) {
             tmem_ld_row(tl + 128, v);
             b_col(sm + tcg::kBY, 64, t, c0, v);
-            plain_row(x, P0, t, c0);
+            if (!mbar_wait_bounded(bar_t, 0, tcg::kMaxPolls)) report(p.status, kDevTimeout);
+            staged_row16(x, P0, t, c0);  // T, unpadded
             a_row(tl + 0, x);
 #pragma unroll
-            for (int i = 0; i < kGW; ++i) x[i] = P0[(c0 + i) * kLD + t];
+            for (int i = 0; i < kGW; ++i) x[i] = P0[(c0 + i) * kN + t];
             a_row(tl + 64, x);
         } else {
             tmem_ld_row(tl + 192, v);
@@ -1256,7 +1267,10 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
         bulk_commit();
     }
     bulk_wait_read<0>();  // every row copy has read its tile (also after a timeout)
-    if (tid == 0) mbar_wait_bounded(bar_st, 0, tcg::kMaxPolls);  // the staged states have landed
+    if (tid == 0) {  // the staged states and T have landed before the shared memory goes away
+        mbar_wait_bounded(bar_st, 0, tcg::kMaxPolls);
+        if (t_issued) mbar_wait_bounded(bar_t, 0, tcg::kMaxPolls);
+    }
     tc_fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, tcg::kTmemCols);
@@ -1271,7 +1285,7 @@ size_t prefill_backward_workspace_bytes(int num_seqs, int T_total, int H) {
     const long long nc = prefill_backward_max_chunks(num_seqs, T_total);
     const size_t table = ((size_t)(num_seqs + 1) * sizeof(int32_t) + 255) & ~(size_t)255;
     const size_t mat = kStateElems * sizeof(float);
-    return table + (size_t)(4 * nc + num_seqs) * H * mat;
+    return table + (size_t)(5 * nc + num_seqs) * H * mat;
 }
 
 cudaError_t launch_prefill_backward(const BackwardArgs &b, void *workspace, cudaStream_t stream) {
@@ -1309,6 +1323,7 @@ cudaError_t launch_prefill_backward(const BackwardArgs &b, void *workspace, cuda
     p.Ack = p.Sck + (size_t)(nc + b.num_seqs) * plane;
     p.Fck = p.Ack + (size_t)nc * plane;
     p.Eck = p.Fck + (size_t)nc * plane;
+    p.Tck = p.Eck + (size_t)nc * plane;
 
     bwd_chunk_table_kernel<<<1, 1024, 0, stream>>>(b.cu_seqlens, b.num_seqs, b.T_total, p.chunk_base, b.status);
     e = cudaGetLastError();
