@@ -169,3 +169,40 @@ def test_rejects_bad_arguments(dev):
     with pytest.raises(wkv7.WKV7Error):  # a gradient aliasing an input
         wkv7.prefill_backward(p["r"], p["w"], p["k"], p["v"], p["kk"], p["a"], cu.to(dev), d_o,
                               grads=(p["r"],) + grads[1:])
+
+
+def test_backward_concurrent_on_two_streams(dev):
+    """Two backward calls with distinct workspaces and gradient buffers, issued on two
+    streams so that their kernels overlap (every chunk-head's states and T travel
+    through its call's workspace by bulk copies): each result is bit-identical to the
+    same call run alone, and within the bound of the oracle."""
+    cases = [([300, 77, 0, 129], 3, torch.bfloat16, 2700), ([2048], 2, torch.float32, 2701)]
+    runs = []
+    for lens, H, dtype, seed in cases:
+        p, cu, d_o, dsf, s0 = _case(lens, H, dtype, dev, seed=seed)
+        T_total = int(cu[-1])
+        ws = torch.empty(wkv7.prefill_backward_workspace_size(len(lens), T_total, H), dtype=torch.uint8, device=dev)
+        ref = wkv7.prefill_backward(p["r"], p["w"], p["k"], p["v"], p["kk"], p["a"], cu.to(dev), d_o,
+                                    initial_state=s0, d_final_state=dsf, workspace=ws, cu_seqlens_host=cu)
+        runs.append((p, cu, d_o, dsf, s0, ws, tuple(None if g is None else g.clone() for g in ref)))
+    torch.cuda.synchronize()
+    wkv7.check_device_status()
+    streams = [torch.cuda.Stream(device=dev) for _ in runs]
+    for _ in range(3):
+        outs = []
+        for (p, cu, d_o, dsf, s0, ws, ref), st in zip(runs, streams):
+            grads = tuple(torch.full_like(g, float("nan")) for g in ref[:6])
+            st.wait_stream(torch.cuda.current_stream(dev))
+            with torch.cuda.stream(st):
+                got = wkv7.prefill_backward(p["r"], p["w"], p["k"], p["v"], p["kk"], p["a"], cu.to(dev), d_o,
+                                            initial_state=s0, d_final_state=dsf, grads=grads, workspace=ws,
+                                            cu_seqlens_host=cu, stream=st)
+            outs.append(got)
+        torch.cuda.synchronize()
+        wkv7.check_device_status()
+        for got, run in zip(outs, runs):
+            for x, y in zip(got, run[6]):
+                if y is not None:
+                    assert torch.equal(x, y)
+    for p, cu, d_o, dsf, s0, _, ref in runs:
+        _compare(ref, _oracle(p, cu, d_o, dsf, s0))
