@@ -409,8 +409,8 @@ WKV7_API wkv7_status wkv7_prefill_noalloc(int num_seqs, int T_total, int H, int 
  *   d_initial_state  : fp32 [num_seqs, H, N, N] or NULL (not written)
  *   workspace        : device memory, 16-byte aligned, of at least
  *                      wkv7_prefill_backward_workspace_size(num_seqs, T_total,
- *                      H, N) bytes (about 1.25 KB per token and head: the
- *                      state at every 64-token boundary plus four 64 x 64
+ *                      H, N) bytes (about 1.5 KB per token and head: the
+ *                      state at every 64-token boundary plus five 64 x 64
  *                      matrices per chunk); contents need not be initialised.
  *
  * Every written range must not overlap any other argument.  Zero-length

@@ -85,6 +85,7 @@ struct BwdArgs {
     float *Fck;  // [n_chunks, H, 64, 64]
     float *Eck;  // [n_chunks, H, 64, 64]; E, then overwritten by the adjoint at the chunk end
     float *Tck;  // [n_chunks, H, 64, 64] T = (I + L_c)^{-1}, from the summary pass to the gradient pass
+    float *Gck;  // [n_chunks, H, 64, 64] the cumulative log-decay g, likewise
     unsigned *status;  // device status word
 };
 
@@ -295,8 +296,8 @@ constexpr uint32_t kDv = 32768;       // after stage 4 (B_F3 done) to stage 6: f
 constexpr uint32_t kPlain0 = 180224;  // fp32 64 x 68: the cumulative decay, then T; then (with kPlain1) B_Pt
 constexpr uint32_t kPlain1 = 197632;  // fp32 64 x 68: Lc
 constexpr uint32_t kVec = 215040;     // rho[64], gC[64], carry parts [4][64]
-constexpr uint32_t kBar = 216576;     // mbarrier, TMEM base slot, the staged states' and T's mbarriers
-constexpr uint32_t kBytes = 216608;
+constexpr uint32_t kBar = 216576;     // mbarrier, TMEM base slot; mbarriers of the states, T, the decay table
+constexpr uint32_t kBytes = 216616;
 // S0, Ghat and S_C (16 KB each, unpadded) arrive by bulk copies at the CTA's start and are
 // read in the B-tile step: places no operand uses before then (B_F3's U^c part, B_F1's and
 // B_F2's first K = 64, written in that step after a barrier)
@@ -307,6 +308,7 @@ constexpr uint32_t kMaxPolls = 1u << 24;
 constexpr uint32_t kAtom64 = 64 * 128, kAtom128 = 128 * 128, kAtom256 = 256 * 128;
 static_assert(kStage + 5 * kMatBytes <= kPlain0, "gradient staging tiles overlap the plain buffers");
 static_assert(kDv >= kBF3 && kDv + kMatBytes <= kBF1, "the dV tile lies outside B_F3");
+static_assert(kPlain1 == kPlain0 + kMatBytes && kPlain1 + kMatBytes <= kVec, "B_Pt spans both plain buffers");
 static_assert(kSt0 >= kBG + 256 * 256 && kSt0 + 16384 <= kBF1 && kSt1 == kBF1 && kSt2 == kBF2,
               "a staged state overlaps an operand in use before the B-tile step");
 static_assert((kLD * sizeof(float)) % 16 == 0, "staged rows must start on 16-byte boundaries for the bulk stores");
@@ -661,9 +663,16 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_summary_tc_kernel(BwdArgs
         rho[tid] = P0[31 * kLD + tid];
         gC[tid] = P0[63 * kLD + tid];
     }
+    fence_proxy_async_smem();
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
+    // the decay table for the gradient pass, one 256-byte bulk copy per row (read before
+    // the inverse writes T over it)
+    if (tid < kC)
+        bulk_store(p.Gck + cidx + tid * kN, sbase + tcs::kPlain0 + (uint32_t)(tid * kLD * sizeof(float)),
+                   kN * sizeof(float));
+    bulk_commit();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm + tcs::kBar + 8);
     const uint32_t tl = tmem + lane_off + c0;
     uint32_t phase = 0;
@@ -739,7 +748,9 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_summary_tc_kernel(BwdArgs
             b_col(sm + tcs::kBdOc, 64, t, c0, ra);
         }
         // Lk V and Mc^T dO need no T: they run while the threads form it (the inverse's
-        // scratch is the T tiles' space, which these products do not read)
+        // scratch is the T tiles' space, which these products do not read); the decay
+        // table's row copies have read the plain buffer before the inverse writes it
+        bulk_wait_read<0>();
         mma_issue([&](int who) {
             if (who == 0) mma_group(tmem, 128, 64, sbase + tcs::kBVc, tcg::kAtom64, 64, 64);   // Lk V (top)
             else mma_group(tmem, 192, 64, sbase + tcs::kBdOc, tcg::kAtom64, 64, 64);           // Mc^T dO (bottom)
@@ -930,8 +941,9 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
     const bool top = L < 64;
     const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
     float *rho = reinterpret_cast<float *>(sm + tcg::kVec), *gC = rho + 64, *carry = gC + 64;  // carry[kGroups][64]
-    float *P0 = reinterpret_cast<float *>(sm + tcg::kPlain0), *P1p = reinterpret_cast<float *>(sm + tcg::kPlain1);
-    const uint32_t bar = sbase + tcg::kBar, bar_st = sbase + tcg::kBar + 16, bar_t = sbase + tcg::kBar + 24;
+    float *P0 = reinterpret_cast<float *>(sm + tcg::kPlain0);
+    const uint32_t bar = sbase + tcg::kBar, bar_st = sbase + tcg::kBar + 16, bar_t = sbase + tcg::kBar + 24,
+                   bar_g = sbase + tcg::kBar + 32;
     const size_t cidx = ((size_t)blockIdx.x * p.H + h) * kStateElems;
     const size_t b0 = ((size_t)(blockIdx.x + c.seq) * p.H + h) * kStateElems;
     const size_t b1 = b0 + (size_t)p.H * kStateElems;
@@ -942,7 +954,12 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
         mbar_init(bar, kIssuers);
         mbar_init(bar_st, 1);
         mbar_init(bar_t, 1);
+        mbar_init(bar_g, 1);
         fence_mbar_init();
+        // the decay table (from the summary pass; unpadded) into the plain buffer, and
+        // later into the epilogue's space: phases 0 and 1 of bar_g
+        mbar_arrive_expect_tx(bar_g, kStateElems * sizeof(float));
+        bulk_load(sbase + tcg::kPlain0, p.Gck + cidx, kStateElems * sizeof(float), bar_g);
         mbar_arrive_expect_tx(bar_st, 3 * kStateElems * sizeof(float));
         bulk_load(sbase + tcg::kSt0, p.Sck + b0, kStateElems * sizeof(float), bar_st);
         bulk_load(sbase + tcg::kSt1, p.Eck + cidx, kStateElems * sizeof(float), bar_st);
@@ -958,10 +975,12 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
     } else {
         zero_row(kk); zero_row(ra); zero_row(rb);
     }
-    decay_cumsum<kGradThreads>(p, c, h, P0, P1p);  // ends with a barrier
+    __syncthreads();  // the mbarriers are initialised
+    const bool got_g = mbar_wait_bounded(bar_g, 0, tcg::kMaxPolls);
+    if (!got_g && tid == 0) report(p.status, kDevTimeout);
     if (tid < 64) {
-        rho[tid] = P0[31 * kLD + tid];
-        gC[tid] = P0[63 * kLD + tid];
+        rho[tid] = P0[31 * kN + tid];
+        gC[tid] = P0[63 * kN + tid];
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -975,8 +994,8 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
     // ---- scaled operands: top rows Q, K; bottom rows Cm, R
     {
         float g[kGW], gx[kGW];
-        plain_row(g, P0, t, c0);
-        if (t > 0) plain_row(gx, P0, t - 1, c0); else zero_row(gx);
+        staged_row16(g, P0, t, c0);  // the decay table, unpadded
+        if (t > 0) staged_row16(gx, P0, t - 1, c0); else zero_row(gx);
         if (top) {
 #pragma unroll
             for (int i = 0; i < kGW; ++i) {
@@ -1164,16 +1183,21 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
         a_row_issue(tl + 256, g3);
         tmem_wait_st();
     }
-    float wq[4096 / kGradThreads];
+    bool g2_issued = false;
     if (ok) {
-        // the epilogue's rows (top kk, a; bottom r, k) and w, in flight during the last products
+        // the epilogue's rows (top kk, a; bottom r, k) and the decay table again (B_P's space
+        // is free), in flight during the last products
         if (row_valid) {
             load_row(kk, top ? p.kk : p.r, p.x_bf16, roff);
             load_row(ra, top ? p.a : p.k, p.x_bf16, roff);
         } else {
             zero_row(kk); zero_row(ra);
         }
-        load_w<kGradThreads>(wq, p, c, h);
+        if (tid == 0) {
+            mbar_arrive_expect_tx(bar_g, kStateElems * sizeof(float));
+            bulk_load(sbase + 0, p.Gck + cidx, kStateElems * sizeof(float), bar_g);
+            g2_issued = true;
+        }
         bulk_wait_read<0>();  // dV's tile is read before the epilogue writes over it
         ok = mma_stage(bar, phase, p.status, [&](int who) {
             if (who == 0) mma_group(tmem, 192, 0, sbase + tcg::kBF1, tcg::kAtom64, 64, 192);  // [dC; dK]
@@ -1184,19 +1208,19 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
     if (ok) {
         // ---- epilogue: top rows hold dC, dKr; bottom rows dK, dR.  Each half writes its
         // part of W = r dr - k dk - c dC + kk dKr; the reverse cumulative sum adds them.
-        float *Gm = reinterpret_cast<float *>(sm + 0);
+        const float *Gm = reinterpret_cast<const float *>(sm + 0);  // the decay table, unpadded
         float *PW = reinterpret_cast<float *>(sm + 17408);  // top part, then the cumulative sum
         float *PB = reinterpret_cast<float *>(sm + 34816);  // bottom part
         float *const stage = reinterpret_cast<float *>(sm + tcg::kStage);
-        decay_cumsum_from<kGradThreads>(wq, Gm, reinterpret_cast<float *>(sm + 52224));
+        if (!mbar_wait_bounded(bar_g, 1, tcg::kMaxPolls)) report(p.status, kDevTimeout);
         float g[kGW], acc1[kGW], acc2[kGW];
-        plain_row(g, Gm, t, c0);
+        staged_row16(g, Gm, t, c0);
         tmem_ld_row(tl + 192, acc1);  // top dC, bottom dK
         tmem_ld_row(tl + 448, acc2);  // top dKr, bottom dR
         float Y[kGW];
         if (top) {
             float gx[kGW];
-            if (t > 0) plain_row(gx, Gm, t - 1, c0); else zero_row(gx);
+            if (t > 0) staged_row16(gx, Gm, t - 1, c0); else zero_row(gx);
 #pragma unroll
             for (int i = 0; i < kGW; ++i) {
                 const float rh = rho[c0 + i];
@@ -1270,6 +1294,7 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
     if (tid == 0) {  // the staged states and T have landed before the shared memory goes away
         mbar_wait_bounded(bar_st, 0, tcg::kMaxPolls);
         if (t_issued) mbar_wait_bounded(bar_t, 0, tcg::kMaxPolls);
+        mbar_wait_bounded(bar_g, g2_issued ? 1 : 0, tcg::kMaxPolls);
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -1285,7 +1310,7 @@ size_t prefill_backward_workspace_bytes(int num_seqs, int T_total, int H) {
     const long long nc = prefill_backward_max_chunks(num_seqs, T_total);
     const size_t table = ((size_t)(num_seqs + 1) * sizeof(int32_t) + 255) & ~(size_t)255;
     const size_t mat = kStateElems * sizeof(float);
-    return table + (size_t)(5 * nc + num_seqs) * H * mat;
+    return table + (size_t)(6 * nc + num_seqs) * H * mat;
 }
 
 cudaError_t launch_prefill_backward(const BackwardArgs &b, void *workspace, cudaStream_t stream) {
@@ -1324,6 +1349,7 @@ cudaError_t launch_prefill_backward(const BackwardArgs &b, void *workspace, cuda
     p.Fck = p.Ack + (size_t)nc * plane;
     p.Eck = p.Fck + (size_t)nc * plane;
     p.Tck = p.Eck + (size_t)nc * plane;
+    p.Gck = p.Tck + (size_t)nc * plane;
 
     bwd_chunk_table_kernel<<<1, 1024, 0, stream>>>(b.cu_seqlens, b.num_seqs, b.T_total, p.chunk_base, b.status);
     e = cudaGetLastError();

@@ -222,11 +222,11 @@ def test_backward_rejects_small_workspace_and_overlaps(lib):
 
 
 def test_backward_workspace_size(lib):
-    # the state at every 64-token boundary plus A, F, E and T per chunk: (5 chunks + seqs) 16 KB planes
+    # the state at every 64-token boundary plus A, F, E, T and the decay table per chunk: (6 chunks + seqs) 16 KB planes
     n, T, H = 8, 32768, 40
     nc = T // 64 + n
     table = ((n + 1) * 4 + 255) // 256 * 256
-    assert lib.wkv7_prefill_backward_workspace_size(n, T, H, 64) == table + (5 * nc + n) * H * 16384
+    assert lib.wkv7_prefill_backward_workspace_size(n, T, H, 64) == table + (6 * nc + n) * H * 16384
     assert lib.wkv7_prefill_backward_workspace_size(n, T, H, 32) == 0
 
 
