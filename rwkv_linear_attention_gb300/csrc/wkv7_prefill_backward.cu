@@ -36,14 +36,19 @@
 //
 // Launches (one stream, no host synchronisation):
 //   1. chunk table: first chunk of every sequence (a prefix sum of ceil(len/64)).
-//   2. summary (one CTA per chunk and head, all in parallel): A, F, E.
+//   2. summary (one CTA per chunk and head, all in parallel): A, F, E, and T and
+//      the decay table g, which the gradient pass reads back instead of forming
+//      them again.
 //   3. chains (one CTA per sequence, head and direction): the states at every
 //      chunk boundary forward, the adjoints at every chunk end backward.
 //   4. gradients (one CTA per chunk and head, all in parallel).
 // The summary and gradient passes run their products on the tensor cores
 // (tcgen05, tf32 operands, fp32 accumulation in tensor memory); the chains
 // multiply in fp32 on the CUDA cores (4 x 4 register tiles, operands in shared
-// memory).  Only the two chains are sequential.
+// memory).  Only the two chains are sequential.  Whole 16 KB matrices (states,
+// adjoints, T, g) move by single bulk copies and 64 x 64 outputs by one bulk copy
+// per 256-byte row from staged shared-memory tiles, so that no warp's load or
+// store touches 32 rows.
 #include <cuda_bf16.h>
 
 #include <cstdint>
