@@ -47,8 +47,9 @@
 // multiply in fp32 on the CUDA cores (4 x 4 register tiles, operands in shared
 // memory).  Only the two chains are sequential.  Whole 16 KB matrices (states,
 // adjoints, T, g) move by single bulk copies and 64 x 64 outputs by one bulk copy
-// per 256-byte row from staged shared-memory tiles, so that no warp's load or
-// store touches 32 rows.
+// per 256-byte row from staged shared-memory tiles, instead of per-thread row
+// accesses (a warp's access touching 32 rows); the token rows of r, k, kk, a, v
+// and dO are still loaded per thread.
 #include <cuda_bf16.h>
 
 #include <cstdint>
