@@ -255,3 +255,20 @@ def test_binding_input_codes():
     assert wkv7._x_code(torch.float32, False) == _lib.F32
     assert wkv7._x_code(torch.float32, True) == _lib.TF32
     assert (_lib.F32, _lib.BF16, _lib.F16, _lib.TF32) == (0, 1, 2, 3)
+
+
+def test_size_limits_are_checked_before_anything_else(lib):
+    """2^30 heads per call is the most the 32-bit index math allows.  One more is rejected
+    before the pointers are looked at; exactly that many passes the size check, so the
+    misaligned pointers given here are what is reported.  Every case is rejected on the
+    host: nothing is launched."""
+    mis = [FAKE + 4 + i * (1 << 24) for i in range(8)]
+    assert _step(lib, B=1 << 15, H=(1 << 15) + 1, ptrs=mis) == _lib.ERR_INVALID_ARG
+    assert _step(lib, B=1 << 15, H=1 << 15, ptrs=mis) == _lib.ERR_ALIGNMENT
+    # the backward's grid holds the heads in its y dimension (at most 65535)
+    bad = [FAKE + 4 + i * (1 << 26) for i in range(18)]
+    assert _backward(lib, num_seqs=1, T=10, H=65536, ptrs=bad, ws_bytes=0) == _lib.ERR_INVALID_ARG
+    assert _backward(lib, num_seqs=1, T=10, H=65535, ptrs=bad, ws_bytes=0) == _lib.ERR_ALIGNMENT
+    # its workspace query answers 0 past the head limit
+    assert lib.wkv7_prefill_backward_workspace_size(1 << 15, 64, (1 << 15) + 1, 64) == 0
+    assert lib.wkv7_prefill_backward_workspace_size(1 << 15, 64, 1 << 15, 64) > 0
