@@ -47,9 +47,10 @@
 // multiply in fp32 on the CUDA cores (4 x 4 register tiles, operands in shared
 // memory).  Only the two chains are sequential.  Whole 16 KB matrices (states,
 // adjoints, T, g) move by single bulk copies and 64 x 64 outputs by one bulk copy
-// per 256-byte row from staged shared-memory tiles, instead of per-thread row
-// accesses (a warp's access touching 32 rows); the token rows of r, k, kk, a, v
-// and dO are still loaded per thread.
+// per 256-byte row from staged shared-memory tiles, and both passes take the chunk's
+// kk, k, a, r as 64-token TMA tiles, instead of per-thread row accesses (a warp's
+// access touching 32 rows); v, dO and the gradient epilogue's rows are still
+// loaded per thread.
 #include <cuda_bf16.h>
 
 #include <cstdint>
@@ -74,6 +75,9 @@ constexpr size_t kStateElems = (size_t)kN * kN;
 constexpr size_t kChainSmem = 3 * kMatBytes;
 
 struct BwdArgs {
+    // 64-token tiles of kk, k, a, r for the TMA (128-byte swizzle: bf16 as one box of
+    // 64 x 64, fp32 as two boxes of 64 x 32)
+    CUtensorMap mkk, mk, ma, mr;
     int num_seqs;
     int H;
     const int32_t *cu;  // device cu_seqlens [num_seqs + 1]
@@ -302,8 +306,9 @@ constexpr uint32_t kDv = 32768;       // after stage 4 (B_F3 done) to stage 6: f
 constexpr uint32_t kPlain0 = 180224;  // fp32 64 x 68: the cumulative decay, then T; then (with kPlain1) B_Pt
 constexpr uint32_t kPlain1 = 197632;  // fp32 64 x 68: Lc
 constexpr uint32_t kVec = 215040;     // rho[64], gC[64], carry parts [4][64]
-constexpr uint32_t kBar = 216576;     // mbarrier, TMEM base slot; mbarriers of the states, T, the decay table
-constexpr uint32_t kBytes = 216616;
+constexpr uint32_t kBar = 216576;     // mbarrier, TMEM base slot; mbarriers of the states, T, the decay table,
+                                      // the raw tiles
+constexpr uint32_t kBytes = 216624;
 // S0, Ghat and S_C (16 KB each, unpadded) arrive by bulk copies at the CTA's start and are
 // read in the B-tile step: places no operand uses before then (B_F3's U^c part, B_F1's and
 // B_F2's first K = 64, written in that step after a barrier)
@@ -599,6 +604,58 @@ __device__ __forceinline__ void staged_row16(float (&v)[16], const float *m, int
     }
 }
 
+// The chunk's raw tiles of kk, k, a, r (in that order, kRawTile apart from dst) by TMA,
+// completion on `bar`; rows past T_total arrive as zeros, rows of the next sequence
+// are loaded and not used.  One thread.
+__device__ __forceinline__ void issue_raw_tiles(const BwdArgs &p, const Chunk &c, int h, uint32_t dst, uint32_t bar) {
+    const uint32_t tile = p.x_bf16 ? 8192u : 16384u;
+    mbar_arrive_expect_tx(bar, 4 * tile);
+    const CUtensorMap *maps[4] = {&p.mkk, &p.mk, &p.ma, &p.mr};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        tma_load_2d(dst + i * tile, maps[i], h * 64, c.tb, bar);
+        if (!p.x_bf16) tma_load_2d(dst + i * tile + 8192, maps[i], h * 64 + 32, c.tb, bar);
+    }
+}
+// 16 values of row t from channel c0 of a raw tile (128-byte rows whose 16-byte chunks
+// are XOR-swizzled by t mod 8), widened from bf16.
+__device__ __forceinline__ void raw_row16(float (&v)[16], const unsigned char *tile, bool bf16, int t, int c0) {
+    if (bf16) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int chunk = (c0 >> 3) + q;
+            const uint4 u = *reinterpret_cast<const uint4 *>(tile + t * 128 + ((chunk ^ (t & 7)) << 4));
+            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                v[8 * q + 2 * e] = __uint_as_float(w4[e] << 16);
+                v[8 * q + 2 * e + 1] = __uint_as_float(w4[e] & 0xffff0000u);
+            }
+        }
+    } else {
+        const unsigned char *box = tile + (c0 >> 5) * 8192;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int chunk = ((c0 & 31) >> 2) + q;
+            const float4 x = *reinterpret_cast<const float4 *>(box + t * 128 + ((chunk ^ (t & 7)) << 4));
+            v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
+        }
+    }
+}
+// This thread's start rows from the raw tiles: top kk, k; bottom kk, a, r (zeros past the chunk).
+__device__ __forceinline__ void raw_start_rows(float (&kk)[16], float (&ra)[16], float (&rb)[16],
+                                               const unsigned char *tiles, bool bf16, bool top, bool valid, int t,
+                                               int c0) {
+    const int tile = bf16 ? 8192 : 16384;
+    if (valid) {
+        raw_row16(kk, tiles, bf16, t, c0);
+        raw_row16(ra, tiles + (top ? 1 : 2) * tile, bf16, t, c0);
+        if (!top) raw_row16(rb, tiles + 3 * tile, bf16, t, c0);
+    } else {
+        zero_row(kk); zero_row(ra); zero_row(rb);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // 2. per-chunk summary on the tensor cores: A, F (forward transition) and E
 // (adjoint input).  Their products contract over tokens, so their left
@@ -626,12 +683,12 @@ constexpr uint32_t kPlain1 = 164864;  // fp32 64 x 68: Lc
 constexpr uint32_t kStage = 0;        // after stage 3: fp32 64 x 68 tiles of F, A, E for the bulk row stores
 static_assert(kStage + 3 * kMatBytes <= kPlain0, "output staging tiles overlap the plain buffers");
 constexpr uint32_t kVec = 182272;     // rho[64], gC[64]
-constexpr uint32_t kBar = 182784;     // mbarrier, TMEM base slot
-constexpr uint32_t kBytes = 182800;
+constexpr uint32_t kBar = 182784;     // mbarrier, TMEM base slot, the raw tiles' mbarrier
+constexpr uint32_t kBytes = 182808;
 constexpr uint32_t kAlloc = kBytes + 1024;
 }  // namespace tcs
 
-__global__ void __launch_bounds__(kGradThreads, 1) bwd_summary_tc_kernel(BwdArgs p) {
+__global__ void __launch_bounds__(kGradThreads, 1) bwd_summary_tc_kernel(const __grid_constant__ BwdArgs p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -646,25 +703,22 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_summary_tc_kernel(BwdArgs
     const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
     float *rho = reinterpret_cast<float *>(sm + tcs::kVec), *gC = rho + 64;
     float *P0 = reinterpret_cast<float *>(sm + tcs::kPlain0), *P1p = reinterpret_cast<float *>(sm + tcs::kPlain1);
-    const uint32_t bar = sbase + tcs::kBar;
+    const uint32_t bar = sbase + tcs::kBar, bar_x = sbase + tcs::kBar + 16;
     const size_t cidx = ((size_t)blockIdx.x * p.H + h) * kStateElems;
     const bool row_valid = t < c.len;
     const size_t roff = ((size_t)(c.tb + (row_valid ? t : 0)) * p.H + h) * kN + c0;
 
     if (tid == 0) {
         mbar_init(bar, kIssuers);
+        mbar_init(bar_x, 1);
         fence_mbar_init();
+        issue_raw_tiles(p, c, h, sbase + tcs::kBG, bar_x);  // B_G's space, written after they are read
     }
     if (warp == 0) tmem_alloc(sbase + tcs::kBar + 8, tcg::kTmemCols);
-    float kk[kGW], ra[kGW], rb[kGW];  // top: kk, k; bottom: kk, a, r (fetched before the cumulative sum)
-    if (row_valid) {
-        load_row(kk, p.kk, p.x_bf16, roff);
-        load_row(ra, top ? p.k : p.a, p.x_bf16, roff);
-        if (!top) load_row(rb, p.r, p.x_bf16, roff);
-    } else {
-        zero_row(kk); zero_row(ra); zero_row(rb);
-    }
-    decay_cumsum<kGradThreads>(p, c, h, P0, P1p);
+    decay_cumsum<kGradThreads>(p, c, h, P0, P1p);  // (its barriers publish bar_x's initialisation)
+    float kk[kGW], ra[kGW], rb[kGW];  // top: kk, k; bottom: kk, a, r
+    if (!mbar_wait_bounded(bar_x, 0, tcg::kMaxPolls)) report(p.status, kDevTimeout);
+    raw_start_rows(kk, ra, rb, sm + tcs::kBG, p.x_bf16, top, row_valid, t, c0);
     if (tid < 64) {
         rho[tid] = P0[31 * kLD + tid];
         gC[tid] = P0[63 * kLD + tid];
@@ -841,6 +895,7 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_summary_tc_kernel(BwdArgs
         bulk_commit();
     }
     bulk_wait_read<0>();  // T's and the outputs' row copies have read their tiles (also after a timeout)
+    if (tid == 0) mbar_wait_bounded(bar_x, 0, tcg::kMaxPolls);  // the raw tiles have landed
     tc_fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, tcg::kTmemCols);
@@ -933,7 +988,7 @@ __global__ void __launch_bounds__(kThreads) bwd_chain_kernel(BwdArgs p) {
 //      [dKr; dR] = [U | P2^T | -P4^T ; dO | P1^T | -P3^T] x [S0' | K^c | Cm^T]^T
 // then the epilogue scales by the decay factors and forms dr, dk, dkk, da, dw.
 
-__global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p) {
+__global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(const __grid_constant__ BwdArgs p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -949,7 +1004,7 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
     float *rho = reinterpret_cast<float *>(sm + tcg::kVec), *gC = rho + 64, *carry = gC + 64;  // carry[kGroups][64]
     float *P0 = reinterpret_cast<float *>(sm + tcg::kPlain0);
     const uint32_t bar = sbase + tcg::kBar, bar_st = sbase + tcg::kBar + 16, bar_t = sbase + tcg::kBar + 24,
-                   bar_g = sbase + tcg::kBar + 32;
+                   bar_g = sbase + tcg::kBar + 32, bar_x = sbase + tcg::kBar + 40;
     const size_t cidx = ((size_t)blockIdx.x * p.H + h) * kStateElems;
     const size_t b0 = ((size_t)(blockIdx.x + c.seq) * p.H + h) * kStateElems;
     const size_t b1 = b0 + (size_t)p.H * kStateElems;
@@ -961,7 +1016,9 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
         mbar_init(bar_st, 1);
         mbar_init(bar_t, 1);
         mbar_init(bar_g, 1);
+        mbar_init(bar_x, 1);
         fence_mbar_init();
+        issue_raw_tiles(p, c, h, sbase + tcg::kBG, bar_x);  // B_G's space, written after they are read
         // the decay table (from the summary pass; unpadded) into the plain buffer, and
         // later into the epilogue's space: phases 0 and 1 of bar_g
         mbar_arrive_expect_tx(bar_g, kStateElems * sizeof(float));
@@ -974,14 +1031,9 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
     if (warp == 0) tmem_alloc(sbase + tcg::kBar + 8, tcg::kTmemCols);
     // raw rows for the scaled operands, fetched before the cumulative sum needs w
     float kk[kGW], ra[kGW], rb[kGW];  // top: kk, k; bottom: kk, a, r
-    if (row_valid) {
-        load_row(kk, p.kk, p.x_bf16, roff);
-        load_row(ra, top ? p.k : p.a, p.x_bf16, roff);
-        if (!top) load_row(rb, p.r, p.x_bf16, roff);
-    } else {
-        zero_row(kk); zero_row(ra); zero_row(rb);
-    }
     __syncthreads();  // the mbarriers are initialised
+    if (!mbar_wait_bounded(bar_x, 0, tcg::kMaxPolls)) report(p.status, kDevTimeout);
+    raw_start_rows(kk, ra, rb, sm + tcg::kBG, p.x_bf16, top, row_valid, t, c0);
     const bool got_g = mbar_wait_bounded(bar_g, 0, tcg::kMaxPolls);
     if (!got_g && tid == 0) report(p.status, kDevTimeout);
     if (tid < 64) {
@@ -1300,11 +1352,47 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(BwdArgs p)
     if (tid == 0) {  // the staged states and T have landed before the shared memory goes away
         mbar_wait_bounded(bar_st, 0, tcg::kMaxPolls);
         if (t_issued) mbar_wait_bounded(bar_t, 0, tcg::kMaxPolls);
+        mbar_wait_bounded(bar_x, 0, tcg::kMaxPolls);
         mbar_wait_bounded(bar_g, g2_issued ? 1 : 0, tcg::kMaxPolls);
     }
     tc_fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, tcg::kTmemCols);
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// 2-D map over a packed [T_total, H*64] input: 64-row boxes of 128-byte rows (64 bf16 or
+// 32 fp32 channels) in the 128-byte swizzle layout.
+bool make_tile_map(CUtensorMap *map, const void *base, bool bf16, int T_total, int H) {
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return false;
+    const cuuint64_t esz = bf16 ? 2 : 4;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(H) * 64, static_cast<cuuint64_t>(T_total)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(H) * 64 * esz};
+    cuuint32_t box[2] = {bf16 ? 64u : 32u, 64};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+               const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -1357,6 +1445,11 @@ cudaError_t launch_prefill_backward(const BackwardArgs &b, void *workspace, cuda
     p.Tck = p.Eck + (size_t)nc * plane;
     p.Gck = p.Tck + (size_t)nc * plane;
 
+    if (nc > 0 && (!make_tile_map(&p.mkk, b.kk, p.x_bf16, b.T_total, b.H) ||
+                   !make_tile_map(&p.mk, b.k, p.x_bf16, b.T_total, b.H) ||
+                   !make_tile_map(&p.ma, b.a, p.x_bf16, b.T_total, b.H) ||
+                   !make_tile_map(&p.mr, b.r, p.x_bf16, b.T_total, b.H)))
+        return cudaErrorInvalidValue;
     bwd_chunk_table_kernel<<<1, 1024, 0, stream>>>(b.cu_seqlens, b.num_seqs, b.T_total, p.chunk_base, b.status);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
