@@ -48,9 +48,9 @@
 // memory).  Only the two chains are sequential.  Whole 16 KB matrices (states,
 // adjoints, T, g) move by single bulk copies and 64 x 64 outputs by one bulk copy
 // per 256-byte row from staged shared-memory tiles, and both passes take the chunk's
-// kk, k, a, r as 64-token TMA tiles, instead of per-thread row accesses (a warp's
-// access touching 32 rows); v, dO and the gradient epilogue's rows are still
-// loaded per thread.
+// token rows (kk, k, a, r, v, dO) as 64-token TMA tiles, instead of per-thread row
+// accesses (a warp's access touching 32 rows); only fp32 v rows and fp32 epilogue
+// rows of the gradient pass, for which no shared memory is left, are loaded per thread.
 #include <cuda_bf16.h>
 
 #include <cstdint>
@@ -78,6 +78,7 @@ struct BwdArgs {
     // 64-token tiles of kk, k, a, r for the TMA (128-byte swizzle: bf16 as one box of
     // 64 x 64, fp32 as two boxes of 64 x 32)
     CUtensorMap mkk, mk, ma, mr;
+    CUtensorMap mv, mdo;  // v (like the above) and dO (fp32, two boxes of 64 x 32)
     int num_seqs;
     int H;
     const int32_t *cu;  // device cu_seqlens [num_seqs + 1]
@@ -307,8 +308,12 @@ constexpr uint32_t kPlain0 = 180224;  // fp32 64 x 68: the cumulative decay, the
 constexpr uint32_t kPlain1 = 197632;  // fp32 64 x 68: Lc
 constexpr uint32_t kVec = 215040;     // rho[64], gC[64], carry parts [4][64]
 constexpr uint32_t kBar = 216576;     // mbarrier, TMEM base slot; mbarriers of the states, T, the decay table,
-                                      // the raw tiles
-constexpr uint32_t kBytes = 216624;
+                                      // the raw tiles, the v and dO tiles, the epilogue's raw tiles
+// the bf16 v tile by TMA (an fp32 one does not fit: fp32 v rows are loaded per thread); the
+// dO tile goes to the second plain buffer (free until B_Pt), the epilogue's raw tiles (bf16)
+// to both plain buffers (free after stage 5)
+constexpr uint32_t kVt = 217088;
+constexpr uint32_t kBytes = kVt + 8192;
 // S0, Ghat and S_C (16 KB each, unpadded) arrive by bulk copies at the CTA's start and are
 // read in the B-tile step: places no operand uses before then (B_F3's U^c part, B_F1's and
 // B_F2's first K = 64, written in that step after a barrier)
@@ -320,6 +325,9 @@ constexpr uint32_t kAtom64 = 64 * 128, kAtom128 = 128 * 128, kAtom256 = 256 * 12
 static_assert(kStage + 5 * kMatBytes <= kPlain0, "gradient staging tiles overlap the plain buffers");
 static_assert(kDv >= kBF3 && kDv + kMatBytes <= kBF1, "the dV tile lies outside B_F3");
 static_assert(kPlain1 == kPlain0 + kMatBytes && kPlain1 + kMatBytes <= kVec, "B_Pt spans both plain buffers");
+static_assert(kVt % 1024 == 0 && kVt >= kBar + 64 && kPlain0 % 1024 == 0 && kPlain1 % 1024 == 0 &&
+                  kPlain1 + 16384 <= kVec && kPlain0 + 4 * 8192 <= kVec,
+              "TMA tiles: 1024-byte aligned, inside their regions");
 static_assert(kSt0 >= kBG + 256 * 256 && kSt0 + 16384 <= kBF1 && kSt1 == kBF1 && kSt2 == kBF2,
               "a staged state overlaps an operand in use before the B-tile step");
 static_assert((kLD * sizeof(float)) % 16 == 0, "staged rows must start on 16-byte boundaries for the bulk stores");
@@ -642,6 +650,19 @@ __device__ __forceinline__ void raw_row16(float (&v)[16], const unsigned char *t
         }
     }
 }
+// The chunk's dO tile (two fp32 boxes) at dst_o and, with_v, its v tile at dst_v, by TMA,
+// completion on `bar`.  One thread.
+__device__ __forceinline__ void issue_vdo_tiles(const BwdArgs &p, const Chunk &c, int h, uint32_t dst_v, uint32_t dst_o,
+                                                uint32_t bar, bool with_v) {
+    const uint32_t vbytes = with_v ? (p.x_bf16 ? 8192u : 16384u) : 0u;
+    mbar_arrive_expect_tx(bar, vbytes + 16384u);
+    if (with_v) {
+        tma_load_2d(dst_v, &p.mv, h * 64, c.tb, bar);
+        if (!p.x_bf16) tma_load_2d(dst_v + 8192, &p.mv, h * 64 + 32, c.tb, bar);
+    }
+    tma_load_2d(dst_o, &p.mdo, h * 64, c.tb, bar);
+    tma_load_2d(dst_o + 8192, &p.mdo, h * 64 + 32, c.tb, bar);
+}
 // This thread's start rows from the raw tiles: top kk, k; bottom kk, a, r (zeros past the chunk).
 __device__ __forceinline__ void raw_start_rows(float (&kk)[16], float (&ra)[16], float (&rb)[16],
                                                const unsigned char *tiles, bool bf16, bool top, bool valid, int t,
@@ -683,8 +704,10 @@ constexpr uint32_t kPlain1 = 164864;  // fp32 64 x 68: Lc
 constexpr uint32_t kStage = 0;        // after stage 3: fp32 64 x 68 tiles of F, A, E for the bulk row stores
 static_assert(kStage + 3 * kMatBytes <= kPlain0, "output staging tiles overlap the plain buffers");
 constexpr uint32_t kVec = 182272;     // rho[64], gC[64]
-constexpr uint32_t kBar = 182784;     // mbarrier, TMEM base slot, the raw tiles' mbarrier
-constexpr uint32_t kBytes = 182808;
+constexpr uint32_t kBar = 182784;     // mbarrier, TMEM base slot, the raw tiles' and the v, dO tiles' mbarriers
+// v and dO tiles by TMA (v: 8 KB bf16 or 16 KB fp32; dO 16 KB), 1024-byte aligned for the swizzle
+constexpr uint32_t kVt = 183296, kdOt = kVt + 16384;
+constexpr uint32_t kBytes = kdOt + 16384;
 constexpr uint32_t kAlloc = kBytes + 1024;
 }  // namespace tcs
 
@@ -703,16 +726,17 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_summary_tc_kernel(const _
     const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
     float *rho = reinterpret_cast<float *>(sm + tcs::kVec), *gC = rho + 64;
     float *P0 = reinterpret_cast<float *>(sm + tcs::kPlain0), *P1p = reinterpret_cast<float *>(sm + tcs::kPlain1);
-    const uint32_t bar = sbase + tcs::kBar, bar_x = sbase + tcs::kBar + 16;
+    const uint32_t bar = sbase + tcs::kBar, bar_x = sbase + tcs::kBar + 16, bar_v = sbase + tcs::kBar + 24;
     const size_t cidx = ((size_t)blockIdx.x * p.H + h) * kStateElems;
     const bool row_valid = t < c.len;
-    const size_t roff = ((size_t)(c.tb + (row_valid ? t : 0)) * p.H + h) * kN + c0;
 
     if (tid == 0) {
         mbar_init(bar, kIssuers);
         mbar_init(bar_x, 1);
+        mbar_init(bar_v, 1);
         fence_mbar_init();
         issue_raw_tiles(p, c, h, sbase + tcs::kBG, bar_x);  // B_G's space, written after they are read
+        issue_vdo_tiles(p, c, h, sbase + tcs::kVt, sbase + tcs::kdOt, bar_v, true);
     }
     if (warp == 0) tmem_alloc(sbase + tcs::kBar + 8, tcg::kTmemCols);
     decay_cumsum<kGradThreads>(p, c, h, P0, P1p);  // (its barriers publish bar_x's initialisation)
@@ -778,10 +802,6 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_summary_tc_kernel(const _
         for (int i = 0; i < kGW; ++i) id[i] = (!top && c0 + i == t) ? 0x3f800000u : 0u;
         tmem_st_row(tl + 320, id);
     }
-    if (!top) {  // V and dO rows, in flight during the first products
-        if (row_valid) { load_row(kk, p.v, p.x_bf16, roff); load_row(ra, p.d_o, false, roff); }
-        else { zero_row(kk); zero_row(ra); }
-    }
     ok = mma_stage(bar, phase, p.status, [&](int who) {
         if (who == 0) {
             mma_group(tmem, 64, 0, sbase + tcs::kBG, tcg::kAtom256, 192, 64);     // G1
@@ -804,6 +824,13 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_summary_tc_kernel(const _
             tmem_ld_row(tl + 192, v);
             mask_row<kUpper, false>(v, t, c0);
             a_row(tl + 64, v);
+            if (!mbar_wait_bounded(bar_v, 0, tcg::kMaxPolls)) report(p.status, kDevTimeout);
+            if (row_valid) {  // this row of v and dO
+                raw_row16(kk, sm + tcs::kVt, p.x_bf16, t, c0);
+                raw_row16(ra, sm + tcs::kdOt, false, t, c0);
+            } else {
+                zero_row(kk); zero_row(ra);
+            }
             b_col(sm + tcs::kBVc, 64, t, c0, kk);
             b_col(sm + tcs::kBdOc, 64, t, c0, ra);
         }
@@ -895,7 +922,10 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_summary_tc_kernel(const _
         bulk_commit();
     }
     bulk_wait_read<0>();  // T's and the outputs' row copies have read their tiles (also after a timeout)
-    if (tid == 0) mbar_wait_bounded(bar_x, 0, tcg::kMaxPolls);  // the raw tiles have landed
+    if (tid == 0) {  // the tiles have landed before the shared memory goes away
+        mbar_wait_bounded(bar_x, 0, tcg::kMaxPolls);
+        mbar_wait_bounded(bar_v, 0, tcg::kMaxPolls);
+    }
     tc_fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, tcg::kTmemCols);
@@ -1004,7 +1034,8 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(const __gr
     float *rho = reinterpret_cast<float *>(sm + tcg::kVec), *gC = rho + 64, *carry = gC + 64;  // carry[kGroups][64]
     float *P0 = reinterpret_cast<float *>(sm + tcg::kPlain0);
     const uint32_t bar = sbase + tcg::kBar, bar_st = sbase + tcg::kBar + 16, bar_t = sbase + tcg::kBar + 24,
-                   bar_g = sbase + tcg::kBar + 32, bar_x = sbase + tcg::kBar + 40;
+                   bar_g = sbase + tcg::kBar + 32, bar_x = sbase + tcg::kBar + 40, bar_v = sbase + tcg::kBar + 48,
+                   bar_e = sbase + tcg::kBar + 56;
     const size_t cidx = ((size_t)blockIdx.x * p.H + h) * kStateElems;
     const size_t b0 = ((size_t)(blockIdx.x + c.seq) * p.H + h) * kStateElems;
     const size_t b1 = b0 + (size_t)p.H * kStateElems;
@@ -1017,8 +1048,11 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(const __gr
         mbar_init(bar_t, 1);
         mbar_init(bar_g, 1);
         mbar_init(bar_x, 1);
+        mbar_init(bar_v, 1);
+        mbar_init(bar_e, 1);
         fence_mbar_init();
         issue_raw_tiles(p, c, h, sbase + tcg::kBG, bar_x);  // B_G's space, written after they are read
+        issue_vdo_tiles(p, c, h, sbase + tcg::kVt, sbase + tcg::kPlain1, bar_v, p.x_bf16);
         // the decay table (from the summary pass; unpadded) into the plain buffer, and
         // later into the epilogue's space: phases 0 and 1 of bar_g
         mbar_arrive_expect_tx(bar_g, kStateElems * sizeof(float));
@@ -1081,15 +1115,11 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(const __gr
             b_col(sm + tcg::kBF2, 64, 128 + t, c0, v);  // Cm^c
         }
     }
-    // the next phase's rows, in flight during the Gram products: bottom V, dO (the top
-    // rows' states come by bulk copy)
-    if (!top) {
-        if (row_valid) {
-            load_row(kk, p.v, p.x_bf16, roff);
-            load_row(ra, p.d_o, false, roff);
-        } else {
-            zero_row(kk); zero_row(ra);
-        }
+    // fp32 v rows (bottom), in flight during the Gram products (bf16 v and dO come as
+    // tiles, the top rows' states by bulk copy)
+    if (!top && !p.x_bf16) {
+        if (row_valid) load_row(kk, p.v, false, roff);
+        else zero_row(kk);
     }
     ok = mma_stage(bar, phase, p.status, [&](int who) {
         if (who == 0) mma_group(tmem, 64, 0, sbase + tcg::kBG, tcg::kAtom256, 192, 64);
@@ -1151,6 +1181,13 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(const __gr
             b_col(sm + tcg::kBF3, 64, t, c0, ra);        // G'^T
             b_row(sm + tcg::kBF1, 64, t, c0, ra);        // G'
         } else {
+            if (!mbar_wait_bounded(bar_v, 0, tcg::kMaxPolls)) report(p.status, kDevTimeout);
+            if (row_valid) {  // this row of dO (and of v, bf16)
+                if (p.x_bf16) raw_row16(kk, sm + tcg::kVt, true, t, c0);
+                raw_row16(ra, sm + tcg::kPlain1, false, t, c0);
+            } else {
+                zero_row(kk); zero_row(ra);
+            }
             b_col(sm + tcg::kBY, 64, 64 + t, c0, kk);    // V^c
             b_col(sm + tcg::kBF3, 64, 64 + t, c0, ra);   // dO^c
         }
@@ -1243,18 +1280,22 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(const __gr
     }
     bool g2_issued = false;
     if (ok) {
-        // the epilogue's rows (top kk, a; bottom r, k) and the decay table again (B_P's space
+        // the epilogue's rows (top kk, a; bottom r, k: bf16 as tiles into the plain buffers,
+        // which B_Pt no longer needs; fp32 per thread) and the decay table again (B_P's space
         // is free), in flight during the last products
-        if (row_valid) {
-            load_row(kk, top ? p.kk : p.r, p.x_bf16, roff);
-            load_row(ra, top ? p.a : p.k, p.x_bf16, roff);
-        } else {
-            zero_row(kk); zero_row(ra);
+        if (!p.x_bf16) {
+            if (row_valid) {
+                load_row(kk, top ? p.kk : p.r, false, roff);
+                load_row(ra, top ? p.a : p.k, false, roff);
+            } else {
+                zero_row(kk); zero_row(ra);
+            }
         }
         if (tid == 0) {
             mbar_arrive_expect_tx(bar_g, kStateElems * sizeof(float));
             bulk_load(sbase + 0, p.Gck + cidx, kStateElems * sizeof(float), bar_g);
             g2_issued = true;
+            if (p.x_bf16) issue_raw_tiles(p, c, h, sbase + tcg::kPlain0, bar_e);
         }
         bulk_wait_read<0>();  // dV's tile is read before the epilogue writes over it
         ok = mma_stage(bar, phase, p.status, [&](int who) {
@@ -1271,6 +1312,16 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(const __gr
         float *PB = reinterpret_cast<float *>(sm + 34816);  // bottom part
         float *const stage = reinterpret_cast<float *>(sm + tcg::kStage);
         if (!mbar_wait_bounded(bar_g, 1, tcg::kMaxPolls)) report(p.status, kDevTimeout);
+        if (p.x_bf16) {  // this row of kk, a (top) or r, k (bottom) from the tiles
+            if (!mbar_wait_bounded(bar_e, 0, tcg::kMaxPolls)) report(p.status, kDevTimeout);
+            if (row_valid) {
+                const unsigned char *tl0 = sm + tcg::kPlain0;  // kk, k, a, r, 8 KB apart
+                raw_row16(kk, tl0 + (top ? 0 : 3) * 8192, true, t, c0);
+                raw_row16(ra, tl0 + (top ? 2 : 1) * 8192, true, t, c0);
+            } else {
+                zero_row(kk); zero_row(ra);
+            }
+        }
         float g[kGW], acc1[kGW], acc2[kGW];
         staged_row16(g, Gm, t, c0);
         tmem_ld_row(tl + 192, acc1);  // top dC, bottom dK
@@ -1354,6 +1405,8 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(const __gr
         if (t_issued) mbar_wait_bounded(bar_t, 0, tcg::kMaxPolls);
         mbar_wait_bounded(bar_x, 0, tcg::kMaxPolls);
         mbar_wait_bounded(bar_g, g2_issued ? 1 : 0, tcg::kMaxPolls);
+        mbar_wait_bounded(bar_v, 0, tcg::kMaxPolls);
+        if (g2_issued && p.x_bf16) mbar_wait_bounded(bar_e, 0, tcg::kMaxPolls);
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -1448,7 +1501,9 @@ cudaError_t launch_prefill_backward(const BackwardArgs &b, void *workspace, cuda
     if (nc > 0 && (!make_tile_map(&p.mkk, b.kk, p.x_bf16, b.T_total, b.H) ||
                    !make_tile_map(&p.mk, b.k, p.x_bf16, b.T_total, b.H) ||
                    !make_tile_map(&p.ma, b.a, p.x_bf16, b.T_total, b.H) ||
-                   !make_tile_map(&p.mr, b.r, p.x_bf16, b.T_total, b.H)))
+                   !make_tile_map(&p.mr, b.r, p.x_bf16, b.T_total, b.H) ||
+                   !make_tile_map(&p.mv, b.v, p.x_bf16, b.T_total, b.H) ||
+                   !make_tile_map(&p.mdo, b.d_o, false, b.T_total, b.H)))
         return cudaErrorInvalidValue;
     bwd_chunk_table_kernel<<<1, 1024, 0, stream>>>(b.cu_seqlens, b.num_seqs, b.T_total, p.chunk_base, b.status);
     e = cudaGetLastError();
