@@ -1063,7 +1063,7 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(const __gr
         bulk_load(sbase + tcg::kSt2, p.Sck + b1, kStateElems * sizeof(float), bar_st);
     }
     if (warp == 0) tmem_alloc(sbase + tcg::kBar + 8, tcg::kTmemCols);
-    // raw rows for the scaled operands, fetched before the cumulative sum needs w
+    // this thread's rows for the scaled operands, from the raw tiles
     float kk[kGW], ra[kGW], rb[kGW];  // top: kk, k; bottom: kk, a, r
     __syncthreads();  // the mbarriers are initialised
     if (!mbar_wait_bounded(bar_x, 0, tcg::kMaxPolls)) report(p.status, kDevTimeout);
@@ -1135,7 +1135,7 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(const __gr
     }
 
     if (ok) {
-        // ---- Grams out: Lc -> plain; A_YY2 = [Q | Lk] (top), [Cm | Mc^T] (bottom); A_F3 = [K | Mk^T | -Lk^T]
+        // ---- Grams out: A_YY2 = [Q | Lk] (top), [Cm | Mc^T] (bottom); A_F3 = [K | Mk^T | -Lk^T]
         if (top) {  // (L_c, in columns 64.., is not needed here: T comes from the summary pass)
             tmem_ld16x2(tl + 128, tl + 320, x, v);
             mask_row<kStrictLower, false>(x, t, c0);
@@ -1158,7 +1158,7 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(const __gr
             staged_row16(ra, reinterpret_cast<const float *>(sm + tcg::kSt1), t, c0);
             staged_row16(rb, reinterpret_cast<const float *>(sm + tcg::kSt2), t, c0);
         }
-        // Lc complete; B_G no longer read; the staged states read (B_F1 and B_F2 go over them)
+        // B_G no longer read; the staged states read (B_F1 and B_F2 go over them)
         if (!__syncthreads_and(got ? 1 : 0)) {
             if (tid == 0) report(p.status, kDevTimeout);
             ok = false;
@@ -1400,7 +1400,7 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_tc_kernel(const __gr
         bulk_commit();
     }
     bulk_wait_read<0>();  // every row copy has read its tile (also after a timeout)
-    if (tid == 0) {  // the staged states and T have landed before the shared memory goes away
+    if (tid == 0) {  // every bulk copy and TMA tile has landed before the shared memory goes away
         mbar_wait_bounded(bar_st, 0, tcg::kMaxPolls);
         if (t_issued) mbar_wait_bounded(bar_t, 0, tcg::kMaxPolls);
         mbar_wait_bounded(bar_x, 0, tcg::kMaxPolls);
