@@ -136,3 +136,23 @@ def test_reference_arm_prints_the_contract_line():
     assert d["e2e"]["value"] == d["value"] and d["e2e"]["unit"] == d["unit"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert "workload" in d["config"]
+
+
+def test_committed_traffic_records_match_the_kernel_sources():
+    """The DRAM traffic the bench reports comes from the committed ncu record only while
+    the kernel's sources are unchanged; the records in profiles/traffic.json must name
+    the current sources (re-capture, or restate an unchanged kernel's digest, after an
+    edit)."""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    csrc = os.path.join(root, "rwkv_linear_attention_gb300", "csrc")
+    shared = [os.path.join(csrc, "sm103_ptx.cuh"), os.path.join(csrc, "wkv7_internal.cuh")]
+    sources = {"wkv7_step_kernel": "wkv7_step.cu", "wkv7_prefill_chunked_kernel": "wkv7_prefill_chunked.cu",
+               "bwd_grad_tc_kernel": "wkv7_prefill_backward.cu", "bwd_summary_tc_kernel": "wkv7_prefill_backward.cu"}
+    with open(os.path.join(root, "profiles", "traffic.json")) as f:
+        records = json.load(f)
+    for kernel, src in sources.items():
+        digest = bench.source_digest([os.path.join(csrc, src)] + shared)
+        assert kernel in records, kernel
+        for workload, rec in records[kernel].items():
+            assert rec["source_digest"] == digest, f"{kernel} / {workload}: record is for other sources"
+            assert rec["dram_bytes_per_launch"] == rec["read_bytes"] + rec["write_bytes"]
