@@ -83,6 +83,8 @@ CASES = [
     ([300, 77], 4, torch.bfloat16),
     ([0, 0, 5], 2, torch.bfloat16),
     ([2048], 2, torch.float32),
+    ([1, 100, 63], 1, torch.bfloat16),  # one head: the token tiles' maps are 64 wide
+    ([65, 3, 128], 5, torch.float32),   # an odd head count, fp32 inputs (two boxes per tile)
 ]
 
 
