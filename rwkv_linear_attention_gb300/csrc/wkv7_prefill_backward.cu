@@ -202,18 +202,14 @@ __device__ __forceinline__ bool locate(const BwdArgs &p, int g, Chunk &c) {
 }
 
 // T = (I + Lc)^{-1} for the strictly lower Lc: the four 16 x 16 diagonal blocks by
-// forward substitution (one thread per column), then the blocks below them by
-// T_IJ = -T_II sum_{K=J}^{I-1} Lc_IK T_KJ, one block diagonal at a time.
-// tmp holds at least 3 * 256 floats.  NT threads.  Ends with a barrier.
+// forward substitution (one thread per column; the other threads meanwhile zero the six
+// blocks above them), then the blocks below them by
+// T_IJ = -T_II sum_{K=J}^{I-1} Lc_IK T_KJ, one block diagonal at a time, each thread
+// taking four consecutive columns of a row (16-byte loads of Lc and T rows, four
+// independent sums).  tmp holds at least 3 * 256 floats.  NT threads.  Ends with a barrier.
 template <int NT>
 __device__ void unit_lower_inverse(const float *Lc, float *T, float *tmp) {
     const int tid = threadIdx.x;
-#pragma unroll 4
-    for (int q = 0; q < 4096 / NT; ++q) {
-        const int e = tid + q * NT;
-        T[(e >> 6) * kLD + (e & 63)] = 0.f;
-    }
-    __syncthreads();
     if (tid < 64) {
         const int o = (tid >> 4) * 16, jj = tid & 15;
         float x[16];
@@ -226,27 +222,56 @@ __device__ void unit_lower_inverse(const float *Lc, float *T, float *tmp) {
         }
 #pragma unroll
         for (int t = 0; t < 16; ++t) T[(o + t) * kLD + o + jj] = x[t];
+    } else {
+        for (int e = tid - 64; e < 6 * 64; e += NT - 64) {  // blocks (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
+            const int blk = e >> 6, row = (e >> 2) & 15, c4 = (e & 3) * 4;
+            const int I = blk < 3 ? 0 : (blk < 5 ? 1 : 2), J = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+            *reinterpret_cast<float4 *>(T + (I * 16 + row) * kLD + J * 16 + c4) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
     }
     __syncthreads();
     for (int d = 1; d < 4; ++d) {
         const int np = 4 - d;
-        for (int e = tid; e < np * 256; e += NT) {
-            const int J = e >> 8, rr = (e >> 4) & 15, cc = e & 15, I = J + d;
+        for (int e = tid; e < np * 64; e += NT) {  // tmp_J = sum_{K=J}^{I-1} Lc_IK T_KJ, row rr, columns c4..
+            const int J = e >> 6, rr = (e >> 2) & 15, c4 = (e & 3) * 4, I = J + d;
             const float *lrow = Lc + (I * 16 + rr) * kLD;
-            float acc = 0.f;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int kb = J; kb < I; ++kb) {
 #pragma unroll
-                for (int q = 0; q < 16; ++q) acc = fmaf(lrow[kb * 16 + q], T[(kb * 16 + q) * kLD + J * 16 + cc], acc);
+                for (int q4 = 0; q4 < 16; q4 += 4) {
+                    const float4 l = *reinterpret_cast<const float4 *>(lrow + kb * 16 + q4);
+                    const float lq[4] = {l.x, l.y, l.z, l.w};
+#pragma unroll
+                    for (int qq = 0; qq < 4; ++qq) {
+                        const float4 tv = *reinterpret_cast<const float4 *>(T + (kb * 16 + q4 + qq) * kLD + J * 16 + c4);
+                        acc.x = fmaf(lq[qq], tv.x, acc.x);
+                        acc.y = fmaf(lq[qq], tv.y, acc.y);
+                        acc.z = fmaf(lq[qq], tv.z, acc.z);
+                        acc.w = fmaf(lq[qq], tv.w, acc.w);
+                    }
+                }
             }
-            tmp[e] = acc;
+            *reinterpret_cast<float4 *>(tmp + (J << 8) + rr * 16 + c4) = acc;
         }
         __syncthreads();
-        for (int e = tid; e < np * 256; e += NT) {
-            const int J = e >> 8, rr = (e >> 4) & 15, cc = e & 15, I = J + d;
-            float acc = 0.f;
+        for (int e = tid; e < np * 64; e += NT) {  // T_IJ = -T_II tmp_J, row rr, columns c4..
+            const int J = e >> 6, rr = (e >> 2) & 15, c4 = (e & 3) * 4, I = J + d;
+            const float *trow = T + (I * 16 + rr) * kLD + I * 16;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int q = 0; q < 16; ++q) acc = fmaf(T[(I * 16 + rr) * kLD + I * 16 + q], tmp[(J << 8) + q * 16 + cc], acc);
-            T[(I * 16 + rr) * kLD + J * 16 + cc] = -acc;
+            for (int q4 = 0; q4 < 16; q4 += 4) {
+                const float4 tr = *reinterpret_cast<const float4 *>(trow + q4);
+                const float tq[4] = {tr.x, tr.y, tr.z, tr.w};
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) {
+                    const float4 m = *reinterpret_cast<const float4 *>(tmp + (J << 8) + (q4 + qq) * 16 + c4);
+                    acc.x = fmaf(tq[qq], m.x, acc.x);
+                    acc.y = fmaf(tq[qq], m.y, acc.y);
+                    acc.z = fmaf(tq[qq], m.z, acc.z);
+                    acc.w = fmaf(tq[qq], m.w, acc.w);
+                }
+            }
+            *reinterpret_cast<float4 *>(T + (I * 16 + rr) * kLD + J * 16 + c4) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
         }
         __syncthreads();
     }
