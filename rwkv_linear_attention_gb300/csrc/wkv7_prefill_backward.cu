@@ -1011,9 +1011,15 @@ __global__ void __launch_bounds__(kThreads) bwd_chain_kernel(BwdArgs p) {
         }
         __syncthreads();
         tile_store(Sm, acc);
-        __syncthreads();
-        if (!adjoint) store_state(p.Sck + ((size_t)(c0 + s + ci + 1) * p.H + h) * kStateElems, Sm);
+        if (!adjoint) {  // the state at this chunk's end, from this thread's own tile (the
+                         // next step's barrier publishes the shared copy)
+            float *dst = p.Sck + ((size_t)(c0 + s + ci + 1) * p.H + h) * kStateElems;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                *reinterpret_cast<float4 *>(dst + (m0 + i) * kN + n0) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+        }
     }
+    __syncthreads();  // the last step's shared copy of the state
     if (adjoint && p.ds0) store_state(p.ds0 + pair, Sm);
 }
 
