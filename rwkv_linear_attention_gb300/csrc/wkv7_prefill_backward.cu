@@ -202,16 +202,17 @@ __device__ __forceinline__ bool locate(const BwdArgs &p, int g, Chunk &c) {
 }
 
 // T = (I + Lc)^{-1} for the strictly lower Lc: the four 16 x 16 diagonal blocks by
-// forward substitution (one thread per column; the other threads meanwhile zero the six
-// blocks above them), then the blocks below them by
+// forward substitution (one thread of warps 2 and 3 per column: warps 0 and 1 may still
+// be issuing products; the other threads meanwhile zero the six blocks above them), then
+// the blocks below them by
 // T_IJ = -T_II sum_{K=J}^{I-1} Lc_IK T_KJ, one block diagonal at a time, each thread
 // taking four consecutive columns of a row (16-byte loads of Lc and T rows, four
 // independent sums).  tmp holds at least 3 * 256 floats.  NT threads.  Ends with a barrier.
 template <int NT>
 __device__ void unit_lower_inverse(const float *Lc, float *T, float *tmp) {
     const int tid = threadIdx.x;
-    if (tid < 64) {
-        const int o = (tid >> 4) * 16, jj = tid & 15;
+    if (tid >= 64 && tid < 128) {
+        const int o = ((tid - 64) >> 4) * 16, jj = tid & 15;
         float x[16];
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
@@ -223,7 +224,7 @@ __device__ void unit_lower_inverse(const float *Lc, float *T, float *tmp) {
 #pragma unroll
         for (int t = 0; t < 16; ++t) T[(o + t) * kLD + o + jj] = x[t];
     } else {
-        for (int e = tid - 64; e < 6 * 64; e += NT - 64) {  // blocks (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
+        for (int e = tid < 64 ? tid : tid - 64; e < 6 * 64; e += NT - 64) {  // blocks (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
             const int blk = e >> 6, row = (e >> 2) & 15, c4 = (e & 3) * 4;
             const int I = blk < 3 ? 0 : (blk < 5 ? 1 : 2), J = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
             *reinterpret_cast<float4 *>(T + (I * 16 + row) * kLD + J * 16 + c4) = make_float4(0.f, 0.f, 0.f, 0.f);
