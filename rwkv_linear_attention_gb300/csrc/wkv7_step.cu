@@ -51,7 +51,6 @@ using namespace ptx;
 
 constexpr int kThreads = 128;
 constexpr int kStages = 4;
-constexpr uint32_t kStateBytes = kN * kN * 4;  // 16 KB
 constexpr uint32_t kVecBytes = kN * 4;         // 256 B
 constexpr uint32_t kMaxPolls = 1u << 24;
 
